@@ -1,0 +1,470 @@
+// bsgg_oracle.cpp -- plain, slow CPU reference for the grouped block-scaled GEMM
+// with fused per-row epilogue and output quantization.
+//
+// TEST INFRASTRUCTURE ONLY.  This file is the parity oracle: nothing in the
+// product library links, includes or calls it.  Only the test suite, the smoke
+// check (__graft_entry__.smoke) and the CPU-baseline leg of bench.py load it.
+// It shares no code, table, header or constant generator with the CUDA path.
+//
+// Every function follows one passage of the cuDNN-frontend documentation pages
+// (cited by page title and section) and is written for a reader to check by
+// eye: decode by table, dequantize, accumulate in fp64, apply the epilogue in
+// fp64, then take the quantization decisions in fp32 (the pages evaluate the
+// epilogue in FP32; "Grouped GEMM + sReLU", section "Tanh soft clamp").
+//
+// Parity pins: every function here is pinned by tests/test_oracle_*.py against
+// closed forms, brute force, invariants and a hand-worked example.  No function
+// is "parity unpinned".  The one unpinned quantity is the *rate* of one-code
+// flips caused by the device's approximate tanh; the tolerance covers it.
+//
+// Readings where the pages are silent are listed in the design doc; the ones this
+// file implements are marked "reading:" below.
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <thread>
+#include <vector>
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// Number formats.  Pages: "Grouped GEMM + Quant (SM100)", Data Types table
+// (MXFP8 = float8_e4m3fn / float8_e5m2 data with float8_e8m0fnu scales per 32;
+// NVF4 = float4_e2m1fn_x2 data with float8_e4m3fn scales per 16).  The values
+// below are the OCP microscaling format definitions written out.
+// ---------------------------------------------------------------------------
+
+enum Fmt { F_E4M3 = 0, F_E5M2 = 1, F_E2M1 = 2, F_UE8M0 = 3 };
+
+// E4M3 ("fn"): 1 sign, 4 exponent (bias 7), 3 mantissa; no infinity;
+// S.1111.111 is NaN; largest finite 448.
+double e4m3_value(uint8_t c) {
+  int s = (c >> 7) & 1, e = (c >> 3) & 0xF, m = c & 7;
+  double v;
+  if (e == 0xF && m == 7) return NAN;
+  if (e == 0) v = std::ldexp(m / 8.0, -6);          // subnormal: 0.m * 2^(1-7)
+  else v = std::ldexp(1.0 + m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+// E5M2: 1 sign, 5 exponent (bias 15), 2 mantissa; IEEE-style inf and NaN;
+// largest finite 57344.
+double e5m2_value(uint8_t c) {
+  int s = (c >> 7) & 1, e = (c >> 2) & 0x1F, m = c & 3;
+  double v;
+  if (e == 0x1F) v = (m == 0) ? INFINITY : NAN;
+  else if (e == 0) v = std::ldexp(m / 4.0, -14);
+  else v = std::ldexp(1.0 + m / 4.0, e - 15);
+  return s ? -v : v;
+}
+
+// E2M1: 1 sign, 2 exponent (bias 1), 1 mantissa; no inf/NaN; values
+// {0, 0.5, 1, 1.5, 2, 3, 4, 6}.
+double e2m1_value(uint8_t nib) {
+  int s = (nib >> 3) & 1, e = (nib >> 1) & 3, m = nib & 1;
+  double v = (e == 0) ? 0.5 * m : std::ldexp(1.0 + m / 2.0, e - 1);
+  return s ? -v : v;
+}
+
+// UE8M0: unsigned power of two 2^(c-127); 0xFF is NaN.
+double ue8m0_value(uint8_t c) { return c == 0xFF ? NAN : std::ldexp(1.0, int(c) - 127); }
+
+struct Tables {
+  double e4m3[256], e5m2[256], e2m1[16], ue8m0[256];
+  Tables() {
+    for (int c = 0; c < 256; ++c) {
+      e4m3[c] = e4m3_value(uint8_t(c));
+      e5m2[c] = e5m2_value(uint8_t(c));
+      ue8m0[c] = ue8m0_value(uint8_t(c));
+    }
+    for (int c = 0; c < 16; ++c) e2m1[c] = e2m1_value(uint8_t(c));
+  }
+};
+const Tables& tables() { static Tables t; return t; }
+
+double decode(int fmt, uint32_t code) {
+  const Tables& t = tables();
+  switch (fmt) {
+    case F_E4M3: return t.e4m3[code & 0xFF];
+    case F_E5M2: return t.e5m2[code & 0xFF];
+    case F_E2M1: return t.e2m1[code & 0xF];
+    case F_UE8M0: return t.ue8m0[code & 0xFF];
+  }
+  return NAN;
+}
+
+// Largest finite positive code of each signed format.
+uint32_t max_code(int fmt) { return fmt == F_E4M3 ? 0x7E : fmt == F_E5M2 ? 0x7B : 0x7; }
+uint32_t sign_bit(int fmt) { return fmt == F_E2M1 ? 0x8 : 0x80; }
+
+// Round-to-nearest-even with saturation to the largest finite value
+// (reading: the pages do not name the output conversion's rounding; we take
+// RNE, satfinite).  Positive codes 0..max_code are increasing in value, so the
+// nearest code is found by bisection; on an exact tie the code whose last
+// mantissa bit is 0 (the even code) wins.
+uint32_t encode_rne_satfinite(int fmt, float x) {
+  if (std::isnan(x)) return fmt == F_E2M1 ? 0x7 : 0x7F;   // E2M1 has no NaN
+  const uint32_t sgn = std::signbit(x) ? sign_bit(fmt) : 0;
+  const double ax = std::fabs(double(x));
+  const uint32_t top = max_code(fmt);
+  if (ax >= decode(fmt, top)) return sgn | top;
+  uint32_t lo = 0, hi = top;              // invariant: value(lo) <= ax < value(hi)
+  while (hi - lo > 1) {
+    uint32_t mid = (lo + hi) / 2;
+    if (decode(fmt, mid) <= ax) lo = mid; else hi = mid;
+  }
+  const double dlo = ax - decode(fmt, lo), dhi = decode(fmt, hi) - ax;
+  uint32_t pick;
+  if (dlo < dhi) pick = lo;
+  else if (dhi < dlo) pick = hi;
+  else pick = (lo % 2 == 0) ? lo : hi;
+  return sgn | pick;
+}
+
+// Scale-factor encoding for UE8M0 (reading: round UP to a power of two, so that
+// |D * norm / SFD| never exceeds q_max; the same rule the inputs use).
+// sf <= 0 (an all-zero block) encodes as code 0.
+uint32_t encode_ue8m0_ceil(float sf) {
+  if (std::isnan(sf)) return 0xFF;
+  if (!(sf > 0.0f)) return 0;
+  int p;
+  double m = std::frexp(double(sf), &p);     // sf = m * 2^p, m in [0.5, 1)
+  int e = (m == 0.5) ? p - 1 : p;            // ceil(log2(sf))
+  int code = e + 127;
+  return uint32_t(std::min(254, std::max(0, code)));
+}
+
+// ---------------------------------------------------------------------------
+// Scale-factor layout.  Pages: "Grouped GEMM + Quant (SM100)", Shapes (SFA is
+// (32, 4, ceil(rows/128), 4, ceil(ceil(K/sf_vec)/4), L)) and "Grouped GEMM +
+// SwiGLU (SM100)", Canonical layouts (physical C-contiguous order
+// (L, ceil(rows/128), ceil(kblocks/4), 32, 4, 4)).  Logical index
+// (i0, i1, i2, i3, i4, l) names row = 128*i2 + 32*i1 + i0 and
+// k-block = 4*i4 + i3.
+// ---------------------------------------------------------------------------
+int64_t sf_offset(int64_t row, int64_t kblk, int64_t l, int64_t rows, int64_t kblocks) {
+  const int64_t R = (rows + 127) / 128, KQ = (kblocks + 3) / 4;
+  const int64_t i0 = row % 32, i1 = (row / 32) % 4, i2 = row / 128;
+  const int64_t i3 = kblk % 4, i4 = kblk / 4;
+  return ((((l * R + i2) * KQ + i4) * 32 + i0) * 4 + i1) * 4 + i3;
+}
+int64_t sf_bytes(int64_t rows, int64_t kblocks, int64_t L) {
+  return L * ((rows + 127) / 128) * ((kblocks + 3) / 4) * 512;
+}
+
+// ---------------------------------------------------------------------------
+// Problem description (the oracle's own; the library's header is not used).
+// ---------------------------------------------------------------------------
+enum InFmt { IN_MXFP8_E4M3 = 0, IN_MXFP8_E5M2 = 1, IN_NVFP4 = 2 };
+enum OutFmt { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2, OUT_E4M3 = 3, OUT_E5M2 = 4, OUT_E2M1 = 5 };
+enum Epi { EPI_GATE = 0, EPI_SWIGLU = 1, EPI_SRELU = 2 };
+
+}  // namespace
+
+extern "C" {
+
+typedef struct {
+  int64_t m_pad, n, k, num_groups;
+  int32_t in_fmt, out_fmt, epi, gate_first, want_col, reserved;
+  double tanh_clamp_s;   // 0 = no clamp
+} orc_desc;
+
+// ---- exported helpers (pinned individually by the tests) ----
+double orc_decode(int fmt, uint32_t code) { return decode(fmt, code); }
+uint32_t orc_encode_rne_satfinite(int fmt, float x) { return encode_rne_satfinite(fmt, x); }
+uint32_t orc_encode_ue8m0_ceil(float sf) { return encode_ue8m0_ceil(sf); }
+int64_t orc_sf_offset(int64_t row, int64_t kblk, int64_t l, int64_t rows, int64_t kblocks) {
+  return sf_offset(row, kblk, l, rows, kblocks);
+}
+int64_t orc_sf_bytes(int64_t rows, int64_t kblocks, int64_t L) { return sf_bytes(rows, kblocks, L); }
+
+// Pack row-major logical scale factors (L, rows, kblocks) into the swizzled
+// physical layout; padding bytes are written as zero (the pages' convention
+// for untouched padding: "Grouped GEMM + SwiGLU (SM100)", JAX execution).
+void orc_pack_sf(const uint8_t* logical, uint8_t* swz, int64_t rows, int64_t kblocks, int64_t L) {
+  std::memset(swz, 0, size_t(sf_bytes(rows, kblocks, L)));
+  for (int64_t l = 0; l < L; ++l)
+    for (int64_t r = 0; r < rows; ++r)
+      for (int64_t kb = 0; kb < kblocks; ++kb)
+        swz[sf_offset(r, kb, l, rows, kblocks)] = logical[(l * rows + r) * kblocks + kb];
+}
+
+// The activation of "Grouped GEMM + SwiGLU (SM100)" Step 2 (swish(x) = x*sigmoid(x))
+// and of "Grouped GEMM + sReLU (SM100)", Equations and Tanh soft clamp.
+double orc_sigmoid(double x) { return 1.0 / (1.0 + std::exp(-x)); }
+double orc_srelu(double c, double s) {
+  double r = c > 0.0 ? c : 0.0;                 // relu
+  if (s > 0.0) r = s * std::min(std::tanh(r / s), 1.0);   // soft clamp, t capped at 1
+  return r * r;
+}
+
+// Which group owns row m: the g with padded_offsets[g-1] <= m < padded_offsets[g]
+// ("Grouped GEMM + Quant (SM100)", Equations, Step 1).  -1 if none.
+int64_t orc_group_of_row(const int32_t* off, int64_t L, int64_t m) {
+  int64_t start = 0;
+  for (int64_t g = 0; g < L; ++g) {
+    if (m >= start && m < off[g]) return g;
+    start = off[g];
+  }
+  return -1;
+}
+
+// Reference computation for the 32-row blocks listed in `blocks` (rows
+// 32*b .. 32*b+31 of the padded M extent).  Writes, for those rows only:
+//   d_ref    [nblocks*32, n_d]  fp64 D before any output conversion
+//   d_q, d_col_q, sfd_row, sfd_col   (quantized outputs; full-size buffers in
+//            the device layout; NULL when not wanted)
+//   amax     [L]: max |D| (fp32) over the computed rows of each group
+//            (reading: amax covers all rows of the group's padded range).
+// Returns 0, or a negative value for an invalid description.
+int orc_run(const orc_desc* P, const uint8_t* A, const uint8_t* SFA, const uint8_t* B,
+            const uint8_t* SFB, const int32_t* padded_offsets, const float* alpha,
+            const float* prob, float norm_const, const int64_t* blocks, int64_t nblocks,
+            double* d_ref, uint8_t* d_q, uint8_t* d_col_q, uint8_t* sfd_row,
+            uint8_t* sfd_col, float* amax, int threads);
+
+}  // extern "C"
+
+namespace {
+
+struct Job {
+  const orc_desc* P;
+  const uint8_t *A, *SFA, *B, *SFB;
+  const int32_t* off;
+  const float *alpha, *prob;
+  float norm;
+  const int64_t* blocks;
+  int64_t nblocks;
+  double* d_ref;
+  uint8_t *d_q, *d_col_q, *sfd_row, *sfd_col;
+  std::vector<float> amax;     // merged under the mutex
+  std::mutex mu;
+};
+
+bool is_fp4_in(const orc_desc* P) { return P->in_fmt == IN_NVFP4; }
+int sf_vec(const orc_desc* P) { return is_fp4_in(P) ? 16 : 32; }
+int sf_fmt(const orc_desc* P) { return is_fp4_in(P) ? F_E4M3 : F_UE8M0; }
+int data_fmt(const orc_desc* P) {
+  return P->in_fmt == IN_MXFP8_E4M3 ? F_E4M3 : P->in_fmt == IN_MXFP8_E5M2 ? F_E5M2 : F_E2M1;
+}
+bool out_quantized(const orc_desc* P) { return P->out_fmt >= OUT_E4M3; }
+int out_code_fmt(const orc_desc* P) {
+  return P->out_fmt == OUT_E4M3 ? F_E4M3 : P->out_fmt == OUT_E5M2 ? F_E5M2 : F_E2M1;
+}
+// q_max: "Grouped GEMM + Quant (SM100)", Step 3 (448 for E4M3, 57344 for E5M2);
+// 6 for E2M1, the format's largest value.
+double q_max(const orc_desc* P) {
+  return P->out_fmt == OUT_E4M3 ? 448.0 : P->out_fmt == OUT_E5M2 ? 57344.0 : 6.0;
+}
+int64_t n_out(const orc_desc* P) { return P->epi == EPI_SWIGLU ? P->n / 2 : P->n; }
+
+// Element (r, k) of a K-major low-precision operand: one byte per FP8 value,
+// two FP4 values per byte with element 2i in the low nibble (reading).
+uint32_t element_code(const orc_desc* P, const uint8_t* base, int64_t row, int64_t k) {
+  if (is_fp4_in(P)) {
+    uint8_t byte = base[row * (P->k / 2) + k / 2];
+    return (k % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+  }
+  return base[row * P->k + k];
+}
+
+// Dequantized operand row: value(code) * value(scale of its k-block).
+void dequant_row(const orc_desc* P, const uint8_t* data, const uint8_t* sf, int64_t row,
+                 int64_t rows, int64_t l, double* out) {
+  const int64_t v = sf_vec(P), kblocks = (P->k + v - 1) / v;
+  for (int64_t k = 0; k < P->k; ++k) {
+    double s = decode(sf_fmt(P), sf[sf_offset(row, k / v, l, rows, kblocks)]);
+    out[k] = decode(data_fmt(P), element_code(P, data, row, k)) * s;
+  }
+}
+
+// Step 3 of "Grouped GEMM + Quant (SM100)": for one block of values of D (a row
+// block or a column block), compute the scale factor code and the scale that
+// multiplies D before the output conversion.  Decisions in fp32:
+//   SFD = norm_const * max|D| * rcp_max,  Dq = D * (norm_const / SFD).
+struct BlockScale { uint32_t code; float scale; };
+BlockScale block_scale(const orc_desc* P, float norm, float amax_blk) {
+  const float rcp_max = float(1.0 / q_max(P));
+  const float sf = (norm * amax_blk) * rcp_max;
+  BlockScale b;
+  b.code = (sf_fmt(P) == F_UE8M0) ? encode_ue8m0_ceil(sf) : encode_rne_satfinite(F_E4M3, sf);
+  const float sfd = float(decode(sf_fmt(P), b.code));
+  // reading: a block whose max is zero (or whose scale decodes to zero) is
+  // written with scale 0, so its values stay (signed) zero.
+  b.scale = (amax_blk == 0.0f || sfd == 0.0f) ? 0.0f : norm / sfd;
+  return b;
+}
+
+void store_code(const orc_desc* P, uint8_t* buf, int64_t m, int64_t j, uint32_t code) {
+  const int64_t nd = n_out(P);
+  if (P->out_fmt == OUT_E2M1) {
+    uint8_t& byte = buf[m * (nd / 2) + j / 2];
+    if (j % 2 == 0) byte = uint8_t((byte & 0xF0) | (code & 0xF));
+    else byte = uint8_t((byte & 0x0F) | ((code & 0xF) << 4));
+  } else {
+    buf[m * nd + j] = uint8_t(code);
+  }
+}
+
+// One work item: 32-row block `bi` (index into the block list) and output
+// columns [j0, j1) of D.
+void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
+  const orc_desc* P = J.P;
+  const int64_t K = P->k, L = P->num_groups, nd = n_out(P);
+  const int64_t m0 = J.blocks[bi] * 32;
+  const int64_t v = sf_vec(P);
+  const int64_t w = j1 - j0;
+  const int64_t b_group_bytes = P->n * (is_fp4_in(P) ? K / 2 : K);
+
+  // C columns needed for D column j; `gate` picks the gate half for SwiGLU.
+  auto c_col_of = [&](int64_t j, bool gate) -> int64_t {
+    if (P->epi != EPI_SWIGLU) return j;
+    // "Grouped GEMM + SwiGLU (SM100)", Step 2: block b = j/32 pairs C columns
+    // [64b, 64b+32) (input X_b) and [64b+32, 64b+64) (gate G_b).  gate_first
+    // swaps the two, which is the order of "Grouped GEMM + GLU + Hadamard +
+    // Quant (SM100)", Equations.
+    const int64_t b = j / 32, r = j % 32;
+    const bool second = (gate != bool(P->gate_first));
+    return 64 * b + (second ? 32 : 0) + r;
+  };
+  const int64_t c0 = (P->epi == EPI_SWIGLU) ? 2 * j0 : j0;
+  const int64_t c1 = (P->epi == EPI_SWIGLU) ? 2 * j1 : j1;
+
+  // Group of each row ("Grouped GEMM + Quant (SM100)", Equations, Step 1).
+  std::vector<int64_t> grp(32);
+  for (int64_t i = 0; i < 32; ++i) grp[size_t(i)] = orc_group_of_row(J.off, L, m0 + i);
+
+  // Step 1: C[m,n] = alpha_g * sum_k dequant(A[m,k], SFA) * dequant(B[n,k,g], SFB).
+  std::vector<double> arows(size_t(32 * K), 0.0);
+  std::vector<double> brow(static_cast<size_t>(K), 0.0);
+  for (int64_t i = 0; i < 32; ++i)
+    if (grp[size_t(i)] >= 0) dequant_row(P, J.A, J.SFA, m0 + i, P->m_pad, 0, &arows[size_t(i * K)]);
+  std::vector<double> C(size_t(32 * (c1 - c0)), 0.0);
+  for (int64_t n = c0; n < c1; ++n) {
+    for (int64_t g = 0; g < L; ++g) {
+      bool used = false;
+      for (int64_t i = 0; i < 32; ++i) used = used || grp[size_t(i)] == g;
+      if (!used) continue;
+      dequant_row(P, J.B + g * b_group_bytes, J.SFB, n, P->n, g, brow.data());
+      for (int64_t i = 0; i < 32; ++i) {
+        if (grp[size_t(i)] != g) continue;
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k) acc += arows[size_t(i * K + k)] * brow[size_t(k)];
+        C[size_t(i * (c1 - c0) + (n - c0))] = double(J.alpha[g]) * acc;
+      }
+    }
+  }
+
+  // Step 2: the epilogue, in fp64.
+  std::vector<double> D(size_t(32 * w), 0.0);
+  std::vector<float> amax_local(size_t(L), 0.0f);
+  for (int64_t i = 0; i < 32; ++i) {
+    const int64_t g = grp[size_t(i)];
+    if (g < 0) continue;
+    const int64_t m = m0 + i;
+    const double p = J.prob[m];
+    auto Cv = [&](int64_t n) { return C[size_t(i * (c1 - c0) + (n - c0))]; };
+    for (int64_t j = j0; j < j1; ++j) {
+      double d;
+      if (P->epi == EPI_GATE) {
+        d = p * Cv(j);                                    // D = prob * ref
+      } else if (P->epi == EPI_SWIGLU) {
+        const double x = Cv(c_col_of(j, false)), gt = Cv(c_col_of(j, true));
+        d = p * x * (gt * orc_sigmoid(gt));               // prob * X * swish(G)
+      } else {
+        d = p * orc_srelu(Cv(j), P->tanh_clamp_s);        // prob * relu(C)^2, clamped
+      }
+      D[size_t(i * w + (j - j0))] = d;
+      J.d_ref[size_t((bi * 32 + i) * nd + j)] = d;
+      amax_local[size_t(g)] = std::max(amax_local[size_t(g)], std::fabs(float(d)));
+    }
+  }
+
+  // Step 3: output quantization (row blocks and column blocks of v values).
+  if (out_quantized(P)) {
+    const int fmt = out_code_fmt(P);
+    const int64_t kb_row = (nd + v - 1) / v;          // SFD_row is SF(m_pad, n_d)
+    const int64_t kb_col = (P->m_pad + v - 1) / v;    // SFD_col is SF(n_d, m_pad)
+    auto Dv = [&](int64_t i, int64_t j) { return float(D[size_t(i * w + (j - j0))]); };
+    if (J.d_q) {
+      for (int64_t i = 0; i < 32; ++i) {
+        if (grp[size_t(i)] < 0) continue;
+        const int64_t m = m0 + i;
+        for (int64_t jb = j0; jb < j1; jb += v) {
+          const int64_t je = std::min(jb + v, j1);
+          float am = 0.0f;
+          for (int64_t j = jb; j < je; ++j) am = std::max(am, std::fabs(Dv(i, j)));
+          const BlockScale bs = block_scale(P, J.norm, am);
+          J.sfd_row[sf_offset(m, jb / v, 0, P->m_pad, kb_row)] = uint8_t(bs.code);
+          for (int64_t j = jb; j < je; ++j)
+            store_code(P, J.d_q, m, j, encode_rne_satfinite(fmt, Dv(i, j) * bs.scale));
+        }
+      }
+    }
+    if (J.d_col_q && P->want_col) {
+      for (int64_t ib = 0; ib < 32; ib += v) {
+        bool any = false;
+        for (int64_t i = ib; i < ib + v; ++i) any = any || grp[size_t(i)] >= 0;
+        if (!any) continue;
+        for (int64_t j = j0; j < j1; ++j) {
+          float am = 0.0f;
+          for (int64_t i = ib; i < ib + v; ++i)
+            if (grp[size_t(i)] >= 0) am = std::max(am, std::fabs(Dv(i, j)));
+          const BlockScale bs = block_scale(P, J.norm, am);
+          J.sfd_col[sf_offset(j, (m0 + ib) / v, 0, nd, kb_col)] = uint8_t(bs.code);
+          for (int64_t i = ib; i < ib + v; ++i)
+            if (grp[size_t(i)] >= 0)
+              store_code(P, J.d_col_q, m0 + i, j, encode_rne_satfinite(fmt, Dv(i, j) * bs.scale));
+        }
+      }
+    }
+  }
+
+  std::lock_guard<std::mutex> lk(J.mu);
+  for (int64_t g = 0; g < L; ++g) J.amax[size_t(g)] = std::max(J.amax[size_t(g)], amax_local[size_t(g)]);
+}
+
+}  // namespace
+
+extern "C" int orc_run(const orc_desc* P, const uint8_t* A, const uint8_t* SFA, const uint8_t* B,
+                       const uint8_t* SFB, const int32_t* padded_offsets, const float* alpha,
+                       const float* prob, float norm_const, const int64_t* blocks,
+                       int64_t nblocks, double* d_ref, uint8_t* d_q, uint8_t* d_col_q,
+                       uint8_t* sfd_row, uint8_t* sfd_col, float* amax, int threads) {
+  if (!P || P->m_pad <= 0 || P->m_pad % 32 || P->n <= 0 || P->k <= 0 || P->num_groups <= 0)
+    return -1;
+  if (P->epi == EPI_SWIGLU && P->n % 64) return -2;
+  if (is_fp4_in(P) && P->k % 2) return -3;
+  const int64_t nd = n_out(P);
+  // One work item per (block, 128-column slice of D); slices are multiples of
+  // the scale-factor vector so that row blocks never straddle two items.
+  const int64_t slice = 128;
+  Job J;
+  J.P = P; J.A = A; J.SFA = SFA; J.B = B; J.SFB = SFB; J.off = padded_offsets;
+  J.alpha = alpha; J.prob = prob; J.norm = norm_const; J.blocks = blocks; J.nblocks = nblocks;
+  J.d_ref = d_ref; J.d_q = d_q; J.d_col_q = d_col_q; J.sfd_row = sfd_row; J.sfd_col = sfd_col;
+  J.amax.assign(size_t(P->num_groups), 0.0f);
+  const int64_t nslices = (nd + slice - 1) / slice;
+  const int64_t nitems = nblocks * nslices;
+  std::atomic<int64_t> next{0};
+  auto worker = [&]() {
+    for (;;) {
+      const int64_t it = next.fetch_add(1);
+      if (it >= nitems) break;
+      const int64_t bi = it / nslices, s = it % nslices;
+      run_item(J, bi, s * slice, std::min(nd, (s + 1) * slice));
+    }
+  };
+  const int nt = std::max(1, threads);
+  std::vector<std::thread> pool;
+  for (int t = 1; t < nt; ++t) pool.emplace_back(worker);
+  worker();
+  for (auto& th : pool) th.join();
+  if (amax)
+    for (int64_t g = 0; g < P->num_groups; ++g) amax[g] = J.amax[size_t(g)];
+  return 0;
+}

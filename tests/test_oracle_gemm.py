@@ -1,0 +1,333 @@
+"""Pins for the oracle's GEMM, epilogue and output quantization.
+
+* brute force: an independent dense dequantization (torch float8 decoding, the
+  listed E2M1 values) and a textbook per-group matmul;
+* closed forms of SwiGLU, sReLU and the tanh soft clamp at chosen points;
+* invariants: zero prob, linearity in alpha, expert permutation, padding rows,
+  empty groups;
+* the hand-worked example in tests/golden/hand_example.json;
+* defining properties of the block quantizer (scale is the power of two at or
+  above norm*amax/q_max; dequantized values within one output step of D).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import expit
+
+import oracle as orc
+from helpers import (E2M1_VALUES, brute_force_C, np_, oracle_inputs, oracle_run, small_problem)
+from block_scaled_grouped_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _randomize_scales(p, seed=5):
+    """Spread the scale codes so that a wrong scale index changes the result."""
+    g = torch.Generator().manual_seed(seed)
+    if p.in_fmt == "nvfp4":
+        lo, hi = 0x28, 0x48          # E4M3 scales 0.125 .. 2.0
+    else:
+        lo, hi = 118, 136            # UE8M0 scales 2^-9 .. 2^9
+    p.sfa_rows = torch.randint(lo, hi, p.sfa_rows.shape, generator=g).to(torch.uint8)
+    p.sfb_rows = torch.randint(lo, hi, p.sfb_rows.shape, generator=g).to(torch.uint8)
+    return p
+
+
+def _rows_in_groups(p):
+    off = np_(p.padded_offsets)
+    return np.arange(p.m_pad) < off[-1]
+
+
+@pytest.mark.parametrize("in_fmt", ["mxfp8_e4m3", "mxfp8_e5m2", "nvfp4"])
+def test_gate_matches_brute_force(in_fmt):
+    p = _randomize_scales(small_problem(in_fmt=in_fmt, k=160, n=96))
+    res = oracle_run(p, threads=4)
+    C = brute_force_C(p)
+    want = np_(p.prob)[:, None].astype(np.float64) * C
+    rows = _rows_in_groups(p)
+    np.testing.assert_allclose(res["d_ref"][rows], want[rows], rtol=1e-12, atol=0)
+
+
+def test_nonsquare_operands_are_not_transposed():
+    p = _randomize_scales(small_problem(counts=(40, 24), k=64, n=160))
+    res = oracle_run(p)
+    C = brute_force_C(p)
+    np.testing.assert_allclose(res["d_ref"], np_(p.prob)[:, None] * C, rtol=1e-12)
+
+
+def test_swiglu_matches_brute_force():
+    p = _randomize_scales(small_problem(epi="swiglu", n=128, k=64))
+    res = oracle_run(p)
+    C = brute_force_C(p)
+    # pair 32-column blocks: [X0 | G0 | X1 | G1 | ...]
+    Cb = C.reshape(p.m_pad, p.n // 64, 2, 32)
+    X, G = Cb[:, :, 0, :], Cb[:, :, 1, :]
+    want = np_(p.prob)[:, None] * (X * G * expit(G)).reshape(p.m_pad, p.n // 2)
+    rows = _rows_in_groups(p)
+    np.testing.assert_allclose(res["d_ref"][rows], want[rows], rtol=1e-12, atol=1e-300)
+
+
+@pytest.mark.parametrize("s", [0.0, 8.0])
+def test_srelu_matches_brute_force(s):
+    p = _randomize_scales(small_problem(epi="srelu", n=64, k=64, tanh_clamp_s=s))
+    res = oracle_run(p)
+    C = brute_force_C(p)
+    r = np.maximum(C, 0.0)
+    if s:
+        r = s * np.tanh(r / s)
+    want = np_(p.prob)[:, None] * r * r
+    rows = _rows_in_groups(p)
+    np.testing.assert_allclose(res["d_ref"][rows], want[rows], rtol=1e-12, atol=1e-300)
+
+
+# ---------------------------------------------------------------------------
+# hand-built single-term problems: C[m, n] = alpha * a_m * b_n exactly
+# ---------------------------------------------------------------------------
+
+def _single_term(b_codes, alpha=1.0, prob=1.0, a_code=0x38, epi="gate", out_fmt="f32",
+                 s=0.0, norm=1.0, want_col=False, m=32):
+    """K = 32 with only k = 0 non-zero; unit scales."""
+    n = len(b_codes)
+    p = small_problem(counts=(m,), k=32, n=n, epi=epi, out_fmt=out_fmt, pad_to=32,
+                      tanh_clamp_s=s, norm_const=norm, want_col=want_col)
+    a = torch.zeros(m, 32, dtype=torch.uint8)
+    a[:, 0] = a_code
+    b = torch.zeros(1, n, 32, dtype=torch.uint8)
+    b[0, :, 0] = torch.tensor(b_codes, dtype=torch.uint8)
+    p.a, p.b = a, b
+    p.sfa_rows = torch.full_like(p.sfa_rows, 127)
+    p.sfb_rows = torch.full_like(p.sfb_rows, 127)
+    p.alpha = torch.tensor([alpha], dtype=torch.float32)
+    p.prob = torch.full((m,), prob, dtype=torch.float32)
+    return p
+
+
+def _e4m3(x):
+    return int(torch.tensor([x]).to(torch.float8_e4m3fn).view(torch.uint8)[0])
+
+
+def test_unit_scales_reproduce_exact_fp8_products():
+    vals = [0.5, -1.5, 448.0, 2.0 ** -9, -0.0, 3.0]
+    codes = [_e4m3(v) for v in vals]
+    p = _single_term(codes, a_code=_e4m3(-6.0), out_fmt="f32")
+    d = oracle_run(p)["d_ref"][0]
+    assert list(d) == [-6.0 * v for v in vals]
+
+
+def test_hand_worked_example():
+    g = json.load(open(os.path.join(GOLDEN, "hand_example.json")))
+    m, n, k = g["m"], g["n"], g["k"]
+    p = small_problem(counts=(m,), k=k, n=n, out_fmt="e4m3", pad_to=32, want_col=True,
+                      norm_const=g["norm_const"])
+    p.a = torch.full((m, k), g["a_code"], dtype=torch.uint8)
+    p.b = torch.full((1, n, k), g["b_code"], dtype=torch.uint8)
+    p.sfa_rows = torch.full_like(p.sfa_rows, g["sf_code"])
+    p.sfb_rows = torch.full_like(p.sfb_rows, g["sf_code"])
+    p.alpha = torch.tensor([g["alpha"]])
+    p.prob = torch.full((m,), g["prob"])
+    res = oracle_run(p)
+    e = g["expected"]
+    assert (res["d_ref"] == e["D"]).all()
+    assert (res["d"] == e["dq_code"]).all() and (res["d_col"] == e["dq_code"]).all()
+    assert (res["sfd_row"][:orc.sf_bytes(m, 1, 1)].reshape(-1)[
+        [orc.sf_offset(r, 0, 0, m, 1) for r in range(m)]] == e["sfd_code"]).all()
+    assert (res["sfd_col"][[orc.sf_offset(c, 0, 0, n, 1) for c in range(n)]] == e["sfd_code"]).all()
+
+
+def test_swiglu_closed_forms_and_block_pairing():
+    # columns [0,32) = X0 = 1, [32,64) = G0 = 8, [64,96) = X1 = 4, [96,128) = G1 = 0
+    codes = [_e4m3(1.0)] * 32 + [_e4m3(8.0)] * 32 + [_e4m3(4.0)] * 32 + [0] * 32
+    p = _single_term(codes, epi="swiglu", prob=0.5)
+    d = oracle_run(p)["d_ref"][0]
+    sig8 = 1.0 / (1.0 + math.exp(-8.0))
+    assert np.allclose(d[:32], 0.5 * 1.0 * 8.0 * sig8, rtol=1e-15)
+    assert (d[32:] == 0.0).all()                      # swish(0) = 0
+    # G = ln 3: sigmoid(ln 3) = 3/4, so D = prob * X * ln3 * 3/4
+    ln3 = float(np.float32(math.log(3.0)))
+    p = _single_term([_e4m3(1.0)] * 64, epi="swiglu", prob=0.25, alpha=ln3)
+    d = oracle_run(p)["d_ref"][0]
+    assert np.allclose(d, 0.25 * ln3 * ln3 * 0.75, rtol=1e-7)
+
+
+def test_swiglu_gate_first_order_is_one_switch_away():
+    codes = [_e4m3(1.0)] * 32 + [_e4m3(8.0)] * 32
+    p = _single_term(codes, epi="swiglu")
+    d_first = oracle_run(p, gate_first=1)["d_ref"][0]
+    sig1 = 1.0 / (1.0 + math.exp(-1.0))
+    assert np.allclose(d_first, 8.0 * 1.0 * sig1, rtol=1e-15)
+
+
+def test_srelu_closed_forms():
+    p = _single_term([_e4m3(2.0), _e4m3(-2.0), 0], epi="srelu", prob=0.75)
+    d = oracle_run(p)["d_ref"][0]
+    assert list(d) == [0.75 * 4.0, 0.0, 0.0]
+    s = 8.0
+    c = float(np.float32(s * math.atanh(0.5)))     # tanh(c/s) = 1/2 -> D = prob*s^2/4
+    p = _single_term([_e4m3(1.0)], epi="srelu", prob=0.5, alpha=c, s=s)
+    d = oracle_run(p)["d_ref"][0]
+    assert np.allclose(d, 0.5 * s * s / 4.0, rtol=1e-6)
+    # soft clamp bounds D by prob * s^2 ("Grouped GEMM + sReLU", Tanh soft clamp)
+    p = _single_term([_e4m3(448.0)], epi="srelu", prob=0.5, alpha=64.0, s=s)
+    d = oracle_run(p)["d_ref"][0]
+    assert d[0] <= 0.5 * s * s and d[0] > 0.5 * s * s * (1 - 1e-12)
+    assert orc.srelu(-3.0, 0.0) == 0.0 and orc.srelu(3.0, 0.0) == 9.0
+    assert orc.sigmoid(0.0) == 0.5
+
+
+# ---------------------------------------------------------------------------
+# invariants
+# ---------------------------------------------------------------------------
+
+def test_zero_prob_rows_are_zero_and_quantize_to_zero():
+    p = small_problem(out_fmt="e4m3", want_col=True, n=64)
+    prob = np_(p.prob).copy()
+    prob[:32] = 0.0
+    res = oracle_run(p, prob=prob)
+    assert (res["d_ref"][:32] == 0.0).all()
+    assert ((res["d"][:32] & 0x7F) == 0).all()
+    kb = p.n_out // 32
+    for r in range(32):
+        for j in range(kb):
+            assert res["sfd_row"][orc.sf_offset(r, j, 0, p.m_pad, kb)] == 0
+
+
+def test_linear_in_alpha():
+    p = _randomize_scales(small_problem())
+    base = oracle_run(p)["d_ref"]
+    doubled = oracle_run(p, alpha=np_(p.alpha) * 2.0)["d_ref"]
+    assert np.array_equal(doubled, 2.0 * base)
+
+
+def test_padding_rows_are_zero_and_empty_groups_have_zero_amax():
+    p = small_problem(counts=(70, 0, 130, 20), pad_to=32)
+    res = oracle_run(p)
+    off = np_(p.padded_offsets)
+    starts = np.concatenate([[0], off[:-1]])
+    for g, c in enumerate(p.counts):
+        assert (res["d_ref"][starts[g] + c:off[g]] == 0.0).all()
+    assert res["amax"][1] == 0.0
+    assert all(res["amax"][g] > 0 for g in (0, 2, 3))
+    # amax is the max |D| over the group's rows
+    for g in (0, 2, 3):
+        blk = res["d_ref"][starts[g]:off[g]]
+        assert res["amax"][g] == np.float32(np.abs(blk).max())
+
+
+def test_expert_permutation_permutes_rows():
+    counts = (64, 32, 96)
+    p = _randomize_scales(small_problem(counts=counts, pad_to=32))
+    ins = oracle_inputs(p)
+    base = oracle_run(p, inputs=ins)["d_ref"]
+    perm = [2, 0, 1]
+    off = np_(p.padded_offsets)
+    starts = np.concatenate([[0], off[:-1]])
+    rows = np.concatenate([np.arange(starts[g], off[g]) for g in perm])
+    sfa_rows = np_(p.sfa_rows)[:, rows]
+    new = dict(ins)
+    new["a"] = ins["a"][rows]
+    new["sfa"] = orc.pack_sf(sfa_rows)
+    new["b"] = ins["b"][perm]
+    new["sfb"] = orc.pack_sf(np_(p.sfb_rows)[perm])
+    new["alpha"] = ins["alpha"][perm]
+    new["prob"] = ins["prob"][rows]
+    new["padded_offsets"] = np.cumsum([off[g] - starts[g] for g in perm]).astype(np.int32)
+    got = oracle_run(p, inputs=new)["d_ref"]
+    assert np.array_equal(got, base[rows])
+
+
+def test_rows_after_last_offset_are_untouched():
+    p = small_problem(counts=(64,), pad_to=32, out_fmt="e4m3")
+    ins = oracle_inputs(p)
+    res = orc.run(m_pad=96, n=p.n, k=p.k, num_groups=1, in_fmt=orc.IN_MXFP8_E4M3,
+                  out_fmt=orc.OUT_E4M3, epi=orc.EPI_GATE,
+                  a=np.concatenate([ins["a"], np.zeros((32, p.k), np.uint8)]),
+                  sfa=orc.pack_sf(np.concatenate([np_(p.sfa_rows), np.full((1, 32, 3), 127, np.uint8)], 1)),
+                  b=ins["b"], sfb=ins["sfb"], padded_offsets=ins["padded_offsets"],
+                  alpha=ins["alpha"], prob=np.concatenate([ins["prob"], np.ones(32, np.float32)]),
+                  outputs={"d": np.full((96, p.n), 0xAB, np.uint8)})
+    assert (res["d"][64:] == 0xAB).all()
+    assert (res["d"][:64] != 0xAB).any()
+
+
+# ---------------------------------------------------------------------------
+# quantizer properties
+# ---------------------------------------------------------------------------
+
+def _decode_out(codes, fmt):
+    if fmt == "e2m1":
+        nib = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(codes.shape[0], -1)
+        return E2M1_VALUES[nib]
+    dt = torch.float8_e4m3fn if fmt == "e4m3" else torch.float8_e5m2
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(dt).double().numpy()
+
+
+def _decode_sf(codes, in_fmt):
+    dt = torch.float8_e4m3fn if in_fmt == "nvfp4" else torch.float8_e8m0fnu
+    return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(dt).double().numpy()
+
+
+@pytest.mark.parametrize("in_fmt,out_fmt,norm", [("mxfp8_e4m3", "e4m3", 1.0),
+                                                 ("mxfp8_e4m3", "e5m2", 0.5),
+                                                 ("mxfp8_e5m2", "e4m3", 2.0),
+                                                 ("mxfp8_e4m3", "e2m1", 1.0),
+                                                 ("nvfp4", "e2m1", 1.0),
+                                                 ("nvfp4", "e2m1", 2.0 ** -12)])
+def test_row_and_column_quantization_properties(in_fmt, out_fmt, norm):
+    want_col = in_fmt != "nvfp4"
+    p = _randomize_scales(small_problem(in_fmt=in_fmt, out_fmt=out_fmt, epi="srelu",
+                                        n=128, k=64, counts=(64, 40), pad_to=32,
+                                        norm_const=norm, want_col=want_col))
+    res = oracle_run(p)
+    v = p.sf_vec
+    qmax = {"e4m3": 448.0, "e5m2": 57344.0, "e2m1": 6.0}[out_fmt]
+    D = res["d_ref"].astype(np.float32).astype(np.float64)
+    nd = p.n_out
+    rows = _rows_in_groups(p)
+    # row blocks
+    Dq = _decode_out(res["d"], out_fmt)
+    sf_row = np.array([[res["sfd_row"][orc.sf_offset(r, j, 0, p.m_pad, nd // v)]
+                        for j in range(nd // v)] for r in range(p.m_pad)])
+    sfd = _decode_sf(sf_row, in_fmt)
+    for r in np.nonzero(rows)[0]:
+        for j in range(nd // v):
+            blk = D[r, j * v:(j + 1) * v]
+            am = np.abs(blk).max()
+            if am == 0:
+                continue
+            target = norm * am / qmax
+            if in_fmt != "nvfp4":
+                # UE8M0: the smallest power of two at or above the target
+                assert sfd[r, j] >= target * (1 - 1e-6) and sfd[r, j] / 2 < target * (1 + 1e-6)
+            else:
+                # E4M3 scale: round to nearest (half a step is 2^-4 relative),
+                # saturating at 448 -- then the data saturate too
+                if target >= 448.0:
+                    assert sfd[r, j] == 448.0
+                    continue
+                assert abs(sfd[r, j] - target) <= target * 2 ** -4 + 2 ** -10
+            deq = Dq[r, j * v:(j + 1) * v] * sfd[r, j] / norm
+            # within one output step of the block's scale (coarsest step at the top)
+            step = {"e4m3": 2 ** -3, "e5m2": 2 ** -2, "e2m1": 1.0 / 3.0}[out_fmt]
+            assert np.all(np.abs(deq - blk) <= step * am + 1e-30)
+    if want_col:
+        Dc = _decode_out(res["d_col"], out_fmt)
+        for j in range(nd):
+            for b in range(p.m_pad // 32):
+                blk_rows = np.arange(b * 32, b * 32 + 32)
+                blk_rows = blk_rows[rows[blk_rows]]
+                if blk_rows.size == 0:
+                    continue
+                am = np.abs(D[blk_rows, j]).max()
+                sf = _decode_sf(np.array([res["sfd_col"][orc.sf_offset(j, b, 0, nd, p.m_pad // 32)]]),
+                                in_fmt)[0]
+                if am == 0:
+                    continue
+                target = norm * am / qmax
+                assert sf >= target * (1 - 1e-6) and sf / 2 < target * (1 + 1e-6)
+                deq = Dc[blk_rows, j] * sf / norm
+                step = {"e4m3": 2 ** -3, "e5m2": 2 ** -2, "e2m1": 1.0 / 3.0}[out_fmt]
+                assert np.all(np.abs(deq - D[blk_rows, j]) <= step * am + 1e-30)
