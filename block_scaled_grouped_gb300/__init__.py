@@ -1,0 +1,207 @@
+"""GB300 grouped block-scaled GEMM with fused MoE epilogue (Python binding).
+
+A thin ctypes binding over the C ABI in ``include/bsgg.h`` (library
+``_build/libbsgg.so``, built by ``build.py``).  It only marshals arguments:
+device pointers are taken from torch tensors, streams from torch's current
+stream.  Every step of the computation runs in the library's CUDA kernels;
+there is no CPU path, and calls fail loudly when the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import build as _build
+
+IN_FORMATS = {"mxfp8_e4m3": 0, "mxfp8_e5m2": 1, "nvfp4": 2}
+OUT_FORMATS = {"bf16": 0, "f16": 1, "f32": 2, "e4m3": 3, "e5m2": 4, "e2m1": 5}
+EPILOGUES = {"gate": 0, "swiglu": 1, "srelu": 2}
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
+          4: "device wait timed out", 5: "padded_offsets invalid"}
+
+SYMBOLS = ("bsgg_create", "bsgg_run", "bsgg_run_host", "bsgg_query_device_status", "bsgg_destroy",
+           "bsgg_status_string", "bsgg_sf_bytes", "bsgg_sf_offset", "bsgg_pack_sf")
+
+
+class BsggError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(code, code)}")
+        self.code = code
+
+
+class Desc(ctypes.Structure):
+    _fields_ = [("m_pad", ctypes.c_int64), ("n", ctypes.c_int64), ("k", ctypes.c_int64),
+                ("num_groups", ctypes.c_int32), ("in_format", ctypes.c_int32),
+                ("out_format", ctypes.c_int32), ("epilogue", ctypes.c_int32),
+                ("want_col", ctypes.c_int32), ("gate_first", ctypes.c_int32),
+                ("tanh_clamp_s", ctypes.c_float), ("reserved", ctypes.c_int32 * 3)]
+
+
+class Args(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_void_p) for name in (
+        "a", "sfa", "b", "sfb", "padded_offsets", "alpha", "prob", "norm_const",
+        "d", "d_col", "sfd_row", "sfd_col", "amax")]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """Load libbsgg.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"libbsgg.so is not built ({path}); run block_scaled_grouped_gb300.build")
+        L = ctypes.CDLL(path)
+        L.bsgg_create.restype = ctypes.c_int
+        L.bsgg_create.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(ctypes.c_void_p)]
+        L.bsgg_run.restype = ctypes.c_int
+        L.bsgg_run.argtypes = [ctypes.c_void_p, ctypes.POINTER(Args), ctypes.c_void_p]
+        L.bsgg_run_host.restype = ctypes.c_int
+        L.bsgg_run_host.argtypes = [ctypes.c_void_p, ctypes.POINTER(Args), ctypes.POINTER(Args),
+                                    ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint64),
+                                    ctypes.POINTER(ctypes.c_uint64)]
+        L.bsgg_query_device_status.restype = ctypes.c_int
+        L.bsgg_query_device_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+        L.bsgg_destroy.restype = None
+        L.bsgg_destroy.argtypes = [ctypes.c_void_p]
+        L.bsgg_status_string.restype = ctypes.c_char_p
+        L.bsgg_status_string.argtypes = [ctypes.c_int]
+        L.bsgg_sf_bytes.restype = ctypes.c_uint64
+        L.bsgg_sf_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]
+        L.bsgg_sf_offset.restype = ctypes.c_int64
+        L.bsgg_sf_offset.argtypes = [ctypes.c_int64] * 5
+        L.bsgg_pack_sf.restype = ctypes.c_int
+        L.bsgg_pack_sf.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                   ctypes.c_int32, ctypes.c_void_p]
+        _lib = L
+    return _lib
+
+
+def _check(code: int, what: str) -> None:
+    if code != 0:
+        raise BsggError(code, what)
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def sf_bytes(rows: int, cols: int, sf_vec: int, num_slices: int = 1) -> int:
+    return int(lib().bsgg_sf_bytes(rows, cols, sf_vec, num_slices))
+
+
+def sf_offset(row: int, kblk: int, l: int, rows: int, kblocks: int) -> int:
+    return int(lib().bsgg_sf_offset(row, kblk, l, rows, kblocks))
+
+
+def pack_sf(rowmajor, out=None, stream=None):
+    """Pack (L, rows, kblocks) uint8 scale codes (device tensor) into the
+    swizzled layout (flat uint8 device tensor)."""
+    import torch
+    L_, rows, kb = rowmajor.shape
+    assert rowmajor.is_cuda and rowmajor.dtype == torch.uint8 and rowmajor.is_contiguous()
+    nbytes = sf_bytes(rows, kb, 1, L_)
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=rowmajor.device)
+    assert out.numel() >= nbytes
+    _check(lib().bsgg_pack_sf(_ptr(rowmajor), _ptr(out), rows, kb, L_, _stream(stream)), "bsgg_pack_sf")
+    return out
+
+
+class Plan:
+    """A validated problem description (bsgg_create); run() launches it."""
+
+    def __init__(self, *, m_pad: int, n: int, k: int, num_groups: int, in_format: str,
+                 out_format: str, epilogue: str, want_col: bool = False, gate_first: bool = False,
+                 tanh_clamp_s: float = 0.0):
+        self.desc = Desc(m_pad, n, k, num_groups, IN_FORMATS[in_format], OUT_FORMATS[out_format],
+                         EPILOGUES[epilogue], int(bool(want_col)), int(bool(gate_first)),
+                         float(tanh_clamp_s), (ctypes.c_int32 * 3)(0, 0, 0))
+        self.in_format, self.out_format, self.epilogue = in_format, out_format, epilogue
+        self.want_col = bool(want_col)
+        h = ctypes.c_void_p()
+        _check(lib().bsgg_create(ctypes.byref(self.desc), ctypes.byref(h)), "bsgg_create")
+        self._h = h
+
+    # shapes --------------------------------------------------------------
+    @property
+    def sf_vec(self) -> int:
+        return 16 if self.in_format == "nvfp4" else 32
+
+    @property
+    def n_out(self) -> int:
+        return self.desc.n // 2 if self.epilogue == "swiglu" else self.desc.n
+
+    @property
+    def out_row_bytes(self) -> int:
+        bits = {"bf16": 16, "f16": 16, "f32": 32, "e4m3": 8, "e5m2": 8, "e2m1": 4}[self.out_format]
+        return self.n_out * bits // 8
+
+    @property
+    def quantized(self) -> bool:
+        return self.out_format in ("e4m3", "e5m2", "e2m1")
+
+    def output_bytes(self) -> dict:
+        d = self.desc
+        out = {"d": d.m_pad * self.out_row_bytes}
+        if self.quantized:
+            out["sfd_row"] = sf_bytes(d.m_pad, self.n_out, self.sf_vec, 1)
+            if self.want_col:
+                out["d_col"] = out["d"]
+                out["sfd_col"] = sf_bytes(self.n_out, d.m_pad, self.sf_vec, 1)
+        else:
+            out["amax"] = 4 * d.num_groups
+        return out
+
+    # calls ---------------------------------------------------------------
+    def _args(self, t: dict) -> Args:
+        return Args(*[_ptr(t.get(name)) for name, _ in Args._fields_])
+
+    def run(self, stream=None, **tensors) -> None:
+        """Enqueue the kernel; tensors by the bsgg_args names (device)."""
+        args = self._args(tensors)
+        _check(lib().bsgg_run(self._h, ctypes.byref(args), _stream(stream)), "bsgg_run")
+
+    def run_host(self, host: dict, dev: dict, stream=None):
+        """Host-buffer call: copies host inputs in, runs, copies outputs out
+        and synchronizes.  Returns (h2d_bytes, d2h_bytes)."""
+        hi, di = self._args(host), self._args(dev)
+        h2d, d2h = ctypes.c_uint64(), ctypes.c_uint64()
+        _check(lib().bsgg_run_host(self._h, ctypes.byref(hi), ctypes.byref(di), _stream(stream),
+                                   ctypes.byref(h2d), ctypes.byref(d2h)), "bsgg_run_host")
+        return int(h2d.value), int(d2h.value)
+
+    def device_status(self, stream=None) -> int:
+        """Synchronize and read/clear the device status word (0 = ok)."""
+        return int(lib().bsgg_query_device_status(self._h, _stream(stream)))
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib().bsgg_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

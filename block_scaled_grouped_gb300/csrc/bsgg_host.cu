@@ -1,0 +1,365 @@
+// bsgg_host.cu -- the C ABI declared in include/bsgg.h: validation (the pages'
+// "Support Surface and Constraints"), plan creation, TMA descriptor encoding,
+// kernel launch, the device status word, the scale-factor packer and the
+// host-buffer end-to-end call.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "../../include/bsgg.h"
+#include "bsgg_internal.h"
+
+struct bsgg_plan {
+  bsgg_desc desc;
+  int device;
+  int num_sms;
+  int bn;
+  int epi;
+  int outc;
+  int sf_vec;
+  int64_t kbytes;          // bytes per row of A / B
+  int64_t n_out;
+  int64_t out_row_bytes;
+  uint32_t* status;        // device word: kStatus* bits
+};
+
+namespace {
+
+using bsgg::Launch;
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+uint64_t sf_bytes_impl(int64_t rows, int64_t cols, int64_t v, int64_t L) {
+  return static_cast<uint64_t>(512) * L * ceil_div(rows, 128) * ceil_div(ceil_div(cols, v), 4);
+}
+
+bool is_quant(int out) { return out == BSGG_OUT_E4M3 || out == BSGG_OUT_E5M2 || out == BSGG_OUT_E2M1; }
+
+int out_elem_bits(int out) {
+  switch (out) {
+    case BSGG_OUT_BF16: case BSGG_OUT_F16: return 16;
+    case BSGG_OUT_F32: return 32;
+    case BSGG_OUT_E4M3: case BSGG_OUT_E5M2: return 8;
+    default: return 4;
+  }
+}
+
+bsgg_status validate(const bsgg_desc* d) {
+  if (!d) return BSGG_ERR_INVALID_ARG;
+  if (d->reserved[0] || d->reserved[1] || d->reserved[2]) return BSGG_ERR_INVALID_ARG;
+  if (d->num_groups < 1 || d->num_groups > 1024) return BSGG_ERR_INVALID_ARG;   // L <= 1024
+  if (d->m_pad <= 0 || d->m_pad % 128 != 0 || d->m_pad > (int64_t(1) << 30)) return BSGG_ERR_INVALID_ARG;
+  if (d->n <= 0 || d->k <= 0 || d->n > (int64_t(1) << 24) || d->k > (int64_t(1) << 24))
+    return BSGG_ERR_INVALID_ARG;
+  if (d->in_format < BSGG_IN_MXFP8_E4M3 || d->in_format > BSGG_IN_NVFP4) return BSGG_ERR_INVALID_ARG;
+  if (d->out_format < BSGG_OUT_BF16 || d->out_format > BSGG_OUT_E2M1) return BSGG_ERR_INVALID_ARG;
+  if (d->epilogue < BSGG_EPI_GATE || d->epilogue > BSGG_EPI_SRELU) return BSGG_ERR_INVALID_ARG;
+  if (d->gate_first != 0 && d->gate_first != 1) return BSGG_ERR_INVALID_ARG;
+  if (d->want_col != 0 && d->want_col != 1) return BSGG_ERR_INVALID_ARG;
+  // K-major rows must be 16-byte aligned ("Support Surface and Constraints",
+  // Layouts and Strides): K % 16 for FP8, K % 32 for packed FP4.
+  const bool fp4 = d->in_format == BSGG_IN_NVFP4;
+  if (d->k % (fp4 ? 32 : 16) != 0) return BSGG_ERR_INVALID_ARG;
+  // SwiGLU pairs 32-column blocks: N % 64 ("Grouped GEMM + SwiGLU (SM100)",
+  // Shapes and Divisibility).  Outputs are written in 32-column chunks.
+  if (d->epilogue == BSGG_EPI_SWIGLU ? (d->n % 64 != 0) : (d->n % 32 != 0)) return BSGG_ERR_INVALID_ARG;
+  if (!(std::isfinite(d->tanh_clamp_s) && d->tanh_clamp_s >= 0.0f)) return BSGG_ERR_INVALID_ARG;
+  if (d->tanh_clamp_s > 0.0f && d->epilogue != BSGG_EPI_SRELU) return BSGG_ERR_INVALID_ARG;
+  if (d->want_col && !is_quant(d->out_format)) return BSGG_ERR_INVALID_ARG;
+  // NVFP4 inputs: the pages allow 16/32-bit float outputs; FP4 output is this
+  // build's reading for the NVFP4 sReLU workload.  FP8 outputs from FP4 inputs
+  // are not on the pages.
+  if (fp4 && (d->out_format == BSGG_OUT_E4M3 || d->out_format == BSGG_OUT_E5M2)) return BSGG_ERR_UNSUPPORTED;
+  if (fp4 && d->want_col) return BSGG_ERR_UNSUPPORTED;   // 16-row column blocks not built
+  return BSGG_OK;
+}
+
+uint32_t make_idesc(int in_format, int bn) {
+  uint32_t fmt, scale_ue8m0;
+  if (in_format == BSGG_IN_NVFP4) { fmt = 1; scale_ue8m0 = 0; }          // E2M1, UE4M3 scales
+  else { fmt = (in_format == BSGG_IN_MXFP8_E4M3) ? 0u : 1u; scale_ue8m0 = 1; }  // E4M3/E5M2, UE8M0
+  uint32_t d = 0;
+  d |= fmt << 7;                                      // A format
+  d |= fmt << 10;                                     // B format
+  d |= static_cast<uint32_t>(bn >> 3) << 17;          // N / 8
+  d |= scale_ue8m0 << 23;                             // scale format
+  d |= static_cast<uint32_t>(bsgg::kBM >> 4) << 24;   // M / 16
+  return d;                                           // both operands K-major, no negation
+}
+
+bsgg_status encode_maps(const bsgg_plan* P, const bsgg_args* a, CUtensorMap* tmA, CUtensorMap* tmB) {
+  auto enc = get_encode_fn();
+  if (!enc) return BSGG_ERR_CUDA;
+  const bsgg_desc& d = P->desc;
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(P->kbytes), static_cast<cuuint64_t>(d.m_pad)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(P->kbytes)};
+    cuuint32_t box[2] = {bsgg::kBKBytes, bsgg::kBM};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a->a), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return BSGG_ERR_CUDA;
+  }
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(P->kbytes), static_cast<cuuint64_t>(d.n),
+                          static_cast<cuuint64_t>(d.num_groups)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(P->kbytes), static_cast<cuuint64_t>(P->kbytes * d.n)};
+    cuuint32_t box[3] = {bsgg::kBKBytes, static_cast<cuuint32_t>(P->bn), 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(a->b), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return BSGG_ERR_CUDA;
+  }
+  return BSGG_OK;
+}
+
+bsgg_status check_args(const bsgg_plan* P, const bsgg_args* a) {
+  if (!a) return BSGG_ERR_INVALID_ARG;
+  const bsgg_desc& d = P->desc;
+  const void* need[] = {a->a, a->sfa, a->b, a->sfb, a->padded_offsets, a->alpha, a->prob, a->d};
+  for (const void* p : need)
+    if (!p || !aligned16(p)) return BSGG_ERR_INVALID_ARG;
+  if (is_quant(d.out_format)) {
+    if (!a->sfd_row || !a->norm_const || !aligned16(a->sfd_row)) return BSGG_ERR_INVALID_ARG;
+    if (d.want_col && (!a->d_col || !a->sfd_col || !aligned16(a->d_col) || !aligned16(a->sfd_col)))
+      return BSGG_ERR_INVALID_ARG;
+  } else if (d.out_format != BSGG_OUT_F32 && !a->amax) {
+    return BSGG_ERR_INVALID_ARG;   // amax required for bf16/f16 D
+  }
+  return BSGG_OK;
+}
+
+__global__ void pack_sf_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t rows,
+                               int64_t kblocks, int64_t R, int64_t KQ, int64_t total) {
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    // physical order (l, row-block, k-atom, row%32, (row/32)%4, kblk%4)
+    const int64_t k4 = i & 3, r4 = (i >> 2) & 3, r32 = (i >> 4) & 31;
+    int64_t rest = i >> 9;
+    const int64_t ka = rest % KQ;
+    rest /= KQ;
+    const int64_t rb = rest % R;
+    const int64_t l = rest / R;
+    const int64_t row = rb * 128 + r4 * 32 + r32, kb = ka * 4 + k4;
+    dst[i] = (row < rows && kb < kblocks) ? src[(l * rows + row) * kblocks + kb] : uint8_t(0);
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* bsgg_status_string(bsgg_status s) {
+  switch (s) {
+    case BSGG_OK: return "ok";
+    case BSGG_ERR_INVALID_ARG: return "invalid argument";
+    case BSGG_ERR_UNSUPPORTED: return "unsupported configuration";
+    case BSGG_ERR_CUDA: return "CUDA error";
+    case BSGG_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case BSGG_ERR_BAD_OFFSETS: return "padded_offsets invalid";
+  }
+  return "unknown status";
+}
+
+uint64_t bsgg_sf_bytes(int64_t rows, int64_t cols, int32_t sf_vec, int32_t num_slices) {
+  if (rows <= 0 || cols <= 0 || sf_vec <= 0 || num_slices <= 0) return 0;
+  return sf_bytes_impl(rows, cols, sf_vec, num_slices);
+}
+
+int64_t bsgg_sf_offset(int64_t row, int64_t kblk, int64_t l, int64_t rows, int64_t kblocks) {
+  const int64_t R = ceil_div(rows, 128), KQ = ceil_div(kblocks, 4);
+  return ((l * R + row / 128) * KQ + kblk / 4) * 512 + (row % 32) * 16 + ((row / 32) % 4) * 4 + kblk % 4;
+}
+
+bsgg_status bsgg_pack_sf(const uint8_t* rowmajor, uint8_t* swizzled, int64_t rows, int64_t kblocks,
+                         int32_t num_slices, void* stream) {
+  if (!rowmajor || !swizzled || rows <= 0 || kblocks <= 0 || num_slices <= 0) return BSGG_ERR_INVALID_ARG;
+  const int64_t R = ceil_div(rows, 128), KQ = ceil_div(kblocks, 4);
+  const int64_t total = int64_t(num_slices) * R * KQ * 512;
+  const int threads = 256;
+  const int64_t blocks = std::min<int64_t>(ceil_div(total, threads), 4096);
+  pack_sf_kernel<<<static_cast<unsigned>(blocks), threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      rowmajor, swizzled, rows, kblocks, R, KQ, total);
+  return cudaGetLastError() == cudaSuccess ? BSGG_OK : BSGG_ERR_CUDA;
+}
+
+bsgg_status bsgg_create(const bsgg_desc* desc, bsgg_plan** plan) {
+  if (!plan) return BSGG_ERR_INVALID_ARG;
+  *plan = nullptr;
+  const bsgg_status v = validate(desc);
+  if (v != BSGG_OK) return v;
+  bsgg_plan* P = new (std::nothrow) bsgg_plan();
+  if (!P) return BSGG_ERR_INVALID_ARG;
+  P->desc = *desc;
+  if (cudaGetDevice(&P->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, P->device) != cudaSuccess) {
+    delete P;
+    return BSGG_ERR_CUDA;
+  }
+  P->bn = 128;
+  P->epi = desc->epilogue;
+  P->outc = desc->out_format == BSGG_OUT_E2M1 ? bsgg::OUTC_FP4
+            : is_quant(desc->out_format)      ? bsgg::OUTC_FP8
+                                              : bsgg::OUTC_FLOAT;
+  P->sf_vec = desc->in_format == BSGG_IN_NVFP4 ? 16 : 32;
+  P->kbytes = desc->in_format == BSGG_IN_NVFP4 ? desc->k / 2 : desc->k;
+  P->n_out = desc->epilogue == BSGG_EPI_SWIGLU ? desc->n / 2 : desc->n;
+  P->out_row_bytes = P->n_out * out_elem_bits(desc->out_format) / 8;
+  if (cudaMalloc(&P->status, 16) != cudaSuccess) {
+    delete P;
+    return BSGG_ERR_CUDA;
+  }
+  if (cudaMemset(P->status, 0, 16) != cudaSuccess) {
+    cudaFree(P->status);
+    delete P;
+    return BSGG_ERR_CUDA;
+  }
+  *plan = P;
+  return BSGG_OK;
+}
+
+void bsgg_destroy(bsgg_plan* plan) {
+  if (!plan) return;
+  if (plan->status) cudaFree(plan->status);
+  delete plan;
+}
+
+bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
+  if (!P) return BSGG_ERR_INVALID_ARG;
+  bsgg_status st = check_args(P, a);
+  if (st != BSGG_OK) return st;
+  const bsgg_desc& d = P->desc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Launch L;
+  std::memset(&L, 0, sizeof(L));
+  st = encode_maps(P, a, &L.tmA, &L.tmB);
+  if (st != BSGG_OK) return st;
+  if (a->amax && cudaMemsetAsync(a->amax, 0, sizeof(float) * d.num_groups, s) != cudaSuccess)
+    return BSGG_ERR_CUDA;
+
+  bsgg::Params& p = L.p;
+  p.sfa = static_cast<const uint8_t*>(a->sfa);
+  p.sfb = static_cast<const uint8_t*>(a->sfb);
+  p.offsets = a->padded_offsets;
+  p.alpha = a->alpha;
+  p.prob = a->prob;
+  p.norm_const = a->norm_const;
+  p.d = a->d;
+  p.d_col = a->d_col;
+  p.sfd_row = static_cast<uint8_t*>(a->sfd_row);
+  p.sfd_col = static_cast<uint8_t*>(a->sfd_col);
+  p.amax = a->amax;
+  p.status = P->status;
+  p.m_pad = static_cast<int32_t>(d.m_pad);
+  p.n = static_cast<int32_t>(d.n);
+  p.k = static_cast<int32_t>(d.k);
+  p.L = d.num_groups;
+  p.n_out = static_cast<int32_t>(P->n_out);
+  p.num_n_tiles = static_cast<int32_t>(ceil_div(d.n, P->bn));
+  p.num_k_stages = static_cast<int32_t>(ceil_div(P->kbytes, bsgg::kBKBytes));
+  p.num_tiles = static_cast<int32_t>((d.m_pad / bsgg::kBM) * p.num_n_tiles);
+  p.raster_w = 16;
+  p.kq_in = static_cast<int32_t>(ceil_div(ceil_div(d.k, P->sf_vec), 4));
+  p.rn_b = static_cast<int32_t>(ceil_div(d.n, 128));
+  p.kq_row = static_cast<int32_t>(ceil_div(ceil_div(P->n_out, P->sf_vec), 4));
+  p.kq_col = static_cast<int32_t>(ceil_div(ceil_div(d.m_pad, P->sf_vec), 4));
+  p.out_kind = d.out_format;
+  p.want_col = d.want_col;
+  p.gate_first = d.gate_first;
+  p.tanh_s = d.tanh_clamp_s;
+  p.tanh_rcp_s = d.tanh_clamp_s > 0.0f ? 1.0f / d.tanh_clamp_s : 0.0f;
+  const double qmax = d.out_format == BSGG_OUT_E4M3 ? 448.0 : d.out_format == BSGG_OUT_E5M2 ? 57344.0 : 6.0;
+  p.rcp_qmax = static_cast<float>(1.0 / qmax);
+  p.idesc = make_idesc(d.in_format, P->bn);
+
+  L.grid = static_cast<int>(std::min<int64_t>(p.num_tiles, P->num_sms));
+  L.bn = P->bn;
+  L.epi = P->epi;
+  L.outc = P->outc;
+  L.stream = s;
+  const cudaError_t e = (d.in_format == BSGG_IN_NVFP4) ? bsgg::launch_nvf4(L) : bsgg::launch_mxf8(L);
+  return e == cudaSuccess ? BSGG_OK : BSGG_ERR_CUDA;
+}
+
+bsgg_status bsgg_query_device_status(bsgg_plan* P, void* stream) {
+  if (!P) return BSGG_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return BSGG_ERR_CUDA;
+  uint32_t w = 0;
+  if (cudaMemcpy(&w, P->status, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return BSGG_ERR_CUDA;
+  if (cudaMemset(P->status, 0, sizeof(w)) != cudaSuccess) return BSGG_ERR_CUDA;
+  if (w & bsgg::kStatusBadOffsets) return BSGG_ERR_BAD_OFFSETS;
+  if (w & bsgg::kStatusTimeout) return BSGG_ERR_DEVICE_TIMEOUT;
+  return BSGG_OK;
+}
+
+bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* dev, void* stream,
+                          uint64_t* h2d_bytes, uint64_t* d2h_bytes) {
+  if (!P || !host || !dev) return BSGG_ERR_INVALID_ARG;
+  const bsgg_desc& d = P->desc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t L = d.num_groups;
+  const uint64_t sz_a = uint64_t(d.m_pad) * P->kbytes;
+  const uint64_t sz_sfa = sf_bytes_impl(d.m_pad, d.k, P->sf_vec, 1);
+  const uint64_t sz_b = uint64_t(L) * d.n * P->kbytes;
+  const uint64_t sz_sfb = sf_bytes_impl(d.n, d.k, P->sf_vec, L);
+  const uint64_t sz_d = uint64_t(d.m_pad) * P->out_row_bytes;
+  const uint64_t sz_sfd_row = sf_bytes_impl(d.m_pad, P->n_out, P->sf_vec, 1);
+  const uint64_t sz_sfd_col = sf_bytes_impl(P->n_out, d.m_pad, P->sf_vec, 1);
+  uint64_t in_bytes = 0, out_bytes = 0;
+  auto h2d = [&](const void* h, const void* dv, uint64_t n) -> bool {
+    if (!h) return true;
+    if (!dv) return false;
+    in_bytes += n;
+    return cudaMemcpyAsync(const_cast<void*>(dv), h, n, cudaMemcpyHostToDevice, s) == cudaSuccess;
+  };
+  auto d2h = [&](void* h, const void* dv, uint64_t n) -> bool {
+    if (!h) return true;
+    if (!dv) return false;
+    out_bytes += n;
+    return cudaMemcpyAsync(h, dv, n, cudaMemcpyDeviceToHost, s) == cudaSuccess;
+  };
+  bool ok = h2d(host->a, dev->a, sz_a) && h2d(host->sfa, dev->sfa, sz_sfa) && h2d(host->b, dev->b, sz_b) &&
+            h2d(host->sfb, dev->sfb, sz_sfb) &&
+            h2d(host->padded_offsets, dev->padded_offsets, sizeof(int32_t) * L) &&
+            h2d(host->alpha, dev->alpha, sizeof(float) * L) &&
+            h2d(host->prob, dev->prob, sizeof(float) * d.m_pad) &&
+            h2d(host->norm_const, dev->norm_const, sizeof(float));
+  if (!ok) return BSGG_ERR_CUDA;
+  bsgg_status st = bsgg_run(P, dev, stream);
+  if (st != BSGG_OK) return st;
+  ok = d2h(host->d, dev->d, sz_d) && d2h(host->d_col, dev->d_col, d.want_col ? sz_d : 0) &&
+       d2h(host->sfd_row, dev->sfd_row, sz_sfd_row) &&
+       d2h(host->sfd_col, dev->sfd_col, d.want_col ? sz_sfd_col : 0) &&
+       d2h(host->amax, dev->amax, sizeof(float) * L);
+  if (!ok) return BSGG_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return BSGG_ERR_CUDA;
+  if (h2d_bytes) *h2d_bytes = in_bytes;
+  if (d2h_bytes) *d2h_bytes = out_bytes;
+  return BSGG_OK;
+}
+
+}  // extern "C"

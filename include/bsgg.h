@@ -1,0 +1,174 @@
+/*
+ * bsgg.h -- C ABI of the GB300 grouped block-scaled GEMM with fused epilogue.
+ *
+ * The operation (cuDNN-frontend documentation, "Grouped GEMM + Quant (SM100)",
+ * Equations, Steps 1-3; "Grouped GEMM + SwiGLU (SM100)", Step 2; "Grouped GEMM
+ * + sReLU (SM100)", Equations and Tanh soft clamp):
+ *
+ *   for every expert group g and every row m in [padded_offsets[g-1], padded_offsets[g]):
+ *     C[m, n] = alpha[g] * sum_k dequant(A[m, k], SFA) * dequant(B[n, k, g], SFB)
+ *     D[m, j] = prob[m] * C[m, j]                                   (GATE)
+ *             = prob[m] * X_b * swish(G_b)  over paired 32-col blocks (SWIGLU, N/2 outputs)
+ *             = prob[m] * relu(C)^2, or (s * min(tanh(relu(C)/s), 1))^2  (SRELU)
+ *   and, for FP8/FP4 outputs, per block of v values of D along a row (SFD_row)
+ *   and along a column (SFD_col, blocks of v rows):
+ *     SFD = norm_const * max|D| / q_max  (rounded up to a power of two for UE8M0,
+ *                                         to nearest for E4M3 scales)
+ *     Dq  = convert_rne_satfinite(D * (norm_const / SFD))
+ *   For 16/32-bit outputs, amax[g] = max |D| over the rows of group g.
+ *
+ * Everything runs in hand-written CUDA kernels for sm_103a (tcgen05 block-scaled
+ * MMAs accumulating in tensor memory, TMA operand pipelines).  There is no CPU
+ * path: every entry point that computes needs a CUDA device.
+ *
+ * Conventions shared by all entry points
+ *  - Pointers in bsgg_args are DEVICE pointers (except in bsgg_run_host), owned
+ *    by the caller, and must stay valid until the stream work completes.
+ *  - All tensors are dense and C-contiguous, 16-byte aligned:
+ *      A        (m_pad, K)      K-major, 1 byte per FP8 value, FP4 packed 2 per
+ *                               byte (element 2i in the low nibble)
+ *      B        (L, N, K)       K-major, same element encoding as A
+ *      SFA      swizzled SF(m_pad, K)          (bsgg_sf_bytes(m_pad, K, v, 1) bytes)
+ *      SFB      swizzled SF(N, K) per expert   (bsgg_sf_bytes(N, K, v, L) bytes)
+ *      padded_offsets int32 (L), alpha float (L), prob float (m_pad),
+ *      norm_const float (1)
+ *      D, D_col (m_pad, N_out)  N-major; N_out = N/2 for SWIGLU, else N;
+ *                               bf16/f16/f32, or 1-byte FP8 codes, or packed FP4
+ *      SFD_row  swizzled SF(m_pad, N_out); SFD_col swizzled SF(N_out, m_pad)
+ *      amax     float (L)
+ *    where SF(rows, cols) is the pages' (32, 4, ceil(rows/128), 4,
+ *    ceil(ceil(cols/v)/4), L) layout in physical order (L, ceil(rows/128),
+ *    ceil(ceil(cols/v)/4), 32, 4, 4) ("Grouped GEMM + SwiGLU (SM100)",
+ *    Canonical layouts) and v is the scale-factor vector size (32 for MXFP8
+ *    with UE8M0 scales, 16 for NVFP4 with E4M3 scales).  Output scale factors
+ *    use the input's scale format and v ("Grouped GEMM + Quant (SM100)",
+ *    Additional Type Constraints: SFA, SFB, SFD_row, SFD_col share a dtype).
+ *  - Streams are passed as `void*` holding a cudaStream_t (NULL = legacy
+ *    default stream).  bsgg_run and bsgg_pack_sf are asynchronous.
+ *  - Errors are returned as bsgg_status; no entry point throws or aborts.
+ *    Host-side validation mirrors the pages' "Support Surface and Constraints".
+ *    Device-side values (padded_offsets) are checked by the kernel itself; a
+ *    violation is reported through bsgg_query_device_status, and the kernel
+ *    then writes no output.
+ */
+#ifndef BSGG_H
+#define BSGG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BSGG_OK = 0,
+  BSGG_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, bad shape or enum */
+  BSGG_ERR_UNSUPPORTED = 2,     /* valid on the pages but not built here */
+  BSGG_ERR_CUDA = 3,            /* a CUDA runtime call failed */
+  BSGG_ERR_DEVICE_TIMEOUT = 4,  /* a kernel wait ran out; the kernel returned early */
+  BSGG_ERR_BAD_OFFSETS = 5      /* padded_offsets not non-decreasing multiples of 128
+                                   ending at m_pad; the kernel wrote nothing */
+} bsgg_status;
+
+/* Input formats ("Grouped GEMM + Quant (SM100)", Data Types table). */
+typedef enum {
+  BSGG_IN_MXFP8_E4M3 = 0,  /* float8_e4m3fn data, float8_e8m0fnu scales, v = 32 */
+  BSGG_IN_MXFP8_E5M2 = 1,  /* float8_e5m2 data,   float8_e8m0fnu scales, v = 32 */
+  BSGG_IN_NVFP4 = 2        /* float4_e2m1fn_x2 data, float8_e4m3fn scales, v = 16 */
+} bsgg_in_format;
+
+/* Output formats of D (and D_col). */
+typedef enum {
+  BSGG_OUT_BF16 = 0, BSGG_OUT_F16 = 1, BSGG_OUT_F32 = 2,
+  BSGG_OUT_E4M3 = 3, BSGG_OUT_E5M2 = 4, BSGG_OUT_E2M1 = 5
+} bsgg_out_format;
+
+typedef enum { BSGG_EPI_GATE = 0, BSGG_EPI_SWIGLU = 1, BSGG_EPI_SRELU = 2 } bsgg_epilogue;
+
+/* Problem description, fixed at plan creation (the pages' constructor +
+ * check_support + compile, "Grouped GEMM + Quant (SM100)", Class API). */
+typedef struct {
+  int64_t m_pad;          /* rows of A/D/prob = padded_offsets[L-1]; multiple of 128 */
+  int64_t n;              /* GEMM N (rows of each expert's B); multiple of 32 (64 for SWIGLU) */
+  int64_t k;              /* reduction length in elements; multiple of 16 (FP8) / 32 (FP4) */
+  int32_t num_groups;     /* L, 1..1024 */
+  int32_t in_format;      /* bsgg_in_format */
+  int32_t out_format;     /* bsgg_out_format */
+  int32_t epilogue;       /* bsgg_epilogue */
+  int32_t want_col;       /* 1: also write D_col and SFD_col (quantized outputs only) */
+  int32_t gate_first;     /* SWIGLU block order: 0 = [X_b | G_b] ("Grouped GEMM + SwiGLU
+                             (SM100)", Step 2), 1 = [G_b | U_b] ("Grouped GEMM + GLU +
+                             Hadamard + Quant (SM100)", Equations) */
+  float tanh_clamp_s;     /* SRELU soft clamp s > 0, or 0 for none */
+  int32_t reserved[3];    /* must be zero */
+} bsgg_desc;
+
+/* Tensors of one call.  Unused outputs may be NULL: d_col/sfd_col unless
+ * want_col; sfd_row/sfd_col/norm_const for 16/32-bit outputs; amax for
+ * quantized outputs.  amax is required for BF16/F16 outputs and optional for
+ * F32 ("Grouped GEMM + Quant (SM100)", Scale Factor Output Requirements). */
+typedef struct {
+  const void* a;
+  const void* sfa;
+  const void* b;
+  const void* sfb;
+  const int32_t* padded_offsets;
+  const float* alpha;
+  const float* prob;         /* required: pass ones for no gating */
+  const float* norm_const;   /* required for quantized outputs */
+  void* d;
+  void* d_col;
+  void* sfd_row;
+  void* sfd_col;
+  float* amax;               /* zeroed by bsgg_run on the stream before the kernel */
+} bsgg_args;
+
+typedef struct bsgg_plan bsgg_plan;
+
+/* Validate `desc` and build a plan (kernel choice, launch shape, a 16-byte
+ * device status word).  The plan belongs to the device that is current at
+ * creation.  Returns BSGG_ERR_INVALID_ARG / BSGG_ERR_UNSUPPORTED for
+ * descriptions the pages or this build reject; *plan is NULL then. */
+bsgg_status bsgg_create(const bsgg_desc* desc, bsgg_plan** plan);
+
+/* Enqueue one grouped GEMM on `stream` (asynchronous, no host sync, graph
+ * capturable).  Checks pointers for presence and 16-byte alignment. */
+bsgg_status bsgg_run(bsgg_plan* plan, const bsgg_args* args, void* stream);
+
+/* End-to-end call with HOST buffers: `host` holds host pointers (pinned for
+ * speed) for every input and output to move; `dev` holds device buffers of the
+ * same shapes.  Inputs present in `host` are copied into `dev`, the kernel runs
+ * on the `dev` buffers, outputs present in `host` are copied back, and the
+ * stream is synchronized.  An input left NULL in `host` is taken as already
+ * resident in `dev`.  Bytes moved are returned in *h2d_bytes / *d2h_bytes
+ * (either may be NULL).  Allocates nothing. */
+bsgg_status bsgg_run_host(bsgg_plan* plan, const bsgg_args* host, const bsgg_args* dev,
+                          void* stream, uint64_t* h2d_bytes, uint64_t* d2h_bytes);
+
+/* Synchronize `stream`, then read and clear the plan's device status word:
+ * BSGG_OK, BSGG_ERR_DEVICE_TIMEOUT or BSGG_ERR_BAD_OFFSETS. */
+bsgg_status bsgg_query_device_status(bsgg_plan* plan, void* stream);
+
+void bsgg_destroy(bsgg_plan* plan);
+const char* bsgg_status_string(bsgg_status status);
+
+/* Bytes of the swizzled SF(rows, cols) layout with L slices and vector v:
+ * 512 * L * ceil(rows/128) * ceil(ceil(cols/v)/4). */
+uint64_t bsgg_sf_bytes(int64_t rows, int64_t cols, int32_t sf_vec, int32_t num_slices);
+
+/* Byte offset of the scale of (row, k-block, slice l) in that layout, where
+ * kblocks = ceil(cols/v).  Pure host function. */
+int64_t bsgg_sf_offset(int64_t row, int64_t kblk, int64_t l, int64_t rows, int64_t kblocks);
+
+/* Pack row-major scale codes (L, rows, kblocks) into the swizzled layout,
+ * writing every byte (padding = 0, "Grouped GEMM + SwiGLU (SM100)", JAX
+ * execution: untouched SF padding is zero).  Device pointers; asynchronous. */
+bsgg_status bsgg_pack_sf(const uint8_t* rowmajor, uint8_t* swizzled, int64_t rows,
+                         int64_t kblocks, int32_t num_slices, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSGG_H */

@@ -1,0 +1,86 @@
+"""The C ABI without a GPU: the library loads, exports every entry point
+include/bsgg.h declares, its host-only helpers agree with the oracle's layout
+map, and bsgg_create rejects what the pages' constraints reject (validation
+runs before any device call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_scaled_grouped_gb300 as bsgg
+from block_scaled_grouped_gb300 import build as bsgg_build
+import oracle as orc
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "bsgg.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    bsgg_build.build()
+    return bsgg.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(bsgg_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_functions() == sorted(bsgg.SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, text in bsgg.STATUS.items():
+        assert lib.bsgg_status_string(code).decode() == text
+
+
+def test_sf_helpers_match_the_oracle(lib):
+    for rows, cols, v, L in [(384, 256, 32, 1), (4096, 7168, 16, 3), (100, 96, 32, 2)]:
+        kb = -(-cols // v)
+        assert bsgg.sf_bytes(rows, cols, v, L) == orc.sf_bytes(rows, kb, L)
+        for (r, k, l) in [(0, 0, 0), (rows - 1, kb - 1, L - 1), (37, kb // 2, L // 2), (129, 5 % kb, 0)]:
+            assert bsgg.sf_offset(r, k, l, rows, kb) == orc.sf_offset(r, k, l, rows, kb)
+
+
+def _create(**over):
+    d = dict(m_pad=384, n=256, k=256, num_groups=2, in_format="mxfp8_e4m3", out_format="bf16",
+             epilogue="gate")
+    d.update(over)
+    desc = bsgg.Desc(d["m_pad"], d["n"], d["k"], d["num_groups"], bsgg.IN_FORMATS[d["in_format"]],
+                     bsgg.OUT_FORMATS[d["out_format"]], bsgg.EPILOGUES[d["epilogue"]],
+                     int(d.get("want_col", 0)), int(d.get("gate_first", 0)),
+                     float(d.get("tanh_clamp_s", 0.0)), (ctypes.c_int32 * 3)(*d.get("reserved", (0, 0, 0))))
+    h = ctypes.c_void_p()
+    return bsgg.lib().bsgg_create(ctypes.byref(desc), ctypes.byref(h))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(m_pad=200), 1),                       # groups are padded to 128 rows
+    (dict(num_groups=0), 1), (dict(num_groups=1025), 1),   # L <= 1024
+    (dict(k=40), 1),                            # 16-byte K-major rows
+    (dict(k=48, in_format="nvfp4"), 1),         # FP4: K % 32
+    (dict(n=96, epilogue="swiglu"), 1),         # SwiGLU pairs 32-column blocks: N % 64
+    (dict(n=80), 1),                            # outputs in 32-column chunks
+    (dict(tanh_clamp_s=-1.0, epilogue="srelu"), 1),
+    (dict(tanh_clamp_s=8.0, epilogue="gate"), 1),
+    (dict(want_col=1, out_format="bf16"), 1),   # D_col only with quantized outputs
+    (dict(reserved=(1, 0, 0)), 1),
+    (dict(in_format="nvfp4", out_format="e4m3"), 2),   # not on the pages
+    (dict(in_format="nvfp4", out_format="e2m1", want_col=1), 2),
+])
+def test_create_rejects(lib, over, code):
+    assert _create(**over) == code
+
+
+def test_null_arguments(lib):
+    assert lib.bsgg_create(None, None) == 1
+    assert lib.bsgg_run(None, None, None) == 1
+    assert lib.bsgg_query_device_status(None, None) == 1
+    lib.bsgg_destroy(None)

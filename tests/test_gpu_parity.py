@@ -1,0 +1,155 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, element
+by element, on problems the oracle finishes in seconds: several tiles, ragged
+groups (empty ones included), K and N tails, every epilogue and output format.
+
+Tolerances: BF16/F16/F32 D within 2^-7 |ref| + 1e-3 rms(ref); FP8/FP4 D and
+the scale factors bit-equal on >= 99.9% of elements and blocks, the rest
+within one code step; amax within 2^-10 relative.
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import oracle_inputs, oracle_run, small_problem
+from gpu_harness import alloc_outputs, compare, make_plan, run_gpu, to_device, SENTINEL
+from block_scaled_grouped_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _spread_scales(p, seed=7):
+    g = torch.Generator().manual_seed(seed)
+    lo, hi = (0x30, 0x40) if p.in_fmt == "nvfp4" else (122, 132)
+    p.sfa_rows = torch.randint(lo, hi, p.sfa_rows.shape, generator=g).to(torch.uint8)
+    p.sfb_rows = torch.randint(lo, hi, p.sfb_rows.shape, generator=g).to(torch.uint8)
+    return p
+
+
+def _parity(p, gate_first=False, check_amax=True):
+    ref = oracle_run(p, gate_first=int(gate_first))
+    outs, sfa, sfb = run_gpu(p, gate_first=gate_first)
+    ins = oracle_inputs(p)
+    # the library's packer and the oracle's index map agree byte for byte
+    assert np.array_equal(sfa.cpu().numpy(), ins["sfa"])
+    assert np.array_equal(sfb.cpu().numpy(), ins["sfb"])
+    compare(p, outs, ref)
+    if "amax" in outs and check_amax:
+        got = outs["amax"].cpu().numpy()
+        np.testing.assert_allclose(got, ref["amax"], rtol=2.0 ** -10, atol=0)
+    return outs, ref
+
+
+def test_tiny_workload():
+    _parity(W.workload("tiny"))
+
+
+def test_gate_bf16_ragged_groups_and_k_tail():
+    # groups 300, 0, 129, 1000, 64 rows -> padded to 128; K=416 leaves a 32-column stage
+    p = small_problem(counts=(300, 0, 129, 1000, 64), k=416, n=384, pad_to=128, seed=21)
+    _parity(_spread_scales(p))
+
+
+def test_first_and_last_group_empty_and_n_tail():
+    p = small_problem(counts=(0, 200, 0, 130, 0), k=256, n=96, pad_to=128, seed=22)
+    _parity(p)
+
+
+def test_single_group_f32_and_f16():
+    for out in ("f32", "f16"):
+        p = small_problem(counts=(256,), k=512, n=256, pad_to=128, out_fmt=out, seed=23)
+        _parity(_spread_scales(p))
+
+
+def test_e5m2_inputs():
+    p = small_problem(counts=(128, 100), k=256, n=128, pad_to=128, in_fmt="mxfp8_e5m2", seed=24)
+    _parity(p)
+
+
+@pytest.mark.parametrize("gate_first", [False, True])
+def test_swiglu_e4m3_row_and_col(gate_first):
+    p = small_problem(counts=(130, 256, 40), k=384, n=512, pad_to=128, epi="swiglu",
+                      out_fmt="e4m3", want_col=True, seed=25)
+    _parity(_spread_scales(p), gate_first=gate_first)
+
+
+def test_srelu_clamp_e4m3_norm_half():
+    p = small_problem(counts=(200, 0, 77), k=256, n=256, pad_to=128, epi="srelu", out_fmt="e4m3",
+                      want_col=True, tanh_clamp_s=8.0, norm_const=0.5, seed=26)
+    _parity(p)
+
+
+def test_srelu_e5m2_and_bf16():
+    p = small_problem(counts=(128, 300), k=512, n=256, pad_to=128, epi="srelu", out_fmt="e5m2",
+                      want_col=True, seed=27)
+    _parity(p)
+    p = small_problem(counts=(128, 300), k=512, n=256, pad_to=128, epi="srelu", out_fmt="bf16",
+                      tanh_clamp_s=4.0, seed=28)
+    _parity(p)
+
+
+def test_mxfp8_to_e2m1_with_columns():
+    p = small_problem(counts=(256, 90), k=256, n=256, pad_to=128, epi="gate", out_fmt="e2m1",
+                      want_col=True, seed=29)
+    _parity(p)
+
+
+def test_nvfp4_gate_bf16():
+    p = small_problem(counts=(150, 0, 300), k=512, n=384, pad_to=128, in_fmt="nvfp4", seed=30)
+    _parity(_spread_scales(p))
+
+
+def test_nvfp4_k_tail():
+    # K = 288: the last stage holds 32 FP4 elements (one MMA of 64, half zero-filled)
+    p = small_problem(counts=(128, 128), k=288, n=128, pad_to=128, in_fmt="nvfp4", seed=31)
+    _parity(p)
+
+
+def test_nvfp4_srelu_clamp_e2m1():
+    p = small_problem(counts=(300, 128, 0, 50), k=512, n=256, pad_to=128, in_fmt="nvfp4",
+                      epi="srelu", out_fmt="e2m1", tanh_clamp_s=8.0, seed=32)
+    _parity(p)
+
+
+def test_nvfp4_swiglu_bf16():
+    p = small_problem(counts=(128, 200), k=256, n=256, pad_to=128, in_fmt="nvfp4",
+                      epi="swiglu", out_fmt="bf16", seed=33)
+    _parity(p)
+
+
+def test_bad_offsets_are_reported_and_nothing_is_written():
+    p = to_device(small_problem(counts=(128, 128), k=128, n=128, pad_to=128, seed=34))
+    for bad in ([100, 256], [256, 128], [128, 384]):
+        p.padded_offsets = torch.tensor(bad, dtype=torch.int32, device="cuda")
+        plan = make_plan(p)
+        outs = alloc_outputs(plan)
+        import block_scaled_grouped_gb300 as bsgg
+        norm = torch.ones(1, device="cuda")
+        plan.run(a=p.a, sfa=bsgg.pack_sf(p.sfa_rows), b=p.b, sfb=bsgg.pack_sf(p.sfb_rows),
+                 padded_offsets=p.padded_offsets, alpha=p.alpha, prob=p.prob, norm_const=norm, **outs)
+        assert plan.device_status() == 5
+        assert (outs["d"] == SENTINEL).all()
+
+
+def test_host_buffer_call_matches_device_call():
+    p = small_problem(counts=(200, 60), k=256, n=256, pad_to=128, epi="swiglu", out_fmt="e4m3",
+                      want_col=True, seed=35)
+    pd = to_device(p)
+    outs, sfa, sfb = run_gpu(pd)
+    plan = make_plan(pd)
+    dev = alloc_outputs(plan)
+    dev.update(a=torch.empty_like(pd.a), sfa=torch.empty_like(sfa), b=torch.empty_like(pd.b),
+               sfb=torch.empty_like(sfb), padded_offsets=torch.empty_like(pd.padded_offsets),
+               alpha=torch.empty_like(pd.alpha), prob=torch.empty_like(pd.prob),
+               norm_const=torch.empty(1, device="cuda"))
+    host = dict(a=p.a.pin_memory(), sfa=sfa.cpu().pin_memory(), b=p.b.pin_memory(),
+                sfb=sfb.cpu().pin_memory(), padded_offsets=p.padded_offsets.pin_memory(),
+                alpha=p.alpha.pin_memory(), prob=p.prob.pin_memory(),
+                norm_const=torch.tensor([p.norm_const]).pin_memory())
+    for k_, t in outs.items():
+        host[k_] = torch.empty(t.shape, dtype=t.dtype).pin_memory()
+    h2d, d2h = plan.run_host(host, dev)
+    assert h2d == sum(host[k_].numel() * host[k_].element_size() for k_ in
+                      ("a", "sfa", "b", "sfb", "padded_offsets", "alpha", "prob", "norm_const"))
+    assert d2h == sum(t.numel() * t.element_size() for t in outs.values())
+    for k_, t in outs.items():
+        assert torch.equal(host[k_], t.cpu()), k_
