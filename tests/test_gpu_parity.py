@@ -55,9 +55,11 @@ def test_first_and_last_group_empty_and_n_tail():
 
 
 def test_single_group_f32_and_f16():
-    for out in ("f32", "f16"):
-        p = small_problem(counts=(256,), k=512, n=256, pad_to=128, out_fmt=out, seed=23)
-        _parity(_spread_scales(p))
+    p = small_problem(counts=(256,), k=512, n=256, pad_to=128, out_fmt="f32", seed=23)
+    _parity(_spread_scales(p))
+    # unit-range scales keep D inside F16's range (65504)
+    p = small_problem(counts=(256,), k=512, n=256, pad_to=128, out_fmt="f16", seed=23)
+    _parity(p)
 
 
 def test_e5m2_inputs():
