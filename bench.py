@@ -1,0 +1,408 @@
+"""Benchmark of the grouped block-scaled GEMM on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gpu|reference]
+                    [--workload fc1_swiglu|fc2_gate|fine_nvfp4|skewed|tiny]
+
+A step is one bsgg_run over one batch of the workload (all of the hot path:
+scheduling, operand fetch, block-scaled MMA, alpha/prob, activation,
+quantization, stores).  The default workload is MoE FC1 + SwiGLU (4096 tokens
+top-2 over 8 experts, K=4096, N=28672, MXFP8 in, E4M3 D and D_col with UE8M0
+SFD_row/SFD_col).  Inputs are seeded synthetic tensors generated on the device
+before timing; they are larger than L2, and steps run back to back.
+
+Metric: TFLOP/s of 2 * valid_rows * N * K (padding rows excluded).  The JSON
+line also carries the roofline of the kernel (against the measured bf16 peak
+scaled to the dtype by the nominal dense ratio), the end-to-end number through
+the host-buffer C-ABI call, the CPU oracle baseline, and the SM clocks sampled
+during the timed region.
+
+N > 1 (torchrun): every rank runs an independent replica on its own GPU (the
+operation has no exchange step); value = all ranks' FLOPs / max rank time.
+--impl reference times the CPU oracle (rank 0 only) on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "grouped GEMM TFLOP/s (valid rows) and % of GB300 dense FP8/FP4 peak, 1 GPU"
+UNIT = "TFLOP/s"
+# nominal dense tensor throughput relative to bf16 (2.25 PFLOP/s): fp8 4.5, fp4 13.5
+DTYPE_RATIO = {"mxfp8_e4m3": 2.0, "mxfp8_e5m2": 2.0, "nvfp4": 6.0}
+DTYPE_NAME = {"mxfp8_e4m3": "mxfp8(e4m3,ue8m0/32)", "mxfp8_e5m2": "mxfp8(e5m2,ue8m0/32)",
+              "nvfp4": "nvfp4(e2m1,e4m3/16)"}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    d = os.path.join(ROOT, "block_scaled_grouped_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        rec = json.load(open(path))
+    except Exception:
+        return None
+    ent = rec.get(workload)
+    if not ent or ent.get("kernel_source") != kernel_source_hash():
+        return None
+    return ent.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled in the background."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = [l for (t, l) in self.lines if self.t0 - 0.06 <= t <= self.t1 + 0.06]
+        if not rows:
+            rows = [l for (_, l) in self.lines]
+        sm, mx, reasons, power = [], [], set(), []
+        for l in rows:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                sm.append(float(f[2]))
+                mx.append(float(f[3]))
+                power.append(float(f[4]))
+            except ValueError:
+                continue
+            for name, col in (("hw_slowdown", 6), ("hw_thermal_slowdown", 7),
+                              ("sw_thermal_slowdown", 8), ("sw_power_cap", 9)):
+                if f[col].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle as a baseline (bounded sample)
+# ---------------------------------------------------------------------------
+
+def oracle_inputs(p):
+    """Host copies of a problem's inputs with the oracle's own scale packing."""
+    import oracle as orc
+    np_ = lambda t: t.detach().cpu().contiguous().numpy()
+    return dict(a=np_(p.a), b=np_(p.b), sfa=orc.pack_sf(np_(p.sfa_rows)), sfb=orc.pack_sf(np_(p.sfb_rows)),
+                padded_offsets=np_(p.padded_offsets), alpha=np_(p.alpha), prob=np_(p.prob))
+
+
+def oracle_sample(p, ins, budget_s: float, max_blocks: int = 64, seed: int = 0):
+    """Time the oracle on 32-row blocks of real rows, one call per block, until
+    budget_s of wall time is spent.  Returns (flops, seconds, blocks, threads)."""
+    import oracle as orc
+    code_in = {"mxfp8_e4m3": orc.IN_MXFP8_E4M3, "mxfp8_e5m2": orc.IN_MXFP8_E5M2, "nvfp4": orc.IN_NVFP4}
+    code_out = {"bf16": orc.OUT_BF16, "f16": orc.OUT_F16, "f32": orc.OUT_F32, "e4m3": orc.OUT_E4M3,
+                "e5m2": orc.OUT_E5M2, "e2m1": orc.OUT_E2M1}
+    code_epi = {"gate": orc.EPI_GATE, "swiglu": orc.EPI_SWIGLU, "srelu": orc.EPI_SRELU}
+    off = ins["padded_offsets"]
+    starts = np.concatenate([[0], off[:-1]])
+    real_blocks = np.unique(np.concatenate(
+        [np.arange(s, s + c) // 32 for s, c in zip(starts, p.counts) if c > 0]))
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(real_blocks)[:max_blocks]
+    threads = os.cpu_count() or 1
+    done, t0 = [], time.perf_counter()
+    for b in order:
+        orc.run(m_pad=p.m_pad, n=p.n, k=p.k, num_groups=p.num_groups, in_fmt=code_in[p.in_fmt],
+                out_fmt=code_out[p.out_fmt], epi=code_epi[p.epi], norm_const=p.norm_const,
+                tanh_clamp_s=p.tanh_clamp_s, want_col=p.want_col, blocks=np.array([b]),
+                threads=threads, **ins)
+        done.append(int(b))
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    secs = time.perf_counter() - t0
+    real = np.zeros(p.m_pad, dtype=bool)
+    for st_, c in zip(starts, p.counts):
+        real[st_:st_ + c] = True
+    rows_real = int(sum(real[32 * b:32 * b + 32].sum() for b in done))
+    flops = 2.0 * rows_real * p.n * p.k
+    return flops, secs, done, threads
+
+
+def make_workload(name: str, device):
+    from block_scaled_grouped_gb300 import workloads as W
+    return W.workload(name, device=device)
+
+
+def config_of(p, extra=None):
+    c = {"workload": p.name, "experts": p.num_groups, "rows_valid": p.m_real, "rows_padded": p.m_pad,
+         "n": p.n, "k": p.k, "in": DTYPE_NAME[p.in_fmt], "out": p.out_fmt, "epilogue": p.epi,
+         "tanh_clamp_s": p.tanh_clamp_s or None, "col_outputs": p.want_col, "norm_const": p.norm_const,
+         "l2": "inputs larger than L2 (no flush between steps)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    p = make_workload(args.workload, device)
+    per_step_budget = args.ref_step_seconds
+    import oracle
+    oracle.build()
+    ins = oracle_inputs(p)
+    for _ in range(args.warmup):
+        oracle_sample(p, ins, 0.0, max_blocks=1, seed=1000 + _)
+    tot_f, tot_s, blocks_all, threads = 0.0, 0.0, [], 1
+    for s in range(args.steps):
+        f, sec, blocks, threads = oracle_sample(p, ins, per_step_budget, max_blocks=1, seed=s)
+        tot_f += f
+        tot_s += sec
+        blocks_all += blocks
+    value = tot_f / tot_s / 1e12
+    sample = (f"{len(blocks_all)} 32-row blocks of valid rows (all N={p.n} columns, K={p.k}), "
+              f"one per step; fp64 oracle, {threads} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "config": config_of(p, {"parallelism": "none (CPU oracle)"}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, world, rank, local):
+    import block_scaled_grouped_gb300 as bsgg
+    from block_scaled_grouped_gb300 import build as bsgg_build
+    bsgg_build.build()
+    dev = torch.device("cuda", local if world > 1 else 0)
+    t0 = time.time()
+    p = make_workload(args.workload, dev)
+    torch.cuda.synchronize()
+    log(f"[bench] workload {p.name}: m_pad={p.m_pad} valid={p.m_real} n={p.n} k={p.k} "
+        f"generated in {time.time() - t0:.1f}s")
+    plan = bsgg.Plan(m_pad=p.m_pad, n=p.n, k=p.k, num_groups=p.num_groups, in_format=p.in_fmt,
+                     out_format=p.out_fmt, epilogue=p.epi, want_col=p.want_col,
+                     tanh_clamp_s=p.tanh_clamp_s)
+    sfa = bsgg.pack_sf(p.sfa_rows)
+    sfb = bsgg.pack_sf(p.sfb_rows)
+    outs = {}
+    for name, nbytes in plan.output_bytes().items():
+        if name == "amax":
+            outs[name] = torch.zeros(p.num_groups, dtype=torch.float32, device=dev)
+        else:
+            outs[name] = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    norm = torch.tensor([p.norm_const], dtype=torch.float32, device=dev)
+    tensors = dict(a=p.a, sfa=sfa, b=p.b, sfb=sfb, padded_offsets=p.padded_offsets, alpha=p.alpha,
+                   prob=p.prob, norm_const=norm, **outs)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        plan.run(stream=stream, **tensors)
+    st = plan.device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.mark(True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        plan.run(stream=stream, **tensors)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.mark(False)
+    barrier(world)
+    clocks = sampler.stop()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    st = plan.device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed region")
+    t_max_ms = max_over_ranks(elapsed_ms, world)
+    ms_per_step = t_max_ms / args.steps
+    value = world * args.steps * p.flops / (t_max_ms * 1e-3) / 1e12
+
+    # roofline of the (single) kernel of a step
+    peaks, peak_kind = measured_peaks()
+    ratio = DTYPE_RATIO[p.in_fmt]
+    peak = peaks["bf16_tflops"] * ratio
+    achieved = p.flops / (elapsed_ms / args.steps * 1e-3) / 1e12
+    traffic = recorded_traffic(p.name)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": (f"{peak_kind} bf16 burst {peaks['bf16_tflops']} TFLOP/s x "
+                                f"{ratio:g} (nominal dense {DTYPE_NAME[p.in_fmt]}/bf16 ratio)"),
+                "kernel": "bsgg_kernel", "flops_per_launch": p.flops,
+                "flops_incl_padding": 2.0 * p.m_pad * p.n * p.k}
+
+    # end to end through the host-buffer C-ABI call
+    e2e = None
+    if not args.no_e2e:
+        host = {}
+        for k_, t in tensors.items():
+            host[k_] = torch.empty(t.shape, dtype=t.dtype).pin_memory()
+        for k_ in ("a", "sfa", "b", "sfb", "padded_offsets", "alpha", "prob", "norm_const"):
+            host[k_].copy_(tensors[k_].cpu())
+        dev_bufs = dict(tensors)
+        plan.run_host(host, dev_bufs, stream=stream)      # warm-up
+        n_e2e = max(3, min(args.steps, 10))
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            h2d, d2h = plan.run_host(host, dev_bufs, stream=stream)
+        e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, world)
+        e2e = {"value": world * p.flops / e2e_s / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
+               "what": "bsgg_run_host: every input (weights included) copied from pinned host "
+                       "memory, every output copied back, stream synchronized"}
+
+    cpu_baseline = None
+    if rank == 0 and not args.no_cpu_baseline:
+        f, secs, blocks, threads = oracle_sample(p, oracle_inputs(p), args.cpu_seconds)
+        cpu_baseline = {"value": f / secs / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+                        "sample": f"{len(blocks)} random 32-row blocks of valid rows, all N={p.n} "
+                                  f"columns, K={p.k}; {secs:.1f} s of fp64 oracle work on "
+                                  f"{threads} threads"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[p.in_fmt],
+                "data": "synthetic (seeded MoE routing, N(0,1) draws quantized to the input format)",
+                "config": config_of(p, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
+                "gpu_launches": args.steps, "clocks": clocks, "roofline": roofline,
+                "e2e": e2e, "cpu_baseline": cpu_baseline,
+                "pct_of_dtype_peak": 100.0 * achieved / peak}
+        print(json.dumps(line), flush=True)
+    plan.close()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("gpu", "reference"), default="gpu")
+    ap.add_argument("--workload", default="fc1_swiglu")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=0.0)
+    args = ap.parse_args()
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py --impl gpu needs a CUDA device")
+        run_gpu(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -10,7 +10,8 @@
 //               atoms to tensor memory (tcgen05.cp) and issues block-scaled
 //               tcgen05.mma (MXFP8 kind::mxf8f6f4 or NVFP4 kind::mxf4nvf4) into
 //               one of NUM_ACC fp32 accumulators in tensor memory
-//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quadrant, alpha, the
+//   warps 2..9  epilogue, two warps per 32-lane tensor-memory quadrant, each
+//               taking every other 32-column chunk: tcgen05.ld, alpha, the
 //               activation and prob (Step 2), then per-group amax or the row /
 //               column block quantization (Step 3), and global stores
 // All waits are bounded; a wait that runs out raises a CTA-wide abort flag and
@@ -32,7 +33,8 @@ enum : int { OK_BF16 = 0, OK_F16 = 1, OK_F32 = 2, OK_E4M3 = 3, OK_E5M2 = 4, OK_E
 
 constexpr int kBM = 128;          // rows per tile (TMEM lanes)
 constexpr int kBKBytes = 128;     // K bytes per pipeline stage (one 128-byte swizzle span)
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;     // two warps per tensor-memory lane quadrant
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxGroups = 1024;
 constexpr uint32_t kStatusTimeout = 1u;
 constexpr uint32_t kStatusBadOffsets = 2u;
@@ -237,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int i = tid; i < p.L; i += kThreads) s_off[i] = p.offsets[i];
   if (tid == 0) {
     for (int s = 0; s < S; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
-    for (int a = 0; a < NA; ++a) { mbar_init(accf_bar(a), 1); mbar_init(acce_bar(a), 4); }
+    for (int a = 0; a < NA; ++a) { mbar_init(accf_bar(a), 1); mbar_init(acce_bar(a), kEpiWarps); }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -377,6 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                       // tensor-memory lane quadrant
+    const int e = (warp - 2) >> 2;                // which of the quadrant's two warps
     const float norm = (OUTC == OUTC_FLOAT) ? 1.0f : *p.norm_const;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -396,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float al = p.alpha[g];
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       float amax_local = 0.0f;
-      for (int ch = 0; ch < kChunks; ++ch) {
+      for (int ch = e; ch < kChunks; ch += 2) {
         uint32_t ra[32], rb[32];
         if (EPI == EPI_SWIGLU) {
           const int cx = ch * 64 + (p.gate_first ? 32 : 0);
@@ -407,8 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(taddr + ch * 32, ra);
         }
         tmem_wait_ld();
-        if (ch == kChunks - 1) {
-          // the accumulator is in registers: hand it back to the MMA warp
+        if (ch + 2 >= kChunks) {
+          // this warp's part of the accumulator is in registers: hand it back
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(acce_bar(acc));
@@ -427,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[i] = pr * (r * r);
           } else {
             const float gt = al * __uint_as_float(rb[i]);
-            const float sig = 1.0f / (1.0f + __expf(-gt));
+            const float sig = __fdividef(1.0f, 1.0f + __expf(-gt));
             v[i] = pr * c * (gt * sig);
           }
         }
@@ -477,16 +480,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           store_q32<OUTC>(static_cast<uint8_t*>(p.d) + row * row_bytes + col_byte0, v, sc, p.out_kind);
           // ---- column blocks: 32 rows = the 32 lanes of this warp (v = 32)
           if (!FP4 && p.want_col) {
-            uint32_t my_code = 0;
+            // column j's max over the warp's 32 rows; lane j keeps it, encodes
+            // that column's scale and shares the factor with the other lanes
+            float my_am = 0.0f;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const float am = __uint_as_float(redux_max_u32(__float_as_uint(fabsf(v[j]))));
-              uint32_t code;
-              float s;
-              block_scale<false>(am, norm, p.rcp_qmax, code, s);
-              sc[j] = s;
-              if (lane == j) my_code = code;
+              my_am = (lane == j) ? am : my_am;
             }
+            uint32_t my_code;
+            float my_scale;
+            block_scale<false>(my_am, norm, p.rcp_qmax, my_code, my_scale);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sc[j] = __shfl_sync(0xffffffffu, my_scale, j);
             store_q32<OUTC>(static_cast<uint8_t*>(p.d_col) + row * row_bytes + col_byte0, v, sc, p.out_kind);
             p.sfd_col[sf_off(col0 + lane, mt * 4 + q, p.kq_col)] = static_cast<uint8_t>(my_code);
           }
