@@ -21,7 +21,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CU
           4: "device wait timed out", 5: "padded_offsets invalid"}
 
 SYMBOLS = ("bsgg_create", "bsgg_run", "bsgg_run_host", "bsgg_query_device_status", "bsgg_destroy",
-           "bsgg_status_string", "bsgg_sf_bytes", "bsgg_sf_offset", "bsgg_pack_sf")
+           "bsgg_status_string", "bsgg_sf_bytes", "bsgg_sf_offset", "bsgg_pack_sf", "bsgg_run_noalloc")
 
 
 class BsggError(RuntimeError):
@@ -77,6 +77,9 @@ def lib():
         L.bsgg_sf_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]
         L.bsgg_sf_offset.restype = ctypes.c_int64
         L.bsgg_sf_offset.argtypes = [ctypes.c_int64] * 5
+        L.bsgg_run_noalloc.restype = ctypes.c_int
+        L.bsgg_run_noalloc.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(Args), ctypes.c_void_p,
+                                       ctypes.c_int32]
         L.bsgg_pack_sf.restype = ctypes.c_int
         L.bsgg_pack_sf.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                    ctypes.c_int32, ctypes.c_void_p]
@@ -205,3 +208,18 @@ class Plan:
             self.close()
         except Exception:
             pass
+
+
+def run_noalloc(*, m_pad: int, n: int, k: int, num_groups: int, in_format: str, out_format: str,
+                epilogue: str, want_col: bool = False, gate_first: bool = False,
+                tanh_clamp_s: float = 0.0, stream=None, wait_status: bool = True, **tensors) -> int:
+    """bsgg_run_noalloc: one call without a plan and without any device
+    allocation (for callers whose device memory is owned by someone else, or
+    who must not let cudaMalloc synchronize the device).  Returns the status
+    code (the device status when wait_status is true)."""
+    desc = Desc(m_pad, n, k, num_groups, IN_FORMATS[in_format], OUT_FORMATS[out_format],
+                EPILOGUES[epilogue], int(bool(want_col)), int(bool(gate_first)), float(tanh_clamp_s),
+                (ctypes.c_int32 * 3)(0, 0, 0))
+    args = Args(*[_ptr(tensors.get(name)) for name, _ in Args._fields_])
+    return int(lib().bsgg_run_noalloc(ctypes.byref(desc), ctypes.byref(args), _stream(stream),
+                                      int(bool(wait_status))))

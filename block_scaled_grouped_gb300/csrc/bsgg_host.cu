@@ -363,3 +363,85 @@ bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.  For callers that cannot allocate device memory
+// when they call in (a framework pool that already holds the device memory, a
+// serving loop that must not let cudaMalloc/cudaFree synchronize the device, a
+// plug-in whose host application owns memory): the status word that a plan
+// would cudaMalloc lives instead in this file-scope device array, which every
+// GPU that loads the library holds until the process exits.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) uint32_t g_noalloc_scratch[BSGG_NOALLOC_SCRATCH_BYTES / sizeof(uint32_t)];
+
+namespace {
+
+constexpr size_t kNoAllocStatusBytes = sizeof(uint32_t);   // scratch one call needs
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoAllocMaxDevices];
+int g_noalloc_sms[kNoAllocMaxDevices];
+
+// Once per device, with that device current: the array's device address (a
+// host-side reference to the array is only a stand-in, never a device
+// pointer) and the SM count.
+bsgg_status noalloc_setup(int dev, uint32_t** scratch, int* sms) {
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr)
+      return BSGG_ERR_CUDA;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return BSGG_ERR_CUDA;
+    g_noalloc_sms[dev] = n;
+    g_noalloc_addr[dev] = addr;
+  }
+  *scratch = static_cast<uint32_t*>(g_noalloc_addr[dev]);
+  *sms = g_noalloc_sms[dev];
+  return BSGG_OK;
+}
+
+}  // namespace
+
+extern "C" bsgg_status bsgg_run_noalloc(const bsgg_desc* desc, const bsgg_args* args, void* stream,
+                                        int32_t wait_status) {
+  const bsgg_status v = validate(desc);
+  if (v != BSGG_OK) return v;
+  if (kNoAllocStatusBytes > sizeof(g_noalloc_scratch)) return BSGG_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return BSGG_ERR_CUDA;
+  uint32_t* scratch = nullptr;
+  int sms = 0;
+  const bsgg_status su = noalloc_setup(dev, &scratch, &sms);
+  if (su != BSGG_OK) return su;
+
+  // A plan on the stack, derived from `desc` exactly as bsgg_create derives
+  // it, whose status word is the static scratch.
+  bsgg_plan P;
+  P.desc = *desc;
+  P.device = dev;
+  P.num_sms = sms;
+  P.bn = 128;
+  P.epi = desc->epilogue;
+  P.outc = desc->out_format == BSGG_OUT_E2M1 ? bsgg::OUTC_FP4
+           : is_quant(desc->out_format)      ? bsgg::OUTC_FP8
+                                             : bsgg::OUTC_FLOAT;
+  P.sf_vec = desc->in_format == BSGG_IN_NVFP4 ? 16 : 32;
+  P.kbytes = desc->in_format == BSGG_IN_NVFP4 ? desc->k / 2 : desc->k;
+  P.n_out = desc->epilogue == BSGG_EPI_SWIGLU ? desc->n / 2 : desc->n;
+  P.out_row_bytes = P.n_out * out_elem_bits(desc->out_format) / 8;
+  P.status = scratch;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(scratch, 0, kNoAllocStatusBytes, s) != cudaSuccess) return BSGG_ERR_CUDA;
+  const bsgg_status st = bsgg_run(&P, args, stream);
+  if (st != BSGG_OK || !wait_status) return st;
+  uint32_t w = 0;
+  if (cudaMemcpyAsync(&w, scratch, sizeof(w), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return BSGG_ERR_CUDA;
+  if (w & bsgg::kStatusBadOffsets) return BSGG_ERR_BAD_OFFSETS;
+  if (w & bsgg::kStatusTimeout) return BSGG_ERR_DEVICE_TIMEOUT;
+  return BSGG_OK;
+}

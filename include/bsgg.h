@@ -167,6 +167,37 @@ int64_t bsgg_sf_offset(int64_t row, int64_t kblk, int64_t l, int64_t rows, int64
 bsgg_status bsgg_pack_sf(const uint8_t* rowmajor, uint8_t* swizzled, int64_t rows,
                          int64_t kblocks, int32_t num_slices, void* stream);
 
+/* Size of the library-owned device scratch used by bsgg_run_noalloc. */
+#define BSGG_NOALLOC_SCRATCH_BYTES 256
+
+/* Allocation-free run (the pages have no counterpart; this is a library
+ * convenience).  Same computation, arguments and validation as bsgg_create +
+ * bsgg_run + bsgg_destroy, but it creates no plan and never calls cudaMalloc
+ * or cudaFree.  It is for callers that cannot allocate device memory at the
+ * point of the call: a framework whose own pool has already reserved the
+ * device memory (a raw cudaMalloc would fail or fragment it), a serving loop
+ * that must not let cudaMalloc/cudaFree synchronize the device, or a plug-in
+ * inside a host application that owns memory management.
+ *
+ * The kernel's only scratch, its 4-byte device status word, lives in a
+ * file-scope static device array of BSGG_NOALLOC_SCRATCH_BYTES bytes that every
+ * GPU which loads the library holds until the process exits.  A call whose
+ * scratch need exceeded that array would be rejected with
+ * BSGG_ERR_UNSUPPORTED; the need is one word for every problem the validation
+ * accepts.
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  Every call clears the status word on `stream` before its
+ * kernel.  All calls share the array, which keeps the last call's contents:
+ * calls whose kernels overlap on the GPU (several streams, several host
+ * threads) race on it, so run them on one stream when the status matters.
+ * With wait_status != 0 the call synchronizes `stream` after the launch and
+ * returns the device status (BSGG_OK, BSGG_ERR_DEVICE_TIMEOUT or
+ * BSGG_ERR_BAD_OFFSETS); with 0 it returns once the kernel is enqueued. */
+bsgg_status bsgg_run_noalloc(const bsgg_desc* desc, const bsgg_args* args, void* stream,
+                             int32_t wait_status);
+
 #ifdef __cplusplus
 }
 #endif
