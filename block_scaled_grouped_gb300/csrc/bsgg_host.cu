@@ -9,6 +9,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <algorithm>
 #include <new>
 
 #include "../../include/bsgg.h"
@@ -18,6 +19,8 @@ struct bsgg_plan {
   bsgg_desc desc;
   int device;
   int num_sms;
+  int grid;                // CTAs per launch (a multiple of 2 for pairs)
+  bool pair;               // 256 x 256 tiles on CTA pairs
   int bn;
   int epi;
   int outc;
@@ -67,7 +70,12 @@ int out_elem_bits(int out) {
 
 bsgg_status validate(const bsgg_desc* d) {
   if (!d) return BSGG_ERR_INVALID_ARG;
-  if (d->reserved[0] || d->reserved[1] || d->reserved[2]) return BSGG_ERR_INVALID_ARG;
+  if (d->reserved != 0) return BSGG_ERR_INVALID_ARG;
+  // tile shape: the pages' mma_tiler_mn with TILE_M in {128, 256} (256 = 2-CTA
+  // instructions) and TILE_N in {128, 256}; pairs are built for 256 x 256 only
+  if (d->tile_m != 0 && d->tile_m != 128 && d->tile_m != 256) return BSGG_ERR_INVALID_ARG;
+  if (d->tile_n != 0 && d->tile_n != 128 && d->tile_n != 256) return BSGG_ERR_INVALID_ARG;
+  if (d->tile_m == 256 && d->tile_n == 128) return BSGG_ERR_UNSUPPORTED;
   if (d->num_groups < 1 || d->num_groups > 1024) return BSGG_ERR_INVALID_ARG;   // L <= 1024
   if (d->m_pad <= 0 || d->m_pad % 128 != 0 || d->m_pad > (int64_t(1) << 30)) return BSGG_ERR_INVALID_ARG;
   if (d->n <= 0 || d->k <= 0 || d->n > (int64_t(1) << 24) || d->k > (int64_t(1) << 24))
@@ -95,7 +103,7 @@ bsgg_status validate(const bsgg_desc* d) {
   return BSGG_OK;
 }
 
-uint32_t make_idesc(int in_format, int bn) {
+uint32_t make_idesc(int in_format, int bn, bool pair) {
   uint32_t fmt, scale_ue8m0;
   if (in_format == BSGG_IN_NVFP4) { fmt = 1; scale_ue8m0 = 0; }          // E2M1, UE4M3 scales
   else { fmt = (in_format == BSGG_IN_MXFP8_E4M3) ? 0u : 1u; scale_ue8m0 = 1; }  // E4M3/E5M2, UE8M0
@@ -104,34 +112,82 @@ uint32_t make_idesc(int in_format, int bn) {
   d |= fmt << 10;                                     // B format
   d |= static_cast<uint32_t>(bn >> 3) << 17;          // N / 8
   d |= scale_ue8m0 << 23;                             // scale format
-  d |= static_cast<uint32_t>(bsgg::kBM >> 4) << 24;   // M / 16
+  d |= static_cast<uint32_t>((pair ? 2 * bsgg::kBM : bsgg::kBM) >> 4) << 24;   // M / 16
   return d;                                           // both operands K-major, no negation
 }
 
-bsgg_status encode_maps(const bsgg_plan* P, const bsgg_args* a, CUtensorMap* tmA, CUtensorMap* tmB) {
+bsgg_status encode_one(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                       const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
   auto enc = get_encode_fn();
   if (!enc) return BSGG_ERR_CUDA;
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
+                         dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BSGG_OK : BSGG_ERR_CUDA;
+}
+
+// A (m_pad, K bytes) and B (L, N, K bytes) as 128-byte-swizzled boxes of
+// 128 K-bytes x 128 rows / x (rows of B this CTA holds); the scale factors as
+// (256 bytes, 2 * atoms, 128-row blocks) so that one box moves a stage's
+// 512-byte atoms of one (SFA) or two (SFB, tile_n = 256) row blocks.
+bsgg_status encode_maps(const bsgg_plan* P, const bsgg_args* a, bsgg::Launch* L) {
   const bsgg_desc& d = P->desc;
+  const int64_t kq = ceil_div(ceil_div(d.k, P->sf_vec), 4);
+  const int atoms = P->desc.in_format == BSGG_IN_NVFP4 ? 4 : 1;
+  bsgg_status st;
   {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(P->kbytes), static_cast<cuuint64_t>(d.m_pad)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(P->kbytes)};
+    cuuint64_t dims[2] = {cuuint64_t(P->kbytes), cuuint64_t(d.m_pad)};
+    cuuint64_t strides[1] = {cuuint64_t(P->kbytes)};
     cuuint32_t box[2] = {bsgg::kBKBytes, bsgg::kBM};
-    cuuint32_t es[2] = {1, 1};
-    CUresult r = enc(tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a->a), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return BSGG_ERR_CUDA;
+    if ((st = encode_one(&L->tmA, a->a, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) != BSGG_OK) return st;
   }
   {
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(P->kbytes), static_cast<cuuint64_t>(d.n),
-                          static_cast<cuuint64_t>(d.num_groups)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(P->kbytes), static_cast<cuuint64_t>(P->kbytes * d.n)};
-    cuuint32_t box[3] = {bsgg::kBKBytes, static_cast<cuuint32_t>(P->bn), 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = enc(tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(a->b), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return BSGG_ERR_CUDA;
+    cuuint64_t dims[3] = {cuuint64_t(P->kbytes), cuuint64_t(d.n), cuuint64_t(d.num_groups)};
+    cuuint64_t strides[2] = {cuuint64_t(P->kbytes), cuuint64_t(P->kbytes * d.n)};
+    cuuint32_t box[3] = {bsgg::kBKBytes, cuuint32_t(P->pair ? P->bn / 2 : P->bn), 1};
+    if ((st = encode_one(&L->tmB, a->b, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) != BSGG_OK) return st;
+  }
+  {
+    cuuint64_t dims[3] = {256, cuuint64_t(2 * kq), cuuint64_t(ceil_div(d.m_pad, 128))};
+    cuuint64_t strides[2] = {256, cuuint64_t(512 * kq)};
+    cuuint32_t box[3] = {256, cuuint32_t(2 * atoms), 1};
+    if ((st = encode_one(&L->tmSFA, a->sfa, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) != BSGG_OK)
+      return st;
+  }
+  {
+    cuuint64_t dims[3] = {256, cuuint64_t(2 * kq), cuuint64_t(ceil_div(d.n, 128) * d.num_groups)};
+    cuuint64_t strides[2] = {256, cuuint64_t(512 * kq)};
+    cuuint32_t box[3] = {256, cuuint32_t(2 * atoms), cuuint32_t(P->bn / 128)};
+    if ((st = encode_one(&L->tmSFB, a->sfb, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) != BSGG_OK)
+      return st;
+  }
+  return BSGG_OK;
+}
+
+// Everything a plan derives from its description and the current device.
+bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan* P) {
+  P->desc = *desc;
+  P->device = device;
+  P->num_sms = num_sms;
+  const int tm = desc->tile_m ? desc->tile_m : 256;
+  const int tn = desc->tile_n ? desc->tile_n : 256;
+  P->pair = (tm == 256);
+  P->bn = P->pair ? 256 : tn;
+  P->epi = desc->epilogue;
+  P->outc = desc->out_format == BSGG_OUT_E2M1 ? bsgg::OUTC_FP4
+            : is_quant(desc->out_format)      ? bsgg::OUTC_FP8
+                                              : bsgg::OUTC_FLOAT;
+  P->sf_vec = desc->in_format == BSGG_IN_NVFP4 ? 16 : 32;
+  P->kbytes = desc->in_format == BSGG_IN_NVFP4 ? desc->k / 2 : desc->k;
+  P->n_out = desc->epilogue == BSGG_EPI_SWIGLU ? desc->n / 2 : desc->n;
+  P->out_row_bytes = P->n_out * out_elem_bits(desc->out_format) / 8;
+  if (P->pair) {
+    int resident = bsgg::pair_resident_ctas(desc->in_format == BSGG_IN_NVFP4);
+    if (resident <= 0) resident = num_sms;
+    P->grid = std::max(2, (std::min(resident, num_sms) / 2) * 2);
+  } else {
+    P->grid = num_sms;
   }
   return BSGG_OK;
 }
@@ -219,15 +275,10 @@ bsgg_status bsgg_create(const bsgg_desc* desc, bsgg_plan** plan) {
     delete P;
     return BSGG_ERR_CUDA;
   }
-  P->bn = 128;
-  P->epi = desc->epilogue;
-  P->outc = desc->out_format == BSGG_OUT_E2M1 ? bsgg::OUTC_FP4
-            : is_quant(desc->out_format)      ? bsgg::OUTC_FP8
-                                              : bsgg::OUTC_FLOAT;
-  P->sf_vec = desc->in_format == BSGG_IN_NVFP4 ? 16 : 32;
-  P->kbytes = desc->in_format == BSGG_IN_NVFP4 ? desc->k / 2 : desc->k;
-  P->n_out = desc->epilogue == BSGG_EPI_SWIGLU ? desc->n / 2 : desc->n;
-  P->out_row_bytes = P->n_out * out_elem_bits(desc->out_format) / 8;
+  if (init_plan(desc, P->device, P->num_sms, P) != BSGG_OK) {
+    delete P;
+    return BSGG_ERR_CUDA;
+  }
   if (cudaMalloc(&P->status, 16) != cudaSuccess) {
     delete P;
     return BSGG_ERR_CUDA;
@@ -255,14 +306,12 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Launch L;
   std::memset(&L, 0, sizeof(L));
-  st = encode_maps(P, a, &L.tmA, &L.tmB);
+  st = encode_maps(P, a, &L);
   if (st != BSGG_OK) return st;
   if (a->amax && cudaMemsetAsync(a->amax, 0, sizeof(float) * d.num_groups, s) != cudaSuccess)
     return BSGG_ERR_CUDA;
 
   bsgg::Params& p = L.p;
-  p.sfa = static_cast<const uint8_t*>(a->sfa);
-  p.sfb = static_cast<const uint8_t*>(a->sfb);
   p.offsets = a->padded_offsets;
   p.alpha = a->alpha;
   p.prob = a->prob;
@@ -280,9 +329,7 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   p.n_out = static_cast<int32_t>(P->n_out);
   p.num_n_tiles = static_cast<int32_t>(ceil_div(d.n, P->bn));
   p.num_k_stages = static_cast<int32_t>(ceil_div(P->kbytes, bsgg::kBKBytes));
-  p.num_tiles = static_cast<int32_t>((d.m_pad / bsgg::kBM) * p.num_n_tiles);
-  p.raster_w = 16;
-  p.kq_in = static_cast<int32_t>(ceil_div(ceil_div(d.k, P->sf_vec), 4));
+  p.raster_w = P->bn == 256 ? 8 : 16;
   p.rn_b = static_cast<int32_t>(ceil_div(d.n, 128));
   p.kq_row = static_cast<int32_t>(ceil_div(ceil_div(P->n_out, P->sf_vec), 4));
   p.kq_col = static_cast<int32_t>(ceil_div(ceil_div(d.m_pad, P->sf_vec), 4));
@@ -293,14 +340,22 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   p.tanh_rcp_s = d.tanh_clamp_s > 0.0f ? 1.0f / d.tanh_clamp_s : 0.0f;
   const double qmax = d.out_format == BSGG_OUT_E4M3 ? 448.0 : d.out_format == BSGG_OUT_E5M2 ? 57344.0 : 6.0;
   p.rcp_qmax = static_cast<float>(1.0 / qmax);
-  p.idesc = make_idesc(d.in_format, P->bn);
+  p.idesc = make_idesc(d.in_format, P->bn, P->pair);
 
-  L.grid = static_cast<int>(std::min<int64_t>(p.num_tiles, P->num_sms));
+  // an upper bound of the tiles (pairs may add one tile row per group)
+  const int64_t rows = P->pair ? ceil_div(d.m_pad, 256) + d.num_groups : d.m_pad / bsgg::kBM;
+  const int64_t tiles = rows * p.num_n_tiles;
+  L.grid = static_cast<int>(std::min<int64_t>(P->grid, P->pair ? 2 * tiles : tiles));
+  L.pair = P->pair;
   L.bn = P->bn;
   L.epi = P->epi;
   L.outc = P->outc;
   L.stream = s;
-  const cudaError_t e = (d.in_format == BSGG_IN_NVFP4) ? bsgg::launch_nvf4(L) : bsgg::launch_mxf8(L);
+  cudaError_t e;
+  if (d.in_format == BSGG_IN_NVFP4)
+    e = P->pair ? bsgg::launch_nvf4_pair(L) : P->bn == 256 ? bsgg::launch_nvf4_256(L) : bsgg::launch_nvf4_128(L);
+  else
+    e = P->pair ? bsgg::launch_mxf8_pair(L) : P->bn == 256 ? bsgg::launch_mxf8_256(L) : bsgg::launch_mxf8_128(L);
   return e == cudaSuccess ? BSGG_OK : BSGG_ERR_CUDA;
 }
 
@@ -419,18 +474,7 @@ extern "C" bsgg_status bsgg_run_noalloc(const bsgg_desc* desc, const bsgg_args* 
   // A plan on the stack, derived from `desc` exactly as bsgg_create derives
   // it, whose status word is the static scratch.
   bsgg_plan P;
-  P.desc = *desc;
-  P.device = dev;
-  P.num_sms = sms;
-  P.bn = 128;
-  P.epi = desc->epilogue;
-  P.outc = desc->out_format == BSGG_OUT_E2M1 ? bsgg::OUTC_FP4
-           : is_quant(desc->out_format)      ? bsgg::OUTC_FP8
-                                             : bsgg::OUTC_FLOAT;
-  P.sf_vec = desc->in_format == BSGG_IN_NVFP4 ? 16 : 32;
-  P.kbytes = desc->in_format == BSGG_IN_NVFP4 ? desc->k / 2 : desc->k;
-  P.n_out = desc->epilogue == BSGG_EPI_SWIGLU ? desc->n / 2 : desc->n;
-  P.out_row_bytes = P.n_out * out_elem_bits(desc->out_format) / 8;
+  if (init_plan(desc, dev, sms, &P) != BSGG_OK) return BSGG_ERR_CUDA;
   P.status = scratch;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -12,19 +12,27 @@ namespace bsgg {
 struct Launch {
   CUtensorMap tmA;
   CUtensorMap tmB;
+  CUtensorMap tmSFA;
+  CUtensorMap tmSFB;
   Params p;
-  int grid;
-  int bn;
+  int grid;      // CTAs (a multiple of 2 for pairs)
+  int bn;        // 128 or 256
+  bool pair;     // 256 x 256 tiles on a CTA pair
   int epi;
   int outc;
   cudaStream_t stream;
 };
 
-// Launchers, one per input family (separate translation units so that the
-// instantiations compile in parallel).  Return the launch's cudaError_t.
-cudaError_t launch_mxf8(const Launch& L);
-cudaError_t launch_nvf4(const Launch& L);
-// Dynamic shared memory a launch of this family needs.
-int smem_bytes(bool fp4, int bn);
+// Launchers, one translation unit per (input family, tile shape) so that the
+// instantiations compile in parallel.  Return the launch's cudaError_t.
+cudaError_t launch_mxf8_128(const Launch& L);
+cudaError_t launch_mxf8_256(const Launch& L);
+cudaError_t launch_mxf8_pair(const Launch& L);
+cudaError_t launch_nvf4_128(const Launch& L);
+cudaError_t launch_nvf4_256(const Launch& L);
+cudaError_t launch_nvf4_pair(const Launch& L);
+// Largest number of CTAs of the pair kernel that can be resident at once
+// (clusters x 2) on the current device, 0 if unknown.
+int pair_resident_ctas(bool fp4);
 
 }  // namespace bsgg

@@ -1,51 +1,83 @@
-// bsgg_launch.cuh -- instantiates the kernel for one input family and
-// dispatches a Launch to the right (BN, epilogue, output class) instance.
+// bsgg_launch.cuh -- instantiates the kernel for one (input family, tile
+// shape) and dispatches a Launch to the right (epilogue, output class) instance.
 #pragma once
 
 #include "bsgg_internal.h"
 
 namespace bsgg {
 
-template <bool FP4, int BN, int EPI, int OUTC>
+template <bool FP4, int BN, bool PAIR, int EPI, int OUTC>
 cudaError_t launch_one(const Launch& L) {
-  auto kern = bsgg_kernel<FP4, BN, EPI, OUTC>;
-  const int smem = Layout<FP4, BN>::kSmemBytes;
+  auto kern = bsgg_kernel<FP4, BN, PAIR, EPI, OUTC>;
+  const int smem = Layout<FP4, BN, PAIR>::kSmemBytes;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    if (PAIR) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+      if (e != cudaSuccess) return e;
+    }
     configured_device = dev;
   }
-  kern<<<L.grid, kThreads, smem, L.stream>>>(L.tmA, L.tmB, L.p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(L.grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = L.stream;
+  cudaLaunchAttribute attr[1];
+  if (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmSFA, L.tmSFB, L.p);
 }
 
-template <bool FP4, int BN, int EPI>
+template <bool FP4, int BN, bool PAIR, int EPI>
 cudaError_t launch_outc(const Launch& L) {
   switch (L.outc) {
-    case OUTC_FLOAT: return launch_one<FP4, BN, EPI, OUTC_FLOAT>(L);
-    case OUTC_FP8: return launch_one<FP4, BN, EPI, OUTC_FP8>(L);
-    case OUTC_FP4: return launch_one<FP4, BN, EPI, OUTC_FP4>(L);
+    case OUTC_FLOAT: return launch_one<FP4, BN, PAIR, EPI, OUTC_FLOAT>(L);
+    case OUTC_FP8: return launch_one<FP4, BN, PAIR, EPI, OUTC_FP8>(L);
+    case OUTC_FP4: return launch_one<FP4, BN, PAIR, EPI, OUTC_FP4>(L);
   }
   return cudaErrorInvalidValue;
 }
 
-template <bool FP4, int BN>
-cudaError_t launch_epi(const Launch& L) {
+template <bool FP4, int BN, bool PAIR>
+cudaError_t launch_shape(const Launch& L) {
   switch (L.epi) {
-    case EPI_GATE: return launch_outc<FP4, BN, EPI_GATE>(L);
-    case EPI_SWIGLU: return launch_outc<FP4, BN, EPI_SWIGLU>(L);
-    case EPI_SRELU: return launch_outc<FP4, BN, EPI_SRELU>(L);
+    case EPI_GATE: return launch_outc<FP4, BN, PAIR, EPI_GATE>(L);
+    case EPI_SWIGLU: return launch_outc<FP4, BN, PAIR, EPI_SWIGLU>(L);
+    case EPI_SRELU: return launch_outc<FP4, BN, PAIR, EPI_SRELU>(L);
   }
   return cudaErrorInvalidValue;
 }
 
 template <bool FP4>
-cudaError_t launch_family(const Launch& L) {
-  if (L.bn == 128) return launch_epi<FP4, 128>(L);
-  return cudaErrorInvalidValue;
+int pair_resident_ctas_impl() {
+  auto kern = bsgg_kernel<FP4, 256, true, EPI_GATE, OUTC_FLOAT>;
+  const int smem = Layout<FP4, 256, true>::kSmemBytes;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) return 0;
+  return 2 * clusters;
 }
 
 }  // namespace bsgg

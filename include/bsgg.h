@@ -101,7 +101,12 @@ typedef struct {
                              (SM100)", Step 2), 1 = [G_b | U_b] ("Grouped GEMM + GLU +
                              Hadamard + Quant (SM100)", Equations) */
   float tanh_clamp_s;     /* SRELU soft clamp s > 0, or 0 for none */
-  int32_t reserved[3];    /* must be zero */
+  int32_t tile_m;         /* rows per MMA tile: 128 (one CTA) or 256 (a pair of CTAs with
+                             2-CTA instructions); 0 = library choice.  The pages' mma_tiler_mn[0]
+                             ("Grouped GEMM + Quant (SM100)", Common Parameters) */
+  int32_t tile_n;         /* columns per MMA tile: 128 or 256 (256 when tile_m = 256); 0 = library
+                             choice.  The pages' mma_tiler_mn[1] */
+  int32_t reserved;       /* must be zero */
 } bsgg_desc;
 
 /* Tensors of one call.  Unused outputs may be NULL: d_col/sfd_col unless

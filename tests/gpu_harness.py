@@ -21,10 +21,13 @@ def to_device(p: W.Problem, device="cuda") -> W.Problem:
         b=p.b.to(device), sfb_rows=p.sfb_rows.to(device))
 
 
-def make_plan(p: W.Problem, gate_first=False) -> bsgg.Plan:
+TILES = [(128, 128), (128, 256), (256, 256)]
+
+
+def make_plan(p: W.Problem, gate_first=False, tile=(0, 0)) -> bsgg.Plan:
     return bsgg.Plan(m_pad=p.m_pad, n=p.n, k=p.k, num_groups=p.num_groups, in_format=p.in_fmt,
                      out_format=p.out_fmt, epilogue=p.epi, want_col=p.want_col,
-                     gate_first=gate_first, tanh_clamp_s=p.tanh_clamp_s)
+                     gate_first=gate_first, tanh_clamp_s=p.tanh_clamp_s, tile=tile)
 
 
 def alloc_outputs(plan: bsgg.Plan, device="cuda") -> dict:
@@ -37,11 +40,11 @@ def alloc_outputs(plan: bsgg.Plan, device="cuda") -> dict:
     return out
 
 
-def run_gpu(p: W.Problem, plan: bsgg.Plan = None, gate_first=False, outputs=None, inputs=None):
+def run_gpu(p: W.Problem, plan: bsgg.Plan = None, gate_first=False, outputs=None, inputs=None, tile=(0, 0)):
     """Pack the scales with the library's packer, launch, check the device
     status word.  Returns (outputs dict of device tensors, packed sfa, sfb)."""
     p = to_device(p)
-    plan = plan or make_plan(p, gate_first)
+    plan = plan or make_plan(p, gate_first, tile)
     if inputs is None:
         sfa = bsgg.pack_sf(p.sfa_rows)
         sfb = bsgg.pack_sf(p.sfb_rows)

@@ -56,7 +56,8 @@ def _create(**over):
     desc = bsgg.Desc(d["m_pad"], d["n"], d["k"], d["num_groups"], bsgg.IN_FORMATS[d["in_format"]],
                      bsgg.OUT_FORMATS[d["out_format"]], bsgg.EPILOGUES[d["epilogue"]],
                      int(d.get("want_col", 0)), int(d.get("gate_first", 0)),
-                     float(d.get("tanh_clamp_s", 0.0)), (ctypes.c_int32 * 3)(*d.get("reserved", (0, 0, 0))))
+                     float(d.get("tanh_clamp_s", 0.0)), int(d.get("tile_m", 0)), int(d.get("tile_n", 0)),
+                     int(d.get("reserved", 0)))
     h = ctypes.c_void_p()
     return bsgg.lib().bsgg_create(ctypes.byref(desc), ctypes.byref(h))
 
@@ -71,7 +72,9 @@ def _create(**over):
     (dict(tanh_clamp_s=-1.0, epilogue="srelu"), 1),
     (dict(tanh_clamp_s=8.0, epilogue="gate"), 1),
     (dict(want_col=1, out_format="bf16"), 1),   # D_col only with quantized outputs
-    (dict(reserved=(1, 0, 0)), 1),
+    (dict(reserved=1), 1),
+    (dict(tile_m=64), 1), (dict(tile_n=192), 1),
+    (dict(tile_m=256, tile_n=128), 2),           # pairs are built for 256 x 256 tiles
     (dict(in_format="nvfp4", out_format="e4m3"), 2),   # not on the pages
     (dict(in_format="nvfp4", out_format="e2m1", want_col=1), 2),
 ])
