@@ -280,9 +280,10 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize()
     log(f"[bench] workload {p.name}: m_pad={p.m_pad} valid={p.m_real} n={p.n} k={p.k} "
         f"generated in {time.time() - t0:.1f}s")
+    tile = tuple(int(x) for x in args.tile.split("x")) if args.tile else (0, 0)
     plan = bsgg.Plan(m_pad=p.m_pad, n=p.n, k=p.k, num_groups=p.num_groups, in_format=p.in_fmt,
                      out_format=p.out_fmt, epilogue=p.epi, want_col=p.want_col,
-                     tanh_clamp_s=p.tanh_clamp_s)
+                     tanh_clamp_s=p.tanh_clamp_s, tile=tile)
     sfa = bsgg.pack_sf(p.sfa_rows)
     sfb = bsgg.pack_sf(p.sfb_rows)
     outs = {}
@@ -372,7 +373,8 @@ def run_gpu(args, world, rank, local):
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[p.in_fmt],
                 "data": "synthetic (seeded MoE routing, N(0,1) draws quantized to the input format)",
-                "config": config_of(p, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
+                "config": config_of(p, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                                        "tile": args.tile or "library default (256x256 CTA pair)"}),
                 "gpu_launches": args.steps, "clocks": clocks, "roofline": roofline,
                 "e2e": e2e, "cpu_baseline": cpu_baseline,
                 "pct_of_dtype_peak": 100.0 * achieved / peak}
@@ -387,6 +389,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("gpu", "reference"), default="gpu")
     ap.add_argument("--workload", default="fc1_swiglu")
+    ap.add_argument("--tile", default="", help="MxN tile shape: 128x128, 128x256 or 256x256 "
+                    "(a CTA pair); default: the library's choice")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -472,11 +472,63 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // One thread issues every tcgen05 operation of the CTA (pair).  Its loop is
+    // kept short: the tcgen05 queue holds little more than one stage, so any
+    // per-MMA scalar work would leave the tensor pipe idle.  All shared-memory
+    // descriptors are formed once and advanced by adds (the start-address field
+    // holds address / 16 in its low 14 bits; every address here is < 256 KB).
     if (lane == 0 && leader) {
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       const uint32_t sf_tmem0 = tmem_base + NA * BN;
+      const uint64_t a_desc0 = sdesc_kmajor_sw128(sbase + Ly::kOffA);
+      const uint64_t b_desc0 = sdesc_kmajor_sw128(sbase + Ly::kOffB);
+      const uint64_t sfa_desc0 = sdesc_sf_block(sbase + Ly::kOffSfa);
+      const uint64_t sfb_desc0 = sdesc_sf_block(sbase + Ly::kOffSfb);
+      // instruction descriptors of the four MMAs of a stage: MXFP8 selects the
+      // scale byte (k-block) of each row's word, NVFP4 uses whole words
+      uint32_t idk[4];
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        idk[kk] = FP4 ? p.idesc : (p.idesc | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4));
+      const int full_stages = p.k / Ly::kKElems;      // stages with all four MMAs
+      auto issue_stage = [&](uint32_t d_tmem, int st, int n_mma, uint32_t acc0) {
+        const uint32_t sfa_t = sf_tmem0 + st * Ly::kSfColsPerStage;
+        const uint32_t sfb_t = sfa_t + Ly::kSfaCols;
+        const uint64_t sfa_d = sfa_desc0 + static_cast<uint64_t>((st * Ly::kSfaBytes) >> 4);
+        const uint64_t sfb_d = sfb_desc0 + static_cast<uint64_t>((st * Ly::kSfbBytes) >> 4);
+        // scale atoms -> tensor memory: atom i of A at columns 4i; atom i of
+        // B's 128-row block h at columns 4 * (i * halves + h)
+#pragma unroll
+        for (int i = 0; i < Ly::kAtoms; ++i) {
+          if (PAIR) tc_cp_32x128b_x4_pair(sfa_t + 4 * i, sfa_d + 32 * i);
+          else tc_cp_32x128b_x4(sfa_t + 4 * i, sfa_d + 32 * i);
+#pragma unroll
+          for (int h = 0; h < Ly::kHalves; ++h) {
+            const uint32_t dst = sfb_t + 4 * (i * Ly::kHalves + h);
+            const uint64_t src = sfb_d + 32 * (h * Ly::kAtoms + i);
+            if (PAIR) tc_cp_32x128b_x4_pair(dst, src); else tc_cp_32x128b_x4(dst, src);
+          }
+        }
+        const uint64_t ad = a_desc0 + static_cast<uint64_t>((st * Ly::kABytes) >> 4);
+        const uint64_t bd = b_desc0 + static_cast<uint64_t>((st * Ly::kBBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          if (kk >= n_mma) break;
+          const uint32_t accum = kk ? 1u : acc0;
+          // one MMA consumes 32 K-bytes: +2 in descriptor units
+          if (FP4) {
+            const uint32_t sa = sfa_t + 4 * kk, sb = sfb_t + 4 * Ly::kHalves * kk;
+            if (PAIR) tc_mma_nvf4_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sa, sb, accum);
+            else tc_mma_nvf4(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sa, sb, accum);
+          } else {
+            if (PAIR) tc_mma_mxf8_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sfa_t, sfb_t, accum);
+            else tc_mma_mxf8(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sfa_t, sfb_t, accum);
+          }
+        }
+        if (PAIR) tc_commit_pair(empty_bar(st), 3); else tc_commit(empty_bar(st));
+      };
       for (int t = unit; t < num_tiles && ok; t += num_units) {
         if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
         tc_fence_after();
@@ -484,44 +536,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ks = 0; ks < p.num_k_stages; ++ks) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag, kWaitLimitNs)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sfa_t = sf_tmem0 + stage * Ly::kSfColsPerStage;
-          const uint32_t sfb_t = sfa_t + Ly::kSfaCols;
-          const uint32_t sfa_s = sbase + Ly::kOffSfa + stage * Ly::kSfaBytes;
-          const uint32_t sfb_s = sbase + Ly::kOffSfb + stage * Ly::kSfbBytes;
-          // scale atoms -> tensor memory: atom i of A at columns 4i; atom i of
-          // B's 128-row block h at columns 4 * (i * halves + h)
-#pragma unroll
-          for (int i = 0; i < Ly::kAtoms; ++i) {
-            if (PAIR) tc_cp_32x128b_x4_pair(sfa_t + 4 * i, sdesc_sf_block(sfa_s + 512 * i));
-            else tc_cp_32x128b_x4(sfa_t + 4 * i, sdesc_sf_block(sfa_s + 512 * i));
-#pragma unroll
-            for (int h = 0; h < Ly::kHalves; ++h) {
-              const uint32_t dst = sfb_t + 4 * (i * Ly::kHalves + h);
-              const uint64_t src = sdesc_sf_block(sfb_s + (h * Ly::kAtoms + i) * 512);
-              if (PAIR) tc_cp_32x128b_x4_pair(dst, src); else tc_cp_32x128b_x4(dst, src);
-            }
+          if (ks < full_stages) {
+            issue_stage(d_tmem, stage, 4, ks ? 1u : 0u);
+          } else {
+            const int k_left = p.k - ks * Ly::kKElems;
+            issue_stage(d_tmem, stage, (k_left + Ly::kMmaK - 1) / Ly::kMmaK, ks ? 1u : 0u);
           }
-          const int k_left = p.k - ks * Ly::kKElems;
-          const int n_mma = min(4, (k_left + Ly::kMmaK - 1) / Ly::kMmaK);
-          const uint32_t a_s = sbase + Ly::kOffA + stage * Ly::kABytes;
-          const uint32_t b_s = sbase + Ly::kOffB + stage * Ly::kBBytes;
-          for (int kk = 0; kk < n_mma; ++kk) {
-            const uint64_t ad = sdesc_kmajor_sw128(a_s + 32 * kk);
-            const uint64_t bd = sdesc_kmajor_sw128(b_s + 32 * kk);
-            const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
-            if (FP4) {
-              // one MMA consumes four 16-element blocks: a whole atom per row
-              const uint32_t sa = sfa_t + 4 * kk, sb = sfb_t + 4 * Ly::kHalves * kk;
-              if (PAIR) tc_mma_nvf4_pair(d_tmem, ad, bd, p.idesc, sa, sb, accum);
-              else tc_mma_nvf4(d_tmem, ad, bd, p.idesc, sa, sb, accum);
-            } else {
-              // one MMA consumes one 32-element block: byte kk of each row's word
-              const uint32_t id = p.idesc | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4);
-              if (PAIR) tc_mma_mxf8_pair(d_tmem, ad, bd, id, sfa_t, sfb_t, accum);
-              else tc_mma_mxf8(d_tmem, ad, bd, id, sfa_t, sfb_t, accum);
-            }
-          }
-          if (PAIR) tc_commit_pair(empty_bar(stage), 3); else tc_commit(empty_bar(stage));
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
