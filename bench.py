@@ -374,7 +374,7 @@ def run_gpu(args, world, rank, local):
                 "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[p.in_fmt],
                 "data": "synthetic (seeded MoE routing, N(0,1) draws quantized to the input format)",
                 "config": config_of(p, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                                        "tile": args.tile or "library default (256x256 CTA pair)"}),
+                                        "tile": args.tile or "library default"}),
                 "gpu_launches": args.steps, "clocks": clocks, "roofline": roofline,
                 "e2e": e2e, "cpu_baseline": cpu_baseline,
                 "pct_of_dtype_peak": 100.0 * achieved / peak}

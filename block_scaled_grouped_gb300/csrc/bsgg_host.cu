@@ -170,8 +170,12 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
   P->desc = *desc;
   P->device = device;
   P->num_sms = num_sms;
-  const int tm = desc->tile_m ? desc->tile_m : 256;
-  const int tn = desc->tile_n ? desc->tile_n : 256;
+  // library choice (measured on GB300): 128 x 256 tiles for NVFP4 and for
+  // short reductions, where per-tile synchronisation weighs more; 256 x 256
+  // tiles on CTA pairs for MXFP8 with K >= 8192
+  int tm = desc->tile_m, tn = desc->tile_n;
+  if (tm == 0) tm = (desc->in_format != BSGG_IN_NVFP4 && desc->k >= 8192 && tn != 128) ? 256 : 128;
+  if (tn == 0) tn = 256;
   P->pair = (tm == 256);
   P->bn = P->pair ? 256 : tn;
   P->epi = desc->epilogue;

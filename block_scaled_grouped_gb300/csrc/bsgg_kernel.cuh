@@ -12,13 +12,16 @@
 //     receives its 128 rows of D.  Half the operand bytes per FLOP of 1-CTA
 //     tiles.  A group with an odd number of 128-row tiles ends in a pair tile
 //     whose odd half recomputes the even half's rows and stores nothing.
-// Ten warps per CTA:
+// Eleven warps per CTA:
 //   warp 0      TMA producer: A, B[g] (128-byte swizzle) and the scale-factor
 //               atoms (512-byte boxes) into a multi-stage ring; in a pair both
 //               producers complete the even CTA's "full" barrier
-//   warp 1      tensor-memory allocator and (even CTA) MMA issuer: tcgen05.cp
-//               of the stage's scale atoms, then block-scaled tcgen05.mma
-//               (MXFP8 kind::mxf8f6f4 or NVFP4 kind::mxf4nvf4)
+//   warp 1      tensor-memory allocator and (even CTA) MMA issuer: block-scaled
+//               tcgen05.mma (MXFP8 kind::mxf8f6f4 or NVFP4 kind::mxf4nvf4)
+//   warp 10     (even CTA) scale copier: tcgen05.cp of each stage's scale atoms
+//               to tensor memory, then a commit that releases the stage to the
+//               MMA issuer.  A copy in the MMA thread's own tcgen05 queue stalls
+//               the MMAs issued around it, so copies run from this thread.
 //   warps 2..9  epilogue, two warps per 32-lane tensor-memory quadrant, each
 //               owning half of the tile's columns: tcgen05.ld of the whole
 //               half into registers (then the accumulator is released), alpha,
@@ -44,7 +47,8 @@ enum : int { OK_BF16 = 0, OK_F16 = 1, OK_F32 = 2, OK_E4M3 = 3, OK_E5M2 = 4, OK_E
 constexpr int kBM = 128;          // rows per CTA tile (TMEM lanes)
 constexpr int kBKBytes = 128;     // K bytes per pipeline stage (one 128-byte swizzle span)
 constexpr int kEpiWarps = 8;      // two warps per tensor-memory lane quadrant
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kScaleWarp = 2 + kEpiWarps;  // the warp that copies scale atoms to tensor memory
+constexpr int kThreads = 96 + 32 * kEpiWarps;
 constexpr int kMaxGroups = 1024;
 constexpr uint32_t kStatusTimeout = 1u;
 constexpr uint32_t kStatusBadOffsets = 2u;
@@ -105,7 +109,7 @@ struct Layout {
   static constexpr int kOffSfa = kOffB + kStages * kBBytes;
   static constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
   static constexpr int kOffBars = kOffSfb + kStages * kSfbBytes;
-  static constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 1;
+  static constexpr int kNumBars = 3 * kStages + 2 * kNumAcc + 2;
   static constexpr int kOffTmemHolder = kOffBars + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemHolder + 4;
   static constexpr int kOffTrows = kOffAbort + 12;
@@ -340,6 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto accf_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
   auto acce_bar = [&](int a) { return bar0 + 8u * (2 * S + NA + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 2 * NA);
+  // stage's scale atoms are in tensor memory (and so its operands in shared memory)
+  auto sfr_bar = [&](int st) { return bar0 + 8u * (2 * S + 2 * NA + 1 + st); };
+  const uint32_t drain_bar2 = bar0 + 8u * (3 * S + 2 * NA + 1);   // the scale copier's own drain
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Ly::kOffTmemHolder);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kOffAbort);
   int32_t* s_trow = reinterpret_cast<int32_t*>(smem + Ly::kOffTrows);
@@ -360,6 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(acce_bar(a), PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(drain_bar, 1);
+    for (int st = 0; st < S; ++st) mbar_init(sfr_bar(st), 1);
+    mbar_init(drain_bar2, 1);
     *abort_flag = 0;
     mbar_fence_init();
     prefetch_tmap(&tmA);
@@ -484,8 +493,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sf_tmem0 = tmem_base + NA * BN;
       const uint64_t a_desc0 = sdesc_kmajor_sw128(sbase + Ly::kOffA);
       const uint64_t b_desc0 = sdesc_kmajor_sw128(sbase + Ly::kOffB);
-      const uint64_t sfa_desc0 = sdesc_sf_block(sbase + Ly::kOffSfa);
-      const uint64_t sfb_desc0 = sdesc_sf_block(sbase + Ly::kOffSfb);
       // instruction descriptors of the four MMAs of a stage: MXFP8 selects the
       // scale byte (k-block) of each row's word, NVFP4 uses whole words
       uint32_t idk[4];
@@ -496,21 +503,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_stage = [&](uint32_t d_tmem, int st, int n_mma, uint32_t acc0) {
         const uint32_t sfa_t = sf_tmem0 + st * Ly::kSfColsPerStage;
         const uint32_t sfb_t = sfa_t + Ly::kSfaCols;
-        const uint64_t sfa_d = sfa_desc0 + static_cast<uint64_t>((st * Ly::kSfaBytes) >> 4);
-        const uint64_t sfb_d = sfb_desc0 + static_cast<uint64_t>((st * Ly::kSfbBytes) >> 4);
-        // scale atoms -> tensor memory: atom i of A at columns 4i; atom i of
-        // B's 128-row block h at columns 4 * (i * halves + h)
-#pragma unroll
-        for (int i = 0; i < Ly::kAtoms; ++i) {
-          if (PAIR) tc_cp_32x128b_x4_pair(sfa_t + 4 * i, sfa_d + 32 * i);
-          else tc_cp_32x128b_x4(sfa_t + 4 * i, sfa_d + 32 * i);
-#pragma unroll
-          for (int h = 0; h < Ly::kHalves; ++h) {
-            const uint32_t dst = sfb_t + 4 * (i * Ly::kHalves + h);
-            const uint64_t src = sfb_d + 32 * (h * Ly::kAtoms + i);
-            if (PAIR) tc_cp_32x128b_x4_pair(dst, src); else tc_cp_32x128b_x4(dst, src);
-          }
-        }
         const uint64_t ad = a_desc0 + static_cast<uint64_t>((st * Ly::kABytes) >> 4);
         const uint64_t bd = b_desc0 + static_cast<uint64_t>((st * Ly::kBBytes) >> 4);
 #pragma unroll
@@ -534,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int ks = 0; ks < p.num_k_stages; ++ks) {
-          if (!mbar_wait(full_bar(stage), phase, abort_flag, kWaitLimitNs)) { ok = false; break; }
+          if (!mbar_wait(sfr_bar(stage), phase, abort_flag, kWaitLimitNs)) { ok = false; break; }
           tc_fence_after();
           if (ks < full_stages) {
             issue_stage(d_tmem, stage, 4, ks ? 1u : 0u);
@@ -554,6 +546,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (PAIR) tc_commit_pair(drain_bar, 1); else tc_commit(drain_bar);
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(drain_bar, 0) && globaltimer_ns() - t0 < kDrainLimitNs) {}
+      }
+    }
+  } else if (warp == kScaleWarp) {
+    // ------------------------------------------------------------ scale copier
+    // Same stage sequence as the MMA issuer.  Writing a stage's tensor-memory
+    // scale slot is safe once its "full" barrier completed: the refill behind
+    // it waited for the MMAs that read the slot's previous contents.
+    if (lane == 0 && leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      const uint32_t sf_tmem0 = tmem_base + NA * BN;
+      const uint64_t sfa_desc0 = sdesc_sf_block(sbase + Ly::kOffSfa);
+      const uint64_t sfb_desc0 = sdesc_sf_block(sbase + Ly::kOffSfb);
+      for (int t = unit; t < num_tiles && ok; t += num_units) {
+        for (int ks = 0; ks < p.num_k_stages; ++ks) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, kWaitLimitNs)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sfa_t = sf_tmem0 + stage * Ly::kSfColsPerStage;
+          const uint32_t sfb_t = sfa_t + Ly::kSfaCols;
+          const uint64_t sfa_d = sfa_desc0 + static_cast<uint64_t>((stage * Ly::kSfaBytes) >> 4);
+          const uint64_t sfb_d = sfb_desc0 + static_cast<uint64_t>((stage * Ly::kSfbBytes) >> 4);
+          // atom i of A at columns 4i; atom i of B's 128-row block h at
+          // columns 4 * (i * halves + h)
+#pragma unroll
+          for (int i = 0; i < Ly::kAtoms; ++i) {
+            if (PAIR) tc_cp_32x128b_x4_pair(sfa_t + 4 * i, sfa_d + 32 * i);
+            else tc_cp_32x128b_x4(sfa_t + 4 * i, sfa_d + 32 * i);
+#pragma unroll
+            for (int h = 0; h < Ly::kHalves; ++h) {
+              const uint32_t dst = sfb_t + 4 * (i * Ly::kHalves + h);
+              const uint64_t src = sfb_d + 32 * (h * Ly::kAtoms + i);
+              if (PAIR) tc_cp_32x128b_x4_pair(dst, src); else tc_cp_32x128b_x4(dst, src);
+            }
+          }
+          if (PAIR) tc_commit_pair(sfr_bar(stage), 1); else tc_commit(sfr_bar(stage));
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        atomicOr(p.status, kStatusTimeout);
+        // drain: wait (bounded) until this thread's copies completed
+        if (PAIR) tc_commit_pair(drain_bar2, 1); else tc_commit(drain_bar2);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(drain_bar2, 0) && globaltimer_ns() - t0 < kDrainLimitNs) {}
       }
     }
   } else {
