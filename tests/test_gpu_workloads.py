@@ -1,0 +1,75 @@
+"""Parity at full size: the four large workloads, generated on the GPU with
+their real shapes and run in every tile shape (the library's default is the
+one bench.py times), compared element by element with the CPU oracle on
+sampled 32-row blocks -- each group's first and last block, the first and last
+block of the problem and random blocks -- with the same tolerances as the
+small parity tests.  For BF16 outputs the per-group amax is checked over whole
+groups against the GPU's own D (|amax - max|D_bf16|| <= 2^-8 amax, as D_bf16 is
+D rounded to 8 significant bits)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from helpers import IN_CODE, OUT_CODE, EPI_CODE, np_
+from gpu_harness import TILES, compare, decode_float_out, make_plan, run_gpu
+from block_scaled_grouped_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _sample_blocks(p, n_random=3, seed=0):
+    """First and last block of the problem; for the first three and last three
+    non-empty groups their first block, last block and the block holding their
+    last real row; a few random blocks."""
+    off = np_(p.padded_offsets)
+    starts = np.concatenate([[0], off[:-1]])
+    nonempty = [g for g in range(p.num_groups) if off[g] > starts[g]]
+    blocks = {0, p.m_pad // 32 - 1}
+    for g in sorted(set(nonempty[:3] + nonempty[-3:])):
+        blocks.add(int(starts[g]) // 32)
+        blocks.add(int(off[g]) // 32 - 1)
+        if p.counts[g] > 0:
+            blocks.add(int(starts[g] + p.counts[g] - 1) // 32)
+    rng = np.random.default_rng(seed)
+    blocks |= set(int(b) for b in rng.integers(0, p.m_pad // 32, n_random))
+    return np.array(sorted(blocks), dtype=np.int64)
+
+
+def _oracle(p, blocks):
+    ins = dict(a=np_(p.a), b=np_(p.b), sfa=orc.pack_sf(np_(p.sfa_rows)), sfb=orc.pack_sf(np_(p.sfb_rows)),
+               padded_offsets=np_(p.padded_offsets), alpha=np_(p.alpha), prob=np_(p.prob))
+    return orc.run(m_pad=p.m_pad, n=p.n, k=p.k, num_groups=p.num_groups, in_fmt=IN_CODE[p.in_fmt],
+                   out_fmt=OUT_CODE[p.out_fmt], epi=EPI_CODE[p.epi], norm_const=p.norm_const,
+                   tanh_clamp_s=p.tanh_clamp_s, want_col=p.want_col, blocks=blocks, **ins)
+
+
+@pytest.fixture(scope="module", params=["fc1_swiglu", "fc2_gate", "fine_nvfp4", "skewed"])
+def workload(request):
+    p = W.workload(request.param, device="cuda")
+    blocks = _sample_blocks(p)
+    ref = _oracle(p, blocks)
+    yield p, blocks, ref
+    del p
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("tile", [(0, 0)] + TILES, ids=lambda t: "default" if t == (0, 0) else f"{t[0]}x{t[1]}")
+def test_full_size_parity_on_sampled_blocks(workload, tile):
+    p, blocks, ref = workload
+    outs, _, _ = run_gpu(p, tile=tile)
+    compare(p, outs, ref, blocks=blocks)
+    if p.out_fmt in ("bf16", "f16"):
+        d = decode_float_out(outs["d"].cpu().numpy(), p.out_fmt, p.m_pad, p.n_out)
+        amax = outs["amax"].cpu().numpy()
+        off = np_(p.padded_offsets)
+        starts = np.concatenate([[0], off[:-1]])
+        for g in range(p.num_groups):
+            if off[g] == starts[g]:
+                assert amax[g] == 0.0
+                continue
+            m = np.abs(d[starts[g]:off[g]]).max()
+            assert abs(amax[g] - m) <= 2.0 ** -8 * amax[g] + 1e-30, (g, amax[g], m)
+        # the oracle's amax over the sampled rows bounds the full amax from below
+        sampled = ref["amax"]
+        assert np.all(amax >= sampled * (1 - 2.0 ** -20))
