@@ -99,7 +99,6 @@ bsgg_status validate(const bsgg_desc* d) {
   // build's reading for the NVFP4 sReLU workload.  FP8 outputs from FP4 inputs
   // are not on the pages.
   if (fp4 && (d->out_format == BSGG_OUT_E4M3 || d->out_format == BSGG_OUT_E5M2)) return BSGG_ERR_UNSUPPORTED;
-  if (fp4 && d->want_col) return BSGG_ERR_UNSUPPORTED;   // 16-row column blocks not built
   return BSGG_OK;
 }
 

@@ -306,23 +306,49 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* 
       p.sfd_row[sf_off(row, col0 / kV + b, p.kq_row)] = static_cast<uint8_t>(code);
     }
     store_q32<OUTC>(static_cast<uint8_t*>(p.d) + row * row_bytes + col_byte0, v, sc, p.out_kind);
-    // ---- column blocks: 32 rows = the 32 lanes of this warp (v = 32)
-    if (!FP4 && p.want_col) {
-      // column j's max over the warp's 32 rows; lane j keeps it, encodes that
-      // column's scale and shares the factor with the other lanes
-      float my_am = 0.0f;
+    // ---- column blocks of v rows: the warp's 32 lanes are its 32 rows
+    if (p.want_col) {
+      if (!FP4) {
+        // v = 32: column j's max over the warp's rows; lane j keeps it,
+        // encodes that column's scale and shares the factor with the others
+        float my_am = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float am = __uint_as_float(redux_max_u32(__float_as_uint(fabsf(v[j]))));
-        my_am = (lane == j) ? am : my_am;
+        for (int j = 0; j < 32; ++j) {
+          const float am = __uint_as_float(redux_max_u32(__float_as_uint(fabsf(v[j]))));
+          my_am = (lane == j) ? am : my_am;
+        }
+        uint32_t my_code;
+        float my_scale;
+        block_scale<false>(my_am, norm, p.rcp_qmax, my_code, my_scale);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sc[j] = __shfl_sync(0xffffffffu, my_scale, j);
+        store_q32<OUTC>(static_cast<uint8_t*>(p.d_col) + row * row_bytes + col_byte0, v, sc, p.out_kind);
+        p.sfd_col[sf_off(col0 + lane, kblk_col, p.kq_col)] = static_cast<uint8_t>(my_code);
+      } else {
+        // v = 16: each half-warp is one block.  Butterfly maxima inside the
+        // half-warp; lane (16h + i) owns columns i and i + 16 of half h.
+        const int h = lane >> 4, i = lane & 15;
+        float am_lo = 0.0f, am_hi = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          float m = fabsf(v[j]);
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          if (j < 16) am_lo = (i == j) ? m : am_lo;
+          else am_hi = (i == j - 16) ? m : am_hi;
+        }
+        uint32_t code_lo, code_hi;
+        float sc_lo, sc_hi;
+        block_scale<true>(am_lo, norm, p.rcp_qmax, code_lo, sc_lo);
+        block_scale<true>(am_hi, norm, p.rcp_qmax, code_hi, sc_hi);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          sc[j] = __shfl_sync(0xffffffffu, j < 16 ? sc_lo : sc_hi, 16 * h + (j & 15));
+        store_q32<OUTC>(static_cast<uint8_t*>(p.d_col) + row * row_bytes + col_byte0, v, sc, p.out_kind);
+        const int kb = 2 * kblk_col + h;     // 16-row block index
+        p.sfd_col[sf_off(col0 + i, kb, p.kq_col)] = static_cast<uint8_t>(code_lo);
+        p.sfd_col[sf_off(col0 + i + 16, kb, p.kq_col)] = static_cast<uint8_t>(code_hi);
       }
-      uint32_t my_code;
-      float my_scale;
-      block_scale<false>(my_am, norm, p.rcp_qmax, my_code, my_scale);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) sc[j] = __shfl_sync(0xffffffffu, my_scale, j);
-      store_q32<OUTC>(static_cast<uint8_t*>(p.d_col) + row * row_bytes + col_byte0, v, sc, p.out_kind);
-      p.sfd_col[sf_off(col0 + lane, kblk_col, p.kq_col)] = static_cast<uint8_t>(my_code);
     }
   }
 }

@@ -76,7 +76,6 @@ def _create(**over):
     (dict(tile_m=64), 1), (dict(tile_n=192), 1),
     (dict(tile_m=256, tile_n=128), 2),           # pairs are built for 256 x 256 tiles
     (dict(in_format="nvfp4", out_format="e4m3"), 2),   # not on the pages
-    (dict(in_format="nvfp4", out_format="e2m1", want_col=1), 2),
 ])
 def test_create_rejects(lib, over, code):
     assert _create(**over) == code

@@ -125,6 +125,17 @@ def test_nvfp4_srelu_clamp_e2m1(tile):
 
 
 @pytest.mark.parametrize("tile", TILES, ids=lambda t: f"{t[0]}x{t[1]}")
+def test_nvfp4_e2m1_row_and_16_row_column_blocks(tile):
+    # NVFP4 inputs: E4M3 scales per 16 values for D rows and for D_col columns
+    p = small_problem(counts=(256, 70, 0, 130), k=512, n=256, pad_to=128, in_fmt="nvfp4",
+                      epi="gate", out_fmt="e2m1", want_col=True, seed=36)
+    _parity(p, tile=tile)
+    p = small_problem(counts=(128, 200), k=256, n=256, pad_to=128, in_fmt="nvfp4",
+                      epi="srelu", out_fmt="e2m1", want_col=True, tanh_clamp_s=4.0, seed=37)
+    _parity(p, tile=tile)
+
+
+@pytest.mark.parametrize("tile", TILES, ids=lambda t: f"{t[0]}x{t[1]}")
 def test_nvfp4_swiglu_bf16(tile):
     p = small_problem(counts=(128, 200), k=256, n=256, pad_to=128, in_fmt="nvfp4",
                       epi="swiglu", out_fmt="bf16", seed=33)
