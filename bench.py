@@ -285,9 +285,10 @@ def run_gpu(args, world, rank, local):
     log(f"[bench] workload {p.name}: m_pad={p.m_pad} valid={p.m_real} n={p.n} k={p.k} "
         f"generated in {time.time() - t0:.1f}s")
     tile = tuple(int(x) for x in args.tile.split("x")) if args.tile else (0, 0)
+    cluster = tuple(int(x) for x in args.cluster.split("x")) if args.cluster else (0, 0)
     plan = bsgg.Plan(m_pad=p.m_pad, n=p.n, k=p.k, num_groups=p.num_groups, in_format=p.in_fmt,
                      out_format=p.out_fmt, epilogue=p.epi, want_col=p.want_col,
-                     tanh_clamp_s=p.tanh_clamp_s, tile=tile)
+                     tanh_clamp_s=p.tanh_clamp_s, tile=tile, cluster=cluster)
     sfa = bsgg.pack_sf(p.sfa_rows)
     sfb = bsgg.pack_sf(p.sfb_rows)
     outs = {}
@@ -378,7 +379,8 @@ def run_gpu(args, world, rank, local):
                 "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[p.in_fmt],
                 "data": "synthetic (seeded MoE routing, N(0,1) draws quantized to the input format)",
                 "config": config_of(p, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                                        "tile": args.tile or "library default"}),
+                                        "tile": args.tile or "library default",
+                                        "cluster": args.cluster or "library default"}),
                 "gpu_launches": args.steps, "clocks": clocks, "roofline": roofline,
                 "e2e": e2e, "cpu_baseline": cpu_baseline,
                 "pct_of_dtype_peak": 100.0 * achieved / peak}
@@ -395,6 +397,9 @@ def main():
     ap.add_argument("--workload", default="fc1_swiglu")
     ap.add_argument("--tile", default="", help="MxN tile shape: 128x128, 128x256 or 256x256 "
                     "(a CTA pair); default: the library's choice")
+    ap.add_argument("--cluster", default="", help="MxN cluster shape: 1x1, or 2x1 (with 256x256 "
+                    "tiles the CTA pair, with 128x256 tiles two CTAs sharing an operand by TMA "
+                    "multicast); default: the library's choice")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

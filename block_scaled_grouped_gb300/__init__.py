@@ -36,7 +36,7 @@ class Desc(ctypes.Structure):
                 ("out_format", ctypes.c_int32), ("epilogue", ctypes.c_int32),
                 ("want_col", ctypes.c_int32), ("gate_first", ctypes.c_int32),
                 ("tanh_clamp_s", ctypes.c_float), ("tile_m", ctypes.c_int32),
-                ("tile_n", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("tile_n", ctypes.c_int32), ("cluster_m", ctypes.c_int32), ("cluster_n", ctypes.c_int32)]
 
 
 class Args(ctypes.Structure):
@@ -137,10 +137,12 @@ class Plan:
 
     def __init__(self, *, m_pad: int, n: int, k: int, num_groups: int, in_format: str,
                  out_format: str, epilogue: str, want_col: bool = False, gate_first: bool = False,
-                 tanh_clamp_s: float = 0.0, tile=(0, 0)):
+                 tanh_clamp_s: float = 0.0, tile=(0, 0), cluster=(0, 0)):
+        """tile = the pages' mma_tiler_mn, cluster = cluster_shape_mn; (0, 0)
+        lets the library choose."""
         self.desc = Desc(m_pad, n, k, num_groups, IN_FORMATS[in_format], OUT_FORMATS[out_format],
                          EPILOGUES[epilogue], int(bool(want_col)), int(bool(gate_first)),
-                         float(tanh_clamp_s), int(tile[0]), int(tile[1]), 0)
+                         float(tanh_clamp_s), int(tile[0]), int(tile[1]), int(cluster[0]), int(cluster[1]))
         self.in_format, self.out_format, self.epilogue = in_format, out_format, epilogue
         self.want_col = bool(want_col)
         h = ctypes.c_void_p()
@@ -213,15 +215,15 @@ class Plan:
 
 def run_noalloc(*, m_pad: int, n: int, k: int, num_groups: int, in_format: str, out_format: str,
                 epilogue: str, want_col: bool = False, gate_first: bool = False,
-                tanh_clamp_s: float = 0.0, tile=(0, 0), stream=None, wait_status: bool = True,
-                **tensors) -> int:
+                tanh_clamp_s: float = 0.0, tile=(0, 0), cluster=(0, 0), stream=None,
+                wait_status: bool = True, **tensors) -> int:
     """bsgg_run_noalloc: one call without a plan and without any device
     allocation (for callers whose device memory is owned by someone else, or
     who must not let cudaMalloc synchronize the device).  Returns the status
     code (the device status when wait_status is true)."""
     desc = Desc(m_pad, n, k, num_groups, IN_FORMATS[in_format], OUT_FORMATS[out_format],
                 EPILOGUES[epilogue], int(bool(want_col)), int(bool(gate_first)), float(tanh_clamp_s),
-                int(tile[0]), int(tile[1]), 0)
+                int(tile[0]), int(tile[1]), int(cluster[0]), int(cluster[1]))
     args = Args(*[_ptr(tensors.get(name)) for name, _ in Args._fields_])
     return int(lib().bsgg_run_noalloc(ctypes.byref(desc), ctypes.byref(args), _stream(stream),
                                       int(bool(wait_status))))

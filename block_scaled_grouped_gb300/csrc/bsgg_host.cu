@@ -19,8 +19,9 @@ struct bsgg_plan {
   bsgg_desc desc;
   int device;
   int num_sms;
-  int grid;                // CTAs per launch (a multiple of 2 for pairs)
-  bool pair;               // 256 x 256 tiles on CTA pairs
+  int grid;                // CTAs per launch (a multiple of 2 for clusters)
+  bool pair;               // 256 x 256 tiles on CTA pairs (2-CTA MMAs)
+  bool mc;                 // clusters of two 128 x 256 CTAs sharing an operand by TMA multicast
   int bn;
   int epi;
   int outc;
@@ -70,12 +71,23 @@ int out_elem_bits(int out) {
 
 bsgg_status validate(const bsgg_desc* d) {
   if (!d) return BSGG_ERR_INVALID_ARG;
-  if (d->reserved != 0) return BSGG_ERR_INVALID_ARG;
   // tile shape: the pages' mma_tiler_mn with TILE_M in {128, 256} (256 = 2-CTA
   // instructions) and TILE_N in {128, 256}; pairs are built for 256 x 256 only
   if (d->tile_m != 0 && d->tile_m != 128 && d->tile_m != 256) return BSGG_ERR_INVALID_ARG;
   if (d->tile_n != 0 && d->tile_n != 128 && d->tile_n != 256) return BSGG_ERR_INVALID_ARG;
   if (d->tile_m == 256 && d->tile_n == 128) return BSGG_ERR_UNSUPPORTED;
+  // cluster shape: the pages' cluster_shape_mn, powers of two <= 4 (both or
+  // neither given); 2-CTA tiles need an even CLUSTER_M ("Grouped GEMM + Quant
+  // (SM100)", Tiling and Cluster).  Built: (1, 1) and (2, 1).
+  auto pow2le4 = [](int v) { return v == 1 || v == 2 || v == 4; };
+  if ((d->cluster_m == 0) != (d->cluster_n == 0)) return BSGG_ERR_INVALID_ARG;
+  if (d->cluster_m != 0) {
+    if (!pow2le4(d->cluster_m) || !pow2le4(d->cluster_n)) return BSGG_ERR_INVALID_ARG;
+    if (d->tile_m == 256 && d->cluster_m % 2 != 0) return BSGG_ERR_INVALID_ARG;
+    if (d->cluster_n != 1 || d->cluster_m > 2) return BSGG_ERR_UNSUPPORTED;
+    // a (2, 1) cluster of 1-CTA tiles is built for 128 x 256 tiles
+    if (d->cluster_m == 2 && d->tile_m != 256 && d->tile_n == 128) return BSGG_ERR_UNSUPPORTED;
+  }
   if (d->num_groups < 1 || d->num_groups > 1024) return BSGG_ERR_INVALID_ARG;   // L <= 1024
   if (d->m_pad <= 0 || d->m_pad % 128 != 0 || d->m_pad > (int64_t(1) << 30)) return BSGG_ERR_INVALID_ARG;
   if (d->n <= 0 || d->k <= 0 || d->n > (int64_t(1) << 24) || d->k > (int64_t(1) << 24))
@@ -127,7 +139,8 @@ bsgg_status encode_one(CUtensorMap* map, const void* base, int rank, const cuuin
 }
 
 // A (m_pad, K bytes) and B (L, N, K bytes) as 128-byte-swizzled boxes of
-// 128 K-bytes x 128 rows / x (rows of B this CTA holds); the scale factors as
+// 128 K-bytes x 128 rows (64 in multicast clusters) / x (rows of B one load
+// moves: the tile's, half of it in clusters); the scale factors as
 // (256 bytes, 2 * atoms, 128-row blocks) so that one box moves a stage's
 // 512-byte atoms of one (SFA) or two (SFB, tile_n = 256) row blocks.
 bsgg_status encode_maps(const bsgg_plan* P, const bsgg_args* a, bsgg::Launch* L) {
@@ -138,13 +151,14 @@ bsgg_status encode_maps(const bsgg_plan* P, const bsgg_args* a, bsgg::Launch* L)
   {
     cuuint64_t dims[2] = {cuuint64_t(P->kbytes), cuuint64_t(d.m_pad)};
     cuuint64_t strides[1] = {cuuint64_t(P->kbytes)};
-    cuuint32_t box[2] = {bsgg::kBKBytes, bsgg::kBM};
+    // multicast clusters move A as 64-row halves
+    cuuint32_t box[2] = {bsgg::kBKBytes, cuuint32_t(P->mc ? bsgg::kBM / 2 : bsgg::kBM)};
     if ((st = encode_one(&L->tmA, a->a, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) != BSGG_OK) return st;
   }
   {
     cuuint64_t dims[3] = {cuuint64_t(P->kbytes), cuuint64_t(d.n), cuuint64_t(d.num_groups)};
     cuuint64_t strides[2] = {cuuint64_t(P->kbytes), cuuint64_t(P->kbytes * d.n)};
-    cuuint32_t box[3] = {bsgg::kBKBytes, cuuint32_t(P->pair ? P->bn / 2 : P->bn), 1};
+    cuuint32_t box[3] = {bsgg::kBKBytes, cuuint32_t(P->pair || P->mc ? P->bn / 2 : P->bn), 1};
     if ((st = encode_one(&L->tmB, a->b, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) != BSGG_OK) return st;
   }
   {
@@ -172,10 +186,12 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
   // library choice (measured on GB300): 128 x 256 tiles for NVFP4 and for
   // short reductions, where per-tile synchronisation weighs more; 256 x 256
   // tiles on CTA pairs for MXFP8 with K >= 8192
-  int tm = desc->tile_m, tn = desc->tile_n;
-  if (tm == 0) tm = (desc->in_format != BSGG_IN_NVFP4 && desc->k >= 8192 && tn != 128) ? 256 : 128;
+  int tm = desc->tile_m, tn = desc->tile_n, cm = desc->cluster_m;
+  if (tm == 0) tm = (desc->in_format != BSGG_IN_NVFP4 && desc->k >= 8192 && tn != 128 && cm != 1) ? 256 : 128;
   if (tn == 0) tn = 256;
+  if (cm == 0) cm = (tm == 256) ? 2 : 1;
   P->pair = (tm == 256);
+  P->mc = (tm == 128 && cm == 2);
   P->bn = P->pair ? 256 : tn;
   P->epi = desc->epilogue;
   P->outc = desc->out_format == BSGG_OUT_E2M1 ? bsgg::OUTC_FP4
@@ -185,8 +201,8 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
   P->kbytes = desc->in_format == BSGG_IN_NVFP4 ? desc->k / 2 : desc->k;
   P->n_out = desc->epilogue == BSGG_EPI_SWIGLU ? desc->n / 2 : desc->n;
   P->out_row_bytes = P->n_out * out_elem_bits(desc->out_format) / 8;
-  if (P->pair) {
-    int resident = bsgg::pair_resident_ctas(desc->in_format == BSGG_IN_NVFP4);
+  if (P->pair || P->mc) {
+    int resident = bsgg::cluster_resident_ctas(desc->in_format == BSGG_IN_NVFP4, P->mc);
     if (resident <= 0) resident = num_sms;
     P->grid = std::max(2, (std::min(resident, num_sms) / 2) * 2);
   } else {
@@ -345,20 +361,27 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   p.rcp_qmax = static_cast<float>(1.0 / qmax);
   p.idesc = make_idesc(d.in_format, P->bn, P->pair);
 
-  // an upper bound of the tiles (pairs may add one tile row per group)
-  const int64_t rows = P->pair ? ceil_div(d.m_pad, 256) + d.num_groups : d.m_pad / bsgg::kBM;
+  // an upper bound of the scheduling units (clusters may add one 256-row
+  // tile row per group)
+  const bool cl = P->pair || P->mc;
+  const int64_t rows = cl ? ceil_div(d.m_pad, 256) + d.num_groups : d.m_pad / bsgg::kBM;
   const int64_t tiles = rows * p.num_n_tiles;
-  L.grid = static_cast<int>(std::min<int64_t>(P->grid, P->pair ? 2 * tiles : tiles));
+  L.grid = static_cast<int>(std::min<int64_t>(P->grid, cl ? 2 * tiles : tiles));
   L.pair = P->pair;
+  L.mc = P->mc;
   L.bn = P->bn;
   L.epi = P->epi;
   L.outc = P->outc;
   L.stream = s;
   cudaError_t e;
   if (d.in_format == BSGG_IN_NVFP4)
-    e = P->pair ? bsgg::launch_nvf4_pair(L) : P->bn == 256 ? bsgg::launch_nvf4_256(L) : bsgg::launch_nvf4_128(L);
+    e = P->pair ? bsgg::launch_nvf4_pair(L)
+        : P->mc ? bsgg::launch_nvf4_mc(L)
+        : P->bn == 256 ? bsgg::launch_nvf4_256(L) : bsgg::launch_nvf4_128(L);
   else
-    e = P->pair ? bsgg::launch_mxf8_pair(L) : P->bn == 256 ? bsgg::launch_mxf8_256(L) : bsgg::launch_mxf8_128(L);
+    e = P->pair ? bsgg::launch_mxf8_pair(L)
+        : P->mc ? bsgg::launch_mxf8_mc(L)
+        : P->bn == 256 ? bsgg::launch_mxf8_256(L) : bsgg::launch_mxf8_128(L);
   return e == cudaSuccess ? BSGG_OK : BSGG_ERR_CUDA;
 }
 

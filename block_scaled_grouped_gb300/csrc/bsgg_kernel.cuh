@@ -2,10 +2,18 @@
 //
 // Tiles never straddle two expert groups because groups are padded to
 // multiples of 128 rows ("Grouped GEMM + Quant (SM100)", Tiling and Cluster:
-// tiles must not span groups).  Two shapes share this file:
-//   * 1-CTA (PAIR = false): one CTA computes a 128 x BN tile (BN = 128 or 256)
+// tiles must not span groups).  Three cluster modes (CM) share this file:
+//   * single (CM_SINGLE): one CTA computes a 128 x BN tile (BN = 128 or 256)
 //     with tcgen05 .cta_group::1 MMAs.
-//   * CTA pair (PAIR = true, BN = 256): a cluster of two CTAs computes a
+//   * multicast cluster (CM_MC, BN = 256): a cluster of two CTAs, each
+//     computing its own 128 x 256 tile with .cta_group::1 MMAs, shares one
+//     operand through TMA multicast: two m-tiles of one n-tile (each CTA loads
+//     half of the common B tile into both CTAs), or, for the last m-tile of a
+//     group with an odd count, two n-tiles of that m-tile (each CTA loads half
+//     of the common A tile).  A stage is refilled only after both CTAs'
+//     MMAs released it.  Two thirds (B shared) or five sixths (A shared) of
+//     the L2-to-SM bytes of a single CTA; no odd-half recomputation.
+//   * CTA pair (CM_PAIR, BN = 256): a cluster of two CTAs computes a
 //     256 x 256 tile with .cta_group::2 MMAs: each CTA loads its own 128 rows
 //     of A and half of the 256 rows of B, both CTAs hold all 256 columns' B
 //     scales, the even CTA issues the MMAs and each CTA's tensor memory
@@ -40,6 +48,7 @@
 namespace bsgg {
 
 enum : int { EPI_GATE = 0, EPI_SWIGLU = 1, EPI_SRELU = 2 };
+enum : int { CM_SINGLE = 0, CM_PAIR = 1, CM_MC = 2 };
 // Output class (template) and exact output kind (runtime) of D.
 enum : int { OUTC_FLOAT = 0, OUTC_FP8 = 1, OUTC_FP4 = 2 };
 enum : int { OK_BF16 = 0, OK_F16 = 1, OK_F32 = 2, OK_E4M3 = 3, OK_E5M2 = 4, OK_E2M1 = 5 };
@@ -126,6 +135,15 @@ __device__ __forceinline__ int64_t sf_off(int64_t row, int64_t kblk, int64_t kq)
   return ((row >> 7) * kq + (kblk >> 2)) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (kblk & 3);
 }
 
+// Scheduling units of a group with mt 128-row tiles and ntn n-tiles: tiles
+// (single), 256-row tile rows (pair; x ntn) or cluster tiles (multicast).
+template <int CM>
+__device__ __forceinline__ int group_units(int mt, int ntn) {
+  if (CM == CM_PAIR) return (mt + 1) / 2;
+  if (CM == CM_MC) return (mt / 2) * ntn + ((mt & 1) ? (ntn + 1) / 2 : 0);
+  return mt;
+}
+
 // Tile t of the static schedule -> (group, this CTA's 128-row tile, n-tile).
 // A "tile row" is 128 rows (1-CTA) or 256 rows (pair); group g holds
 // trows_g = ceil(m-tiles_g / (PAIR ? 2 : 1)) of them and s_trow is their
@@ -135,10 +153,48 @@ __device__ __forceinline__ int64_t sf_off(int64_t row, int64_t kblk, int64_t kq)
 // while the group's rows pass over it.  Empty groups own no tiles.  `valid` is
 // false only for the odd half of a pair tile past the group's last row; that
 // half then reuses the even half's rows (m_load) and stores nothing.
-template <bool PAIR>
+//
+// Multicast clusters: t is a cluster tile and s_trow the prefix of
+// group_units<CM_MC>.  A group's first (mt / 2) * ntn cluster tiles pair
+// m-tiles (2i, 2i + 1) on one n-tile (B shared; banded like the other modes);
+// an odd group's last m-tile then takes n-tiles (2j, 2j + 1) (A shared).  For
+// an odd ntn the last of those has no second n-tile: that CTA loads the
+// group's last n-tile again and stores nothing (valid = false).
+template <int CM>
 __device__ __forceinline__ void decode_tile(int t, const Params& p, const int32_t* s_off, const int32_t* s_trow,
-                                            uint32_t rank, int& g, int& m_load, int& n_tile, bool& valid) {
+                                            uint32_t rank, int& g, int& m_load, int& n_tile, bool& valid,
+                                            bool& share_b) {
+  constexpr bool PAIR = CM == CM_PAIR;
   const int ntn = p.num_n_tiles;
+  share_b = true;
+  if (CM == CM_MC) {
+    int lo = 0, hi = p.L;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_trow[mid] > t) hi = mid; else lo = mid + 1;
+    }
+    g = lo;
+    const int r = t - (g ? s_trow[g - 1] : 0);
+    const int m0 = (g ? s_off[g - 1] : 0) / kBM;
+    const int mtg = s_off[g] / kBM - m0;
+    const int pairs = mtg / 2;
+    if (r < pairs * ntn) {
+      const int W = p.raster_w;
+      const int band = r / (pairs * W);
+      const int w = min(W, ntn - band * W);
+      const int rr = r - band * pairs * W;
+      n_tile = band * W + rr % w;
+      m_load = m0 + 2 * (rr / w) + static_cast<int>(rank);
+      valid = true;
+    } else {
+      const int nt = 2 * (r - pairs * ntn) + static_cast<int>(rank);
+      valid = nt < ntn;
+      n_tile = valid ? nt : ntn - 1;
+      m_load = m0 + mtg - 1;
+      share_b = false;
+    }
+    return;
+  }
   const int u = t / ntn;
   int lo = 0, hi = p.L;
   while (lo < hi) {
@@ -353,14 +409,19 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* 
   }
 }
 
-template <bool FP4, int BN, bool PAIR, int EPI, int OUTC>
+template <bool FP4, int BN, int CM, int EPI, int OUTC>
 __global__ void __launch_bounds__(kThreads, 1)
     bsgg_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                 const __grid_constant__ Params p) {
+  constexpr bool PAIR = CM == CM_PAIR;
+  constexpr bool MC = CM == CM_MC;
+  constexpr bool CLUSTER = CM != CM_SINGLE;
+  static_assert(!MC || BN == 256, "multicast clusters use 128 x 256 tiles");
   using Ly = Layout<FP4, BN, PAIR>;
   constexpr int S = Ly::kStages;
   constexpr int NA = Ly::kNumAcc;
+  constexpr uint32_t kABytesHalf = Ly::kABytes / 2;   // one 64-row A box (multicast clusters)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -380,14 +441,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const uint32_t rank = CLUSTER ? cluster_ctarank() : 0u;
   const bool leader = (rank == 0);
-  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int num_units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const bool issues_mma = !PAIR || leader;       // the CTA that issues this CTA's MMAs and copies
+  const int unit = CLUSTER ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int num_units = CLUSTER ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   for (int i = tid; i < p.L; i += kThreads) s_off[i] = p.offsets[i];
   if (tid == 0) {
-    for (int s = 0; s < S; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
+    // multicast clusters: a stage is free once both CTAs' MMAs released it
+    for (int s = 0; s < S; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), MC ? 2 : 1); }
     for (int a = 0; a < NA; ++a) {
       mbar_init(accf_bar(a), 1);
       mbar_init(acce_bar(a), PAIR ? 2 * kEpiWarps : kEpiWarps);
@@ -407,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     else { tmem_alloc(smem_u32(tmem_holder), Ly::kTmemCols); tmem_relinquish(); }
   }
   tc_fence_before();
-  if (PAIR) cluster_sync(); else __syncthreads();
+  if (CLUSTER) cluster_sync(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
@@ -426,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int local = 0;
     for (int g = g0; g < g1; ++g) {
       const int mt = (s_off[g] - (g ? s_off[g - 1] : 0)) / kBM;
-      local += PAIR ? (mt + 1) / 2 : mt;
+      local += group_units<CM>(mt, p.num_n_tiles);
     }
     int incl = local;
 #pragma unroll
@@ -437,12 +500,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int run = incl - local;
     for (int g = g0; g < g1; ++g) {
       const int mt = (s_off[g] - (g ? s_off[g - 1] : 0)) / kBM;
-      run += PAIR ? (mt + 1) / 2 : mt;
+      run += group_units<CM>(mt, p.num_n_tiles);
       s_trow[g] = run;
     }
   }
   __syncthreads();
-  const int num_tiles = bad ? 0 : s_trow[p.L - 1] * p.num_n_tiles;
+  const int num_tiles = bad ? 0 : s_trow[p.L - 1] * (MC ? 1 : p.num_n_tiles);
 
   if (bad) {
     if (blockIdx.x == 0 && tid == 0) atomicOr(p.status, kStatusBadOffsets);
@@ -458,8 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = unit; t < num_tiles && ok; t += num_units) {
         int g, mt, nt;
-        bool valid;
-        decode_tile<PAIR>(t, p, s_off, s_trow, rank, g, mt, nt, valid);
+        bool valid, share_b;
+        decode_tile<CM>(t, p, s_off, s_trow, rank, g, mt, nt, valid, share_b);
         const int b_row = nt * BN + (PAIR ? static_cast<int>(rank) * Ly::kBRows : 0);
         const int sfb_rb = g * p.rn_b + nt * Ly::kHalves;
         for (int ks = 0; ks < p.num_k_stages; ++ks) {
@@ -478,6 +541,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d_pair(sB, &tmB, fbl, k0, b_row, g);
             tma_load_3d_pair(sSa, &tmSFA, fbl, 0, ka, mt);
             tma_load_3d_pair(sSb, &tmSFB, fbl, 0, ka, sfb_rb);
+          } else if (MC) {
+            // every byte of this CTA's stage counts on its own barrier; the
+            // shared operand arrives half from each CTA (A boxes are 64 rows,
+            // B boxes 128 rows)
+            const int r = static_cast<int>(rank);
+            mbar_expect_tx(fb, Ly::kStageBytes);
+            if (share_b) {
+              tma_load_2d(sA, &tmA, fb, k0, mt * kBM);
+              tma_load_2d(sA + kABytesHalf, &tmA, fb, k0, mt * kBM + kBM / 2);
+              tma_load_3d_mc(sB + r * (Ly::kBBytes / 2), &tmB, fb, k0, b_row + r * (BN / 2), g, 0x3);
+            } else {
+              tma_load_2d_mc(sA + r * kABytesHalf, &tmA, fb, k0, mt * kBM + r * (kBM / 2), 0x3);
+              tma_load_3d(sB, &tmB, fb, k0, b_row, g);
+              tma_load_3d(sB + Ly::kBBytes / 2, &tmB, fb, k0, b_row + BN / 2, g);
+            }
+            tma_load_3d(sSa, &tmSFA, fb, 0, ka, mt);
+            tma_load_3d(sSb, &tmSFB, fb, 0, ka, sfb_rb);
           } else {
             mbar_expect_tx(fb, Ly::kStageBytes);
             tma_load_2d(sA, &tmA, fb, k0, mt * kBM);
@@ -490,18 +570,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
       }
+      if (ok && CLUSTER) {
+        // wait until the last use of every stage was released (by both CTAs'
+        // MMAs in a multicast cluster): no commit or load of the other CTA
+        // still targets this CTA's shared memory when the CTAs part
+        for (int i = 0; i < S; ++i) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+      }
       if (!ok) {
         atomicOr(p.status, kStatusTimeout);
         // drain: wait (bounded) for every load this thread issued to land.  In a
-        // pair the loads complete the even CTA's barriers, which cannot be
-        // polled from here: wait out the drain bound instead.
+        // cluster the loads also complete barriers of the other CTA (pair: the
+        // even CTA's; multicast: both), which cannot be polled from here: wait
+        // out the drain bound instead.
         for (int s = 0; s < S; ++s)
           if (issued[s]) {
             const uint64_t t0 = globaltimer_ns();
             while (globaltimer_ns() - t0 < kDrainLimitNs) {
-              if (!PAIR && mbar_try_wait(full_bar(s), issued_phase[s])) break;
+              if (!CLUSTER && mbar_try_wait(full_bar(s), issued_phase[s])) break;
             }
-            if (PAIR) break;
+            if (CLUSTER) break;
           }
       }
     }
@@ -512,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // per-MMA scalar work would leave the tensor pipe idle.  All shared-memory
     // descriptors are formed once and advanced by adds (the start-address field
     // holds address / 16 in its low 14 bits; every address here is < 256 KB).
-    if (lane == 0 && leader) {
+    if (lane == 0 && issues_mma) {
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -545,7 +635,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             else tc_mma_mxf8(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sfa_t, sfb_t, accum);
           }
         }
-        if (PAIR) tc_commit_pair(empty_bar(st), 3); else tc_commit(empty_bar(st));
+        // release the stage (in both CTAs of a cluster)
+        if (PAIR) tc_commit_pair(empty_bar(st), 3);
+        else if (MC) tc_commit_mc(empty_bar(st), 3);
+        else tc_commit(empty_bar(st));
       };
       for (int t = unit; t < num_tiles && ok; t += num_units) {
         if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
@@ -579,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Same stage sequence as the MMA issuer.  Writing a stage's tensor-memory
     // scale slot is safe once its "full" barrier completed: the refill behind
     // it waited for the MMAs that read the slot's previous contents.
-    if (lane == 0 && leader) {
+    if (lane == 0 && issues_mma) {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -629,8 +722,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int t = unit; t < num_tiles; t += num_units) {
       int g, mt, nt;
-      bool valid;
-      decode_tile<PAIR>(t, p, s_off, s_trow, rank, g, mt, nt, valid);
+      bool valid, share_b;
+      decode_tile<CM>(t, p, s_off, s_trow, rank, g, mt, nt, valid, share_b);
       const bool got = __all_sync(0xffffffffu, mbar_wait(accf_bar(acc), acc_phase, abort_flag, kWaitLimitNs));
       if (!got) {
         if (lane == 0) atomicOr(p.status, kStatusTimeout);
@@ -688,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  if (PAIR) cluster_sync(); else __syncthreads();
+  if (CLUSTER) cluster_sync(); else __syncthreads();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();

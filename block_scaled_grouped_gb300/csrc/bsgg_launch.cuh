@@ -1,22 +1,24 @@
 // bsgg_launch.cuh -- instantiates the kernel for one (input family, tile
-// shape) and dispatches a Launch to the right (epilogue, output class) instance.
+// shape, cluster mode) and dispatches a Launch to the right (epilogue, output
+// class) instance.
 #pragma once
 
 #include "bsgg_internal.h"
 
 namespace bsgg {
 
-template <bool FP4, int BN, bool PAIR, int EPI, int OUTC>
+template <bool FP4, int BN, int CM, int EPI, int OUTC>
 cudaError_t launch_one(const Launch& L) {
-  auto kern = bsgg_kernel<FP4, BN, PAIR, EPI, OUTC>;
-  const int smem = Layout<FP4, BN, PAIR>::kSmemBytes;
+  auto kern = bsgg_kernel<FP4, BN, CM, EPI, OUTC>;
+  constexpr bool kCluster = CM != CM_SINGLE;
+  const int smem = Layout<FP4, BN, CM == CM_PAIR>::kSmemBytes;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    if (PAIR) {
+    if (kCluster) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
       if (e != cudaSuccess) return e;
     }
@@ -28,7 +30,7 @@ cudaError_t launch_one(const Launch& L) {
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = L.stream;
   cudaLaunchAttribute attr[1];
-  if (PAIR) {
+  if (kCluster) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
@@ -39,30 +41,31 @@ cudaError_t launch_one(const Launch& L) {
   return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmSFA, L.tmSFB, L.p);
 }
 
-template <bool FP4, int BN, bool PAIR, int EPI>
+template <bool FP4, int BN, int CM, int EPI>
 cudaError_t launch_outc(const Launch& L) {
   switch (L.outc) {
-    case OUTC_FLOAT: return launch_one<FP4, BN, PAIR, EPI, OUTC_FLOAT>(L);
-    case OUTC_FP8: return launch_one<FP4, BN, PAIR, EPI, OUTC_FP8>(L);
-    case OUTC_FP4: return launch_one<FP4, BN, PAIR, EPI, OUTC_FP4>(L);
+    case OUTC_FLOAT: return launch_one<FP4, BN, CM, EPI, OUTC_FLOAT>(L);
+    case OUTC_FP8: return launch_one<FP4, BN, CM, EPI, OUTC_FP8>(L);
+    case OUTC_FP4: return launch_one<FP4, BN, CM, EPI, OUTC_FP4>(L);
   }
   return cudaErrorInvalidValue;
 }
 
-template <bool FP4, int BN, bool PAIR>
+template <bool FP4, int BN, int CM>
 cudaError_t launch_shape(const Launch& L) {
   switch (L.epi) {
-    case EPI_GATE: return launch_outc<FP4, BN, PAIR, EPI_GATE>(L);
-    case EPI_SWIGLU: return launch_outc<FP4, BN, PAIR, EPI_SWIGLU>(L);
-    case EPI_SRELU: return launch_outc<FP4, BN, PAIR, EPI_SRELU>(L);
+    case EPI_GATE: return launch_outc<FP4, BN, CM, EPI_GATE>(L);
+    case EPI_SWIGLU: return launch_outc<FP4, BN, CM, EPI_SWIGLU>(L);
+    case EPI_SRELU: return launch_outc<FP4, BN, CM, EPI_SRELU>(L);
   }
   return cudaErrorInvalidValue;
 }
 
-template <bool FP4>
-int pair_resident_ctas_impl() {
-  auto kern = bsgg_kernel<FP4, 256, true, EPI_GATE, OUTC_FLOAT>;
-  const int smem = Layout<FP4, 256, true>::kSmemBytes;
+// Clusters of two of this kernel that fit on the device at once, x 2.
+template <bool FP4, int CM>
+int cluster_resident_ctas_impl() {
+  auto kern = bsgg_kernel<FP4, 256, CM, EPI_GATE, OUTC_FLOAT>;
+  const int smem = Layout<FP4, 256, CM == CM_PAIR>::kSmemBytes;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);

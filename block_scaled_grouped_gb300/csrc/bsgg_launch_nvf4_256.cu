@@ -2,5 +2,5 @@
 #include "bsgg_launch.cuh"
 
 namespace bsgg {
-cudaError_t launch_nvf4_256(const Launch& L) { return launch_shape<true, 256, false>(L); }
+cudaError_t launch_nvf4_256(const Launch& L) { return launch_shape<true, 256, CM_SINGLE>(L); }
 }  // namespace bsgg

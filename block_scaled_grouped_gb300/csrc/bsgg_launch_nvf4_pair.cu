@@ -2,8 +2,9 @@
 #include "bsgg_launch.cuh"
 
 namespace bsgg {
-cudaError_t launch_nvf4_pair(const Launch& L) { return launch_shape<true, 256, true>(L); }
-int pair_resident_ctas(bool fp4) {
-  return fp4 ? pair_resident_ctas_impl<true>() : pair_resident_ctas_impl<false>();
+cudaError_t launch_nvf4_pair(const Launch& L) { return launch_shape<true, 256, CM_PAIR>(L); }
+int cluster_resident_ctas(bool fp4, bool mc) {
+  if (mc) return fp4 ? cluster_resident_ctas_impl<true, CM_MC>() : cluster_resident_ctas_impl<false, CM_MC>();
+  return fp4 ? cluster_resident_ctas_impl<true, CM_PAIR>() : cluster_resident_ctas_impl<false, CM_PAIR>();
 }
 }  // namespace bsgg

@@ -106,7 +106,15 @@ typedef struct {
                              ("Grouped GEMM + Quant (SM100)", Common Parameters) */
   int32_t tile_n;         /* columns per MMA tile: 128 or 256 (256 when tile_m = 256); 0 = library
                              choice.  The pages' mma_tiler_mn[1] */
-  int32_t reserved;       /* must be zero */
+  /* Thread-block cluster shape (cluster_m, cluster_n): the pages' cluster_shape_mn
+     ("Grouped GEMM + Quant (SM100)", Common Parameters; Support Surface and Constraints,
+     Tiling and Cluster).  Built: (1, 1) with tile_m = 128; (2, 1) with tile 256 x 256 (the
+     CTA pair); (2, 1) with tile 128 x 256: two CTAs, each computing its own 128 x 256 tile,
+     share one operand tile through TMA multicast.  (0, 0) = the library's choice.  Other
+     powers of two up to 4 are valid on the pages and return BSGG_ERR_UNSUPPORTED; any other
+     value returns BSGG_ERR_INVALID_ARG. */
+  int32_t cluster_m;
+  int32_t cluster_n;
 } bsgg_desc;
 
 /* Tensors of one call.  Unused outputs may be NULL: d_col/sfd_col unless

@@ -21,13 +21,24 @@ def to_device(p: W.Problem, device="cuda") -> W.Problem:
         b=p.b.to(device), sfb_rows=p.sfb_rows.to(device))
 
 
-TILES = [(128, 128), (128, 256), (256, 256)]
+# (tile_m, tile_n, cluster_m, cluster_n): single CTA 128 x 128 and 128 x 256,
+# multicast clusters of two 128 x 256 CTAs, and 256 x 256 CTA pairs
+TILES = [(128, 128, 1, 1), (128, 256, 1, 1), (128, 256, 2, 1), (256, 256, 2, 1)]
+
+
+def tile_id(t) -> str:
+    if tuple(t[:2]) == (0, 0):
+        return "default"
+    return f"{t[0]}x{t[1]}" + (f"c{t[2]}x{t[3]}" if len(t) > 2 else "")
 
 
 def make_plan(p: W.Problem, gate_first=False, tile=(0, 0)) -> bsgg.Plan:
+    """tile: (tile_m, tile_n) or (tile_m, tile_n, cluster_m, cluster_n)."""
+    cluster = tuple(tile[2:4]) if len(tile) > 2 else (0, 0)
     return bsgg.Plan(m_pad=p.m_pad, n=p.n, k=p.k, num_groups=p.num_groups, in_format=p.in_fmt,
                      out_format=p.out_fmt, epilogue=p.epi, want_col=p.want_col,
-                     gate_first=gate_first, tanh_clamp_s=p.tanh_clamp_s, tile=tile)
+                     gate_first=gate_first, tanh_clamp_s=p.tanh_clamp_s, tile=tuple(tile[:2]),
+                     cluster=cluster)
 
 
 def alloc_outputs(plan: bsgg.Plan, device="cuda") -> dict:

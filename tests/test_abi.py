@@ -57,7 +57,7 @@ def _create(**over):
                      bsgg.OUT_FORMATS[d["out_format"]], bsgg.EPILOGUES[d["epilogue"]],
                      int(d.get("want_col", 0)), int(d.get("gate_first", 0)),
                      float(d.get("tanh_clamp_s", 0.0)), int(d.get("tile_m", 0)), int(d.get("tile_n", 0)),
-                     int(d.get("reserved", 0)))
+                     int(d.get("cluster_m", 0)), int(d.get("cluster_n", 0)))
     h = ctypes.c_void_p()
     return bsgg.lib().bsgg_create(ctypes.byref(desc), ctypes.byref(h))
 
@@ -72,9 +72,13 @@ def _create(**over):
     (dict(tanh_clamp_s=-1.0, epilogue="srelu"), 1),
     (dict(tanh_clamp_s=8.0, epilogue="gate"), 1),
     (dict(want_col=1, out_format="bf16"), 1),   # D_col only with quantized outputs
-    (dict(reserved=1), 1),
     (dict(tile_m=64), 1), (dict(tile_n=192), 1),
     (dict(tile_m=256, tile_n=128), 2),           # pairs are built for 256 x 256 tiles
+    (dict(cluster_m=1), 1), (dict(cluster_n=1), 1),          # cluster shape: both or neither
+    (dict(cluster_m=3, cluster_n=1), 1), (dict(cluster_m=8, cluster_n=1), 1),   # powers of 2 <= 4
+    (dict(tile_m=256, cluster_m=1, cluster_n=1), 1),         # 2-CTA tiles need an even CLUSTER_M
+    (dict(cluster_m=4, cluster_n=1), 2), (dict(cluster_m=1, cluster_n=2), 2),   # valid, not built
+    (dict(tile_m=128, tile_n=128, cluster_m=2, cluster_n=1), 2),
     (dict(in_format="nvfp4", out_format="e4m3"), 2),   # not on the pages
 ])
 def test_create_rejects(lib, over, code):

@@ -20,6 +20,8 @@ def _torchrun(args, timeout=240):
 
 
 def test_max_over_ranks_with_gloo(tmp_path):
+    # each rank writes its result to its own file: the ranks' stdout streams
+    # interleave
     script = tmp_path / "ranks.py"
     script.write_text(
         "import os, sys\n"
@@ -28,13 +30,12 @@ def test_max_over_ranks_with_gloo(tmp_path):
         "world, rank, local = bench.dist_setup(2)\n"
         "m = bench.max_over_ranks(float(rank + 1) * 10.0, world)\n"
         "bench.barrier(world)\n"
-        "print('RESULT', rank, m, flush=True)\n"
+        f"open(os.path.join({str(tmp_path)!r}, 'rank%d.txt' % rank), 'w').write(repr(m))\n"
         "import torch.distributed as dist; dist.destroy_process_group()\n")
     r = _torchrun([str(script)])
     assert r.returncode == 0, r.stderr[-2000:]
-    import re
-    got = sorted(re.findall(r"RESULT (\d) ([0-9.]+)", r.stdout))
-    assert got == [("0", "20.0"), ("1", "20.0")]
+    got = [float((tmp_path / f"rank{i}.txt").read_text()) for i in range(2)]
+    assert got == [20.0, 20.0]
 
 
 def test_reference_arm_prints_once_from_rank_zero():

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from helpers import oracle_inputs, oracle_run, small_problem
-from gpu_harness import TILES, alloc_outputs, compare, make_plan, run_gpu, to_device, SENTINEL
+from gpu_harness import TILES, tile_id, alloc_outputs, compare, make_plan, run_gpu, to_device, SENTINEL
 from block_scaled_grouped_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -39,25 +39,25 @@ def _parity(p, gate_first=False, check_amax=True, tile=(0, 0)):
     return outs, ref
 
 
-@pytest.mark.parametrize("tile", TILES, ids=lambda t: f"{t[0]}x{t[1]}")
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
 def test_tiny_workload(tile):
     _parity(W.workload("tiny"), tile=tile)
 
 
-@pytest.mark.parametrize("tile", TILES, ids=lambda t: f"{t[0]}x{t[1]}")
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
 def test_gate_bf16_ragged_groups_and_k_tail(tile):
     # groups 300, 0, 129, 1000, 64 rows -> padded to 128; K=416 leaves a 32-column stage
     p = small_problem(counts=(300, 0, 129, 1000, 64), k=416, n=384, pad_to=128, seed=21)
     _parity(_spread_scales(p), tile=tile)
 
 
-@pytest.mark.parametrize("tile", TILES, ids=lambda t: f"{t[0]}x{t[1]}")
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
 def test_first_and_last_group_empty_and_n_tail(tile):
     p = small_problem(counts=(0, 200, 0, 130, 0), k=256, n=96, pad_to=128, seed=22)
     _parity(p, tile=tile)
 
 
-@pytest.mark.parametrize("tile", TILES, ids=lambda t: f"{t[0]}x{t[1]}")
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
 def test_single_group_f32_and_f16(tile):
     p = small_problem(counts=(256,), k=512, n=256, pad_to=128, out_fmt="f32", seed=23)
     _parity(_spread_scales(p), tile=tile)
@@ -66,28 +66,28 @@ def test_single_group_f32_and_f16(tile):
     _parity(p, tile=tile)
 
 
-@pytest.mark.parametrize("tile", TILES, ids=lambda t: f"{t[0]}x{t[1]}")
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
 def test_e5m2_inputs(tile):
     p = small_problem(counts=(128, 100), k=256, n=128, pad_to=128, in_fmt="mxfp8_e5m2", seed=24)
     _parity(p, tile=tile)
 
 
 @pytest.mark.parametrize("gate_first", [False, True])
-@pytest.mark.parametrize("tile", TILES, ids=lambda t: f"{t[0]}x{t[1]}")
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
 def test_swiglu_e4m3_row_and_col(gate_first, tile):
     p = small_problem(counts=(130, 256, 40), k=384, n=512, pad_to=128, epi="swiglu",
                       out_fmt="e4m3", want_col=True, seed=25)
     _parity(_spread_scales(p), gate_first=gate_first, tile=tile)
 
 
-@pytest.mark.parametrize("tile", TILES, ids=lambda t: f"{t[0]}x{t[1]}")
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
 def test_srelu_clamp_e4m3_norm_half(tile):
     p = small_problem(counts=(200, 0, 77), k=256, n=256, pad_to=128, epi="srelu", out_fmt="e4m3",
                       want_col=True, tanh_clamp_s=8.0, norm_const=0.5, seed=26)
     _parity(p, tile=tile)
 
 
-@pytest.mark.parametrize("tile", TILES, ids=lambda t: f"{t[0]}x{t[1]}")
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
 def test_srelu_e5m2_and_bf16(tile):
     p = small_problem(counts=(128, 300), k=512, n=256, pad_to=128, epi="srelu", out_fmt="e5m2",
                       want_col=True, seed=27)
@@ -97,34 +97,34 @@ def test_srelu_e5m2_and_bf16(tile):
     _parity(p, tile=tile)
 
 
-@pytest.mark.parametrize("tile", TILES, ids=lambda t: f"{t[0]}x{t[1]}")
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
 def test_mxfp8_to_e2m1_with_columns(tile):
     p = small_problem(counts=(256, 90), k=256, n=256, pad_to=128, epi="gate", out_fmt="e2m1",
                       want_col=True, seed=29)
     _parity(p, tile=tile)
 
 
-@pytest.mark.parametrize("tile", TILES, ids=lambda t: f"{t[0]}x{t[1]}")
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
 def test_nvfp4_gate_bf16(tile):
     p = small_problem(counts=(150, 0, 300), k=512, n=384, pad_to=128, in_fmt="nvfp4", seed=30)
     _parity(_spread_scales(p), tile=tile)
 
 
-@pytest.mark.parametrize("tile", TILES, ids=lambda t: f"{t[0]}x{t[1]}")
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
 def test_nvfp4_k_tail(tile):
     # K = 288: the last stage holds 32 FP4 elements (one MMA of 64, half zero-filled)
     p = small_problem(counts=(128, 128), k=288, n=128, pad_to=128, in_fmt="nvfp4", seed=31)
     _parity(p, tile=tile)
 
 
-@pytest.mark.parametrize("tile", TILES, ids=lambda t: f"{t[0]}x{t[1]}")
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
 def test_nvfp4_srelu_clamp_e2m1(tile):
     p = small_problem(counts=(300, 128, 0, 50), k=512, n=256, pad_to=128, in_fmt="nvfp4",
                       epi="srelu", out_fmt="e2m1", tanh_clamp_s=8.0, seed=32)
     _parity(p, tile=tile)
 
 
-@pytest.mark.parametrize("tile", TILES, ids=lambda t: f"{t[0]}x{t[1]}")
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
 def test_nvfp4_e2m1_row_and_16_row_column_blocks(tile):
     # NVFP4 inputs: E4M3 scales per 16 values for D rows and for D_col columns
     p = small_problem(counts=(256, 70, 0, 130), k=512, n=256, pad_to=128, in_fmt="nvfp4",
@@ -135,7 +135,7 @@ def test_nvfp4_e2m1_row_and_16_row_column_blocks(tile):
     _parity(p, tile=tile)
 
 
-@pytest.mark.parametrize("tile", TILES, ids=lambda t: f"{t[0]}x{t[1]}")
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
 def test_nvfp4_swiglu_bf16(tile):
     p = small_problem(counts=(128, 200), k=256, n=256, pad_to=128, in_fmt="nvfp4",
                       epi="swiglu", out_fmt="bf16", seed=33)

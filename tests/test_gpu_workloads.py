@@ -12,7 +12,7 @@ import torch
 
 import oracle as orc
 from helpers import IN_CODE, OUT_CODE, EPI_CODE, np_
-from gpu_harness import TILES, compare, decode_float_out, make_plan, run_gpu
+from gpu_harness import TILES, tile_id, compare, decode_float_out, make_plan, run_gpu
 from block_scaled_grouped_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -54,7 +54,7 @@ def workload(request):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("tile", [(0, 0)] + TILES, ids=lambda t: "default" if t == (0, 0) else f"{t[0]}x{t[1]}")
+@pytest.mark.parametrize("tile", [(0, 0)] + TILES, ids=tile_id)
 def test_full_size_parity_on_sampled_blocks(workload, tile):
     p, blocks, ref = workload
     outs, _, _ = run_gpu(p, tile=tile)
