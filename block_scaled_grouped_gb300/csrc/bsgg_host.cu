@@ -183,11 +183,12 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
   P->desc = *desc;
   P->device = device;
   P->num_sms = num_sms;
-  // library choice (measured on GB300): 128 x 256 tiles for NVFP4 and for
-  // short reductions, where per-tile synchronisation weighs more; 256 x 256
-  // tiles on CTA pairs for MXFP8 with K >= 8192
+  // library choice (measured on GB300): 256 x 256 tiles on CTA pairs for
+  // MXFP8 (half the shared-memory operand traffic per MMA of 1-CTA tiles),
+  // 128 x 256 single-CTA tiles for NVFP4 (a pair copies each CTA's scale
+  // atoms with every stage and gains nothing there)
   int tm = desc->tile_m, tn = desc->tile_n, cm = desc->cluster_m;
-  if (tm == 0) tm = (desc->in_format != BSGG_IN_NVFP4 && desc->k >= 8192 && tn != 128 && cm != 1) ? 256 : 128;
+  if (tm == 0) tm = (desc->in_format != BSGG_IN_NVFP4 && tn != 128 && cm != 1) ? 256 : 128;
   if (tn == 0) tn = 256;
   if (cm == 0) cm = (tm == 256) ? 2 : 1;
   P->pair = (tm == 256);

@@ -266,9 +266,14 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Arrive on an mbarrier given by its shared::cluster address (any CTA of the cluster).
+// Arrive on an mbarrier given by its shared::cluster address (any CTA of the
+// cluster), with the default CTA-scope release: the arrival orders only what
+// the tcgen05 fences before it already order (tensor-memory reads).  A
+// cluster-scope release would first wait until every earlier global store of
+// the thread is visible to the cluster, about a microsecond per tile behind
+// the epilogue's stores.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // TMA loads whose completion may be signalled on the peer CTA's mbarrier.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
