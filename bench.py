@@ -335,7 +335,8 @@ def run_gpu(args, world, rank, local):
     ratio = DTYPE_RATIO[p.in_fmt]
     peak = peaks["bf16_tflops"] * ratio
     achieved = p.flops / (elapsed_ms / args.steps * 1e-3) / 1e12
-    traffic = recorded_traffic(p.name)
+    # the recorded counters are of the library's default tile shape
+    traffic = recorded_traffic(p.name) if not (args.tile or args.cluster) else None
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": (f"{peak_kind} bf16 burst {peaks['bf16_tflops']} TFLOP/s x "
