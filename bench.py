@@ -60,9 +60,13 @@ def measured_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources that make up bsgg_kernel and its launch (not the
+    peak-measurement unit)."""
     d = os.path.join(ROOT, "block_scaled_grouped_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(d)):
+        if name == "bsgg_peak.cu":
+            continue
         with open(os.path.join(d, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -230,6 +234,30 @@ def make_workload(name: str, device):
     return W.workload(name, device=device)
 
 
+def algorithmic_bytes(p) -> int:
+    """Bytes a launch must move at least: A, SFA, the B and SFB slices of the
+    non-empty groups, and the outputs (D, D_col, SFD_row, SFD_col or amax)."""
+    def cdiv(a, b):
+        return -(-a // b)
+
+    def sfb(rows, cols, v, slices=1):
+        return 512 * slices * cdiv(rows, 128) * cdiv(cdiv(cols, v), 4)
+    fp4 = p.in_fmt == "nvfp4"
+    v = 16 if fp4 else 32
+    kb = p.k // 2 if fp4 else p.k
+    off = [int(x) for x in p.padded_offsets.tolist()]
+    nonempty = sum(1 for g, e in enumerate(off) if e > (off[g - 1] if g else 0))
+    n_out = p.n // 2 if p.epi == "swiglu" else p.n
+    bits = {"bf16": 16, "f16": 16, "f32": 32, "e4m3": 8, "e5m2": 8, "e2m1": 4}[p.out_fmt]
+    d = p.m_pad * n_out * bits // 8
+    out = d * (2 if p.want_col else 1)
+    if p.out_fmt in ("e4m3", "e5m2", "e2m1"):
+        out += sfb(p.m_pad, n_out, v) + (sfb(n_out, p.m_pad, v) if p.want_col else 0)
+    else:
+        out += 4 * p.num_groups
+    return (p.m_pad * kb + sfb(p.m_pad, p.k, v) + nonempty * p.n * kb + sfb(p.n, p.k, v, nonempty) + out)
+
+
 def config_of(p, extra=None):
     c = {"workload": p.name, "experts": p.num_groups, "rows_valid": p.m_real, "rows_padded": p.m_pad,
          "n": p.n, "k": p.k, "in": DTYPE_NAME[p.in_fmt], "out": p.out_fmt, "epilogue": p.epi,
@@ -337,6 +365,11 @@ def run_gpu(args, world, rank, local):
     achieved = p.flops / (elapsed_ms / args.steps * 1e-3) / 1e12
     # the recorded counters are of the library's default tile shape
     traffic = recorded_traffic(p.name) if not (args.tile or args.cluster) else None
+    alg_bytes = algorithmic_bytes(p)
+    hbm_gbs = alg_bytes / (elapsed_ms / args.steps * 1e-3) / 1e9
+    hbm = {"algorithmic_bytes": alg_bytes, "achieved_gbs": hbm_gbs, "peak_gbs": peaks["hbm_gbs"],
+           "frac": hbm_gbs / peaks["hbm_gbs"],
+           "what": "algorithmic bytes per launch / kernel time (not the bound of this kernel)"}
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": (f"{peak_kind} bf16 burst {peaks['bf16_tflops']} TFLOP/s x "
@@ -383,10 +416,32 @@ def run_gpu(args, world, rank, local):
                                         "tile": args.tile or "library default",
                                         "cluster": args.cluster or "library default"}),
                 "gpu_launches": args.steps, "clocks": clocks, "roofline": roofline,
-                "e2e": e2e, "cpu_baseline": cpu_baseline,
+                "e2e": e2e, "cpu_baseline": cpu_baseline, "hbm": hbm,
                 "pct_of_dtype_peak": 100.0 * achieved / peak}
         print(json.dumps(line), flush=True)
     plan.close()
+
+
+def run_mma_peak():
+    """The tensor pipe's dense block-scaled rate on resident operands, with the
+    SM clock sampled meanwhile."""
+    import block_scaled_grouped_gb300 as bsgg
+    from block_scaled_grouped_gb300 import build as bsgg_build
+    bsgg_build.build()
+    sampler = ClockSampler(0)
+    res = {}
+    for fmt in ("mxfp8_e4m3", "nvfp4"):
+        for n in (128, 256):
+            bsgg.measure_mma_peak(fmt, n, 40000)          # warm-up
+    sampler.start()
+    sampler.mark(True)
+    for fmt in ("mxfp8_e4m3", "nvfp4"):
+        for n in (128, 256):
+            res[f"{DTYPE_NAME[fmt]} M=128 N={n}"] = max(bsgg.measure_mma_peak(fmt, n, 1 << 20) for _ in range(3))
+    sampler.mark(False)
+    clocks = sampler.stop()
+    print(json.dumps({"metric": "dense block-scaled MMA TFLOP/s, operands resident in shared memory",
+                      "unit": "TFLOP/s", "values": res, "clocks": clocks}), flush=True)
 
 
 def main():
@@ -405,7 +460,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=0.0)
+    ap.add_argument("--mma-peak", action="store_true", help="print the measured dense block-scaled "
+                    "MMA throughput (bsgg_measure_mma_peak) for MXFP8 and NVFP4 and exit")
     args = ap.parse_args()
+    if args.mma_peak:
+        run_mma_peak()
+        return
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, world, rank)

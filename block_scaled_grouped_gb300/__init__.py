@@ -21,7 +21,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CU
           4: "device wait timed out", 5: "padded_offsets invalid"}
 
 SYMBOLS = ("bsgg_create", "bsgg_run", "bsgg_run_host", "bsgg_query_device_status", "bsgg_destroy",
-           "bsgg_status_string", "bsgg_sf_bytes", "bsgg_sf_offset", "bsgg_pack_sf", "bsgg_run_noalloc")
+           "bsgg_status_string", "bsgg_sf_bytes", "bsgg_sf_offset", "bsgg_pack_sf", "bsgg_run_noalloc",
+           "bsgg_measure_mma_peak")
 
 
 class BsggError(RuntimeError):
@@ -81,6 +82,9 @@ def lib():
         L.bsgg_run_noalloc.restype = ctypes.c_int
         L.bsgg_run_noalloc.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(Args), ctypes.c_void_p,
                                        ctypes.c_int32]
+        L.bsgg_measure_mma_peak.restype = ctypes.c_int
+        L.bsgg_measure_mma_peak.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                            ctypes.POINTER(ctypes.c_double), ctypes.c_void_p]
         L.bsgg_pack_sf.restype = ctypes.c_int
         L.bsgg_pack_sf.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                    ctypes.c_int32, ctypes.c_void_p]
@@ -211,6 +215,15 @@ class Plan:
             self.close()
         except Exception:
             pass
+
+
+def measure_mma_peak(in_format: str, tile_n: int = 256, mmas_per_sm: int = 400000, stream=None) -> float:
+    """bsgg_measure_mma_peak: TFLOP/s of back-to-back block-scaled MMAs on
+    resident operands (no loads, no epilogue) on the current device."""
+    out = ctypes.c_double()
+    _check(lib().bsgg_measure_mma_peak(IN_FORMATS[in_format], int(tile_n), int(mmas_per_sm),
+                                       ctypes.byref(out), _stream(stream)), "bsgg_measure_mma_peak")
+    return float(out.value)
 
 
 def run_noalloc(*, m_pad: int, n: int, k: int, num_groups: int, in_format: str, out_format: str,

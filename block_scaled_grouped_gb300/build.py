@@ -19,7 +19,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libbsgg.so")
 UNITS = ["bsgg_host.cu", "bsgg_launch_mxf8_128.cu", "bsgg_launch_mxf8_256.cu", "bsgg_launch_mxf8_pair.cu",
          "bsgg_launch_mxf8_mc.cu", "bsgg_launch_nvf4_128.cu", "bsgg_launch_nvf4_256.cu",
-         "bsgg_launch_nvf4_pair.cu", "bsgg_launch_nvf4_mc.cu"]
+         "bsgg_launch_nvf4_pair.cu", "bsgg_launch_nvf4_mc.cu", "bsgg_peak.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE]

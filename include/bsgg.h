@@ -211,6 +211,20 @@ bsgg_status bsgg_pack_sf(const uint8_t* rowmajor, uint8_t* swizzled, int64_t row
 bsgg_status bsgg_run_noalloc(const bsgg_desc* desc, const bsgg_args* args, void* stream,
                              int32_t wait_status);
 
+/* Measurement utility; the pages have no counterpart.  Measures the dense
+ * block-scaled tensor-core throughput of the current device, the denominator of
+ * the kernel's roofline: one CTA per SM issues `mmas_per_sm` tcgen05.mma
+ * block_scale instructions (M = 128, N = tile_n, K = 32 for MXFP8 or 64 for
+ * NVFP4) on operands and unit scales resident in shared memory, with no loads and
+ * no epilogue, timed with CUDA events on `stream`.  Synchronizes the stream.
+ * in_format: a bsgg_in_format; tile_n: 128 or 256; mmas_per_sm: 4 .. 2^22.
+ * Writes TFLOP/s (2*M*N*K per instruction) to *tflops.  Allocates and frees a
+ * 4-byte status word.  Errors: BSGG_ERR_INVALID_ARG for other arguments,
+ * BSGG_ERR_CUDA for a failed CUDA call, BSGG_ERR_DEVICE_TIMEOUT if the final
+ * wait ran out (2 s). */
+bsgg_status bsgg_measure_mma_peak(int32_t in_format, int32_t tile_n, int64_t mmas_per_sm, double* tflops,
+                                  void* stream);
+
 #ifdef __cplusplus
 }
 #endif
