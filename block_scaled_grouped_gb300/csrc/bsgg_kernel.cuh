@@ -20,7 +20,7 @@
 //     receives its 128 rows of D.  Half the operand bytes per FLOP of 1-CTA
 //     tiles.  A group with an odd number of 128-row tiles ends in a pair tile
 //     whose odd half recomputes the even half's rows and stores nothing.
-// Eleven warps per CTA:
+// Warp roles.  Eleven warps (352 threads) when the scale factors are copied:
 //   warp 0      TMA producer: A, B[g] (128-byte swizzle) and the scale-factor
 //               atoms (512-byte boxes) into a multi-stage ring; in a pair both
 //               producers complete the even CTA's "full" barrier
@@ -35,6 +35,12 @@
 //               half into registers (then the accumulator is released), alpha,
 //               the activation and prob (Step 2), per-group amax or the row /
 //               column block quantization (Step 3), global stores
+// NVFP4 single-CTA tiles (sixteen warps, 512 threads) store the scales
+// instead: an NVFP4 stage has twelve atoms, and the copies of them held the
+// tensor pipe back.  Warps 0 and 1 as above; warps 2..5 write the scales with
+// tcgen05.st, one per lane quadrant, A's atoms without the copy path's
+// four-fold replication; warps 6, 7 idle; warps 8..15 the epilogue.  Warps
+// 0..7 give registers to the epilogue (setmaxnreg: 64 / 192 per thread).
 // All waits are bounded; a wait that runs out raises a CTA-wide abort flag and
 // a device status bit, and every role then drains its in-flight asynchronous
 // work (again with a bound) and returns.
@@ -48,7 +54,6 @@
 namespace bsgg {
 
 enum : int { EPI_GATE = 0, EPI_SWIGLU = 1, EPI_SRELU = 2 };
-enum : int { CM_SINGLE = 0, CM_PAIR = 1, CM_MC = 2 };
 // Output class (template) and exact output kind (runtime) of D.
 enum : int { OUTC_FLOAT = 0, OUTC_FP8 = 1, OUTC_FP4 = 2 };
 enum : int { OK_BF16 = 0, OK_F16 = 1, OK_F32 = 2, OK_E4M3 = 3, OK_E5M2 = 4, OK_E2M1 = 5 };
@@ -56,8 +61,25 @@ enum : int { OK_BF16 = 0, OK_F16 = 1, OK_F32 = 2, OK_E4M3 = 3, OK_E5M2 = 4, OK_E
 constexpr int kBM = 128;          // rows per CTA tile (TMEM lanes)
 constexpr int kBKBytes = 128;     // K bytes per pipeline stage (one 128-byte swizzle span)
 constexpr int kEpiWarps = 8;      // two warps per tensor-memory lane quadrant
-constexpr int kScaleWarp = 2 + kEpiWarps;  // the warp that copies scale atoms to tensor memory
-constexpr int kThreads = 96 + 32 * kEpiWarps;
+enum : int { CM_SINGLE = 0, CM_PAIR = 1, CM_MC = 2 };
+// Scale factors reach tensor memory by tcgen05.st from four warps (one per
+// lane quadrant) for NVFP4 single-CTA tiles, by tcgen05.cp from one thread
+// otherwise (see the kernel's role table).
+template <bool FP4, int CM>
+constexpr bool scale_stores() { return FP4 && CM == CM_SINGLE; }
+template <bool ST>
+struct Roles {
+  static constexpr int kThreads = ST ? 512 : 96 + 32 * kEpiWarps;
+  static constexpr int kEpiFirst = ST ? 8 : 2;   // epilogue warps [kEpiFirst, kEpiFirst + 8)
+  static constexpr int kCopyWarp = 10;           // tcgen05.cp mode: the copying warp
+  // tcgen05.st mode: warps 0-7 drop to kLowRegs, warps 8-15 rise to kHighRegs;
+  // 256 x kLowRegs + 256 x kHighRegs = 512 x 128, the launch's registers
+  static constexpr int kLaunchRegs = 128;
+  static constexpr int kLowRegs = 64;
+  static constexpr int kHighRegs = 192;
+};
+static_assert(256 * Roles<true>::kLowRegs + 256 * Roles<true>::kHighRegs == 512 * Roles<true>::kLaunchRegs,
+              "the register split must add up to the launch's registers");
 constexpr int kMaxGroups = 1024;
 constexpr uint32_t kStatusTimeout = 1u;
 constexpr uint32_t kStatusBadOffsets = 2u;
@@ -410,7 +432,7 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* 
 }
 
 template <bool FP4, int BN, int CM, int EPI, int OUTC>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
     bsgg_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                 const __grid_constant__ Params p) {
@@ -418,6 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool MC = CM == CM_MC;
   constexpr bool CLUSTER = CM != CM_SINGLE;
   static_assert(!MC || BN == 256, "multicast clusters use 128 x 256 tiles");
+  constexpr bool ST = scale_stores<FP4, CM>();
+  using Ro = Roles<ST>;
   using Ly = Layout<FP4, BN, PAIR>;
   constexpr int S = Ly::kStages;
   constexpr int NA = Ly::kNumAcc;
@@ -447,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int unit = CLUSTER ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int num_units = CLUSTER ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
-  for (int i = tid; i < p.L; i += kThreads) s_off[i] = p.offsets[i];
+  for (int i = tid; i < p.L; i += Ro::kThreads) s_off[i] = p.offsets[i];
   if (tid == 0) {
     // multicast clusters: a stage is free once both CTAs' MMAs released it
     for (int s = 0; s < S; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), MC ? 2 : 1); }
@@ -456,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(acce_bar(a), PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(drain_bar, 1);
-    for (int st = 0; st < S; ++st) mbar_init(sfr_bar(st), 1);
+    for (int st = 0; st < S; ++st) mbar_init(sfr_bar(st), ST ? 4 : 1);
     mbar_init(drain_bar2, 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -476,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // padded_offsets must be non-decreasing multiples of 128 ending at m_pad.
   int bad = 0;
-  for (int i = tid; i < p.L; i += kThreads) {
+  for (int i = tid; i < p.L; i += Ro::kThreads) {
     const int prev = i ? s_off[i - 1] : 0;
     if (s_off[i] < prev || (s_off[i] % kBM) != 0) bad = 1;
   }
@@ -509,214 +533,259 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (bad) {
     if (blockIdx.x == 0 && tid == 0) atomicOr(p.status, kStatusBadOffsets);
-  } else if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued_phase[S];
-      bool issued[S];
-#pragma unroll
-      for (int s = 0; s < S; ++s) { issued[s] = false; issued_phase[s] = 0; }
-      bool ok = true;
-      for (int t = unit; t < num_tiles && ok; t += num_units) {
-        int g, mt, nt;
-        bool valid, share_b;
-        decode_tile<CM>(t, p, s_off, s_trow, rank, g, mt, nt, valid, share_b);
-        const int b_row = nt * BN + (PAIR ? static_cast<int>(rank) * Ly::kBRows : 0);
-        const int sfb_rb = g * p.rn_b + nt * Ly::kHalves;
-        for (int ks = 0; ks < p.num_k_stages; ++ks) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
-          const uint32_t fb = full_bar(stage);
-          const int k0 = ks * kBKBytes, ka = 2 * ks * Ly::kAtoms;
-          const uint32_t sA = sbase + Ly::kOffA + stage * Ly::kABytes;
-          const uint32_t sB = sbase + Ly::kOffB + stage * Ly::kBBytes;
-          const uint32_t sSa = sbase + Ly::kOffSfa + stage * Ly::kSfaBytes;
-          const uint32_t sSb = sbase + Ly::kOffSfb + stage * Ly::kSfbBytes;
-          if (PAIR) {
-            // both CTAs' bytes complete the even CTA's barrier
-            const uint32_t fbl = mapa_shared(fb, 0);
-            if (leader) mbar_expect_tx(fb, 2u * Ly::kStageBytes);
-            tma_load_2d_pair(sA, &tmA, fbl, k0, mt * kBM);
-            tma_load_3d_pair(sB, &tmB, fbl, k0, b_row, g);
-            tma_load_3d_pair(sSa, &tmSFA, fbl, 0, ka, mt);
-            tma_load_3d_pair(sSb, &tmSFB, fbl, 0, ka, sfb_rb);
-          } else if (MC) {
-            // every byte of this CTA's stage counts on its own barrier; the
-            // shared operand arrives half from each CTA (A boxes are 64 rows,
-            // B boxes 128 rows)
-            const int r = static_cast<int>(rank);
-            mbar_expect_tx(fb, Ly::kStageBytes);
-            if (share_b) {
-              tma_load_2d(sA, &tmA, fb, k0, mt * kBM);
-              tma_load_2d(sA + kABytesHalf, &tmA, fb, k0, mt * kBM + kBM / 2);
-              tma_load_3d_mc(sB + r * (Ly::kBBytes / 2), &tmB, fb, k0, b_row + r * (BN / 2), g, 0x3);
+  } else if (ST ? warp < 8 : (warp < 2 || warp == Ro::kCopyWarp)) {
+    // producer, MMA issuer, scale warps (and, storing scales, two idle warps)
+    if constexpr (ST) setmaxnreg_dec<Ro::kLowRegs>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_phase[S];
+        bool issued[S];
+  #pragma unroll
+        for (int s = 0; s < S; ++s) { issued[s] = false; issued_phase[s] = 0; }
+        bool ok = true;
+        for (int t = unit; t < num_tiles && ok; t += num_units) {
+          int g, mt, nt;
+          bool valid, share_b;
+          decode_tile<CM>(t, p, s_off, s_trow, rank, g, mt, nt, valid, share_b);
+          const int b_row = nt * BN + (PAIR ? static_cast<int>(rank) * Ly::kBRows : 0);
+          const int sfb_rb = g * p.rn_b + nt * Ly::kHalves;
+          for (int ks = 0; ks < p.num_k_stages; ++ks) {
+            if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            const uint32_t fb = full_bar(stage);
+            const int k0 = ks * kBKBytes, ka = 2 * ks * Ly::kAtoms;
+            const uint32_t sA = sbase + Ly::kOffA + stage * Ly::kABytes;
+            const uint32_t sB = sbase + Ly::kOffB + stage * Ly::kBBytes;
+            const uint32_t sSa = sbase + Ly::kOffSfa + stage * Ly::kSfaBytes;
+            const uint32_t sSb = sbase + Ly::kOffSfb + stage * Ly::kSfbBytes;
+            if (PAIR) {
+              // both CTAs' bytes complete the even CTA's barrier
+              const uint32_t fbl = mapa_shared(fb, 0);
+              if (leader) mbar_expect_tx(fb, 2u * Ly::kStageBytes);
+              tma_load_2d_pair(sA, &tmA, fbl, k0, mt * kBM);
+              tma_load_3d_pair(sB, &tmB, fbl, k0, b_row, g);
+              tma_load_3d_pair(sSa, &tmSFA, fbl, 0, ka, mt);
+              tma_load_3d_pair(sSb, &tmSFB, fbl, 0, ka, sfb_rb);
+            } else if (MC) {
+              // every byte of this CTA's stage counts on its own barrier; the
+              // shared operand arrives half from each CTA (A boxes are 64 rows,
+              // B boxes 128 rows)
+              const int r = static_cast<int>(rank);
+              mbar_expect_tx(fb, Ly::kStageBytes);
+              if (share_b) {
+                tma_load_2d(sA, &tmA, fb, k0, mt * kBM);
+                tma_load_2d(sA + kABytesHalf, &tmA, fb, k0, mt * kBM + kBM / 2);
+                tma_load_3d_mc(sB + r * (Ly::kBBytes / 2), &tmB, fb, k0, b_row + r * (BN / 2), g, 0x3);
+              } else {
+                tma_load_2d_mc(sA + r * kABytesHalf, &tmA, fb, k0, mt * kBM + r * (kBM / 2), 0x3);
+                tma_load_3d(sB, &tmB, fb, k0, b_row, g);
+                tma_load_3d(sB + Ly::kBBytes / 2, &tmB, fb, k0, b_row + BN / 2, g);
+              }
+              tma_load_3d(sSa, &tmSFA, fb, 0, ka, mt);
+              tma_load_3d(sSb, &tmSFB, fb, 0, ka, sfb_rb);
             } else {
-              tma_load_2d_mc(sA + r * kABytesHalf, &tmA, fb, k0, mt * kBM + r * (kBM / 2), 0x3);
+              mbar_expect_tx(fb, Ly::kStageBytes);
+              tma_load_2d(sA, &tmA, fb, k0, mt * kBM);
               tma_load_3d(sB, &tmB, fb, k0, b_row, g);
-              tma_load_3d(sB + Ly::kBBytes / 2, &tmB, fb, k0, b_row + BN / 2, g);
+              tma_load_3d(sSa, &tmSFA, fb, 0, ka, mt);
+              tma_load_3d(sSb, &tmSFB, fb, 0, ka, sfb_rb);
             }
-            tma_load_3d(sSa, &tmSFA, fb, 0, ka, mt);
-            tma_load_3d(sSb, &tmSFB, fb, 0, ka, sfb_rb);
-          } else {
-            mbar_expect_tx(fb, Ly::kStageBytes);
-            tma_load_2d(sA, &tmA, fb, k0, mt * kBM);
-            tma_load_3d(sB, &tmB, fb, k0, b_row, g);
-            tma_load_3d(sSa, &tmSFA, fb, 0, ka, mt);
-            tma_load_3d(sSb, &tmSFB, fb, 0, ka, sfb_rb);
+            issued[stage] = true;
+            issued_phase[stage] = phase;
+            if (++stage == S) { stage = 0; phase ^= 1u; }
           }
-          issued[stage] = true;
-          issued_phase[stage] = phase;
-          if (++stage == S) { stage = 0; phase ^= 1u; }
         }
-      }
-      if (ok && CLUSTER) {
-        // wait until the last use of every stage was released (by both CTAs'
-        // MMAs in a multicast cluster): no commit or load of the other CTA
-        // still targets this CTA's shared memory when the CTAs part
-        for (int i = 0; i < S; ++i) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
-          if (++stage == S) { stage = 0; phase ^= 1u; }
+        if (ok && CLUSTER) {
+          // wait until the last use of every stage was released (by both CTAs'
+          // MMAs in a multicast cluster): no commit or load of the other CTA
+          // still targets this CTA's shared memory when the CTAs part
+          for (int i = 0; i < S; ++i) {
+            if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            if (++stage == S) { stage = 0; phase ^= 1u; }
+          }
         }
-      }
-      if (!ok) {
-        atomicOr(p.status, kStatusTimeout);
-        // drain: wait (bounded) for every load this thread issued to land.  In a
-        // cluster the loads also complete barriers of the other CTA (pair: the
-        // even CTA's; multicast: both), which cannot be polled from here: wait
-        // out the drain bound instead.
-        for (int s = 0; s < S; ++s)
-          if (issued[s]) {
-            const uint64_t t0 = globaltimer_ns();
-            while (globaltimer_ns() - t0 < kDrainLimitNs) {
-              if (!CLUSTER && mbar_try_wait(full_bar(s), issued_phase[s])) break;
+        if (!ok) {
+          atomicOr(p.status, kStatusTimeout);
+          // drain: wait (bounded) for every load this thread issued to land.  In a
+          // cluster the loads also complete barriers of the other CTA (pair: the
+          // even CTA's; multicast: both), which cannot be polled from here: wait
+          // out the drain bound instead.
+          for (int s = 0; s < S; ++s)
+            if (issued[s]) {
+              const uint64_t t0 = globaltimer_ns();
+              while (globaltimer_ns() - t0 < kDrainLimitNs) {
+                if (!CLUSTER && mbar_try_wait(full_bar(s), issued_phase[s])) break;
+              }
+              if (CLUSTER) break;
             }
-            if (CLUSTER) break;
-          }
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // One thread issues every tcgen05 operation of the CTA (pair).  Its loop is
-    // kept short: the tcgen05 queue holds little more than one stage, so any
-    // per-MMA scalar work would leave the tensor pipe idle.  All shared-memory
-    // descriptors are formed once and advanced by adds (the start-address field
-    // holds address / 16 in its low 14 bits; every address here is < 256 KB).
-    if (lane == 0 && issues_mma) {
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
-      const uint32_t sf_tmem0 = tmem_base + NA * BN;
-      const uint64_t a_desc0 = sdesc_kmajor_sw128(sbase + Ly::kOffA);
-      const uint64_t b_desc0 = sdesc_kmajor_sw128(sbase + Ly::kOffB);
-      // instruction descriptors of the four MMAs of a stage: MXFP8 selects the
-      // scale byte (k-block) of each row's word, NVFP4 uses whole words
-      uint32_t idk[4];
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        idk[kk] = FP4 ? p.idesc : (p.idesc | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4));
-      const int full_stages = p.k / Ly::kKElems;      // stages with all four MMAs
-      auto issue_stage = [&](uint32_t d_tmem, int st, int n_mma, uint32_t acc0) {
-        const uint32_t sfa_t = sf_tmem0 + st * Ly::kSfColsPerStage;
-        const uint32_t sfb_t = sfa_t + Ly::kSfaCols;
-        const uint64_t ad = a_desc0 + static_cast<uint64_t>((st * Ly::kABytes) >> 4);
-        const uint64_t bd = b_desc0 + static_cast<uint64_t>((st * Ly::kBBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          if (kk >= n_mma) break;
-          const uint32_t accum = kk ? 1u : acc0;
-          // one MMA consumes 32 K-bytes: +2 in descriptor units
-          if (FP4) {
-            const uint32_t sa = sfa_t + 4 * kk, sb = sfb_t + 4 * Ly::kHalves * kk;
-            if (PAIR) tc_mma_nvf4_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sa, sb, accum);
-            else tc_mma_nvf4(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sa, sb, accum);
-          } else {
-            if (PAIR) tc_mma_mxf8_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sfa_t, sfb_t, accum);
-            else tc_mma_mxf8(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sfa_t, sfb_t, accum);
-          }
         }
-        // release the stage (in both CTAs of a cluster)
-        if (PAIR) tc_commit_pair(empty_bar(st), 3);
-        else if (MC) tc_commit_mc(empty_bar(st), 3);
-        else tc_commit(empty_bar(st));
-      };
-      for (int t = unit; t < num_tiles && ok; t += num_units) {
-        if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int ks = 0; ks < p.num_k_stages; ++ks) {
-          if (!mbar_wait(sfr_bar(stage), phase, abort_flag, kWaitLimitNs)) { ok = false; break; }
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      // One thread issues every tcgen05 operation of the CTA (pair).  Its loop is
+      // kept short: the tcgen05 queue holds little more than one stage, so any
+      // per-MMA scalar work would leave the tensor pipe idle.  All shared-memory
+      // descriptors are formed once and advanced by adds (the start-address field
+      // holds address / 16 in its low 14 bits; every address here is < 256 KB).
+      if (lane == 0 && issues_mma) {
+        int stage = 0, acc = 0;
+        uint32_t phase = 0, acc_phase = 0;
+        bool ok = true;
+        const uint32_t sf_tmem0 = tmem_base + NA * BN;
+        const uint64_t a_desc0 = sdesc_kmajor_sw128(sbase + Ly::kOffA);
+        const uint64_t b_desc0 = sdesc_kmajor_sw128(sbase + Ly::kOffB);
+        // instruction descriptors of the four MMAs of a stage: MXFP8 selects the
+        // scale byte (k-block) of each row's word, NVFP4 uses whole words
+        uint32_t idk[4];
+  #pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          idk[kk] = FP4 ? p.idesc : (p.idesc | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4));
+        const int full_stages = p.k / Ly::kKElems;      // stages with all four MMAs
+        auto issue_stage = [&](uint32_t d_tmem, int st, int n_mma, uint32_t acc0) {
+          const uint32_t sfa_t = sf_tmem0 + st * Ly::kSfColsPerStage;
+          const uint32_t sfb_t = sfa_t + Ly::kSfaCols;
+          const uint64_t ad = a_desc0 + static_cast<uint64_t>((st * Ly::kABytes) >> 4);
+          const uint64_t bd = b_desc0 + static_cast<uint64_t>((st * Ly::kBBytes) >> 4);
+  #pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            if (kk >= n_mma) break;
+            const uint32_t accum = kk ? 1u : acc0;
+            // one MMA consumes 32 K-bytes: +2 in descriptor units
+            if (FP4) {
+              const uint32_t sa = sfa_t + 4 * kk, sb = sfb_t + 4 * Ly::kHalves * kk;
+              if (PAIR) tc_mma_nvf4_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sa, sb, accum);
+              else tc_mma_nvf4(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sa, sb, accum);
+            } else {
+              if (PAIR) tc_mma_mxf8_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sfa_t, sfb_t, accum);
+              else tc_mma_mxf8(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sfa_t, sfb_t, accum);
+            }
+          }
+          // release the stage (in both CTAs of a cluster)
+          if (PAIR) tc_commit_pair(empty_bar(st), 3);
+          else if (MC) tc_commit_mc(empty_bar(st), 3);
+          else tc_commit(empty_bar(st));
+        };
+        for (int t = unit; t < num_tiles && ok; t += num_units) {
+          if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
           tc_fence_after();
-          if (ks < full_stages) {
-            issue_stage(d_tmem, stage, 4, ks ? 1u : 0u);
-          } else {
-            const int k_left = p.k - ks * Ly::kKElems;
-            issue_stage(d_tmem, stage, (k_left + Ly::kMmaK - 1) / Ly::kMmaK, ks ? 1u : 0u);
+          const uint32_t d_tmem = tmem_base + acc * BN;
+          for (int ks = 0; ks < p.num_k_stages; ++ks) {
+            if (!mbar_wait(sfr_bar(stage), phase, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            tc_fence_after();
+            if (ks < full_stages) {
+              issue_stage(d_tmem, stage, 4, ks ? 1u : 0u);
+            } else {
+              const int k_left = p.k - ks * Ly::kKElems;
+              issue_stage(d_tmem, stage, (k_left + Ly::kMmaK - 1) / Ly::kMmaK, ks ? 1u : 0u);
+            }
+            if (++stage == S) { stage = 0; phase ^= 1u; }
           }
-          if (++stage == S) { stage = 0; phase ^= 1u; }
+          if (!ok) break;
+          if (PAIR) tc_commit_pair(accf_bar(acc), 3); else tc_commit(accf_bar(acc));
+          if (++acc == NA) { acc = 0; acc_phase ^= 1u; }
         }
-        if (!ok) break;
-        if (PAIR) tc_commit_pair(accf_bar(acc), 3); else tc_commit(accf_bar(acc));
-        if (++acc == NA) { acc = 0; acc_phase ^= 1u; }
+        if (!ok) {
+          atomicOr(p.status, kStatusTimeout);
+          // drain: wait (bounded) until every issued tcgen05 operation completed
+          if (PAIR) tc_commit_pair(drain_bar, 1); else tc_commit(drain_bar);
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(drain_bar, 0) && globaltimer_ns() - t0 < kDrainLimitNs) {}
+        }
       }
-      if (!ok) {
-        atomicOr(p.status, kStatusTimeout);
-        // drain: wait (bounded) until every issued tcgen05 operation completed
-        if (PAIR) tc_commit_pair(drain_bar, 1); else tc_commit(drain_bar);
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(drain_bar, 0) && globaltimer_ns() - t0 < kDrainLimitNs) {}
-      }
-    }
-  } else if (warp == kScaleWarp) {
-    // ------------------------------------------------------------ scale copier
-    // Same stage sequence as the MMA issuer.  Writing a stage's tensor-memory
-    // scale slot is safe once its "full" barrier completed: the refill behind
-    // it waited for the MMAs that read the slot's previous contents.
-    if (lane == 0 && issues_mma) {
+    } else if (ST ? warp < 6 : true) {
+     if constexpr (ST) {
+      // ------------------------------------------------------------ scale stores
+      // One warp per tensor-memory lane quadrant q.  The MMA reads row r's A
+      // scales from lane r, column (r / 32) % 4 of the atom's 4-column group, so
+      // the warp writes A's atoms into column q of its own 32 lanes only; every
+      // quadrant reads the scales of every B row, so B's atoms go into all four
+      // columns.  A quarter of A's tensor-memory writes of the copy path.
+      const uint32_t q = static_cast<uint32_t>(warp & 3);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      const uint32_t sf_tmem0 = tmem_base + NA * BN;
-      const uint64_t sfa_desc0 = sdesc_sf_block(sbase + Ly::kOffSfa);
-      const uint64_t sfb_desc0 = sdesc_sf_block(sbase + Ly::kOffSfb);
+      const uint32_t sf_tmem0 = tmem_base + NA * BN + ((q * 32u) << 16);
       for (int t = unit; t < num_tiles && ok; t += num_units) {
         for (int ks = 0; ks < p.num_k_stages; ++ks) {
-          if (!mbar_wait(full_bar(stage), phase, abort_flag, kWaitLimitNs)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t sfa_t = sf_tmem0 + stage * Ly::kSfColsPerStage;
-          const uint32_t sfb_t = sfa_t + Ly::kSfaCols;
-          const uint64_t sfa_d = sfa_desc0 + static_cast<uint64_t>((stage * Ly::kSfaBytes) >> 4);
-          const uint64_t sfb_d = sfb_desc0 + static_cast<uint64_t>((stage * Ly::kSfbBytes) >> 4);
-          // atom i of A at columns 4i; atom i of B's 128-row block h at
-          // columns 4 * (i * halves + h)
-#pragma unroll
-          for (int i = 0; i < Ly::kAtoms; ++i) {
-            if (PAIR) tc_cp_32x128b_x4_pair(sfa_t + 4 * i, sfa_d + 32 * i);
-            else tc_cp_32x128b_x4(sfa_t + 4 * i, sfa_d + 32 * i);
-#pragma unroll
-            for (int h = 0; h < Ly::kHalves; ++h) {
-              const uint32_t dst = sfb_t + 4 * (i * Ly::kHalves + h);
-              const uint64_t src = sfb_d + 32 * (h * Ly::kAtoms + i);
-              if (PAIR) tc_cp_32x128b_x4_pair(dst, src); else tc_cp_32x128b_x4(dst, src);
-            }
+          if (!__all_sync(0xffffffffu, mbar_wait(full_bar(stage), phase, abort_flag, kWaitLimitNs))) {
+            ok = false;
+            break;
           }
-          if (PAIR) tc_commit_pair(sfr_bar(stage), 1); else tc_commit(sfr_bar(stage));
+          const uint32_t slot = sf_tmem0 + stage * Ly::kSfColsPerStage;
+          const uint8_t* sa = smem + Ly::kOffSfa + stage * Ly::kSfaBytes + 16 * lane;
+          const uint8_t* sb = smem + Ly::kOffSfb + stage * Ly::kSfbBytes + 16 * lane;
+  #pragma unroll
+          for (int i = 0; i < Ly::kAtoms; ++i) {
+            const uint4 va = *reinterpret_cast<const uint4*>(sa + 512 * i);
+            tmem_st_x1(slot + 4 * i + q, q == 0 ? va.x : q == 1 ? va.y : q == 2 ? va.z : va.w);
+  #pragma unroll
+            for (int h = 0; h < Ly::kHalves; ++h)
+              tmem_st_x4(slot + Ly::kSfaCols + 4 * (i * Ly::kHalves + h),
+                         *reinterpret_cast<const uint4*>(sb + 512 * (h * Ly::kAtoms + i)));
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sfr_bar(stage));
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
       }
-      if (!ok) {
-        atomicOr(p.status, kStatusTimeout);
-        // drain: wait (bounded) until this thread's copies completed
-        if (PAIR) tc_commit_pair(drain_bar2, 1); else tc_commit(drain_bar2);
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(drain_bar2, 0) && globaltimer_ns() - t0 < kDrainLimitNs) {}
+      if (!ok && lane == 0) atomicOr(p.status, kStatusTimeout);
+     } else {
+      // ------------------------------------------------------------ scale copier
+      // Same stage sequence as the MMA issuer.  Writing a stage's tensor-memory
+      // scale slot is safe once its "full" barrier completed: the refill behind
+      // it waited for the MMAs that read the slot's previous contents.
+      if (lane == 0 && issues_mma) {
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        const uint32_t sf_tmem0 = tmem_base + NA * BN;
+        const uint64_t sfa_desc0 = sdesc_sf_block(sbase + Ly::kOffSfa);
+        const uint64_t sfb_desc0 = sdesc_sf_block(sbase + Ly::kOffSfb);
+        for (int t = unit; t < num_tiles && ok; t += num_units) {
+          for (int ks = 0; ks < p.num_k_stages; ++ks) {
+            if (!mbar_wait(full_bar(stage), phase, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sfa_t = sf_tmem0 + stage * Ly::kSfColsPerStage;
+            const uint32_t sfb_t = sfa_t + Ly::kSfaCols;
+            const uint64_t sfa_d = sfa_desc0 + static_cast<uint64_t>((stage * Ly::kSfaBytes) >> 4);
+            const uint64_t sfb_d = sfb_desc0 + static_cast<uint64_t>((stage * Ly::kSfbBytes) >> 4);
+            // atom i of A at columns 4i; atom i of B's 128-row block h at
+            // columns 4 * (i * halves + h)
+  #pragma unroll
+            for (int i = 0; i < Ly::kAtoms; ++i) {
+              if (PAIR) tc_cp_32x128b_x4_pair(sfa_t + 4 * i, sfa_d + 32 * i);
+              else tc_cp_32x128b_x4(sfa_t + 4 * i, sfa_d + 32 * i);
+  #pragma unroll
+              for (int h = 0; h < Ly::kHalves; ++h) {
+                const uint32_t dst = sfb_t + 4 * (i * Ly::kHalves + h);
+                const uint64_t src = sfb_d + 32 * (h * Ly::kAtoms + i);
+                if (PAIR) tc_cp_32x128b_x4_pair(dst, src); else tc_cp_32x128b_x4(dst, src);
+              }
+            }
+            if (PAIR) tc_commit_pair(sfr_bar(stage), 1); else tc_commit(sfr_bar(stage));
+            if (++stage == S) { stage = 0; phase ^= 1u; }
+          }
+        }
+        if (!ok) {
+          atomicOr(p.status, kStatusTimeout);
+          // drain: wait (bounded) until this thread's copies completed
+          if (PAIR) tc_commit_pair(drain_bar2, 1); else tc_commit(drain_bar2);
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(drain_bar2, 0) && globaltimer_ns() - t0 < kDrainLimitNs) {}
+        }
       }
+     }
     }
   } else {
+    if constexpr (ST) setmaxnreg_inc<Ro::kHighRegs>();
     // ------------------------------------------------------------ epilogue
     constexpr int kWarpCols = BN / 2;                 // accumulator columns per warp
     const int q = warp & 3;                           // tensor-memory lane quadrant
-    const int e = (warp - 2) >> 2;                    // which half of the columns
+    const int e = (warp - Ro::kEpiFirst) >> 2;        // which half of the columns
     const float norm = (OUTC == OUTC_FLOAT) ? 1.0f : *p.norm_const;
     int acc = 0;
     uint32_t acc_phase = 0;

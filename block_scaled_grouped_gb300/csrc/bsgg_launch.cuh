@@ -11,6 +11,8 @@ template <bool FP4, int BN, int CM, int EPI, int OUTC>
 cudaError_t launch_one(const Launch& L) {
   auto kern = bsgg_kernel<FP4, BN, CM, EPI, OUTC>;
   constexpr bool kCluster = CM != CM_SINGLE;
+  constexpr bool kStores = scale_stores<FP4, CM>();
+  using Ro = Roles<kStores>;
   const int smem = Layout<FP4, BN, CM == CM_PAIR>::kSmemBytes;
   static int configured_device = -1;
   int dev = 0;
@@ -22,11 +24,20 @@ cudaError_t launch_one(const Launch& L) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
       if (e != cudaSuccess) return e;
     }
+    if (kStores) {
+      // the warpgroups' setmaxnreg shares add up to exactly the launch's
+      // registers only if the kernel was compiled to kLaunchRegs per thread;
+      // with fewer the raising warps would wait forever: refuse to launch
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs != Ro::kLaunchRegs) return cudaErrorInvalidConfiguration;
+    }
     configured_device = dev;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(L.grid), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(Ro::kThreads, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = L.stream;
   cudaLaunchAttribute attr[1];
@@ -69,7 +80,7 @@ int cluster_resident_ctas_impl() {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(Roles<scale_stores<FP4, CM>()>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
