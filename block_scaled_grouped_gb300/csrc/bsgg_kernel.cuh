@@ -35,12 +35,13 @@
 //               half into registers (then the accumulator is released), alpha,
 //               the activation and prob (Step 2), per-group amax or the row /
 //               column block quantization (Step 3), global stores
-// NVFP4 single-CTA tiles (sixteen warps, 512 threads) store the scales
-// instead: an NVFP4 stage has twelve atoms, and the copies of them held the
+// NVFP4 single-CTA tiles and CTA pairs (sixteen warps, 512 threads) store
+// the scales instead: the copies of an NVFP4 stage's twelve atoms held the
 // tensor pipe back.  Warps 0 and 1 as above; warps 2..5 write the scales with
 // tcgen05.st, one per lane quadrant, A's atoms without the copy path's
-// four-fold replication; warps 6, 7 idle; warps 8..15 the epilogue.  Warps
-// 0..7 give registers to the epilogue (setmaxnreg: 64 / 192 per thread).
+// four-fold replication (in a pair each CTA's warps write its own tensor
+// memory and report to the even CTA); warps 6, 7 idle; warps 8..15 the
+// epilogue.  Warps 0..7 give registers to the epilogue (setmaxnreg: 64 / 192).
 // All waits are bounded; a wait that runs out raises a CTA-wide abort flag and
 // a device status bit, and every role then drains its in-flight asynchronous
 // work (again with a bound) and returns.
@@ -63,10 +64,11 @@ constexpr int kBKBytes = 128;     // K bytes per pipeline stage (one 128-byte sw
 constexpr int kEpiWarps = 8;      // two warps per tensor-memory lane quadrant
 enum : int { CM_SINGLE = 0, CM_PAIR = 1, CM_MC = 2 };
 // Scale factors reach tensor memory by tcgen05.st from four warps (one per
-// lane quadrant) for NVFP4 single-CTA tiles, by tcgen05.cp from one thread
-// otherwise (see the kernel's role table).
+// lane quadrant) for NVFP4 single-CTA tiles and pairs, by tcgen05.cp from one
+// thread otherwise (see the kernel's role table).  Measured on GB300: stores
+// raise NVFP4 by 19 % (single) and 14 % (pairs) and lower MXFP8 pairs by 17 %.
 template <bool FP4, int CM>
-constexpr bool scale_stores() { return FP4 && CM == CM_SINGLE; }
+constexpr bool scale_stores() { return FP4 && CM != CM_MC; }
 template <bool ST>
 struct Roles {
   static constexpr int kThreads = ST ? 512 : 96 + 32 * kEpiWarps;
@@ -140,7 +142,7 @@ struct Layout {
   static constexpr int kOffSfa = kOffB + kStages * kBBytes;
   static constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
   static constexpr int kOffBars = kOffSfb + kStages * kSfbBytes;
-  static constexpr int kNumBars = 3 * kStages + 2 * kNumAcc + 2;
+  static constexpr int kNumBars = 4 * kStages + 2 * kNumAcc + 2;
   static constexpr int kOffTmemHolder = kOffBars + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemHolder + 4;
   static constexpr int kOffTrows = kOffAbort + 12;
@@ -458,6 +460,9 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
   // stage's scale atoms are in tensor memory (and so its operands in shared memory)
   auto sfr_bar = [&](int st) { return bar0 + 8u * (2 * S + 2 * NA + 1 + st); };
   const uint32_t drain_bar2 = bar0 + 8u * (3 * S + 2 * NA + 1);   // the scale copier's own drain
+  // pairs storing scales: this CTA's scale atoms of the stage have landed (the
+  // operands complete the even CTA's "full" barrier, the scales their own CTA's)
+  auto sfull_bar = [&](int st) { return bar0 + 8u * (3 * S + 2 * NA + 2 + st); };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Ly::kOffTmemHolder);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kOffAbort);
   int32_t* s_trow = reinterpret_cast<int32_t*>(smem + Ly::kOffTrows);
@@ -480,7 +485,9 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
       mbar_init(acce_bar(a), PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(drain_bar, 1);
-    for (int st = 0; st < S; ++st) mbar_init(sfr_bar(st), ST ? 4 : 1);
+    // stores: the four scale warps of each CTA report to the even CTA
+    for (int st = 0; st < S; ++st) mbar_init(sfr_bar(st), ST ? (PAIR ? 8 : 4) : 1);
+    for (int st = 0; st < S; ++st) mbar_init(sfull_bar(st), 1);
     mbar_init(drain_bar2, 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -543,7 +550,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
         uint32_t phase = 0;
         uint32_t issued_phase[S];
         bool issued[S];
-  #pragma unroll
+#pragma unroll
         for (int s = 0; s < S; ++s) { issued[s] = false; issued_phase[s] = 0; }
         bool ok = true;
         for (int t = unit; t < num_tiles && ok; t += num_units) {
@@ -560,7 +567,18 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
             const uint32_t sB = sbase + Ly::kOffB + stage * Ly::kBBytes;
             const uint32_t sSa = sbase + Ly::kOffSfa + stage * Ly::kSfaBytes;
             const uint32_t sSb = sbase + Ly::kOffSfb + stage * Ly::kSfbBytes;
-            if (PAIR) {
+            if (PAIR && ST) {
+              // both CTAs' operand bytes complete the even CTA's barrier, each
+              // CTA's scale bytes its own (its scale warps wait there)
+              const uint32_t fbl = mapa_shared(fb, 0);
+              const uint32_t sfb_own = sfull_bar(stage);
+              if (leader) mbar_expect_tx(fb, 2u * (Ly::kABytes + Ly::kBBytes));
+              mbar_expect_tx(sfb_own, Ly::kSfaBytes + Ly::kSfbBytes);
+              tma_load_2d_pair(sA, &tmA, fbl, k0, mt * kBM);
+              tma_load_3d_pair(sB, &tmB, fbl, k0, b_row, g);
+              tma_load_3d(sSa, &tmSFA, sfb_own, 0, ka, mt);
+              tma_load_3d(sSb, &tmSFB, sfb_own, 0, ka, sfb_rb);
+            } else if (PAIR) {
               // both CTAs' bytes complete the even CTA's barrier
               const uint32_t fbl = mapa_shared(fb, 0);
               if (leader) mbar_expect_tx(fb, 2u * Ly::kStageBytes);
@@ -639,7 +657,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
         // instruction descriptors of the four MMAs of a stage: MXFP8 selects the
         // scale byte (k-block) of each row's word, NVFP4 uses whole words
         uint32_t idk[4];
-  #pragma unroll
+#pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           idk[kk] = FP4 ? p.idesc : (p.idesc | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4));
         const int full_stages = p.k / Ly::kKElems;      // stages with all four MMAs
@@ -648,7 +666,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
           const uint32_t sfb_t = sfa_t + Ly::kSfaCols;
           const uint64_t ad = a_desc0 + static_cast<uint64_t>((st * Ly::kABytes) >> 4);
           const uint64_t bd = b_desc0 + static_cast<uint64_t>((st * Ly::kBBytes) >> 4);
-  #pragma unroll
+#pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             if (kk >= n_mma) break;
             const uint32_t accum = kk ? 1u : acc0;
@@ -672,6 +690,8 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * BN;
           for (int ks = 0; ks < p.num_k_stages; ++ks) {
+            // pairs storing scales: the scale warps waited for the scales only
+            if (PAIR && ST && !mbar_wait(full_bar(stage), phase, abort_flag, kWaitLimitNs)) { ok = false; break; }
             if (!mbar_wait(sfr_bar(stage), phase, abort_flag, kWaitLimitNs)) { ok = false; break; }
             tc_fence_after();
             if (ks < full_stages) {
@@ -709,18 +729,19 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
       const uint32_t sf_tmem0 = tmem_base + NA * BN + ((q * 32u) << 16);
       for (int t = unit; t < num_tiles && ok; t += num_units) {
         for (int ks = 0; ks < p.num_k_stages; ++ks) {
-          if (!__all_sync(0xffffffffu, mbar_wait(full_bar(stage), phase, abort_flag, kWaitLimitNs))) {
+          const uint32_t landed = PAIR ? sfull_bar(stage) : full_bar(stage);
+          if (!__all_sync(0xffffffffu, mbar_wait(landed, phase, abort_flag, kWaitLimitNs))) {
             ok = false;
             break;
           }
           const uint32_t slot = sf_tmem0 + stage * Ly::kSfColsPerStage;
           const uint8_t* sa = smem + Ly::kOffSfa + stage * Ly::kSfaBytes + 16 * lane;
           const uint8_t* sb = smem + Ly::kOffSfb + stage * Ly::kSfbBytes + 16 * lane;
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < Ly::kAtoms; ++i) {
             const uint4 va = *reinterpret_cast<const uint4*>(sa + 512 * i);
             tmem_st_x1(slot + 4 * i + q, q == 0 ? va.x : q == 1 ? va.y : q == 2 ? va.z : va.w);
-  #pragma unroll
+#pragma unroll
             for (int h = 0; h < Ly::kHalves; ++h)
               tmem_st_x4(slot + Ly::kSfaCols + 4 * (i * Ly::kHalves + h),
                          *reinterpret_cast<const uint4*>(sb + 512 * (h * Ly::kAtoms + i)));
@@ -728,7 +749,10 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
           tmem_wait_st();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(sfr_bar(stage));
+          if (lane == 0) {
+            if (PAIR) mbar_arrive_cluster(mapa_shared(sfr_bar(stage), 0));
+            else mbar_arrive(sfr_bar(stage));
+          }
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
       }
@@ -755,11 +779,11 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
             const uint64_t sfb_d = sfb_desc0 + static_cast<uint64_t>((stage * Ly::kSfbBytes) >> 4);
             // atom i of A at columns 4i; atom i of B's 128-row block h at
             // columns 4 * (i * halves + h)
-  #pragma unroll
+#pragma unroll
             for (int i = 0; i < Ly::kAtoms; ++i) {
               if (PAIR) tc_cp_32x128b_x4_pair(sfa_t + 4 * i, sfa_d + 32 * i);
               else tc_cp_32x128b_x4(sfa_t + 4 * i, sfa_d + 32 * i);
-  #pragma unroll
+#pragma unroll
               for (int h = 0; h < Ly::kHalves; ++h) {
                 const uint32_t dst = sfb_t + 4 * (i * Ly::kHalves + h);
                 const uint64_t src = sfb_d + 32 * (h * Ly::kAtoms + i);
