@@ -142,6 +142,31 @@ def test_nvfp4_swiglu_bf16(tile):
     _parity(p, tile=tile)
 
 
+def _sparse_counts(num_groups, filled, seed):
+    """num_groups groups, all empty except `filled` ones (first, last and
+    random ones), each 1..300 rows."""
+    rng = np.random.default_rng(seed)
+    counts = [0] * num_groups
+    idx = {0, num_groups - 1} | set(int(i) for i in rng.choice(num_groups, filled - 2, replace=False))
+    for i in idx:
+        counts[i] = int(rng.integers(1, 301))
+    return counts
+
+
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
+def test_1024_groups_mostly_empty(tile):
+    # the largest expert count the pages allow (L <= 1024), 14 groups non-empty
+    p = small_problem(counts=_sparse_counts(1024, 14, seed=40), k=128, n=256, pad_to=128, seed=40)
+    _parity(_spread_scales(p), tile=tile)
+
+
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
+def test_1024_groups_nvfp4_e2m1(tile):
+    p = small_problem(counts=_sparse_counts(1024, 10, seed=41), k=256, n=256, pad_to=128,
+                      in_fmt="nvfp4", epi="srelu", out_fmt="e2m1", want_col=True, seed=41)
+    _parity(p, tile=tile)
+
+
 def test_bad_offsets_are_reported_and_nothing_is_written():
     p = to_device(small_problem(counts=(128, 128), k=128, n=128, pad_to=128, seed=34))
     for bad in ([100, 256], [256, 128], [128, 384]):
