@@ -22,7 +22,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CU
 
 SYMBOLS = ("bsgg_create", "bsgg_run", "bsgg_run_host", "bsgg_query_device_status", "bsgg_destroy",
            "bsgg_status_string", "bsgg_sf_bytes", "bsgg_sf_offset", "bsgg_pack_sf", "bsgg_run_noalloc",
-           "bsgg_measure_mma_peak")
+           "bsgg_measure_mma_peak", "bsgg_debug_force_timeout")
 
 
 class BsggError(RuntimeError):
@@ -85,6 +85,8 @@ def lib():
         L.bsgg_measure_mma_peak.restype = ctypes.c_int
         L.bsgg_measure_mma_peak.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
                                             ctypes.POINTER(ctypes.c_double), ctypes.c_void_p]
+        L.bsgg_debug_force_timeout.restype = ctypes.c_int
+        L.bsgg_debug_force_timeout.argtypes = [ctypes.c_void_p, ctypes.c_int32]
         L.bsgg_pack_sf.restype = ctypes.c_int
         L.bsgg_pack_sf.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                    ctypes.c_int32, ctypes.c_void_p]
@@ -204,6 +206,11 @@ class Plan:
     def device_status(self, stream=None) -> int:
         """Synchronize and read/clear the device status word (0 = ok)."""
         return int(lib().bsgg_query_device_status(self._h, _stream(stream)))
+
+    def debug_force_timeout(self, enable: bool) -> None:
+        """Test hook (bsgg_debug_force_timeout): later launches give up after a
+        forced barrier timeout and report BSGG_ERR_DEVICE_TIMEOUT."""
+        _check(lib().bsgg_debug_force_timeout(self._h, int(bool(enable))), "bsgg_debug_force_timeout")
 
     def close(self) -> None:
         if getattr(self, "_h", None):

@@ -30,6 +30,7 @@ struct bsgg_plan {
   int64_t n_out;
   int64_t out_row_bytes;
   uint32_t* status;        // device word: kStatus* bits
+  bool force_timeout;      // bsgg_debug_force_timeout
 };
 
 namespace {
@@ -51,6 +52,10 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Barrier-wait bound while bsgg_debug_force_timeout is on: short, so that the
+// test's launch ends quickly.
+constexpr uint64_t kTestWaitLimitNs = 50000000ull;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -361,6 +366,8 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   const double qmax = d.out_format == BSGG_OUT_E4M3 ? 448.0 : d.out_format == BSGG_OUT_E5M2 ? 57344.0 : 6.0;
   p.rcp_qmax = static_cast<float>(1.0 / qmax);
   p.idesc = make_idesc(d.in_format, P->bn, P->pair);
+  p.force_timeout = P->force_timeout ? 1u : 0u;
+  p.wait_limit_ns = P->force_timeout ? kTestWaitLimitNs : bsgg::kWaitLimitNs;
 
   // an upper bound of the scheduling units (clusters may add one 256-row
   // tile row per group)
@@ -384,6 +391,12 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
         : P->mc ? bsgg::launch_mxf8_mc(L)
         : P->bn == 256 ? bsgg::launch_mxf8_256(L) : bsgg::launch_mxf8_128(L);
   return e == cudaSuccess ? BSGG_OK : BSGG_ERR_CUDA;
+}
+
+bsgg_status bsgg_debug_force_timeout(bsgg_plan* P, int32_t enable) {
+  if (!P || (enable != 0 && enable != 1)) return BSGG_ERR_INVALID_ARG;
+  P->force_timeout = enable != 0;
+  return BSGG_OK;
 }
 
 bsgg_status bsgg_query_device_status(bsgg_plan* P, void* stream) {
@@ -500,7 +513,7 @@ extern "C" bsgg_status bsgg_run_noalloc(const bsgg_desc* desc, const bsgg_args* 
 
   // A plan on the stack, derived from `desc` exactly as bsgg_create derives
   // it, whose status word is the static scratch.
-  bsgg_plan P;
+  bsgg_plan P{};
   if (init_plan(desc, dev, sms, &P) != BSGG_OK) return BSGG_ERR_CUDA;
   P.status = scratch;
 

@@ -85,7 +85,7 @@ static_assert(256 * Roles<true>::kLowRegs + 256 * Roles<true>::kHighRegs == 512 
 constexpr int kMaxGroups = 1024;
 constexpr uint32_t kStatusTimeout = 1u;
 constexpr uint32_t kStatusBadOffsets = 2u;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;     // 2 s per wait
+constexpr uint64_t kWaitLimitNs = 2000000000ull;     // 2 s per wait (Params::wait_limit_ns)
 constexpr uint64_t kDrainLimitNs = 200000000ull;     // 0.2 s per drain wait
 
 struct Params {
@@ -113,6 +113,9 @@ struct Params {
   float tanh_s, tanh_rcp_s; // soft clamp s and 1/s (s = 0: off)
   float rcp_qmax;           // fp32(1/q_max) of the output format
   uint32_t idesc;           // tcgen05 instruction descriptor without scale ids
+  uint32_t force_timeout;   // test of the failure path: the MMA thread first waits on a
+                            // barrier nothing completes, so every role gives up and returns
+  uint64_t wait_limit_ns;   // bound of every barrier wait (kWaitLimitNs; shorter in that test)
 };
 
 template <bool FP4, int BN, bool PAIR>
@@ -560,7 +563,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
           const int b_row = nt * BN + (PAIR ? static_cast<int>(rank) * Ly::kBRows : 0);
           const int sfb_rb = g * p.rn_b + nt * Ly::kHalves;
           for (int ks = 0; ks < p.num_k_stages; ++ks) {
-            if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit_ns)) { ok = false; break; }
             const uint32_t fb = full_bar(stage);
             const int k0 = ks * kBKBytes, ka = 2 * ks * Ly::kAtoms;
             const uint32_t sA = sbase + Ly::kOffA + stage * Ly::kABytes;
@@ -620,7 +623,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
           // MMAs in a multicast cluster): no commit or load of the other CTA
           // still targets this CTA's shared memory when the CTAs part
           for (int i = 0; i < S; ++i) {
-            if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit_ns)) { ok = false; break; }
             if (++stage == S) { stage = 0; phase ^= 1u; }
           }
         }
@@ -685,14 +688,16 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
           else if (MC) tc_commit_mc(empty_bar(st), 3);
           else tc_commit(empty_bar(st));
         };
+        // failure-path test: nothing arrives on the drain barrier before an abort
+        if (p.force_timeout && !mbar_wait(drain_bar, 0, abort_flag, p.wait_limit_ns)) ok = false;
         for (int t = unit; t < num_tiles && ok; t += num_units) {
-          if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, kWaitLimitNs)) { ok = false; break; }
+          if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.wait_limit_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * BN;
           for (int ks = 0; ks < p.num_k_stages; ++ks) {
             // pairs storing scales: the scale warps waited for the scales only
-            if (PAIR && ST && !mbar_wait(full_bar(stage), phase, abort_flag, kWaitLimitNs)) { ok = false; break; }
-            if (!mbar_wait(sfr_bar(stage), phase, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            if (PAIR && ST && !mbar_wait(full_bar(stage), phase, abort_flag, p.wait_limit_ns)) { ok = false; break; }
+            if (!mbar_wait(sfr_bar(stage), phase, abort_flag, p.wait_limit_ns)) { ok = false; break; }
             tc_fence_after();
             if (ks < full_stages) {
               issue_stage(d_tmem, stage, 4, ks ? 1u : 0u);
@@ -730,7 +735,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
       for (int t = unit; t < num_tiles && ok; t += num_units) {
         for (int ks = 0; ks < p.num_k_stages; ++ks) {
           const uint32_t landed = PAIR ? sfull_bar(stage) : full_bar(stage);
-          if (!__all_sync(0xffffffffu, mbar_wait(landed, phase, abort_flag, kWaitLimitNs))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(landed, phase, abort_flag, p.wait_limit_ns))) {
             ok = false;
             break;
           }
@@ -771,7 +776,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
         const uint64_t sfb_desc0 = sdesc_sf_block(sbase + Ly::kOffSfb);
         for (int t = unit; t < num_tiles && ok; t += num_units) {
           for (int ks = 0; ks < p.num_k_stages; ++ks) {
-            if (!mbar_wait(full_bar(stage), phase, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            if (!mbar_wait(full_bar(stage), phase, abort_flag, p.wait_limit_ns)) { ok = false; break; }
             tc_fence_after();
             const uint32_t sfa_t = sf_tmem0 + stage * Ly::kSfColsPerStage;
             const uint32_t sfb_t = sfa_t + Ly::kSfaCols;
@@ -817,7 +822,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
       int g, mt, nt;
       bool valid, share_b;
       decode_tile<CM>(t, p, s_off, s_trow, rank, g, mt, nt, valid, share_b);
-      const bool got = __all_sync(0xffffffffu, mbar_wait(accf_bar(acc), acc_phase, abort_flag, kWaitLimitNs));
+      const bool got = __all_sync(0xffffffffu, mbar_wait(accf_bar(acc), acc_phase, abort_flag, p.wait_limit_ns));
       if (!got) {
         if (lane == 0) atomicOr(p.status, kStatusTimeout);
         break;

@@ -163,6 +163,15 @@ bsgg_status bsgg_run_host(bsgg_plan* plan, const bsgg_args* host, const bsgg_arg
  * BSGG_OK, BSGG_ERR_DEVICE_TIMEOUT or BSGG_ERR_BAD_OFFSETS. */
 bsgg_status bsgg_query_device_status(bsgg_plan* plan, void* stream);
 
+/* Test hook for the failure path; the pages have no counterpart.  With enable =
+ * 1, every later bsgg_run / bsgg_run_host of this plan launches a kernel whose
+ * MMA thread first waits on a barrier that nothing completes, with every
+ * barrier wait bounded by 50 ms instead of 2 s: each role gives up, drains its
+ * in-flight work and returns, no output is complete, and the status word reads
+ * BSGG_ERR_DEVICE_TIMEOUT; the CUDA context stays usable.  enable = 0 restores
+ * normal launches.  Errors: BSGG_ERR_INVALID_ARG (null plan, enable not 0/1). */
+bsgg_status bsgg_debug_force_timeout(bsgg_plan* plan, int32_t enable);
+
 void bsgg_destroy(bsgg_plan* plan);
 const char* bsgg_status_string(bsgg_status status);
 
