@@ -720,94 +720,94 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
         }
       }
     } else if (ST ? warp < 6 : true) {
-     if constexpr (ST) {
-      // ------------------------------------------------------------ scale stores
-      // One warp per tensor-memory lane quadrant q.  The MMA reads row r's A
-      // scales from lane r, column (r / 32) % 4 of the atom's 4-column group, so
-      // the warp writes A's atoms into column q of its own 32 lanes only; every
-      // quadrant reads the scales of every B row, so B's atoms go into all four
-      // columns.  A quarter of A's tensor-memory writes of the copy path.
-      const uint32_t q = static_cast<uint32_t>(warp & 3);
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      const uint32_t sf_tmem0 = tmem_base + NA * BN + ((q * 32u) << 16);
-      for (int t = unit; t < num_tiles && ok; t += num_units) {
-        for (int ks = 0; ks < p.num_k_stages; ++ks) {
-          const uint32_t landed = PAIR ? sfull_bar(stage) : full_bar(stage);
-          if (!__all_sync(0xffffffffu, mbar_wait(landed, phase, abort_flag, p.wait_limit_ns))) {
-            ok = false;
-            break;
-          }
-          const uint32_t slot = sf_tmem0 + stage * Ly::kSfColsPerStage;
-          const uint8_t* sa = smem + Ly::kOffSfa + stage * Ly::kSfaBytes + 16 * lane;
-          const uint8_t* sb = smem + Ly::kOffSfb + stage * Ly::kSfbBytes + 16 * lane;
-#pragma unroll
-          for (int i = 0; i < Ly::kAtoms; ++i) {
-            const uint4 va = *reinterpret_cast<const uint4*>(sa + 512 * i);
-            tmem_st_x1(slot + 4 * i + q, q == 0 ? va.x : q == 1 ? va.y : q == 2 ? va.z : va.w);
-#pragma unroll
-            for (int h = 0; h < Ly::kHalves; ++h)
-              tmem_st_x4(slot + Ly::kSfaCols + 4 * (i * Ly::kHalves + h),
-                         *reinterpret_cast<const uint4*>(sb + 512 * (h * Ly::kAtoms + i)));
-          }
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            if (PAIR) mbar_arrive_cluster(mapa_shared(sfr_bar(stage), 0));
-            else mbar_arrive(sfr_bar(stage));
-          }
-          if (++stage == S) { stage = 0; phase ^= 1u; }
-        }
-      }
-      if (!ok && lane == 0) atomicOr(p.status, kStatusTimeout);
-     } else {
-      // ------------------------------------------------------------ scale copier
-      // Same stage sequence as the MMA issuer.  Writing a stage's tensor-memory
-      // scale slot is safe once its "full" barrier completed: the refill behind
-      // it waited for the MMAs that read the slot's previous contents.
-      if (lane == 0 && issues_mma) {
+      if constexpr (ST) {
+        // ------------------------------------------------------------ scale stores
+        // One warp per tensor-memory lane quadrant q.  The MMA reads row r's A
+        // scales from lane r, column (r / 32) % 4 of the atom's 4-column group, so
+        // the warp writes A's atoms into column q of its own 32 lanes only; every
+        // quadrant reads the scales of every B row, so B's atoms go into all four
+        // columns.  A quarter of A's tensor-memory writes of the copy path.
+        const uint32_t q = static_cast<uint32_t>(warp & 3);
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        const uint32_t sf_tmem0 = tmem_base + NA * BN;
-        const uint64_t sfa_desc0 = sdesc_sf_block(sbase + Ly::kOffSfa);
-        const uint64_t sfb_desc0 = sdesc_sf_block(sbase + Ly::kOffSfb);
+        const uint32_t sf_tmem0 = tmem_base + NA * BN + ((q * 32u) << 16);
         for (int t = unit; t < num_tiles && ok; t += num_units) {
           for (int ks = 0; ks < p.num_k_stages; ++ks) {
-            if (!mbar_wait(full_bar(stage), phase, abort_flag, p.wait_limit_ns)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t sfa_t = sf_tmem0 + stage * Ly::kSfColsPerStage;
-            const uint32_t sfb_t = sfa_t + Ly::kSfaCols;
-            const uint64_t sfa_d = sfa_desc0 + static_cast<uint64_t>((stage * Ly::kSfaBytes) >> 4);
-            const uint64_t sfb_d = sfb_desc0 + static_cast<uint64_t>((stage * Ly::kSfbBytes) >> 4);
-            // atom i of A at columns 4i; atom i of B's 128-row block h at
-            // columns 4 * (i * halves + h)
+            const uint32_t landed = PAIR ? sfull_bar(stage) : full_bar(stage);
+            if (!__all_sync(0xffffffffu, mbar_wait(landed, phase, abort_flag, p.wait_limit_ns))) {
+              ok = false;
+              break;
+            }
+            const uint32_t slot = sf_tmem0 + stage * Ly::kSfColsPerStage;
+            const uint8_t* sa = smem + Ly::kOffSfa + stage * Ly::kSfaBytes + 16 * lane;
+            const uint8_t* sb = smem + Ly::kOffSfb + stage * Ly::kSfbBytes + 16 * lane;
 #pragma unroll
             for (int i = 0; i < Ly::kAtoms; ++i) {
-              if (PAIR) tc_cp_32x128b_x4_pair(sfa_t + 4 * i, sfa_d + 32 * i);
-              else tc_cp_32x128b_x4(sfa_t + 4 * i, sfa_d + 32 * i);
+              const uint4 va = *reinterpret_cast<const uint4*>(sa + 512 * i);
+              tmem_st_x1(slot + 4 * i + q, q == 0 ? va.x : q == 1 ? va.y : q == 2 ? va.z : va.w);
 #pragma unroll
-              for (int h = 0; h < Ly::kHalves; ++h) {
-                const uint32_t dst = sfb_t + 4 * (i * Ly::kHalves + h);
-                const uint64_t src = sfb_d + 32 * (h * Ly::kAtoms + i);
-                if (PAIR) tc_cp_32x128b_x4_pair(dst, src); else tc_cp_32x128b_x4(dst, src);
-              }
+              for (int h = 0; h < Ly::kHalves; ++h)
+                tmem_st_x4(slot + Ly::kSfaCols + 4 * (i * Ly::kHalves + h),
+                           *reinterpret_cast<const uint4*>(sb + 512 * (h * Ly::kAtoms + i)));
             }
-            if (PAIR) tc_commit_pair(sfr_bar(stage), 1); else tc_commit(sfr_bar(stage));
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if (PAIR) mbar_arrive_cluster(mapa_shared(sfr_bar(stage), 0));
+              else mbar_arrive(sfr_bar(stage));
+            }
             if (++stage == S) { stage = 0; phase ^= 1u; }
           }
         }
-        if (!ok) {
-          atomicOr(p.status, kStatusTimeout);
-          // drain: wait (bounded) until this thread's copies completed
-          if (PAIR) tc_commit_pair(drain_bar2, 1); else tc_commit(drain_bar2);
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(drain_bar2, 0) && globaltimer_ns() - t0 < kDrainLimitNs) {}
+        if (!ok && lane == 0) atomicOr(p.status, kStatusTimeout);
+      } else {
+        // ------------------------------------------------------------ scale copier
+        // Same stage sequence as the MMA issuer.  Writing a stage's tensor-memory
+        // scale slot is safe once its "full" barrier completed: the refill behind
+        // it waited for the MMAs that read the slot's previous contents.
+        if (lane == 0 && issues_mma) {
+          int stage = 0;
+          uint32_t phase = 0;
+          bool ok = true;
+          const uint32_t sf_tmem0 = tmem_base + NA * BN;
+          const uint64_t sfa_desc0 = sdesc_sf_block(sbase + Ly::kOffSfa);
+          const uint64_t sfb_desc0 = sdesc_sf_block(sbase + Ly::kOffSfb);
+          for (int t = unit; t < num_tiles && ok; t += num_units) {
+            for (int ks = 0; ks < p.num_k_stages; ++ks) {
+              if (!mbar_wait(full_bar(stage), phase, abort_flag, p.wait_limit_ns)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t sfa_t = sf_tmem0 + stage * Ly::kSfColsPerStage;
+              const uint32_t sfb_t = sfa_t + Ly::kSfaCols;
+              const uint64_t sfa_d = sfa_desc0 + static_cast<uint64_t>((stage * Ly::kSfaBytes) >> 4);
+              const uint64_t sfb_d = sfb_desc0 + static_cast<uint64_t>((stage * Ly::kSfbBytes) >> 4);
+              // atom i of A at columns 4i; atom i of B's 128-row block h at
+              // columns 4 * (i * halves + h)
+#pragma unroll
+              for (int i = 0; i < Ly::kAtoms; ++i) {
+                if (PAIR) tc_cp_32x128b_x4_pair(sfa_t + 4 * i, sfa_d + 32 * i);
+                else tc_cp_32x128b_x4(sfa_t + 4 * i, sfa_d + 32 * i);
+#pragma unroll
+                for (int h = 0; h < Ly::kHalves; ++h) {
+                  const uint32_t dst = sfb_t + 4 * (i * Ly::kHalves + h);
+                  const uint64_t src = sfb_d + 32 * (h * Ly::kAtoms + i);
+                  if (PAIR) tc_cp_32x128b_x4_pair(dst, src); else tc_cp_32x128b_x4(dst, src);
+                }
+              }
+              if (PAIR) tc_commit_pair(sfr_bar(stage), 1); else tc_commit(sfr_bar(stage));
+              if (++stage == S) { stage = 0; phase ^= 1u; }
+            }
+          }
+          if (!ok) {
+            atomicOr(p.status, kStatusTimeout);
+            // drain: wait (bounded) until this thread's copies completed
+            if (PAIR) tc_commit_pair(drain_bar2, 1); else tc_commit(drain_bar2);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(drain_bar2, 0) && globaltimer_ns() - t0 < kDrainLimitNs) {}
+          }
         }
       }
-     }
     }
   } else {
     if constexpr (ST) setmaxnreg_inc<Ro::kHighRegs>();
