@@ -203,7 +203,7 @@ def oracle_sample(p, ins, budget_s: float, max_blocks: int = 64, seed: int = 0):
     code_in = {"mxfp8_e4m3": orc.IN_MXFP8_E4M3, "mxfp8_e5m2": orc.IN_MXFP8_E5M2, "nvfp4": orc.IN_NVFP4}
     code_out = {"bf16": orc.OUT_BF16, "f16": orc.OUT_F16, "f32": orc.OUT_F32, "e4m3": orc.OUT_E4M3,
                 "e5m2": orc.OUT_E5M2, "e2m1": orc.OUT_E2M1}
-    code_epi = {"gate": orc.EPI_GATE, "swiglu": orc.EPI_SWIGLU, "srelu": orc.EPI_SRELU}
+    code_epi = {"gate": orc.EPI_GATE, "swiglu": orc.EPI_SWIGLU, "srelu": orc.EPI_SRELU, "geglu": orc.EPI_GEGLU}
     off = ins["padded_offsets"]
     starts = np.concatenate([[0], off[:-1]])
     real_blocks = np.unique(np.concatenate(
@@ -247,7 +247,7 @@ def algorithmic_bytes(p) -> int:
     kb = p.k // 2 if fp4 else p.k
     off = [int(x) for x in p.padded_offsets.tolist()]
     nonempty = sum(1 for g, e in enumerate(off) if e > (off[g - 1] if g else 0))
-    n_out = p.n // 2 if p.epi == "swiglu" else p.n
+    n_out = p.n // 2 if p.epi in ("swiglu", "geglu") else p.n
     bits = {"bf16": 16, "f16": 16, "f32": 32, "e4m3": 8, "e5m2": 8, "e2m1": 4}[p.out_fmt]
     d = p.m_pad * n_out * bits // 8
     out = d * (2 if p.want_col else 1)

@@ -33,7 +33,7 @@ import torch
 
 IN_FORMATS = ("mxfp8_e4m3", "mxfp8_e5m2", "nvfp4")
 OUT_FORMATS = ("bf16", "f16", "f32", "e4m3", "e5m2", "e2m1")
-EPILOGUES = ("gate", "swiglu", "srelu")
+EPILOGUES = ("gate", "swiglu", "srelu", "geglu")
 
 _ROW_CHUNK = 4096
 
@@ -67,7 +67,7 @@ class Problem:
 
     @property
     def n_out(self) -> int:
-        return self.n // 2 if self.epi == "swiglu" else self.n
+        return self.n // 2 if self.epi in ("swiglu", "geglu") else self.n
 
     @property
     def m_real(self) -> int:

@@ -29,7 +29,7 @@ _lib = None
 F_E4M3, F_E5M2, F_E2M1, F_UE8M0 = 0, 1, 2, 3
 IN_MXFP8_E4M3, IN_MXFP8_E5M2, IN_NVFP4 = 0, 1, 2
 OUT_BF16, OUT_F16, OUT_F32, OUT_E4M3, OUT_E5M2, OUT_E2M1 = 0, 1, 2, 3, 4, 5
-EPI_GATE, EPI_SWIGLU, EPI_SRELU = 0, 1, 2
+EPI_GATE, EPI_SWIGLU, EPI_SRELU, EPI_GEGLU = 0, 1, 2, 3
 
 
 class OrcDesc(ctypes.Structure):
@@ -38,7 +38,7 @@ class OrcDesc(ctypes.Structure):
         ("num_groups", ctypes.c_int64),
         ("in_fmt", ctypes.c_int32), ("out_fmt", ctypes.c_int32), ("epi", ctypes.c_int32),
         ("gate_first", ctypes.c_int32), ("want_col", ctypes.c_int32), ("reserved", ctypes.c_int32),
-        ("tanh_clamp_s", ctypes.c_double),
+        ("tanh_clamp_s", ctypes.c_double), ("glu_limit", ctypes.c_double), ("glu_alpha", ctypes.c_double),
     ]
 
 
@@ -82,8 +82,8 @@ def lib():
         L.orc_group_of_row.restype = ctypes.c_int64
         L.orc_group_of_row.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64]
         L.orc_run.restype = ctypes.c_int
-        L.orc_run.argtypes = [ctypes.POINTER(OrcDesc)] + [ctypes.c_void_p] * 7 + [
-            ctypes.c_float, ctypes.c_void_p, ctypes.c_int64] + [ctypes.c_void_p] * 6 + [ctypes.c_int]
+        L.orc_run.argtypes = [ctypes.POINTER(OrcDesc)] + [ctypes.c_void_p] * 8 + [
+            ctypes.c_float, ctypes.c_void_p, ctypes.c_int64] + [ctypes.c_void_p] * 7 + [ctypes.c_int]
         _lib = L
     return _lib
 
@@ -138,12 +138,13 @@ def group_of_row(offsets: np.ndarray, m: int) -> int:
 
 
 def n_out(n: int, epi: int) -> int:
-    return n // 2 if epi == EPI_SWIGLU else n
+    return n // 2 if epi in (EPI_SWIGLU, EPI_GEGLU) else n
 
 
 def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded_offsets,
         alpha, prob, norm_const=1.0, tanh_clamp_s=0.0, gate_first=0, want_col=False,
-        blocks=None, threads=None, outputs=None):
+        blocks=None, threads=None, outputs=None, bias=None, glu_limit=0.0, glu_alpha=1.0,
+        want_c=False):
     """Run the oracle on the listed 32-row blocks (default: all of them).
 
     Inputs are numpy arrays in the device layouts: ``a`` (m_pad, k or k/2)
@@ -152,10 +153,13 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     (m_pad,).  Returns a dict with ``d_ref`` (fp64, rows of the listed blocks),
     ``amax`` and, for quantized outputs, full-size ``d``, ``d_col``,
     ``sfd_row``, ``sfd_col`` buffers written for the listed rows only.
+    ``bias`` (L, n) float32 is added to C; ``want_c`` adds ``c_ref`` (fp64 C of
+    the listed rows, before any clamp or activation).  ``glu_limit`` (0 = none)
+    and ``glu_alpha`` apply to SwiGLU and GeGLU.
     """
     L = lib()
     desc = OrcDesc(m_pad, n, k, num_groups, in_fmt, out_fmt, epi, int(gate_first),
-                   int(bool(want_col)), 0, float(tanh_clamp_s))
+                   int(bool(want_col)), 0, float(tanh_clamp_s), float(glu_limit), float(glu_alpha))
     nd = n_out(n, epi)
     if blocks is None:
         blocks = np.arange(m_pad // 32, dtype=np.int64)
@@ -163,6 +167,8 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     if threads is None:
         threads = os.cpu_count() or 1
     d_ref = np.zeros((blocks.size * 32, nd), dtype=np.float64)
+    c_ref = np.zeros((blocks.size * 32, n), dtype=np.float64) if want_c else None
+    bias_arr = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32).reshape(num_groups, n)
     amax = np.zeros(num_groups, dtype=np.float32)
     outs = dict(outputs or {})
     quant = out_fmt >= OUT_E4M3
@@ -183,11 +189,13 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     )
     rc = L.orc_run(ctypes.byref(desc), _ptr(arrs["a"]), _ptr(arrs["sfa"]), _ptr(arrs["b"]),
                    _ptr(arrs["sfb"]), _ptr(arrs["off"]), _ptr(arrs["alpha"]), _ptr(arrs["prob"]),
-                   float(norm_const), _ptr(blocks), blocks.size, _ptr(d_ref),
-                   _ptr(outs.get("d")), _ptr(outs.get("d_col")), _ptr(outs.get("sfd_row")),
+                   _ptr(bias_arr), float(norm_const), _ptr(blocks), blocks.size, _ptr(d_ref),
+                   _ptr(c_ref), _ptr(outs.get("d")), _ptr(outs.get("d_col")), _ptr(outs.get("sfd_row")),
                    _ptr(outs.get("sfd_col")), _ptr(amax), int(threads))
     if rc != 0:
         raise ValueError(f"oracle rejected the problem (code {rc})")
     res = {"d_ref": d_ref, "amax": amax, "blocks": blocks}
+    if want_c:
+        res["c_ref"] = c_ref
     res.update(outs)
     return res

@@ -161,7 +161,7 @@ int64_t sf_bytes(int64_t rows, int64_t kblocks, int64_t L) {
 // ---------------------------------------------------------------------------
 enum InFmt { IN_MXFP8_E4M3 = 0, IN_MXFP8_E5M2 = 1, IN_NVFP4 = 2 };
 enum OutFmt { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2, OUT_E4M3 = 3, OUT_E5M2 = 4, OUT_E2M1 = 5 };
-enum Epi { EPI_GATE = 0, EPI_SWIGLU = 1, EPI_SRELU = 2 };
+enum Epi { EPI_GATE = 0, EPI_SWIGLU = 1, EPI_SRELU = 2, EPI_GEGLU = 3 };
 
 }  // namespace
 
@@ -171,6 +171,11 @@ typedef struct {
   int64_t m_pad, n, k, num_groups;
   int32_t in_fmt, out_fmt, epi, gate_first, want_col, reserved;
   double tanh_clamp_s;   // 0 = no clamp
+  // "Grouped GEMM + GLU + Hadamard + Quant (SM100)", Equations: both GLU
+  // halves clamped to [-glu_limit, glu_limit] (0 = no clamp) and the GLU
+  // output scaled by gamma = glu_alpha (1 = none); SwiGLU and GeGLU only.
+  double glu_limit;
+  double glu_alpha;
 } orc_desc;
 
 // ---- exported helpers (pinned individually by the tests) ----
@@ -196,6 +201,9 @@ void orc_pack_sf(const uint8_t* logical, uint8_t* swz, int64_t rows, int64_t kbl
 // The activation of "Grouped GEMM + SwiGLU (SM100)" Step 2 (swish(x) = x*sigmoid(x))
 // and of "Grouped GEMM + sReLU (SM100)", Equations and Tanh soft clamp.
 double orc_sigmoid(double x) { return 1.0 / (1.0 + std::exp(-x)); }
+// "Grouped GEMM + GLU + Hadamard + Quant (SM100)", Equations: GeGLU of an up
+// value u and a gate value g is (u + 1) * g * sigmoid(1.702 * g).
+double orc_geglu(double u, double g) { return (u + 1.0) * g * orc_sigmoid(1.702 * g); }
 double orc_srelu(double c, double s) {
   double r = c > 0.0 ? c : 0.0;                 // relu
   if (s > 0.0) r = s * std::min(std::tanh(r / s), 1.0);   // soft clamp, t capped at 1
@@ -221,11 +229,14 @@ int64_t orc_group_of_row(const int32_t* off, int64_t L, int64_t m) {
 //   amax     [L]: max |D| (fp32) over the computed rows of each group
 //            (reading: amax covers all rows of the group's padded range).
 // Returns 0, or a negative value for an invalid description.
+//   c_ref    [nblocks*32, n] fp64 C (GEMM plus bias, before any clamp or
+//            activation) when not NULL
+// `bias` (L x n, bias[g*n + col]) is added to C when not NULL.
 int orc_run(const orc_desc* P, const uint8_t* A, const uint8_t* SFA, const uint8_t* B,
             const uint8_t* SFB, const int32_t* padded_offsets, const float* alpha,
-            const float* prob, float norm_const, const int64_t* blocks, int64_t nblocks,
-            double* d_ref, uint8_t* d_q, uint8_t* d_col_q, uint8_t* sfd_row,
-            uint8_t* sfd_col, float* amax, int threads);
+            const float* prob, const float* bias, float norm_const, const int64_t* blocks,
+            int64_t nblocks, double* d_ref, double* c_ref, uint8_t* d_q, uint8_t* d_col_q,
+            uint8_t* sfd_row, uint8_t* sfd_col, float* amax, int threads);
 
 }  // extern "C"
 
@@ -233,6 +244,8 @@ namespace {
 
 struct Job {
   const orc_desc* P;
+  const float* bias;
+  double* c_ref;
   const uint8_t *A, *SFA, *B, *SFB;
   const int32_t* off;
   const float *alpha, *prob;
@@ -260,7 +273,8 @@ int out_code_fmt(const orc_desc* P) {
 double q_max(const orc_desc* P) {
   return P->out_fmt == OUT_E4M3 ? 448.0 : P->out_fmt == OUT_E5M2 ? 57344.0 : 6.0;
 }
-int64_t n_out(const orc_desc* P) { return P->epi == EPI_SWIGLU ? P->n / 2 : P->n; }
+bool is_glu(const orc_desc* P) { return P->epi == EPI_SWIGLU || P->epi == EPI_GEGLU; }
+int64_t n_out(const orc_desc* P) { return is_glu(P) ? P->n / 2 : P->n; }
 
 // Element (r, k) of a K-major low-precision operand: one byte per FP8 value,
 // two FP4 values per byte with element 2i in the low nibble (reading).
@@ -322,7 +336,7 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
 
   // C columns needed for D column j; `gate` picks the gate half for SwiGLU.
   auto c_col_of = [&](int64_t j, bool gate) -> int64_t {
-    if (P->epi != EPI_SWIGLU) return j;
+    if (!is_glu(P)) return j;
     // "Grouped GEMM + SwiGLU (SM100)", Step 2: block b = j/32 pairs C columns
     // [64b, 64b+32) (input X_b) and [64b+32, 64b+64) (gate G_b).  gate_first
     // swaps the two, which is the order of "Grouped GEMM + GLU + Hadamard +
@@ -331,8 +345,8 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
     const bool second = (gate != bool(P->gate_first));
     return 64 * b + (second ? 32 : 0) + r;
   };
-  const int64_t c0 = (P->epi == EPI_SWIGLU) ? 2 * j0 : j0;
-  const int64_t c1 = (P->epi == EPI_SWIGLU) ? 2 * j1 : j1;
+  const int64_t c0 = is_glu(P) ? 2 * j0 : j0;
+  const int64_t c1 = is_glu(P) ? 2 * j1 : j1;
 
   // Group of each row ("Grouped GEMM + Quant (SM100)", Equations, Step 1).
   std::vector<int64_t> grp(32);
@@ -358,6 +372,17 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
       }
     }
   }
+  // "Grouped GEMM + GLU + Hadamard + Quant (SM100)", Equations: + bias_g[n].
+  // C (stored when asked for) is this value, before any clamp or activation.
+  for (int64_t i = 0; i < 32; ++i) {
+    const int64_t g = grp[size_t(i)];
+    if (g < 0) continue;
+    for (int64_t n = c0; n < c1; ++n) {
+      double& c = C[size_t(i * (c1 - c0) + (n - c0))];
+      if (J.bias) c += double(J.bias[g * P->n + n]);
+      if (J.c_ref) J.c_ref[size_t((bi * 32 + i) * P->n + n)] = c;
+    }
+  }
 
   // Step 2: the epilogue, in fp64.
   std::vector<double> D(size_t(32 * w), 0.0);
@@ -372,9 +397,15 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
       double d;
       if (P->epi == EPI_GATE) {
         d = p * Cv(j);                                    // D = prob * ref
-      } else if (P->epi == EPI_SWIGLU) {
-        const double x = Cv(c_col_of(j, false)), gt = Cv(c_col_of(j, true));
-        d = p * x * (gt * orc_sigmoid(gt));               // prob * X * swish(G)
+      } else if (is_glu(P)) {
+        double x = Cv(c_col_of(j, false)), gt = Cv(c_col_of(j, true));
+        if (P->glu_limit > 0.0) {                         // both halves clamped first
+          x = std::min(std::max(x, -P->glu_limit), P->glu_limit);
+          gt = std::min(std::max(gt, -P->glu_limit), P->glu_limit);
+        }
+        if (P->epi == EPI_SWIGLU) d = p * x * (gt * orc_sigmoid(gt));   // prob * X * swish(G)
+        else d = p * orc_geglu(x, gt);                                  // prob * (U+1) * G * sig(1.702 G)
+        d *= P->glu_alpha;                                              // gamma
       } else {
         d = p * orc_srelu(Cv(j), P->tanh_clamp_s);        // prob * relu(C)^2, clamped
       }
@@ -432,19 +463,19 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
 
 extern "C" int orc_run(const orc_desc* P, const uint8_t* A, const uint8_t* SFA, const uint8_t* B,
                        const uint8_t* SFB, const int32_t* padded_offsets, const float* alpha,
-                       const float* prob, float norm_const, const int64_t* blocks,
-                       int64_t nblocks, double* d_ref, uint8_t* d_q, uint8_t* d_col_q,
+                       const float* prob, const float* bias, float norm_const, const int64_t* blocks,
+                       int64_t nblocks, double* d_ref, double* c_ref, uint8_t* d_q, uint8_t* d_col_q,
                        uint8_t* sfd_row, uint8_t* sfd_col, float* amax, int threads) {
   if (!P || P->m_pad <= 0 || P->m_pad % 32 || P->n <= 0 || P->k <= 0 || P->num_groups <= 0)
     return -1;
-  if (P->epi == EPI_SWIGLU && P->n % 64) return -2;
+  if (is_glu(P) && P->n % 64) return -2;
   if (is_fp4_in(P) && P->k % 2) return -3;
   const int64_t nd = n_out(P);
   // One work item per (block, 128-column slice of D); slices are multiples of
   // the scale-factor vector so that row blocks never straddle two items.
   const int64_t slice = 128;
   Job J;
-  J.P = P; J.A = A; J.SFA = SFA; J.B = B; J.SFB = SFB; J.off = padded_offsets;
+  J.P = P; J.bias = bias; J.c_ref = c_ref; J.A = A; J.SFA = SFA; J.B = B; J.SFB = SFB; J.off = padded_offsets;
   J.alpha = alpha; J.prob = prob; J.norm = norm_const; J.blocks = blocks; J.nblocks = nblocks;
   J.d_ref = d_ref; J.d_q = d_q; J.d_col_q = d_col_q; J.sfd_row = sfd_row; J.sfd_col = sfd_col;
   J.amax.assign(size_t(P->num_groups), 0.0f);
