@@ -16,7 +16,8 @@ from . import build as _build
 
 IN_FORMATS = {"mxfp8_e4m3": 0, "mxfp8_e5m2": 1, "nvfp4": 2}
 OUT_FORMATS = {"bf16": 0, "f16": 1, "f32": 2, "e4m3": 3, "e5m2": 4, "e2m1": 5}
-EPILOGUES = {"gate": 0, "swiglu": 1, "srelu": 2}
+EPILOGUES = {"gate": 0, "swiglu": 1, "srelu": 2, "geglu": 3}
+GLU_EPILOGUES = ("swiglu", "geglu")
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
           4: "device wait timed out", 5: "padded_offsets invalid"}
 
@@ -37,13 +38,30 @@ class Desc(ctypes.Structure):
                 ("out_format", ctypes.c_int32), ("epilogue", ctypes.c_int32),
                 ("want_col", ctypes.c_int32), ("gate_first", ctypes.c_int32),
                 ("tanh_clamp_s", ctypes.c_float), ("tile_m", ctypes.c_int32),
-                ("tile_n", ctypes.c_int32), ("cluster_m", ctypes.c_int32), ("cluster_n", ctypes.c_int32)]
+                ("tile_n", ctypes.c_int32), ("cluster_m", ctypes.c_int32), ("cluster_n", ctypes.c_int32),
+                ("glu_limit", ctypes.c_float), ("glu_alpha", ctypes.c_float),
+                ("want_c", ctypes.c_int32), ("c_format", ctypes.c_int32),
+                ("want_bias", ctypes.c_int32), ("bias_format", ctypes.c_int32)]
+
+
+def make_desc(*, m_pad: int, n: int, k: int, num_groups: int, in_format: str, out_format: str,
+              epilogue: str, want_col: bool = False, gate_first: bool = False,
+              tanh_clamp_s: float = 0.0, tile=(0, 0), cluster=(0, 0), glu_limit: float = 0.0,
+              glu_alpha: float = 0.0, c_format: Optional[str] = None,
+              bias_format: Optional[str] = None) -> "Desc":
+    """A bsgg_desc.  c_format ("bf16"/"f16") asks for the pre-activation C
+    output, bias_format ("bf16"/"f16"/"f32") for a bias; None = neither."""
+    return Desc(m_pad, n, k, num_groups, IN_FORMATS[in_format], OUT_FORMATS[out_format],
+                EPILOGUES[epilogue], int(bool(want_col)), int(bool(gate_first)), float(tanh_clamp_s),
+                int(tile[0]), int(tile[1]), int(cluster[0]), int(cluster[1]), float(glu_limit),
+                float(glu_alpha), int(c_format is not None), OUT_FORMATS[c_format or "bf16"],
+                int(bias_format is not None), OUT_FORMATS[bias_format or "bf16"])
 
 
 class Args(ctypes.Structure):
     _fields_ = [(name, ctypes.c_void_p) for name in (
         "a", "sfa", "b", "sfb", "padded_offsets", "alpha", "prob", "norm_const",
-        "d", "d_col", "sfd_row", "sfd_col", "amax")]
+        "d", "d_col", "sfd_row", "sfd_col", "amax", "bias", "c")]
 
 
 _lib = None
@@ -141,16 +159,13 @@ def pack_sf(rowmajor, out=None, stream=None):
 class Plan:
     """A validated problem description (bsgg_create); run() launches it."""
 
-    def __init__(self, *, m_pad: int, n: int, k: int, num_groups: int, in_format: str,
-                 out_format: str, epilogue: str, want_col: bool = False, gate_first: bool = False,
-                 tanh_clamp_s: float = 0.0, tile=(0, 0), cluster=(0, 0)):
-        """tile = the pages' mma_tiler_mn, cluster = cluster_shape_mn; (0, 0)
-        lets the library choose."""
-        self.desc = Desc(m_pad, n, k, num_groups, IN_FORMATS[in_format], OUT_FORMATS[out_format],
-                         EPILOGUES[epilogue], int(bool(want_col)), int(bool(gate_first)),
-                         float(tanh_clamp_s), int(tile[0]), int(tile[1]), int(cluster[0]), int(cluster[1]))
-        self.in_format, self.out_format, self.epilogue = in_format, out_format, epilogue
-        self.want_col = bool(want_col)
+    def __init__(self, **kw):
+        """Keyword arguments of make_desc.  tile = the pages' mma_tiler_mn,
+        cluster = cluster_shape_mn; (0, 0) lets the library choose."""
+        self.desc = make_desc(**kw)
+        self.in_format, self.out_format, self.epilogue = kw["in_format"], kw["out_format"], kw["epilogue"]
+        self.want_col = bool(kw.get("want_col", False))
+        self.c_format = kw.get("c_format")
         h = ctypes.c_void_p()
         _check(lib().bsgg_create(ctypes.byref(self.desc), ctypes.byref(h)), "bsgg_create")
         self._h = h
@@ -162,7 +177,7 @@ class Plan:
 
     @property
     def n_out(self) -> int:
-        return self.desc.n // 2 if self.epilogue == "swiglu" else self.desc.n
+        return self.desc.n // 2 if self.epilogue in GLU_EPILOGUES else self.desc.n
 
     @property
     def out_row_bytes(self) -> int:
@@ -183,6 +198,8 @@ class Plan:
                 out["sfd_col"] = sf_bytes(self.n_out, d.m_pad, self.sf_vec, 1)
         else:
             out["amax"] = 4 * d.num_groups
+        if self.c_format is not None:
+            out["c"] = d.m_pad * d.n * 2
         return out
 
     # calls ---------------------------------------------------------------
@@ -233,17 +250,19 @@ def measure_mma_peak(in_format: str, tile_n: int = 256, mmas_per_sm: int = 40000
     return float(out.value)
 
 
-def run_noalloc(*, m_pad: int, n: int, k: int, num_groups: int, in_format: str, out_format: str,
-                epilogue: str, want_col: bool = False, gate_first: bool = False,
-                tanh_clamp_s: float = 0.0, tile=(0, 0), cluster=(0, 0), stream=None,
-                wait_status: bool = True, **tensors) -> int:
+_DESC_KEYS = ("m_pad", "n", "k", "num_groups", "in_format", "out_format", "epilogue", "want_col",
+              "gate_first", "tanh_clamp_s", "tile", "cluster", "glu_limit", "glu_alpha", "c_format",
+              "bias_format")
+
+
+def run_noalloc(*, stream=None, wait_status: bool = True, **kw) -> int:
     """bsgg_run_noalloc: one call without a plan and without any device
     allocation (for callers whose device memory is owned by someone else, or
-    who must not let cudaMalloc synchronize the device).  Returns the status
-    code (the device status when wait_status is true)."""
-    desc = Desc(m_pad, n, k, num_groups, IN_FORMATS[in_format], OUT_FORMATS[out_format],
-                EPILOGUES[epilogue], int(bool(want_col)), int(bool(gate_first)), float(tanh_clamp_s),
-                int(tile[0]), int(tile[1]), int(cluster[0]), int(cluster[1]))
+    who must not let cudaMalloc synchronize the device).  Keyword arguments:
+    those of make_desc plus the tensors by their bsgg_args names.  Returns the
+    status code (the device status when wait_status is true)."""
+    desc = make_desc(**{k_: v for k_, v in kw.items() if k_ in _DESC_KEYS})
+    tensors = {k_: v for k_, v in kw.items() if k_ not in _DESC_KEYS}
     args = Args(*[_ptr(tensors.get(name)) for name, _ in Args._fields_])
     return int(lib().bsgg_run_noalloc(ctypes.byref(desc), ctypes.byref(args), _stream(stream),
                                       int(bool(wait_status))))

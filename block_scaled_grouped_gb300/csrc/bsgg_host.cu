@@ -99,7 +99,8 @@ bsgg_status validate(const bsgg_desc* d) {
     return BSGG_ERR_INVALID_ARG;
   if (d->in_format < BSGG_IN_MXFP8_E4M3 || d->in_format > BSGG_IN_NVFP4) return BSGG_ERR_INVALID_ARG;
   if (d->out_format < BSGG_OUT_BF16 || d->out_format > BSGG_OUT_E2M1) return BSGG_ERR_INVALID_ARG;
-  if (d->epilogue < BSGG_EPI_GATE || d->epilogue > BSGG_EPI_SRELU) return BSGG_ERR_INVALID_ARG;
+  if (d->epilogue < BSGG_EPI_GATE || d->epilogue > BSGG_EPI_GEGLU) return BSGG_ERR_INVALID_ARG;
+  const bool glu = d->epilogue == BSGG_EPI_SWIGLU || d->epilogue == BSGG_EPI_GEGLU;
   if (d->gate_first != 0 && d->gate_first != 1) return BSGG_ERR_INVALID_ARG;
   if (d->want_col != 0 && d->want_col != 1) return BSGG_ERR_INVALID_ARG;
   // K-major rows must be 16-byte aligned ("Support Surface and Constraints",
@@ -108,9 +109,23 @@ bsgg_status validate(const bsgg_desc* d) {
   if (d->k % (fp4 ? 32 : 16) != 0) return BSGG_ERR_INVALID_ARG;
   // SwiGLU pairs 32-column blocks: N % 64 ("Grouped GEMM + SwiGLU (SM100)",
   // Shapes and Divisibility).  Outputs are written in 32-column chunks.
-  if (d->epilogue == BSGG_EPI_SWIGLU ? (d->n % 64 != 0) : (d->n % 32 != 0)) return BSGG_ERR_INVALID_ARG;
+  if (glu ? (d->n % 64 != 0) : (d->n % 32 != 0)) return BSGG_ERR_INVALID_ARG;
   if (!(std::isfinite(d->tanh_clamp_s) && d->tanh_clamp_s >= 0.0f)) return BSGG_ERR_INVALID_ARG;
   if (d->tanh_clamp_s > 0.0f && d->epilogue != BSGG_EPI_SRELU) return BSGG_ERR_INVALID_ARG;
+  // glu_limit and glu_alpha belong to the GLUs ("Grouped GEMM + GLU + Hadamard +
+  // Quant (SM100)", Configuration); 0 leaves either unset
+  if (!(std::isfinite(d->glu_limit) && d->glu_limit >= 0.0f) || !std::isfinite(d->glu_alpha))
+    return BSGG_ERR_INVALID_ARG;
+  if (!glu && (d->glu_limit != 0.0f || (d->glu_alpha != 0.0f && d->glu_alpha != 1.0f)))
+    return BSGG_ERR_INVALID_ARG;
+  // C is stored as float16 or bfloat16; the bias is float16, bfloat16 or float32
+  // ("Grouped GEMM + GLU + Hadamard + Quant (SM100)", Input/output tensors)
+  if (d->want_c != 0 && d->want_c != 1) return BSGG_ERR_INVALID_ARG;
+  if (d->want_c && d->c_format != BSGG_OUT_BF16 && d->c_format != BSGG_OUT_F16) return BSGG_ERR_INVALID_ARG;
+  if (d->want_bias != 0 && d->want_bias != 1) return BSGG_ERR_INVALID_ARG;
+  if (d->want_bias && d->bias_format != BSGG_OUT_BF16 && d->bias_format != BSGG_OUT_F16 &&
+      d->bias_format != BSGG_OUT_F32)
+    return BSGG_ERR_INVALID_ARG;
   if (d->want_col && !is_quant(d->out_format)) return BSGG_ERR_INVALID_ARG;
   // NVFP4 inputs: the pages allow 16/32-bit float outputs; FP4 output is this
   // build's reading for the NVFP4 sReLU workload.  FP8 outputs from FP4 inputs
@@ -199,13 +214,14 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
   P->pair = (tm == 256);
   P->mc = (tm == 128 && cm == 2);
   P->bn = P->pair ? 256 : tn;
-  P->epi = desc->epilogue;
+  // GeGLU runs in the SwiGLU instances (Params::glu_kind selects the activation)
+  P->epi = desc->epilogue == BSGG_EPI_GEGLU ? bsgg::EPI_SWIGLU : desc->epilogue;
   P->outc = desc->out_format == BSGG_OUT_E2M1 ? bsgg::OUTC_FP4
             : is_quant(desc->out_format)      ? bsgg::OUTC_FP8
                                               : bsgg::OUTC_FLOAT;
   P->sf_vec = desc->in_format == BSGG_IN_NVFP4 ? 16 : 32;
   P->kbytes = desc->in_format == BSGG_IN_NVFP4 ? desc->k / 2 : desc->k;
-  P->n_out = desc->epilogue == BSGG_EPI_SWIGLU ? desc->n / 2 : desc->n;
+  P->n_out = (desc->epilogue == BSGG_EPI_SWIGLU || desc->epilogue == BSGG_EPI_GEGLU) ? desc->n / 2 : desc->n;
   P->out_row_bytes = P->n_out * out_elem_bits(desc->out_format) / 8;
   if (P->pair || P->mc) {
     int resident = bsgg::cluster_resident_ctas(desc->in_format == BSGG_IN_NVFP4, P->mc);
@@ -230,6 +246,8 @@ bsgg_status check_args(const bsgg_plan* P, const bsgg_args* a) {
   } else if (d.out_format != BSGG_OUT_F32 && !a->amax) {
     return BSGG_ERR_INVALID_ARG;   // amax required for bf16/f16 D
   }
+  if (d.want_bias && (!a->bias || !aligned16(a->bias))) return BSGG_ERR_INVALID_ARG;
+  if (d.want_c && (!a->c || !aligned16(a->c))) return BSGG_ERR_INVALID_ARG;
   return BSGG_OK;
 }
 
@@ -366,6 +384,13 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   const double qmax = d.out_format == BSGG_OUT_E4M3 ? 448.0 : d.out_format == BSGG_OUT_E5M2 ? 57344.0 : 6.0;
   p.rcp_qmax = static_cast<float>(1.0 / qmax);
   p.idesc = make_idesc(d.in_format, P->bn, P->pair);
+  p.bias = d.want_bias ? a->bias : nullptr;
+  p.c_out = d.want_c ? a->c : nullptr;
+  p.bias_kind = d.bias_format;
+  p.c_kind = d.c_format;
+  p.glu_kind = d.epilogue == BSGG_EPI_GEGLU ? 1 : 0;
+  p.glu_limit = d.glu_limit;
+  p.glu_gamma = d.glu_alpha == 0.0f ? 1.0f : d.glu_alpha;
   p.force_timeout = P->force_timeout ? 1u : 0u;
   p.wait_limit_ns = P->force_timeout ? kTestWaitLimitNs : bsgg::kWaitLimitNs;
 
@@ -442,14 +467,17 @@ bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* 
             h2d(host->padded_offsets, dev->padded_offsets, sizeof(int32_t) * L) &&
             h2d(host->alpha, dev->alpha, sizeof(float) * L) &&
             h2d(host->prob, dev->prob, sizeof(float) * d.m_pad) &&
-            h2d(host->norm_const, dev->norm_const, sizeof(float));
+            h2d(host->norm_const, dev->norm_const, sizeof(float)) &&
+            h2d(d.want_bias ? host->bias : nullptr, dev->bias,
+                uint64_t(L) * d.n * (d.bias_format == BSGG_OUT_F32 ? 4 : 2));
   if (!ok) return BSGG_ERR_CUDA;
   bsgg_status st = bsgg_run(P, dev, stream);
   if (st != BSGG_OK) return st;
   ok = d2h(host->d, dev->d, sz_d) && d2h(host->d_col, dev->d_col, d.want_col ? sz_d : 0) &&
        d2h(host->sfd_row, dev->sfd_row, sz_sfd_row) &&
        d2h(host->sfd_col, dev->sfd_col, d.want_col ? sz_sfd_col : 0) &&
-       d2h(host->amax, dev->amax, sizeof(float) * L);
+       d2h(host->amax, dev->amax, sizeof(float) * L) &&
+       d2h(d.want_c ? host->c : nullptr, dev->c, uint64_t(d.m_pad) * d.n * 2);
   if (!ok) return BSGG_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return BSGG_ERR_CUDA;
   if (h2d_bytes) *h2d_bytes = in_bytes;

@@ -54,6 +54,7 @@
 
 namespace bsgg {
 
+// Epilogue instances; EPI_SWIGLU also computes GeGLU (Params::glu_kind).
 enum : int { EPI_GATE = 0, EPI_SWIGLU = 1, EPI_SRELU = 2 };
 // Output class (template) and exact output kind (runtime) of D.
 enum : int { OUTC_FLOAT = 0, OUTC_FP8 = 1, OUTC_FP4 = 2 };
@@ -116,6 +117,15 @@ struct Params {
   uint32_t force_timeout;   // test of the failure path: the MMA thread first waits on a
                             // barrier nothing completes, so every role gives up and returns
   uint64_t wait_limit_ns;   // bound of every barrier wait (kWaitLimitNs; shorter in that test)
+  // "Grouped GEMM + GLU + Hadamard + Quant (SM100)", Equations: C = alpha_g * acc +
+  // bias_g[n], optionally stored before any clamp or activation; GLU clamp and scale
+  const void* bias;         // (L, N), N contiguous, or null
+  void* c_out;              // (m_pad, N) N-major, or null
+  int32_t bias_kind;        // OK_BF16, OK_F16 or OK_F32
+  int32_t c_kind;           // OK_BF16 or OK_F16
+  int32_t glu_kind;         // EPI_SWIGLU instances: 0 = SwiGLU, 1 = GeGLU
+  float glu_limit;          // both GLU halves clamped to [-glu_limit, glu_limit]; 0 = none
+  float glu_gamma;          // GLU output scale (1 = none)
 };
 
 template <bool FP4, int BN, bool PAIR>
@@ -286,6 +296,61 @@ __device__ __forceinline__ void st_v4(void* ptr, uint32_t a, uint32_t b, uint32_
                : "memory");
 }
 
+__device__ __forceinline__ float as_f32(float x) { return x; }
+__device__ __forceinline__ float as_f32(uint32_t x) { return __uint_as_float(x); }
+
+// 32 values of one row (floats, or fp32 bit patterns) stored as bf16 or f16
+// at `dst` (64 bytes, 16-byte aligned).
+template <typename T>
+__device__ __forceinline__ void store_h32(void* dst, const T* v, int kind) {
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    if (kind == OK_BF16) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(as_f32(v[2 * i]), as_f32(v[2 * i + 1]));
+      w[i] = *reinterpret_cast<uint32_t*>(&h);
+    } else {
+      __half2 h = __floats2half2_rn(as_f32(v[2 * i]), as_f32(v[2 * i + 1]));
+      w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+  }
+  uint8_t* d = static_cast<uint8_t*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) st_v4(d + 16 * i, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+// Adds the 32 bias values at `src` (bf16, f16 or f32; 16-byte aligned) to 32
+// fp32 bit patterns in place.  Every lane of the warp reads the same addresses.
+__device__ __forceinline__ void add_bias32(uint32_t* v, const void* src, int kind) {
+  auto add = [&](int i, float b) { v[i] = __float_as_uint(__uint_as_float(v[i]) + b); };
+  if (kind == OK_F32) {
+    const float4* b = static_cast<const float4*>(src);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 x = __ldg(b + i);
+      add(4 * i, x.x); add(4 * i + 1, x.y); add(4 * i + 2, x.z); add(4 * i + 3, x.w);
+    }
+  } else {
+    const uint4* b = static_cast<const uint4*>(src);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 x = __ldg(b + i);
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (kind == OK_BF16) {
+          add(8 * i + 2 * j, __uint_as_float(w[j] << 16));
+          add(8 * i + 2 * j + 1, __uint_as_float(w[j] & 0xFFFF0000u));
+        } else {
+          const __half2 h = *reinterpret_cast<const __half2*>(&w[j]);
+          add(8 * i + 2 * j, __low2float(h));
+          add(8 * i + 2 * j + 1, __high2float(h));
+        }
+      }
+    }
+  }
+}
+
 // 32 values of one row -> quantized codes stored at `dst` (32 bytes for FP8,
 // 16 bytes for FP4), each value multiplied by its block's scale first.
 template <int OUTC>
@@ -323,8 +388,9 @@ __device__ __forceinline__ void store_q32(void* dst, const float (&v)[32], const
   }
 }
 
-// Step 2 and Step 3 for one 32-column chunk of one row: xs holds the
-// accumulator values (the input half for SwiGLU), gs the gate half.
+// Step 2 and Step 3 for one 32-column chunk of one row: C = al * xs (the
+// input half for the GLUs; fp32 bits), al * gs the gate half.  al is alpha_g,
+// or 1 where alpha and the bias were already applied in place.
 template <bool FP4, int EPI, int OUTC>
 __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* xs, const uint32_t* gs, int row,
                                                int col0, float al, float pr, float norm, int lane, int kblk_col,
@@ -340,9 +406,21 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* 
       if (p.tanh_s > 0.0f) r = p.tanh_s * fminf(tanh_approx(r * p.tanh_rcp_s), 1.0f);
       v[i] = pr * (r * r);
     } else {
-      const float gt = al * __uint_as_float(gs[i]);
-      const float sig = __fdividef(1.0f, 1.0f + __expf(-gt));
-      v[i] = pr * c * (gt * sig);
+      // SwiGLU: X * G * sigmoid(G); GeGLU: (X + 1) * G * sigmoid(1.702 G); both
+      // halves first clamped to [-glu_limit, glu_limit] when a limit is set
+      float x = c, gt = al * __uint_as_float(gs[i]);
+      if (p.glu_limit > 0.0f) {
+        x = fminf(fmaxf(x, -p.glu_limit), p.glu_limit);
+        gt = fminf(fmaxf(gt, -p.glu_limit), p.glu_limit);
+      }
+      if (p.glu_kind) {
+        const float sig = __fdividef(1.0f, 1.0f + __expf(-1.702f * gt));
+        v[i] = pr * (x + 1.0f) * (gt * sig);
+      } else {
+        const float sig = __fdividef(1.0f, 1.0f + __expf(-gt));
+        v[i] = pr * x * (gt * sig);
+      }
+      if (p.glu_gamma != 1.0f) v[i] *= p.glu_gamma;
     }
   }
   if (OUTC == OUTC_FLOAT) {
@@ -355,20 +433,7 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* 
         st_v4(dst + 4 * i, __float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
               __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
     } else {
-      uint32_t w[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if (p.out_kind == OK_BF16) {
-          __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-          w[i] = *reinterpret_cast<uint32_t*>(&h);
-        } else {
-          __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
-          w[i] = *reinterpret_cast<uint32_t*>(&h);
-        }
-      }
-      uint16_t* dst = static_cast<uint16_t*>(p.d) + static_cast<int64_t>(row) * p.n_out + col0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) st_v4(dst + 8 * i, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      store_h32(static_cast<uint16_t*>(p.d) + static_cast<int64_t>(row) * p.n_out + col0, &v[0], p.out_kind);
     }
   } else {
     // ---- row blocks (v = 32 for UE8M0 scales, 16 for E4M3 scales)
@@ -436,7 +501,9 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* 
   }
 }
 
-template <bool FP4, int BN, int CM, int EPI, int OUTC>
+// XC: the launch adds a bias to C or stores C (a separate instance, so that the
+// register budget of the plain epilogue is untouched).
+template <bool FP4, int BN, int CM, int EPI, int OUTC, bool XC>
 __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
     bsgg_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -846,6 +913,31 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
       const float pr = p.prob[row];
       const float al = p.alpha[g];
       const int kblk_col = mt * 4 + q;                // this warp's 32-row block
+      // With a bias or a C output: C = alpha_g * acc + bias_g[n] in place (then
+      // al = 1), stored when asked for ("Grouped GEMM + GLU + Hadamard + Quant
+      // (SM100)", Equations)
+      float al_epi = al;
+      if (XC) {
+        const int ccol0 = nt * BN + e * kWarpCols;    // first C column of this warp's half
+#pragma unroll
+        for (int c = 0; c < kWarpCols / 32; ++c) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[32 * c + i] = __float_as_uint(al * __uint_as_float(r[32 * c + i]));
+          const int col0 = ccol0 + 32 * c;
+          if (col0 < p.n) {
+            if (p.bias != nullptr) {
+              const int esz = p.bias_kind == OK_F32 ? 4 : 2;
+              add_bias32(&r[32 * c],
+                         static_cast<const uint8_t*>(p.bias) + (static_cast<int64_t>(g) * p.n + col0) * esz,
+                         p.bias_kind);
+            }
+            if (p.c_out != nullptr)
+              store_h32(static_cast<uint16_t*>(p.c_out) + static_cast<int64_t>(row) * p.n + col0, &r[32 * c],
+                        p.c_kind);
+          }
+        }
+        al_epi = 1.0f;
+      }
       float amax_local = 0.0f;
       if (EPI == EPI_SWIGLU) {
         const bool gf = p.gate_first != 0;
@@ -859,15 +951,15 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
             xs[i] = gf ? r[64 * j + 32 + i] : r[64 * j + i];
             gs[i] = gf ? r[64 * j + i] : r[64 * j + 32 + i];
           }
-          epilogue_chunk<FP4, EPI, OUTC>(p, xs, gs, row, col0, al, pr, norm, lane, kblk_col, amax_local);
+          epilogue_chunk<FP4, EPI, OUTC>(p, xs, gs, row, col0, al_epi, pr, norm, lane, kblk_col, amax_local);
         }
       } else {
 #pragma unroll
         for (int c = 0; c < kWarpCols / 32; ++c) {
           const int col0 = nt * BN + e * kWarpCols + 32 * c;
           if (col0 >= p.n_out) continue;
-          epilogue_chunk<FP4, EPI, OUTC>(p, &r[32 * c], &r[32 * c], row, col0, al, pr, norm, lane, kblk_col,
-                                         amax_local);
+          epilogue_chunk<FP4, EPI, OUTC>(p, &r[32 * c], &r[32 * c], row, col0, al_epi, pr, norm, lane,
+                                         kblk_col, amax_local);
         }
       }
       if (OUTC == OUTC_FLOAT && p.amax != nullptr) {

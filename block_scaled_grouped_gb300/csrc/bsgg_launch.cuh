@@ -7,9 +7,9 @@
 
 namespace bsgg {
 
-template <bool FP4, int BN, int CM, int EPI, int OUTC>
+template <bool FP4, int BN, int CM, int EPI, int OUTC, bool XC>
 cudaError_t launch_one(const Launch& L) {
-  auto kern = bsgg_kernel<FP4, BN, CM, EPI, OUTC>;
+  auto kern = bsgg_kernel<FP4, BN, CM, EPI, OUTC, XC>;
   constexpr bool kCluster = CM != CM_SINGLE;
   constexpr bool kStores = scale_stores<FP4, CM>();
   using Ro = Roles<kStores>;
@@ -52,22 +52,29 @@ cudaError_t launch_one(const Launch& L) {
   return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmSFA, L.tmSFB, L.p);
 }
 
-template <bool FP4, int BN, int CM, int EPI>
+template <bool FP4, int BN, int CM, int EPI, bool XC>
 cudaError_t launch_outc(const Launch& L) {
   switch (L.outc) {
-    case OUTC_FLOAT: return launch_one<FP4, BN, CM, EPI, OUTC_FLOAT>(L);
-    case OUTC_FP8: return launch_one<FP4, BN, CM, EPI, OUTC_FP8>(L);
-    case OUTC_FP4: return launch_one<FP4, BN, CM, EPI, OUTC_FP4>(L);
+    case OUTC_FLOAT: return launch_one<FP4, BN, CM, EPI, OUTC_FLOAT, XC>(L);
+    case OUTC_FP8: return launch_one<FP4, BN, CM, EPI, OUTC_FP8, XC>(L);
+    case OUTC_FP4: return launch_one<FP4, BN, CM, EPI, OUTC_FP4, XC>(L);
   }
   return cudaErrorInvalidValue;
+}
+
+// with a bias or a stored C: the XC instances
+template <bool FP4, int BN, int CM, int EPI>
+cudaError_t launch_xc(const Launch& L) {
+  if (L.p.bias != nullptr || L.p.c_out != nullptr) return launch_outc<FP4, BN, CM, EPI, true>(L);
+  return launch_outc<FP4, BN, CM, EPI, false>(L);
 }
 
 template <bool FP4, int BN, int CM>
 cudaError_t launch_shape(const Launch& L) {
   switch (L.epi) {
-    case EPI_GATE: return launch_outc<FP4, BN, CM, EPI_GATE>(L);
-    case EPI_SWIGLU: return launch_outc<FP4, BN, CM, EPI_SWIGLU>(L);
-    case EPI_SRELU: return launch_outc<FP4, BN, CM, EPI_SRELU>(L);
+    case EPI_GATE: return launch_xc<FP4, BN, CM, EPI_GATE>(L);
+    case EPI_SWIGLU: return launch_xc<FP4, BN, CM, EPI_SWIGLU>(L);
+    case EPI_SRELU: return launch_xc<FP4, BN, CM, EPI_SRELU>(L);
   }
   return cudaErrorInvalidValue;
 }
@@ -75,7 +82,7 @@ cudaError_t launch_shape(const Launch& L) {
 // Clusters of two of this kernel that fit on the device at once, x 2.
 template <bool FP4, int CM>
 int cluster_resident_ctas_impl() {
-  auto kern = bsgg_kernel<FP4, 256, CM, EPI_GATE, OUTC_FLOAT>;
+  auto kern = bsgg_kernel<FP4, 256, CM, EPI_GATE, OUTC_FLOAT, false>;
   const int smem = Layout<FP4, 256, CM == CM_PAIR>::kSmemBytes;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};

@@ -7,8 +7,14 @@
  *
  *   for every expert group g and every row m in [padded_offsets[g-1], padded_offsets[g]):
  *     C[m, n] = alpha[g] * sum_k dequant(A[m, k], SFA) * dequant(B[n, k, g], SFB)
+ *             (+ bias_g[n] when a bias is given; C itself can be stored, before any
+ *              clamp or activation: "Grouped GEMM + GLU + Hadamard + Quant (SM100)",
+ *              Equations)
  *     D[m, j] = prob[m] * C[m, j]                                   (GATE)
- *             = prob[m] * X_b * swish(G_b)  over paired 32-col blocks (SWIGLU, N/2 outputs)
+ *             = gamma * prob[m] * X_b * swish(G_b)  over paired 32-col blocks (SWIGLU,
+ *               N/2 outputs)
+ *             = gamma * prob[m] * (X_b + 1) * G_b * sigmoid(1.702 G_b)  (GEGLU, N/2 outputs)
+ *               with X_b, G_b first clamped to [-glu_limit, glu_limit] when a limit is set
  *             = prob[m] * relu(C)^2, or (s * min(tanh(relu(C)/s), 1))^2  (SRELU)
  *   and, for FP8/FP4 outputs, per block of v values of D along a row (SFD_row)
  *   and along a column (SFD_col, blocks of v rows):
@@ -32,8 +38,10 @@
  *      SFB      swizzled SF(N, K) per expert   (bsgg_sf_bytes(N, K, v, L) bytes)
  *      padded_offsets int32 (L), alpha float (L), prob float (m_pad),
  *      norm_const float (1)
- *      D, D_col (m_pad, N_out)  N-major; N_out = N/2 for SWIGLU, else N;
+ *      D, D_col (m_pad, N_out)  N-major; N_out = N/2 for SWIGLU/GEGLU, else N;
  *                               bf16/f16/f32, or 1-byte FP8 codes, or packed FP4
+ *      C        (m_pad, N)      N-major, bf16/f16 (optional pre-activation output)
+ *      bias     (L, N)          N contiguous, bf16/f16/f32 (optional)
  *      SFD_row  swizzled SF(m_pad, N_out); SFD_col swizzled SF(N_out, m_pad)
  *      amax     float (L)
  *    where SF(rows, cols) is the pages' (32, 4, ceil(rows/128), 4,
@@ -84,21 +92,25 @@ typedef enum {
   BSGG_OUT_E4M3 = 3, BSGG_OUT_E5M2 = 4, BSGG_OUT_E2M1 = 5
 } bsgg_out_format;
 
-typedef enum { BSGG_EPI_GATE = 0, BSGG_EPI_SWIGLU = 1, BSGG_EPI_SRELU = 2 } bsgg_epilogue;
+/* Epilogues: gating ("Grouped GEMM + Quant (SM100)", Step 2), SwiGLU ("Grouped GEMM +
+ * SwiGLU (SM100)", Step 2), squared ReLU with optional tanh soft clamp ("Grouped GEMM +
+ * sReLU (SM100)"), GeGLU ("Grouped GEMM + GLU + Hadamard + Quant (SM100)", Equations). */
+typedef enum { BSGG_EPI_GATE = 0, BSGG_EPI_SWIGLU = 1, BSGG_EPI_SRELU = 2, BSGG_EPI_GEGLU = 3 } bsgg_epilogue;
 
 /* Problem description, fixed at plan creation (the pages' constructor +
  * check_support + compile, "Grouped GEMM + Quant (SM100)", Class API). */
 typedef struct {
   int64_t m_pad;          /* rows of A/D/prob = padded_offsets[L-1]; multiple of 128 */
-  int64_t n;              /* GEMM N (rows of each expert's B); multiple of 32 (64 for SWIGLU) */
+  int64_t n;              /* GEMM N (rows of each expert's B); multiple of 32 (64 for SWIGLU
+                             and GEGLU) */
   int64_t k;              /* reduction length in elements; multiple of 16 (FP8) / 32 (FP4) */
   int32_t num_groups;     /* L, 1..1024 */
   int32_t in_format;      /* bsgg_in_format */
   int32_t out_format;     /* bsgg_out_format */
   int32_t epilogue;       /* bsgg_epilogue */
   int32_t want_col;       /* 1: also write D_col and SFD_col (quantized outputs only) */
-  int32_t gate_first;     /* SWIGLU block order: 0 = [X_b | G_b] ("Grouped GEMM + SwiGLU
-                             (SM100)", Step 2), 1 = [G_b | U_b] ("Grouped GEMM + GLU +
+  int32_t gate_first;     /* SWIGLU/GEGLU block order: 0 = [X_b | G_b] ("Grouped GEMM +
+                             SwiGLU (SM100)", Step 2), 1 = [G_b | U_b] ("Grouped GEMM + GLU +
                              Hadamard + Quant (SM100)", Equations) */
   float tanh_clamp_s;     /* SRELU soft clamp s > 0, or 0 for none */
   int32_t tile_m;         /* rows per MMA tile: 128 (one CTA) or 256 (a pair of CTAs with
@@ -115,12 +127,24 @@ typedef struct {
      value returns BSGG_ERR_INVALID_ARG. */
   int32_t cluster_m;
   int32_t cluster_n;
+  /* Forward epilogue options of "Grouped GEMM + GLU + Hadamard + Quant (SM100)"
+     (Equations; Configuration).  All zero = none of them. */
+  float glu_limit;        /* SWIGLU/GEGLU: both halves clamped to [-glu_limit, glu_limit]
+                             before the activation; 0 = no clamp; must be finite, >= 0 */
+  float glu_alpha;        /* SWIGLU/GEGLU: output scale gamma; 0 (unset) or 1 = none; finite */
+  int32_t want_c;         /* 1: also store C = alpha_g * acc (+ bias), before any clamp or
+                             activation, (m_pad, N) N-major, in c_format */
+  int32_t c_format;       /* BSGG_OUT_BF16 or BSGG_OUT_F16 (when want_c) */
+  int32_t want_bias;      /* 1: add bias_g[n] to C; bias is (L, N), N contiguous per expert
+                             (the pages' (N, L) tensor with stride (1, N)) */
+  int32_t bias_format;    /* BSGG_OUT_BF16, BSGG_OUT_F16 or BSGG_OUT_F32 (when want_bias) */
 } bsgg_desc;
 
 /* Tensors of one call.  Unused outputs may be NULL: d_col/sfd_col unless
  * want_col; sfd_row/sfd_col/norm_const for 16/32-bit outputs; amax for
- * quantized outputs.  amax is required for BF16/F16 outputs and optional for
- * F32 ("Grouped GEMM + Quant (SM100)", Scale Factor Output Requirements). */
+ * quantized outputs; bias unless want_bias; c unless want_c.  amax is
+ * required for BF16/F16 outputs and optional for F32 ("Grouped GEMM + Quant
+ * (SM100)", Scale Factor Output Requirements). */
 typedef struct {
   const void* a;
   const void* sfa;
@@ -135,6 +159,8 @@ typedef struct {
   void* sfd_row;
   void* sfd_col;
   float* amax;               /* zeroed by bsgg_run on the stream before the kernel */
+  const void* bias;          /* (L, N) in bias_format; required iff want_bias */
+  void* c;                   /* (m_pad, N) in c_format; required iff want_c */
 } bsgg_args;
 
 typedef struct bsgg_plan bsgg_plan;

@@ -50,16 +50,27 @@ def test_sf_helpers_match_the_oracle(lib):
 
 
 def _create(**over):
+    """bsgg_create's status for the default description with `over` applied;
+    a plan it makes is destroyed at once."""
     d = dict(m_pad=384, n=256, k=256, num_groups=2, in_format="mxfp8_e4m3", out_format="bf16",
              epilogue="gate")
+    raw = {k_: over.pop(k_) for k_ in ("c_format_code", "bias_format_code", "want_c_raw") if k_ in over}
     d.update(over)
-    desc = bsgg.Desc(d["m_pad"], d["n"], d["k"], d["num_groups"], bsgg.IN_FORMATS[d["in_format"]],
-                     bsgg.OUT_FORMATS[d["out_format"]], bsgg.EPILOGUES[d["epilogue"]],
-                     int(d.get("want_col", 0)), int(d.get("gate_first", 0)),
-                     float(d.get("tanh_clamp_s", 0.0)), int(d.get("tile_m", 0)), int(d.get("tile_n", 0)),
-                     int(d.get("cluster_m", 0)), int(d.get("cluster_n", 0)))
+    tile = (d.pop("tile_m", 0), d.pop("tile_n", 0))
+    cluster = (d.pop("cluster_m", 0), d.pop("cluster_n", 0))
+    desc = bsgg.make_desc(tile=tile, cluster=cluster, **d)
+    # raw enum values the Python names cannot express
+    if "c_format_code" in raw:
+        desc.want_c, desc.c_format = 1, raw["c_format_code"]
+    if "bias_format_code" in raw:
+        desc.want_bias, desc.bias_format = 1, raw["bias_format_code"]
+    if "want_c_raw" in raw:
+        desc.want_c = raw["want_c_raw"]
     h = ctypes.c_void_p()
-    return bsgg.lib().bsgg_create(ctypes.byref(desc), ctypes.byref(h))
+    code = bsgg.lib().bsgg_create(ctypes.byref(desc), ctypes.byref(h))
+    if h.value:
+        bsgg.lib().bsgg_destroy(h)
+    return code
 
 
 @pytest.mark.parametrize("over,code", [
@@ -80,9 +91,30 @@ def _create(**over):
     (dict(cluster_m=4, cluster_n=1), 2), (dict(cluster_m=1, cluster_n=2), 2),   # valid, not built
     (dict(tile_m=128, tile_n=128, cluster_m=2, cluster_n=1), 2),
     (dict(in_format="nvfp4", out_format="e4m3"), 2),   # not on the pages
+    (dict(n=96, epilogue="geglu"), 1),          # GeGLU pairs 32-column blocks too
+    (dict(glu_limit=-1.0, epilogue="swiglu"), 1),
+    (dict(glu_limit=float("inf"), epilogue="geglu"), 1),
+    (dict(glu_alpha=float("nan"), epilogue="swiglu"), 1),
+    (dict(glu_limit=7.0, epilogue="gate"), 1),  # GLU options belong to the GLUs
+    (dict(glu_alpha=2.0, epilogue="srelu"), 1),
+    (dict(c_format="f32"), 1), (dict(c_format_code=3), 1),    # C is bf16 or f16
+    (dict(bias_format="e4m3"), 1), (dict(bias_format_code=9), 1),
+    (dict(want_c_raw=2), 1),
 ])
 def test_create_rejects(lib, over, code):
     assert _create(**over) == code
+
+
+@pytest.mark.parametrize("over", [
+    dict(epilogue="geglu", n=128, glu_limit=7.0, glu_alpha=1.5),
+    dict(epilogue="swiglu", glu_alpha=1.0, c_format="bf16", bias_format="f32"),
+    dict(epilogue="srelu", glu_alpha=0.0, c_format="f16", bias_format="bf16"),
+    dict(epilogue="gate", bias_format="f16"),
+])
+def test_create_accepts_epilogue_options(lib, over):
+    # validation passes: 0 with a GPU, else the device query that follows
+    # validation fails with BSGG_ERR_CUDA
+    assert _create(**over) in (0, 3)
 
 
 def test_null_arguments(lib):
