@@ -31,6 +31,7 @@ struct bsgg_plan {
   int64_t out_row_bytes;
   uint32_t* status;        // device word: kStatus* bits
   bool force_timeout;      // bsgg_debug_force_timeout
+  CUtensorMap* maps;       // discrete weight mode: {B_g, SFB_g} per expert, then the bad-pointer flag
 };
 
 namespace {
@@ -126,6 +127,7 @@ bsgg_status validate(const bsgg_desc* d) {
   if (d->want_bias && d->bias_format != BSGG_OUT_BF16 && d->bias_format != BSGG_OUT_F16 &&
       d->bias_format != BSGG_OUT_F32)
     return BSGG_ERR_INVALID_ARG;
+  if (d->discrete_b != 0 && d->discrete_b != 1) return BSGG_ERR_INVALID_ARG;
   if (d->want_col && !is_quant(d->out_format)) return BSGG_ERR_INVALID_ARG;
   // NVFP4 inputs: the pages allow 16/32-bit float outputs; FP4 output is this
   // build's reading for the NVFP4 sReLU workload.  FP8 outputs from FP4 inputs
@@ -175,11 +177,19 @@ bsgg_status encode_maps(const bsgg_plan* P, const bsgg_args* a, bsgg::Launch* L)
     cuuint32_t box[2] = {bsgg::kBKBytes, cuuint32_t(P->mc ? bsgg::kBM / 2 : bsgg::kBM)};
     if ((st = encode_one(&L->tmA, a->a, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) != BSGG_OK) return st;
   }
+  // discrete weight mode: B and SFB maps of one expert (one slice) whose global
+  // address, a placeholder here (the plan's own workspace), is replaced per
+  // expert on the device
+  const bool disc = d.discrete_b != 0;
+  const int64_t slices = disc ? 1 : d.num_groups;
+  const void* b_base = disc ? static_cast<const void*>(P->maps) : a->b;
+  const void* sfb_base = disc ? static_cast<const void*>(P->maps) : a->sfb;
   {
-    cuuint64_t dims[3] = {cuuint64_t(P->kbytes), cuuint64_t(d.n), cuuint64_t(d.num_groups)};
+    cuuint64_t dims[3] = {cuuint64_t(P->kbytes), cuuint64_t(d.n), cuuint64_t(slices)};
     cuuint64_t strides[2] = {cuuint64_t(P->kbytes), cuuint64_t(P->kbytes * d.n)};
     cuuint32_t box[3] = {bsgg::kBKBytes, cuuint32_t(P->pair || P->mc ? P->bn / 2 : P->bn), 1};
-    if ((st = encode_one(&L->tmB, a->b, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) != BSGG_OK) return st;
+    if ((st = encode_one(&L->tmB, b_base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) != BSGG_OK)
+      return st;
   }
   {
     cuuint64_t dims[3] = {256, cuuint64_t(2 * kq), cuuint64_t(ceil_div(d.m_pad, 128))};
@@ -189,10 +199,10 @@ bsgg_status encode_maps(const bsgg_plan* P, const bsgg_args* a, bsgg::Launch* L)
       return st;
   }
   {
-    cuuint64_t dims[3] = {256, cuuint64_t(2 * kq), cuuint64_t(ceil_div(d.n, 128) * d.num_groups)};
+    cuuint64_t dims[3] = {256, cuuint64_t(2 * kq), cuuint64_t(ceil_div(d.n, 128) * slices)};
     cuuint64_t strides[2] = {256, cuuint64_t(512 * kq)};
     cuuint32_t box[3] = {256, cuuint32_t(2 * atoms), cuuint32_t(P->bn / 128)};
-    if ((st = encode_one(&L->tmSFB, a->sfb, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) != BSGG_OK)
+    if ((st = encode_one(&L->tmSFB, sfb_base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) != BSGG_OK)
       return st;
   }
   return BSGG_OK;
@@ -236,9 +246,18 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
 bsgg_status check_args(const bsgg_plan* P, const bsgg_args* a) {
   if (!a) return BSGG_ERR_INVALID_ARG;
   const bsgg_desc& d = P->desc;
-  const void* need[] = {a->a, a->sfa, a->b, a->sfb, a->padded_offsets, a->alpha, a->prob, a->d};
+  const void* need[] = {a->a, a->sfa, a->padded_offsets, a->alpha, a->prob, a->d};
   for (const void* p : need)
     if (!p || !aligned16(p)) return BSGG_ERR_INVALID_ARG;
+  // dense and discrete weights are mutually exclusive ("Grouped GEMM + GLU +
+  // Hadamard + Quant (SM100)", Constraints)
+  if (d.discrete_b) {
+    if (a->b || a->sfb || !a->b_ptrs || !a->sfb_ptrs || !aligned16(a->b_ptrs) || !aligned16(a->sfb_ptrs))
+      return BSGG_ERR_INVALID_ARG;
+  } else {
+    if (a->b_ptrs || a->sfb_ptrs || !a->b || !a->sfb || !aligned16(a->b) || !aligned16(a->sfb))
+      return BSGG_ERR_INVALID_ARG;
+  }
   if (is_quant(d.out_format)) {
     if (!a->sfd_row || !a->norm_const || !aligned16(a->sfd_row)) return BSGG_ERR_INVALID_ARG;
     if (d.want_col && (!a->d_col || !a->sfd_col || !aligned16(a->d_col) || !aligned16(a->sfd_col)))
@@ -267,6 +286,43 @@ __global__ void pack_sf_kernel(const uint8_t* __restrict__ src, uint8_t* __restr
   }
 }
 
+// Discrete weight mode: expert g's maps are the templates with the global
+// address replaced by b_ptrs[g] / sfb_ptrs[g].  One block, one thread per
+// expert.  An expert that owns rows needs both pointers non-null and 16-byte
+// aligned; otherwise the flag after the maps is raised (the GEMM then writes
+// nothing) along with the status bit.  Experts without rows keep the
+// placeholder address; their maps are never used.
+__global__ void expert_maps_kernel(const __grid_constant__ CUtensorMap tB, const __grid_constant__ CUtensorMap tSFB,
+                                   const int64_t* __restrict__ b_ptrs, const int64_t* __restrict__ sfb_ptrs,
+                                   const int32_t* __restrict__ offsets, int L, CUtensorMap* maps, uint32_t* status) {
+  const int g = threadIdx.x;
+  int bad = 0;
+  if (g < L) {
+    const int32_t start = g ? offsets[g - 1] : 0;
+    const bool used = offsets[g] != start;
+    const uint64_t pb = static_cast<uint64_t>(b_ptrs[g]), ps = static_cast<uint64_t>(sfb_ptrs[g]);
+    maps[2 * g] = tB;
+    maps[2 * g + 1] = tSFB;
+    if (used) {
+      if (pb == 0 || ps == 0 || (pb & 15u) != 0 || (ps & 15u) != 0) {
+        bad = 1;
+      } else {
+        bsgg::tmap_replace_address(&maps[2 * g], pb);
+        bsgg::tmap_replace_address(&maps[2 * g + 1], ps);
+      }
+    }
+    bsgg::tmap_release();
+  }
+  bad = __syncthreads_or(bad);
+  if (g == 0) {
+    *reinterpret_cast<uint32_t*>(maps + 2 * L) = bad ? 1u : 0u;
+    if (bad) atomicOr(status, bsgg::kStatusBadPointers);
+  }
+}
+
+// Bytes of the discrete-mode workspace: two maps per expert and a flag word.
+size_t maps_bytes(int L) { return sizeof(CUtensorMap) * (2 * size_t(L) + 1); }
+
 }  // namespace
 
 extern "C" {
@@ -279,6 +335,7 @@ const char* bsgg_status_string(bsgg_status s) {
     case BSGG_ERR_CUDA: return "CUDA error";
     case BSGG_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case BSGG_ERR_BAD_OFFSETS: return "padded_offsets invalid";
+    case BSGG_ERR_BAD_POINTERS: return "expert weight pointer invalid";
   }
   return "unknown status";
 }
@@ -331,6 +388,11 @@ bsgg_status bsgg_create(const bsgg_desc* desc, bsgg_plan** plan) {
     delete P;
     return BSGG_ERR_CUDA;
   }
+  if (desc->discrete_b && cudaMalloc(&P->maps, maps_bytes(desc->num_groups)) != cudaSuccess) {
+    cudaFree(P->status);
+    delete P;
+    return BSGG_ERR_CUDA;
+  }
   *plan = P;
   return BSGG_OK;
 }
@@ -338,6 +400,7 @@ bsgg_status bsgg_create(const bsgg_desc* desc, bsgg_plan** plan) {
 void bsgg_destroy(bsgg_plan* plan) {
   if (!plan) return;
   if (plan->status) cudaFree(plan->status);
+  if (plan->maps) cudaFree(plan->maps);
   delete plan;
 }
 
@@ -391,6 +454,10 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   p.glu_kind = d.epilogue == BSGG_EPI_GEGLU ? 1 : 0;
   p.glu_limit = d.glu_limit;
   p.glu_gamma = d.glu_alpha == 0.0f ? 1.0f : d.glu_alpha;
+  if (d.discrete_b) {
+    p.b_maps = P->maps;
+    p.maps_bad = reinterpret_cast<const uint32_t*>(P->maps + 2 * d.num_groups);
+  }
   p.force_timeout = P->force_timeout ? 1u : 0u;
   p.wait_limit_ns = P->force_timeout ? kTestWaitLimitNs : bsgg::kWaitLimitNs;
 
@@ -406,6 +473,12 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   L.epi = P->epi;
   L.outc = P->outc;
   L.stream = s;
+  if (d.discrete_b) {
+    const unsigned threads = static_cast<unsigned>(ceil_div(d.num_groups, 32) * 32);
+    expert_maps_kernel<<<1, threads, 0, s>>>(L.tmB, L.tmSFB, a->b_ptrs, a->sfb_ptrs, a->padded_offsets,
+                                             d.num_groups, P->maps, P->status);
+    if (cudaGetLastError() != cudaSuccess) return BSGG_ERR_CUDA;
+  }
   cudaError_t e;
   if (d.in_format == BSGG_IN_NVFP4)
     e = P->pair ? bsgg::launch_nvf4_pair(L)
@@ -431,6 +504,7 @@ bsgg_status bsgg_query_device_status(bsgg_plan* P, void* stream) {
   uint32_t w = 0;
   if (cudaMemcpy(&w, P->status, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return BSGG_ERR_CUDA;
   if (cudaMemset(P->status, 0, sizeof(w)) != cudaSuccess) return BSGG_ERR_CUDA;
+  if (w & bsgg::kStatusBadPointers) return BSGG_ERR_BAD_POINTERS;
   if (w & bsgg::kStatusBadOffsets) return BSGG_ERR_BAD_OFFSETS;
   if (w & bsgg::kStatusTimeout) return BSGG_ERR_DEVICE_TIMEOUT;
   return BSGG_OK;
@@ -440,6 +514,8 @@ bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* 
                           uint64_t* h2d_bytes, uint64_t* d2h_bytes) {
   if (!P || !host || !dev) return BSGG_ERR_INVALID_ARG;
   const bsgg_desc& d = P->desc;
+  // discrete weights are taken as resident on the device
+  if (d.discrete_b && (host->b || host->sfb || host->b_ptrs || host->sfb_ptrs)) return BSGG_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t L = d.num_groups;
   const uint64_t sz_a = uint64_t(d.m_pad) * P->kbytes;
@@ -531,7 +607,10 @@ extern "C" bsgg_status bsgg_run_noalloc(const bsgg_desc* desc, const bsgg_args* 
                                         int32_t wait_status) {
   const bsgg_status v = validate(desc);
   if (v != BSGG_OK) return v;
-  if (kNoAllocStatusBytes > sizeof(g_noalloc_scratch)) return BSGG_ERR_UNSUPPORTED;
+  // scratch this call needs: the status word, plus the per-expert tensor maps in
+  // discrete weight mode (which never fit)
+  const size_t need = kNoAllocStatusBytes + (desc->discrete_b ? maps_bytes(desc->num_groups) : 0);
+  if (need > sizeof(g_noalloc_scratch)) return BSGG_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return BSGG_ERR_CUDA;
   uint32_t* scratch = nullptr;

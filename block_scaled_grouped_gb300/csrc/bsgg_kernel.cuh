@@ -86,6 +86,7 @@ static_assert(256 * Roles<true>::kLowRegs + 256 * Roles<true>::kHighRegs == 512 
 constexpr int kMaxGroups = 1024;
 constexpr uint32_t kStatusTimeout = 1u;
 constexpr uint32_t kStatusBadOffsets = 2u;
+constexpr uint32_t kStatusBadPointers = 4u;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;     // 2 s per wait (Params::wait_limit_ns)
 constexpr uint64_t kDrainLimitNs = 200000000ull;     // 0.2 s per drain wait
 
@@ -126,6 +127,11 @@ struct Params {
   int32_t glu_kind;         // EPI_SWIGLU instances: 0 = SwiGLU, 1 = GeGLU
   float glu_limit;          // both GLU halves clamped to [-glu_limit, glu_limit]; 0 = none
   float glu_gamma;          // GLU output scale (1 = none)
+  // discrete weight mode: per-expert tensor maps {B_g, SFB_g} (2 per expert, in
+  // global memory) and the flag their writer raises for a bad pointer; null in
+  // dense mode
+  const CUtensorMap* b_maps;
+  const uint32_t* maps_bad;
 };
 
 template <bool FP4, int BN, bool PAIR>
@@ -582,6 +588,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
     if (s_off[i] < prev || (s_off[i] % kBM) != 0) bad = 1;
   }
   if (tid == 0 && s_off[p.L - 1] != p.m_pad) bad = 1;
+  if (tid == 0 && p.b_maps != nullptr && *p.maps_bad != 0u) bad = 1;   // discrete mode: bad pointers
   bad = __syncthreads_or(bad);
   // tile rows per group, inclusive prefix (warp 0: contiguous chunks per lane)
   if (!bad && warp == 0) {
@@ -609,7 +616,9 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
   const int num_tiles = bad ? 0 : s_trow[p.L - 1] * (MC ? 1 : p.num_n_tiles);
 
   if (bad) {
-    if (blockIdx.x == 0 && tid == 0) atomicOr(p.status, kStatusBadOffsets);
+    // (bad pointers were reported by the kernel that wrote the maps)
+    if (blockIdx.x == 0 && tid == 0 && !(p.b_maps != nullptr && *p.maps_bad != 0u))
+      atomicOr(p.status, kStatusBadOffsets);
   } else if (ST ? warp < 8 : (warp < 2 || warp == Ro::kCopyWarp)) {
     // producer, MMA issuer, scale warps (and, storing scales, two idle warps)
     if constexpr (ST) setmaxnreg_dec<Ro::kLowRegs>();
@@ -623,12 +632,28 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
 #pragma unroll
         for (int s = 0; s < S; ++s) { issued[s] = false; issued_phase[s] = 0; }
         bool ok = true;
+        int fenced_g = -1;
         for (int t = unit; t < num_tiles && ok; t += num_units) {
           int g, mt, nt;
           bool valid, share_b;
           decode_tile<CM>(t, p, s_off, s_trow, rank, g, mt, nt, valid, share_b);
           const int b_row = nt * BN + (PAIR ? static_cast<int>(rank) * Ly::kBRows : 0);
-          const int sfb_rb = g * p.rn_b + nt * Ly::kHalves;
+          // dense weights: expert g is slice g of B and of SFB; discrete weights:
+          // expert g's own maps, each of one slice
+          const CUtensorMap* mB = &tmB;
+          const CUtensorMap* mSFB = &tmSFB;
+          int bz = g, sfb_rb = g * p.rn_b + nt * Ly::kHalves;
+          if (p.b_maps != nullptr) {
+            mB = p.b_maps + 2 * g;
+            mSFB = mB + 1;
+            bz = 0;
+            sfb_rb = nt * Ly::kHalves;
+            if (g != fenced_g) {
+              tmap_acquire(mB);
+              tmap_acquire(mSFB);
+              fenced_g = g;
+            }
+          }
           for (int ks = 0; ks < p.num_k_stages; ++ks) {
             if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit_ns)) { ok = false; break; }
             const uint32_t fb = full_bar(stage);
@@ -645,17 +670,17 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
               if (leader) mbar_expect_tx(fb, 2u * (Ly::kABytes + Ly::kBBytes));
               mbar_expect_tx(sfb_own, Ly::kSfaBytes + Ly::kSfbBytes);
               tma_load_2d_pair(sA, &tmA, fbl, k0, mt * kBM);
-              tma_load_3d_pair(sB, &tmB, fbl, k0, b_row, g);
+              tma_load_3d_pair(sB, mB, fbl, k0, b_row, bz);
               tma_load_3d(sSa, &tmSFA, sfb_own, 0, ka, mt);
-              tma_load_3d(sSb, &tmSFB, sfb_own, 0, ka, sfb_rb);
+              tma_load_3d(sSb, mSFB, sfb_own, 0, ka, sfb_rb);
             } else if (PAIR) {
               // both CTAs' bytes complete the even CTA's barrier
               const uint32_t fbl = mapa_shared(fb, 0);
               if (leader) mbar_expect_tx(fb, 2u * Ly::kStageBytes);
               tma_load_2d_pair(sA, &tmA, fbl, k0, mt * kBM);
-              tma_load_3d_pair(sB, &tmB, fbl, k0, b_row, g);
+              tma_load_3d_pair(sB, mB, fbl, k0, b_row, bz);
               tma_load_3d_pair(sSa, &tmSFA, fbl, 0, ka, mt);
-              tma_load_3d_pair(sSb, &tmSFB, fbl, 0, ka, sfb_rb);
+              tma_load_3d_pair(sSb, mSFB, fbl, 0, ka, sfb_rb);
             } else if (MC) {
               // every byte of this CTA's stage counts on its own barrier; the
               // shared operand arrives half from each CTA (A boxes are 64 rows,
@@ -665,20 +690,20 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
               if (share_b) {
                 tma_load_2d(sA, &tmA, fb, k0, mt * kBM);
                 tma_load_2d(sA + kABytesHalf, &tmA, fb, k0, mt * kBM + kBM / 2);
-                tma_load_3d_mc(sB + r * (Ly::kBBytes / 2), &tmB, fb, k0, b_row + r * (BN / 2), g, 0x3);
+                tma_load_3d_mc(sB + r * (Ly::kBBytes / 2), mB, fb, k0, b_row + r * (BN / 2), bz, 0x3);
               } else {
                 tma_load_2d_mc(sA + r * kABytesHalf, &tmA, fb, k0, mt * kBM + r * (kBM / 2), 0x3);
-                tma_load_3d(sB, &tmB, fb, k0, b_row, g);
-                tma_load_3d(sB + Ly::kBBytes / 2, &tmB, fb, k0, b_row + BN / 2, g);
+                tma_load_3d(sB, mB, fb, k0, b_row, bz);
+                tma_load_3d(sB + Ly::kBBytes / 2, mB, fb, k0, b_row + BN / 2, bz);
               }
               tma_load_3d(sSa, &tmSFA, fb, 0, ka, mt);
-              tma_load_3d(sSb, &tmSFB, fb, 0, ka, sfb_rb);
+              tma_load_3d(sSb, mSFB, fb, 0, ka, sfb_rb);
             } else {
               mbar_expect_tx(fb, Ly::kStageBytes);
               tma_load_2d(sA, &tmA, fb, k0, mt * kBM);
-              tma_load_3d(sB, &tmB, fb, k0, b_row, g);
+              tma_load_3d(sB, mB, fb, k0, b_row, bz);
               tma_load_3d(sSa, &tmSFA, fb, 0, ka, mt);
-              tma_load_3d(sSb, &tmSFB, fb, 0, ka, sfb_rb);
+              tma_load_3d(sSb, mSFB, fb, 0, ka, sfb_rb);
             }
             issued[stage] = true;
             issued_phase[stage] = phase;

@@ -100,6 +100,20 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// Per-expert tensor maps in global memory (discrete weight mode): the global
+// address field of a 128-byte map is rewritten in place; the writer releases
+// the maps to the tensor-map proxy, the TMA-issuing thread acquires each map
+// before its first use.
+__device__ __forceinline__ void tmap_replace_address(CUtensorMap* map, uint64_t addr) {
+  asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(map), "l"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void tmap_release() {
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+__device__ __forceinline__ void tmap_acquire(const CUtensorMap* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }

@@ -75,8 +75,11 @@ typedef enum {
   BSGG_ERR_UNSUPPORTED = 2,     /* valid on the pages but not built here */
   BSGG_ERR_CUDA = 3,            /* a CUDA runtime call failed */
   BSGG_ERR_DEVICE_TIMEOUT = 4,  /* a kernel wait ran out; the kernel returned early */
-  BSGG_ERR_BAD_OFFSETS = 5      /* padded_offsets not non-decreasing multiples of 128
+  BSGG_ERR_BAD_OFFSETS = 5,     /* padded_offsets not non-decreasing multiples of 128
                                    ending at m_pad; the kernel wrote nothing */
+  BSGG_ERR_BAD_POINTERS = 6     /* discrete weight mode: a b_ptrs / sfb_ptrs entry of a
+                                   non-empty group is null or not 16-byte aligned; the
+                                   kernel wrote nothing */
 } bsgg_status;
 
 /* Input formats ("Grouped GEMM + Quant (SM100)", Data Types table). */
@@ -138,6 +141,14 @@ typedef struct {
   int32_t want_bias;      /* 1: add bias_g[n] to C; bias is (L, N), N contiguous per expert
                              (the pages' (N, L) tensor with stride (1, N)) */
   int32_t bias_format;    /* BSGG_OUT_BF16, BSGG_OUT_F16 or BSGG_OUT_F32 (when want_bias) */
+  /* Discrete weight mode ("Grouped GEMM + GLU + Hadamard + Quant (SM100)", Discrete weight
+     mode): 1 = each expert's B and SFB are separate allocations named by the device
+     pointer arrays b_ptrs / sfb_ptrs instead of the dense b / sfb tensors (the two
+     modes are mutually exclusive).  B_g is (N, K) K-major, SFB_g is SF(N, K) with one
+     slice (bsgg_sf_bytes(N, K, v, 1) bytes).  The plan then owns 256 * L + 256 bytes
+     of device memory for one TMA descriptor pair per expert, written by a small
+     kernel on the stream before every launch. */
+  int32_t discrete_b;
 } bsgg_desc;
 
 /* Tensors of one call.  Unused outputs may be NULL: d_col/sfd_col unless
@@ -161,6 +172,12 @@ typedef struct {
   float* amax;               /* zeroed by bsgg_run on the stream before the kernel */
   const void* bias;          /* (L, N) in bias_format; required iff want_bias */
   void* c;                   /* (m_pad, N) in c_format; required iff want_c */
+  /* discrete_b only (b and sfb then NULL): device arrays of L int64 device
+     addresses.  Entries of empty groups are not read by the GEMM and may be 0;
+     the others must be 16-byte aligned (checked on the device: a violation is
+     BSGG_ERR_BAD_POINTERS from bsgg_query_device_status, and nothing is written). */
+  const int64_t* b_ptrs;
+  const int64_t* sfb_ptrs;
 } bsgg_args;
 
 typedef struct bsgg_plan bsgg_plan;
@@ -181,12 +198,14 @@ bsgg_status bsgg_run(bsgg_plan* plan, const bsgg_args* args, void* stream);
  * on the `dev` buffers, outputs present in `host` are copied back, and the
  * stream is synchronized.  An input left NULL in `host` is taken as already
  * resident in `dev`.  Bytes moved are returned in *h2d_bytes / *d2h_bytes
- * (either may be NULL).  Allocates nothing. */
+ * (either may be NULL).  Allocates nothing.  In discrete weight mode the
+ * experts' weights are taken as resident (dev->b_ptrs / dev->sfb_ptrs; host->b
+ * and host->sfb must be NULL). */
 bsgg_status bsgg_run_host(bsgg_plan* plan, const bsgg_args* host, const bsgg_args* dev,
                           void* stream, uint64_t* h2d_bytes, uint64_t* d2h_bytes);
 
 /* Synchronize `stream`, then read and clear the plan's device status word:
- * BSGG_OK, BSGG_ERR_DEVICE_TIMEOUT or BSGG_ERR_BAD_OFFSETS. */
+ * BSGG_OK, BSGG_ERR_DEVICE_TIMEOUT, BSGG_ERR_BAD_OFFSETS or BSGG_ERR_BAD_POINTERS. */
 bsgg_status bsgg_query_device_status(bsgg_plan* plan, void* stream);
 
 /* Test hook for the failure path; the pages have no counterpart.  With enable =
@@ -230,9 +249,9 @@ bsgg_status bsgg_pack_sf(const uint8_t* rowmajor, uint8_t* swizzled, int64_t row
  * The kernel's only scratch, its 4-byte device status word, lives in a
  * file-scope static device array of BSGG_NOALLOC_SCRATCH_BYTES bytes that every
  * GPU which loads the library holds until the process exits.  A call whose
- * scratch need exceeded that array would be rejected with
- * BSGG_ERR_UNSUPPORTED; the need is one word for every problem the validation
- * accepts.
+ * scratch need exceeds that array is rejected with BSGG_ERR_UNSUPPORTED: the
+ * need is one word, except in discrete weight mode, whose per-expert
+ * descriptors (256 * L + 256 bytes) never fit, so discrete_b = 1 is rejected.
  *
  * The first call on a device looks up the array's device address with that
  * device current (cudaGetSymbolAddress); make that first call before any

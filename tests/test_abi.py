@@ -54,7 +54,8 @@ def _create(**over):
     a plan it makes is destroyed at once."""
     d = dict(m_pad=384, n=256, k=256, num_groups=2, in_format="mxfp8_e4m3", out_format="bf16",
              epilogue="gate")
-    raw = {k_: over.pop(k_) for k_ in ("c_format_code", "bias_format_code", "want_c_raw") if k_ in over}
+    raw = {k_: over.pop(k_) for k_ in ("c_format_code", "bias_format_code", "want_c_raw", "discrete_raw")
+           if k_ in over}
     d.update(over)
     tile = (d.pop("tile_m", 0), d.pop("tile_n", 0))
     cluster = (d.pop("cluster_m", 0), d.pop("cluster_n", 0))
@@ -66,6 +67,8 @@ def _create(**over):
         desc.want_bias, desc.bias_format = 1, raw["bias_format_code"]
     if "want_c_raw" in raw:
         desc.want_c = raw["want_c_raw"]
+    if "discrete_raw" in raw:
+        desc.discrete_b = raw["discrete_raw"]
     h = ctypes.c_void_p()
     code = bsgg.lib().bsgg_create(ctypes.byref(desc), ctypes.byref(h))
     if h.value:
@@ -100,6 +103,7 @@ def _create(**over):
     (dict(c_format="f32"), 1), (dict(c_format_code=3), 1),    # C is bf16 or f16
     (dict(bias_format="e4m3"), 1), (dict(bias_format_code=9), 1),
     (dict(want_c_raw=2), 1),
+    (dict(discrete_raw=2), 1),
 ])
 def test_create_rejects(lib, over, code):
     assert _create(**over) == code
@@ -110,6 +114,7 @@ def test_create_rejects(lib, over, code):
     dict(epilogue="swiglu", glu_alpha=1.0, c_format="bf16", bias_format="f32"),
     dict(epilogue="srelu", glu_alpha=0.0, c_format="f16", bias_format="bf16"),
     dict(epilogue="gate", bias_format="f16"),
+    dict(discrete_b=True, num_groups=1024),
 ])
 def test_create_accepts_epilogue_options(lib, over):
     # validation passes: 0 with a GPU, else the device query that follows
