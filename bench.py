@@ -429,7 +429,7 @@ def run_gpu(args, world, rank, local):
                 "config": config_of(p, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                                         "tile": args.tile or "library default",
                                         "cluster": args.cluster or "library default"}),
-                "gpu_launches": args.steps, "clocks": clocks, "roofline": roofline,
+                "gpu_launches": args.steps * plan.launches_per_run, "clocks": clocks, "roofline": roofline,
                 "e2e": e2e, "cpu_baseline": cpu_baseline, "hbm": hbm,
                 "pct_of_dtype_peak": 100.0 * achieved / peak}
         print(json.dumps(line), flush=True)

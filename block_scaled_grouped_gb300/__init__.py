@@ -23,7 +23,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CU
 
 SYMBOLS = ("bsgg_create", "bsgg_run", "bsgg_run_host", "bsgg_query_device_status", "bsgg_destroy",
            "bsgg_status_string", "bsgg_sf_bytes", "bsgg_sf_offset", "bsgg_pack_sf", "bsgg_run_noalloc",
-           "bsgg_measure_mma_peak", "bsgg_debug_force_timeout")
+           "bsgg_measure_mma_peak", "bsgg_debug_force_timeout", "bsgg_launches_per_run")
 
 
 class BsggError(RuntimeError):
@@ -107,6 +107,8 @@ def lib():
                                             ctypes.POINTER(ctypes.c_double), ctypes.c_void_p]
         L.bsgg_debug_force_timeout.restype = ctypes.c_int
         L.bsgg_debug_force_timeout.argtypes = [ctypes.c_void_p, ctypes.c_int32]
+        L.bsgg_launches_per_run.restype = ctypes.c_int32
+        L.bsgg_launches_per_run.argtypes = [ctypes.c_void_p]
         L.bsgg_pack_sf.restype = ctypes.c_int
         L.bsgg_pack_sf.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                    ctypes.c_int32, ctypes.c_void_p]
@@ -221,6 +223,11 @@ class Plan:
         _check(lib().bsgg_run_host(self._h, ctypes.byref(hi), ctypes.byref(di), _stream(stream),
                                    ctypes.byref(h2d), ctypes.byref(d2h)), "bsgg_run_host")
         return int(h2d.value), int(d2h.value)
+
+    @property
+    def launches_per_run(self) -> int:
+        """Kernel launches one run() enqueues (bsgg_launches_per_run)."""
+        return int(lib().bsgg_launches_per_run(self._h))
 
     def device_status(self, stream=None) -> int:
         """Synchronize and read/clear the device status word (0 = ok)."""

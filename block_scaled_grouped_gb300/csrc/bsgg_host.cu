@@ -491,6 +491,11 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   return e == cudaSuccess ? BSGG_OK : BSGG_ERR_CUDA;
 }
 
+int32_t bsgg_launches_per_run(const bsgg_plan* P) {
+  if (!P) return -1;
+  return P->desc.discrete_b ? 2 : 1;   // the per-expert descriptor kernel, then the GEMM
+}
+
 bsgg_status bsgg_debug_force_timeout(bsgg_plan* P, int32_t enable) {
   if (!P || (enable != 0 && enable != 1)) return BSGG_ERR_INVALID_ARG;
   P->force_timeout = enable != 0;

@@ -204,6 +204,11 @@ bsgg_status bsgg_run(bsgg_plan* plan, const bsgg_args* args, void* stream);
 bsgg_status bsgg_run_host(bsgg_plan* plan, const bsgg_args* host, const bsgg_args* dev,
                           void* stream, uint64_t* h2d_bytes, uint64_t* d2h_bytes);
 
+/* Number of kernel launches one bsgg_run of this plan enqueues (the pages have
+ * no counterpart): 1, or 2 in discrete weight mode (the per-expert descriptor
+ * kernel, then the GEMM).  -1 for a null plan. */
+int32_t bsgg_launches_per_run(const bsgg_plan* plan);
+
 /* Synchronize `stream`, then read and clear the plan's device status word:
  * BSGG_OK, BSGG_ERR_DEVICE_TIMEOUT, BSGG_ERR_BAD_OFFSETS or BSGG_ERR_BAD_POINTERS. */
 bsgg_status bsgg_query_device_status(bsgg_plan* plan, void* stream);
