@@ -247,7 +247,7 @@ def algorithmic_bytes(p) -> int:
     kb = p.k // 2 if fp4 else p.k
     off = [int(x) for x in p.padded_offsets.tolist()]
     nonempty = sum(1 for g, e in enumerate(off) if e > (off[g - 1] if g else 0))
-    n_out = p.n // 2 if p.epi in ("swiglu", "geglu") else p.n
+    n_out = p.n_out
     bits = {"bf16": 16, "f16": 16, "f32": 32, "e4m3": 8, "e5m2": 8, "e2m1": 4}[p.out_fmt]
     d = p.m_pad * n_out * bits // 8
     out = d * (2 if p.want_col else 1)

@@ -33,7 +33,7 @@ import torch
 
 IN_FORMATS = ("mxfp8_e4m3", "mxfp8_e5m2", "nvfp4")
 OUT_FORMATS = ("bf16", "f16", "f32", "e4m3", "e5m2", "e2m1")
-EPILOGUES = ("gate", "swiglu", "srelu", "geglu")
+EPILOGUES = ("gate", "swiglu", "srelu", "geglu", "dswiglu")
 
 _ROW_CHUNK = 4096
 
@@ -60,6 +60,10 @@ class Problem:
     sfa_rows: torch.Tensor      # uint8 (1, m_pad, k/v) scale codes, row-major
     b: torch.Tensor             # uint8 (L, n, k or k/2)
     sfb_rows: torch.Tensor      # uint8 (L, n, k/v) scale codes, row-major
+    # the dSwiGLU backward's extra inputs (None otherwise): the saved forward
+    # pre-activation C (m_pad, 2n) bf16 and its per-group scale beta (L,)
+    saved_c: Optional[torch.Tensor] = None
+    beta: Optional[torch.Tensor] = None
 
     @property
     def sf_vec(self) -> int:
@@ -67,7 +71,9 @@ class Problem:
 
     @property
     def n_out(self) -> int:
-        return self.n // 2 if self.epi in ("swiglu", "geglu") else self.n
+        if self.epi in ("swiglu", "geglu"):
+            return self.n // 2
+        return 2 * self.n if self.epi == "dswiglu" else self.n
 
     @property
     def m_real(self) -> int:
@@ -325,6 +331,17 @@ def build_problem(*, name: str, counts: Sequence[int], k: int, n: int, in_fmt: s
             b[g, c0:c0 + r] = q
             sfb[g, c0:c0 + r] = s
 
+    # dSwiGLU backward: the saved forward C, N(0, 2) rounded to bf16 (a
+    # pre-activation's typical spread), and beta ~ U(0.5, 2) per group
+    saved_c = beta = None
+    if epi == "dswiglu":
+        beta = torch.as_tensor(rng.uniform(0.5, 2.0, size=L).astype(np.float32), device=device)
+        saved_c = torch.empty(m_pad, 2 * n, dtype=torch.bfloat16, device=device)
+        for c0 in range(0, m_pad, _ROW_CHUNK):
+            r = min(_ROW_CHUNK, m_pad - c0)
+            saved_c[c0:c0 + r] = (_draw(r, 2 * n, "normal", device, seed, 200_000 + c0 // _ROW_CHUNK)
+                                  * 2.0).to(torch.bfloat16)
+
     return Problem(
         name=name, m_pad=m_pad, n=n, k=k, num_groups=L, in_fmt=in_fmt, out_fmt=out_fmt, epi=epi,
         tanh_clamp_s=float(tanh_clamp_s), want_col=bool(want_col), norm_const=float(norm_const),
@@ -332,7 +349,7 @@ def build_problem(*, name: str, counts: Sequence[int], k: int, n: int, in_fmt: s
         padded_offsets=torch.as_tensor(offsets.astype(np.int32), device=device),
         alpha=torch.as_tensor(alpha, device=device),
         prob=torch.as_tensor(prob, device=device),
-        a=a, sfa_rows=sfa, b=b, sfb_rows=sfb)
+        a=a, sfa_rows=sfa, b=b, sfb_rows=sfb, saved_c=saved_c, beta=beta)
 
 
 WORKLOADS = ("tiny", "fc1_swiglu", "fc2_gate", "fine_nvfp4", "skewed")

@@ -29,7 +29,7 @@ _lib = None
 F_E4M3, F_E5M2, F_E2M1, F_UE8M0 = 0, 1, 2, 3
 IN_MXFP8_E4M3, IN_MXFP8_E5M2, IN_NVFP4 = 0, 1, 2
 OUT_BF16, OUT_F16, OUT_F32, OUT_E4M3, OUT_E5M2, OUT_E2M1 = 0, 1, 2, 3, 4, 5
-EPI_GATE, EPI_SWIGLU, EPI_SRELU, EPI_GEGLU = 0, 1, 2, 3
+EPI_GATE, EPI_SWIGLU, EPI_SRELU, EPI_GEGLU, EPI_DSWIGLU = 0, 1, 2, 3, 4
 
 
 class OrcDesc(ctypes.Structure):
@@ -82,8 +82,8 @@ def lib():
         L.orc_group_of_row.restype = ctypes.c_int64
         L.orc_group_of_row.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64]
         L.orc_run.restype = ctypes.c_int
-        L.orc_run.argtypes = [ctypes.POINTER(OrcDesc)] + [ctypes.c_void_p] * 8 + [
-            ctypes.c_float, ctypes.c_void_p, ctypes.c_int64] + [ctypes.c_void_p] * 7 + [ctypes.c_int]
+        L.orc_run.argtypes = [ctypes.POINTER(OrcDesc)] + [ctypes.c_void_p] * 10 + [
+            ctypes.c_float, ctypes.c_void_p, ctypes.c_int64] + [ctypes.c_void_p] * 8 + [ctypes.c_int]
         _lib = L
     return _lib
 
@@ -138,13 +138,15 @@ def group_of_row(offsets: np.ndarray, m: int) -> int:
 
 
 def n_out(n: int, epi: int) -> int:
-    return n // 2 if epi in (EPI_SWIGLU, EPI_GEGLU) else n
+    if epi in (EPI_SWIGLU, EPI_GEGLU):
+        return n // 2
+    return 2 * n if epi == EPI_DSWIGLU else n
 
 
 def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded_offsets,
         alpha, prob, norm_const=1.0, tanh_clamp_s=0.0, gate_first=0, want_col=False,
         blocks=None, threads=None, outputs=None, bias=None, glu_limit=0.0, glu_alpha=1.0,
-        want_c=False):
+        want_c=False, saved_c=None, beta=None):
     """Run the oracle on the listed 32-row blocks (default: all of them).
 
     Inputs are numpy arrays in the device layouts: ``a`` (m_pad, k or k/2)
@@ -155,7 +157,11 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     ``sfd_row``, ``sfd_col`` buffers written for the listed rows only.
     ``bias`` (L, n) float32 is added to C; ``want_c`` adds ``c_ref`` (fp64 C of
     the listed rows, before any clamp or activation).  ``glu_limit`` (0 = none)
-    and ``glu_alpha`` apply to SwiGLU and GeGLU.
+    and ``glu_alpha`` apply to SwiGLU and GeGLU.  The dSwiGLU backward
+    (``epi=EPI_DSWIGLU``) takes ``saved_c`` (m_pad, 2n) values of the saved
+    forward C (any float dtype, widened to fp64) and ``beta`` float32 (L,), and
+    adds ``dprob_ref`` (fp64, rows of the listed blocks); its ``amax`` has 2L
+    entries (input-gradient and gate-gradient blocks of each group).
     """
     L = lib()
     desc = OrcDesc(m_pad, n, k, num_groups, in_fmt, out_fmt, epi, int(gate_first),
@@ -169,7 +175,10 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     d_ref = np.zeros((blocks.size * 32, nd), dtype=np.float64)
     c_ref = np.zeros((blocks.size * 32, n), dtype=np.float64) if want_c else None
     bias_arr = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32).reshape(num_groups, n)
-    amax = np.zeros(num_groups, dtype=np.float32)
+    amax = np.zeros(2 * num_groups if epi == EPI_DSWIGLU else num_groups, dtype=np.float32)
+    dprob_ref = np.zeros(blocks.size * 32, dtype=np.float64) if epi == EPI_DSWIGLU else None
+    saved_arr = None if saved_c is None else np.ascontiguousarray(saved_c, dtype=np.float64).reshape(m_pad, 2 * n)
+    beta_arr = None if beta is None else np.ascontiguousarray(beta, dtype=np.float32).reshape(num_groups)
     outs = dict(outputs or {})
     quant = out_fmt >= OUT_E4M3
     v = 16 if in_fmt == IN_NVFP4 else 32
@@ -189,13 +198,16 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     )
     rc = L.orc_run(ctypes.byref(desc), _ptr(arrs["a"]), _ptr(arrs["sfa"]), _ptr(arrs["b"]),
                    _ptr(arrs["sfb"]), _ptr(arrs["off"]), _ptr(arrs["alpha"]), _ptr(arrs["prob"]),
-                   _ptr(bias_arr), float(norm_const), _ptr(blocks), blocks.size, _ptr(d_ref),
-                   _ptr(c_ref), _ptr(outs.get("d")), _ptr(outs.get("d_col")), _ptr(outs.get("sfd_row")),
-                   _ptr(outs.get("sfd_col")), _ptr(amax), int(threads))
+                   _ptr(bias_arr), _ptr(saved_arr), _ptr(beta_arr), float(norm_const), _ptr(blocks),
+                   blocks.size, _ptr(d_ref), _ptr(c_ref), _ptr(dprob_ref), _ptr(outs.get("d")),
+                   _ptr(outs.get("d_col")), _ptr(outs.get("sfd_row")), _ptr(outs.get("sfd_col")),
+                   _ptr(amax), int(threads))
     if rc != 0:
         raise ValueError(f"oracle rejected the problem (code {rc})")
     res = {"d_ref": d_ref, "amax": amax, "blocks": blocks}
     if want_c:
         res["c_ref"] = c_ref
+    if dprob_ref is not None:
+        res["dprob_ref"] = dprob_ref
     res.update(outs)
     return res

@@ -161,7 +161,8 @@ int64_t sf_bytes(int64_t rows, int64_t kblocks, int64_t L) {
 // ---------------------------------------------------------------------------
 enum InFmt { IN_MXFP8_E4M3 = 0, IN_MXFP8_E5M2 = 1, IN_NVFP4 = 2 };
 enum OutFmt { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2, OUT_E4M3 = 3, OUT_E5M2 = 4, OUT_E2M1 = 5 };
-enum Epi { EPI_GATE = 0, EPI_SWIGLU = 1, EPI_SRELU = 2, EPI_GEGLU = 3 };
+// EPI_DSWIGLU: the dSwiGLU backward of "Grouped GEMM + dGLU (SM100)".
+enum Epi { EPI_GATE = 0, EPI_SWIGLU = 1, EPI_SRELU = 2, EPI_GEGLU = 3, EPI_DSWIGLU = 4 };
 
 }  // namespace
 
@@ -232,11 +233,21 @@ int64_t orc_group_of_row(const int32_t* off, int64_t L, int64_t m) {
 //   c_ref    [nblocks*32, n] fp64 C (GEMM plus bias, before any clamp or
 //            activation) when not NULL
 // `bias` (L x n, bias[g*n + col]) is added to C when not NULL.
+// The dSwiGLU backward (epi = EPI_DSWIGLU, "Grouped GEMM + dGLU (SM100)",
+// Block-scaled contract, Steps 1-3) also takes
+//   saved_c  [m_pad, 2n] fp64 values of the saved forward C (its input and gate
+//            32-column blocks interleaved; the caller decodes its storage type)
+//   beta     [L] scale of C per group
+// and writes dprob_ref [nblocks*32] fp64 (the listed rows' dprob) and, for
+// 16/32-bit D, amax [2L]: index 2g for the input-gradient blocks, 2g+1 for the
+// gate-gradient blocks (reading of the pages' amax shape (L, 2, 1)).  D is
+// (m_pad, 2n).
 int orc_run(const orc_desc* P, const uint8_t* A, const uint8_t* SFA, const uint8_t* B,
             const uint8_t* SFB, const int32_t* padded_offsets, const float* alpha,
-            const float* prob, const float* bias, float norm_const, const int64_t* blocks,
-            int64_t nblocks, double* d_ref, double* c_ref, uint8_t* d_q, uint8_t* d_col_q,
-            uint8_t* sfd_row, uint8_t* sfd_col, float* amax, int threads);
+            const float* prob, const float* bias, const double* saved_c, const float* beta,
+            float norm_const, const int64_t* blocks, int64_t nblocks, double* d_ref, double* c_ref,
+            double* dprob_ref, uint8_t* d_q, uint8_t* d_col_q, uint8_t* sfd_row, uint8_t* sfd_col,
+            float* amax, int threads);
 
 }  // extern "C"
 
@@ -246,6 +257,9 @@ struct Job {
   const orc_desc* P;
   const float* bias;
   double* c_ref;
+  const double* saved_c;
+  const float* beta;
+  double* dprob_ref;
   const uint8_t *A, *SFA, *B, *SFB;
   const int32_t* off;
   const float *alpha, *prob;
@@ -274,7 +288,10 @@ double q_max(const orc_desc* P) {
   return P->out_fmt == OUT_E4M3 ? 448.0 : P->out_fmt == OUT_E5M2 ? 57344.0 : 6.0;
 }
 bool is_glu(const orc_desc* P) { return P->epi == EPI_SWIGLU || P->epi == EPI_GEGLU; }
-int64_t n_out(const orc_desc* P) { return is_glu(P) ? P->n / 2 : P->n; }
+bool is_bwd(const orc_desc* P) { return P->epi == EPI_DSWIGLU; }
+// D width: N/2 for the forward GLUs (two C blocks per D block), 2N for the
+// backward (two gradient blocks per GEMM block), else N.
+int64_t n_out(const orc_desc* P) { return is_glu(P) ? P->n / 2 : is_bwd(P) ? 2 * P->n : P->n; }
 
 // Element (r, k) of a K-major low-precision operand: one byte per FP8 value,
 // two FP4 values per byte with element 2i in the low nibble (reading).
@@ -345,8 +362,11 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
     const bool second = (gate != bool(P->gate_first));
     return 64 * b + (second ? 32 : 0) + r;
   };
-  const int64_t c0 = is_glu(P) ? 2 * j0 : j0;
-  const int64_t c1 = is_glu(P) ? 2 * j1 : j1;
+  // GEMM columns behind D columns [j0, j1): twice as many for the GLUs, half as
+  // many for the backward (D columns 64b..64b+63 come from GEMM columns
+  // 32b..32b+31)
+  const int64_t c0 = is_glu(P) ? 2 * j0 : is_bwd(P) ? j0 / 2 : j0;
+  const int64_t c1 = is_glu(P) ? 2 * j1 : is_bwd(P) ? j1 / 2 : j1;
 
   // Group of each row ("Grouped GEMM + Quant (SM100)", Equations, Step 1).
   std::vector<int64_t> grp(32);
@@ -368,7 +388,10 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
         if (grp[size_t(i)] != g) continue;
         double acc = 0.0;
         for (int64_t k = 0; k < K; ++k) acc += arows[size_t(i * K + k)] * brow[size_t(k)];
-        C[size_t(i * (c1 - c0) + (n - c0))] = double(J.alpha[g]) * acc;
+        // the backward's GEMM is scaled by alpha_g^2 ("Grouped GEMM + dGLU
+        // (SM100)", Block-scaled contract, Step 1)
+        const double a = double(J.alpha[g]);
+        C[size_t(i * (c1 - c0) + (n - c0))] = (is_bwd(P) ? a * a : a) * acc;
       }
     }
   }
@@ -386,16 +409,45 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
 
   // Step 2: the epilogue, in fp64.
   std::vector<double> D(size_t(32 * w), 0.0);
-  std::vector<float> amax_local(size_t(L), 0.0f);
+  std::vector<float> amax_local(size_t(is_bwd(P) ? 2 * L : L), 0.0f);
+  std::vector<double> dprob_local(32, 0.0);
   for (int64_t i = 0; i < 32; ++i) {
     const int64_t g = grp[size_t(i)];
     if (g < 0) continue;
     const int64_t m = m0 + i;
     const double p = J.prob[m];
     auto Cv = [&](int64_t n) { return C[size_t(i * (c1 - c0) + (n - c0))]; };
+    // dSwiGLU backward ("Grouped GEMM + dGLU (SM100)", Block-scaled contract,
+    // Step 2): the saved C, scaled by beta_g, split into the input X and gate G
+    // 32-column blocks of pair b (same block order as the forward SwiGLU).
+    auto saved = [&](int64_t jr, bool gate) {
+      const int64_t b = jr / 32, r = jr % 32;
+      const bool second = (gate != bool(P->gate_first));
+      return double(J.beta[g]) * J.saved_c[m * 2 * P->n + 64 * b + (second ? 32 : 0) + r];
+    };
+    if (is_bwd(P)) {
+      // dprob += sum over the GEMM columns of X * swish(G) * ref
+      for (int64_t jr = c0; jr < c1; ++jr) {
+        const double x = saved(jr, false), gt = saved(jr, true);
+        dprob_local[size_t(i)] += x * (gt * orc_sigmoid(gt)) * Cv(jr);
+      }
+    }
     for (int64_t j = j0; j < j1; ++j) {
       double d;
-      if (P->epi == EPI_GATE) {
+      int64_t amax_idx = g;
+      if (is_bwd(P)) {
+        // D column j: pair b = j/64; its first or second 32-column block holds
+        // the gradient of the C block at the same place (X or G)
+        const int64_t b = j / 64, r = j % 32;
+        const bool second = (j % 64) >= 32;
+        const bool is_input = (second == bool(P->gate_first));
+        const int64_t jr = 32 * b + r;
+        const double x = saved(jr, false), gt = saved(jr, true), ref = Cv(jr);
+        const double sg = orc_sigmoid(gt);
+        if (is_input) d = ref * p * (gt * sg);                          // d input = ref prob swish(G)
+        else d = ref * p * x * sg * (1.0 + gt * (1.0 - sg));            // d gate
+        amax_idx = 2 * g + (is_input ? 0 : 1);
+      } else if (P->epi == EPI_GATE) {
         d = p * Cv(j);                                    // D = prob * ref
       } else if (is_glu(P)) {
         double x = Cv(c_col_of(j, false)), gt = Cv(c_col_of(j, true));
@@ -411,7 +463,7 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
       }
       D[size_t(i * w + (j - j0))] = d;
       J.d_ref[size_t((bi * 32 + i) * nd + j)] = d;
-      amax_local[size_t(g)] = std::max(amax_local[size_t(g)], std::fabs(float(d)));
+      amax_local[size_t(amax_idx)] = std::max(amax_local[size_t(amax_idx)], std::fabs(float(d)));
     }
   }
 
@@ -456,19 +508,23 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
   }
 
   std::lock_guard<std::mutex> lk(J.mu);
-  for (int64_t g = 0; g < L; ++g) J.amax[size_t(g)] = std::max(J.amax[size_t(g)], amax_local[size_t(g)]);
+  for (size_t g = 0; g < amax_local.size(); ++g) J.amax[g] = std::max(J.amax[g], amax_local[g]);
+  if (is_bwd(P) && J.dprob_ref)
+    for (int64_t i = 0; i < 32; ++i) J.dprob_ref[size_t(bi * 32 + i)] += dprob_local[size_t(i)];
 }
 
 }  // namespace
 
 extern "C" int orc_run(const orc_desc* P, const uint8_t* A, const uint8_t* SFA, const uint8_t* B,
                        const uint8_t* SFB, const int32_t* padded_offsets, const float* alpha,
-                       const float* prob, const float* bias, float norm_const, const int64_t* blocks,
-                       int64_t nblocks, double* d_ref, double* c_ref, uint8_t* d_q, uint8_t* d_col_q,
-                       uint8_t* sfd_row, uint8_t* sfd_col, float* amax, int threads) {
+                       const float* prob, const float* bias, const double* saved_c, const float* beta,
+                       float norm_const, const int64_t* blocks, int64_t nblocks, double* d_ref, double* c_ref,
+                       double* dprob_ref, uint8_t* d_q, uint8_t* d_col_q, uint8_t* sfd_row, uint8_t* sfd_col,
+                       float* amax, int threads) {
   if (!P || P->m_pad <= 0 || P->m_pad % 32 || P->n <= 0 || P->k <= 0 || P->num_groups <= 0)
     return -1;
   if (is_glu(P) && P->n % 64) return -2;
+  if (is_bwd(P) && (P->n % 32 || !saved_c || !beta || bias)) return -4;
   if (is_fp4_in(P) && P->k % 2) return -3;
   const int64_t nd = n_out(P);
   // One work item per (block, 128-column slice of D); slices are multiples of
@@ -476,9 +532,10 @@ extern "C" int orc_run(const orc_desc* P, const uint8_t* A, const uint8_t* SFA, 
   const int64_t slice = 128;
   Job J;
   J.P = P; J.bias = bias; J.c_ref = c_ref; J.A = A; J.SFA = SFA; J.B = B; J.SFB = SFB; J.off = padded_offsets;
+  J.saved_c = saved_c; J.beta = beta; J.dprob_ref = dprob_ref;
   J.alpha = alpha; J.prob = prob; J.norm = norm_const; J.blocks = blocks; J.nblocks = nblocks;
   J.d_ref = d_ref; J.d_q = d_q; J.d_col_q = d_col_q; J.sfd_row = sfd_row; J.sfd_col = sfd_col;
-  J.amax.assign(size_t(P->num_groups), 0.0f);
+  J.amax.assign(size_t(is_bwd(P) ? 2 * P->num_groups : P->num_groups), 0.0f);
   const int64_t nslices = (nd + slice - 1) / slice;
   const int64_t nitems = nblocks * nslices;
   std::atomic<int64_t> next{0};
@@ -496,6 +553,6 @@ extern "C" int orc_run(const orc_desc* P, const uint8_t* A, const uint8_t* SFA, 
   worker();
   for (auto& th : pool) th.join();
   if (amax)
-    for (int64_t g = 0; g < P->num_groups; ++g) amax[g] = J.amax[size_t(g)];
+    for (size_t g = 0; g < J.amax.size(); ++g) amax[g] = J.amax[g];
   return 0;
 }

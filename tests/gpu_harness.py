@@ -18,7 +18,9 @@ def to_device(p: W.Problem, device="cuda") -> W.Problem:
     return dataclasses.replace(
         p, padded_offsets=p.padded_offsets.to(device), alpha=p.alpha.to(device),
         prob=p.prob.to(device), a=p.a.to(device), sfa_rows=p.sfa_rows.to(device),
-        b=p.b.to(device), sfb_rows=p.sfb_rows.to(device))
+        b=p.b.to(device), sfb_rows=p.sfb_rows.to(device),
+        saved_c=None if p.saved_c is None else p.saved_c.to(device),
+        beta=None if p.beta is None else p.beta.to(device))
 
 
 # (tile_m, tile_n, cluster_m, cluster_n): single CTA 128 x 128 and 128 x 256,
