@@ -100,8 +100,9 @@ bsgg_status validate(const bsgg_desc* d) {
     return BSGG_ERR_INVALID_ARG;
   if (d->in_format < BSGG_IN_MXFP8_E4M3 || d->in_format > BSGG_IN_NVFP4) return BSGG_ERR_INVALID_ARG;
   if (d->out_format < BSGG_OUT_BF16 || d->out_format > BSGG_OUT_E2M1) return BSGG_ERR_INVALID_ARG;
-  if (d->epilogue < BSGG_EPI_GATE || d->epilogue > BSGG_EPI_GEGLU) return BSGG_ERR_INVALID_ARG;
+  if (d->epilogue < BSGG_EPI_GATE || d->epilogue > BSGG_EPI_DSWIGLU) return BSGG_ERR_INVALID_ARG;
   const bool glu = d->epilogue == BSGG_EPI_SWIGLU || d->epilogue == BSGG_EPI_GEGLU;
+  const bool bwd = d->epilogue == BSGG_EPI_DSWIGLU;
   if (d->gate_first != 0 && d->gate_first != 1) return BSGG_ERR_INVALID_ARG;
   if (d->want_col != 0 && d->want_col != 1) return BSGG_ERR_INVALID_ARG;
   // K-major rows must be 16-byte aligned ("Support Surface and Constraints",
@@ -128,6 +129,12 @@ bsgg_status validate(const bsgg_desc* d) {
       d->bias_format != BSGG_OUT_F32)
     return BSGG_ERR_INVALID_ARG;
   if (d->discrete_b != 0 && d->discrete_b != 1) return BSGG_ERR_INVALID_ARG;
+  // the dSwiGLU backward reads the saved C (bf16, f16 or f32); it adds no bias
+  // and stores no C of its own
+  if (bwd && (d->want_c || d->want_bias)) return BSGG_ERR_INVALID_ARG;
+  if (bwd && d->saved_c_format != BSGG_OUT_BF16 && d->saved_c_format != BSGG_OUT_F16 &&
+      d->saved_c_format != BSGG_OUT_F32)
+    return BSGG_ERR_INVALID_ARG;
   if (d->want_col && !is_quant(d->out_format)) return BSGG_ERR_INVALID_ARG;
   // NVFP4 inputs: the pages allow 16/32-bit float outputs; FP4 output is this
   // build's reading for the NVFP4 sReLU workload.  FP8 outputs from FP4 inputs
@@ -225,13 +232,17 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
   P->mc = (tm == 128 && cm == 2);
   P->bn = P->pair ? 256 : tn;
   // GeGLU runs in the SwiGLU instances (Params::glu_kind selects the activation)
-  P->epi = desc->epilogue == BSGG_EPI_GEGLU ? bsgg::EPI_SWIGLU : desc->epilogue;
+  P->epi = desc->epilogue == BSGG_EPI_GEGLU     ? bsgg::EPI_SWIGLU
+           : desc->epilogue == BSGG_EPI_DSWIGLU ? bsgg::EPI_DSWIGLU
+                                                : desc->epilogue;
   P->outc = desc->out_format == BSGG_OUT_E2M1 ? bsgg::OUTC_FP4
             : is_quant(desc->out_format)      ? bsgg::OUTC_FP8
                                               : bsgg::OUTC_FLOAT;
   P->sf_vec = desc->in_format == BSGG_IN_NVFP4 ? 16 : 32;
   P->kbytes = desc->in_format == BSGG_IN_NVFP4 ? desc->k / 2 : desc->k;
-  P->n_out = (desc->epilogue == BSGG_EPI_SWIGLU || desc->epilogue == BSGG_EPI_GEGLU) ? desc->n / 2 : desc->n;
+  P->n_out = (desc->epilogue == BSGG_EPI_SWIGLU || desc->epilogue == BSGG_EPI_GEGLU) ? desc->n / 2
+             : desc->epilogue == BSGG_EPI_DSWIGLU                                     ? 2 * desc->n
+                                                                                      : desc->n;
   P->out_row_bytes = P->n_out * out_elem_bits(desc->out_format) / 8;
   if (P->pair || P->mc) {
     int resident = bsgg::cluster_resident_ctas(desc->in_format == BSGG_IN_NVFP4, P->mc);
@@ -266,6 +277,8 @@ bsgg_status check_args(const bsgg_plan* P, const bsgg_args* a) {
     return BSGG_ERR_INVALID_ARG;   // amax required for bf16/f16 D
   }
   if (d.want_bias && (!a->bias || !aligned16(a->bias))) return BSGG_ERR_INVALID_ARG;
+  if (d.epilogue == BSGG_EPI_DSWIGLU && (!a->saved_c || !aligned16(a->saved_c) || !a->beta || !a->dprob))
+    return BSGG_ERR_INVALID_ARG;
   if (d.want_c && (!a->c || !aligned16(a->c))) return BSGG_ERR_INVALID_ARG;
   return BSGG_OK;
 }
@@ -414,7 +427,9 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   std::memset(&L, 0, sizeof(L));
   st = encode_maps(P, a, &L);
   if (st != BSGG_OK) return st;
-  if (a->amax && cudaMemsetAsync(a->amax, 0, sizeof(float) * d.num_groups, s) != cudaSuccess)
+  // amax: one float per group, two for the backward (input / gate gradients)
+  const int64_t n_amax = d.num_groups * (d.epilogue == BSGG_EPI_DSWIGLU ? 2 : 1);
+  if (a->amax && cudaMemsetAsync(a->amax, 0, sizeof(float) * n_amax, s) != cudaSuccess)
     return BSGG_ERR_CUDA;
 
   bsgg::Params& p = L.p;
@@ -454,6 +469,12 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   p.glu_kind = d.epilogue == BSGG_EPI_GEGLU ? 1 : 0;
   p.glu_limit = d.glu_limit;
   p.glu_gamma = d.glu_alpha == 0.0f ? 1.0f : d.glu_alpha;
+  if (d.epilogue == BSGG_EPI_DSWIGLU) {
+    p.saved_c = a->saved_c;
+    p.saved_c_kind = d.saved_c_format;
+    p.beta = a->beta;
+    p.dprob = a->dprob;
+  }
   if (d.discrete_b) {
     p.b_maps = P->maps;
     p.maps_bad = reinterpret_cast<const uint32_t*>(P->maps + 2 * d.num_groups);
@@ -530,6 +551,9 @@ bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* 
   const uint64_t sz_d = uint64_t(d.m_pad) * P->out_row_bytes;
   const uint64_t sz_sfd_row = sf_bytes_impl(d.m_pad, P->n_out, P->sf_vec, 1);
   const uint64_t sz_sfd_col = sf_bytes_impl(P->n_out, d.m_pad, P->sf_vec, 1);
+  const bool bwd = d.epilogue == BSGG_EPI_DSWIGLU;
+  const uint64_t sz_saved_c = bwd ? uint64_t(d.m_pad) * 2 * d.n * (d.saved_c_format == BSGG_OUT_F32 ? 4 : 2) : 0;
+  const uint64_t n_amax = uint64_t(L) * (bwd ? 2 : 1);
   uint64_t in_bytes = 0, out_bytes = 0;
   auto h2d = [&](const void* h, const void* dv, uint64_t n) -> bool {
     if (!h) return true;
@@ -550,14 +574,19 @@ bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* 
             h2d(host->prob, dev->prob, sizeof(float) * d.m_pad) &&
             h2d(host->norm_const, dev->norm_const, sizeof(float)) &&
             h2d(d.want_bias ? host->bias : nullptr, dev->bias,
-                uint64_t(L) * d.n * (d.bias_format == BSGG_OUT_F32 ? 4 : 2));
+                uint64_t(L) * d.n * (d.bias_format == BSGG_OUT_F32 ? 4 : 2)) &&
+            // backward: the saved C and beta in, dprob in (it is accumulated) and out
+            h2d(bwd ? host->saved_c : nullptr, dev->saved_c, sz_saved_c) &&
+            h2d(bwd ? host->beta : nullptr, dev->beta, sizeof(float) * L) &&
+            h2d(bwd ? host->dprob : nullptr, dev->dprob, sizeof(float) * d.m_pad);
   if (!ok) return BSGG_ERR_CUDA;
   bsgg_status st = bsgg_run(P, dev, stream);
   if (st != BSGG_OK) return st;
   ok = d2h(host->d, dev->d, sz_d) && d2h(host->d_col, dev->d_col, d.want_col ? sz_d : 0) &&
        d2h(host->sfd_row, dev->sfd_row, sz_sfd_row) &&
        d2h(host->sfd_col, dev->sfd_col, d.want_col ? sz_sfd_col : 0) &&
-       d2h(host->amax, dev->amax, sizeof(float) * L) &&
+       d2h(host->amax, dev->amax, sizeof(float) * n_amax) &&
+       d2h(bwd ? host->dprob : nullptr, dev->dprob, sizeof(float) * d.m_pad) &&
        d2h(d.want_c ? host->c : nullptr, dev->c, uint64_t(d.m_pad) * d.n * 2);
   if (!ok) return BSGG_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return BSGG_ERR_CUDA;

@@ -54,8 +54,9 @@
 
 namespace bsgg {
 
-// Epilogue instances; EPI_SWIGLU also computes GeGLU (Params::glu_kind).
-enum : int { EPI_GATE = 0, EPI_SWIGLU = 1, EPI_SRELU = 2 };
+// Epilogue instances; EPI_SWIGLU also computes GeGLU (Params::glu_kind);
+// EPI_DSWIGLU is the dSwiGLU backward.
+enum : int { EPI_GATE = 0, EPI_SWIGLU = 1, EPI_SRELU = 2, EPI_DSWIGLU = 3 };
 // Output class (template) and exact output kind (runtime) of D.
 enum : int { OUTC_FLOAT = 0, OUTC_FP8 = 1, OUTC_FP4 = 2 };
 enum : int { OK_BF16 = 0, OK_F16 = 1, OK_F32 = 2, OK_E4M3 = 3, OK_E5M2 = 4, OK_E2M1 = 5 };
@@ -127,6 +128,12 @@ struct Params {
   int32_t glu_kind;         // EPI_SWIGLU instances: 0 = SwiGLU, 1 = GeGLU
   float glu_limit;          // both GLU halves clamped to [-glu_limit, glu_limit]; 0 = none
   float glu_gamma;          // GLU output scale (1 = none)
+  // dSwiGLU backward ("Grouped GEMM + dGLU (SM100)"): the saved forward C
+  // (m_pad, 2N), its per-group scale, and the accumulated dprob (m_pad)
+  const void* saved_c;
+  int32_t saved_c_kind;     // OK_BF16, OK_F16 or OK_F32
+  const float* beta;
+  float* dprob;
   // discrete weight mode: per-expert tensor maps {B_g, SFB_g} (2 per expert, in
   // global memory) and the flag their writer raises for a bad pointer; null in
   // dense mode
@@ -357,6 +364,36 @@ __device__ __forceinline__ void add_bias32(uint32_t* v, const void* src, int kin
   }
 }
 
+// 32 consecutive values (bf16, f16 or f32; 16-byte aligned) read as floats.
+__device__ __forceinline__ void load_f32x32(float (&v)[32], const void* src, int kind) {
+  if (kind == OK_F32) {
+    const float4* b = static_cast<const float4*>(src);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 x = __ldg(b + i);
+      v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
+    }
+  } else {
+    const uint4* b = static_cast<const uint4*>(src);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 x = __ldg(b + i);
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (kind == OK_BF16) {
+          v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+          v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        } else {
+          const __half2 h = *reinterpret_cast<const __half2*>(&w[j]);
+          v[8 * i + 2 * j] = __low2float(h);
+          v[8 * i + 2 * j + 1] = __high2float(h);
+        }
+      }
+    }
+  }
+}
+
 // 32 values of one row -> quantized codes stored at `dst` (32 bytes for FP8,
 // 16 bytes for FP4), each value multiplied by its block's scale first.
 template <int OUTC>
@@ -394,41 +431,12 @@ __device__ __forceinline__ void store_q32(void* dst, const float (&v)[32], const
   }
 }
 
-// Step 2 and Step 3 for one 32-column chunk of one row: C = al * xs (the
-// input half for the GLUs; fp32 bits), al * gs the gate half.  al is alpha_g,
-// or 1 where alpha and the bias were already applied in place.
-template <bool FP4, int EPI, int OUTC>
-__device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* xs, const uint32_t* gs, int row,
-                                               int col0, float al, float pr, float norm, int lane, int kblk_col,
-                                               float& amax_local) {
-  float v[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float c = al * __uint_as_float(xs[i]);
-    if (EPI == EPI_GATE) {
-      v[i] = pr * c;
-    } else if (EPI == EPI_SRELU) {
-      float r = fmaxf(c, 0.0f);
-      if (p.tanh_s > 0.0f) r = p.tanh_s * fminf(tanh_approx(r * p.tanh_rcp_s), 1.0f);
-      v[i] = pr * (r * r);
-    } else {
-      // SwiGLU: X * G * sigmoid(G); GeGLU: (X + 1) * G * sigmoid(1.702 G); both
-      // halves first clamped to [-glu_limit, glu_limit] when a limit is set
-      float x = c, gt = al * __uint_as_float(gs[i]);
-      if (p.glu_limit > 0.0f) {
-        x = fminf(fmaxf(x, -p.glu_limit), p.glu_limit);
-        gt = fminf(fmaxf(gt, -p.glu_limit), p.glu_limit);
-      }
-      if (p.glu_kind) {
-        const float sig = __fdividef(1.0f, 1.0f + __expf(-1.702f * gt));
-        v[i] = pr * (x + 1.0f) * (gt * sig);
-      } else {
-        const float sig = __fdividef(1.0f, 1.0f + __expf(-gt));
-        v[i] = pr * x * (gt * sig);
-      }
-      if (p.glu_gamma != 1.0f) v[i] *= p.glu_gamma;
-    }
-  }
+// Step 3 (or the 16/32-bit store) of one 32-column chunk of D of one row:
+// v[32] at D columns [col0, col0 + 32).  Row blocks of v columns lie inside the
+// chunk; column blocks of v rows span the warp's 32 lanes (its 32 rows).
+template <bool FP4, int OUTC>
+__device__ __forceinline__ void output_chunk(const Params& p, const float (&v)[32], int row, int col0,
+                                             float norm, int lane, int kblk_col, float& amax_local) {
   if (OUTC == OUTC_FLOAT) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) amax_local = fmaxf(amax_local, fabsf(v[i]));
@@ -505,6 +513,44 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* 
       }
     }
   }
+}
+
+// Step 2 and Step 3 for one 32-column chunk of one row: C = al * xs (the
+// input half for the GLUs; fp32 bits), al * gs the gate half.  al is alpha_g,
+// or 1 where alpha and the bias were already applied in place.
+template <bool FP4, int EPI, int OUTC>
+__device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* xs, const uint32_t* gs, int row,
+                                               int col0, float al, float pr, float norm, int lane, int kblk_col,
+                                               float& amax_local) {
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float c = al * __uint_as_float(xs[i]);
+    if (EPI == EPI_GATE) {
+      v[i] = pr * c;
+    } else if (EPI == EPI_SRELU) {
+      float r = fmaxf(c, 0.0f);
+      if (p.tanh_s > 0.0f) r = p.tanh_s * fminf(tanh_approx(r * p.tanh_rcp_s), 1.0f);
+      v[i] = pr * (r * r);
+    } else {
+      // SwiGLU: X * G * sigmoid(G); GeGLU: (X + 1) * G * sigmoid(1.702 G); both
+      // halves first clamped to [-glu_limit, glu_limit] when a limit is set
+      float x = c, gt = al * __uint_as_float(gs[i]);
+      if (p.glu_limit > 0.0f) {
+        x = fminf(fmaxf(x, -p.glu_limit), p.glu_limit);
+        gt = fminf(fmaxf(gt, -p.glu_limit), p.glu_limit);
+      }
+      if (p.glu_kind) {
+        const float sig = __fdividef(1.0f, 1.0f + __expf(-1.702f * gt));
+        v[i] = pr * (x + 1.0f) * (gt * sig);
+      } else {
+        const float sig = __fdividef(1.0f, 1.0f + __expf(-gt));
+        v[i] = pr * x * (gt * sig);
+      }
+      if (p.glu_gamma != 1.0f) v[i] *= p.glu_gamma;
+    }
+  }
+  output_chunk<FP4, OUTC>(p, v, row, col0, norm, lane, kblk_col, amax_local);
 }
 
 // XC: the launch adds a bias to C or stores C (a separate instance, so that the
@@ -964,7 +1010,39 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
         al_epi = 1.0f;
       }
       float amax_local = 0.0f;
-      if (EPI == EPI_SWIGLU) {
+      float amax_local2 = 0.0f;                       // backward: the gate-gradient blocks
+      if (EPI == EPI_DSWIGLU) {
+        // dSwiGLU backward ("Grouped GEMM + dGLU (SM100)", Block-scaled contract):
+        // GEMM column j of pair b = j / 32 -> D (and saved C) columns 64b + r of
+        // the input block and of the gate block, in the forward's block order
+        const float al2 = al * al, bt = p.beta[g];
+        const bool gf = p.gate_first != 0;
+        float dprob_local = 0.0f;
+#pragma unroll
+        for (int c = 0; c < kWarpCols / 32; ++c) {
+          const int j0 = nt * BN + e * kWarpCols + 32 * c;
+          if (j0 >= p.n) continue;
+          const int xo = 2 * j0 + (gf ? 32 : 0), go = 2 * j0 + (gf ? 0 : 32);
+          const int64_t srow = static_cast<int64_t>(row) * 2 * p.n;
+          const int esz = p.saved_c_kind == OK_F32 ? 4 : 2;
+          float x[32], gv[32];
+          load_f32x32(x, static_cast<const uint8_t*>(p.saved_c) + (srow + xo) * esz, p.saved_c_kind);
+          load_f32x32(gv, static_cast<const uint8_t*>(p.saved_c) + (srow + go) * esz, p.saved_c_kind);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float ref = al2 * __uint_as_float(r[32 * c + i]);
+            const float X = bt * x[i], G = bt * gv[i];
+            const float sg = __fdividef(1.0f, 1.0f + __expf(-G));
+            const float sw = G * sg;
+            dprob_local += X * sw * ref;                              // dprob += X swish(G) ref
+            x[i] = ref * pr * sw;                                     // d input
+            gv[i] = ref * pr * X * sg * (1.0f + G * (1.0f - sg));     // d gate
+          }
+          output_chunk<FP4, OUTC>(p, x, row, xo, norm, lane, kblk_col, amax_local);
+          output_chunk<FP4, OUTC>(p, gv, row, go, norm, lane, kblk_col, amax_local2);
+        }
+        atomicAdd(p.dprob + row, dprob_local);
+      } else if (EPI == EPI_SWIGLU) {
         const bool gf = p.gate_first != 0;
 #pragma unroll
         for (int j = 0; j < kWarpCols / 64; ++j) {
@@ -988,9 +1066,18 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
         }
       }
       if (OUTC == OUTC_FLOAT && p.amax != nullptr) {
+        // backward: amax[2g] over the input-gradient blocks, amax[2g + 1] over
+        // the gate-gradient blocks
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax_local = fmaxf(amax_local, __shfl_xor_sync(0xffffffffu, amax_local, o));
-        if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(p.amax) + g, __float_as_uint(amax_local));
+        const int ai = EPI == EPI_DSWIGLU ? 2 * g : g;
+        if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(p.amax) + ai, __float_as_uint(amax_local));
+        if (EPI == EPI_DSWIGLU) {
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1)
+            amax_local2 = fmaxf(amax_local2, __shfl_xor_sync(0xffffffffu, amax_local2, o));
+          if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(p.amax) + ai + 1, __float_as_uint(amax_local2));
+        }
       }
     }
   }

@@ -38,7 +38,8 @@
  *      SFB      swizzled SF(N, K) per expert   (bsgg_sf_bytes(N, K, v, L) bytes)
  *      padded_offsets int32 (L), alpha float (L), prob float (m_pad),
  *      norm_const float (1)
- *      D, D_col (m_pad, N_out)  N-major; N_out = N/2 for SWIGLU/GEGLU, else N;
+ *      D, D_col (m_pad, N_out)  N-major; N_out = N/2 for SWIGLU/GEGLU, 2N for
+ *                               DSWIGLU, else N;
  *                               bf16/f16/f32, or 1-byte FP8 codes, or packed FP4
  *      C        (m_pad, N)      N-major, bf16/f16 (optional pre-activation output)
  *      bias     (L, N)          N contiguous, bf16/f16/f32 (optional)
@@ -97,15 +98,21 @@ typedef enum {
 
 /* Epilogues: gating ("Grouped GEMM + Quant (SM100)", Step 2), SwiGLU ("Grouped GEMM +
  * SwiGLU (SM100)", Step 2), squared ReLU with optional tanh soft clamp ("Grouped GEMM +
- * sReLU (SM100)"), GeGLU ("Grouped GEMM + GLU + Hadamard + Quant (SM100)", Equations). */
-typedef enum { BSGG_EPI_GATE = 0, BSGG_EPI_SWIGLU = 1, BSGG_EPI_SRELU = 2, BSGG_EPI_GEGLU = 3 } bsgg_epilogue;
+ * sReLU (SM100)"), GeGLU ("Grouped GEMM + GLU + Hadamard + Quant (SM100)", Equations),
+ * and the dSwiGLU backward ("Grouped GEMM + dGLU (SM100)", Block-scaled contract):
+ *   ref = alpha_g^2 * sum_k A B;  X, G = beta_g * the saved forward C's input and gate
+ *   32-column blocks;  D = [ref*prob*swish(G) | ref*prob*X*sigmoid(G)*(1 + G*(1 - sigmoid(G)))]
+ *   in C's block order (width 2N);  dprob[m] += sum_n X*swish(G)*ref. */
+typedef enum {
+  BSGG_EPI_GATE = 0, BSGG_EPI_SWIGLU = 1, BSGG_EPI_SRELU = 2, BSGG_EPI_GEGLU = 3, BSGG_EPI_DSWIGLU = 4
+} bsgg_epilogue;
 
 /* Problem description, fixed at plan creation (the pages' constructor +
  * check_support + compile, "Grouped GEMM + Quant (SM100)", Class API). */
 typedef struct {
   int64_t m_pad;          /* rows of A/D/prob = padded_offsets[L-1]; multiple of 128 */
   int64_t n;              /* GEMM N (rows of each expert's B); multiple of 32 (64 for SWIGLU
-                             and GEGLU) */
+                             and GEGLU); for DSWIGLU the compact gradient width (D is 2N wide) */
   int64_t k;              /* reduction length in elements; multiple of 16 (FP8) / 32 (FP4) */
   int32_t num_groups;     /* L, 1..1024 */
   int32_t in_format;      /* bsgg_in_format */
@@ -149,6 +156,9 @@ typedef struct {
      of device memory for one TMA descriptor pair per expert, written by a small
      kernel on the stream before every launch. */
   int32_t discrete_b;
+  /* DSWIGLU: storage type of the saved forward C, BSGG_OUT_BF16, BSGG_OUT_F16 or
+     BSGG_OUT_F32 ("Grouped GEMM + dGLU (SM100)", BF16 contract: C in BF16/FP16/FP32). */
+  int32_t saved_c_format;
 } bsgg_desc;
 
 /* Tensors of one call.  Unused outputs may be NULL: d_col/sfd_col unless
@@ -178,6 +188,14 @@ typedef struct {
      BSGG_ERR_BAD_POINTERS from bsgg_query_device_status, and nothing is written). */
   const int64_t* b_ptrs;
   const int64_t* sfb_ptrs;
+  /* DSWIGLU only: the saved forward C (m_pad, 2N) N-major in saved_c_format, its
+     per-group scale beta (L), and dprob (m_pad), which the kernel ACCUMULATES into:
+     zero it before the call ("Grouped GEMM + dGLU (SM100)": dprob must be
+     zero-initialized).  amax then holds 2L floats: [2g] over the input-gradient
+     blocks, [2g + 1] over the gate-gradient blocks of group g. */
+  const void* saved_c;
+  const float* beta;
+  float* dprob;
 } bsgg_args;
 
 typedef struct bsgg_plan bsgg_plan;

@@ -47,7 +47,7 @@ def alloc_outputs(plan: bsgg.Plan, device="cuda") -> dict:
     out = {}
     for name, nbytes in plan.output_bytes().items():
         if name == "amax":
-            out[name] = torch.full((plan.desc.num_groups,), -1.0, dtype=torch.float32, device=device)
+            out[name] = torch.full((nbytes // 4,), -1.0, dtype=torch.float32, device=device)
         else:
             out[name] = torch.full((nbytes,), SENTINEL, dtype=torch.uint8, device=device)
     return out

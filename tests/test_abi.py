@@ -104,6 +104,11 @@ def _create(**over):
     (dict(bias_format="e4m3"), 1), (dict(bias_format_code=9), 1),
     (dict(want_c_raw=2), 1),
     (dict(discrete_raw=2), 1),
+    (dict(epilogue="dswiglu", c_format="bf16"), 1),      # the backward stores no C
+    (dict(epilogue="dswiglu", bias_format="f32"), 1),    # and adds no bias
+    (dict(epilogue="dswiglu", saved_c_format="e4m3"), 1),
+    (dict(epilogue="dswiglu", n=80), 1),
+    (dict(epilogue="dswiglu", tanh_clamp_s=4.0), 1),
 ])
 def test_create_rejects(lib, over, code):
     assert _create(**over) == code
@@ -115,6 +120,7 @@ def test_create_rejects(lib, over, code):
     dict(epilogue="srelu", glu_alpha=0.0, c_format="f16", bias_format="bf16"),
     dict(epilogue="gate", bias_format="f16"),
     dict(discrete_b=True, num_groups=1024),
+    dict(epilogue="dswiglu", n=96, saved_c_format="f32", out_format="e4m3", want_col=1),
 ])
 def test_create_accepts_epilogue_options(lib, over):
     # validation passes: 0 with a GPU, else the device query that follows
