@@ -37,8 +37,9 @@ class OrcDesc(ctypes.Structure):
         ("m_pad", ctypes.c_int64), ("n", ctypes.c_int64), ("k", ctypes.c_int64),
         ("num_groups", ctypes.c_int64),
         ("in_fmt", ctypes.c_int32), ("out_fmt", ctypes.c_int32), ("epi", ctypes.c_int32),
-        ("gate_first", ctypes.c_int32), ("want_col", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("gate_first", ctypes.c_int32), ("want_col", ctypes.c_int32), ("rht", ctypes.c_int32),
         ("tanh_clamp_s", ctypes.c_double), ("glu_limit", ctypes.c_double), ("glu_alpha", ctypes.c_double),
+        ("rht_norm", ctypes.c_double),
     ]
 
 
@@ -83,7 +84,11 @@ def lib():
         L.orc_group_of_row.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64]
         L.orc_run.restype = ctypes.c_int
         L.orc_run.argtypes = [ctypes.POINTER(OrcDesc)] + [ctypes.c_void_p] * 10 + [
-            ctypes.c_float, ctypes.c_void_p, ctypes.c_int64] + [ctypes.c_void_p] * 8 + [ctypes.c_int]
+            ctypes.c_float, ctypes.c_void_p, ctypes.c_int64] + [ctypes.c_void_p] * 11 + [ctypes.c_int]
+        L.orc_round_bf16.restype = ctypes.c_double
+        L.orc_round_bf16.argtypes = [ctypes.c_double]
+        L.orc_hadamard16.restype = ctypes.c_double
+        L.orc_hadamard16.argtypes = [ctypes.c_int, ctypes.c_int]
         _lib = L
     return _lib
 
@@ -137,6 +142,14 @@ def group_of_row(offsets: np.ndarray, m: int) -> int:
     return lib().orc_group_of_row(_ptr(off), off.size, m)
 
 
+def round_bf16(x: float) -> float:
+    return float(lib().orc_round_bf16(float(x)))
+
+
+def hadamard16(i: int, j: int) -> float:
+    return float(lib().orc_hadamard16(int(i), int(j)))
+
+
 def n_out(n: int, epi: int) -> int:
     if epi in (EPI_SWIGLU, EPI_GEGLU):
         return n // 2
@@ -146,7 +159,7 @@ def n_out(n: int, epi: int) -> int:
 def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded_offsets,
         alpha, prob, norm_const=1.0, tanh_clamp_s=0.0, gate_first=0, want_col=False,
         blocks=None, threads=None, outputs=None, bias=None, glu_limit=0.0, glu_alpha=1.0,
-        want_c=False, saved_c=None, beta=None):
+        want_c=False, saved_c=None, beta=None, rht=None, rht_norm=1.0):
     """Run the oracle on the listed 32-row blocks (default: all of them).
 
     Inputs are numpy arrays in the device layouts: ``a`` (m_pad, k or k/2)
@@ -162,10 +175,15 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     forward C (any float dtype, widened to fp64) and ``beta`` float32 (L,), and
     adds ``dprob_ref`` (fp64, rows of the listed blocks); its ``amax`` has 2L
     entries (input-gradient and gate-gradient blocks of each group).
+    ``rht`` ("bf16" or "e2m1") adds the rowwise Hadamard output: ``rht_ref``
+    (fp64) and, for "e2m1", full-size ``rht_q`` / ``sfrht`` buffers (E4M3
+    scales per 16 under ``rht_norm``).
     """
     L = lib()
+    rht_code = {None: 0, "bf16": 1, "e2m1": 2}[rht]
     desc = OrcDesc(m_pad, n, k, num_groups, in_fmt, out_fmt, epi, int(gate_first),
-                   int(bool(want_col)), 0, float(tanh_clamp_s), float(glu_limit), float(glu_alpha))
+                   int(bool(want_col)), rht_code, float(tanh_clamp_s), float(glu_limit), float(glu_alpha),
+                   float(rht_norm))
     nd = n_out(n, epi)
     if blocks is None:
         blocks = np.arange(m_pad // 32, dtype=np.int64)
@@ -176,10 +194,14 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     c_ref = np.zeros((blocks.size * 32, n), dtype=np.float64) if want_c else None
     bias_arr = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32).reshape(num_groups, n)
     amax = np.zeros(2 * num_groups if epi == EPI_DSWIGLU else num_groups, dtype=np.float32)
+    rht_ref = np.zeros((blocks.size * 32, nd), dtype=np.float64) if rht_code else None
     dprob_ref = np.zeros(blocks.size * 32, dtype=np.float64) if epi == EPI_DSWIGLU else None
     saved_arr = None if saved_c is None else np.ascontiguousarray(saved_c, dtype=np.float64).reshape(m_pad, 2 * n)
     beta_arr = None if beta is None else np.ascontiguousarray(beta, dtype=np.float32).reshape(num_groups)
     outs = dict(outputs or {})
+    if rht_code == 2:
+        outs.setdefault("rht_q", np.zeros((m_pad, nd // 2), dtype=np.uint8))
+        outs.setdefault("sfrht", np.zeros(sf_bytes(m_pad, -(-nd // 16), 1), dtype=np.uint8))
     quant = out_fmt >= OUT_E4M3
     v = 16 if in_fmt == IN_NVFP4 else 32
     if quant:
@@ -201,7 +223,7 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
                    _ptr(bias_arr), _ptr(saved_arr), _ptr(beta_arr), float(norm_const), _ptr(blocks),
                    blocks.size, _ptr(d_ref), _ptr(c_ref), _ptr(dprob_ref), _ptr(outs.get("d")),
                    _ptr(outs.get("d_col")), _ptr(outs.get("sfd_row")), _ptr(outs.get("sfd_col")),
-                   _ptr(amax), int(threads))
+                   _ptr(amax), _ptr(rht_ref), _ptr(outs.get("rht_q")), _ptr(outs.get("sfrht")), int(threads))
     if rc != 0:
         raise ValueError(f"oracle rejected the problem (code {rc})")
     res = {"d_ref": d_ref, "amax": amax, "blocks": blocks}
@@ -209,5 +231,7 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
         res["c_ref"] = c_ref
     if dprob_ref is not None:
         res["dprob_ref"] = dprob_ref
+    if rht_ref is not None:
+        res["rht_ref"] = rht_ref
     res.update(outs)
     return res

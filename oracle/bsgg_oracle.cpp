@@ -170,13 +170,16 @@ extern "C" {
 
 typedef struct {
   int64_t m_pad, n, k, num_groups;
-  int32_t in_fmt, out_fmt, epi, gate_first, want_col, reserved;
+  // rht: the rowwise Hadamard output of "Grouped GEMM + GLU + Hadamard + Quant
+  // (SM100)" (0 = none, 1 = bf16, 2 = NVFP4 with E4M3 scales per 16)
+  int32_t in_fmt, out_fmt, epi, gate_first, want_col, rht;
   double tanh_clamp_s;   // 0 = no clamp
   // "Grouped GEMM + GLU + Hadamard + Quant (SM100)", Equations: both GLU
   // halves clamped to [-glu_limit, glu_limit] (0 = no clamp) and the GLU
   // output scaled by gamma = glu_alpha (1 = none); SwiGLU and GeGLU only.
   double glu_limit;
   double glu_alpha;
+  double rht_norm;       // global encode scale of an NVFP4 RHT output (rht_norm_const)
 } orc_desc;
 
 // ---- exported helpers (pinned individually by the tests) ----
@@ -211,6 +214,28 @@ double orc_srelu(double c, double s) {
   return r * r;
 }
 
+// Round to the nearest bfloat16 value, ties to even (1 sign, 8 exponent, 7
+// stored mantissa bits: 8 significant bits for normal values, a fixed quantum
+// of 2^-133 below 2^-126).  "Grouped GEMM + GLU + Hadamard + Quant (SM100)",
+// Equations: the RHT transforms bf16-rounded D.
+double orc_round_bf16(double x) {
+  if (x == 0.0 || !std::isfinite(x)) return x;
+  int p;
+  std::frexp(x, &p);                          // |x| in [2^(p-1), 2^p)
+  const int q = std::max(p - 8, -133);        // exponent of the last kept bit
+  const double r = std::nearbyint(std::ldexp(x, -q));   // default rounding: to nearest, ties even
+  const double y = std::ldexp(r, q);
+  return std::fabs(y) > 3.3895313892515355e38 ? std::copysign(INFINITY, y) : y;
+}
+// Entry (i, j) of the 16 x 16 Sylvester Hadamard matrix, (-1)^popcount(i & j);
+// the pages' "fixed 16-wide orthonormal Hadamard transform" is this matrix / 4
+// (reading: Sylvester order, no random signs).
+double orc_hadamard16(int i, int j) {
+  int c = i & j, bits = 0;
+  while (c) { bits += c & 1; c >>= 1; }
+  return (bits % 2) ? -1.0 : 1.0;
+}
+
 // Which group owns row m: the g with padded_offsets[g-1] <= m < padded_offsets[g]
 // ("Grouped GEMM + Quant (SM100)", Equations, Step 1).  -1 if none.
 int64_t orc_group_of_row(const int32_t* off, int64_t L, int64_t m) {
@@ -233,6 +258,11 @@ int64_t orc_group_of_row(const int32_t* off, int64_t L, int64_t m) {
 //   c_ref    [nblocks*32, n] fp64 C (GEMM plus bias, before any clamp or
 //            activation) when not NULL
 // `bias` (L x n, bias[g*n + col]) is added to C when not NULL.
+// The rowwise RHT (P->rht != 0; "Grouped GEMM + GLU + Hadamard + Quant
+// (SM100)", Equations): every 16-column block x of bf16-rounded D becomes
+// y = (H16 / 4) x, written to rht_ref [nblocks*32, n_d] (fp64) and, for NVFP4,
+// quantized into rht_q (packed E2M1, full size) with E4M3 scales per 16 in
+// sfrht (swizzled SF(m_pad, n_d)) under rht_norm.
 // The dSwiGLU backward (epi = EPI_DSWIGLU, "Grouped GEMM + dGLU (SM100)",
 // Block-scaled contract, Steps 1-3) also takes
 //   saved_c  [m_pad, 2n] fp64 values of the saved forward C (its input and gate
@@ -247,7 +277,7 @@ int orc_run(const orc_desc* P, const uint8_t* A, const uint8_t* SFA, const uint8
             const float* prob, const float* bias, const double* saved_c, const float* beta,
             float norm_const, const int64_t* blocks, int64_t nblocks, double* d_ref, double* c_ref,
             double* dprob_ref, uint8_t* d_q, uint8_t* d_col_q, uint8_t* sfd_row, uint8_t* sfd_col,
-            float* amax, int threads);
+            float* amax, double* rht_ref, uint8_t* rht_q, uint8_t* sfrht, int threads);
 
 }  // extern "C"
 
@@ -260,6 +290,8 @@ struct Job {
   const double* saved_c;
   const float* beta;
   double* dprob_ref;
+  double* rht_ref;
+  uint8_t *rht_q, *sfrht;
   const uint8_t *A, *SFA, *B, *SFB;
   const int32_t* off;
   const float *alpha, *prob;
@@ -467,6 +499,43 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
     }
   }
 
+  // Rowwise RHT of the bf16-rounded D, block by block of 16 columns.
+  if (P->rht) {
+    const int64_t kb16 = (nd + 15) / 16;
+    for (int64_t i = 0; i < 32; ++i) {
+      if (grp[size_t(i)] < 0) continue;
+      const int64_t m = m0 + i;
+      for (int64_t jb = j0; jb < j1; jb += 16) {
+        double x[16], y[16];
+        for (int t = 0; t < 16; ++t) x[t] = orc_round_bf16(D[size_t(i * w + (jb - j0) + t)]);
+        for (int r = 0; r < 16; ++r) {
+          double acc = 0.0;
+          for (int t = 0; t < 16; ++t) acc += orc_hadamard16(r, t) * x[t];
+          y[r] = acc / 4.0;
+        }
+        for (int t = 0; t < 16; ++t) J.rht_ref[size_t((bi * 32 + i) * nd + jb + t)] = y[t];
+        if (P->rht == 2 && J.rht_q) {
+          // the Step-3 quantization with E4M3 scales per 16 and q_max 6 under
+          // rht_norm (SFRHT is E4M3 whatever the input scale type)
+          float am = 0.0f;
+          for (int t = 0; t < 16; ++t) am = std::max(am, std::fabs(float(y[t])));
+          const float norm = float(P->rht_norm);
+          const float sf = (norm * am) * float(1.0 / 6.0);
+          const uint32_t code = encode_rne_satfinite(F_E4M3, sf);
+          const float sfd = float(decode(F_E4M3, code));
+          const float scale = (am == 0.0f || sfd == 0.0f) ? 0.0f : norm / sfd;
+          J.sfrht[sf_offset(m, jb / 16, 0, P->m_pad, kb16)] = uint8_t(code);
+          for (int t = 0; t < 16; ++t) {
+            const uint32_t c = encode_rne_satfinite(F_E2M1, float(y[t]) * scale);
+            uint8_t& byte = J.rht_q[m * (nd / 2) + (jb + t) / 2];
+            if ((jb + t) % 2 == 0) byte = uint8_t((byte & 0xF0) | (c & 0xF));
+            else byte = uint8_t((byte & 0x0F) | ((c & 0xF) << 4));
+          }
+        }
+      }
+    }
+  }
+
   // Step 3: output quantization (row blocks and column blocks of v values).
   if (out_quantized(P)) {
     const int fmt = out_code_fmt(P);
@@ -520,11 +589,12 @@ extern "C" int orc_run(const orc_desc* P, const uint8_t* A, const uint8_t* SFA, 
                        const float* prob, const float* bias, const double* saved_c, const float* beta,
                        float norm_const, const int64_t* blocks, int64_t nblocks, double* d_ref, double* c_ref,
                        double* dprob_ref, uint8_t* d_q, uint8_t* d_col_q, uint8_t* sfd_row, uint8_t* sfd_col,
-                       float* amax, int threads) {
+                       float* amax, double* rht_ref, uint8_t* rht_q, uint8_t* sfrht, int threads) {
   if (!P || P->m_pad <= 0 || P->m_pad % 32 || P->n <= 0 || P->k <= 0 || P->num_groups <= 0)
     return -1;
   if (is_glu(P) && P->n % 64) return -2;
   if (is_bwd(P) && (P->n % 32 || !saved_c || !beta || bias)) return -4;
+  if (P->rht && (is_bwd(P) || !rht_ref || (P->rht == 2 && (!rht_q || !sfrht)))) return -5;
   if (is_fp4_in(P) && P->k % 2) return -3;
   const int64_t nd = n_out(P);
   // One work item per (block, 128-column slice of D); slices are multiples of
@@ -533,6 +603,7 @@ extern "C" int orc_run(const orc_desc* P, const uint8_t* A, const uint8_t* SFA, 
   Job J;
   J.P = P; J.bias = bias; J.c_ref = c_ref; J.A = A; J.SFA = SFA; J.B = B; J.SFB = SFB; J.off = padded_offsets;
   J.saved_c = saved_c; J.beta = beta; J.dprob_ref = dprob_ref;
+  J.rht_ref = rht_ref; J.rht_q = rht_q; J.sfrht = sfrht;
   J.alpha = alpha; J.prob = prob; J.norm = norm_const; J.blocks = blocks; J.nblocks = nblocks;
   J.d_ref = d_ref; J.d_q = d_q; J.d_col_q = d_col_q; J.sfd_row = sfd_row; J.sfd_col = sfd_col;
   J.amax.assign(size_t(is_bwd(P) ? 2 * P->num_groups : P->num_groups), 0.0f);
