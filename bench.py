@@ -192,8 +192,11 @@ def oracle_inputs(p):
     """Host copies of a problem's inputs with the oracle's own scale packing."""
     import oracle as orc
     np_ = lambda t: t.detach().cpu().contiguous().numpy()
-    return dict(a=np_(p.a), b=np_(p.b), sfa=orc.pack_sf(np_(p.sfa_rows)), sfb=orc.pack_sf(np_(p.sfb_rows)),
-                padded_offsets=np_(p.padded_offsets), alpha=np_(p.alpha), prob=np_(p.prob))
+    ins = dict(a=np_(p.a), b=np_(p.b), sfa=orc.pack_sf(np_(p.sfa_rows)), sfb=orc.pack_sf(np_(p.sfb_rows)),
+               padded_offsets=np_(p.padded_offsets), alpha=np_(p.alpha), prob=np_(p.prob))
+    if p.epi == "dswiglu":
+        ins.update(saved_c=np_(p.saved_c.double()), beta=np_(p.beta))
+    return ins
 
 
 def oracle_sample(p, ins, budget_s: float, max_blocks: int = 64, seed: int = 0):
@@ -203,7 +206,8 @@ def oracle_sample(p, ins, budget_s: float, max_blocks: int = 64, seed: int = 0):
     code_in = {"mxfp8_e4m3": orc.IN_MXFP8_E4M3, "mxfp8_e5m2": orc.IN_MXFP8_E5M2, "nvfp4": orc.IN_NVFP4}
     code_out = {"bf16": orc.OUT_BF16, "f16": orc.OUT_F16, "f32": orc.OUT_F32, "e4m3": orc.OUT_E4M3,
                 "e5m2": orc.OUT_E5M2, "e2m1": orc.OUT_E2M1}
-    code_epi = {"gate": orc.EPI_GATE, "swiglu": orc.EPI_SWIGLU, "srelu": orc.EPI_SRELU, "geglu": orc.EPI_GEGLU}
+    code_epi = {"gate": orc.EPI_GATE, "swiglu": orc.EPI_SWIGLU, "srelu": orc.EPI_SRELU, "geglu": orc.EPI_GEGLU,
+                "dswiglu": orc.EPI_DSWIGLU}
     off = ins["padded_offsets"]
     starts = np.concatenate([[0], off[:-1]])
     real_blocks = np.unique(np.concatenate(
@@ -236,7 +240,8 @@ def make_workload(name: str, device):
 
 def algorithmic_bytes(p) -> int:
     """Bytes a launch must move at least: A, SFA, the B and SFB slices of the
-    non-empty groups, and the outputs (D, D_col, SFD_row, SFD_col or amax)."""
+    non-empty groups, and the outputs (D, D_col, SFD_row, SFD_col or amax);
+    for the dSwiGLU backward also the saved C read and dprob written."""
     def cdiv(a, b):
         return -(-a // b)
 
@@ -254,8 +259,12 @@ def algorithmic_bytes(p) -> int:
     if p.out_fmt in ("e4m3", "e5m2", "e2m1"):
         out += sfb(p.m_pad, n_out, v) + (sfb(n_out, p.m_pad, v) if p.want_col else 0)
     else:
-        out += 4 * p.num_groups
-    return (p.m_pad * kb + sfb(p.m_pad, p.k, v) + nonempty * p.n * kb + sfb(p.n, p.k, v, nonempty) + out)
+        out += 4 * p.num_groups * (2 if p.epi == "dswiglu" else 1)
+    extra = 0
+    if p.epi == "dswiglu":
+        extra = p.saved_c.numel() * p.saved_c.element_size() + 4 * p.m_pad + 4 * p.num_groups
+    return (p.m_pad * kb + sfb(p.m_pad, p.k, v) + nonempty * p.n * kb + sfb(p.n, p.k, v, nonempty) + out
+            + extra)
 
 
 def config_of(p, extra=None):
@@ -322,12 +331,17 @@ def run_gpu(args, world, rank, local):
     outs = {}
     for name, nbytes in plan.output_bytes().items():
         if name == "amax":
-            outs[name] = torch.zeros(p.num_groups, dtype=torch.float32, device=dev)
+            outs[name] = torch.zeros(nbytes // 4, dtype=torch.float32, device=dev)
         else:
             outs[name] = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
     norm = torch.tensor([p.norm_const], dtype=torch.float32, device=dev)
     tensors = dict(a=p.a, sfa=sfa, b=p.b, sfb=sfb, padded_offsets=p.padded_offsets, alpha=p.alpha,
                    prob=p.prob, norm_const=norm, **outs)
+    if p.epi == "dswiglu":
+        # the backward's saved C and beta, and dprob (accumulated across steps:
+        # the timing does not depend on its values)
+        tensors.update(saved_c=p.saved_c, beta=p.beta,
+                       dprob=torch.zeros(p.m_pad, dtype=torch.float32, device=dev))
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(args.warmup):
@@ -387,10 +401,12 @@ def run_gpu(args, world, rank, local):
         host = {}
         for k_, t in tensors.items():
             host[k_] = torch.empty(t.shape, dtype=t.dtype).pin_memory()
-        for k_ in ("a", "sfa", "b", "sfb", "padded_offsets", "alpha", "prob", "norm_const"):
-            host[k_].copy_(tensors[k_].cpu())
+        for k_ in ("a", "sfa", "b", "sfb", "padded_offsets", "alpha", "prob", "norm_const", "saved_c",
+                   "beta", "dprob"):
+            if k_ in tensors:
+                host[k_].copy_(tensors[k_].cpu())
         dev_bufs = dict(tensors)
-        resident = ("b", "sfb", "alpha")
+        resident = ("b", "sfb", "alpha", "beta")
         host_layer = {k_: v for k_, v in host.items() if k_ not in resident}
         n_e2e = max(3, min(args.steps, 10))
 

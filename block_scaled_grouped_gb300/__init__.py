@@ -42,7 +42,8 @@ class Desc(ctypes.Structure):
                 ("glu_limit", ctypes.c_float), ("glu_alpha", ctypes.c_float),
                 ("want_c", ctypes.c_int32), ("c_format", ctypes.c_int32),
                 ("want_bias", ctypes.c_int32), ("bias_format", ctypes.c_int32),
-                ("discrete_b", ctypes.c_int32), ("saved_c_format", ctypes.c_int32)]
+                ("discrete_b", ctypes.c_int32), ("saved_c_format", ctypes.c_int32),
+                ("want_rht", ctypes.c_int32), ("rht_format", ctypes.c_int32)]
 
 
 def make_desc(*, m_pad: int, n: int, k: int, num_groups: int, in_format: str, out_format: str,
@@ -50,24 +51,25 @@ def make_desc(*, m_pad: int, n: int, k: int, num_groups: int, in_format: str, ou
               tanh_clamp_s: float = 0.0, tile=(0, 0), cluster=(0, 0), glu_limit: float = 0.0,
               glu_alpha: float = 0.0, c_format: Optional[str] = None,
               bias_format: Optional[str] = None, discrete_b: bool = False,
-              saved_c_format: str = "bf16") -> "Desc":
+              saved_c_format: str = "bf16", rht_format: Optional[str] = None) -> "Desc":
     """A bsgg_desc.  c_format ("bf16"/"f16") asks for the pre-activation C
     output, bias_format ("bf16"/"f16"/"f32") for a bias; None = neither.
     discrete_b: per-expert weights through the b_ptrs / sfb_ptrs arrays.
-    saved_c_format: storage type of the saved C read by the dSwiGLU backward."""
+    saved_c_format: storage type of the saved C read by the dSwiGLU backward.
+    rht_format ("bf16"/"e2m1"): the rowwise Hadamard output; None = none."""
     return Desc(m_pad, n, k, num_groups, IN_FORMATS[in_format], OUT_FORMATS[out_format],
                 EPILOGUES[epilogue], int(bool(want_col)), int(bool(gate_first)), float(tanh_clamp_s),
                 int(tile[0]), int(tile[1]), int(cluster[0]), int(cluster[1]), float(glu_limit),
                 float(glu_alpha), int(c_format is not None), OUT_FORMATS[c_format or "bf16"],
                 int(bias_format is not None), OUT_FORMATS[bias_format or "bf16"], int(bool(discrete_b)),
-                OUT_FORMATS[saved_c_format])
+                OUT_FORMATS[saved_c_format], int(rht_format is not None), OUT_FORMATS[rht_format or "bf16"])
 
 
 class Args(ctypes.Structure):
     _fields_ = [(name, ctypes.c_void_p) for name in (
         "a", "sfa", "b", "sfb", "padded_offsets", "alpha", "prob", "norm_const",
         "d", "d_col", "sfd_row", "sfd_col", "amax", "bias", "c", "b_ptrs", "sfb_ptrs", "saved_c", "beta",
-        "dprob")]
+        "dprob", "rht", "sfrht", "rht_norm_const")]
 
 
 _lib = None
@@ -174,6 +176,7 @@ class Plan:
         self.in_format, self.out_format, self.epilogue = kw["in_format"], kw["out_format"], kw["epilogue"]
         self.want_col = bool(kw.get("want_col", False))
         self.c_format = kw.get("c_format")
+        self.rht_format = kw.get("rht_format")
         h = ctypes.c_void_p()
         _check(lib().bsgg_create(ctypes.byref(self.desc), ctypes.byref(h)), "bsgg_create")
         self._h = h
@@ -210,6 +213,11 @@ class Plan:
             out["amax"] = 4 * d.num_groups * (2 if self.epilogue == "dswiglu" else 1)
         if self.c_format is not None:
             out["c"] = d.m_pad * d.n * 2
+        if self.rht_format == "bf16":
+            out["rht"] = d.m_pad * self.n_out * 2
+        elif self.rht_format == "e2m1":
+            out["rht"] = d.m_pad * self.n_out // 2
+            out["sfrht"] = sf_bytes(d.m_pad, self.n_out, 16, 1)
         return out
 
     # calls ---------------------------------------------------------------
@@ -267,7 +275,7 @@ def measure_mma_peak(in_format: str, tile_n: int = 256, mmas_per_sm: int = 40000
 
 _DESC_KEYS = ("m_pad", "n", "k", "num_groups", "in_format", "out_format", "epilogue", "want_col",
               "gate_first", "tanh_clamp_s", "tile", "cluster", "glu_limit", "glu_alpha", "c_format",
-              "bias_format", "discrete_b", "saved_c_format")
+              "bias_format", "discrete_b", "saved_c_format", "rht_format")
 
 
 def run_noalloc(*, stream=None, wait_status: bool = True, **kw) -> int:

@@ -135,6 +135,10 @@ bsgg_status validate(const bsgg_desc* d) {
   if (bwd && d->saved_c_format != BSGG_OUT_BF16 && d->saved_c_format != BSGG_OUT_F16 &&
       d->saved_c_format != BSGG_OUT_F32)
     return BSGG_ERR_INVALID_ARG;
+  // the Hadamard output: bf16 or NVFP4, forward epilogues only
+  if (d->want_rht != 0 && d->want_rht != 1) return BSGG_ERR_INVALID_ARG;
+  if (d->want_rht && ((d->rht_format != BSGG_OUT_BF16 && d->rht_format != BSGG_OUT_E2M1) || bwd))
+    return BSGG_ERR_INVALID_ARG;
   if (d->want_col && !is_quant(d->out_format)) return BSGG_ERR_INVALID_ARG;
   // NVFP4 inputs: the pages allow 16/32-bit float outputs; FP4 output is this
   // build's reading for the NVFP4 sReLU workload.  FP8 outputs from FP4 inputs
@@ -224,9 +228,15 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
   // MXFP8 (half the shared-memory operand traffic per MMA of 1-CTA tiles),
   // 128 x 256 single-CTA tiles for NVFP4 (a pair copies each CTA's scale
   // atoms with every stage and gains nothing there)
+  // The dSwiGLU backward writes four outputs per accumulator value and reads
+  // two saved values: with 128-column tiles its epilogue holds half the
+  // accumulator columns per thread and runs without register spills (measured
+  // on GB300: 1418 TFLOP/s on the FC1 backward against 582 with 256 x 256
+  // pairs, whose epilogue spills to local memory).
+  const bool bwd = desc->epilogue == BSGG_EPI_DSWIGLU;
   int tm = desc->tile_m, tn = desc->tile_n, cm = desc->cluster_m;
-  if (tm == 0) tm = (desc->in_format != BSGG_IN_NVFP4 && tn != 128 && cm != 1) ? 256 : 128;
-  if (tn == 0) tn = 256;
+  if (tm == 0) tm = (desc->in_format != BSGG_IN_NVFP4 && tn != 128 && cm != 1 && !bwd) ? 256 : 128;
+  if (tn == 0) tn = (bwd && tm == 128 && cm != 2) ? 128 : 256;
   if (cm == 0) cm = (tm == 256) ? 2 : 1;
   P->pair = (tm == 256);
   P->mc = (tm == 128 && cm == 2);
@@ -278,6 +288,9 @@ bsgg_status check_args(const bsgg_plan* P, const bsgg_args* a) {
   }
   if (d.want_bias && (!a->bias || !aligned16(a->bias))) return BSGG_ERR_INVALID_ARG;
   if (d.epilogue == BSGG_EPI_DSWIGLU && (!a->saved_c || !aligned16(a->saved_c) || !a->beta || !a->dprob))
+    return BSGG_ERR_INVALID_ARG;
+  if (d.want_rht && (!a->rht || !aligned16(a->rht))) return BSGG_ERR_INVALID_ARG;
+  if (d.want_rht && d.rht_format == BSGG_OUT_E2M1 && (!a->sfrht || !a->rht_norm_const))
     return BSGG_ERR_INVALID_ARG;
   if (d.want_c && (!a->c || !aligned16(a->c))) return BSGG_ERR_INVALID_ARG;
   return BSGG_OK;
@@ -469,6 +482,13 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   p.glu_kind = d.epilogue == BSGG_EPI_GEGLU ? 1 : 0;
   p.glu_limit = d.glu_limit;
   p.glu_gamma = d.glu_alpha == 0.0f ? 1.0f : d.glu_alpha;
+  if (d.want_rht) {
+    p.rht = a->rht;
+    p.sfrht = static_cast<uint8_t*>(a->sfrht);
+    p.rht_norm_const = a->rht_norm_const;
+    p.rht_kind = d.rht_format == BSGG_OUT_E2M1 ? bsgg::OK_E2M1 : bsgg::OK_BF16;
+    p.kq_rht = static_cast<int32_t>(ceil_div(ceil_div(P->n_out, 16), 4));
+  }
   if (d.epilogue == BSGG_EPI_DSWIGLU) {
     p.saved_c = a->saved_c;
     p.saved_c_kind = d.saved_c_format;
@@ -578,7 +598,8 @@ bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* 
             // backward: the saved C and beta in, dprob in (it is accumulated) and out
             h2d(bwd ? host->saved_c : nullptr, dev->saved_c, sz_saved_c) &&
             h2d(bwd ? host->beta : nullptr, dev->beta, sizeof(float) * L) &&
-            h2d(bwd ? host->dprob : nullptr, dev->dprob, sizeof(float) * d.m_pad);
+            h2d(bwd ? host->dprob : nullptr, dev->dprob, sizeof(float) * d.m_pad) &&
+            h2d(d.want_rht ? host->rht_norm_const : nullptr, dev->rht_norm_const, sizeof(float));
   if (!ok) return BSGG_ERR_CUDA;
   bsgg_status st = bsgg_run(P, dev, stream);
   if (st != BSGG_OK) return st;
@@ -587,6 +608,10 @@ bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* 
        d2h(host->sfd_col, dev->sfd_col, d.want_col ? sz_sfd_col : 0) &&
        d2h(host->amax, dev->amax, sizeof(float) * n_amax) &&
        d2h(bwd ? host->dprob : nullptr, dev->dprob, sizeof(float) * d.m_pad) &&
+       d2h(d.want_rht ? host->rht : nullptr, dev->rht,
+           uint64_t(d.m_pad) * (d.rht_format == BSGG_OUT_E2M1 ? P->n_out / 2 : P->n_out * 2)) &&
+       d2h(d.want_rht && d.rht_format == BSGG_OUT_E2M1 ? host->sfrht : nullptr, dev->sfrht,
+           sf_bytes_impl(d.m_pad, P->n_out, 16, 1)) &&
        d2h(d.want_c ? host->c : nullptr, dev->c, uint64_t(d.m_pad) * d.n * 2);
   if (!ok) return BSGG_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return BSGG_ERR_CUDA;

@@ -134,6 +134,13 @@ struct Params {
   int32_t saved_c_kind;     // OK_BF16, OK_F16 or OK_F32
   const float* beta;
   float* dprob;
+  // rowwise Hadamard output of bf16-rounded D ("Grouped GEMM + GLU + Hadamard +
+  // Quant (SM100)"): bf16 or NVFP4 with E4M3 scales per 16 (SFRHT)
+  void* rht;                // (m_pad, n_out), or null
+  uint8_t* sfrht;
+  const float* rht_norm_const;
+  int32_t rht_kind;         // OK_BF16 or OK_E2M1
+  int32_t kq_rht;           // SF atoms per 128 rows of SFRHT: ceil(ceil(n_out/16)/4)
   // discrete weight mode: per-expert tensor maps {B_g, SFB_g} (2 per expert, in
   // global memory) and the flag their writer raises for a bad pointer; null in
   // dense mode
@@ -515,10 +522,55 @@ __device__ __forceinline__ void output_chunk(const Params& p, const float (&v)[3
   }
 }
 
+// Rowwise Hadamard output of one 32-column chunk of D of one row: each 16-value
+// block of bf16-rounded D times H16 / 4 (H16 the Sylvester Hadamard matrix,
+// entry (i, j) = (-1)^popcount(i & j): four in-register butterfly stages),
+// stored as bf16 or quantized to NVFP4 with E4M3 scales per 16 under rnorm.
+__device__ __forceinline__ void rht_chunk(const Params& p, const float (&v)[32], int row, int col0,
+                                          float rnorm) {
+  float y[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) y[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (i & o) continue;
+        const float a = y[16 * h + i], b = y[16 * h + i + o];
+        y[16 * h + i] = a + b;
+        y[16 * h + i + o] = a - b;
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) y[i] *= 0.25f;
+  if (p.rht_kind == OK_BF16) {
+    store_h32(static_cast<uint16_t*>(p.rht) + static_cast<int64_t>(row) * p.n_out + col0, &y[0], OK_BF16);
+  } else {
+    float sc[32];
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      float am = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(y[16 * b + i]));
+      uint32_t code;
+      float s;
+      block_scale<true>(am, rnorm, 1.0f / 6.0f, code, s);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sc[16 * b + i] = s;
+      p.sfrht[sf_off(row, col0 / 16 + b, p.kq_rht)] = static_cast<uint8_t>(code);
+    }
+    store_q32<OUTC_FP4>(static_cast<uint8_t*>(p.rht) + static_cast<int64_t>(row) * (p.n_out / 2) + col0 / 2, y,
+                        sc, OK_E2M1);
+  }
+}
+
 // Step 2 and Step 3 for one 32-column chunk of one row: C = al * xs (the
 // input half for the GLUs; fp32 bits), al * gs the gate half.  al is alpha_g,
 // or 1 where alpha and the bias were already applied in place.
-template <bool FP4, int EPI, int OUTC>
+template <bool FP4, int EPI, int OUTC, bool XC>
 __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* xs, const uint32_t* gs, int row,
                                                int col0, float al, float pr, float norm, int lane, int kblk_col,
                                                float& amax_local) {
@@ -551,10 +603,12 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* 
     }
   }
   output_chunk<FP4, OUTC>(p, v, row, col0, norm, lane, kblk_col, amax_local);
+  if (XC && p.rht != nullptr) rht_chunk(p, v, row, col0, *p.rht_norm_const);
 }
 
-// XC: the launch adds a bias to C or stores C (a separate instance, so that the
-// register budget of the plain epilogue is untouched).
+// XC: the launch adds a bias to C, stores C or writes the Hadamard output (a
+// separate instance, so that the register budget of the plain epilogue is
+// untouched).
 template <bool FP4, int BN, int CM, int EPI, int OUTC, bool XC>
 __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
     bsgg_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -988,7 +1042,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
       // al = 1), stored when asked for ("Grouped GEMM + GLU + Hadamard + Quant
       // (SM100)", Equations)
       float al_epi = al;
-      if (XC) {
+      if (XC && (p.bias != nullptr || p.c_out != nullptr)) {
         const int ccol0 = nt * BN + e * kWarpCols;    // first C column of this warp's half
 #pragma unroll
         for (int c = 0; c < kWarpCols / 32; ++c) {
@@ -1054,15 +1108,15 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
             xs[i] = gf ? r[64 * j + 32 + i] : r[64 * j + i];
             gs[i] = gf ? r[64 * j + i] : r[64 * j + 32 + i];
           }
-          epilogue_chunk<FP4, EPI, OUTC>(p, xs, gs, row, col0, al_epi, pr, norm, lane, kblk_col, amax_local);
+          epilogue_chunk<FP4, EPI, OUTC, XC>(p, xs, gs, row, col0, al_epi, pr, norm, lane, kblk_col, amax_local);
         }
       } else {
 #pragma unroll
         for (int c = 0; c < kWarpCols / 32; ++c) {
           const int col0 = nt * BN + e * kWarpCols + 32 * c;
           if (col0 >= p.n_out) continue;
-          epilogue_chunk<FP4, EPI, OUTC>(p, &r[32 * c], &r[32 * c], row, col0, al_epi, pr, norm, lane,
-                                         kblk_col, amax_local);
+          epilogue_chunk<FP4, EPI, OUTC, XC>(p, &r[32 * c], &r[32 * c], row, col0, al_epi, pr, norm, lane,
+                                             kblk_col, amax_local);
         }
       }
       if (OUTC == OUTC_FLOAT && p.amax != nullptr) {

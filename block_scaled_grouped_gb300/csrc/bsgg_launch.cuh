@@ -68,7 +68,8 @@ cudaError_t launch_xc(const Launch& L) {
   if constexpr (EPI == EPI_DSWIGLU) {
     return launch_outc<FP4, BN, CM, EPI, false>(L);   // the backward takes no bias and stores no C
   } else {
-    if (L.p.bias != nullptr || L.p.c_out != nullptr) return launch_outc<FP4, BN, CM, EPI, true>(L);
+    if (L.p.bias != nullptr || L.p.c_out != nullptr || L.p.rht != nullptr)
+      return launch_outc<FP4, BN, CM, EPI, true>(L);
     return launch_outc<FP4, BN, CM, EPI, false>(L);
   }
 }

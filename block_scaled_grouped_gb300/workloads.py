@@ -352,7 +352,7 @@ def build_problem(*, name: str, counts: Sequence[int], k: int, n: int, in_fmt: s
         a=a, sfa_rows=sfa, b=b, sfb_rows=sfb, saved_c=saved_c, beta=beta)
 
 
-WORKLOADS = ("tiny", "fc1_swiglu", "fc2_gate", "fine_nvfp4", "skewed")
+WORKLOADS = ("tiny", "fc1_swiglu", "fc2_gate", "fine_nvfp4", "skewed", "fc1_dswiglu")
 
 
 def workload(name: str, device="cpu") -> Problem:
@@ -363,10 +363,19 @@ def workload(name: str, device="cpu") -> Problem:
         return build_problem(name=name, counts=[128, 256], k=256, n=256, in_fmt="mxfp8_e4m3",
                              out_fmt="bf16", epi="gate", seed=0, device=device,
                              alpha=[1.0, 0.5])
-    if name in ("fc1_swiglu", "fc2_gate"):
+    if name in ("fc1_swiglu", "fc2_gate", "fc1_dswiglu"):
         T, L = 4096, 8
         tokens, probs = route_softmax_topk(T, L, 2, seed=1)
         counts = [t.size for t in tokens]
+        if name == "fc1_dswiglu":
+            # the backward of the FC1 + SwiGLU layer: the routed output gradients
+            # (K = 4096) against the down-projection weights (N = 14336, the
+            # SwiGLU output width) give the gradient of the 28672-wide saved C;
+            # E4M3 row and column outputs for the next GEMMs
+            return build_problem(name=name, counts=counts, k=4096, n=14336, in_fmt="mxfp8_e4m3",
+                                 out_fmt="e4m3", epi="dswiglu", seed=5, device=device,
+                                 token_rows=tokens, num_tokens=T, row_prob=probs,
+                                 norm_const=1.0, want_col=True)
         if name == "fc1_swiglu":
             return build_problem(name=name, counts=counts, k=4096, n=28672, in_fmt="mxfp8_e4m3",
                                  out_fmt="e4m3", epi="swiglu", seed=1, device=device,

@@ -159,6 +159,14 @@ typedef struct {
   /* DSWIGLU: storage type of the saved forward C, BSGG_OUT_BF16, BSGG_OUT_F16 or
      BSGG_OUT_F32 ("Grouped GEMM + dGLU (SM100)", BF16 contract: C in BF16/FP16/FP32). */
   int32_t saved_c_format;
+  /* Rowwise Hadamard output ("Grouped GEMM + GLU + Hadamard + Quant (SM100)",
+     Equations): 1 = also write RHT = (H16 / 4) x for every 16-column block x of
+     bf16-rounded D, H16 the 16 x 16 Sylvester Hadamard matrix; (m_pad, N_out)
+     N-major in rht_format: BSGG_OUT_BF16, or BSGG_OUT_E2M1 (packed NVFP4 with
+     E4M3 scales per 16 in SFRHT = swizzled SF(m_pad, N_out) under
+     rht_norm_const, whatever the input's scale type).  Forward epilogues only. */
+  int32_t want_rht;
+  int32_t rht_format;
 } bsgg_desc;
 
 /* Tensors of one call.  Unused outputs may be NULL: d_col/sfd_col unless
@@ -196,6 +204,11 @@ typedef struct {
   const void* saved_c;
   const float* beta;
   float* dprob;
+  /* want_rht only: the RHT output; SFRHT and rht_norm_const (1 float) for an
+     NVFP4 RHT. */
+  void* rht;
+  void* sfrht;
+  const float* rht_norm_const;
 } bsgg_args;
 
 typedef struct bsgg_plan bsgg_plan;

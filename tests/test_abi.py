@@ -109,6 +109,8 @@ def _create(**over):
     (dict(epilogue="dswiglu", saved_c_format="e4m3"), 1),
     (dict(epilogue="dswiglu", n=80), 1),
     (dict(epilogue="dswiglu", tanh_clamp_s=4.0), 1),
+    (dict(rht_format="e4m3"), 1), (dict(rht_format="f16"), 1),   # RHT is bf16 or NVFP4
+    (dict(epilogue="dswiglu", rht_format="bf16"), 1),            # forward epilogues only
 ])
 def test_create_rejects(lib, over, code):
     assert _create(**over) == code
@@ -121,6 +123,7 @@ def test_create_rejects(lib, over, code):
     dict(epilogue="gate", bias_format="f16"),
     dict(discrete_b=True, num_groups=1024),
     dict(epilogue="dswiglu", n=96, saved_c_format="f32", out_format="e4m3", want_col=1),
+    dict(epilogue="swiglu", rht_format="e2m1", in_format="nvfp4", out_format="e2m1"),
 ])
 def test_create_accepts_epilogue_options(lib, over):
     # validation passes: 0 with a GPU, else the device query that follows
