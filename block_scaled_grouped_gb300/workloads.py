@@ -33,7 +33,7 @@ import torch
 
 IN_FORMATS = ("mxfp8_e4m3", "mxfp8_e5m2", "nvfp4")
 OUT_FORMATS = ("bf16", "f16", "f32", "e4m3", "e5m2", "e2m1")
-EPILOGUES = ("gate", "swiglu", "srelu", "geglu", "dswiglu")
+EPILOGUES = ("gate", "swiglu", "srelu", "geglu", "dswiglu", "dgeglu")
 
 _ROW_CHUNK = 4096
 
@@ -60,7 +60,7 @@ class Problem:
     sfa_rows: torch.Tensor      # uint8 (1, m_pad, k/v) scale codes, row-major
     b: torch.Tensor             # uint8 (L, n, k or k/2)
     sfb_rows: torch.Tensor      # uint8 (L, n, k/v) scale codes, row-major
-    # the dSwiGLU backward's extra inputs (None otherwise): the saved forward
+    # the backward epilogues' extra inputs (None otherwise): the saved forward
     # pre-activation C (m_pad, 2n) bf16 and its per-group scale beta (L,)
     saved_c: Optional[torch.Tensor] = None
     beta: Optional[torch.Tensor] = None
@@ -73,7 +73,7 @@ class Problem:
     def n_out(self) -> int:
         if self.epi in ("swiglu", "geglu"):
             return self.n // 2
-        return 2 * self.n if self.epi == "dswiglu" else self.n
+        return 2 * self.n if self.epi in ("dswiglu", "dgeglu") else self.n
 
     @property
     def m_real(self) -> int:
@@ -331,10 +331,11 @@ def build_problem(*, name: str, counts: Sequence[int], k: int, n: int, in_fmt: s
             b[g, c0:c0 + r] = q
             sfb[g, c0:c0 + r] = s
 
-    # dSwiGLU backward: the saved forward C, N(0, 2) rounded to bf16 (a
-    # pre-activation's typical spread), and beta ~ U(0.5, 2) per group
+    # backward epilogues: the saved forward C, N(0, 2) rounded to bf16 (a
+    # pre-activation's typical spread), and beta ~ U(0.5, 2) per group (read
+    # by dSwiGLU only)
     saved_c = beta = None
-    if epi == "dswiglu":
+    if epi in ("dswiglu", "dgeglu"):
         beta = torch.as_tensor(rng.uniform(0.5, 2.0, size=L).astype(np.float32), device=device)
         saved_c = torch.empty(m_pad, 2 * n, dtype=torch.bfloat16, device=device)
         for c0 in range(0, m_pad, _ROW_CHUNK):

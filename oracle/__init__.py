@@ -29,7 +29,7 @@ _lib = None
 F_E4M3, F_E5M2, F_E2M1, F_UE8M0 = 0, 1, 2, 3
 IN_MXFP8_E4M3, IN_MXFP8_E5M2, IN_NVFP4 = 0, 1, 2
 OUT_BF16, OUT_F16, OUT_F32, OUT_E4M3, OUT_E5M2, OUT_E2M1 = 0, 1, 2, 3, 4, 5
-EPI_GATE, EPI_SWIGLU, EPI_SRELU, EPI_GEGLU, EPI_DSWIGLU = 0, 1, 2, 3, 4
+EPI_GATE, EPI_SWIGLU, EPI_SRELU, EPI_GEGLU, EPI_DSWIGLU, EPI_DGEGLU = 0, 1, 2, 3, 4, 5
 
 
 class OrcDesc(ctypes.Structure):
@@ -39,7 +39,8 @@ class OrcDesc(ctypes.Structure):
         ("in_fmt", ctypes.c_int32), ("out_fmt", ctypes.c_int32), ("epi", ctypes.c_int32),
         ("gate_first", ctypes.c_int32), ("want_col", ctypes.c_int32), ("rht", ctypes.c_int32),
         ("tanh_clamp_s", ctypes.c_double), ("glu_limit", ctypes.c_double), ("glu_alpha", ctypes.c_double),
-        ("rht_norm", ctypes.c_double),
+        ("rht_norm", ctypes.c_double), ("geglu_alpha", ctypes.c_double), ("glu_clamp_min", ctypes.c_double),
+        ("glu_clamp_max", ctypes.c_double), ("linear_offset", ctypes.c_double),
     ]
 
 
@@ -153,13 +154,14 @@ def hadamard16(i: int, j: int) -> float:
 def n_out(n: int, epi: int) -> int:
     if epi in (EPI_SWIGLU, EPI_GEGLU):
         return n // 2
-    return 2 * n if epi == EPI_DSWIGLU else n
+    return 2 * n if epi in (EPI_DSWIGLU, EPI_DGEGLU) else n
 
 
 def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded_offsets,
         alpha, prob, norm_const=1.0, tanh_clamp_s=0.0, gate_first=0, want_col=False,
         blocks=None, threads=None, outputs=None, bias=None, glu_limit=0.0, glu_alpha=1.0,
-        want_c=False, saved_c=None, beta=None, rht=None, rht_norm=1.0):
+        want_c=False, saved_c=None, beta=None, rht=None, rht_norm=1.0, geglu_alpha=1.702,
+        glu_clamp_min=-7.0, glu_clamp_max=7.0, linear_offset=1.0):
     """Run the oracle on the listed 32-row blocks (default: all of them).
 
     Inputs are numpy arrays in the device layouts: ``a`` (m_pad, k or k/2)
@@ -174,7 +176,10 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     (``epi=EPI_DSWIGLU``) takes ``saved_c`` (m_pad, 2n) values of the saved
     forward C (any float dtype, widened to fp64) and ``beta`` float32 (L,), and
     adds ``dprob_ref`` (fp64, rows of the listed blocks); its ``amax`` has 2L
-    entries (input-gradient and gate-gradient blocks of each group).
+    entries (input-gradient and gate-gradient blocks of each group).  The dGeGLU
+    backward (``epi=EPI_DGEGLU``) takes the saved C unscaled and
+    ``geglu_alpha``, ``glu_clamp_min``/``glu_clamp_max`` and ``linear_offset``
+    (the page's defaults 1.702, -7, 7, 1).
     ``rht`` ("bf16" or "e2m1") adds the rowwise Hadamard output: ``rht_ref``
     (fp64) and, for "e2m1", full-size ``rht_q`` / ``sfrht`` buffers (E4M3
     scales per 16 under ``rht_norm``).
@@ -183,7 +188,8 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     rht_code = {None: 0, "bf16": 1, "e2m1": 2}[rht]
     desc = OrcDesc(m_pad, n, k, num_groups, in_fmt, out_fmt, epi, int(gate_first),
                    int(bool(want_col)), rht_code, float(tanh_clamp_s), float(glu_limit), float(glu_alpha),
-                   float(rht_norm))
+                   float(rht_norm), float(geglu_alpha), float(glu_clamp_min), float(glu_clamp_max),
+                   float(linear_offset))
     nd = n_out(n, epi)
     if blocks is None:
         blocks = np.arange(m_pad // 32, dtype=np.int64)
@@ -193,9 +199,10 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     d_ref = np.zeros((blocks.size * 32, nd), dtype=np.float64)
     c_ref = np.zeros((blocks.size * 32, n), dtype=np.float64) if want_c else None
     bias_arr = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32).reshape(num_groups, n)
-    amax = np.zeros(2 * num_groups if epi == EPI_DSWIGLU else num_groups, dtype=np.float32)
+    bwd = epi in (EPI_DSWIGLU, EPI_DGEGLU)
+    amax = np.zeros(2 * num_groups if bwd else num_groups, dtype=np.float32)
     rht_ref = np.zeros((blocks.size * 32, nd), dtype=np.float64) if rht_code else None
-    dprob_ref = np.zeros(blocks.size * 32, dtype=np.float64) if epi == EPI_DSWIGLU else None
+    dprob_ref = np.zeros(blocks.size * 32, dtype=np.float64) if bwd else None
     saved_arr = None if saved_c is None else np.ascontiguousarray(saved_c, dtype=np.float64).reshape(m_pad, 2 * n)
     beta_arr = None if beta is None else np.ascontiguousarray(beta, dtype=np.float32).reshape(num_groups)
     outs = dict(outputs or {})

@@ -161,8 +161,8 @@ int64_t sf_bytes(int64_t rows, int64_t kblocks, int64_t L) {
 // ---------------------------------------------------------------------------
 enum InFmt { IN_MXFP8_E4M3 = 0, IN_MXFP8_E5M2 = 1, IN_NVFP4 = 2 };
 enum OutFmt { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2, OUT_E4M3 = 3, OUT_E5M2 = 4, OUT_E2M1 = 5 };
-// EPI_DSWIGLU: the dSwiGLU backward of "Grouped GEMM + dGLU (SM100)".
-enum Epi { EPI_GATE = 0, EPI_SWIGLU = 1, EPI_SRELU = 2, EPI_GEGLU = 3, EPI_DSWIGLU = 4 };
+// EPI_DSWIGLU, EPI_DGEGLU: the backward epilogues of "Grouped GEMM + dGLU (SM100)".
+enum Epi { EPI_GATE = 0, EPI_SWIGLU = 1, EPI_SRELU = 2, EPI_GEGLU = 3, EPI_DSWIGLU = 4, EPI_DGEGLU = 5 };
 
 }  // namespace
 
@@ -180,6 +180,9 @@ typedef struct {
   double glu_limit;
   double glu_alpha;
   double rht_norm;       // global encode scale of an NVFP4 RHT output (rht_norm_const)
+  // dGeGLU ("Grouped GEMM + dGLU (SM100)", Block-scaled contract, Step 2):
+  // sigmoid slope, clamp bounds and the offset added to the clamped up value
+  double geglu_alpha, glu_clamp_min, glu_clamp_max, linear_offset;
 } orc_desc;
 
 // ---- exported helpers (pinned individually by the tests) ----
@@ -320,7 +323,7 @@ double q_max(const orc_desc* P) {
   return P->out_fmt == OUT_E4M3 ? 448.0 : P->out_fmt == OUT_E5M2 ? 57344.0 : 6.0;
 }
 bool is_glu(const orc_desc* P) { return P->epi == EPI_SWIGLU || P->epi == EPI_GEGLU; }
-bool is_bwd(const orc_desc* P) { return P->epi == EPI_DSWIGLU; }
+bool is_bwd(const orc_desc* P) { return P->epi == EPI_DSWIGLU || P->epi == EPI_DGEGLU; }
 // D width: N/2 for the forward GLUs (two C blocks per D block), 2N for the
 // backward (two gradient blocks per GEMM block), else N.
 int64_t n_out(const orc_desc* P) { return is_glu(P) ? P->n / 2 : is_bwd(P) ? 2 * P->n : P->n; }
@@ -449,19 +452,39 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
     const int64_t m = m0 + i;
     const double p = J.prob[m];
     auto Cv = [&](int64_t n) { return C[size_t(i * (c1 - c0) + (n - c0))]; };
-    // dSwiGLU backward ("Grouped GEMM + dGLU (SM100)", Block-scaled contract,
-    // Step 2): the saved C, scaled by beta_g, split into the input X and gate G
-    // 32-column blocks of pair b (same block order as the forward SwiGLU).
+    // Backward ("Grouped GEMM + dGLU (SM100)", Block-scaled contract, Step 2):
+    // the saved C split into the input (up) X and gate G 32-column blocks of
+    // pair b (the forward's block order); dSwiGLU scales it by beta_g, dGeGLU
+    // uses it as saved.
     auto saved = [&](int64_t jr, bool gate) {
       const int64_t b = jr / 32, r = jr % 32;
       const bool second = (gate != bool(P->gate_first));
-      return double(J.beta[g]) * J.saved_c[m * 2 * P->n + 64 * b + (second ? 32 : 0) + r];
+      const double c = J.saved_c[m * 2 * P->n + 64 * b + (second ? 32 : 0) + r];
+      return P->epi == EPI_DSWIGLU ? double(J.beta[g]) * c : c;
+    };
+    // dGeGLU: the gate has only an upper clamp, the up value both; the masks
+    // test the values before clamping and keep the gradient at either bound
+    auto dgeglu = [&](double up, double gate, double ref, double& d_up, double& d_gate, double& dprob_term) {
+      const double gc = std::min(gate, P->glu_clamp_max);
+      const double uc = std::min(std::max(up, P->glu_clamp_min), P->glu_clamp_max);
+      const double s = orc_sigmoid(P->geglu_alpha * gc);
+      const double gate_mask = gate <= P->glu_clamp_max ? 1.0 : 0.0;
+      const double up_mask = (P->glu_clamp_min <= up && up <= P->glu_clamp_max) ? 1.0 : 0.0;
+      d_gate = ref * p * (uc + P->linear_offset) * s * (1.0 + P->geglu_alpha * gc * (1.0 - s)) * gate_mask;
+      d_up = ref * p * gc * s * up_mask;
+      dprob_term = ref * gc * s * (uc + P->linear_offset);
     };
     if (is_bwd(P)) {
-      // dprob += sum over the GEMM columns of X * swish(G) * ref
+      // dprob += sum over the GEMM columns of ref times the activation
       for (int64_t jr = c0; jr < c1; ++jr) {
         const double x = saved(jr, false), gt = saved(jr, true);
-        dprob_local[size_t(i)] += x * (gt * orc_sigmoid(gt)) * Cv(jr);
+        if (P->epi == EPI_DSWIGLU) {
+          dprob_local[size_t(i)] += x * (gt * orc_sigmoid(gt)) * Cv(jr);
+        } else {
+          double du, dg, t;
+          dgeglu(x, gt, Cv(jr), du, dg, t);
+          dprob_local[size_t(i)] += t;
+        }
       }
     }
     for (int64_t j = j0; j < j1; ++j) {
@@ -475,9 +498,15 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
         const bool is_input = (second == bool(P->gate_first));
         const int64_t jr = 32 * b + r;
         const double x = saved(jr, false), gt = saved(jr, true), ref = Cv(jr);
-        const double sg = orc_sigmoid(gt);
-        if (is_input) d = ref * p * (gt * sg);                          // d input = ref prob swish(G)
-        else d = ref * p * x * sg * (1.0 + gt * (1.0 - sg));            // d gate
+        if (P->epi == EPI_DSWIGLU) {
+          const double sg = orc_sigmoid(gt);
+          if (is_input) d = ref * p * (gt * sg);                        // d input = ref prob swish(G)
+          else d = ref * p * x * sg * (1.0 + gt * (1.0 - sg));          // d gate
+        } else {
+          double du, dg, t;
+          dgeglu(x, gt, ref, du, dg, t);
+          d = is_input ? du : dg;
+        }
         amax_idx = 2 * g + (is_input ? 0 : 1);
       } else if (P->epi == EPI_GATE) {
         d = p * Cv(j);                                    // D = prob * ref
@@ -593,7 +622,7 @@ extern "C" int orc_run(const orc_desc* P, const uint8_t* A, const uint8_t* SFA, 
   if (!P || P->m_pad <= 0 || P->m_pad % 32 || P->n <= 0 || P->k <= 0 || P->num_groups <= 0)
     return -1;
   if (is_glu(P) && P->n % 64) return -2;
-  if (is_bwd(P) && (P->n % 32 || !saved_c || !beta || bias)) return -4;
+  if (is_bwd(P) && (P->n % 32 || !saved_c || (P->epi == EPI_DSWIGLU && !beta) || bias)) return -4;
   if (P->rht && (is_bwd(P) || !rht_ref || (P->rht == 2 && (!rht_q || !sfrht)))) return -5;
   if (is_fp4_in(P) && P->k % 2) return -3;
   const int64_t nd = n_out(P);

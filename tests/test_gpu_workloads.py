@@ -1,6 +1,7 @@
-"""Parity at full size: the four large workloads, generated on the GPU with
-their real shapes and run in every tile shape (the library's default is the
-one bench.py times), compared element by element with the CPU oracle on
+"""Parity at full size: the four large forward workloads and the FC1 backward
+(dSwiGLU), generated on the GPU with their real shapes and run in every tile
+shape (the library's default is the one bench.py times; two shapes for the
+backward), compared element by element with the CPU oracle on
 sampled 32-row blocks -- each group's first and last block, the first and last
 block of the problem and random blocks -- with the same tolerances as the
 small parity tests.  For BF16 outputs the per-group amax is checked over whole
@@ -39,6 +40,8 @@ def _sample_blocks(p, n_random=3, seed=0):
 def _oracle(p, blocks):
     ins = dict(a=np_(p.a), b=np_(p.b), sfa=orc.pack_sf(np_(p.sfa_rows)), sfb=orc.pack_sf(np_(p.sfb_rows)),
                padded_offsets=np_(p.padded_offsets), alpha=np_(p.alpha), prob=np_(p.prob))
+    if p.epi == "dswiglu":
+        ins.update(saved_c=np_(p.saved_c.double()), beta=np_(p.beta))
     return orc.run(m_pad=p.m_pad, n=p.n, k=p.k, num_groups=p.num_groups, in_fmt=IN_CODE[p.in_fmt],
                    out_fmt=OUT_CODE[p.out_fmt], epi=EPI_CODE[p.epi], norm_const=p.norm_const,
                    tanh_clamp_s=p.tanh_clamp_s, want_col=p.want_col, blocks=blocks, **ins)
@@ -73,3 +76,30 @@ def test_full_size_parity_on_sampled_blocks(workload, tile):
         # the oracle's amax over the sampled rows bounds the full amax from below
         sampled = ref["amax"]
         assert np.all(amax >= sampled * (1 - 2.0 ** -20))
+
+
+@pytest.mark.parametrize("tile", [(0, 0), (256, 256, 2, 1)], ids=tile_id)
+def test_full_size_backward_on_sampled_blocks(tile):
+    """The FC1 + SwiGLU backward at full size (T=4096 top-2 of 8, K=4096,
+    N=14336, E4M3 row and column outputs 28672 wide): D, D_col and the scale
+    factors on sampled blocks, and dprob on every row of those blocks."""
+    import block_scaled_grouped_gb300 as bsgg
+    from gpu_harness import alloc_outputs, check_float_d
+    p = W.workload("fc1_dswiglu", device="cuda")
+    blocks = _sample_blocks(p)
+    ref = _oracle(p, blocks)
+    plan = bsgg.Plan(m_pad=p.m_pad, n=p.n, k=p.k, num_groups=p.num_groups, in_format=p.in_fmt,
+                     out_format=p.out_fmt, epilogue=p.epi, want_col=p.want_col, tile=tuple(tile[:2]),
+                     cluster=tuple(tile[2:4]) or (0, 0))
+    outs = alloc_outputs(plan)
+    dprob = torch.zeros(p.m_pad, dtype=torch.float32, device="cuda")
+    norm = torch.tensor([p.norm_const], dtype=torch.float32, device="cuda")
+    plan.run(a=p.a, sfa=bsgg.pack_sf(p.sfa_rows), b=p.b, sfb=bsgg.pack_sf(p.sfb_rows),
+             padded_offsets=p.padded_offsets, alpha=p.alpha, prob=p.prob, norm_const=norm,
+             saved_c=p.saved_c, beta=p.beta, dprob=dprob, **outs)
+    assert plan.device_status() == 0
+    compare(p, outs, ref, blocks=blocks)
+    rows = (blocks[:, None] * 32 + np.arange(32)[None, :]).reshape(-1)
+    check_float_d(dprob.cpu().double().numpy()[rows], ref["dprob_ref"], what="dprob")
+    del p, outs
+    torch.cuda.empty_cache()
