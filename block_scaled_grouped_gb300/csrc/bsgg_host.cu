@@ -100,9 +100,15 @@ bsgg_status validate(const bsgg_desc* d) {
     return BSGG_ERR_INVALID_ARG;
   if (d->in_format < BSGG_IN_MXFP8_E4M3 || d->in_format > BSGG_IN_NVFP4) return BSGG_ERR_INVALID_ARG;
   if (d->out_format < BSGG_OUT_BF16 || d->out_format > BSGG_OUT_E2M1) return BSGG_ERR_INVALID_ARG;
-  if (d->epilogue < BSGG_EPI_GATE || d->epilogue > BSGG_EPI_DSWIGLU) return BSGG_ERR_INVALID_ARG;
+  if (d->epilogue < BSGG_EPI_GATE || d->epilogue > BSGG_EPI_DGEGLU) return BSGG_ERR_INVALID_ARG;
   const bool glu = d->epilogue == BSGG_EPI_SWIGLU || d->epilogue == BSGG_EPI_GEGLU;
-  const bool bwd = d->epilogue == BSGG_EPI_DSWIGLU;
+  const bool bwd = d->epilogue == BSGG_EPI_DSWIGLU || d->epilogue == BSGG_EPI_DGEGLU;
+  if (d->dgeglu_custom != 0 && d->dgeglu_custom != 1) return BSGG_ERR_INVALID_ARG;
+  if (d->dgeglu_custom &&
+      (d->epilogue != BSGG_EPI_DGEGLU || !std::isfinite(d->dgeglu_alpha) || !std::isfinite(d->dgeglu_clamp_min) ||
+       !std::isfinite(d->dgeglu_clamp_max) || !std::isfinite(d->dgeglu_linear_offset) ||
+       d->dgeglu_clamp_min > d->dgeglu_clamp_max))
+    return BSGG_ERR_INVALID_ARG;
   if (d->gate_first != 0 && d->gate_first != 1) return BSGG_ERR_INVALID_ARG;
   if (d->want_col != 0 && d->want_col != 1) return BSGG_ERR_INVALID_ARG;
   // K-major rows must be 16-byte aligned ("Support Surface and Constraints",
@@ -233,7 +239,7 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
   // accumulator columns per thread and runs without register spills (measured
   // on GB300: 1418 TFLOP/s on the FC1 backward against 582 with 256 x 256
   // pairs, whose epilogue spills to local memory).
-  const bool bwd = desc->epilogue == BSGG_EPI_DSWIGLU;
+  const bool bwd = desc->epilogue == BSGG_EPI_DSWIGLU || desc->epilogue == BSGG_EPI_DGEGLU;
   int tm = desc->tile_m, tn = desc->tile_n, cm = desc->cluster_m;
   if (tm == 0) tm = (desc->in_format != BSGG_IN_NVFP4 && tn != 128 && cm != 1 && !bwd) ? 256 : 128;
   if (tn == 0) tn = (bwd && tm == 128 && cm != 2) ? 128 : 256;
@@ -242,17 +248,18 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
   P->mc = (tm == 128 && cm == 2);
   P->bn = P->pair ? 256 : tn;
   // GeGLU runs in the SwiGLU instances (Params::glu_kind selects the activation)
-  P->epi = desc->epilogue == BSGG_EPI_GEGLU     ? bsgg::EPI_SWIGLU
-           : desc->epilogue == BSGG_EPI_DSWIGLU ? bsgg::EPI_DSWIGLU
-                                                : desc->epilogue;
+  // the dGeGLU backward runs in the dSwiGLU instances (Params::bwd_kind)
+  P->epi = desc->epilogue == BSGG_EPI_GEGLU                                              ? bsgg::EPI_SWIGLU
+           : (desc->epilogue == BSGG_EPI_DSWIGLU || desc->epilogue == BSGG_EPI_DGEGLU) ? bsgg::EPI_DSWIGLU
+                                                                                        : desc->epilogue;
   P->outc = desc->out_format == BSGG_OUT_E2M1 ? bsgg::OUTC_FP4
             : is_quant(desc->out_format)      ? bsgg::OUTC_FP8
                                               : bsgg::OUTC_FLOAT;
   P->sf_vec = desc->in_format == BSGG_IN_NVFP4 ? 16 : 32;
   P->kbytes = desc->in_format == BSGG_IN_NVFP4 ? desc->k / 2 : desc->k;
-  P->n_out = (desc->epilogue == BSGG_EPI_SWIGLU || desc->epilogue == BSGG_EPI_GEGLU) ? desc->n / 2
-             : desc->epilogue == BSGG_EPI_DSWIGLU                                     ? 2 * desc->n
-                                                                                      : desc->n;
+  P->n_out = (desc->epilogue == BSGG_EPI_SWIGLU || desc->epilogue == BSGG_EPI_GEGLU)    ? desc->n / 2
+             : (desc->epilogue == BSGG_EPI_DSWIGLU || desc->epilogue == BSGG_EPI_DGEGLU) ? 2 * desc->n
+                                                                                         : desc->n;
   P->out_row_bytes = P->n_out * out_elem_bits(desc->out_format) / 8;
   if (P->pair || P->mc) {
     int resident = bsgg::cluster_resident_ctas(desc->in_format == BSGG_IN_NVFP4, P->mc);
@@ -288,6 +295,8 @@ bsgg_status check_args(const bsgg_plan* P, const bsgg_args* a) {
   }
   if (d.want_bias && (!a->bias || !aligned16(a->bias))) return BSGG_ERR_INVALID_ARG;
   if (d.epilogue == BSGG_EPI_DSWIGLU && (!a->saved_c || !aligned16(a->saved_c) || !a->beta || !a->dprob))
+    return BSGG_ERR_INVALID_ARG;
+  if (d.epilogue == BSGG_EPI_DGEGLU && (!a->saved_c || !aligned16(a->saved_c) || !a->dprob))
     return BSGG_ERR_INVALID_ARG;
   if (d.want_rht && (!a->rht || !aligned16(a->rht))) return BSGG_ERR_INVALID_ARG;
   if (d.want_rht && d.rht_format == BSGG_OUT_E2M1 && (!a->sfrht || !a->rht_norm_const))
@@ -441,7 +450,7 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   st = encode_maps(P, a, &L);
   if (st != BSGG_OK) return st;
   // amax: one float per group, two for the backward (input / gate gradients)
-  const int64_t n_amax = d.num_groups * (d.epilogue == BSGG_EPI_DSWIGLU ? 2 : 1);
+  const int64_t n_amax = d.num_groups * ((d.epilogue == BSGG_EPI_DSWIGLU || d.epilogue == BSGG_EPI_DGEGLU) ? 2 : 1);
   if (a->amax && cudaMemsetAsync(a->amax, 0, sizeof(float) * n_amax, s) != cudaSuccess)
     return BSGG_ERR_CUDA;
 
@@ -489,11 +498,17 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
     p.rht_kind = d.rht_format == BSGG_OUT_E2M1 ? bsgg::OK_E2M1 : bsgg::OK_BF16;
     p.kq_rht = static_cast<int32_t>(ceil_div(ceil_div(P->n_out, 16), 4));
   }
-  if (d.epilogue == BSGG_EPI_DSWIGLU) {
+  if (d.epilogue == BSGG_EPI_DSWIGLU || d.epilogue == BSGG_EPI_DGEGLU) {
     p.saved_c = a->saved_c;
     p.saved_c_kind = d.saved_c_format;
     p.beta = a->beta;
     p.dprob = a->dprob;
+    p.bwd_kind = d.epilogue == BSGG_EPI_DGEGLU ? 1 : 0;
+    const bool cust = d.dgeglu_custom != 0;
+    p.geglu_a = cust ? d.dgeglu_alpha : 1.702f;
+    p.clamp_min = cust ? d.dgeglu_clamp_min : -7.0f;
+    p.clamp_max = cust ? d.dgeglu_clamp_max : 7.0f;
+    p.lin_offset = cust ? d.dgeglu_linear_offset : 1.0f;
   }
   if (d.discrete_b) {
     p.b_maps = P->maps;
@@ -571,7 +586,7 @@ bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* 
   const uint64_t sz_d = uint64_t(d.m_pad) * P->out_row_bytes;
   const uint64_t sz_sfd_row = sf_bytes_impl(d.m_pad, P->n_out, P->sf_vec, 1);
   const uint64_t sz_sfd_col = sf_bytes_impl(P->n_out, d.m_pad, P->sf_vec, 1);
-  const bool bwd = d.epilogue == BSGG_EPI_DSWIGLU;
+  const bool bwd = d.epilogue == BSGG_EPI_DSWIGLU || d.epilogue == BSGG_EPI_DGEGLU;
   const uint64_t sz_saved_c = bwd ? uint64_t(d.m_pad) * 2 * d.n * (d.saved_c_format == BSGG_OUT_F32 ? 4 : 2) : 0;
   const uint64_t n_amax = uint64_t(L) * (bwd ? 2 : 1);
   uint64_t in_bytes = 0, out_bytes = 0;
@@ -597,7 +612,7 @@ bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* 
                 uint64_t(L) * d.n * (d.bias_format == BSGG_OUT_F32 ? 4 : 2)) &&
             // backward: the saved C and beta in, dprob in (it is accumulated) and out
             h2d(bwd ? host->saved_c : nullptr, dev->saved_c, sz_saved_c) &&
-            h2d(bwd ? host->beta : nullptr, dev->beta, sizeof(float) * L) &&
+            h2d(d.epilogue == BSGG_EPI_DSWIGLU ? host->beta : nullptr, dev->beta, sizeof(float) * L) &&
             h2d(bwd ? host->dprob : nullptr, dev->dprob, sizeof(float) * d.m_pad) &&
             h2d(d.want_rht ? host->rht_norm_const : nullptr, dev->rht_norm_const, sizeof(float));
   if (!ok) return BSGG_ERR_CUDA;

@@ -55,7 +55,7 @@
 namespace bsgg {
 
 // Epilogue instances; EPI_SWIGLU also computes GeGLU (Params::glu_kind);
-// EPI_DSWIGLU is the dSwiGLU backward.
+// EPI_DSWIGLU is the dSwiGLU backward, and the dGeGLU backward (Params::bwd_kind).
 enum : int { EPI_GATE = 0, EPI_SWIGLU = 1, EPI_SRELU = 2, EPI_DSWIGLU = 3 };
 // Output class (template) and exact output kind (runtime) of D.
 enum : int { OUTC_FLOAT = 0, OUTC_FP8 = 1, OUTC_FP4 = 2 };
@@ -132,8 +132,10 @@ struct Params {
   // (m_pad, 2N), its per-group scale, and the accumulated dprob (m_pad)
   const void* saved_c;
   int32_t saved_c_kind;     // OK_BF16, OK_F16 or OK_F32
-  const float* beta;
+  const float* beta;        // dSwiGLU only
   float* dprob;
+  int32_t bwd_kind;         // EPI_DSWIGLU instances: 0 = dSwiGLU, 1 = dGeGLU
+  float geglu_a, clamp_min, clamp_max, lin_offset;   // dGeGLU
   // rowwise Hadamard output of bf16-rounded D ("Grouped GEMM + GLU + Hadamard +
   // Quant (SM100)"): bf16 or NVFP4 with E4M3 scales per 16 (SFRHT)
   void* rht;                // (m_pad, n_out), or null
@@ -1086,7 +1088,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
         // dSwiGLU backward ("Grouped GEMM + dGLU (SM100)", Block-scaled contract):
         // GEMM column j of pair b = j / 32 -> D (and saved C) columns 64b + r of
         // the input block and of the gate block, in the forward's block order
-        const float al2 = al * al, bt = p.beta[g];
+        const float al2 = al * al, bt = p.bwd_kind ? 1.0f : p.beta[g];
         const bool gf = p.gate_first != 0;
         float dprob_local = 0.0f;
 #pragma unroll
@@ -1099,15 +1101,37 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
           const int esz = p.saved_c_kind == OK_F32 ? 4 : 2;
           load_f32x32(x, static_cast<const uint8_t*>(p.saved_c) + (srow + xo) * esz, p.saved_c_kind);
           load_f32x32(gv, static_cast<const uint8_t*>(p.saved_c) + (srow + go) * esz, p.saved_c_kind);
+          if (p.bwd_kind == 0) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float ref = al2 * __uint_as_float(r[32 * c + i]);
-            const float X = bt * x[i], G = bt * gv[i];
-            const float sg = __fdividef(1.0f, 1.0f + __expf(-G));
-            const float sw = G * sg;
-            dprob_local += X * sw * ref;                              // dprob += X swish(G) ref
-            x[i] = ref * pr * sw;                                     // d input
-            gv[i] = ref * pr * X * sg * (1.0f + G * (1.0f - sg));     // d gate
+            for (int i = 0; i < 32; ++i) {
+              const float ref = al2 * __uint_as_float(r[32 * c + i]);
+              const float X = bt * x[i], G = bt * gv[i];
+              const float sg = __fdividef(1.0f, 1.0f + __expf(-G));
+              const float sw = G * sg;
+              dprob_local += X * sw * ref;                              // dprob += X swish(G) ref
+              x[i] = ref * pr * sw;                                     // d input
+              gv[i] = ref * pr * X * sg * (1.0f + G * (1.0f - sg));     // d gate
+            }
+          } else {
+            // dGeGLU: the gate clamped above, the up value both ways; each
+            // gradient masked where its own raw value lies beyond a bound
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float ref = al2 * __uint_as_float(r[32 * c + i]);
+              const float U = x[i], G = gv[i];
+              const float gc = fminf(G, p.clamp_max);
+              const float uc = fminf(fmaxf(U, p.clamp_min), p.clamp_max);
+              const float sg = __fdividef(1.0f, 1.0f + __expf(-p.geglu_a * gc));
+              const float t = gc * sg;
+              const float uo = uc + p.lin_offset;
+              dprob_local += ref * t * uo;                              // dprob += ref Gc s (Uc + offset)
+              // the masks multiply, as the page writes them: a masked gradient
+              // keeps the sign of the rest of the product (+-0)
+              const float up_mask = (U >= p.clamp_min && U <= p.clamp_max) ? 1.0f : 0.0f;
+              const float gate_mask = (G <= p.clamp_max) ? 1.0f : 0.0f;
+              x[i] = ref * pr * t * up_mask;                                                        // d up
+              gv[i] = ref * pr * uo * sg * (1.0f + p.geglu_a * gc * (1.0f - sg)) * gate_mask;      // d gate
+            }
           }
           output_chunk<FP4, OUTC>(p, x, row, xo, norm, lane, kblk_col, amax_local);
           output_chunk<FP4, OUTC>(p, gv, row, go, norm, lane, kblk_col, amax_local2);

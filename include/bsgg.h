@@ -39,7 +39,7 @@
  *      padded_offsets int32 (L), alpha float (L), prob float (m_pad),
  *      norm_const float (1)
  *      D, D_col (m_pad, N_out)  N-major; N_out = N/2 for SWIGLU/GEGLU, 2N for
- *                               DSWIGLU, else N;
+ *                               DSWIGLU/DGEGLU, else N;
  *                               bf16/f16/f32, or 1-byte FP8 codes, or packed FP4
  *      C        (m_pad, N)      N-major, bf16/f16 (optional pre-activation output)
  *      bias     (L, N)          N contiguous, bf16/f16/f32 (optional)
@@ -104,7 +104,13 @@ typedef enum {
  *   32-column blocks;  D = [ref*prob*swish(G) | ref*prob*X*sigmoid(G)*(1 + G*(1 - sigmoid(G)))]
  *   in C's block order (width 2N);  dprob[m] += sum_n X*swish(G)*ref. */
 typedef enum {
-  BSGG_EPI_GATE = 0, BSGG_EPI_SWIGLU = 1, BSGG_EPI_SRELU = 2, BSGG_EPI_GEGLU = 3, BSGG_EPI_DSWIGLU = 4
+  BSGG_EPI_GATE = 0, BSGG_EPI_SWIGLU = 1, BSGG_EPI_SRELU = 2, BSGG_EPI_GEGLU = 3, BSGG_EPI_DSWIGLU = 4,
+  BSGG_EPI_DGEGLU = 5   /* dGeGLU backward (same page): the saved C unscaled (beta not read),
+                           gate G clamped above at clamp_max, up U clamped to [clamp_min,
+                           clamp_max]; s = sigmoid(a * Gc);
+                           d gate = ref*prob*(Uc + offset)*s*(1 + a*Gc*(1 - s)) if G <= clamp_max,
+                           d up = ref*prob*Gc*s if clamp_min <= U <= clamp_max, else 0;
+                           dprob[m] += sum_n ref*Gc*s*(Uc + offset) */
 } bsgg_epilogue;
 
 /* Problem description, fixed at plan creation (the pages' constructor +
@@ -167,6 +173,13 @@ typedef struct {
      rht_norm_const, whatever the input's scale type).  Forward epilogues only. */
   int32_t want_rht;
   int32_t rht_format;
+  /* DGEGLU: 0 = the page's defaults (geglu_alpha 1.702, clamp [-7, 7], linear_offset 1),
+     1 = the four values below (finite, clamp_min <= clamp_max). */
+  int32_t dgeglu_custom;
+  float dgeglu_alpha;
+  float dgeglu_clamp_min;
+  float dgeglu_clamp_max;
+  float dgeglu_linear_offset;
 } bsgg_desc;
 
 /* Tensors of one call.  Unused outputs may be NULL: d_col/sfd_col unless
@@ -196,8 +209,9 @@ typedef struct {
      BSGG_ERR_BAD_POINTERS from bsgg_query_device_status, and nothing is written). */
   const int64_t* b_ptrs;
   const int64_t* sfb_ptrs;
-  /* DSWIGLU only: the saved forward C (m_pad, 2N) N-major in saved_c_format, its
-     per-group scale beta (L), and dprob (m_pad), which the kernel ACCUMULATES into:
+  /* DSWIGLU and DGEGLU: the saved forward C (m_pad, 2N) N-major in saved_c_format,
+     its per-group scale beta (L; DSWIGLU only), and dprob (m_pad), which the kernel
+     ACCUMULATES into:
      zero it before the call ("Grouped GEMM + dGLU (SM100)": dprob must be
      zero-initialized).  amax then holds 2L floats: [2g] over the input-gradient
      blocks, [2g + 1] over the gate-gradient blocks of group g. */

@@ -111,6 +111,9 @@ def _create(**over):
     (dict(epilogue="dswiglu", tanh_clamp_s=4.0), 1),
     (dict(rht_format="e4m3"), 1), (dict(rht_format="f16"), 1),   # RHT is bf16 or NVFP4
     (dict(epilogue="dswiglu", rht_format="bf16"), 1),            # forward epilogues only
+    (dict(epilogue="dswiglu", dgeglu_params=(1.0, -7.0, 7.0, 1.0)), 1),   # dGeGLU's own
+    (dict(epilogue="dgeglu", dgeglu_params=(1.0, 7.0, -7.0, 1.0)), 1),    # min <= max
+    (dict(epilogue="dgeglu", dgeglu_params=(float("nan"), -7.0, 7.0, 1.0)), 1),
 ])
 def test_create_rejects(lib, over, code):
     assert _create(**over) == code
@@ -124,6 +127,7 @@ def test_create_rejects(lib, over, code):
     dict(discrete_b=True, num_groups=1024),
     dict(epilogue="dswiglu", n=96, saved_c_format="f32", out_format="e4m3", want_col=1),
     dict(epilogue="swiglu", rht_format="e2m1", in_format="nvfp4", out_format="e2m1"),
+    dict(epilogue="dgeglu", dgeglu_params=(1.0, -10.0, 10.0, 0.0)),
 ])
 def test_create_accepts_epilogue_options(lib, over):
     # validation passes: 0 with a GPU, else the device query that follows

@@ -19,24 +19,28 @@ from helpers import oracle_run, small_problem
 pytestmark = pytest.mark.gpu
 
 
-def _run(p, tile=(0, 0), gate_first=False, saved_fmt="bf16", dprob=None):
+def _run(p, tile=(0, 0), gate_first=False, saved_fmt="bf16", dprob=None, dgeglu_params=None):
     pd = to_device(p)
     plan = bsgg.Plan(m_pad=p.m_pad, n=p.n, k=p.k, num_groups=p.num_groups, in_format=p.in_fmt,
-                     out_format=p.out_fmt, epilogue="dswiglu", want_col=p.want_col, gate_first=gate_first,
-                     tile=tuple(tile[:2]), cluster=tuple(tile[2:4]) or (0, 0), saved_c_format=saved_fmt)
+                     out_format=p.out_fmt, epilogue=p.epi, want_col=p.want_col, gate_first=gate_first,
+                     tile=tuple(tile[:2]), cluster=tuple(tile[2:4]) or (0, 0), saved_c_format=saved_fmt,
+                     dgeglu_params=dgeglu_params)
     outs = alloc_outputs(plan)
     if dprob is None:
         dprob = torch.zeros(p.m_pad, dtype=torch.float32, device="cuda")
     norm = torch.tensor([p.norm_const], dtype=torch.float32, device="cuda")
     plan.run(a=pd.a, sfa=bsgg.pack_sf(pd.sfa_rows), b=pd.b, sfb=bsgg.pack_sf(pd.sfb_rows),
              padded_offsets=pd.padded_offsets, alpha=pd.alpha, prob=pd.prob, norm_const=norm,
-             saved_c=pd.saved_c, beta=pd.beta, dprob=dprob, **outs)
+             saved_c=pd.saved_c, beta=pd.beta if p.epi == "dswiglu" else None, dprob=dprob, **outs)
     assert plan.device_status() == 0
     return plan, outs, dprob
 
 
-def _check(p, outs, dprob, gate_first=False):
-    ref = oracle_run(p, gate_first=int(gate_first))
+def _check(p, outs, dprob, gate_first=False, dgeglu_params=None):
+    over = {}
+    if dgeglu_params is not None:
+        over = dict(zip(("geglu_alpha", "glu_clamp_min", "glu_clamp_max", "linear_offset"), dgeglu_params))
+    ref = oracle_run(p, gate_first=int(gate_first), **over)
     compare(p, outs, ref)
     if "amax" in outs:
         np.testing.assert_allclose(outs["amax"].cpu().numpy(), ref["amax"], rtol=2.0 ** -10, atol=0)
@@ -108,3 +112,33 @@ def test_backward_requires_its_inputs():
         with pytest.raises(bsgg.BsggError) as e:
             plan.run(**base, **extra)
         assert e.value.code == 1
+
+
+@pytest.mark.parametrize("gate_first", [False, True])
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
+def test_dgeglu_bf16_with_clamped_values(tile, gate_first):
+    # saved C ~ N(0, 8): many values beyond the +-7 clamp, masks and clamps hit
+    p = small_problem(counts=(130, 0, 256, 40), k=256, n=256, pad_to=128, epi="dgeglu", out_fmt="bf16",
+                      seed=90)
+    p.saved_c = (p.saved_c.float() * 4.0).to(torch.bfloat16)
+    plan, outs, dprob = _run(p, tile, gate_first)
+    _check(p, outs, dprob, gate_first)
+
+
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
+def test_dgeglu_custom_params_e4m3(tile):
+    # the clamped-SwiGLU configuration the page gives: alpha 1, offset 0, +-10
+    params = (1.0, -10.0, 10.0, 0.0)
+    p = small_problem(counts=(200, 77), k=384, n=96, pad_to=128, epi="dgeglu", out_fmt="e4m3",
+                      want_col=True, seed=91)
+    p.saved_c = (p.saved_c.float() * 5.0).to(torch.bfloat16)
+    plan, outs, dprob = _run(p, tile, dgeglu_params=params)
+    _check(p, outs, dprob, dgeglu_params=params)
+
+
+def test_dgeglu_nvfp4_f16_saved_c():
+    p = small_problem(counts=(150, 0, 300), k=512, n=128, pad_to=128, in_fmt="nvfp4", epi="dgeglu",
+                      out_fmt="e2m1", want_col=True, seed=92)
+    p.saved_c = (p.saved_c.float() * 4.0).to(torch.float16)
+    plan, outs, dprob = _run(p, saved_fmt="f16")
+    _check(p, outs, dprob)
