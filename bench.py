@@ -194,7 +194,7 @@ def oracle_inputs(p):
     np_ = lambda t: t.detach().cpu().contiguous().numpy()
     ins = dict(a=np_(p.a), b=np_(p.b), sfa=orc.pack_sf(np_(p.sfa_rows)), sfb=orc.pack_sf(np_(p.sfb_rows)),
                padded_offsets=np_(p.padded_offsets), alpha=np_(p.alpha), prob=np_(p.prob))
-    if p.epi in ("dswiglu", "dgeglu"):
+    if p.saved_c is not None:
         ins.update(saved_c=np_(p.saved_c.double()), beta=np_(p.beta))
     return ins
 
@@ -207,7 +207,7 @@ def oracle_sample(p, ins, budget_s: float, max_blocks: int = 64, seed: int = 0):
     code_out = {"bf16": orc.OUT_BF16, "f16": orc.OUT_F16, "f32": orc.OUT_F32, "e4m3": orc.OUT_E4M3,
                 "e5m2": orc.OUT_E5M2, "e2m1": orc.OUT_E2M1}
     code_epi = {"gate": orc.EPI_GATE, "swiglu": orc.EPI_SWIGLU, "srelu": orc.EPI_SRELU, "geglu": orc.EPI_GEGLU,
-                "dswiglu": orc.EPI_DSWIGLU, "dgeglu": orc.EPI_DGEGLU}
+                "dswiglu": orc.EPI_DSWIGLU, "dgeglu": orc.EPI_DGEGLU, "dsituglu": orc.EPI_DSITUGLU}
     off = ins["padded_offsets"]
     starts = np.concatenate([[0], off[:-1]])
     real_blocks = np.unique(np.concatenate(
@@ -241,7 +241,8 @@ def make_workload(name: str, device):
 def algorithmic_bytes(p) -> int:
     """Bytes a launch must move at least: A, SFA, the B and SFB slices of the
     non-empty groups, and the outputs (D, D_col, SFD_row, SFD_col or amax);
-    for the dSwiGLU backward also the saved C read and dprob written."""
+    for the backward epilogues also the saved C read and dprob written."""
+    from block_scaled_grouped_gb300 import workloads as W
     def cdiv(a, b):
         return -(-a // b)
 
@@ -259,9 +260,9 @@ def algorithmic_bytes(p) -> int:
     if p.out_fmt in ("e4m3", "e5m2", "e2m1"):
         out += sfb(p.m_pad, n_out, v) + (sfb(n_out, p.m_pad, v) if p.want_col else 0)
     else:
-        out += 4 * p.num_groups * (2 if p.epi in ("dswiglu", "dgeglu") else 1)
+        out += 4 * p.num_groups * (2 if p.epi in W.BWD_EPILOGUES else 1)
     extra = 0
-    if p.epi in ("dswiglu", "dgeglu"):
+    if p.epi in W.BWD_EPILOGUES:
         extra = p.saved_c.numel() * p.saved_c.element_size() + 4 * p.m_pad + 4 * p.num_groups
     return (p.m_pad * kb + sfb(p.m_pad, p.k, v) + nonempty * p.n * kb + sfb(p.n, p.k, v, nonempty) + out
             + extra)
@@ -337,7 +338,7 @@ def run_gpu(args, world, rank, local):
     norm = torch.tensor([p.norm_const], dtype=torch.float32, device=dev)
     tensors = dict(a=p.a, sfa=sfa, b=p.b, sfb=sfb, padded_offsets=p.padded_offsets, alpha=p.alpha,
                    prob=p.prob, norm_const=norm, **outs)
-    if p.epi in ("dswiglu", "dgeglu"):
+    if p.saved_c is not None:
         # the backward's saved C and beta, and dprob (accumulated across steps:
         # the timing does not depend on its values)
         tensors.update(saved_c=p.saved_c, beta=p.beta,

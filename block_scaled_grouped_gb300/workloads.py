@@ -33,7 +33,8 @@ import torch
 
 IN_FORMATS = ("mxfp8_e4m3", "mxfp8_e5m2", "nvfp4")
 OUT_FORMATS = ("bf16", "f16", "f32", "e4m3", "e5m2", "e2m1")
-EPILOGUES = ("gate", "swiglu", "srelu", "geglu", "dswiglu", "dgeglu")
+EPILOGUES = ("gate", "swiglu", "srelu", "geglu", "dswiglu", "dgeglu", "dsituglu")
+BWD_EPILOGUES = ("dswiglu", "dgeglu", "dsituglu")
 
 _ROW_CHUNK = 4096
 
@@ -73,7 +74,7 @@ class Problem:
     def n_out(self) -> int:
         if self.epi in ("swiglu", "geglu"):
             return self.n // 2
-        return 2 * self.n if self.epi in ("dswiglu", "dgeglu") else self.n
+        return 2 * self.n if self.epi in BWD_EPILOGUES else self.n
 
     @property
     def m_real(self) -> int:
@@ -335,7 +336,7 @@ def build_problem(*, name: str, counts: Sequence[int], k: int, n: int, in_fmt: s
     # pre-activation's typical spread), and beta ~ U(0.5, 2) per group (read
     # by dSwiGLU only)
     saved_c = beta = None
-    if epi in ("dswiglu", "dgeglu"):
+    if epi in BWD_EPILOGUES:
         beta = torch.as_tensor(rng.uniform(0.5, 2.0, size=L).astype(np.float32), device=device)
         saved_c = torch.empty(m_pad, 2 * n, dtype=torch.bfloat16, device=device)
         for c0 in range(0, m_pad, _ROW_CHUNK):

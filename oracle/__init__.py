@@ -29,7 +29,8 @@ _lib = None
 F_E4M3, F_E5M2, F_E2M1, F_UE8M0 = 0, 1, 2, 3
 IN_MXFP8_E4M3, IN_MXFP8_E5M2, IN_NVFP4 = 0, 1, 2
 OUT_BF16, OUT_F16, OUT_F32, OUT_E4M3, OUT_E5M2, OUT_E2M1 = 0, 1, 2, 3, 4, 5
-EPI_GATE, EPI_SWIGLU, EPI_SRELU, EPI_GEGLU, EPI_DSWIGLU, EPI_DGEGLU = 0, 1, 2, 3, 4, 5
+EPI_GATE, EPI_SWIGLU, EPI_SRELU, EPI_GEGLU, EPI_DSWIGLU, EPI_DGEGLU, EPI_DSITUGLU = 0, 1, 2, 3, 4, 5, 6
+BWD_EPIS = (EPI_DSWIGLU, EPI_DGEGLU, EPI_DSITUGLU)
 
 
 class OrcDesc(ctypes.Structure):
@@ -41,6 +42,7 @@ class OrcDesc(ctypes.Structure):
         ("tanh_clamp_s", ctypes.c_double), ("glu_limit", ctypes.c_double), ("glu_alpha", ctypes.c_double),
         ("rht_norm", ctypes.c_double), ("geglu_alpha", ctypes.c_double), ("glu_clamp_min", ctypes.c_double),
         ("glu_clamp_max", ctypes.c_double), ("linear_offset", ctypes.c_double),
+        ("situ_beta1", ctypes.c_double), ("situ_beta2", ctypes.c_double),
     ]
 
 
@@ -154,14 +156,14 @@ def hadamard16(i: int, j: int) -> float:
 def n_out(n: int, epi: int) -> int:
     if epi in (EPI_SWIGLU, EPI_GEGLU):
         return n // 2
-    return 2 * n if epi in (EPI_DSWIGLU, EPI_DGEGLU) else n
+    return 2 * n if epi in BWD_EPIS else n
 
 
 def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded_offsets,
         alpha, prob, norm_const=1.0, tanh_clamp_s=0.0, gate_first=0, want_col=False,
         blocks=None, threads=None, outputs=None, bias=None, glu_limit=0.0, glu_alpha=1.0,
         want_c=False, saved_c=None, beta=None, rht=None, rht_norm=1.0, geglu_alpha=1.702,
-        glu_clamp_min=-7.0, glu_clamp_max=7.0, linear_offset=1.0):
+        glu_clamp_min=-7.0, glu_clamp_max=7.0, linear_offset=1.0, situ_beta1=1.0, situ_beta2=1.0):
     """Run the oracle on the listed 32-row blocks (default: all of them).
 
     Inputs are numpy arrays in the device layouts: ``a`` (m_pad, k or k/2)
@@ -179,7 +181,9 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     entries (input-gradient and gate-gradient blocks of each group).  The dGeGLU
     backward (``epi=EPI_DGEGLU``) takes the saved C unscaled and
     ``geglu_alpha``, ``glu_clamp_min``/``glu_clamp_max`` and ``linear_offset``
-    (the page's defaults 1.702, -7, 7, 1).
+    (the page's defaults 1.702, -7, 7, 1); the dSiTU-GLU backward
+    (``epi=EPI_DSITUGLU``) takes the saved C unscaled and ``situ_beta1``,
+    ``situ_beta2``.
     ``rht`` ("bf16" or "e2m1") adds the rowwise Hadamard output: ``rht_ref``
     (fp64) and, for "e2m1", full-size ``rht_q`` / ``sfrht`` buffers (E4M3
     scales per 16 under ``rht_norm``).
@@ -189,7 +193,7 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     desc = OrcDesc(m_pad, n, k, num_groups, in_fmt, out_fmt, epi, int(gate_first),
                    int(bool(want_col)), rht_code, float(tanh_clamp_s), float(glu_limit), float(glu_alpha),
                    float(rht_norm), float(geglu_alpha), float(glu_clamp_min), float(glu_clamp_max),
-                   float(linear_offset))
+                   float(linear_offset), float(situ_beta1), float(situ_beta2))
     nd = n_out(n, epi)
     if blocks is None:
         blocks = np.arange(m_pad // 32, dtype=np.int64)
@@ -199,7 +203,7 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     d_ref = np.zeros((blocks.size * 32, nd), dtype=np.float64)
     c_ref = np.zeros((blocks.size * 32, n), dtype=np.float64) if want_c else None
     bias_arr = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32).reshape(num_groups, n)
-    bwd = epi in (EPI_DSWIGLU, EPI_DGEGLU)
+    bwd = epi in BWD_EPIS
     amax = np.zeros(2 * num_groups if bwd else num_groups, dtype=np.float32)
     rht_ref = np.zeros((blocks.size * 32, nd), dtype=np.float64) if rht_code else None
     dprob_ref = np.zeros(blocks.size * 32, dtype=np.float64) if bwd else None

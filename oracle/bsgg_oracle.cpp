@@ -161,8 +161,12 @@ int64_t sf_bytes(int64_t rows, int64_t kblocks, int64_t L) {
 // ---------------------------------------------------------------------------
 enum InFmt { IN_MXFP8_E4M3 = 0, IN_MXFP8_E5M2 = 1, IN_NVFP4 = 2 };
 enum OutFmt { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2, OUT_E4M3 = 3, OUT_E5M2 = 4, OUT_E2M1 = 5 };
-// EPI_DSWIGLU, EPI_DGEGLU: the backward epilogues of "Grouped GEMM + dGLU (SM100)".
-enum Epi { EPI_GATE = 0, EPI_SWIGLU = 1, EPI_SRELU = 2, EPI_GEGLU = 3, EPI_DSWIGLU = 4, EPI_DGEGLU = 5 };
+// EPI_DSWIGLU, EPI_DGEGLU, EPI_DSITUGLU: the backward epilogues of "Grouped GEMM +
+// dGLU (SM100)".
+enum Epi {
+  EPI_GATE = 0, EPI_SWIGLU = 1, EPI_SRELU = 2, EPI_GEGLU = 3, EPI_DSWIGLU = 4, EPI_DGEGLU = 5,
+  EPI_DSITUGLU = 6
+};
 
 }  // namespace
 
@@ -183,6 +187,8 @@ typedef struct {
   // dGeGLU ("Grouped GEMM + dGLU (SM100)", Block-scaled contract, Step 2):
   // sigmoid slope, clamp bounds and the offset added to the clamped up value
   double geglu_alpha, glu_clamp_min, glu_clamp_max, linear_offset;
+  // dSiTU-GLU (same page, Equations): the tanh scales beta1 (gate) and beta2 (up)
+  double situ_beta1, situ_beta2;
 } orc_desc;
 
 // ---- exported helpers (pinned individually by the tests) ----
@@ -323,7 +329,9 @@ double q_max(const orc_desc* P) {
   return P->out_fmt == OUT_E4M3 ? 448.0 : P->out_fmt == OUT_E5M2 ? 57344.0 : 6.0;
 }
 bool is_glu(const orc_desc* P) { return P->epi == EPI_SWIGLU || P->epi == EPI_GEGLU; }
-bool is_bwd(const orc_desc* P) { return P->epi == EPI_DSWIGLU || P->epi == EPI_DGEGLU; }
+bool is_bwd(const orc_desc* P) {
+  return P->epi == EPI_DSWIGLU || P->epi == EPI_DGEGLU || P->epi == EPI_DSITUGLU;
+}
 // D width: N/2 for the forward GLUs (two C blocks per D block), 2N for the
 // backward (two gradient blocks per GEMM block), else N.
 int64_t n_out(const orc_desc* P) { return is_glu(P) ? P->n / 2 : is_bwd(P) ? 2 * P->n : P->n; }
@@ -460,7 +468,7 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
       const int64_t b = jr / 32, r = jr % 32;
       const bool second = (gate != bool(P->gate_first));
       const double c = J.saved_c[m * 2 * P->n + 64 * b + (second ? 32 : 0) + r];
-      return P->epi == EPI_DSWIGLU ? double(J.beta[g]) * c : c;
+      return P->epi == EPI_DSWIGLU ? double(J.beta[g]) * c : c;   // (reading: dSiTU-GLU unscaled too)
     };
     // dGeGLU: the gate has only an upper clamp, the up value both; the masks
     // test the values before clamping and keep the gradient at either bound
@@ -474,12 +482,28 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
       d_up = ref * p * gc * s * up_mask;
       dprob_term = ref * gc * s * (uc + P->linear_offset);
     };
+    // dSiTU-GLU: T_g = b1 tanh(G/b1) sigmoid(G), T_u = b2 tanh(U/b2); the
+    // gate gradient is ref prob T_u dT_g/dG, the up gradient ref prob T_g dT_u/dU
+    auto dsitu = [&](double up, double gate, double ref, double& d_up, double& d_gate, double& dprob_term) {
+      const double b1 = P->situ_beta1, b2 = P->situ_beta2;
+      const double th_g = std::tanh(gate / b1), th_u = std::tanh(up / b2), sg = orc_sigmoid(gate);
+      const double t_g = b1 * th_g * sg, t_u = b2 * th_u;
+      const double dtg = (1.0 - th_g * th_g) * sg + b1 * th_g * sg * (1.0 - sg);
+      const double dtu = 1.0 - th_u * th_u;
+      d_gate = ref * p * t_u * dtg;
+      d_up = ref * p * t_g * dtu;
+      dprob_term = ref * t_g * t_u;
+    };
     if (is_bwd(P)) {
       // dprob += sum over the GEMM columns of ref times the activation
       for (int64_t jr = c0; jr < c1; ++jr) {
         const double x = saved(jr, false), gt = saved(jr, true);
         if (P->epi == EPI_DSWIGLU) {
           dprob_local[size_t(i)] += x * (gt * orc_sigmoid(gt)) * Cv(jr);
+        } else if (P->epi == EPI_DSITUGLU) {
+          double du, dg, t;
+          dsitu(x, gt, Cv(jr), du, dg, t);
+          dprob_local[size_t(i)] += t;
         } else {
           double du, dg, t;
           dgeglu(x, gt, Cv(jr), du, dg, t);
@@ -504,7 +528,8 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
           else d = ref * p * x * sg * (1.0 + gt * (1.0 - sg));          // d gate
         } else {
           double du, dg, t;
-          dgeglu(x, gt, ref, du, dg, t);
+          if (P->epi == EPI_DSITUGLU) dsitu(x, gt, ref, du, dg, t);
+          else dgeglu(x, gt, ref, du, dg, t);
           d = is_input ? du : dg;
         }
         amax_idx = 2 * g + (is_input ? 0 : 1);

@@ -13,7 +13,7 @@ IN_CODE = {"mxfp8_e4m3": orc.IN_MXFP8_E4M3, "mxfp8_e5m2": orc.IN_MXFP8_E5M2, "nv
 OUT_CODE = {"bf16": orc.OUT_BF16, "f16": orc.OUT_F16, "f32": orc.OUT_F32, "e4m3": orc.OUT_E4M3,
             "e5m2": orc.OUT_E5M2, "e2m1": orc.OUT_E2M1}
 EPI_CODE = {"gate": orc.EPI_GATE, "swiglu": orc.EPI_SWIGLU, "srelu": orc.EPI_SRELU, "geglu": orc.EPI_GEGLU,
-            "dswiglu": orc.EPI_DSWIGLU, "dgeglu": orc.EPI_DGEGLU}
+            "dswiglu": orc.EPI_DSWIGLU, "dgeglu": orc.EPI_DGEGLU, "dsituglu": orc.EPI_DSITUGLU}
 
 E2M1_VALUES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
                         -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0])
@@ -33,7 +33,7 @@ def oracle_inputs(p: W.Problem) -> dict:
 def oracle_run(p: W.Problem, blocks=None, inputs=None, gate_first=0, threads=None, **over):
     ins = inputs if inputs is not None else oracle_inputs(p)
     ins = dict(ins)
-    if p.epi in ("dswiglu", "dgeglu"):
+    if p.epi in W.BWD_EPILOGUES:
         ins.setdefault("saved_c", np_(p.saved_c.double()))
         ins.setdefault("beta", np_(p.beta))
     ins.update(over)

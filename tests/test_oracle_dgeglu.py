@@ -11,6 +11,11 @@ Block-scaled contract, Step 2, dGeGLU):
 * geglu_alpha = 1 and linear_offset = 0 make dGeGLU the dSwiGLU of the same
   saved C (beta = 1), itself pinned by finite differences;
 * beta is not read.
+
+And for the dSiTU-GLU backward (same page, Equations): the gradients against
+central finite differences of the page's defining product T_g * T_u
+(T_g = b1 tanh(G/b1) sigmoid(G), T_u = b2 tanh(U/b2)) for several b1, b2, dprob
+against ref * T_g * T_u, and closed forms at G = 0 and U = 0.
 """
 import numpy as np
 import pytest
@@ -132,3 +137,36 @@ def test_beta_is_not_read():
     _, _, o2 = _backward(pts, REF_CODES[:2], beta=3.0)
     assert np.array_equal(o1["d_ref"], o2["d_ref"])
     assert np.array_equal(o1["dprob_ref"], o2["dprob_ref"])
+
+
+# ---------------------------------------------------------------- dSiTU-GLU
+def _situ_forward(u, g, b1, b2):
+    """The page's definitions: T_g = b1 tanh(G/b1) sigmoid(G), T_u = b2 tanh(U/b2);
+    the gradients returned are those of T_g * T_u."""
+    return b1 * np.tanh(g / b1) * _sig(g) * (b2 * np.tanh(u / b2))
+
+
+@pytest.mark.parametrize("b1,b2", [(1.0, 1.0), (2.0, 0.5), (8.0, 8.0)])
+def test_dsitu_gradients_are_finite_differences(b1, b2):
+    pts = [(_bf16(u), _bf16(g)) for u, g in POINTS]
+    d_up, d_gate, out = _backward(pts, REF_CODES, prob=0.75, epi="dsituglu", situ_beta1=b1, situ_beta2=b2)
+    u = np.array([q[0] for q in pts])
+    g = np.array([q[1] for q in pts])
+    h = 1e-6
+    dfdu = (_situ_forward(u + h, g, b1, b2) - _situ_forward(u - h, g, b1, b2)) / (2 * h)
+    dfdg = (_situ_forward(u, g + h, b1, b2) - _situ_forward(u, g - h, b1, b2)) / (2 * h)
+    np.testing.assert_allclose(d_up, REF * 0.75 * dfdu, rtol=1e-6, atol=1e-10)
+    np.testing.assert_allclose(d_gate, REF * 0.75 * dfdg, rtol=1e-6, atol=1e-10)
+    np.testing.assert_allclose(out["dprob_ref"][0], 32 * np.sum(REF * _situ_forward(u, g, b1, b2)), rtol=1e-12)
+
+
+def test_dsitu_closed_forms():
+    # G = 0: T_g = 0, dT_g/dG = 1/2; U = 0: T_u = 0, dT_u/dU = 1
+    d_up, d_gate, out = _backward([(0.0, 0.0), (1.0, 0.0), (0.0, 1.0)], [0x40] * 3, prob=0.5, epi="dsituglu",
+                                  situ_beta1=2.0, situ_beta2=3.0)
+    assert d_up[0] == 0.0 and d_gate[0] == 0.0            # T_u = 0 and T_g = 0
+    np.testing.assert_allclose(d_gate[1], 2 * 0.5 * 3.0 * np.tanh(1.0 / 3.0) * 0.5, rtol=1e-15)
+    assert d_up[1] == 0.0                                 # T_g = 0 at G = 0
+    tg = 2.0 * np.tanh(0.5) * _sig(1.0)
+    np.testing.assert_allclose(d_up[2], 2 * 0.5 * tg * 1.0, rtol=1e-15)
+    np.testing.assert_allclose(out["dprob_ref"][0], 0.0, atol=0)
