@@ -16,8 +16,8 @@ from . import build as _build
 
 IN_FORMATS = {"mxfp8_e4m3": 0, "mxfp8_e5m2": 1, "nvfp4": 2}
 OUT_FORMATS = {"bf16": 0, "f16": 1, "f32": 2, "e4m3": 3, "e5m2": 4, "e2m1": 5}
-EPILOGUES = {"gate": 0, "swiglu": 1, "srelu": 2, "geglu": 3, "dswiglu": 4, "dgeglu": 5}
-BWD_EPILOGUES = ("dswiglu", "dgeglu")
+EPILOGUES = {"gate": 0, "swiglu": 1, "srelu": 2, "geglu": 3, "dswiglu": 4, "dgeglu": 5, "dsituglu": 6}
+BWD_EPILOGUES = ("dswiglu", "dgeglu", "dsituglu")
 GLU_EPILOGUES = ("swiglu", "geglu")
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
           4: "device wait timed out", 5: "padded_offsets invalid", 6: "expert weight pointer invalid"}
@@ -47,7 +47,8 @@ class Desc(ctypes.Structure):
                 ("want_rht", ctypes.c_int32), ("rht_format", ctypes.c_int32),
                 ("dgeglu_custom", ctypes.c_int32), ("dgeglu_alpha", ctypes.c_float),
                 ("dgeglu_clamp_min", ctypes.c_float), ("dgeglu_clamp_max", ctypes.c_float),
-                ("dgeglu_linear_offset", ctypes.c_float)]
+                ("dgeglu_linear_offset", ctypes.c_float), ("situ_beta1", ctypes.c_float),
+                ("situ_beta2", ctypes.c_float)]
 
 
 def make_desc(*, m_pad: int, n: int, k: int, num_groups: int, in_format: str, out_format: str,
@@ -56,14 +57,15 @@ def make_desc(*, m_pad: int, n: int, k: int, num_groups: int, in_format: str, ou
               glu_alpha: float = 0.0, c_format: Optional[str] = None,
               bias_format: Optional[str] = None, discrete_b: bool = False,
               saved_c_format: str = "bf16", rht_format: Optional[str] = None,
-              dgeglu_params: Optional[tuple] = None) -> "Desc":
+              dgeglu_params: Optional[tuple] = None, situ_betas: Optional[tuple] = None) -> "Desc":
     """A bsgg_desc.  c_format ("bf16"/"f16") asks for the pre-activation C
     output, bias_format ("bf16"/"f16"/"f32") for a bias; None = neither.
     discrete_b: per-expert weights through the b_ptrs / sfb_ptrs arrays.
     saved_c_format: storage type of the saved C read by the dSwiGLU backward.
     rht_format ("bf16"/"e2m1"): the rowwise Hadamard output; None = none.
     dgeglu_params: (geglu_alpha, clamp_min, clamp_max, linear_offset) of the
-    dGeGLU backward; None = the page's defaults (1.702, -7, 7, 1)."""
+    dGeGLU backward; None = the page's defaults (1.702, -7, 7, 1).
+    situ_betas: (beta1, beta2) of the dSiTU-GLU backward; None = (1, 1)."""
     dg = tuple(float(x) for x in dgeglu_params) if dgeglu_params is not None else (0.0, 0.0, 0.0, 0.0)
     return Desc(m_pad, n, k, num_groups, IN_FORMATS[in_format], OUT_FORMATS[out_format],
                 EPILOGUES[epilogue], int(bool(want_col)), int(bool(gate_first)), float(tanh_clamp_s),
@@ -71,7 +73,8 @@ def make_desc(*, m_pad: int, n: int, k: int, num_groups: int, in_format: str, ou
                 float(glu_alpha), int(c_format is not None), OUT_FORMATS[c_format or "bf16"],
                 int(bias_format is not None), OUT_FORMATS[bias_format or "bf16"], int(bool(discrete_b)),
                 OUT_FORMATS[saved_c_format], int(rht_format is not None), OUT_FORMATS[rht_format or "bf16"],
-                int(dgeglu_params is not None), *dg)
+                int(dgeglu_params is not None), *dg,
+                *(tuple(float(x) for x in situ_betas) if situ_betas is not None else (0.0, 0.0)))
 
 
 class Args(ctypes.Structure):
@@ -284,7 +287,7 @@ def measure_mma_peak(in_format: str, tile_n: int = 256, mmas_per_sm: int = 40000
 
 _DESC_KEYS = ("m_pad", "n", "k", "num_groups", "in_format", "out_format", "epilogue", "want_col",
               "gate_first", "tanh_clamp_s", "tile", "cluster", "glu_limit", "glu_alpha", "c_format",
-              "bias_format", "discrete_b", "saved_c_format", "rht_format", "dgeglu_params")
+              "bias_format", "discrete_b", "saved_c_format", "rht_format", "dgeglu_params", "situ_betas")
 
 
 def run_noalloc(*, stream=None, wait_status: bool = True, **kw) -> int:

@@ -66,6 +66,12 @@ uint64_t sf_bytes_impl(int64_t rows, int64_t cols, int64_t v, int64_t L) {
 
 bool is_quant(int out) { return out == BSGG_OUT_E4M3 || out == BSGG_OUT_E5M2 || out == BSGG_OUT_E2M1; }
 
+// The backward epilogues ("Grouped GEMM + dGLU (SM100)"): GEMM scaled by alpha^2,
+// the saved C read, D twice as wide as the GEMM, dprob accumulated.
+bool is_bwd_epi(int epi) {
+  return epi == BSGG_EPI_DSWIGLU || epi == BSGG_EPI_DGEGLU || epi == BSGG_EPI_DSITUGLU;
+}
+
 int out_elem_bits(int out) {
   switch (out) {
     case BSGG_OUT_BF16: case BSGG_OUT_F16: return 16;
@@ -100,9 +106,13 @@ bsgg_status validate(const bsgg_desc* d) {
     return BSGG_ERR_INVALID_ARG;
   if (d->in_format < BSGG_IN_MXFP8_E4M3 || d->in_format > BSGG_IN_NVFP4) return BSGG_ERR_INVALID_ARG;
   if (d->out_format < BSGG_OUT_BF16 || d->out_format > BSGG_OUT_E2M1) return BSGG_ERR_INVALID_ARG;
-  if (d->epilogue < BSGG_EPI_GATE || d->epilogue > BSGG_EPI_DGEGLU) return BSGG_ERR_INVALID_ARG;
+  if (d->epilogue < BSGG_EPI_GATE || d->epilogue > BSGG_EPI_DSITUGLU) return BSGG_ERR_INVALID_ARG;
   const bool glu = d->epilogue == BSGG_EPI_SWIGLU || d->epilogue == BSGG_EPI_GEGLU;
-  const bool bwd = d->epilogue == BSGG_EPI_DSWIGLU || d->epilogue == BSGG_EPI_DGEGLU;
+  const bool bwd = is_bwd_epi(d->epilogue);
+  // dSiTU-GLU's tanh scales: finite, > 0 (0 = 1); nothing else reads them
+  if (!std::isfinite(d->situ_beta1) || !std::isfinite(d->situ_beta2) || d->situ_beta1 < 0.0f ||
+      d->situ_beta2 < 0.0f || (d->epilogue != BSGG_EPI_DSITUGLU && (d->situ_beta1 != 0.0f || d->situ_beta2 != 0.0f)))
+    return BSGG_ERR_INVALID_ARG;
   if (d->dgeglu_custom != 0 && d->dgeglu_custom != 1) return BSGG_ERR_INVALID_ARG;
   if (d->dgeglu_custom &&
       (d->epilogue != BSGG_EPI_DGEGLU || !std::isfinite(d->dgeglu_alpha) || !std::isfinite(d->dgeglu_clamp_min) ||
@@ -239,7 +249,7 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
   // accumulator columns per thread and runs without register spills (measured
   // on GB300: 1418 TFLOP/s on the FC1 backward against 582 with 256 x 256
   // pairs, whose epilogue spills to local memory).
-  const bool bwd = desc->epilogue == BSGG_EPI_DSWIGLU || desc->epilogue == BSGG_EPI_DGEGLU;
+  const bool bwd = is_bwd_epi(desc->epilogue);
   int tm = desc->tile_m, tn = desc->tile_n, cm = desc->cluster_m;
   if (tm == 0) tm = (desc->in_format != BSGG_IN_NVFP4 && tn != 128 && cm != 1 && !bwd) ? 256 : 128;
   if (tn == 0) tn = (bwd && tm == 128 && cm != 2) ? 128 : 256;
@@ -249,17 +259,18 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
   P->bn = P->pair ? 256 : tn;
   // GeGLU runs in the SwiGLU instances (Params::glu_kind selects the activation)
   // the dGeGLU backward runs in the dSwiGLU instances (Params::bwd_kind)
-  P->epi = desc->epilogue == BSGG_EPI_GEGLU                                              ? bsgg::EPI_SWIGLU
-           : (desc->epilogue == BSGG_EPI_DSWIGLU || desc->epilogue == BSGG_EPI_DGEGLU) ? bsgg::EPI_DSWIGLU
-                                                                                        : desc->epilogue;
+  P->epi = desc->epilogue == BSGG_EPI_GEGLU ? bsgg::EPI_SWIGLU
+           : desc->epilogue == BSGG_EPI_DSITUGLU ? bsgg::EPI_DSITUGLU
+           : is_bwd_epi(desc->epilogue)     ? bsgg::EPI_DSWIGLU
+                                            : desc->epilogue;
   P->outc = desc->out_format == BSGG_OUT_E2M1 ? bsgg::OUTC_FP4
             : is_quant(desc->out_format)      ? bsgg::OUTC_FP8
                                               : bsgg::OUTC_FLOAT;
   P->sf_vec = desc->in_format == BSGG_IN_NVFP4 ? 16 : 32;
   P->kbytes = desc->in_format == BSGG_IN_NVFP4 ? desc->k / 2 : desc->k;
-  P->n_out = (desc->epilogue == BSGG_EPI_SWIGLU || desc->epilogue == BSGG_EPI_GEGLU)    ? desc->n / 2
-             : (desc->epilogue == BSGG_EPI_DSWIGLU || desc->epilogue == BSGG_EPI_DGEGLU) ? 2 * desc->n
-                                                                                         : desc->n;
+  P->n_out = (desc->epilogue == BSGG_EPI_SWIGLU || desc->epilogue == BSGG_EPI_GEGLU) ? desc->n / 2
+             : is_bwd_epi(desc->epilogue)                                             ? 2 * desc->n
+                                                                                      : desc->n;
   P->out_row_bytes = P->n_out * out_elem_bits(desc->out_format) / 8;
   if (P->pair || P->mc) {
     int resident = bsgg::cluster_resident_ctas(desc->in_format == BSGG_IN_NVFP4, P->mc);
@@ -296,7 +307,8 @@ bsgg_status check_args(const bsgg_plan* P, const bsgg_args* a) {
   if (d.want_bias && (!a->bias || !aligned16(a->bias))) return BSGG_ERR_INVALID_ARG;
   if (d.epilogue == BSGG_EPI_DSWIGLU && (!a->saved_c || !aligned16(a->saved_c) || !a->beta || !a->dprob))
     return BSGG_ERR_INVALID_ARG;
-  if (d.epilogue == BSGG_EPI_DGEGLU && (!a->saved_c || !aligned16(a->saved_c) || !a->dprob))
+  if ((d.epilogue == BSGG_EPI_DGEGLU || d.epilogue == BSGG_EPI_DSITUGLU) &&
+      (!a->saved_c || !aligned16(a->saved_c) || !a->dprob))
     return BSGG_ERR_INVALID_ARG;
   if (d.want_rht && (!a->rht || !aligned16(a->rht))) return BSGG_ERR_INVALID_ARG;
   if (d.want_rht && d.rht_format == BSGG_OUT_E2M1 && (!a->sfrht || !a->rht_norm_const))
@@ -450,7 +462,7 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   st = encode_maps(P, a, &L);
   if (st != BSGG_OK) return st;
   // amax: one float per group, two for the backward (input / gate gradients)
-  const int64_t n_amax = d.num_groups * ((d.epilogue == BSGG_EPI_DSWIGLU || d.epilogue == BSGG_EPI_DGEGLU) ? 2 : 1);
+  const int64_t n_amax = d.num_groups * (is_bwd_epi(d.epilogue) ? 2 : 1);
   if (a->amax && cudaMemsetAsync(a->amax, 0, sizeof(float) * n_amax, s) != cudaSuccess)
     return BSGG_ERR_CUDA;
 
@@ -498,12 +510,14 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
     p.rht_kind = d.rht_format == BSGG_OUT_E2M1 ? bsgg::OK_E2M1 : bsgg::OK_BF16;
     p.kq_rht = static_cast<int32_t>(ceil_div(ceil_div(P->n_out, 16), 4));
   }
-  if (d.epilogue == BSGG_EPI_DSWIGLU || d.epilogue == BSGG_EPI_DGEGLU) {
+  if (is_bwd_epi(d.epilogue)) {
     p.saved_c = a->saved_c;
     p.saved_c_kind = d.saved_c_format;
     p.beta = a->beta;
     p.dprob = a->dprob;
     p.bwd_kind = d.epilogue == BSGG_EPI_DGEGLU ? 1 : 0;
+    p.situ_b1 = d.situ_beta1 == 0.0f ? 1.0f : d.situ_beta1;
+    p.situ_b2 = d.situ_beta2 == 0.0f ? 1.0f : d.situ_beta2;
     const bool cust = d.dgeglu_custom != 0;
     p.geglu_a = cust ? d.dgeglu_alpha : 1.702f;
     p.clamp_min = cust ? d.dgeglu_clamp_min : -7.0f;
@@ -586,7 +600,7 @@ bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* 
   const uint64_t sz_d = uint64_t(d.m_pad) * P->out_row_bytes;
   const uint64_t sz_sfd_row = sf_bytes_impl(d.m_pad, P->n_out, P->sf_vec, 1);
   const uint64_t sz_sfd_col = sf_bytes_impl(P->n_out, d.m_pad, P->sf_vec, 1);
-  const bool bwd = d.epilogue == BSGG_EPI_DSWIGLU || d.epilogue == BSGG_EPI_DGEGLU;
+  const bool bwd = is_bwd_epi(d.epilogue);
   const uint64_t sz_saved_c = bwd ? uint64_t(d.m_pad) * 2 * d.n * (d.saved_c_format == BSGG_OUT_F32 ? 4 : 2) : 0;
   const uint64_t n_amax = uint64_t(L) * (bwd ? 2 : 1);
   uint64_t in_bytes = 0, out_bytes = 0;

@@ -55,8 +55,11 @@
 namespace bsgg {
 
 // Epilogue instances; EPI_SWIGLU also computes GeGLU (Params::glu_kind);
-// EPI_DSWIGLU is the dSwiGLU backward, and the dGeGLU backward (Params::bwd_kind).
-enum : int { EPI_GATE = 0, EPI_SWIGLU = 1, EPI_SRELU = 2, EPI_DSWIGLU = 3 };
+// EPI_DSWIGLU is the dSwiGLU backward, and the dGeGLU backward (Params::bwd_kind);
+// EPI_DSITUGLU the dSiTU-GLU backward (its tanh and sech^2 need registers the
+// other two instances must not give up).
+enum : int { EPI_GATE = 0, EPI_SWIGLU = 1, EPI_SRELU = 2, EPI_DSWIGLU = 3, EPI_DSITUGLU = 4 };
+__host__ __device__ constexpr bool is_bwd_inst(int epi) { return epi == EPI_DSWIGLU || epi == EPI_DSITUGLU; }
 // Output class (template) and exact output kind (runtime) of D.
 enum : int { OUTC_FLOAT = 0, OUTC_FP8 = 1, OUTC_FP4 = 2 };
 enum : int { OK_BF16 = 0, OK_F16 = 1, OK_F32 = 2, OK_E4M3 = 3, OK_E5M2 = 4, OK_E2M1 = 5 };
@@ -136,6 +139,7 @@ struct Params {
   float* dprob;
   int32_t bwd_kind;         // EPI_DSWIGLU instances: 0 = dSwiGLU, 1 = dGeGLU
   float geglu_a, clamp_min, clamp_max, lin_offset;   // dGeGLU
+  float situ_b1, situ_b2;                            // dSiTU-GLU
   // rowwise Hadamard output of bf16-rounded D ("Grouped GEMM + GLU + Hadamard +
   // Quant (SM100)"): bf16 or NVFP4 with E4M3 scales per 16 (SFRHT)
   void* rht;                // (m_pad, n_out), or null
@@ -1020,7 +1024,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
       // into L2 while the tile's MMAs run (+3.6 % on the FC1 backward).  Holding
       // them in registers instead spills the epilogue to local memory, which
       // misses L1 here (nearly all of it is shared memory): 43 % slower.
-      if (EPI == EPI_DSWIGLU && valid) {
+      if (is_bwd_inst(EPI) && valid) {
         // the saved-C values this thread will read, fetched into L2 while the
         // tile's MMAs run: 2 * kWarpCols values of its row from column
         // 2 * (first GEMM column of its half)
@@ -1084,11 +1088,11 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
       }
       float amax_local = 0.0f;
       float amax_local2 = 0.0f;                       // backward: the gate-gradient blocks
-      if (EPI == EPI_DSWIGLU) {
+      if (is_bwd_inst(EPI)) {
         // dSwiGLU backward ("Grouped GEMM + dGLU (SM100)", Block-scaled contract):
         // GEMM column j of pair b = j / 32 -> D (and saved C) columns 64b + r of
         // the input block and of the gate block, in the forward's block order
-        const float al2 = al * al, bt = p.bwd_kind ? 1.0f : p.beta[g];
+        const float al2 = al * al, bt = (EPI == EPI_DSWIGLU && p.bwd_kind == 0) ? p.beta[g] : 1.0f;
         const bool gf = p.gate_first != 0;
         float dprob_local = 0.0f;
 #pragma unroll
@@ -1101,7 +1105,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
           const int esz = p.saved_c_kind == OK_F32 ? 4 : 2;
           load_f32x32(x, static_cast<const uint8_t*>(p.saved_c) + (srow + xo) * esz, p.saved_c_kind);
           load_f32x32(gv, static_cast<const uint8_t*>(p.saved_c) + (srow + go) * esz, p.saved_c_kind);
-          if (p.bwd_kind == 0) {
+          if (EPI == EPI_DSWIGLU && p.bwd_kind == 0) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float ref = al2 * __uint_as_float(r[32 * c + i]);
@@ -1111,6 +1115,29 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
               dprob_local += X * sw * ref;                              // dprob += X swish(G) ref
               x[i] = ref * pr * sw;                                     // d input
               gv[i] = ref * pr * X * sg * (1.0f + G * (1.0f - sg));     // d gate
+            }
+          } else if (EPI == EPI_DSITUGLU) {
+            // dSiTU-GLU: T_g = b1 tanh(G/b1) sigmoid(G), T_u = b2 tanh(U/b2).
+            // tanhf, not the approximate instruction (its 2^-11 error would flip
+            // quantized codes far more often than rounding does), and
+            // 1 - tanh^2(y) as sech^2(y) = 4e / (1 + e)^2 with e = exp(-2|y|),
+            // which keeps its relative precision where tanh^2 rounds to 1
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float ref = al2 * __uint_as_float(r[32 * c + i]);
+              const float U = x[i], G = gv[i];
+              const float yg = G / p.situ_b1, yu = U / p.situ_b2;
+              const float thg = tanhf(yg), thu = tanhf(yu);
+              const float eg = __expf(-2.0f * fabsf(yg)), eu = __expf(-2.0f * fabsf(yu));
+              const float sech2_g = __fdividef(4.0f * eg, (1.0f + eg) * (1.0f + eg));
+              const float sech2_u = __fdividef(4.0f * eu, (1.0f + eu) * (1.0f + eu));
+              const float sg = __fdividef(1.0f, 1.0f + __expf(-G));
+              const float tg = p.situ_b1 * thg * sg, tu = p.situ_b2 * thu;
+              const float dtg = sech2_g * sg + p.situ_b1 * thg * sg * (1.0f - sg);
+              const float dtu = sech2_u;
+              dprob_local += ref * tg * tu;                             // dprob += ref T_g T_u
+              x[i] = ref * pr * tg * dtu;                               // d up
+              gv[i] = ref * pr * tu * dtg;                              // d gate
             }
           } else {
             // dGeGLU: the gate clamped above, the up value both ways; each
@@ -1165,9 +1192,9 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
         // the gate-gradient blocks
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax_local = fmaxf(amax_local, __shfl_xor_sync(0xffffffffu, amax_local, o));
-        const int ai = EPI == EPI_DSWIGLU ? 2 * g : g;
+        const int ai = is_bwd_inst(EPI) ? 2 * g : g;
         if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(p.amax) + ai, __float_as_uint(amax_local));
-        if (EPI == EPI_DSWIGLU) {
+        if (is_bwd_inst(EPI)) {
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1)
             amax_local2 = fmaxf(amax_local2, __shfl_xor_sync(0xffffffffu, amax_local2, o));

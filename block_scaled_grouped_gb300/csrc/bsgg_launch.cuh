@@ -65,7 +65,7 @@ cudaError_t launch_outc(const Launch& L) {
 // with a bias or a stored C: the XC instances
 template <bool FP4, int BN, int CM, int EPI>
 cudaError_t launch_xc(const Launch& L) {
-  if constexpr (EPI == EPI_DSWIGLU) {
+  if constexpr (is_bwd_inst(EPI)) {
     return launch_outc<FP4, BN, CM, EPI, false>(L);   // the backward takes no bias and stores no C
   } else {
     if (L.p.bias != nullptr || L.p.c_out != nullptr || L.p.rht != nullptr)
@@ -81,6 +81,7 @@ cudaError_t launch_shape(const Launch& L) {
     case EPI_SWIGLU: return launch_xc<FP4, BN, CM, EPI_SWIGLU>(L);
     case EPI_SRELU: return launch_xc<FP4, BN, CM, EPI_SRELU>(L);
     case EPI_DSWIGLU: return launch_xc<FP4, BN, CM, EPI_DSWIGLU>(L);
+    case EPI_DSITUGLU: return launch_xc<FP4, BN, CM, EPI_DSITUGLU>(L);
   }
   return cudaErrorInvalidValue;
 }

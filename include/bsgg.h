@@ -39,7 +39,7 @@
  *      padded_offsets int32 (L), alpha float (L), prob float (m_pad),
  *      norm_const float (1)
  *      D, D_col (m_pad, N_out)  N-major; N_out = N/2 for SWIGLU/GEGLU, 2N for
- *                               DSWIGLU/DGEGLU, else N;
+ *                               the backward epilogues, else N;
  *                               bf16/f16/f32, or 1-byte FP8 codes, or packed FP4
  *      C        (m_pad, N)      N-major, bf16/f16 (optional pre-activation output)
  *      bias     (L, N)          N contiguous, bf16/f16/f32 (optional)
@@ -105,12 +105,16 @@ typedef enum {
  *   in C's block order (width 2N);  dprob[m] += sum_n X*swish(G)*ref. */
 typedef enum {
   BSGG_EPI_GATE = 0, BSGG_EPI_SWIGLU = 1, BSGG_EPI_SRELU = 2, BSGG_EPI_GEGLU = 3, BSGG_EPI_DSWIGLU = 4,
-  BSGG_EPI_DGEGLU = 5   /* dGeGLU backward (same page): the saved C unscaled (beta not read),
+  BSGG_EPI_DGEGLU = 5,  /* dGeGLU backward (same page): the saved C unscaled (beta not read),
                            gate G clamped above at clamp_max, up U clamped to [clamp_min,
                            clamp_max]; s = sigmoid(a * Gc);
                            d gate = ref*prob*(Uc + offset)*s*(1 + a*Gc*(1 - s)) if G <= clamp_max,
                            d up = ref*prob*Gc*s if clamp_min <= U <= clamp_max, else 0;
                            dprob[m] += sum_n ref*Gc*s*(Uc + offset) */
+  BSGG_EPI_DSITUGLU = 6 /* dSiTU-GLU backward (same page, Equations): the saved C unscaled;
+                           T_g = b1*tanh(G/b1)*sigmoid(G), T_u = b2*tanh(U/b2);
+                           d gate = ref*prob*T_u*dT_g/dG, d up = ref*prob*T_g*dT_u/dU;
+                           dprob[m] += sum_n ref*T_g*T_u */
 } bsgg_epilogue;
 
 /* Problem description, fixed at plan creation (the pages' constructor +
@@ -180,6 +184,9 @@ typedef struct {
   float dgeglu_clamp_min;
   float dgeglu_clamp_max;
   float dgeglu_linear_offset;
+  /* DSITUGLU: the tanh scales b1 (gate) and b2 (up), finite and > 0; 0 = 1. */
+  float situ_beta1;
+  float situ_beta2;
 } bsgg_desc;
 
 /* Tensors of one call.  Unused outputs may be NULL: d_col/sfd_col unless
@@ -209,7 +216,7 @@ typedef struct {
      BSGG_ERR_BAD_POINTERS from bsgg_query_device_status, and nothing is written). */
   const int64_t* b_ptrs;
   const int64_t* sfb_ptrs;
-  /* DSWIGLU and DGEGLU: the saved forward C (m_pad, 2N) N-major in saved_c_format,
+  /* DSWIGLU, DGEGLU and DSITUGLU: the saved forward C (m_pad, 2N) N-major in saved_c_format,
      its per-group scale beta (L; DSWIGLU only), and dprob (m_pad), which the kernel
      ACCUMULATES into:
      zero it before the call ("Grouped GEMM + dGLU (SM100)": dprob must be

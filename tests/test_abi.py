@@ -114,6 +114,9 @@ def _create(**over):
     (dict(epilogue="dswiglu", dgeglu_params=(1.0, -7.0, 7.0, 1.0)), 1),   # dGeGLU's own
     (dict(epilogue="dgeglu", dgeglu_params=(1.0, 7.0, -7.0, 1.0)), 1),    # min <= max
     (dict(epilogue="dgeglu", dgeglu_params=(float("nan"), -7.0, 7.0, 1.0)), 1),
+    (dict(epilogue="dsituglu", situ_betas=(-1.0, 1.0)), 1),
+    (dict(epilogue="dsituglu", situ_betas=(1.0, float("inf"))), 1),
+    (dict(epilogue="dswiglu", situ_betas=(2.0, 2.0)), 1),          # dSiTU-GLU's own
 ])
 def test_create_rejects(lib, over, code):
     assert _create(**over) == code
@@ -128,6 +131,7 @@ def test_create_rejects(lib, over, code):
     dict(epilogue="dswiglu", n=96, saved_c_format="f32", out_format="e4m3", want_col=1),
     dict(epilogue="swiglu", rht_format="e2m1", in_format="nvfp4", out_format="e2m1"),
     dict(epilogue="dgeglu", dgeglu_params=(1.0, -10.0, 10.0, 0.0)),
+    dict(epilogue="dsituglu", situ_betas=(2.0, 0.5)),
 ])
 def test_create_accepts_epilogue_options(lib, over):
     # validation passes: 0 with a GPU, else the device query that follows

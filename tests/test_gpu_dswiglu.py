@@ -1,5 +1,6 @@
-"""Parity of the dSwiGLU backward ("Grouped GEMM + dGLU (SM100)", Block-scaled
-contract) through the C ABI against the oracle, in every tile shape: the
+"""Parity of the dSwiGLU, dGeGLU and dSiTU-GLU backward ("Grouped GEMM + dGLU
+(SM100)", Block-scaled contract) through the C ABI against the oracle, in every
+tile shape: the
 2N-wide interleaved input/gate gradients (16/32-bit with the two amax halves,
 or FP8/FP4 with row and column scale factors), and dprob, which the kernel
 accumulates into the caller's zeroed buffer.
@@ -19,12 +20,12 @@ from helpers import oracle_run, small_problem
 pytestmark = pytest.mark.gpu
 
 
-def _run(p, tile=(0, 0), gate_first=False, saved_fmt="bf16", dprob=None, dgeglu_params=None):
+def _run(p, tile=(0, 0), gate_first=False, saved_fmt="bf16", dprob=None, dgeglu_params=None, situ_betas=None):
     pd = to_device(p)
     plan = bsgg.Plan(m_pad=p.m_pad, n=p.n, k=p.k, num_groups=p.num_groups, in_format=p.in_fmt,
                      out_format=p.out_fmt, epilogue=p.epi, want_col=p.want_col, gate_first=gate_first,
                      tile=tuple(tile[:2]), cluster=tuple(tile[2:4]) or (0, 0), saved_c_format=saved_fmt,
-                     dgeglu_params=dgeglu_params)
+                     dgeglu_params=dgeglu_params, situ_betas=situ_betas)
     outs = alloc_outputs(plan)
     if dprob is None:
         dprob = torch.zeros(p.m_pad, dtype=torch.float32, device="cuda")
@@ -36,10 +37,12 @@ def _run(p, tile=(0, 0), gate_first=False, saved_fmt="bf16", dprob=None, dgeglu_
     return plan, outs, dprob
 
 
-def _check(p, outs, dprob, gate_first=False, dgeglu_params=None):
+def _check(p, outs, dprob, gate_first=False, dgeglu_params=None, situ_betas=None):
     over = {}
     if dgeglu_params is not None:
         over = dict(zip(("geglu_alpha", "glu_clamp_min", "glu_clamp_max", "linear_offset"), dgeglu_params))
+    if situ_betas is not None:
+        over.update(situ_beta1=situ_betas[0], situ_beta2=situ_betas[1])
     ref = oracle_run(p, gate_first=int(gate_first), **over)
     compare(p, outs, ref)
     if "amax" in outs:
@@ -142,3 +145,15 @@ def test_dgeglu_nvfp4_f16_saved_c():
     p.saved_c = (p.saved_c.float() * 4.0).to(torch.float16)
     plan, outs, dprob = _run(p, saved_fmt="f16")
     _check(p, outs, dprob)
+
+
+@pytest.mark.parametrize("betas", [None, (2.0, 0.5)], ids=["unit", "b2_05"])
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
+def test_dsituglu_e4m3_and_bf16(tile, betas):
+    p = small_problem(counts=(130, 0, 256, 40), k=256, n=128, pad_to=128, epi="dsituglu", out_fmt="e4m3",
+                      want_col=True, seed=93)
+    plan, outs, dprob = _run(p, tile, situ_betas=betas)
+    _check(p, outs, dprob, situ_betas=betas)
+    p = small_problem(counts=(200, 77), k=384, n=96, pad_to=128, epi="dsituglu", out_fmt="bf16", seed=94)
+    plan, outs, dprob = _run(p, tile, situ_betas=betas)
+    _check(p, outs, dprob, situ_betas=betas)
