@@ -87,7 +87,7 @@ def lib():
         L.orc_group_of_row.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64]
         L.orc_run.restype = ctypes.c_int
         L.orc_run.argtypes = [ctypes.POINTER(OrcDesc)] + [ctypes.c_void_p] * 10 + [
-            ctypes.c_float, ctypes.c_void_p, ctypes.c_int64] + [ctypes.c_void_p] * 11 + [ctypes.c_int]
+            ctypes.c_float, ctypes.c_void_p, ctypes.c_int64] + [ctypes.c_void_p] * 12 + [ctypes.c_int]
         L.orc_round_bf16.restype = ctypes.c_double
         L.orc_round_bf16.argtypes = [ctypes.c_double]
         L.orc_hadamard16.restype = ctypes.c_double
@@ -183,7 +183,8 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     ``geglu_alpha``, ``glu_clamp_min``/``glu_clamp_max`` and ``linear_offset``
     (the page's defaults 1.702, -7, 7, 1); the dSiTU-GLU backward
     (``epi=EPI_DSITUGLU``) takes the saved C unscaled and ``situ_beta1``,
-    ``situ_beta2``.
+    ``situ_beta2``.  Every backward also returns ``dbias`` (L, 2n) fp64: the
+    sum of D over the listed rows of each group.
     ``rht`` ("bf16" or "e2m1") adds the rowwise Hadamard output: ``rht_ref``
     (fp64) and, for "e2m1", full-size ``rht_q`` / ``sfrht`` buffers (E4M3
     scales per 16 under ``rht_norm``).
@@ -207,6 +208,7 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     amax = np.zeros(2 * num_groups if bwd else num_groups, dtype=np.float32)
     rht_ref = np.zeros((blocks.size * 32, nd), dtype=np.float64) if rht_code else None
     dprob_ref = np.zeros(blocks.size * 32, dtype=np.float64) if bwd else None
+    dbias = np.zeros((num_groups, nd), dtype=np.float64) if bwd else None
     saved_arr = None if saved_c is None else np.ascontiguousarray(saved_c, dtype=np.float64).reshape(m_pad, 2 * n)
     beta_arr = None if beta is None else np.ascontiguousarray(beta, dtype=np.float32).reshape(num_groups)
     outs = dict(outputs or {})
@@ -234,7 +236,8 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
                    _ptr(bias_arr), _ptr(saved_arr), _ptr(beta_arr), float(norm_const), _ptr(blocks),
                    blocks.size, _ptr(d_ref), _ptr(c_ref), _ptr(dprob_ref), _ptr(outs.get("d")),
                    _ptr(outs.get("d_col")), _ptr(outs.get("sfd_row")), _ptr(outs.get("sfd_col")),
-                   _ptr(amax), _ptr(rht_ref), _ptr(outs.get("rht_q")), _ptr(outs.get("sfrht")), int(threads))
+                   _ptr(amax), _ptr(rht_ref), _ptr(outs.get("rht_q")), _ptr(outs.get("sfrht")), _ptr(dbias),
+                   int(threads))
     if rc != 0:
         raise ValueError(f"oracle rejected the problem (code {rc})")
     res = {"d_ref": d_ref, "amax": amax, "blocks": blocks}
@@ -242,6 +245,7 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
         res["c_ref"] = c_ref
     if dprob_ref is not None:
         res["dprob_ref"] = dprob_ref
+        res["dbias"] = dbias
     if rht_ref is not None:
         res["rht_ref"] = rht_ref
     res.update(outs)

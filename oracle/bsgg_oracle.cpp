@@ -277,7 +277,10 @@ int64_t orc_group_of_row(const int32_t* off, int64_t L, int64_t m) {
 //   saved_c  [m_pad, 2n] fp64 values of the saved forward C (its input and gate
 //            32-column blocks interleaved; the caller decodes its storage type)
 //   beta     [L] scale of C per group
-// and writes dprob_ref [nblocks*32] fp64 (the listed rows' dprob) and, for
+// and writes dprob_ref [nblocks*32] fp64 (the listed rows' dprob), dbias
+// [L, 2n] fp64 when not NULL (the sum of D over the listed rows of each group:
+// "dbias is the per-expert row reduction of interleaved D_row"; reading: of D
+// before any output conversion) and, for
 // 16/32-bit D, amax [2L]: index 2g for the input-gradient blocks, 2g+1 for the
 // gate-gradient blocks (reading of the pages' amax shape (L, 2, 1)).  D is
 // (m_pad, 2n).
@@ -286,7 +289,7 @@ int orc_run(const orc_desc* P, const uint8_t* A, const uint8_t* SFA, const uint8
             const float* prob, const float* bias, const double* saved_c, const float* beta,
             float norm_const, const int64_t* blocks, int64_t nblocks, double* d_ref, double* c_ref,
             double* dprob_ref, uint8_t* d_q, uint8_t* d_col_q, uint8_t* sfd_row, uint8_t* sfd_col,
-            float* amax, double* rht_ref, uint8_t* rht_q, uint8_t* sfrht, int threads);
+            float* amax, double* rht_ref, uint8_t* rht_q, uint8_t* sfrht, double* dbias, int threads);
 
 }  // extern "C"
 
@@ -301,6 +304,7 @@ struct Job {
   double* dprob_ref;
   double* rht_ref;
   uint8_t *rht_q, *sfrht;
+  double* dbias;          // backward: [L, n_d] row sums of D per group, or null
   const uint8_t *A, *SFA, *B, *SFB;
   const int32_t* off;
   const float *alpha, *prob;
@@ -632,6 +636,12 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
 
   std::lock_guard<std::mutex> lk(J.mu);
   for (size_t g = 0; g < amax_local.size(); ++g) J.amax[g] = std::max(J.amax[g], amax_local[g]);
+  if (is_bwd(P) && J.dbias)
+    for (int64_t i = 0; i < 32; ++i) {
+      const int64_t g = grp[size_t(i)];
+      if (g < 0) continue;
+      for (int64_t j = j0; j < j1; ++j) J.dbias[g * nd + j] += D[size_t(i * w + (j - j0))];
+    }
   if (is_bwd(P) && J.dprob_ref)
     for (int64_t i = 0; i < 32; ++i) J.dprob_ref[size_t(bi * 32 + i)] += dprob_local[size_t(i)];
 }
@@ -643,7 +653,8 @@ extern "C" int orc_run(const orc_desc* P, const uint8_t* A, const uint8_t* SFA, 
                        const float* prob, const float* bias, const double* saved_c, const float* beta,
                        float norm_const, const int64_t* blocks, int64_t nblocks, double* d_ref, double* c_ref,
                        double* dprob_ref, uint8_t* d_q, uint8_t* d_col_q, uint8_t* sfd_row, uint8_t* sfd_col,
-                       float* amax, double* rht_ref, uint8_t* rht_q, uint8_t* sfrht, int threads) {
+                       float* amax, double* rht_ref, uint8_t* rht_q, uint8_t* sfrht, double* dbias,
+                       int threads) {
   if (!P || P->m_pad <= 0 || P->m_pad % 32 || P->n <= 0 || P->k <= 0 || P->num_groups <= 0)
     return -1;
   if (is_glu(P) && P->n % 64) return -2;
@@ -657,7 +668,7 @@ extern "C" int orc_run(const orc_desc* P, const uint8_t* A, const uint8_t* SFA, 
   Job J;
   J.P = P; J.bias = bias; J.c_ref = c_ref; J.A = A; J.SFA = SFA; J.B = B; J.SFB = SFB; J.off = padded_offsets;
   J.saved_c = saved_c; J.beta = beta; J.dprob_ref = dprob_ref;
-  J.rht_ref = rht_ref; J.rht_q = rht_q; J.sfrht = sfrht;
+  J.rht_ref = rht_ref; J.rht_q = rht_q; J.sfrht = sfrht; J.dbias = dbias;
   J.alpha = alpha; J.prob = prob; J.norm = norm_const; J.blocks = blocks; J.nblocks = nblocks;
   J.d_ref = d_ref; J.d_q = d_q; J.d_col_q = d_col_q; J.sfd_row = sfd_row; J.sfd_col = sfd_col;
   J.amax.assign(size_t(is_bwd(P) ? 2 * P->num_groups : P->num_groups), 0.0f);

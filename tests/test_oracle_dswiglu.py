@@ -210,3 +210,17 @@ def test_quantized_backward_output_is_the_step3_quantization_of_d():
             assert sfd >= am / 448 * (1 - 1e-7) and sfd / 2 < am / 448
             deq = q[r, 32 * blk:32 * blk + 32] * sfd
             assert np.all(np.abs(deq - d[r, 32 * blk:32 * blk + 32]) <= am * 2.0 ** -3 + 1e-30)
+
+
+@pytest.mark.parametrize("epi", ["dswiglu", "dgeglu", "dsituglu"])
+def test_dbias_is_the_row_sum_of_d_per_group(epi):
+    # every row of every group listed: dbias[g] is numpy's sum of the oracle's
+    # D over the group's padded rows (padding rows contribute 0)
+    p = small_problem(counts=(40, 0, 70, 33), k=64, n=96, epi=epi, out_fmt="f32", pad_to=32, seed=12)
+    out = oracle_run(p)
+    off = np_(p.padded_offsets)
+    start = 0
+    for g in range(p.num_groups):
+        want = out["d_ref"][start:int(off[g])].sum(axis=0) if off[g] > start else np.zeros(2 * p.n)
+        np.testing.assert_allclose(out["dbias"][g], want, rtol=1e-12, atol=1e-12 * np.abs(want).max(initial=1.0))
+        start = int(off[g])
