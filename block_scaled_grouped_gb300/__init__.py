@@ -81,7 +81,7 @@ class Args(ctypes.Structure):
     _fields_ = [(name, ctypes.c_void_p) for name in (
         "a", "sfa", "b", "sfb", "padded_offsets", "alpha", "prob", "norm_const",
         "d", "d_col", "sfd_row", "sfd_col", "amax", "bias", "c", "b_ptrs", "sfb_ptrs", "saved_c", "beta",
-        "dprob", "rht", "sfrht", "rht_norm_const")]
+        "dprob", "rht", "sfrht", "rht_norm_const", "dbias")]
 
 
 _lib = None

@@ -17,9 +17,11 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libbsgg.so")
-UNITS = ["bsgg_host.cu", "bsgg_launch_mxf8_128.cu", "bsgg_launch_mxf8_256.cu", "bsgg_launch_mxf8_pair.cu",
-         "bsgg_launch_mxf8_mc.cu", "bsgg_launch_nvf4_128.cu", "bsgg_launch_nvf4_256.cu",
-         "bsgg_launch_nvf4_pair.cu", "bsgg_launch_nvf4_mc.cu", "bsgg_peak.cu"]
+_SHAPES = ["mxf8_128", "mxf8_256", "mxf8_pair", "mxf8_mc", "nvf4_128", "nvf4_256", "nvf4_pair", "nvf4_mc"]
+# forward and backward instances of each input family and tile shape in units
+# of their own, so that they compile in parallel
+UNITS = (["bsgg_host.cu", "bsgg_peak.cu"] + [f"bsgg_launch_{s}.cu" for s in _SHAPES] +
+         [f"bsgg_launch_{s}_bwd.cu" for s in _SHAPES])
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE]

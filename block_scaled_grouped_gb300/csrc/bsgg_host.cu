@@ -311,6 +311,7 @@ bsgg_status check_args(const bsgg_plan* P, const bsgg_args* a) {
       (!a->saved_c || !aligned16(a->saved_c) || !a->dprob))
     return BSGG_ERR_INVALID_ARG;
   if (d.want_rht && (!a->rht || !aligned16(a->rht))) return BSGG_ERR_INVALID_ARG;
+  if (a->dbias && !is_bwd_epi(d.epilogue)) return BSGG_ERR_INVALID_ARG;   // a backward output
   if (d.want_rht && d.rht_format == BSGG_OUT_E2M1 && (!a->sfrht || !a->rht_norm_const))
     return BSGG_ERR_INVALID_ARG;
   if (d.want_c && (!a->c || !aligned16(a->c))) return BSGG_ERR_INVALID_ARG;
@@ -516,6 +517,7 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
     p.beta = a->beta;
     p.dprob = a->dprob;
     p.bwd_kind = d.epilogue == BSGG_EPI_DGEGLU ? 1 : 0;
+    p.dbias = a->dbias;
     p.situ_b1 = d.situ_beta1 == 0.0f ? 1.0f : d.situ_beta1;
     p.situ_b2 = d.situ_beta2 == 0.0f ? 1.0f : d.situ_beta2;
     const bool cust = d.dgeglu_custom != 0;
@@ -550,7 +552,16 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
     if (cudaGetLastError() != cudaSuccess) return BSGG_ERR_CUDA;
   }
   cudaError_t e;
-  if (d.in_format == BSGG_IN_NVFP4)
+  if (is_bwd_epi(d.epilogue)) {
+    if (d.in_format == BSGG_IN_NVFP4)
+      e = P->pair ? bsgg::launch_nvf4_pair_bwd(L)
+          : P->mc ? bsgg::launch_nvf4_mc_bwd(L)
+          : P->bn == 256 ? bsgg::launch_nvf4_256_bwd(L) : bsgg::launch_nvf4_128_bwd(L);
+    else
+      e = P->pair ? bsgg::launch_mxf8_pair_bwd(L)
+          : P->mc ? bsgg::launch_mxf8_mc_bwd(L)
+          : P->bn == 256 ? bsgg::launch_mxf8_256_bwd(L) : bsgg::launch_mxf8_128_bwd(L);
+  } else if (d.in_format == BSGG_IN_NVFP4)
     e = P->pair ? bsgg::launch_nvf4_pair(L)
         : P->mc ? bsgg::launch_nvf4_mc(L)
         : P->bn == 256 ? bsgg::launch_nvf4_256(L) : bsgg::launch_nvf4_128(L);
@@ -628,7 +639,8 @@ bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* 
             h2d(bwd ? host->saved_c : nullptr, dev->saved_c, sz_saved_c) &&
             h2d(d.epilogue == BSGG_EPI_DSWIGLU ? host->beta : nullptr, dev->beta, sizeof(float) * L) &&
             h2d(bwd ? host->dprob : nullptr, dev->dprob, sizeof(float) * d.m_pad) &&
-            h2d(d.want_rht ? host->rht_norm_const : nullptr, dev->rht_norm_const, sizeof(float));
+            h2d(d.want_rht ? host->rht_norm_const : nullptr, dev->rht_norm_const, sizeof(float)) &&
+            h2d(bwd ? host->dbias : nullptr, dev->dbias, sizeof(float) * L * P->n_out);
   if (!ok) return BSGG_ERR_CUDA;
   bsgg_status st = bsgg_run(P, dev, stream);
   if (st != BSGG_OK) return st;
@@ -637,6 +649,7 @@ bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* 
        d2h(host->sfd_col, dev->sfd_col, d.want_col ? sz_sfd_col : 0) &&
        d2h(host->amax, dev->amax, sizeof(float) * n_amax) &&
        d2h(bwd ? host->dprob : nullptr, dev->dprob, sizeof(float) * d.m_pad) &&
+       d2h(bwd ? host->dbias : nullptr, dev->dbias, sizeof(float) * L * P->n_out) &&
        d2h(d.want_rht ? host->rht : nullptr, dev->rht,
            uint64_t(d.m_pad) * (d.rht_format == BSGG_OUT_E2M1 ? P->n_out / 2 : P->n_out * 2)) &&
        d2h(d.want_rht && d.rht_format == BSGG_OUT_E2M1 ? host->sfrht : nullptr, dev->sfrht,

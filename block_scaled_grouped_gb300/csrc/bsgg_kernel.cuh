@@ -138,6 +138,7 @@ struct Params {
   const float* beta;        // dSwiGLU only
   float* dprob;
   int32_t bwd_kind;         // EPI_DSWIGLU instances: 0 = dSwiGLU, 1 = dGeGLU
+  float* dbias;             // backward: (L, n_out) accumulated row sums of D per group, or null
   float geglu_a, clamp_min, clamp_max, lin_offset;   // dGeGLU
   float situ_b1, situ_b2;                            // dSiTU-GLU
   // rowwise Hadamard output of bf16-rounded D ("Grouped GEMM + GLU + Hadamard +
@@ -528,6 +529,24 @@ __device__ __forceinline__ void output_chunk(const Params& p, const float (&v)[3
   }
 }
 
+// Adds the column sums of a warp's 32 x 32 chunk (lane = row, v[i] = column i)
+// to dst[0..31]: five exchange-and-add rounds halve the columns each lane
+// keeps (31 shuffles), after which lane l holds column l's sum; one coalesced
+// atomic add per lane.  v is consumed.
+__device__ __forceinline__ void add_column_sums32(float (&v)[32], float* dst, int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = upper ? v[i] : v[i + o];
+      const float keep = upper ? v[i + o] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  atomicAdd(dst + lane, v[0]);
+}
+
 // Rowwise Hadamard output of one 32-column chunk of D of one row: each 16-value
 // block of bf16-rounded D times H16 / 4 (H16 the Sylvester Hadamard matrix,
 // entry (i, j) = (-1)^popcount(i & j): four in-register butterfly stages),
@@ -612,9 +631,9 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* 
   if (XC && p.rht != nullptr) rht_chunk(p, v, row, col0, *p.rht_norm_const);
 }
 
-// XC: the launch adds a bias to C, stores C or writes the Hadamard output (a
-// separate instance, so that the register budget of the plain epilogue is
-// untouched).
+// XC: a forward launch adds a bias to C, stores C or writes the Hadamard
+// output; a backward launch accumulates dbias (separate instances, so that the
+// register budget of the plain epilogue is untouched).
 template <bool FP4, int BN, int CM, int EPI, int OUTC, bool XC>
 __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
     bsgg_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -1162,6 +1181,11 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
           }
           output_chunk<FP4, OUTC>(p, x, row, xo, norm, lane, kblk_col, amax_local);
           output_chunk<FP4, OUTC>(p, gv, row, go, norm, lane, kblk_col, amax_local2);
+          if (XC && p.dbias != nullptr) {
+            float* db = p.dbias + static_cast<int64_t>(g) * p.n_out;
+            add_column_sums32(x, db + xo, lane);
+            add_column_sums32(gv, db + go, lane);
+          }
         }
         atomicAdd(p.dprob + row, dprob_local);
       } else if (EPI == EPI_SWIGLU) {

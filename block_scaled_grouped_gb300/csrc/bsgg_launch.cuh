@@ -62,24 +62,29 @@ cudaError_t launch_outc(const Launch& L) {
   return cudaErrorInvalidValue;
 }
 
-// with a bias or a stored C: the XC instances
+// The XC instances: forward launches with a bias, a stored C or the Hadamard
+// output; backward launches with dbias.
 template <bool FP4, int BN, int CM, int EPI>
 cudaError_t launch_xc(const Launch& L) {
-  if constexpr (is_bwd_inst(EPI)) {
-    return launch_outc<FP4, BN, CM, EPI, false>(L);   // the backward takes no bias and stores no C
-  } else {
-    if (L.p.bias != nullptr || L.p.c_out != nullptr || L.p.rht != nullptr)
-      return launch_outc<FP4, BN, CM, EPI, true>(L);
-    return launch_outc<FP4, BN, CM, EPI, false>(L);
-  }
+  const bool xc = is_bwd_inst(EPI) ? L.p.dbias != nullptr
+                                   : (L.p.bias != nullptr || L.p.c_out != nullptr || L.p.rht != nullptr);
+  return xc ? launch_outc<FP4, BN, CM, EPI, true>(L) : launch_outc<FP4, BN, CM, EPI, false>(L);
 }
 
+// Forward epilogues (one translation unit per input family and tile shape) and
+// backward epilogues (another), so that the instances compile in parallel.
 template <bool FP4, int BN, int CM>
-cudaError_t launch_shape(const Launch& L) {
+cudaError_t launch_shape_fwd(const Launch& L) {
   switch (L.epi) {
     case EPI_GATE: return launch_xc<FP4, BN, CM, EPI_GATE>(L);
     case EPI_SWIGLU: return launch_xc<FP4, BN, CM, EPI_SWIGLU>(L);
     case EPI_SRELU: return launch_xc<FP4, BN, CM, EPI_SRELU>(L);
+  }
+  return cudaErrorInvalidValue;
+}
+template <bool FP4, int BN, int CM>
+cudaError_t launch_shape_bwd(const Launch& L) {
+  switch (L.epi) {
     case EPI_DSWIGLU: return launch_xc<FP4, BN, CM, EPI_DSWIGLU>(L);
     case EPI_DSITUGLU: return launch_xc<FP4, BN, CM, EPI_DSITUGLU>(L);
   }

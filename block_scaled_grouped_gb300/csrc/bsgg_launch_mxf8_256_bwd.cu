@@ -1,0 +1,6 @@
+// Kernel instances of the backward epilogues: MXFP8 inputs (E4M3 / E5M2 data, UE8M0 scales per 32), 1-CTA 128 x 256 tiles.
+#include "bsgg_launch.cuh"
+
+namespace bsgg {
+cudaError_t launch_mxf8_256_bwd(const Launch& L) { return launch_shape_bwd<false, 256, CM_SINGLE>(L); }
+}  // namespace bsgg

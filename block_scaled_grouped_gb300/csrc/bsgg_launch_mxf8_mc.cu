@@ -1,7 +1,7 @@
-// Kernel instances: MXFP8 inputs (E4M3 / E5M2 data, UE8M0 scales per 32), 128 x 256 tiles in
+// Kernel instances of the forward epilogues: MXFP8 inputs (E4M3 / E5M2 data, UE8M0 scales per 32), 128 x 256 tiles in
 // clusters of two CTAs sharing an operand tile through TMA multicast.
 #include "bsgg_launch.cuh"
 
 namespace bsgg {
-cudaError_t launch_mxf8_mc(const Launch& L) { return launch_shape<false, 256, CM_MC>(L); }
+cudaError_t launch_mxf8_mc(const Launch& L) { return launch_shape_fwd<false, 256, CM_MC>(L); }
 }  // namespace bsgg

@@ -1,0 +1,7 @@
+// Kernel instances of the backward epilogues: MXFP8 inputs (E4M3 / E5M2 data, UE8M0 scales per 32), 128 x 256 tiles in
+// clusters of two CTAs sharing an operand tile through TMA multicast.
+#include "bsgg_launch.cuh"
+
+namespace bsgg {
+cudaError_t launch_mxf8_mc_bwd(const Launch& L) { return launch_shape_bwd<false, 256, CM_MC>(L); }
+}  // namespace bsgg

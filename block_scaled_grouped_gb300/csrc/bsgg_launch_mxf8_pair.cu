@@ -1,6 +1,6 @@
-// Kernel instances: MXFP8 inputs (E4M3 / E5M2 data, UE8M0 scales per 32), 256 x 256 tiles on CTA pairs.
+// Kernel instances of the forward epilogues: MXFP8 inputs (E4M3 / E5M2 data, UE8M0 scales per 32), 256 x 256 tiles on CTA pairs.
 #include "bsgg_launch.cuh"
 
 namespace bsgg {
-cudaError_t launch_mxf8_pair(const Launch& L) { return launch_shape<false, 256, CM_PAIR>(L); }
+cudaError_t launch_mxf8_pair(const Launch& L) { return launch_shape_fwd<false, 256, CM_PAIR>(L); }
 }  // namespace bsgg

@@ -1,6 +1,6 @@
-// Kernel instances: NVFP4 inputs (E2M1 data, E4M3 scales per 16), 1-CTA 128 x 128 tiles.
+// Kernel instances of the forward epilogues: NVFP4 inputs (E2M1 data, E4M3 scales per 16), 1-CTA 128 x 128 tiles.
 #include "bsgg_launch.cuh"
 
 namespace bsgg {
-cudaError_t launch_nvf4_128(const Launch& L) { return launch_shape<true, 128, CM_SINGLE>(L); }
+cudaError_t launch_nvf4_128(const Launch& L) { return launch_shape_fwd<true, 128, CM_SINGLE>(L); }
 }  // namespace bsgg

@@ -1,0 +1,6 @@
+// Kernel instances of the backward epilogues: NVFP4 inputs (E2M1 data, E4M3 scales per 16), 1-CTA 128 x 256 tiles.
+#include "bsgg_launch.cuh"
+
+namespace bsgg {
+cudaError_t launch_nvf4_256_bwd(const Launch& L) { return launch_shape_bwd<true, 256, CM_SINGLE>(L); }
+}  // namespace bsgg

@@ -1,0 +1,7 @@
+// Kernel instances of the backward epilogues: NVFP4 inputs (E2M1 data, E4M3 scales per 16), 128 x 256 tiles in
+// clusters of two CTAs sharing an operand tile through TMA multicast.
+#include "bsgg_launch.cuh"
+
+namespace bsgg {
+cudaError_t launch_nvf4_mc_bwd(const Launch& L) { return launch_shape_bwd<true, 256, CM_MC>(L); }
+}  // namespace bsgg

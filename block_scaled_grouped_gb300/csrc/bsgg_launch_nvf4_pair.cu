@@ -1,8 +1,8 @@
-// Kernel instances: NVFP4 inputs (E2M1 data, E4M3 scales per 16), 256 x 256 tiles on CTA pairs.
+// Kernel instances of the forward epilogues: NVFP4 inputs (E2M1 data, E4M3 scales per 16), 256 x 256 tiles on CTA pairs.
 #include "bsgg_launch.cuh"
 
 namespace bsgg {
-cudaError_t launch_nvf4_pair(const Launch& L) { return launch_shape<true, 256, CM_PAIR>(L); }
+cudaError_t launch_nvf4_pair(const Launch& L) { return launch_shape_fwd<true, 256, CM_PAIR>(L); }
 int cluster_resident_ctas(bool fp4, bool mc) {
   if (mc) return fp4 ? cluster_resident_ctas_impl<true, CM_MC>() : cluster_resident_ctas_impl<false, CM_MC>();
   return fp4 ? cluster_resident_ctas_impl<true, CM_PAIR>() : cluster_resident_ctas_impl<false, CM_PAIR>();

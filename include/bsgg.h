@@ -230,6 +230,11 @@ typedef struct {
   void* rht;
   void* sfrht;
   const float* rht_norm_const;
+  /* Backward epilogues, optional: dbias (L, 2N) float, ACCUMULATED like dprob
+     (zero it before the call): dbias[g][n] += sum over the rows of group g of
+     D[m][n] before any output conversion ("Grouped GEMM + dGLU (SM100)": the
+     per-expert row reduction of the interleaved D).  NULL = not computed. */
+  float* dbias;
 } bsgg_args;
 
 typedef struct bsgg_plan bsgg_plan;

@@ -144,3 +144,24 @@ def test_null_arguments(lib):
     assert lib.bsgg_run(None, None, None) == 1
     assert lib.bsgg_query_device_status(None, None) == 1
     lib.bsgg_destroy(None)
+
+
+def _struct_fields(name):
+    src = open(HEADER).read()
+    end = src.index("} " + name + ";")
+    start = src.rindex("typedef struct {", 0, end)
+    body = re.sub(r"/\*.*?\*/", "", src[start + len("typedef struct {"):end], flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?([A-Za-z0-9_]+)\s*(\*?)\s*([A-Za-z0-9_]+);", body, flags=re.M)
+
+
+def test_binding_structs_match_the_header():
+    """Field names, order and types of bsgg_desc and bsgg_args in the header
+    equal the Python binding's ctypes structures (the ABI is positional)."""
+    ctype = {"int64_t": ctypes.c_int64, "int32_t": ctypes.c_int32, "float": ctypes.c_float}
+    desc = _struct_fields("bsgg_desc")
+    assert [n for _, _, n in desc] == [n for n, _ in bsgg.Desc._fields_]
+    for (t, star, n), (pn, pt) in zip(desc, bsgg.Desc._fields_):
+        assert star == "" and ctype[t] is pt, n
+    args = _struct_fields("bsgg_args")
+    assert [n for _, _, n in args] == [n for n, _ in bsgg.Args._fields_]
+    assert all(star == "*" for _, star, _ in args)

@@ -157,3 +157,40 @@ def test_dsituglu_e4m3_and_bf16(tile, betas):
     p = small_problem(counts=(200, 77), k=384, n=96, pad_to=128, epi="dsituglu", out_fmt="bf16", seed=94)
     plan, outs, dprob = _run(p, tile, situ_betas=betas)
     _check(p, outs, dprob, situ_betas=betas)
+
+
+@pytest.mark.parametrize("epi", ["dswiglu", "dgeglu", "dsituglu"])
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
+def test_dbias_row_sums_per_group(tile, epi):
+    """dbias (L, 2N) accumulates the rows of D of each group (caller-zeroed),
+    within 2^-7 |ref| + 1e-3 rms(ref) of the oracle's fp64 sums; D and dprob
+    are unchanged by asking for it."""
+    p = small_problem(counts=(130, 0, 256, 40), k=256, n=128, pad_to=128, epi=epi, out_fmt="e4m3",
+                      want_col=True, seed=95)
+    pd = to_device(p)
+    plan = bsgg.Plan(m_pad=p.m_pad, n=p.n, k=p.k, num_groups=p.num_groups, in_format=p.in_fmt,
+                     out_format=p.out_fmt, epilogue=epi, want_col=True, tile=tuple(tile[:2]),
+                     cluster=tuple(tile[2:4]) or (0, 0))
+    outs = alloc_outputs(plan)
+    dprob = torch.zeros(p.m_pad, dtype=torch.float32, device="cuda")
+    dbias = torch.zeros(p.num_groups, 2 * p.n, dtype=torch.float32, device="cuda")
+    norm = torch.tensor([p.norm_const], dtype=torch.float32, device="cuda")
+    plan.run(a=pd.a, sfa=bsgg.pack_sf(pd.sfa_rows), b=pd.b, sfb=bsgg.pack_sf(pd.sfb_rows),
+             padded_offsets=pd.padded_offsets, alpha=pd.alpha, prob=pd.prob, norm_const=norm,
+             saved_c=pd.saved_c, beta=pd.beta if epi == "dswiglu" else None, dprob=dprob, dbias=dbias, **outs)
+    assert plan.device_status() == 0
+    ref = _check(p, outs, dprob)
+    check_float_d(dbias.cpu().double().numpy(), ref["dbias"], what="dbias")
+    assert torch.all(dbias[1] == 0)                  # the empty group
+
+
+def test_dbias_only_with_a_backward_epilogue():
+    p = to_device(small_problem(counts=(128,), k=128, n=128, pad_to=128, seed=96))
+    plan = bsgg.Plan(m_pad=p.m_pad, n=p.n, k=p.k, num_groups=1, in_format=p.in_fmt, out_format="bf16",
+                     epilogue="gate")
+    outs = alloc_outputs(plan)
+    with pytest.raises(bsgg.BsggError) as e:
+        plan.run(a=p.a, sfa=bsgg.pack_sf(p.sfa_rows), b=p.b, sfb=bsgg.pack_sf(p.sfb_rows),
+                 padded_offsets=p.padded_offsets, alpha=p.alpha, prob=p.prob,
+                 dbias=torch.zeros(1, 128, device="cuda"), **outs)
+    assert e.value.code == 1
