@@ -240,10 +240,10 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
   P->desc = *desc;
   P->device = device;
   P->num_sms = num_sms;
-  // library choice (measured on GB300): 256 x 256 tiles on CTA pairs for
-  // MXFP8 (half the shared-memory operand traffic per MMA of 1-CTA tiles),
-  // 128 x 256 single-CTA tiles for NVFP4 (a pair copies each CTA's scale
-  // atoms with every stage and gains nothing there)
+  // library choice (measured on GB300): 256 x 256 tiles on CTA pairs (half
+  // the shared-memory operand traffic per MMA of 1-CTA tiles): MXFP8 FC1
+  // 2741-2779 vs 2608-2655 TFLOP/s for 128 x 256, NVFP4 fine-grained
+  // 4937-4985 vs 4859-4907 (three alternating bench runs each)
   // The dSwiGLU backward writes four outputs per accumulator value and reads
   // two saved values: with 128-column tiles its epilogue holds half the
   // accumulator columns per thread and runs without register spills (measured
@@ -251,7 +251,7 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
   // pairs, whose epilogue spills to local memory).
   const bool bwd = is_bwd_epi(desc->epilogue);
   int tm = desc->tile_m, tn = desc->tile_n, cm = desc->cluster_m;
-  if (tm == 0) tm = (desc->in_format != BSGG_IN_NVFP4 && tn != 128 && cm != 1 && !bwd) ? 256 : 128;
+  if (tm == 0) tm = (tn != 128 && cm != 1 && !bwd) ? 256 : 128;
   if (tn == 0) tn = (bwd && tm == 128 && cm != 2) ? 128 : 256;
   if (cm == 0) cm = (tm == 256) ? 2 : 1;
   P->pair = (tm == 256);
