@@ -187,10 +187,11 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     sum of D over the listed rows of each group.
     ``rht`` ("bf16" or "e2m1") adds the rowwise Hadamard output: ``rht_ref``
     (fp64) and, for "e2m1", full-size ``rht_q`` / ``sfrht`` buffers (E4M3
-    scales per 16 under ``rht_norm``).
+    scales per 16 under ``rht_norm``); "col_e2m1" the colwise one (16-token
+    blocks per column, flat per-expert transposed ``rht_q`` and ``sfrht``).
     """
     L = lib()
-    rht_code = {None: 0, "bf16": 1, "e2m1": 2}[rht]
+    rht_code = {None: 0, "bf16": 1, "e2m1": 2, "col_e2m1": 3}[rht]
     desc = OrcDesc(m_pad, n, k, num_groups, in_fmt, out_fmt, epi, int(gate_first),
                    int(bool(want_col)), rht_code, float(tanh_clamp_s), float(glu_limit), float(glu_alpha),
                    float(rht_norm), float(geglu_alpha), float(glu_clamp_min), float(glu_clamp_max),
@@ -215,6 +216,9 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     if rht_code == 2:
         outs.setdefault("rht_q", np.zeros((m_pad, nd // 2), dtype=np.uint8))
         outs.setdefault("sfrht", np.zeros(sf_bytes(m_pad, -(-nd // 16), 1), dtype=np.uint8))
+    if rht_code == 3:   # flat per-expert segments: m_pad * nd / 2 data bytes, m_pad * nd / 16 scales
+        outs.setdefault("rht_q", np.zeros(m_pad * nd // 2, dtype=np.uint8))
+        outs.setdefault("sfrht", np.zeros(m_pad * nd // 16, dtype=np.uint8))
     quant = out_fmt >= OUT_E4M3
     v = 16 if in_fmt == IN_NVFP4 else 32
     if quant:

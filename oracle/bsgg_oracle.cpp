@@ -174,8 +174,9 @@ extern "C" {
 
 typedef struct {
   int64_t m_pad, n, k, num_groups;
-  // rht: the rowwise Hadamard output of "Grouped GEMM + GLU + Hadamard + Quant
-  // (SM100)" (0 = none, 1 = bf16, 2 = NVFP4 with E4M3 scales per 16)
+  // rht: the Hadamard output of "Grouped GEMM + GLU + Hadamard + Quant (SM100)"
+  // (0 = none, 1 = rowwise bf16, 2 = rowwise NVFP4 with E4M3 scales per 16,
+  // 3 = colwise NVFP4: 16-token blocks per column, per-expert transposed)
   int32_t in_fmt, out_fmt, epi, gate_first, want_col, rht;
   double tanh_clamp_s;   // 0 = no clamp
   // "Grouped GEMM + GLU + Hadamard + Quant (SM100)", Equations: both GLU
@@ -557,8 +558,48 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
     }
   }
 
+  // Colwise RHT ("Grouped GEMM + GLU + Hadamard + Quant (SM100)", Outputs and
+  // Equations): for every column n and every block of 16 consecutive tokens of
+  // an expert (rows of its padded range, counted from the group's start), the
+  // transform of bf16-rounded D along the tokens, quantized to NVFP4 with one
+  // E4M3 scale per block under rht_norm.  Expert g's data is the logical
+  // (n_d, expert_m) matrix, tokens contiguous, at flat element n_d * start_g;
+  // its scales the swizzled SF(n_d, expert_m) at byte n_d * start_g / 16.
+  if (P->rht == 3) {
+    for (int64_t ib = 0; ib < 32; ib += 16) {
+      const int64_t g = grp[size_t(ib)];
+      if (g < 0) continue;
+      const int64_t start = g ? J.off[g - 1] : 0, em = J.off[g] - start;
+      const int64_t t0 = m0 + ib - start;            // first token of the block within the expert
+      for (int64_t j = j0; j < j1; ++j) {
+        double x[16], y[16];
+        for (int t = 0; t < 16; ++t) x[t] = orc_round_bf16(D[size_t((ib + t) * w + (j - j0))]);
+        for (int r = 0; r < 16; ++r) {
+          double acc = 0.0;
+          for (int t = 0; t < 16; ++t) acc += orc_hadamard16(r, t) * x[t];
+          y[r] = acc / 4.0;
+        }
+        for (int t = 0; t < 16; ++t) J.rht_ref[size_t((bi * 32 + ib + t) * nd + j)] = y[t];
+        float am = 0.0f;
+        for (int t = 0; t < 16; ++t) am = std::max(am, std::fabs(float(y[t])));
+        const float norm = float(P->rht_norm);
+        const float sf = (norm * am) * float(1.0 / 6.0);
+        const uint32_t code = encode_rne_satfinite(F_E4M3, sf);
+        const float sfd = float(decode(F_E4M3, code));
+        const float scale = (am == 0.0f || sfd == 0.0f) ? 0.0f : norm / sfd;
+        J.sfrht[nd * start / 16 + sf_offset(j, t0 / 16, 0, nd, (em + 15) / 16)] = uint8_t(code);
+        for (int t = 0; t < 16; ++t) {
+          const uint32_t c = encode_rne_satfinite(F_E2M1, float(y[t]) * scale);
+          const int64_t e = nd * start + j * em + t0 + t;            // flat element index
+          uint8_t& byte = J.rht_q[e / 2];
+          if (e % 2 == 0) byte = uint8_t((byte & 0xF0) | (c & 0xF));
+          else byte = uint8_t((byte & 0x0F) | ((c & 0xF) << 4));
+        }
+      }
+    }
+  }
   // Rowwise RHT of the bf16-rounded D, block by block of 16 columns.
-  if (P->rht) {
+  if (P->rht == 1 || P->rht == 2) {
     const int64_t kb16 = (nd + 15) / 16;
     for (int64_t i = 0; i < 32; ++i) {
       if (grp[size_t(i)] < 0) continue;
@@ -659,7 +700,15 @@ extern "C" int orc_run(const orc_desc* P, const uint8_t* A, const uint8_t* SFA, 
     return -1;
   if (is_glu(P) && P->n % 64) return -2;
   if (is_bwd(P) && (P->n % 32 || !saved_c || (P->epi == EPI_DSWIGLU && !beta) || bias)) return -4;
-  if (P->rht && (is_bwd(P) || !rht_ref || (P->rht == 2 && (!rht_q || !sfrht)))) return -5;
+  if (P->rht && (is_bwd(P) || !rht_ref || (P->rht >= 2 && (!rht_q || !sfrht)))) return -5;
+  // colwise: a segment's swizzled scales SF(n_d, expert_m) occupy exactly
+  // n_d * expert_m / 16 bytes (the page's flat segment length) only when n_d is
+  // a multiple of 128 and expert_m of 64
+  if (P->rht == 3) {
+    if (n_out(P) % 128) return -6;
+    for (int64_t g = 0; g < P->num_groups; ++g)
+      if ((padded_offsets[g] - (g ? padded_offsets[g - 1] : 0)) % 64) return -6;
+  }
   if (is_fp4_in(P) && P->k % 2) return -3;
   const int64_t nd = n_out(P);
   // One work item per (block, 128-column slice of D); slices are multiples of

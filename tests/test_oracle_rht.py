@@ -18,7 +18,7 @@ import scipy.linalg
 import torch
 
 import oracle as orc
-from helpers import E2M1_VALUES, oracle_run, small_problem
+from helpers import E2M1_VALUES, np_, oracle_run, small_problem
 
 
 def test_round_bf16_matches_torch():
@@ -91,3 +91,45 @@ def test_nvfp4_rht_quantization(norm):
             # within half the largest E2M1 gap (2, between 4 and 6) at the block's
             # scale, plus the saturation an E4M3 scale rounded down can cause
             assert np.all(np.abs(deq - blk) <= sfd / norm + 0.07 * am)
+
+
+def test_colwise_rht_per_expert_transposed():
+    """Colwise RHT: for every column and every 16-token block of an expert, the
+    transform along the tokens (scipy's hadamard(16) / 4 of bf16(D)), quantized
+    to NVFP4 with one E4M3 scale per block, stored per expert as the (n_d,
+    expert_m) matrix with tokens contiguous at flat element n_d * start_g, and
+    the scales as swizzled SF(n_d, expert_m) at byte n_d * start_g / 16."""
+    p = small_problem(counts=(64, 0, 100, 64), k=128, n=256, epi="srelu", out_fmt="bf16", pad_to=64, seed=11)
+    norm = 0.5
+    out = oracle_run(p, rht="col_e2m1", rht_norm=norm)
+    d = out["d_ref"]
+    nd = d.shape[1]
+    off = np_(p.padded_offsets)
+    H = scipy.linalg.hadamard(16) / 4.0
+    xb = np.vectorize(orc.round_bf16)(d)
+    nib = np.stack([out["rht_q"] & 0xF, out["rht_q"] >> 4], -1).reshape(-1)
+    start = 0
+    for g in range(p.num_groups):
+        em = int(off[g]) - start
+        for t0 in range(0, em, 16):
+            blk = xb[start + t0:start + t0 + 16]              # (16 tokens, nd)
+            y = H @ blk                                        # per column, along the tokens
+            np.testing.assert_allclose(out["rht_ref"][start + t0:start + t0 + 16], y, rtol=1e-14, atol=1e-300)
+            for n in (0, 1, nd // 2, nd - 1):
+                code = int(out["sfrht"][nd * start // 16 + orc.sf_offset(n, t0 // 16, 0, nd, em // 16)])
+                am = float(np.abs(y[:, n]).astype(np.float32).max())
+                sf = np.float32(np.float32(norm) * np.float32(am)) * np.float32(1.0 / 6.0)
+                assert code == int(torch.tensor([float(sf)]).to(torch.float8_e4m3fn).view(torch.uint8)[0])
+                if am == 0:
+                    continue
+                sfd = float(torch.tensor([code], dtype=torch.uint8).view(torch.float8_e4m3fn).double()[0])
+                e0 = nd * start + n * em + t0                  # flat element of (n, t0)
+                deq = E2M1_VALUES[nib[e0:e0 + 16]] * sfd / norm
+                assert np.all(np.abs(deq - y[:, n]) <= sfd / norm + 0.07 * am)
+        start = int(off[g])
+
+
+def test_colwise_rht_needs_64_row_groups_and_128_columns():
+    p = small_problem(counts=(32, 64), k=64, n=256, epi="srelu", out_fmt="bf16", pad_to=32, seed=12)
+    with pytest.raises(ValueError):
+        oracle_run(p, rht="col_e2m1")
