@@ -57,12 +57,14 @@ def make_desc(*, m_pad: int, n: int, k: int, num_groups: int, in_format: str, ou
               glu_alpha: float = 0.0, c_format: Optional[str] = None,
               bias_format: Optional[str] = None, discrete_b: bool = False,
               saved_c_format: str = "bf16", rht_format: Optional[str] = None,
-              dgeglu_params: Optional[tuple] = None, situ_betas: Optional[tuple] = None) -> "Desc":
+              dgeglu_params: Optional[tuple] = None, situ_betas: Optional[tuple] = None,
+              rht_colwise: bool = False) -> "Desc":
     """A bsgg_desc.  c_format ("bf16"/"f16") asks for the pre-activation C
     output, bias_format ("bf16"/"f16"/"f32") for a bias; None = neither.
     discrete_b: per-expert weights through the b_ptrs / sfb_ptrs arrays.
     saved_c_format: storage type of the saved C read by the dSwiGLU backward.
-    rht_format ("bf16"/"e2m1"): the rowwise Hadamard output; None = none.
+    rht_format ("bf16"/"e2m1"): the rowwise Hadamard output; None = none;
+    with rht_colwise the colwise one (e2m1, per-expert transposed).
     dgeglu_params: (geglu_alpha, clamp_min, clamp_max, linear_offset) of the
     dGeGLU backward; None = the page's defaults (1.702, -7, 7, 1).
     situ_betas: (beta1, beta2) of the dSiTU-GLU backward; None = (1, 1)."""
@@ -72,7 +74,8 @@ def make_desc(*, m_pad: int, n: int, k: int, num_groups: int, in_format: str, ou
                 int(tile[0]), int(tile[1]), int(cluster[0]), int(cluster[1]), float(glu_limit),
                 float(glu_alpha), int(c_format is not None), OUT_FORMATS[c_format or "bf16"],
                 int(bias_format is not None), OUT_FORMATS[bias_format or "bf16"], int(bool(discrete_b)),
-                OUT_FORMATS[saved_c_format], int(rht_format is not None), OUT_FORMATS[rht_format or "bf16"],
+                OUT_FORMATS[saved_c_format], (2 if rht_colwise else 1) if rht_format is not None else 0,
+                OUT_FORMATS[rht_format or "bf16"],
                 int(dgeglu_params is not None), *dg,
                 *(tuple(float(x) for x in situ_betas) if situ_betas is not None else (0.0, 0.0)))
 
@@ -189,6 +192,7 @@ class Plan:
         self.want_col = bool(kw.get("want_col", False))
         self.c_format = kw.get("c_format")
         self.rht_format = kw.get("rht_format")
+        self.rht_colwise = bool(kw.get("rht_colwise", False))
         h = ctypes.c_void_p()
         _check(lib().bsgg_create(ctypes.byref(self.desc), ctypes.byref(h)), "bsgg_create")
         self._h = h
@@ -229,7 +233,8 @@ class Plan:
             out["rht"] = d.m_pad * self.n_out * 2
         elif self.rht_format == "e2m1":
             out["rht"] = d.m_pad * self.n_out // 2
-            out["sfrht"] = sf_bytes(d.m_pad, self.n_out, 16, 1)
+            out["sfrht"] = (d.m_pad * self.n_out // 16 if self.rht_colwise
+                            else sf_bytes(d.m_pad, self.n_out, 16, 1))
         return out
 
     # calls ---------------------------------------------------------------
@@ -287,7 +292,8 @@ def measure_mma_peak(in_format: str, tile_n: int = 256, mmas_per_sm: int = 40000
 
 _DESC_KEYS = ("m_pad", "n", "k", "num_groups", "in_format", "out_format", "epilogue", "want_col",
               "gate_first", "tanh_clamp_s", "tile", "cluster", "glu_limit", "glu_alpha", "c_format",
-              "bias_format", "discrete_b", "saved_c_format", "rht_format", "dgeglu_params", "situ_betas")
+              "bias_format", "discrete_b", "saved_c_format", "rht_format", "dgeglu_params", "situ_betas",
+              "rht_colwise")
 
 
 def run_noalloc(*, stream=None, wait_status: bool = True, **kw) -> int:

@@ -152,9 +152,15 @@ bsgg_status validate(const bsgg_desc* d) {
       d->saved_c_format != BSGG_OUT_F32)
     return BSGG_ERR_INVALID_ARG;
   // the Hadamard output: bf16 or NVFP4, forward epilogues only
-  if (d->want_rht != 0 && d->want_rht != 1) return BSGG_ERR_INVALID_ARG;
+  if (d->want_rht < 0 || d->want_rht > 2) return BSGG_ERR_INVALID_ARG;
   if (d->want_rht && ((d->rht_format != BSGG_OUT_BF16 && d->rht_format != BSGG_OUT_E2M1) || bwd))
     return BSGG_ERR_INVALID_ARG;
+  // colwise: NVFP4 only, N_out % 128 (per-expert scale segments of N_out * expert_m / 16
+  // bytes; "Grouped GEMM + GLU + Hadamard + Quant (SM100)", Constraints)
+  if (d->want_rht == 2) {
+    const int64_t n_out = glu ? d->n / 2 : d->n;
+    if (d->rht_format != BSGG_OUT_E2M1 || n_out % 128 != 0) return BSGG_ERR_INVALID_ARG;
+  }
   if (d->want_col && !is_quant(d->out_format)) return BSGG_ERR_INVALID_ARG;
   // NVFP4 inputs: the pages allow 16/32-bit float outputs; FP4 output is this
   // build's reading for the NVFP4 sReLU workload.  FP8 outputs from FP4 inputs
@@ -510,6 +516,7 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
     p.rht_norm_const = a->rht_norm_const;
     p.rht_kind = d.rht_format == BSGG_OUT_E2M1 ? bsgg::OK_E2M1 : bsgg::OK_BF16;
     p.kq_rht = static_cast<int32_t>(ceil_div(ceil_div(P->n_out, 16), 4));
+    p.rht_colwise = d.want_rht == 2 ? 1 : 0;
   }
   if (is_bwd_epi(d.epilogue)) {
     p.saved_c = a->saved_c;
@@ -653,7 +660,7 @@ bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* 
        d2h(d.want_rht ? host->rht : nullptr, dev->rht,
            uint64_t(d.m_pad) * (d.rht_format == BSGG_OUT_E2M1 ? P->n_out / 2 : P->n_out * 2)) &&
        d2h(d.want_rht && d.rht_format == BSGG_OUT_E2M1 ? host->sfrht : nullptr, dev->sfrht,
-           sf_bytes_impl(d.m_pad, P->n_out, 16, 1)) &&
+           d.want_rht == 2 ? uint64_t(d.m_pad) * P->n_out / 16 : sf_bytes_impl(d.m_pad, P->n_out, 16, 1)) &&
        d2h(d.want_c ? host->c : nullptr, dev->c, uint64_t(d.m_pad) * d.n * 2);
   if (!ok) return BSGG_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return BSGG_ERR_CUDA;

@@ -148,6 +148,7 @@ struct Params {
   const float* rht_norm_const;
   int32_t rht_kind;         // OK_BF16 or OK_E2M1
   int32_t kq_rht;           // SF atoms per 128 rows of SFRHT: ceil(ceil(n_out/16)/4)
+  int32_t rht_colwise;      // 1: 16-token blocks per column, per-expert transposed (NVFP4)
   // discrete weight mode: per-expert tensor maps {B_g, SFB_g} (2 per expert, in
   // global memory) and the flag their writer raises for a bad pointer; null in
   // dense mode
@@ -592,13 +593,51 @@ __device__ __forceinline__ void rht_chunk(const Params& p, const float (&v)[32],
   }
 }
 
+// Colwise Hadamard output of one 32-column chunk of D held by a warp (lane =
+// row): each half-warp's 16 rows are a block of 16 consecutive tokens of the
+// expert whose padded rows start at seg_start (em of them).  Per column: bf16
+// rounding, the 16-point transform across the half-warp's lanes (four xor
+// butterfly stages, entry (i, j) of H16 = (-1)^popcount(i & j)) times 1/4, the
+// block's E4M3 scale under rnorm, E2M1 codes paired by neighbouring lanes into
+// bytes at flat element n_out * seg_start + column * em + token.
+__device__ __forceinline__ void rht_col_chunk(const Params& p, const float (&v)[32], int row, int col0, int lane,
+                                              int64_t seg_start, int em, float rnorm) {
+  const int t = static_cast<int>(row - seg_start);     // token within the expert
+  const int64_t seg_elem = static_cast<int64_t>(p.n_out) * seg_start;
+  const int kq = (em / 16 + 3) / 4;                    // SF atoms per 128 columns of the segment
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    float y = __bfloat162float(__float2bfloat16_rn(v[j]));
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+      const float other = __shfl_xor_sync(0xffffffffu, y, o);
+      y = (lane & o) ? (other - y) : (y + other);
+    }
+    y *= 0.25f;
+    float am = fabsf(y);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    uint32_t code;
+    float s;
+    block_scale<true>(am, rnorm, 1.0f / 6.0f, code, s);
+    const float q = y * s;
+    const float q_odd = __shfl_xor_sync(0xffffffffu, q, 1);
+    const int n = col0 + j;
+    if ((lane & 1) == 0) {
+      const int64_t e = seg_elem + static_cast<int64_t>(n) * em + t;   // even: low nibble
+      static_cast<uint8_t*>(p.rht)[e >> 1] = static_cast<uint8_t>(cvt_e2m1x2(q, q_odd));
+    }
+    if ((lane & 15) == 0) p.sfrht[seg_elem / 16 + sf_off(n, t / 16, kq)] = static_cast<uint8_t>(code);
+  }
+}
+
 // Step 2 and Step 3 for one 32-column chunk of one row: C = al * xs (the
 // input half for the GLUs; fp32 bits), al * gs the gate half.  al is alpha_g,
 // or 1 where alpha and the bias were already applied in place.
 template <bool FP4, int EPI, int OUTC, bool XC>
 __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* xs, const uint32_t* gs, int row,
                                                int col0, float al, float pr, float norm, int lane, int kblk_col,
-                                               float& amax_local) {
+                                               float& amax_local, int64_t seg_start, int seg_rows) {
   float v[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
@@ -628,7 +667,10 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* 
     }
   }
   output_chunk<FP4, OUTC>(p, v, row, col0, norm, lane, kblk_col, amax_local);
-  if (XC && p.rht != nullptr) rht_chunk(p, v, row, col0, *p.rht_norm_const);
+  if (XC && p.rht != nullptr) {
+    if (p.rht_colwise) rht_col_chunk(p, v, row, col0, lane, seg_start, seg_rows, *p.rht_norm_const);
+    else rht_chunk(p, v, row, col0, *p.rht_norm_const);
+  }
 }
 
 // XC: a forward launch adds a bias to C, stores C or writes the Hadamard
@@ -1080,6 +1122,8 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
       const float pr = p.prob[row];
       const float al = p.alpha[g];
       const int kblk_col = mt * 4 + q;                // this warp's 32-row block
+      const int64_t seg_start = g ? s_off[g - 1] : 0;  // the group's padded rows (colwise RHT)
+      const int seg_rows = static_cast<int>(s_off[g] - seg_start);
       // With a bias or a C output: C = alpha_g * acc + bias_g[n] in place (then
       // al = 1), stored when asked for ("Grouped GEMM + GLU + Hadamard + Quant
       // (SM100)", Equations)
@@ -1200,7 +1244,8 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
             xs[i] = gf ? r[64 * j + 32 + i] : r[64 * j + i];
             gs[i] = gf ? r[64 * j + i] : r[64 * j + 32 + i];
           }
-          epilogue_chunk<FP4, EPI, OUTC, XC>(p, xs, gs, row, col0, al_epi, pr, norm, lane, kblk_col, amax_local);
+          epilogue_chunk<FP4, EPI, OUTC, XC>(p, xs, gs, row, col0, al_epi, pr, norm, lane, kblk_col, amax_local,
+                                             seg_start, seg_rows);
         }
       } else {
 #pragma unroll
@@ -1208,7 +1253,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
           const int col0 = nt * BN + e * kWarpCols + 32 * c;
           if (col0 >= p.n_out) continue;
           epilogue_chunk<FP4, EPI, OUTC, XC>(p, &r[32 * c], &r[32 * c], row, col0, al_epi, pr, norm, lane,
-                                             kblk_col, amax_local);
+                                             kblk_col, amax_local, seg_start, seg_rows);
         }
       }
       if (OUTC == OUTC_FLOAT && p.amax != nullptr) {

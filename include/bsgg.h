@@ -169,12 +169,20 @@ typedef struct {
   /* DSWIGLU: storage type of the saved forward C, BSGG_OUT_BF16, BSGG_OUT_F16 or
      BSGG_OUT_F32 ("Grouped GEMM + dGLU (SM100)", BF16 contract: C in BF16/FP16/FP32). */
   int32_t saved_c_format;
-  /* Rowwise Hadamard output ("Grouped GEMM + GLU + Hadamard + Quant (SM100)",
-     Equations): 1 = also write RHT = (H16 / 4) x for every 16-column block x of
-     bf16-rounded D, H16 the 16 x 16 Sylvester Hadamard matrix; (m_pad, N_out)
-     N-major in rht_format: BSGG_OUT_BF16, or BSGG_OUT_E2M1 (packed NVFP4 with
-     E4M3 scales per 16 in SFRHT = swizzled SF(m_pad, N_out) under
-     rht_norm_const, whatever the input's scale type).  Forward epilogues only. */
+  /* Hadamard output ("Grouped GEMM + GLU + Hadamard + Quant (SM100)", Outputs and
+     Equations), forward epilogues only; H16 is the 16 x 16 Sylvester Hadamard matrix.
+     1 = rowwise: RHT = (H16 / 4) x for every 16-column block x of bf16-rounded D;
+         (m_pad, N_out) N-major in rht_format: BSGG_OUT_BF16, or BSGG_OUT_E2M1 (packed
+         NVFP4 with E4M3 scales per 16 in SFRHT = swizzled SF(m_pad, N_out) under
+         rht_norm_const, whatever the input's scale type).
+     2 = colwise (rht_format BSGG_OUT_E2M1, N_out % 128 == 0): (H16 / 4) x for every
+         column and every block x of 16 consecutive tokens of an expert (rows of its
+         padded range, counted from its start), NVFP4 with one E4M3 scale per block;
+         expert g (padded rows [start_g, end_g), expert_m = end_g - start_g) is the
+         logical (N_out, expert_m) matrix, tokens contiguous, from flat element
+         N_out * start_g of RHT (m_pad * N_out / 2 bytes in all), its scales the
+         swizzled SF(N_out, expert_m) from byte N_out * start_g / 16 of SFRHT
+         (m_pad * N_out / 16 bytes in all). */
   int32_t want_rht;
   int32_t rht_format;
   /* DGEGLU: 0 = the page's defaults (geglu_alpha 1.702, clamp [-7, 7], linear_offset 1),

@@ -115,6 +115,8 @@ def _create(**over):
     (dict(epilogue="dgeglu", dgeglu_params=(1.0, 7.0, -7.0, 1.0)), 1),    # min <= max
     (dict(epilogue="dgeglu", dgeglu_params=(float("nan"), -7.0, 7.0, 1.0)), 1),
     (dict(epilogue="dsituglu", situ_betas=(-1.0, 1.0)), 1),
+    (dict(rht_format="bf16", rht_colwise=True), 1),               # colwise RHT is NVFP4
+    (dict(n=128, epilogue="swiglu", rht_format="e2m1", rht_colwise=True), 1),   # N_out % 128
     (dict(epilogue="dsituglu", situ_betas=(1.0, float("inf"))), 1),
     (dict(epilogue="dswiglu", situ_betas=(2.0, 2.0)), 1),          # dSiTU-GLU's own
 ])

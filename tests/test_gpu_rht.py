@@ -34,6 +34,31 @@ def _check_bf16_rht(got, ref, d_ref):
     assert not bad.any(), f"RHT: {int(bad.sum())} of {bad.size} out of tolerance"
 
 
+def _check_colwise(p, outs, ref, rht_norm):
+    """Per expert: the (n_out, expert_m) code matrix and its per-16-token scales
+    of the GPU against the oracle's, by the quantized-output rule."""
+    nd = p.n_out
+    off = np.asarray(p.padded_offsets.cpu())
+    gq_all = outs["rht"].cpu().numpy()
+    gs_all = outs["sfrht"].cpu().numpy()
+    nib = lambda b: np.stack([b & 0xF, b >> 4], -1).reshape(-1)
+    g_codes, r_codes = nib(gq_all), nib(ref["rht_q"])
+    start = 0
+    for g in range(p.num_groups):
+        em = int(off[g]) - start
+        if em == 0:
+            continue
+        e0 = nd * start
+        gq = g_codes[e0:e0 + nd * em].reshape(nd, em)
+        rq = r_codes[e0:e0 + nd * em].reshape(nd, em)
+        offs = np.array([[nd * start // 16 + orc.sf_offset(n, b, 0, nd, em // 16) for b in range(em // 16)]
+                         for n in range(nd)])
+        y = ref["rht_ref"][start:start + em].T                 # (n_out, expert_m)
+        _check_quant_plane(gq, rq, gs_all[offs], ref["sfrht"][offs], y, "e2m1", "nvfp4", rht_norm, 16, 1,
+                           f"colwise RHT expert {g}")
+        start = int(off[g])
+
+
 def _run(p, tile, rht_format, rht_norm=1.0, **desc):
     pd = to_device(p)
     plan = bsgg.Plan(m_pad=p.m_pad, n=p.n, k=p.k, num_groups=p.num_groups, in_format=p.in_fmt,
@@ -49,10 +74,13 @@ def _run(p, tile, rht_format, rht_norm=1.0, **desc):
     over = {}
     if "glu_limit" in desc:
         over["glu_limit"] = desc["glu_limit"]
-    ref = oracle_run(p, rht=rht_format, rht_norm=rht_norm, **over)
+    colwise = desc.get("rht_colwise", False)
+    ref = oracle_run(p, rht="col_e2m1" if colwise else rht_format, rht_norm=rht_norm, **over)
     compare(p, outs, ref)
     nd = p.n_out
-    if rht_format == "bf16":
+    if colwise:
+        _check_colwise(p, outs, ref, rht_norm)
+    elif rht_format == "bf16":
         got = decode_float_out(outs["rht"].cpu().numpy(), "bf16", p.m_pad, nd)
         _check_bf16_rht(got, ref["rht_ref"], ref["d_ref"])
         if p.out_fmt == "bf16":
@@ -96,3 +124,14 @@ def test_geglu_srelu_with_rht_bias_and_c(tile):
     p = small_problem(counts=(128, 60), k=256, n=128, pad_to=128, epi="srelu", out_fmt="e4m3",
                       want_col=True, tanh_clamp_s=8.0, seed=83)
     _run(p, tile, "bf16")
+
+
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
+def test_colwise_rht_nvfp4(tile):
+    # experts of 256, 0, 384 and 128 padded rows; N_out = 256
+    p = small_problem(counts=(150, 0, 300, 128), k=512, n=512, pad_to=128, in_fmt="nvfp4", epi="swiglu",
+                      out_fmt="e2m1", seed=84)
+    _run(p, tile, "e2m1", rht_norm=0.5, rht_colwise=True)
+    p = small_problem(counts=(200, 77), k=256, n=256, pad_to=128, epi="srelu", out_fmt="e4m3",
+                      want_col=True, tanh_clamp_s=8.0, seed=85)
+    _run(p, tile, "e2m1", rht_norm=2.0, rht_colwise=True)
