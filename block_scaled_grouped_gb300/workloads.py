@@ -31,7 +31,8 @@ from typing import List, Optional, Sequence
 import numpy as np
 import torch
 
-IN_FORMATS = ("mxfp8_e4m3", "mxfp8_e5m2", "nvfp4")
+IN_FORMATS = ("mxfp8_e4m3", "mxfp8_e5m2", "nvfp4", "fp4_ue8m0_16", "mxfp4")
+FP4_FORMATS = ("nvfp4", "fp4_ue8m0_16", "mxfp4")
 OUT_FORMATS = ("bf16", "f16", "f32", "e4m3", "e5m2", "e2m1")
 EPILOGUES = ("gate", "swiglu", "srelu", "geglu", "dswiglu", "dgeglu", "dsituglu")
 BWD_EPILOGUES = ("dswiglu", "dgeglu", "dsituglu")
@@ -68,7 +69,7 @@ class Problem:
 
     @property
     def sf_vec(self) -> int:
-        return 16 if self.in_fmt == "nvfp4" else 32
+        return 16 if self.in_fmt in ("nvfp4", "fp4_ue8m0_16") else 32
 
     @property
     def n_out(self) -> int:
@@ -182,9 +183,34 @@ def quantize_nvfp4(x: torch.Tensor):
     return packed, scode
 
 
+def quantize_fp4_ue8m0(x: torch.Tensor, v: int):
+    """float32 (R, K) -> (packed codes uint8 (R, K/2), scale codes uint8 (R, ceil(K/v))).
+
+    One UE8M0 scale per 1xv block, scale = 2^ceil(log2(amax/6)) (so that every
+    value lands inside E2M1's range), data the E2M1 RNE of x/scale; an all-zero
+    block gets scale 1.0 (code 127).  Element 2i in the low nibble of byte i.
+    """
+    R, K = x.shape
+    assert K % 2 == 0
+    xp = _pad_cols(x, v)
+    xb = xp.view(R, -1, v)
+    amax = xb.abs().amax(-1)
+    mant, ex = torch.frexp(amax / 6.0)
+    e = torch.where(mant == 0.5, ex - 1, ex).to(torch.int32)
+    e = torch.where(amax == 0, torch.zeros_like(e), e).clamp(-127, 127)
+    scale = torch.ldexp(torch.ones_like(amax), e)
+    codes = _e2m1_rne(xb / scale.unsqueeze(-1)).reshape(R, -1)[:, :K]
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).contiguous()
+    return packed, (e + 127).to(torch.uint8)
+
+
 def quantize(x: torch.Tensor, in_fmt: str):
     if in_fmt == "nvfp4":
         return quantize_nvfp4(x)
+    if in_fmt == "fp4_ue8m0_16":
+        return quantize_fp4_ue8m0(x, 16)
+    if in_fmt == "mxfp4":
+        return quantize_fp4_ue8m0(x, 32)
     return quantize_mxfp8(x, in_fmt)
 
 
@@ -285,8 +311,8 @@ def build_problem(*, name: str, counts: Sequence[int], k: int, n: int, in_fmt: s
     if row_prob is None:
         row_prob = [rng.uniform(0.0, 1.0, size=int(c)).astype(np.float32) for c in counts]
 
-    v = 16 if in_fmt == "nvfp4" else 32
-    kbytes = k // 2 if in_fmt == "nvfp4" else k
+    v = 16 if in_fmt in ("nvfp4", "fp4_ue8m0_16") else 32
+    kbytes = k // 2 if in_fmt in FP4_FORMATS else k
     kblocks = -(-k // v)
     prob = np.zeros(m_pad, dtype=np.float32)
     a = torch.zeros(m_pad, kbytes, dtype=torch.uint8, device=device)

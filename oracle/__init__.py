@@ -27,7 +27,7 @@ _lib = None
 
 # Format codes of the oracle (its own numbering, see bsgg_oracle.cpp).
 F_E4M3, F_E5M2, F_E2M1, F_UE8M0 = 0, 1, 2, 3
-IN_MXFP8_E4M3, IN_MXFP8_E5M2, IN_NVFP4 = 0, 1, 2
+IN_MXFP8_E4M3, IN_MXFP8_E5M2, IN_NVFP4, IN_FP4_UE8M0_16, IN_MXFP4 = 0, 1, 2, 3, 4
 OUT_BF16, OUT_F16, OUT_F32, OUT_E4M3, OUT_E5M2, OUT_E2M1 = 0, 1, 2, 3, 4, 5
 EPI_GATE, EPI_SWIGLU, EPI_SRELU, EPI_GEGLU, EPI_DSWIGLU, EPI_DGEGLU, EPI_DSITUGLU = 0, 1, 2, 3, 4, 5, 6
 BWD_EPIS = (EPI_DSWIGLU, EPI_DGEGLU, EPI_DSITUGLU)
@@ -220,7 +220,7 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
         outs.setdefault("rht_q", np.zeros(m_pad * nd // 2, dtype=np.uint8))
         outs.setdefault("sfrht", np.zeros(m_pad * nd // 16, dtype=np.uint8))
     quant = out_fmt >= OUT_E4M3
-    v = 16 if in_fmt == IN_NVFP4 else 32
+    v = 16 if in_fmt in (IN_NVFP4, IN_FP4_UE8M0_16) else 32
     if quant:
         row_bytes = nd // 2 if out_fmt == OUT_E2M1 else nd
         outs.setdefault("d", np.zeros((m_pad, row_bytes), dtype=np.uint8))

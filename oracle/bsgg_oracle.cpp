@@ -159,7 +159,9 @@ int64_t sf_bytes(int64_t rows, int64_t kblocks, int64_t L) {
 // ---------------------------------------------------------------------------
 // Problem description (the oracle's own; the library's header is not used).
 // ---------------------------------------------------------------------------
-enum InFmt { IN_MXFP8_E4M3 = 0, IN_MXFP8_E5M2 = 1, IN_NVFP4 = 2 };
+// "Grouped GEMM + Quant (SM100)", Data Types: FP4 data takes E4M3 scales per 16
+// (NVFP4) or UE8M0 scales per 16 or 32 (E4M3 is incompatible with 32).
+enum InFmt { IN_MXFP8_E4M3 = 0, IN_MXFP8_E5M2 = 1, IN_NVFP4 = 2, IN_FP4_UE8M0_16 = 3, IN_MXFP4 = 4 };
 enum OutFmt { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2, OUT_E4M3 = 3, OUT_E5M2 = 4, OUT_E2M1 = 5 };
 // EPI_DSWIGLU, EPI_DGEGLU, EPI_DSITUGLU: the backward epilogues of "Grouped GEMM +
 // dGLU (SM100)".
@@ -318,9 +320,11 @@ struct Job {
   std::mutex mu;
 };
 
-bool is_fp4_in(const orc_desc* P) { return P->in_fmt == IN_NVFP4; }
-int sf_vec(const orc_desc* P) { return is_fp4_in(P) ? 16 : 32; }
-int sf_fmt(const orc_desc* P) { return is_fp4_in(P) ? F_E4M3 : F_UE8M0; }
+bool is_fp4_in(const orc_desc* P) {
+  return P->in_fmt == IN_NVFP4 || P->in_fmt == IN_FP4_UE8M0_16 || P->in_fmt == IN_MXFP4;
+}
+int sf_vec(const orc_desc* P) { return (P->in_fmt == IN_NVFP4 || P->in_fmt == IN_FP4_UE8M0_16) ? 16 : 32; }
+int sf_fmt(const orc_desc* P) { return P->in_fmt == IN_NVFP4 ? F_E4M3 : F_UE8M0; }
 int data_fmt(const orc_desc* P) {
   return P->in_fmt == IN_MXFP8_E4M3 ? F_E4M3 : P->in_fmt == IN_MXFP8_E5M2 ? F_E5M2 : F_E2M1;
 }

@@ -134,7 +134,7 @@ def check_sf_codes(got: np.ndarray, ref: np.ndarray, what: str, min_equal=0.999)
 
 
 def _sf_value(codes: np.ndarray, in_fmt: str) -> np.ndarray:
-    dt = torch.float8_e4m3fn if in_fmt == "nvfp4" else torch.float8_e8m0fnu
+    dt = torch.float8_e4m3fn if in_fmt == "nvfp4" else torch.float8_e8m0fnu   # UE8M0 for MXFP8 and the UE8M0 FP4 forms
     return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(dt).double().numpy()
 
 

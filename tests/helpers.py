@@ -9,7 +9,8 @@ import torch
 import oracle as orc
 from block_scaled_grouped_gb300 import workloads as W
 
-IN_CODE = {"mxfp8_e4m3": orc.IN_MXFP8_E4M3, "mxfp8_e5m2": orc.IN_MXFP8_E5M2, "nvfp4": orc.IN_NVFP4}
+IN_CODE = {"mxfp8_e4m3": orc.IN_MXFP8_E4M3, "mxfp8_e5m2": orc.IN_MXFP8_E5M2, "nvfp4": orc.IN_NVFP4,
+           "fp4_ue8m0_16": orc.IN_FP4_UE8M0_16, "mxfp4": orc.IN_MXFP4}
 OUT_CODE = {"bf16": orc.OUT_BF16, "f16": orc.OUT_F16, "f32": orc.OUT_F32, "e4m3": orc.OUT_E4M3,
             "e5m2": orc.OUT_E5M2, "e2m1": orc.OUT_E2M1}
 EPI_CODE = {"gate": orc.EPI_GATE, "swiglu": orc.EPI_SWIGLU, "srelu": orc.EPI_SRELU, "geglu": orc.EPI_GEGLU,
@@ -47,13 +48,14 @@ def dequant_dense(codes: np.ndarray, sf_rows: np.ndarray, in_fmt: str, k: int) -
     """Brute-force dequantization of a K-major operand with row-major scale
     codes (R, k/v), independent of the oracle's tables."""
     codes = np.ascontiguousarray(codes)
-    if in_fmt == "nvfp4":
+    if in_fmt in ("nvfp4", "fp4_ue8m0_16", "mxfp4"):
         lo = codes & 0xF
         hi = codes >> 4
         nib = np.stack([lo, hi], axis=-1).reshape(codes.shape[0], -1)[:, :k]
         vals = E2M1_VALUES[nib]
-        sc = torch.from_numpy(np.ascontiguousarray(sf_rows)).view(torch.float8_e4m3fn).double().numpy()
-        v = 16
+        sdt = torch.float8_e4m3fn if in_fmt == "nvfp4" else torch.float8_e8m0fnu
+        sc = torch.from_numpy(np.ascontiguousarray(sf_rows)).view(sdt).double().numpy()
+        v = 32 if in_fmt == "mxfp4" else 16
     else:
         dt = torch.float8_e4m3fn if in_fmt == "mxfp8_e4m3" else torch.float8_e5m2
         vals = torch.from_numpy(codes).view(dt).double().numpy()[:, :k]

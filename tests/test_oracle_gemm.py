@@ -331,3 +331,35 @@ def test_row_and_column_quantization_properties(in_fmt, out_fmt, norm):
                 deq = Dc[blk_rows, j] * sf / norm
                 step = {"e4m3": 2 ** -3, "e5m2": 2 ** -2, "e2m1": 1.0 / 3.0}[out_fmt]
                 assert np.all(np.abs(deq - D[blk_rows, j]) <= step * am + 1e-30)
+
+
+@pytest.mark.parametrize("in_fmt", ["fp4_ue8m0_16", "mxfp4"])
+def test_fp4_with_ue8m0_scales_against_brute_force(in_fmt):
+    """FP4 data with UE8M0 scales per 16 or per 32 ("Grouped GEMM + Quant
+    (SM100)", Data Types: NVF4 with float8_e8m0fnu scales): C against the
+    brute-force dense matmul (torch's e8m0 decoding, E2M1 listed values), with
+    spread scales; quantized E2M1 output with UE8M0 block scales rounded up."""
+    from helpers import brute_force_C, oracle_run, small_problem, np_
+    p = small_problem(counts=(40, 0, 70), k=192, n=64, in_fmt=in_fmt, out_fmt="f32", seed=17)
+    g = torch.Generator().manual_seed(4)
+    p.sfa_rows = torch.randint(120, 134, p.sfa_rows.shape, generator=g).to(torch.uint8)
+    p.sfb_rows = torch.randint(120, 134, p.sfb_rows.shape, generator=g).to(torch.uint8)
+    out = oracle_run(p)
+    C = brute_force_C(p)
+    rows = ~np.isnan(C[:, 0])
+    want = C * np_(p.prob)[:, None]
+    np.testing.assert_allclose(out["d_ref"][rows], want[rows], rtol=1e-12, atol=1e-9)
+    # E2M1 output: per 16 (or 32) columns a UE8M0 scale = least power of two >= max|D| / 6
+    q = small_problem(counts=(64,), k=128, n=64, in_fmt=in_fmt, out_fmt="e2m1", seed=18)
+    oq = oracle_run(q)
+    v = 32 if in_fmt == "mxfp4" else 16
+    import oracle as orc
+    for r in range(0, 64, 9):
+        for b in range(64 // v):
+            code = int(oq["sfd_row"][orc.sf_offset(r, b, 0, q.m_pad, 64 // v)])
+            am = float(np.abs(oq["d_ref"][r, v * b:v * b + v]).astype(np.float32).max())
+            if am == 0:
+                assert code == 0
+                continue
+            sf = 2.0 ** (code - 127)
+            assert sf >= am / 6 * (1 - 1e-6) and sf / 2 < am / 6
