@@ -40,9 +40,9 @@ sys.path.insert(0, ROOT)
 METRIC = "grouped GEMM TFLOP/s (valid rows) and % of GB300 dense FP8/FP4 peak, 1 GPU"
 UNIT = "TFLOP/s"
 # nominal dense tensor throughput relative to bf16 (2.25 PFLOP/s): fp8 4.5, fp4 13.5
-DTYPE_RATIO = {"mxfp8_e4m3": 2.0, "mxfp8_e5m2": 2.0, "nvfp4": 6.0}
+DTYPE_RATIO = {"mxfp8_e4m3": 2.0, "mxfp8_e5m2": 2.0, "nvfp4": 6.0, "fp4_ue8m0_16": 6.0, "mxfp4": 6.0}
 DTYPE_NAME = {"mxfp8_e4m3": "mxfp8(e4m3,ue8m0/32)", "mxfp8_e5m2": "mxfp8(e5m2,ue8m0/32)",
-              "nvfp4": "nvfp4(e2m1,e4m3/16)"}
+              "nvfp4": "nvfp4(e2m1,e4m3/16)", "fp4_ue8m0_16": "fp4(e2m1,ue8m0/16)", "mxfp4": "mxfp4(e2m1,ue8m0/32)"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -203,7 +203,8 @@ def oracle_sample(p, ins, budget_s: float, max_blocks: int = 64, seed: int = 0):
     """Time the oracle on 32-row blocks of real rows, one call per block, until
     budget_s of wall time is spent.  Returns (flops, seconds, blocks, threads)."""
     import oracle as orc
-    code_in = {"mxfp8_e4m3": orc.IN_MXFP8_E4M3, "mxfp8_e5m2": orc.IN_MXFP8_E5M2, "nvfp4": orc.IN_NVFP4}
+    code_in = {"mxfp8_e4m3": orc.IN_MXFP8_E4M3, "mxfp8_e5m2": orc.IN_MXFP8_E5M2, "nvfp4": orc.IN_NVFP4,
+               "fp4_ue8m0_16": orc.IN_FP4_UE8M0_16, "mxfp4": orc.IN_MXFP4}
     code_out = {"bf16": orc.OUT_BF16, "f16": orc.OUT_F16, "f32": orc.OUT_F32, "e4m3": orc.OUT_E4M3,
                 "e5m2": orc.OUT_E5M2, "e2m1": orc.OUT_E2M1}
     code_epi = {"gate": orc.EPI_GATE, "swiglu": orc.EPI_SWIGLU, "srelu": orc.EPI_SRELU, "geglu": orc.EPI_GEGLU,
@@ -248,8 +249,8 @@ def algorithmic_bytes(p) -> int:
 
     def sfb(rows, cols, v, slices=1):
         return 512 * slices * cdiv(rows, 128) * cdiv(cdiv(cols, v), 4)
-    fp4 = p.in_fmt == "nvfp4"
-    v = 16 if fp4 else 32
+    fp4 = p.in_fmt in ("nvfp4", "fp4_ue8m0_16", "mxfp4")
+    v = p.sf_vec
     kb = p.k // 2 if fp4 else p.k
     off = [int(x) for x in p.padded_offsets.tolist()]
     nonempty = sum(1 for g, e in enumerate(off) if e > (off[g - 1] if g else 0))

@@ -14,7 +14,7 @@ from typing import Optional
 
 from . import build as _build
 
-IN_FORMATS = {"mxfp8_e4m3": 0, "mxfp8_e5m2": 1, "nvfp4": 2}
+IN_FORMATS = {"mxfp8_e4m3": 0, "mxfp8_e5m2": 1, "nvfp4": 2, "fp4_ue8m0_16": 3, "mxfp4": 4}
 OUT_FORMATS = {"bf16": 0, "f16": 1, "f32": 2, "e4m3": 3, "e5m2": 4, "e2m1": 5}
 EPILOGUES = {"gate": 0, "swiglu": 1, "srelu": 2, "geglu": 3, "dswiglu": 4, "dgeglu": 5, "dsituglu": 6}
 BWD_EPILOGUES = ("dswiglu", "dgeglu", "dsituglu")
@@ -200,7 +200,7 @@ class Plan:
     # shapes --------------------------------------------------------------
     @property
     def sf_vec(self) -> int:
-        return 16 if self.in_format == "nvfp4" else 32
+        return 16 if self.in_format in ("nvfp4", "fp4_ue8m0_16") else 32
 
     @property
     def n_out(self) -> int:

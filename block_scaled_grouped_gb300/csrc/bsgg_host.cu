@@ -104,7 +104,7 @@ bsgg_status validate(const bsgg_desc* d) {
   if (d->m_pad <= 0 || d->m_pad % 128 != 0 || d->m_pad > (int64_t(1) << 30)) return BSGG_ERR_INVALID_ARG;
   if (d->n <= 0 || d->k <= 0 || d->n > (int64_t(1) << 24) || d->k > (int64_t(1) << 24))
     return BSGG_ERR_INVALID_ARG;
-  if (d->in_format < BSGG_IN_MXFP8_E4M3 || d->in_format > BSGG_IN_NVFP4) return BSGG_ERR_INVALID_ARG;
+  if (d->in_format < BSGG_IN_MXFP8_E4M3 || d->in_format > BSGG_IN_MXFP4) return BSGG_ERR_INVALID_ARG;
   if (d->out_format < BSGG_OUT_BF16 || d->out_format > BSGG_OUT_E2M1) return BSGG_ERR_INVALID_ARG;
   if (d->epilogue < BSGG_EPI_GATE || d->epilogue > BSGG_EPI_DSITUGLU) return BSGG_ERR_INVALID_ARG;
   const bool glu = d->epilogue == BSGG_EPI_SWIGLU || d->epilogue == BSGG_EPI_GEGLU;
@@ -123,8 +123,12 @@ bsgg_status validate(const bsgg_desc* d) {
   if (d->want_col != 0 && d->want_col != 1) return BSGG_ERR_INVALID_ARG;
   // K-major rows must be 16-byte aligned ("Support Surface and Constraints",
   // Layouts and Strides): K % 16 for FP8, K % 32 for packed FP4.
-  const bool fp4 = d->in_format == BSGG_IN_NVFP4;
+  const bool fp4 = d->in_format >= BSGG_IN_NVFP4;
   if (d->k % (fp4 ? 32 : 16) != 0) return BSGG_ERR_INVALID_ARG;
+  // UE8M0-scaled FP4 has kernel instances for single CTAs and CTA pairs only
+  // (one scale per 32 values reaches the MMA through the scale-store warps,
+  // which the multicast clusters do not have)
+  if (d->in_format > BSGG_IN_NVFP4 && d->cluster_m == 2 && d->tile_m != 256) return BSGG_ERR_UNSUPPORTED;
   // SwiGLU pairs 32-column blocks: N % 64 ("Grouped GEMM + SwiGLU (SM100)",
   // Shapes and Divisibility).  Outputs are written in 32-column chunks.
   if (glu ? (d->n % 64 != 0) : (d->n % 32 != 0)) return BSGG_ERR_INVALID_ARG;
@@ -172,6 +176,7 @@ bsgg_status validate(const bsgg_desc* d) {
 uint32_t make_idesc(int in_format, int bn, bool pair) {
   uint32_t fmt, scale_ue8m0;
   if (in_format == BSGG_IN_NVFP4) { fmt = 1; scale_ue8m0 = 0; }          // E2M1, UE4M3 scales
+  else if (in_format > BSGG_IN_NVFP4) { fmt = 1; scale_ue8m0 = 1; }      // E2M1, UE8M0 scales (per 16 slots)
   else { fmt = (in_format == BSGG_IN_MXFP8_E4M3) ? 0u : 1u; scale_ue8m0 = 1; }  // E4M3/E5M2, UE8M0
   uint32_t d = 0;
   d |= fmt << 7;                                      // A format
@@ -201,7 +206,10 @@ bsgg_status encode_one(CUtensorMap* map, const void* base, int rank, const cuuin
 bsgg_status encode_maps(const bsgg_plan* P, const bsgg_args* a, bsgg::Launch* L) {
   const bsgg_desc& d = P->desc;
   const int64_t kq = ceil_div(ceil_div(d.k, P->sf_vec), 4);
-  const int atoms = P->desc.in_format == BSGG_IN_NVFP4 ? 4 : 1;
+  // scale atoms per stage (an atom = 4 scales of 128 rows): 4 for FP4 with one
+  // scale per 16 values, 2 per 32, 1 for MXFP8
+  const bool fp4 = P->desc.in_format >= BSGG_IN_NVFP4;
+  const int atoms = !fp4 ? 1 : P->sf_vec == 32 ? 2 : 4;
   bsgg_status st;
   {
     cuuint64_t dims[2] = {cuuint64_t(P->kbytes), cuuint64_t(d.m_pad)};
@@ -272,14 +280,15 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
   P->outc = desc->out_format == BSGG_OUT_E2M1 ? bsgg::OUTC_FP4
             : is_quant(desc->out_format)      ? bsgg::OUTC_FP8
                                               : bsgg::OUTC_FLOAT;
-  P->sf_vec = desc->in_format == BSGG_IN_NVFP4 ? 16 : 32;
-  P->kbytes = desc->in_format == BSGG_IN_NVFP4 ? desc->k / 2 : desc->k;
+  const bool fp4 = desc->in_format >= BSGG_IN_NVFP4;
+  P->sf_vec = (desc->in_format == BSGG_IN_NVFP4 || desc->in_format == BSGG_IN_FP4_UE8M0_16) ? 16 : 32;
+  P->kbytes = fp4 ? desc->k / 2 : desc->k;
   P->n_out = (desc->epilogue == BSGG_EPI_SWIGLU || desc->epilogue == BSGG_EPI_GEGLU) ? desc->n / 2
              : is_bwd_epi(desc->epilogue)                                             ? 2 * desc->n
                                                                                       : desc->n;
   P->out_row_bytes = P->n_out * out_elem_bits(desc->out_format) / 8;
   if (P->pair || P->mc) {
-    int resident = bsgg::cluster_resident_ctas(desc->in_format == BSGG_IN_NVFP4, P->mc);
+    int resident = bsgg::cluster_resident_ctas(fp4, P->mc);
     if (resident <= 0) resident = num_sms;
     P->grid = std::max(2, (std::min(resident, num_sms) / 2) * 2);
   } else {
@@ -496,6 +505,8 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   p.kq_row = static_cast<int32_t>(ceil_div(ceil_div(P->n_out, P->sf_vec), 4));
   p.kq_col = static_cast<int32_t>(ceil_div(ceil_div(d.m_pad, P->sf_vec), 4));
   p.out_kind = d.out_format;
+  p.sf_atoms = d.in_format < BSGG_IN_NVFP4 ? 1 : P->sf_vec == 32 ? 2 : 4;
+  p.sf_v32 = P->sf_vec == 32 ? 1 : 0;
   p.want_col = d.want_col;
   p.gate_first = d.gate_first;
   p.tanh_s = d.tanh_clamp_s;
@@ -560,7 +571,10 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   }
   cudaError_t e;
   if (is_bwd_epi(d.epilogue)) {
-    if (d.in_format == BSGG_IN_NVFP4)
+    if (d.in_format > BSGG_IN_NVFP4)
+      e = P->pair ? bsgg::launch_f4e8_pair_bwd(L)
+          : P->bn == 256 ? bsgg::launch_f4e8_256_bwd(L) : bsgg::launch_f4e8_128_bwd(L);
+    else if (d.in_format == BSGG_IN_NVFP4)
       e = P->pair ? bsgg::launch_nvf4_pair_bwd(L)
           : P->mc ? bsgg::launch_nvf4_mc_bwd(L)
           : P->bn == 256 ? bsgg::launch_nvf4_256_bwd(L) : bsgg::launch_nvf4_128_bwd(L);
@@ -568,7 +582,10 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
       e = P->pair ? bsgg::launch_mxf8_pair_bwd(L)
           : P->mc ? bsgg::launch_mxf8_mc_bwd(L)
           : P->bn == 256 ? bsgg::launch_mxf8_256_bwd(L) : bsgg::launch_mxf8_128_bwd(L);
-  } else if (d.in_format == BSGG_IN_NVFP4)
+  } else if (d.in_format > BSGG_IN_NVFP4)
+    e = P->pair ? bsgg::launch_f4e8_pair(L)
+        : P->bn == 256 ? bsgg::launch_f4e8_256(L) : bsgg::launch_f4e8_128(L);
+  else if (d.in_format == BSGG_IN_NVFP4)
     e = P->pair ? bsgg::launch_nvf4_pair(L)
         : P->mc ? bsgg::launch_nvf4_mc(L)
         : P->bn == 256 ? bsgg::launch_nvf4_256(L) : bsgg::launch_nvf4_128(L);

@@ -34,6 +34,9 @@ cudaError_t launch_nvf4_128(const Launch& L);
 cudaError_t launch_nvf4_256(const Launch& L);
 cudaError_t launch_nvf4_pair(const Launch& L);
 cudaError_t launch_nvf4_mc(const Launch& L);
+cudaError_t launch_f4e8_128(const Launch& L);
+cudaError_t launch_f4e8_256(const Launch& L);
+cudaError_t launch_f4e8_pair(const Launch& L);
 // the same for the backward epilogues
 cudaError_t launch_mxf8_128_bwd(const Launch& L);
 cudaError_t launch_mxf8_256_bwd(const Launch& L);
@@ -43,6 +46,9 @@ cudaError_t launch_nvf4_128_bwd(const Launch& L);
 cudaError_t launch_nvf4_256_bwd(const Launch& L);
 cudaError_t launch_nvf4_pair_bwd(const Launch& L);
 cudaError_t launch_nvf4_mc_bwd(const Launch& L);
+cudaError_t launch_f4e8_128_bwd(const Launch& L);
+cudaError_t launch_f4e8_256_bwd(const Launch& L);
+cudaError_t launch_f4e8_pair_bwd(const Launch& L);
 // Largest number of CTAs of the pair (mc = false) or multicast-cluster kernel
 // that can be resident at once (clusters x 2) on the current device, 0 if unknown.
 int cluster_resident_ctas(bool fp4, bool mc);

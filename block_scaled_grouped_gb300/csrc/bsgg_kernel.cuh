@@ -60,6 +60,12 @@ namespace bsgg {
 // other two instances must not give up).
 enum : int { EPI_GATE = 0, EPI_SWIGLU = 1, EPI_SRELU = 2, EPI_DSWIGLU = 3, EPI_DSITUGLU = 4 };
 __host__ __device__ constexpr bool is_bwd_inst(int epi) { return epi == EPI_DSWIGLU || epi == EPI_DSITUGLU; }
+// Input class (template): MXFP8 (E4M3/E5M2 data, UE8M0 scales per 32), NVFP4
+// (E2M1 data, E4M3 scales per 16), or E2M1 data with UE8M0 scales, whose block
+// length (16 or 32) is a runtime choice (Params::sf_v32).  NVFP4 keeps its own
+// instances: the runtime choices cost it 2 % on GB300.
+enum : int { IC_MXF8 = 0, IC_NVF4 = 1, IC_F4E8 = 2 };
+__host__ __device__ constexpr bool ic_fp4(int ic) { return ic != IC_MXF8; }
 // Output class (template) and exact output kind (runtime) of D.
 enum : int { OUTC_FLOAT = 0, OUTC_FP8 = 1, OUTC_FP4 = 2 };
 enum : int { OK_BF16 = 0, OK_F16 = 1, OK_F32 = 2, OK_E4M3 = 3, OK_E5M2 = 4, OK_E2M1 = 5 };
@@ -114,6 +120,11 @@ struct Params {
   int32_t kq_row;           // SF atoms per 128 rows of SFD_row: ceil(ceil(n_out/v)/4)
   int32_t kq_col;           // SF atoms per 128 columns of SFD_col: ceil(ceil(m_pad/v)/4)
   int32_t out_kind;         // OK_*
+  // IC_F4E8 instances: scale atoms a stage loads (4: one scale per 16 values;
+  // 2: one per 32, each written into both 16-value slots it covers) and the
+  // block length of the input (and so of the quantized outputs)
+  int32_t sf_atoms;
+  int32_t sf_v32;           // 1: blocks of 32 values, 0: of 16
   int32_t want_col;
   int32_t gate_first;
   float tanh_s, tanh_rcp_s; // soft clamp s and 1/s (s = 0: off)
@@ -449,7 +460,7 @@ __device__ __forceinline__ void store_q32(void* dst, const float (&v)[32], const
 // Step 3 (or the 16/32-bit store) of one 32-column chunk of D of one row:
 // v[32] at D columns [col0, col0 + 32).  Row blocks of v columns lie inside the
 // chunk; column blocks of v rows span the warp's 32 lanes (its 32 rows).
-template <bool FP4, int OUTC>
+template <int IC, int OUTC>
 __device__ __forceinline__ void output_chunk(const Params& p, const float (&v)[32], int row, int col0,
                                              float norm, int lane, int kblk_col, float& amax_local) {
   if (OUTC == OUTC_FLOAT) {
@@ -465,22 +476,45 @@ __device__ __forceinline__ void output_chunk(const Params& p, const float (&v)[3
       store_h32(static_cast<uint16_t*>(p.d) + static_cast<int64_t>(row) * p.n_out + col0, &v[0], p.out_kind);
     }
   } else {
-    // ---- row blocks (v = 32 for UE8M0 scales, 16 for E4M3 scales)
-    constexpr int kV = FP4 ? 16 : 32;
+    // ---- row blocks in the input's scale type and block length: 32 with UE8M0
+    // scales for MXFP8; for FP4 two 16-value blocks with E4M3 or UE8M0 scales,
+    // which one scale per 32 values (MXFP4) joins into one block
+    constexpr bool FP4 = ic_fp4(IC);
+    constexpr bool e4m3_sf = IC == IC_NVF4;
+    const bool v32 = IC == IC_F4E8 && p.sf_v32;
     const int64_t row_bytes = (OUTC == OUTC_FP8) ? p.n_out : p.n_out / 2;
     const int64_t col_byte0 = (OUTC == OUTC_FP8) ? col0 : col0 / 2;
     float sc[32];
+    if (FP4) {
+      float am[2];
 #pragma unroll
-    for (int b = 0; b < 32 / kV; ++b) {
+      for (int b = 0; b < 2; ++b) {
+        am[b] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) am[b] = fmaxf(am[b], fabsf(v[b * 16 + i]));
+      }
+      if (v32) am[0] = am[1] = fmaxf(am[0], am[1]);
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        uint32_t code;
+        float s;
+        if (e4m3_sf) block_scale<true>(am[b], norm, p.rcp_qmax, code, s);
+        else block_scale<false>(am[b], norm, p.rcp_qmax, code, s);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sc[b * 16 + i] = s;
+        if (!v32) p.sfd_row[sf_off(row, col0 / 16 + b, p.kq_row)] = static_cast<uint8_t>(code);
+        else if (b == 0) p.sfd_row[sf_off(row, col0 / 32, p.kq_row)] = static_cast<uint8_t>(code);
+      }
+    } else {
       float am = 0.0f;
 #pragma unroll
-      for (int i = 0; i < kV; ++i) am = fmaxf(am, fabsf(v[b * kV + i]));
+      for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(v[i]));
       uint32_t code;
       float s;
-      block_scale<FP4>(am, norm, p.rcp_qmax, code, s);
+      block_scale<false>(am, norm, p.rcp_qmax, code, s);
 #pragma unroll
-      for (int i = 0; i < kV; ++i) sc[b * kV + i] = s;
-      p.sfd_row[sf_off(row, col0 / kV + b, p.kq_row)] = static_cast<uint8_t>(code);
+      for (int i = 0; i < 32; ++i) sc[i] = s;
+      p.sfd_row[sf_off(row, col0 / 32, p.kq_row)] = static_cast<uint8_t>(code);
     }
     store_q32<OUTC>(static_cast<uint8_t*>(p.d) + row * row_bytes + col_byte0, v, sc, p.out_kind);
     // ---- column blocks of v rows: the warp's 32 lanes are its 32 rows
@@ -502,7 +536,8 @@ __device__ __forceinline__ void output_chunk(const Params& p, const float (&v)[3
         store_q32<OUTC>(static_cast<uint8_t*>(p.d_col) + row * row_bytes + col_byte0, v, sc, p.out_kind);
         p.sfd_col[sf_off(col0 + lane, kblk_col, p.kq_col)] = static_cast<uint8_t>(my_code);
       } else {
-        // v = 16: each half-warp is one block.  Butterfly maxima inside the
+        // FP4: each half-warp is one 16-row block (the whole warp one 32-row
+        // block with one scale per 32 values).  Butterfly maxima inside the
         // half-warp; lane (16h + i) owns columns i and i + 16 of half h.
         const int h = lane >> 4, i = lane & 15;
         float am_lo = 0.0f, am_hi = 0.0f;
@@ -514,17 +549,28 @@ __device__ __forceinline__ void output_chunk(const Params& p, const float (&v)[3
           if (j < 16) am_lo = (i == j) ? m : am_lo;
           else am_hi = (i == j - 16) ? m : am_hi;
         }
+        if (v32) {
+          am_lo = fmaxf(am_lo, __shfl_xor_sync(0xffffffffu, am_lo, 16));
+          am_hi = fmaxf(am_hi, __shfl_xor_sync(0xffffffffu, am_hi, 16));
+        }
         uint32_t code_lo, code_hi;
         float sc_lo, sc_hi;
-        block_scale<true>(am_lo, norm, p.rcp_qmax, code_lo, sc_lo);
-        block_scale<true>(am_hi, norm, p.rcp_qmax, code_hi, sc_hi);
+        if (e4m3_sf) {
+          block_scale<true>(am_lo, norm, p.rcp_qmax, code_lo, sc_lo);
+          block_scale<true>(am_hi, norm, p.rcp_qmax, code_hi, sc_hi);
+        } else {
+          block_scale<false>(am_lo, norm, p.rcp_qmax, code_lo, sc_lo);
+          block_scale<false>(am_hi, norm, p.rcp_qmax, code_hi, sc_hi);
+        }
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           sc[j] = __shfl_sync(0xffffffffu, j < 16 ? sc_lo : sc_hi, 16 * h + (j & 15));
         store_q32<OUTC>(static_cast<uint8_t*>(p.d_col) + row * row_bytes + col_byte0, v, sc, p.out_kind);
-        const int kb = 2 * kblk_col + h;     // 16-row block index
-        p.sfd_col[sf_off(col0 + i, kb, p.kq_col)] = static_cast<uint8_t>(code_lo);
-        p.sfd_col[sf_off(col0 + i + 16, kb, p.kq_col)] = static_cast<uint8_t>(code_hi);
+        if (!v32 || h == 0) {
+          const int kb = v32 ? kblk_col : 2 * kblk_col + h;   // row-block index
+          p.sfd_col[sf_off(col0 + i, kb, p.kq_col)] = static_cast<uint8_t>(code_lo);
+          p.sfd_col[sf_off(col0 + i + 16, kb, p.kq_col)] = static_cast<uint8_t>(code_hi);
+        }
       }
     }
   }
@@ -634,7 +680,7 @@ __device__ __forceinline__ void rht_col_chunk(const Params& p, const float (&v)[
 // Step 2 and Step 3 for one 32-column chunk of one row: C = al * xs (the
 // input half for the GLUs; fp32 bits), al * gs the gate half.  al is alpha_g,
 // or 1 where alpha and the bias were already applied in place.
-template <bool FP4, int EPI, int OUTC, bool XC>
+template <int IC, int EPI, int OUTC, bool XC>
 __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* xs, const uint32_t* gs, int row,
                                                int col0, float al, float pr, float norm, int lane, int kblk_col,
                                                float& amax_local, int64_t seg_start, int seg_rows) {
@@ -666,7 +712,7 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* 
       if (p.glu_gamma != 1.0f) v[i] *= p.glu_gamma;
     }
   }
-  output_chunk<FP4, OUTC>(p, v, row, col0, norm, lane, kblk_col, amax_local);
+  output_chunk<IC, OUTC>(p, v, row, col0, norm, lane, kblk_col, amax_local);
   if (XC && p.rht != nullptr) {
     if (p.rht_colwise) rht_col_chunk(p, v, row, col0, lane, seg_start, seg_rows, *p.rht_norm_const);
     else rht_chunk(p, v, row, col0, *p.rht_norm_const);
@@ -676,11 +722,13 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* 
 // XC: a forward launch adds a bias to C, stores C or writes the Hadamard
 // output; a backward launch accumulates dbias (separate instances, so that the
 // register budget of the plain epilogue is untouched).
-template <bool FP4, int BN, int CM, int EPI, int OUTC, bool XC>
-__global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
+template <int IC, int BN, int CM, int EPI, int OUTC, bool XC>
+__global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThreads, 1)
     bsgg_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                 const __grid_constant__ Params p) {
+  constexpr bool FP4 = ic_fp4(IC);
+  static_assert(IC != IC_F4E8 || CM != CM_MC, "UE8M0-scaled FP4 needs the scale stores");
   constexpr bool PAIR = CM == CM_PAIR;
   constexpr bool MC = CM == CM_MC;
   constexpr bool CLUSTER = CM != CM_SINGLE;
@@ -824,7 +872,10 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
           for (int ks = 0; ks < p.num_k_stages; ++ks) {
             if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit_ns)) { ok = false; break; }
             const uint32_t fb = full_bar(stage);
-            const int k0 = ks * kBKBytes, ka = 2 * ks * Ly::kAtoms;
+            // scale atoms this stage loads (FP4 with one scale per 32 values: half)
+            const int atoms_ld = IC == IC_F4E8 ? p.sf_atoms : Ly::kAtoms;
+            const uint32_t sf_tx = static_cast<uint32_t>(atoms_ld * 512 * (1 + Ly::kHalves));
+            const int k0 = ks * kBKBytes, ka = 2 * ks * atoms_ld;
             const uint32_t sA = sbase + Ly::kOffA + stage * Ly::kABytes;
             const uint32_t sB = sbase + Ly::kOffB + stage * Ly::kBBytes;
             const uint32_t sSa = sbase + Ly::kOffSfa + stage * Ly::kSfaBytes;
@@ -835,7 +886,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
               const uint32_t fbl = mapa_shared(fb, 0);
               const uint32_t sfb_own = sfull_bar(stage);
               if (leader) mbar_expect_tx(fb, 2u * (Ly::kABytes + Ly::kBBytes));
-              mbar_expect_tx(sfb_own, Ly::kSfaBytes + Ly::kSfbBytes);
+              mbar_expect_tx(sfb_own, sf_tx);
               tma_load_2d_pair(sA, &tmA, fbl, k0, mt * kBM);
               tma_load_3d_pair(sB, mB, fbl, k0, b_row, bz);
               tma_load_3d(sSa, &tmSFA, sfb_own, 0, ka, mt);
@@ -866,7 +917,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
               tma_load_3d(sSa, &tmSFA, fb, 0, ka, mt);
               tma_load_3d(sSb, mSFB, fb, 0, ka, sfb_rb);
             } else {
-              mbar_expect_tx(fb, Ly::kStageBytes);
+              mbar_expect_tx(fb, Ly::kABytes + Ly::kBBytes + sf_tx);
               tma_load_2d(sA, &tmA, fb, k0, mt * kBM);
               tma_load_3d(sB, mB, fb, k0, b_row, bz);
               tma_load_3d(sSa, &tmSFA, fb, 0, ka, mt);
@@ -1001,14 +1052,35 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
             const uint32_t slot = sf_tmem0 + stage * Ly::kSfColsPerStage;
             const uint8_t* sa = smem + Ly::kOffSfa + stage * Ly::kSfaBytes + 16 * lane;
             const uint8_t* sb = smem + Ly::kOffSfb + stage * Ly::kSfbBytes + 16 * lane;
+            if (IC != IC_F4E8 || p.sf_atoms == Ly::kAtoms) {
 #pragma unroll
-            for (int i = 0; i < Ly::kAtoms; ++i) {
-              const uint4 va = *reinterpret_cast<const uint4*>(sa + 512 * i);
-              tmem_st_x1(slot + 4 * i + q, q == 0 ? va.x : q == 1 ? va.y : q == 2 ? va.z : va.w);
+              for (int i = 0; i < Ly::kAtoms; ++i) {
+                const uint4 va = *reinterpret_cast<const uint4*>(sa + 512 * i);
+                tmem_st_x1(slot + 4 * i + q, q == 0 ? va.x : q == 1 ? va.y : q == 2 ? va.z : va.w);
 #pragma unroll
-              for (int h = 0; h < Ly::kHalves; ++h)
-                tmem_st_x4(slot + Ly::kSfaCols + 4 * (i * Ly::kHalves + h),
-                           *reinterpret_cast<const uint4*>(sb + 512 * (h * Ly::kAtoms + i)));
+                for (int h = 0; h < Ly::kHalves; ++h)
+                  tmem_st_x4(slot + Ly::kSfaCols + 4 * (i * Ly::kHalves + h),
+                             *reinterpret_cast<const uint4*>(sb + 512 * (h * Ly::kAtoms + i)));
+              }
+            } else {
+              // one scale per 32 values: a loaded word [s0 s1 s2 s3] covers two
+              // MMAs; the MMA's 16-value slots get [s0 s0 s1 s1] and [s2 s2 s3 s3]
+              // (the same products as one scale per 32 values)
+              constexpr int kSrc = Ly::kAtoms / 2;
+#pragma unroll
+              for (int i = 0; i < Ly::kAtoms; ++i) {
+                const uint32_t sel = (i & 1) ? 0x3322u : 0x1100u;
+                const uint4 va = *reinterpret_cast<const uint4*>(sa + 512 * (i / 2));
+                const uint32_t wa = q == 0 ? va.x : q == 1 ? va.y : q == 2 ? va.z : va.w;
+                tmem_st_x1(slot + 4 * i + q, __byte_perm(wa, 0u, sel));
+#pragma unroll
+                for (int h = 0; h < Ly::kHalves; ++h) {
+                  const uint4 vb = *reinterpret_cast<const uint4*>(sb + 512 * (h * kSrc + i / 2));
+                  tmem_st_x4(slot + Ly::kSfaCols + 4 * (i * Ly::kHalves + h),
+                             make_uint4(__byte_perm(vb.x, 0u, sel), __byte_perm(vb.y, 0u, sel),
+                                        __byte_perm(vb.z, 0u, sel), __byte_perm(vb.w, 0u, sel)));
+                }
+              }
             }
             tmem_wait_st();
             tc_fence_before();
@@ -1223,8 +1295,8 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
               gv[i] = ref * pr * uo * sg * (1.0f + p.geglu_a * gc * (1.0f - sg)) * gate_mask;      // d gate
             }
           }
-          output_chunk<FP4, OUTC>(p, x, row, xo, norm, lane, kblk_col, amax_local);
-          output_chunk<FP4, OUTC>(p, gv, row, go, norm, lane, kblk_col, amax_local2);
+          output_chunk<IC, OUTC>(p, x, row, xo, norm, lane, kblk_col, amax_local);
+          output_chunk<IC, OUTC>(p, gv, row, go, norm, lane, kblk_col, amax_local2);
           if (XC && p.dbias != nullptr) {
             float* db = p.dbias + static_cast<int64_t>(g) * p.n_out;
             add_column_sums32(x, db + xo, lane);
@@ -1244,7 +1316,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
             xs[i] = gf ? r[64 * j + 32 + i] : r[64 * j + i];
             gs[i] = gf ? r[64 * j + i] : r[64 * j + 32 + i];
           }
-          epilogue_chunk<FP4, EPI, OUTC, XC>(p, xs, gs, row, col0, al_epi, pr, norm, lane, kblk_col, amax_local,
+          epilogue_chunk<IC, EPI, OUTC, XC>(p, xs, gs, row, col0, al_epi, pr, norm, lane, kblk_col, amax_local,
                                              seg_start, seg_rows);
         }
       } else {
@@ -1252,7 +1324,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<FP4, CM>()>::kThreads, 1)
         for (int c = 0; c < kWarpCols / 32; ++c) {
           const int col0 = nt * BN + e * kWarpCols + 32 * c;
           if (col0 >= p.n_out) continue;
-          epilogue_chunk<FP4, EPI, OUTC, XC>(p, &r[32 * c], &r[32 * c], row, col0, al_epi, pr, norm, lane,
+          epilogue_chunk<IC, EPI, OUTC, XC>(p, &r[32 * c], &r[32 * c], row, col0, al_epi, pr, norm, lane,
                                              kblk_col, amax_local, seg_start, seg_rows);
         }
       }

@@ -7,9 +7,10 @@
 
 namespace bsgg {
 
-template <bool FP4, int BN, int CM, int EPI, int OUTC, bool XC>
+template <int IC, int BN, int CM, int EPI, int OUTC, bool XC>
 cudaError_t launch_one(const Launch& L) {
-  auto kern = bsgg_kernel<FP4, BN, CM, EPI, OUTC, XC>;
+  auto kern = bsgg_kernel<IC, BN, CM, EPI, OUTC, XC>;
+  constexpr bool FP4 = ic_fp4(IC);
   constexpr bool kCluster = CM != CM_SINGLE;
   constexpr bool kStores = scale_stores<FP4, CM>();
   using Ro = Roles<kStores>;
@@ -52,49 +53,53 @@ cudaError_t launch_one(const Launch& L) {
   return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmSFA, L.tmSFB, L.p);
 }
 
-template <bool FP4, int BN, int CM, int EPI, bool XC>
+template <int IC, int BN, int CM, int EPI, bool XC>
 cudaError_t launch_outc(const Launch& L) {
   switch (L.outc) {
-    case OUTC_FLOAT: return launch_one<FP4, BN, CM, EPI, OUTC_FLOAT, XC>(L);
-    case OUTC_FP8: return launch_one<FP4, BN, CM, EPI, OUTC_FP8, XC>(L);
-    case OUTC_FP4: return launch_one<FP4, BN, CM, EPI, OUTC_FP4, XC>(L);
+    case OUTC_FLOAT: return launch_one<IC, BN, CM, EPI, OUTC_FLOAT, XC>(L);
+    case OUTC_FP8:
+      // FP8 outputs come from MXFP8 inputs only (the host refuses them for FP4)
+      if constexpr (ic_fp4(IC)) return cudaErrorInvalidValue;
+      else return launch_one<IC, BN, CM, EPI, OUTC_FP8, XC>(L);
+    case OUTC_FP4: return launch_one<IC, BN, CM, EPI, OUTC_FP4, XC>(L);
   }
   return cudaErrorInvalidValue;
 }
 
 // The XC instances: forward launches with a bias, a stored C or the Hadamard
 // output; backward launches with dbias.
-template <bool FP4, int BN, int CM, int EPI>
+template <int IC, int BN, int CM, int EPI>
 cudaError_t launch_xc(const Launch& L) {
   const bool xc = is_bwd_inst(EPI) ? L.p.dbias != nullptr
                                    : (L.p.bias != nullptr || L.p.c_out != nullptr || L.p.rht != nullptr);
-  return xc ? launch_outc<FP4, BN, CM, EPI, true>(L) : launch_outc<FP4, BN, CM, EPI, false>(L);
+  return xc ? launch_outc<IC, BN, CM, EPI, true>(L) : launch_outc<IC, BN, CM, EPI, false>(L);
 }
 
 // Forward epilogues (one translation unit per input family and tile shape) and
 // backward epilogues (another), so that the instances compile in parallel.
-template <bool FP4, int BN, int CM>
+template <int IC, int BN, int CM>
 cudaError_t launch_shape_fwd(const Launch& L) {
   switch (L.epi) {
-    case EPI_GATE: return launch_xc<FP4, BN, CM, EPI_GATE>(L);
-    case EPI_SWIGLU: return launch_xc<FP4, BN, CM, EPI_SWIGLU>(L);
-    case EPI_SRELU: return launch_xc<FP4, BN, CM, EPI_SRELU>(L);
+    case EPI_GATE: return launch_xc<IC, BN, CM, EPI_GATE>(L);
+    case EPI_SWIGLU: return launch_xc<IC, BN, CM, EPI_SWIGLU>(L);
+    case EPI_SRELU: return launch_xc<IC, BN, CM, EPI_SRELU>(L);
   }
   return cudaErrorInvalidValue;
 }
-template <bool FP4, int BN, int CM>
+template <int IC, int BN, int CM>
 cudaError_t launch_shape_bwd(const Launch& L) {
   switch (L.epi) {
-    case EPI_DSWIGLU: return launch_xc<FP4, BN, CM, EPI_DSWIGLU>(L);
-    case EPI_DSITUGLU: return launch_xc<FP4, BN, CM, EPI_DSITUGLU>(L);
+    case EPI_DSWIGLU: return launch_xc<IC, BN, CM, EPI_DSWIGLU>(L);
+    case EPI_DSITUGLU: return launch_xc<IC, BN, CM, EPI_DSITUGLU>(L);
   }
   return cudaErrorInvalidValue;
 }
 
 // Clusters of two of this kernel that fit on the device at once, x 2.
-template <bool FP4, int CM>
+template <int IC, int CM>
 int cluster_resident_ctas_impl() {
-  auto kern = bsgg_kernel<FP4, 256, CM, EPI_GATE, OUTC_FLOAT, false>;
+  constexpr bool FP4 = ic_fp4(IC);
+  auto kern = bsgg_kernel<IC, 256, CM, EPI_GATE, OUTC_FLOAT, false>;
   const int smem = Layout<FP4, 256, CM == CM_PAIR>::kSmemBytes;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};

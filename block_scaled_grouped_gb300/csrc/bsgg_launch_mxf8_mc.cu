@@ -3,5 +3,5 @@
 #include "bsgg_launch.cuh"
 
 namespace bsgg {
-cudaError_t launch_mxf8_mc(const Launch& L) { return launch_shape_fwd<false, 256, CM_MC>(L); }
+cudaError_t launch_mxf8_mc(const Launch& L) { return launch_shape_fwd<IC_MXF8, 256, CM_MC>(L); }
 }  // namespace bsgg

@@ -3,5 +3,5 @@
 #include "bsgg_launch.cuh"
 
 namespace bsgg {
-cudaError_t launch_mxf8_mc_bwd(const Launch& L) { return launch_shape_bwd<false, 256, CM_MC>(L); }
+cudaError_t launch_mxf8_mc_bwd(const Launch& L) { return launch_shape_bwd<IC_MXF8, 256, CM_MC>(L); }
 }  // namespace bsgg

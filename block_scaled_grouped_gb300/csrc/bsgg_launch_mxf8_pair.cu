@@ -2,5 +2,5 @@
 #include "bsgg_launch.cuh"
 
 namespace bsgg {
-cudaError_t launch_mxf8_pair(const Launch& L) { return launch_shape_fwd<false, 256, CM_PAIR>(L); }
+cudaError_t launch_mxf8_pair(const Launch& L) { return launch_shape_fwd<IC_MXF8, 256, CM_PAIR>(L); }
 }  // namespace bsgg

@@ -2,5 +2,5 @@
 #include "bsgg_launch.cuh"
 
 namespace bsgg {
-cudaError_t launch_nvf4_128(const Launch& L) { return launch_shape_fwd<true, 128, CM_SINGLE>(L); }
+cudaError_t launch_nvf4_128(const Launch& L) { return launch_shape_fwd<IC_NVF4, 128, CM_SINGLE>(L); }
 }  // namespace bsgg

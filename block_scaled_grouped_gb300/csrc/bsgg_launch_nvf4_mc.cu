@@ -3,5 +3,5 @@
 #include "bsgg_launch.cuh"
 
 namespace bsgg {
-cudaError_t launch_nvf4_mc(const Launch& L) { return launch_shape_fwd<true, 256, CM_MC>(L); }
+cudaError_t launch_nvf4_mc(const Launch& L) { return launch_shape_fwd<IC_NVF4, 256, CM_MC>(L); }
 }  // namespace bsgg

@@ -2,9 +2,9 @@
 #include "bsgg_launch.cuh"
 
 namespace bsgg {
-cudaError_t launch_nvf4_pair(const Launch& L) { return launch_shape_fwd<true, 256, CM_PAIR>(L); }
+cudaError_t launch_nvf4_pair(const Launch& L) { return launch_shape_fwd<IC_NVF4, 256, CM_PAIR>(L); }
 int cluster_resident_ctas(bool fp4, bool mc) {
-  if (mc) return fp4 ? cluster_resident_ctas_impl<true, CM_MC>() : cluster_resident_ctas_impl<false, CM_MC>();
-  return fp4 ? cluster_resident_ctas_impl<true, CM_PAIR>() : cluster_resident_ctas_impl<false, CM_PAIR>();
+  if (mc) return fp4 ? cluster_resident_ctas_impl<IC_NVF4, CM_MC>() : cluster_resident_ctas_impl<IC_MXF8, CM_MC>();
+  return fp4 ? cluster_resident_ctas_impl<IC_NVF4, CM_PAIR>() : cluster_resident_ctas_impl<IC_MXF8, CM_PAIR>();
 }
 }  // namespace bsgg

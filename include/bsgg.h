@@ -87,7 +87,11 @@ typedef enum {
 typedef enum {
   BSGG_IN_MXFP8_E4M3 = 0,  /* float8_e4m3fn data, float8_e8m0fnu scales, v = 32 */
   BSGG_IN_MXFP8_E5M2 = 1,  /* float8_e5m2 data,   float8_e8m0fnu scales, v = 32 */
-  BSGG_IN_NVFP4 = 2        /* float4_e2m1fn_x2 data, float8_e4m3fn scales, v = 16 */
+  BSGG_IN_NVFP4 = 2,       /* float4_e2m1fn_x2 data, float8_e4m3fn scales, v = 16 */
+  BSGG_IN_FP4_UE8M0_16 = 3,/* float4_e2m1fn_x2 data, float8_e8m0fnu scales, v = 16 */
+  BSGG_IN_MXFP4 = 4        /* float4_e2m1fn_x2 data, float8_e8m0fnu scales, v = 32 */
+  /* The two UE8M0-scaled FP4 formats run on single CTAs and CTA pairs; the (2, 1)
+     multicast clusters of 128 x 256 tiles return BSGG_ERR_UNSUPPORTED for them. */
 } bsgg_in_format;
 
 /* Output formats of D (and D_col). */

@@ -119,6 +119,11 @@ def _create(**over):
     (dict(n=128, epilogue="swiglu", rht_format="e2m1", rht_colwise=True), 1),   # N_out % 128
     (dict(epilogue="dsituglu", situ_betas=(1.0, float("inf"))), 1),
     (dict(epilogue="dswiglu", situ_betas=(2.0, 2.0)), 1),          # dSiTU-GLU's own
+    # UE8M0-scaled FP4: no multicast-cluster instances; no FP8 outputs from FP4
+    (dict(in_format="mxfp4", tile_m=128, tile_n=256, cluster_m=2, cluster_n=1), 2),
+    (dict(in_format="fp4_ue8m0_16", tile_m=128, tile_n=256, cluster_m=2, cluster_n=1), 2),
+    (dict(in_format="mxfp4", out_format="e5m2"), 2),
+    (dict(in_format="mxfp4", k=48), 1),                           # K % 32 for packed FP4
 ])
 def test_create_rejects(lib, over, code):
     assert _create(**over) == code
@@ -134,6 +139,9 @@ def test_create_rejects(lib, over, code):
     dict(epilogue="swiglu", rht_format="e2m1", in_format="nvfp4", out_format="e2m1"),
     dict(epilogue="dgeglu", dgeglu_params=(1.0, -10.0, 10.0, 0.0)),
     dict(epilogue="dsituglu", situ_betas=(2.0, 0.5)),
+    dict(in_format="mxfp4", epilogue="srelu", out_format="e2m1", want_col=1, tile_m=256, tile_n=256,
+         cluster_m=2, cluster_n=1),
+    dict(in_format="fp4_ue8m0_16", epilogue="dswiglu", out_format="bf16"),
 ])
 def test_create_accepts_epilogue_options(lib, over):
     # validation passes: 0 with a GPU, else the device query that follows

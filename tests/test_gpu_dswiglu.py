@@ -89,6 +89,15 @@ def test_dswiglu_nvfp4_e2m1_and_bf16(tile):
     _check(p, outs, dprob)
 
 
+@pytest.mark.parametrize("in_fmt", ["fp4_ue8m0_16", "mxfp4"])
+@pytest.mark.parametrize("tile", [(0, 0), (256, 256, 2, 1)], ids=tile_id)
+def test_dswiglu_fp4_with_ue8m0_scales(tile, in_fmt):
+    p = small_problem(counts=(150, 0, 300), k=544, n=256, pad_to=128, in_fmt=in_fmt, epi="dswiglu",
+                      out_fmt="e2m1", want_col=True, seed=75)
+    plan, outs, dprob = _run(p, tile)
+    _check(p, outs, dprob)
+
+
 def test_dprob_accumulates_and_zero_prob_rows_still_get_it():
     p = small_problem(counts=(128, 100), k=256, n=128, pad_to=128, epi="dswiglu", out_fmt="bf16", seed=75)
     p.prob[:64] = 0.0                        # routing weight 0: D rows 0, dprob not
