@@ -31,7 +31,7 @@ from typing import List, Optional, Sequence
 import numpy as np
 import torch
 
-IN_FORMATS = ("mxfp8_e4m3", "mxfp8_e5m2", "nvfp4", "fp4_ue8m0_16", "mxfp4")
+IN_FORMATS = ("mxfp8_e4m3", "mxfp8_e5m2", "nvfp4", "fp4_ue8m0_16", "mxfp4", "bf16")
 FP4_FORMATS = ("nvfp4", "fp4_ue8m0_16", "mxfp4")
 OUT_FORMATS = ("bf16", "f16", "f32", "e4m3", "e5m2", "e2m1")
 EPILOGUES = ("gate", "swiglu", "srelu", "geglu", "dswiglu", "dgeglu", "dsituglu")
@@ -58,10 +58,10 @@ class Problem:
     padded_offsets: torch.Tensor  # int32 (L,)
     alpha: torch.Tensor         # float32 (L,)
     prob: torch.Tensor          # float32 (m_pad,)
-    a: torch.Tensor             # uint8 (m_pad, k or k/2)
-    sfa_rows: torch.Tensor      # uint8 (1, m_pad, k/v) scale codes, row-major
-    b: torch.Tensor             # uint8 (L, n, k or k/2)
-    sfb_rows: torch.Tensor      # uint8 (L, n, k/v) scale codes, row-major
+    a: torch.Tensor             # uint8 (m_pad, k or k/2; bf16: 2k bytes, little-endian values)
+    sfa_rows: torch.Tensor      # uint8 (1, m_pad, k/v) scale codes, row-major (bf16: 0 columns)
+    b: torch.Tensor             # uint8 (L, n, k or k/2 or 2k)
+    sfb_rows: torch.Tensor      # uint8 (L, n, k/v) scale codes, row-major (bf16: 0 columns)
     # the backward epilogues' extra inputs (None otherwise): the saved forward
     # pre-activation C (m_pad, 2n) bf16 and its per-group scale beta (L,)
     saved_c: Optional[torch.Tensor] = None
@@ -204,7 +204,17 @@ def quantize_fp4_ue8m0(x: torch.Tensor, v: int):
     return packed, (e + 127).to(torch.uint8)
 
 
+def as_bf16_bytes(x: torch.Tensor):
+    """float32 (R, K) -> (bytes uint8 (R, 2K) of its round-to-nearest-even bfloat16
+    values, little-endian; no scale codes: uint8 (R, 0))."""
+    R, K = x.shape
+    q = x.to(torch.bfloat16).contiguous().view(torch.uint8).reshape(R, 2 * K)
+    return q, torch.empty(R, 0, dtype=torch.uint8, device=x.device)
+
+
 def quantize(x: torch.Tensor, in_fmt: str):
+    if in_fmt == "bf16":
+        return as_bf16_bytes(x)
     if in_fmt == "nvfp4":
         return quantize_nvfp4(x)
     if in_fmt == "fp4_ue8m0_16":
@@ -312,8 +322,8 @@ def build_problem(*, name: str, counts: Sequence[int], k: int, n: int, in_fmt: s
         row_prob = [rng.uniform(0.0, 1.0, size=int(c)).astype(np.float32) for c in counts]
 
     v = 16 if in_fmt in ("nvfp4", "fp4_ue8m0_16") else 32
-    kbytes = k // 2 if in_fmt in FP4_FORMATS else k
-    kblocks = -(-k // v)
+    kbytes = k // 2 if in_fmt in FP4_FORMATS else 2 * k if in_fmt == "bf16" else k
+    kblocks = 0 if in_fmt == "bf16" else -(-k // v)
     prob = np.zeros(m_pad, dtype=np.float32)
     a = torch.zeros(m_pad, kbytes, dtype=torch.uint8, device=device)
     one_code = 0x38 if in_fmt == "nvfp4" else 127
@@ -360,7 +370,7 @@ def build_problem(*, name: str, counts: Sequence[int], k: int, n: int, in_fmt: s
 
     # backward epilogues: the saved forward C, N(0, 2) rounded to bf16 (a
     # pre-activation's typical spread), and beta ~ U(0.5, 2) per group (read
-    # by dSwiGLU only)
+    # by dSwiGLU, and by dGeGLU on bf16 inputs)
     saved_c = beta = None
     if epi in BWD_EPILOGUES:
         beta = torch.as_tensor(rng.uniform(0.5, 2.0, size=L).astype(np.float32), device=device)

@@ -27,7 +27,7 @@ _lib = None
 
 # Format codes of the oracle (its own numbering, see bsgg_oracle.cpp).
 F_E4M3, F_E5M2, F_E2M1, F_UE8M0 = 0, 1, 2, 3
-IN_MXFP8_E4M3, IN_MXFP8_E5M2, IN_NVFP4, IN_FP4_UE8M0_16, IN_MXFP4 = 0, 1, 2, 3, 4
+IN_MXFP8_E4M3, IN_MXFP8_E5M2, IN_NVFP4, IN_FP4_UE8M0_16, IN_MXFP4, IN_BF16 = 0, 1, 2, 3, 4, 5
 OUT_BF16, OUT_F16, OUT_F32, OUT_E4M3, OUT_E5M2, OUT_E2M1 = 0, 1, 2, 3, 4, 5
 EPI_GATE, EPI_SWIGLU, EPI_SRELU, EPI_GEGLU, EPI_DSWIGLU, EPI_DGEGLU, EPI_DSITUGLU = 0, 1, 2, 3, 4, 5, 6
 BWD_EPIS = (EPI_DSWIGLU, EPI_DGEGLU, EPI_DSITUGLU)
@@ -167,7 +167,9 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     """Run the oracle on the listed 32-row blocks (default: all of them).
 
     Inputs are numpy arrays in the device layouts: ``a`` (m_pad, k or k/2)
-    uint8 codes, ``b`` (L, n, k or k/2), ``sfa``/``sfb`` swizzled flat uint8,
+    uint8 codes (``IN_BF16``: (m_pad, 2k) bytes of little-endian bfloat16
+    values, and no scales: ``sfa``/``sfb`` may be empty), ``b`` (L, n, k or
+    k/2, or 2k), ``sfa``/``sfb`` swizzled flat uint8,
     ``padded_offsets`` int32 (L,), ``alpha`` float32 (L,), ``prob`` float32
     (m_pad,).  Returns a dict with ``d_ref`` (fp64, rows of the listed blocks),
     ``amax`` and, for quantized outputs, full-size ``d``, ``d_col``,
@@ -179,7 +181,8 @@ def run(*, m_pad, n, k, num_groups, in_fmt, out_fmt, epi, a, sfa, b, sfb, padded
     forward C (any float dtype, widened to fp64) and ``beta`` float32 (L,), and
     adds ``dprob_ref`` (fp64, rows of the listed blocks); its ``amax`` has 2L
     entries (input-gradient and gate-gradient blocks of each group).  The dGeGLU
-    backward (``epi=EPI_DGEGLU``) takes the saved C unscaled and
+    backward (``epi=EPI_DGEGLU``) takes the saved C unscaled (scaled by
+    ``beta`` with ``IN_BF16``: the BF16 contract's X = beta C) and
     ``geglu_alpha``, ``glu_clamp_min``/``glu_clamp_max`` and ``linear_offset``
     (the page's defaults 1.702, -7, 7, 1); the dSiTU-GLU backward
     (``epi=EPI_DSITUGLU``) takes the saved C unscaled and ``situ_beta1``,

@@ -17,8 +17,8 @@
 // is "parity unpinned".  The one unpinned quantity is the *rate* of one-code
 // flips caused by the device's approximate tanh; the tolerance covers it.
 //
-// Readings where the pages are silent are listed in the design doc; the ones this
-// file implements are marked "reading:" below.
+// Where the pages are silent this file takes a reading of them, marked
+// "reading:" where it is implemented.
 
 #include <algorithm>
 #include <atomic>
@@ -161,7 +161,9 @@ int64_t sf_bytes(int64_t rows, int64_t kblocks, int64_t L) {
 // ---------------------------------------------------------------------------
 // "Grouped GEMM + Quant (SM100)", Data Types: FP4 data takes E4M3 scales per 16
 // (NVFP4) or UE8M0 scales per 16 or 32 (E4M3 is incompatible with 32).
-enum InFmt { IN_MXFP8_E4M3 = 0, IN_MXFP8_E5M2 = 1, IN_NVFP4 = 2, IN_FP4_UE8M0_16 = 3, IN_MXFP4 = 4 };
+// IN_BF16: the BF16 backend of "Grouped GEMM + dGLU (SM100)" (BF16 contract):
+// bfloat16 A and B, no scale factors.
+enum InFmt { IN_MXFP8_E4M3 = 0, IN_MXFP8_E5M2 = 1, IN_NVFP4 = 2, IN_FP4_UE8M0_16 = 3, IN_MXFP4 = 4, IN_BF16 = 5 };
 enum OutFmt { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2, OUT_E4M3 = 3, OUT_E5M2 = 4, OUT_E2M1 = 5 };
 // EPI_DSWIGLU, EPI_DGEGLU, EPI_DSITUGLU: the backward epilogues of "Grouped GEMM +
 // dGLU (SM100)".
@@ -345,6 +347,21 @@ bool is_bwd(const orc_desc* P) {
 // backward (two gradient blocks per GEMM block), else N.
 int64_t n_out(const orc_desc* P) { return is_glu(P) ? P->n / 2 : is_bwd(P) ? 2 * P->n : P->n; }
 
+// A bfloat16 value is the upper half of the binary32 value with the same bits;
+// its two bytes are stored little-endian.
+double bf16_value(const uint8_t* two_bytes) {
+  const uint32_t bits = (uint32_t(two_bytes[0]) | (uint32_t(two_bytes[1]) << 8)) << 16;
+  float f;
+  std::memcpy(&f, &bits, 4);
+  return double(f);
+}
+
+// Bytes of one K-major operand row: one per FP8 value, half for FP4, two per
+// bfloat16 value.
+int64_t row_bytes(const orc_desc* P) {
+  return P->in_fmt == IN_BF16 ? 2 * P->k : is_fp4_in(P) ? P->k / 2 : P->k;
+}
+
 // Element (r, k) of a K-major low-precision operand: one byte per FP8 value,
 // two FP4 values per byte with element 2i in the low nibble (reading).
 uint32_t element_code(const orc_desc* P, const uint8_t* base, int64_t row, int64_t k) {
@@ -355,9 +372,14 @@ uint32_t element_code(const orc_desc* P, const uint8_t* base, int64_t row, int64
   return base[row * P->k + k];
 }
 
-// Dequantized operand row: value(code) * value(scale of its k-block).
+// Dequantized operand row: value(code) * value(scale of its k-block); a
+// bfloat16 row is its values (no scales on the BF16 backend).
 void dequant_row(const orc_desc* P, const uint8_t* data, const uint8_t* sf, int64_t row,
                  int64_t rows, int64_t l, double* out) {
+  if (P->in_fmt == IN_BF16) {
+    for (int64_t k = 0; k < P->k; ++k) out[k] = bf16_value(data + row * 2 * P->k + 2 * k);
+    return;
+  }
   const int64_t v = sf_vec(P), kblocks = (P->k + v - 1) / v;
   for (int64_t k = 0; k < P->k; ++k) {
     double s = decode(sf_fmt(P), sf[sf_offset(row, k / v, l, rows, kblocks)]);
@@ -401,7 +423,7 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
   const int64_t m0 = J.blocks[bi] * 32;
   const int64_t v = sf_vec(P);
   const int64_t w = j1 - j0;
-  const int64_t b_group_bytes = P->n * (is_fp4_in(P) ? K / 2 : K);
+  const int64_t b_group_bytes = P->n * row_bytes(P);
 
   // C columns needed for D column j; `gate` picks the gate half for SwiGLU.
   auto c_col_of = [&](int64_t j, bool gate) -> int64_t {
@@ -472,12 +494,14 @@ void run_item(Job& J, int64_t bi, int64_t j0, int64_t j1) {
     // Backward ("Grouped GEMM + dGLU (SM100)", Block-scaled contract, Step 2):
     // the saved C split into the input (up) X and gate G 32-column blocks of
     // pair b (the forward's block order); dSwiGLU scales it by beta_g, dGeGLU
-    // uses it as saved.
+    // uses it as saved.  The BF16 contract scales C by beta_g for both
+    // (X_g = beta_g C_g, then the gate and input of X).
+    const bool scale_c = P->epi == EPI_DSWIGLU || (P->in_fmt == IN_BF16 && P->epi == EPI_DGEGLU);
     auto saved = [&](int64_t jr, bool gate) {
       const int64_t b = jr / 32, r = jr % 32;
       const bool second = (gate != bool(P->gate_first));
       const double c = J.saved_c[m * 2 * P->n + 64 * b + (second ? 32 : 0) + r];
-      return P->epi == EPI_DSWIGLU ? double(J.beta[g]) * c : c;   // (reading: dSiTU-GLU unscaled too)
+      return scale_c ? double(J.beta[g]) * c : c;   // (reading: dSiTU-GLU unscaled too)
     };
     // dGeGLU: the gate has only an upper clamp, the up value both; the masks
     // test the values before clamping and keep the gradient at either bound
@@ -704,6 +728,7 @@ extern "C" int orc_run(const orc_desc* P, const uint8_t* A, const uint8_t* SFA, 
     return -1;
   if (is_glu(P) && P->n % 64) return -2;
   if (is_bwd(P) && (P->n % 32 || !saved_c || (P->epi == EPI_DSWIGLU && !beta) || bias)) return -4;
+  if (P->in_fmt == IN_BF16 && P->epi == EPI_DGEGLU && !beta) return -4;
   if (P->rht && (is_bwd(P) || !rht_ref || (P->rht >= 2 && (!rht_q || !sfrht)))) return -5;
   // colwise: a segment's swizzled scales SF(n_d, expert_m) occupy exactly
   // n_d * expert_m / 16 bytes (the page's flat segment length) only when n_d is

@@ -10,7 +10,7 @@ import oracle as orc
 from block_scaled_grouped_gb300 import workloads as W
 
 IN_CODE = {"mxfp8_e4m3": orc.IN_MXFP8_E4M3, "mxfp8_e5m2": orc.IN_MXFP8_E5M2, "nvfp4": orc.IN_NVFP4,
-           "fp4_ue8m0_16": orc.IN_FP4_UE8M0_16, "mxfp4": orc.IN_MXFP4}
+           "fp4_ue8m0_16": orc.IN_FP4_UE8M0_16, "mxfp4": orc.IN_MXFP4, "bf16": orc.IN_BF16}
 OUT_CODE = {"bf16": orc.OUT_BF16, "f16": orc.OUT_F16, "f32": orc.OUT_F32, "e4m3": orc.OUT_E4M3,
             "e5m2": orc.OUT_E5M2, "e2m1": orc.OUT_E2M1}
 EPI_CODE = {"gate": orc.EPI_GATE, "swiglu": orc.EPI_SWIGLU, "srelu": orc.EPI_SRELU, "geglu": orc.EPI_GEGLU,
@@ -48,6 +48,9 @@ def dequant_dense(codes: np.ndarray, sf_rows: np.ndarray, in_fmt: str, k: int) -
     """Brute-force dequantization of a K-major operand with row-major scale
     codes (R, k/v), independent of the oracle's tables."""
     codes = np.ascontiguousarray(codes)
+    if in_fmt == "bf16":
+        # torch's bfloat16 decoding of the little-endian byte pairs; no scales
+        return torch.from_numpy(codes).view(torch.bfloat16).double().numpy()[:, :k]
     if in_fmt in ("nvfp4", "fp4_ue8m0_16", "mxfp4"):
         lo = codes & 0xF
         hi = codes >> 4
