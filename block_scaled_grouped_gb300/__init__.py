@@ -14,7 +14,7 @@ from typing import Optional
 
 from . import build as _build
 
-IN_FORMATS = {"mxfp8_e4m3": 0, "mxfp8_e5m2": 1, "nvfp4": 2, "fp4_ue8m0_16": 3, "mxfp4": 4}
+IN_FORMATS = {"mxfp8_e4m3": 0, "mxfp8_e5m2": 1, "nvfp4": 2, "fp4_ue8m0_16": 3, "mxfp4": 4, "bf16": 5}
 OUT_FORMATS = {"bf16": 0, "f16": 1, "f32": 2, "e4m3": 3, "e5m2": 4, "e2m1": 5}
 EPILOGUES = {"gate": 0, "swiglu": 1, "srelu": 2, "geglu": 3, "dswiglu": 4, "dgeglu": 5, "dsituglu": 6}
 BWD_EPILOGUES = ("dswiglu", "dgeglu", "dsituglu")
@@ -173,6 +173,8 @@ def pack_sf(rowmajor, out=None, stream=None):
     import torch
     L_, rows, kb = rowmajor.shape
     assert rowmajor.is_cuda and rowmajor.dtype == torch.uint8 and rowmajor.is_contiguous()
+    if kb == 0:   # no scale factors (bf16 operands): nothing to pack
+        return torch.empty(0, dtype=torch.uint8, device=rowmajor.device)
     nbytes = sf_bytes(rows, kb, 1, L_)
     if out is None:
         out = torch.empty(nbytes, dtype=torch.uint8, device=rowmajor.device)

@@ -22,7 +22,7 @@ _SHAPES = ["mxf8_128", "mxf8_256", "mxf8_pair", "mxf8_mc", "nvf4_128", "nvf4_256
 # forward and backward instances of each input family and tile shape in units
 # of their own, so that they compile in parallel
 UNITS = (["bsgg_host.cu", "bsgg_peak.cu"] + [f"bsgg_launch_{s}.cu" for s in _SHAPES] +
-         [f"bsgg_launch_{s}_bwd.cu" for s in _SHAPES])
+         [f"bsgg_launch_{s}_bwd.cu" for s in _SHAPES] + ["bsgg_launch_bf16_bwd.cu"])
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE]

@@ -81,6 +81,11 @@ int out_elem_bits(int out) {
   }
 }
 
+// FP4 data (E2M1) with E4M3 or UE8M0 scales; the UE8M0-scaled ones; bfloat16
+// operands without scales (the BF16 backend of the dGLU backward)
+bool is_fp4_in(int f) { return f == BSGG_IN_NVFP4 || f == BSGG_IN_FP4_UE8M0_16 || f == BSGG_IN_MXFP4; }
+bool is_f4e8_in(int f) { return f == BSGG_IN_FP4_UE8M0_16 || f == BSGG_IN_MXFP4; }
+
 bsgg_status validate(const bsgg_desc* d) {
   if (!d) return BSGG_ERR_INVALID_ARG;
   // tile shape: the pages' mma_tiler_mn with TILE_M in {128, 256} (256 = 2-CTA
@@ -104,7 +109,7 @@ bsgg_status validate(const bsgg_desc* d) {
   if (d->m_pad <= 0 || d->m_pad % 128 != 0 || d->m_pad > (int64_t(1) << 30)) return BSGG_ERR_INVALID_ARG;
   if (d->n <= 0 || d->k <= 0 || d->n > (int64_t(1) << 24) || d->k > (int64_t(1) << 24))
     return BSGG_ERR_INVALID_ARG;
-  if (d->in_format < BSGG_IN_MXFP8_E4M3 || d->in_format > BSGG_IN_MXFP4) return BSGG_ERR_INVALID_ARG;
+  if (d->in_format < BSGG_IN_MXFP8_E4M3 || d->in_format > BSGG_IN_BF16) return BSGG_ERR_INVALID_ARG;
   if (d->out_format < BSGG_OUT_BF16 || d->out_format > BSGG_OUT_E2M1) return BSGG_ERR_INVALID_ARG;
   if (d->epilogue < BSGG_EPI_GATE || d->epilogue > BSGG_EPI_DSITUGLU) return BSGG_ERR_INVALID_ARG;
   const bool glu = d->epilogue == BSGG_EPI_SWIGLU || d->epilogue == BSGG_EPI_GEGLU;
@@ -122,13 +127,20 @@ bsgg_status validate(const bsgg_desc* d) {
   if (d->gate_first != 0 && d->gate_first != 1) return BSGG_ERR_INVALID_ARG;
   if (d->want_col != 0 && d->want_col != 1) return BSGG_ERR_INVALID_ARG;
   // K-major rows must be 16-byte aligned ("Support Surface and Constraints",
-  // Layouts and Strides): K % 16 for FP8, K % 32 for packed FP4.
-  const bool fp4 = d->in_format >= BSGG_IN_NVFP4;
-  if (d->k % (fp4 ? 32 : 16) != 0) return BSGG_ERR_INVALID_ARG;
-  // UE8M0-scaled FP4 has kernel instances for single CTAs and CTA pairs only
-  // (one scale per 32 values reaches the MMA through the scale-store warps,
-  // which the multicast clusters do not have)
-  if (d->in_format > BSGG_IN_NVFP4 && d->cluster_m == 2 && d->tile_m != 256) return BSGG_ERR_UNSUPPORTED;
+  // Layouts and Strides): K % 16 for FP8, K % 32 for packed FP4, K % 8 for bf16.
+  const bool fp4 = is_fp4_in(d->in_format), bf16_in = d->in_format == BSGG_IN_BF16;
+  if (d->k % (fp4 ? 32 : bf16_in ? 8 : 16) != 0) return BSGG_ERR_INVALID_ARG;
+  // UE8M0-scaled FP4 and bfloat16 operands have kernel instances for single
+  // CTAs and CTA pairs only (one scale per 32 values reaches the MMA through
+  // the scale-store warps, which the multicast clusters do not have)
+  if ((is_f4e8_in(d->in_format) || bf16_in) && d->cluster_m == 2 && d->tile_m != 256)
+    return BSGG_ERR_UNSUPPORTED;
+  // The BF16 backend ("Grouped GEMM + dGLU (SM100)", Backend dispatch and BF16
+  // contract): dSwiGLU and dGeGLU with the source GeGLU constants, 16/32-bit
+  // D_row, no D_col, scale factors or norm_const
+  if (bf16_in && ((d->epilogue != BSGG_EPI_DSWIGLU && d->epilogue != BSGG_EPI_DGEGLU) || d->dgeglu_custom ||
+                  is_quant(d->out_format)))
+    return BSGG_ERR_INVALID_ARG;
   // SwiGLU pairs 32-column blocks: N % 64 ("Grouped GEMM + SwiGLU (SM100)",
   // Shapes and Divisibility).  Outputs are written in 32-column chunks.
   if (glu ? (d->n % 64 != 0) : (d->n % 32 != 0)) return BSGG_ERR_INVALID_ARG;
@@ -175,8 +187,13 @@ bsgg_status validate(const bsgg_desc* d) {
 
 uint32_t make_idesc(int in_format, int bn, bool pair) {
   uint32_t fmt, scale_ue8m0;
+  if (in_format == BSGG_IN_BF16) {
+    // kind::f16: F32 accumulator (bits 4-5 = 1), BF16 A and B (format 1)
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(bn >> 3) << 17) |
+           (static_cast<uint32_t>((pair ? 2 * bsgg::kBM : bsgg::kBM) >> 4) << 24);
+  }
   if (in_format == BSGG_IN_NVFP4) { fmt = 1; scale_ue8m0 = 0; }          // E2M1, UE4M3 scales
-  else if (in_format > BSGG_IN_NVFP4) { fmt = 1; scale_ue8m0 = 1; }      // E2M1, UE8M0 scales (per 16 slots)
+  else if (is_f4e8_in(in_format)) { fmt = 1; scale_ue8m0 = 1; }       // E2M1, UE8M0 scales (per 16 slots)
   else { fmt = (in_format == BSGG_IN_MXFP8_E4M3) ? 0u : 1u; scale_ue8m0 = 1; }  // E4M3/E5M2, UE8M0
   uint32_t d = 0;
   d |= fmt << 7;                                      // A format
@@ -208,7 +225,7 @@ bsgg_status encode_maps(const bsgg_plan* P, const bsgg_args* a, bsgg::Launch* L)
   const int64_t kq = ceil_div(ceil_div(d.k, P->sf_vec), 4);
   // scale atoms per stage (an atom = 4 scales of 128 rows): 4 for FP4 with one
   // scale per 16 values, 2 per 32, 1 for MXFP8
-  const bool fp4 = P->desc.in_format >= BSGG_IN_NVFP4;
+  const bool fp4 = is_fp4_in(P->desc.in_format);
   const int atoms = !fp4 ? 1 : P->sf_vec == 32 ? 2 : 4;
   bsgg_status st;
   {
@@ -231,6 +248,12 @@ bsgg_status encode_maps(const bsgg_plan* P, const bsgg_args* a, bsgg::Launch* L)
     cuuint32_t box[3] = {bsgg::kBKBytes, cuuint32_t(P->pair || P->mc ? P->bn / 2 : P->bn), 1};
     if ((st = encode_one(&L->tmB, b_base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) != BSGG_OK)
       return st;
+  }
+  // bfloat16 operands have no scale factors: the scale maps stay zero (unused)
+  if (d.in_format == BSGG_IN_BF16) {
+    std::memset(&L->tmSFA, 0, sizeof(L->tmSFA));
+    std::memset(&L->tmSFB, 0, sizeof(L->tmSFB));
+    return BSGG_OK;
   }
   {
     cuuint64_t dims[3] = {256, cuuint64_t(2 * kq), cuuint64_t(ceil_div(d.m_pad, 128))};
@@ -280,9 +303,9 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
   P->outc = desc->out_format == BSGG_OUT_E2M1 ? bsgg::OUTC_FP4
             : is_quant(desc->out_format)      ? bsgg::OUTC_FP8
                                               : bsgg::OUTC_FLOAT;
-  const bool fp4 = desc->in_format >= BSGG_IN_NVFP4;
+  const bool fp4 = is_fp4_in(desc->in_format);
   P->sf_vec = (desc->in_format == BSGG_IN_NVFP4 || desc->in_format == BSGG_IN_FP4_UE8M0_16) ? 16 : 32;
-  P->kbytes = fp4 ? desc->k / 2 : desc->k;
+  P->kbytes = fp4 ? desc->k / 2 : desc->in_format == BSGG_IN_BF16 ? 2 * desc->k : desc->k;
   P->n_out = (desc->epilogue == BSGG_EPI_SWIGLU || desc->epilogue == BSGG_EPI_GEGLU) ? desc->n / 2
              : is_bwd_epi(desc->epilogue)                                             ? 2 * desc->n
                                                                                       : desc->n;
@@ -300,24 +323,26 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
 bsgg_status check_args(const bsgg_plan* P, const bsgg_args* a) {
   if (!a) return BSGG_ERR_INVALID_ARG;
   const bsgg_desc& d = P->desc;
-  const void* need[] = {a->a, a->sfa, a->padded_offsets, a->alpha, a->prob, a->d};
+  // bfloat16 operands take no scale factors (sfa, sfb and sfb_ptrs are not read)
+  const bool scaled = d.in_format != BSGG_IN_BF16;
+  const void* need[] = {a->a, scaled ? a->sfa : a->a, a->padded_offsets, a->alpha, a->prob, a->d};
   for (const void* p : need)
     if (!p || !aligned16(p)) return BSGG_ERR_INVALID_ARG;
   // dense and discrete weights are mutually exclusive ("Grouped GEMM + GLU +
   // Hadamard + Quant (SM100)", Constraints)
   if (d.discrete_b) {
-    if (a->b || a->sfb || !a->b_ptrs || !a->sfb_ptrs || !aligned16(a->b_ptrs) || !aligned16(a->sfb_ptrs))
-      return BSGG_ERR_INVALID_ARG;
+    if (a->b || a->sfb || !a->b_ptrs || !aligned16(a->b_ptrs)) return BSGG_ERR_INVALID_ARG;
+    if (scaled && (!a->sfb_ptrs || !aligned16(a->sfb_ptrs))) return BSGG_ERR_INVALID_ARG;
   } else {
-    if (a->b_ptrs || a->sfb_ptrs || !a->b || !a->sfb || !aligned16(a->b) || !aligned16(a->sfb))
-      return BSGG_ERR_INVALID_ARG;
+    if (a->b_ptrs || a->sfb_ptrs || !a->b || !aligned16(a->b)) return BSGG_ERR_INVALID_ARG;
+    if (scaled && (!a->sfb || !aligned16(a->sfb))) return BSGG_ERR_INVALID_ARG;
   }
   if (is_quant(d.out_format)) {
     if (!a->sfd_row || !a->norm_const || !aligned16(a->sfd_row)) return BSGG_ERR_INVALID_ARG;
     if (d.want_col && (!a->d_col || !a->sfd_col || !aligned16(a->d_col) || !aligned16(a->sfd_col)))
       return BSGG_ERR_INVALID_ARG;
-  } else if (d.out_format != BSGG_OUT_F32 && !a->amax) {
-    return BSGG_ERR_INVALID_ARG;   // amax required for bf16/f16 D
+  } else if (d.out_format != BSGG_OUT_F32 && scaled && !a->amax) {
+    return BSGG_ERR_INVALID_ARG;   // amax required for bf16/f16 D (optional on the BF16 backend)
   }
   if (d.want_bias && (!a->bias || !aligned16(a->bias))) return BSGG_ERR_INVALID_ARG;
   if (d.epilogue == BSGG_EPI_DSWIGLU && (!a->saved_c || !aligned16(a->saved_c) || !a->beta || !a->dprob))
@@ -325,6 +350,8 @@ bsgg_status check_args(const bsgg_plan* P, const bsgg_args* a) {
   if ((d.epilogue == BSGG_EPI_DGEGLU || d.epilogue == BSGG_EPI_DSITUGLU) &&
       (!a->saved_c || !aligned16(a->saved_c) || !a->dprob))
     return BSGG_ERR_INVALID_ARG;
+  // the BF16 contract scales C by beta for dGeGLU too (X = beta C)
+  if (!scaled && d.epilogue == BSGG_EPI_DGEGLU && !a->beta) return BSGG_ERR_INVALID_ARG;
   if (d.want_rht && (!a->rht || !aligned16(a->rht))) return BSGG_ERR_INVALID_ARG;
   if (a->dbias && !is_bwd_epi(d.epilogue)) return BSGG_ERR_INVALID_ARG;   // a backward output
   if (d.want_rht && d.rht_format == BSGG_OUT_E2M1 && (!a->sfrht || !a->rht_norm_const))
@@ -354,16 +381,20 @@ __global__ void pack_sf_kernel(const uint8_t* __restrict__ src, uint8_t* __restr
 // expert.  An expert that owns rows needs both pointers non-null and 16-byte
 // aligned; otherwise the flag after the maps is raised (the GEMM then writes
 // nothing) along with the status bit.  Experts without rows keep the
-// placeholder address; their maps are never used.
+// placeholder address; their maps are never used.  Without scale factors
+// (bfloat16 operands, scaled = 0) sfb_ptrs is not read and the scale maps are
+// left as the (unused) template.
 __global__ void expert_maps_kernel(const __grid_constant__ CUtensorMap tB, const __grid_constant__ CUtensorMap tSFB,
                                    const int64_t* __restrict__ b_ptrs, const int64_t* __restrict__ sfb_ptrs,
-                                   const int32_t* __restrict__ offsets, int L, CUtensorMap* maps, uint32_t* status) {
+                                   int scaled, const int32_t* __restrict__ offsets, int L, CUtensorMap* maps,
+                                   uint32_t* status) {
   const int g = threadIdx.x;
   int bad = 0;
   if (g < L) {
     const int32_t start = g ? offsets[g - 1] : 0;
     const bool used = offsets[g] != start;
-    const uint64_t pb = static_cast<uint64_t>(b_ptrs[g]), ps = static_cast<uint64_t>(sfb_ptrs[g]);
+    const uint64_t pb = static_cast<uint64_t>(b_ptrs[g]);
+    const uint64_t ps = scaled ? static_cast<uint64_t>(sfb_ptrs[g]) : 16u;
     maps[2 * g] = tB;
     maps[2 * g + 1] = tSFB;
     if (used) {
@@ -371,7 +402,7 @@ __global__ void expert_maps_kernel(const __grid_constant__ CUtensorMap tB, const
         bad = 1;
       } else {
         bsgg::tmap_replace_address(&maps[2 * g], pb);
-        bsgg::tmap_replace_address(&maps[2 * g + 1], ps);
+        if (scaled) bsgg::tmap_replace_address(&maps[2 * g + 1], ps);
       }
     }
     bsgg::tmap_release();
@@ -505,7 +536,7 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   p.kq_row = static_cast<int32_t>(ceil_div(ceil_div(P->n_out, P->sf_vec), 4));
   p.kq_col = static_cast<int32_t>(ceil_div(ceil_div(d.m_pad, P->sf_vec), 4));
   p.out_kind = d.out_format;
-  p.sf_atoms = d.in_format < BSGG_IN_NVFP4 ? 1 : P->sf_vec == 32 ? 2 : 4;
+  p.sf_atoms = !is_fp4_in(d.in_format) ? 1 : P->sf_vec == 32 ? 2 : 4;
   p.sf_v32 = P->sf_vec == 32 ? 1 : 0;
   p.want_col = d.want_col;
   p.gate_first = d.gate_first;
@@ -565,13 +596,17 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   L.stream = s;
   if (d.discrete_b) {
     const unsigned threads = static_cast<unsigned>(ceil_div(d.num_groups, 32) * 32);
-    expert_maps_kernel<<<1, threads, 0, s>>>(L.tmB, L.tmSFB, a->b_ptrs, a->sfb_ptrs, a->padded_offsets,
+    expert_maps_kernel<<<1, threads, 0, s>>>(L.tmB, L.tmSFB, a->b_ptrs, a->sfb_ptrs,
+                                             d.in_format != BSGG_IN_BF16 ? 1 : 0, a->padded_offsets,
                                              d.num_groups, P->maps, P->status);
     if (cudaGetLastError() != cudaSuccess) return BSGG_ERR_CUDA;
   }
   cudaError_t e;
   if (is_bwd_epi(d.epilogue)) {
-    if (d.in_format > BSGG_IN_NVFP4)
+    if (d.in_format == BSGG_IN_BF16)
+      e = P->pair ? bsgg::launch_bf16_pair_bwd(L)
+          : P->bn == 256 ? bsgg::launch_bf16_256_bwd(L) : bsgg::launch_bf16_128_bwd(L);
+    else if (is_f4e8_in(d.in_format))
       e = P->pair ? bsgg::launch_f4e8_pair_bwd(L)
           : P->bn == 256 ? bsgg::launch_f4e8_256_bwd(L) : bsgg::launch_f4e8_128_bwd(L);
     else if (d.in_format == BSGG_IN_NVFP4)
@@ -582,7 +617,7 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
       e = P->pair ? bsgg::launch_mxf8_pair_bwd(L)
           : P->mc ? bsgg::launch_mxf8_mc_bwd(L)
           : P->bn == 256 ? bsgg::launch_mxf8_256_bwd(L) : bsgg::launch_mxf8_128_bwd(L);
-  } else if (d.in_format > BSGG_IN_NVFP4)
+  } else if (is_f4e8_in(d.in_format))
     e = P->pair ? bsgg::launch_f4e8_pair(L)
         : P->bn == 256 ? bsgg::launch_f4e8_256(L) : bsgg::launch_f4e8_128(L);
   else if (d.in_format == BSGG_IN_NVFP4)
@@ -629,9 +664,10 @@ bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t L = d.num_groups;
   const uint64_t sz_a = uint64_t(d.m_pad) * P->kbytes;
-  const uint64_t sz_sfa = sf_bytes_impl(d.m_pad, d.k, P->sf_vec, 1);
+  const bool scaled = d.in_format != BSGG_IN_BF16;   // bfloat16 operands: no scale factors
+  const uint64_t sz_sfa = scaled ? sf_bytes_impl(d.m_pad, d.k, P->sf_vec, 1) : 0;
   const uint64_t sz_b = uint64_t(L) * d.n * P->kbytes;
-  const uint64_t sz_sfb = sf_bytes_impl(d.n, d.k, P->sf_vec, L);
+  const uint64_t sz_sfb = scaled ? sf_bytes_impl(d.n, d.k, P->sf_vec, L) : 0;
   const uint64_t sz_d = uint64_t(d.m_pad) * P->out_row_bytes;
   const uint64_t sz_sfd_row = sf_bytes_impl(d.m_pad, P->n_out, P->sf_vec, 1);
   const uint64_t sz_sfd_col = sf_bytes_impl(P->n_out, d.m_pad, P->sf_vec, 1);
@@ -661,7 +697,8 @@ bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* 
                 uint64_t(L) * d.n * (d.bias_format == BSGG_OUT_F32 ? 4 : 2)) &&
             // backward: the saved C and beta in, dprob in (it is accumulated) and out
             h2d(bwd ? host->saved_c : nullptr, dev->saved_c, sz_saved_c) &&
-            h2d(d.epilogue == BSGG_EPI_DSWIGLU ? host->beta : nullptr, dev->beta, sizeof(float) * L) &&
+            h2d(d.epilogue == BSGG_EPI_DSWIGLU || (!scaled && d.epilogue == BSGG_EPI_DGEGLU) ? host->beta : nullptr,
+                dev->beta, sizeof(float) * L) &&
             h2d(bwd ? host->dprob : nullptr, dev->dprob, sizeof(float) * d.m_pad) &&
             h2d(d.want_rht ? host->rht_norm_const : nullptr, dev->rht_norm_const, sizeof(float)) &&
             h2d(bwd ? host->dbias : nullptr, dev->dbias, sizeof(float) * L * P->n_out);

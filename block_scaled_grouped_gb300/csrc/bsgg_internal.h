@@ -49,6 +49,9 @@ cudaError_t launch_nvf4_mc_bwd(const Launch& L);
 cudaError_t launch_f4e8_128_bwd(const Launch& L);
 cudaError_t launch_f4e8_256_bwd(const Launch& L);
 cudaError_t launch_f4e8_pair_bwd(const Launch& L);
+cudaError_t launch_bf16_128_bwd(const Launch& L);
+cudaError_t launch_bf16_256_bwd(const Launch& L);
+cudaError_t launch_bf16_pair_bwd(const Launch& L);
 // Largest number of CTAs of the pair (mc = false) or multicast-cluster kernel
 // that can be resident at once (clusters x 2) on the current device, 0 if unknown.
 int cluster_resident_ctas(bool fp4, bool mc);

@@ -63,9 +63,11 @@ __host__ __device__ constexpr bool is_bwd_inst(int epi) { return epi == EPI_DSWI
 // Input class (template): MXFP8 (E4M3/E5M2 data, UE8M0 scales per 32), NVFP4
 // (E2M1 data, E4M3 scales per 16), or E2M1 data with UE8M0 scales, whose block
 // length (16 or 32) is a runtime choice (Params::sf_v32).  NVFP4 keeps its own
-// instances: the runtime choices cost it 2 % on GB300.
-enum : int { IC_MXF8 = 0, IC_NVF4 = 1, IC_F4E8 = 2 };
-__host__ __device__ constexpr bool ic_fp4(int ic) { return ic != IC_MXF8; }
+// instances: the runtime choices cost it 2 % on GB300.  IC_BF16: bfloat16 A
+// and B without scale factors (the BF16 backend of the dGLU backward).
+enum : int { IC_MXF8 = 0, IC_NVF4 = 1, IC_F4E8 = 2, IC_BF16 = 3 };
+__host__ __device__ constexpr bool ic_fp4(int ic) { return ic == IC_NVF4 || ic == IC_F4E8; }
+__host__ __device__ constexpr bool ic_scaled(int ic) { return ic != IC_BF16; }
 // Output class (template) and exact output kind (runtime) of D.
 enum : int { OUTC_FLOAT = 0, OUTC_FP8 = 1, OUTC_FP4 = 2 };
 enum : int { OK_BF16 = 0, OK_F16 = 1, OK_F32 = 2, OK_E4M3 = 3, OK_E5M2 = 4, OK_E2M1 = 5 };
@@ -167,15 +169,17 @@ struct Params {
   const uint32_t* maps_bad;
 };
 
-template <bool FP4, int BN, bool PAIR>
+// SCALED = false (bfloat16 operands): no scale buffers, 64 K elements per
+// 128-byte stage, 16 per MMA.
+template <bool FP4, int BN, bool PAIR, bool SCALED = true>
 struct Layout {
   static_assert(BN == 128 || BN == 256, "tile width");
   static_assert(!PAIR || BN == 256, "CTA pairs use 256 x 256 tiles");
   static constexpr int kHalves = BN / 128;                 // 128-row SF blocks of the MMA's N
   static constexpr int kBRows = PAIR ? BN / 2 : BN;        // B rows held by this CTA
-  static constexpr int kAtoms = FP4 ? 4 : 1;               // SF atoms per stage per 128 rows
-  static constexpr int kKElems = FP4 ? 256 : 128;          // K elements per stage
-  static constexpr int kMmaK = FP4 ? 64 : 32;              // K elements per MMA instruction
+  static constexpr int kAtoms = !SCALED ? 0 : FP4 ? 4 : 1;          // SF atoms per stage per 128 rows
+  static constexpr int kKElems = !SCALED ? 64 : FP4 ? 256 : 128;    // K elements per stage
+  static constexpr int kMmaK = !SCALED ? 16 : FP4 ? 64 : 32;        // K elements per MMA instruction
   static constexpr int kABytes = kBM * kBKBytes;
   static constexpr int kBBytes = kBRows * kBKBytes;
   static constexpr int kSfaBytes = kAtoms * 512;
@@ -728,14 +732,16 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                 const __grid_constant__ Params p) {
   constexpr bool FP4 = ic_fp4(IC);
+  constexpr bool SCALED = ic_scaled(IC);
   static_assert(IC != IC_F4E8 || CM != CM_MC, "UE8M0-scaled FP4 needs the scale stores");
+  static_assert(SCALED || CM != CM_MC, "bfloat16 operands run on single CTAs and pairs");
   constexpr bool PAIR = CM == CM_PAIR;
   constexpr bool MC = CM == CM_MC;
   constexpr bool CLUSTER = CM != CM_SINGLE;
   static_assert(!MC || BN == 256, "multicast clusters use 128 x 256 tiles");
   constexpr bool ST = scale_stores<FP4, CM>();
   using Ro = Roles<ST>;
-  using Ly = Layout<FP4, BN, PAIR>;
+  using Ly = Layout<FP4, BN, PAIR, SCALED>;
   constexpr int S = Ly::kStages;
   constexpr int NA = Ly::kNumAcc;
   constexpr uint32_t kABytesHalf = Ly::kABytes / 2;   // one 64-row A box (multicast clusters)
@@ -784,8 +790,10 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
     mbar_fence_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-    prefetch_tmap(&tmSFA);
-    prefetch_tmap(&tmSFB);
+    if (SCALED) {
+      prefetch_tmap(&tmSFA);
+      prefetch_tmap(&tmSFB);
+    }
   }
   if (warp == 1) {
     if (PAIR) { tmem_alloc_pair(smem_u32(tmem_holder), Ly::kTmemCols); tmem_relinquish_pair(); }
@@ -865,7 +873,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
             sfb_rb = nt * Ly::kHalves;
             if (g != fenced_g) {
               tmap_acquire(mB);
-              tmap_acquire(mSFB);
+              if (SCALED) tmap_acquire(mSFB);
               fenced_g = g;
             }
           }
@@ -897,8 +905,10 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
               if (leader) mbar_expect_tx(fb, 2u * Ly::kStageBytes);
               tma_load_2d_pair(sA, &tmA, fbl, k0, mt * kBM);
               tma_load_3d_pair(sB, mB, fbl, k0, b_row, bz);
-              tma_load_3d_pair(sSa, &tmSFA, fbl, 0, ka, mt);
-              tma_load_3d_pair(sSb, mSFB, fbl, 0, ka, sfb_rb);
+              if (SCALED) {
+                tma_load_3d_pair(sSa, &tmSFA, fbl, 0, ka, mt);
+                tma_load_3d_pair(sSb, mSFB, fbl, 0, ka, sfb_rb);
+              }
             } else if (MC) {
               // every byte of this CTA's stage counts on its own barrier; the
               // shared operand arrives half from each CTA (A boxes are 64 rows,
@@ -920,8 +930,10 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
               mbar_expect_tx(fb, Ly::kABytes + Ly::kBBytes + sf_tx);
               tma_load_2d(sA, &tmA, fb, k0, mt * kBM);
               tma_load_3d(sB, mB, fb, k0, b_row, bz);
-              tma_load_3d(sSa, &tmSFA, fb, 0, ka, mt);
-              tma_load_3d(sSb, mSFB, fb, 0, ka, sfb_rb);
+              if (SCALED) {
+                tma_load_3d(sSa, &tmSFA, fb, 0, ka, mt);
+                tma_load_3d(sSb, mSFB, fb, 0, ka, sfb_rb);
+              }
             }
             issued[stage] = true;
             issued_phase[stage] = phase;
@@ -972,7 +984,8 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
         uint32_t idk[4];
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          idk[kk] = FP4 ? p.idesc : (p.idesc | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4));
+          idk[kk] = (FP4 || !SCALED) ? p.idesc
+                                     : (p.idesc | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4));
         const int full_stages = p.k / Ly::kKElems;      // stages with all four MMAs
         auto issue_stage = [&](uint32_t d_tmem, int st, int n_mma, uint32_t acc0) {
           const uint32_t sfa_t = sf_tmem0 + st * Ly::kSfColsPerStage;
@@ -984,7 +997,10 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
             if (kk >= n_mma) break;
             const uint32_t accum = kk ? 1u : acc0;
             // one MMA consumes 32 K-bytes: +2 in descriptor units
-            if (FP4) {
+            if (!SCALED) {
+              if (PAIR) tc_mma_bf16_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], accum);
+              else tc_mma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], accum);
+            } else if (FP4) {
               const uint32_t sa = sfa_t + 4 * kk, sb = sfb_t + 4 * Ly::kHalves * kk;
               if (PAIR) tc_mma_nvf4_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sa, sb, accum);
               else tc_mma_nvf4(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sa, sb, accum);
@@ -1007,7 +1023,9 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
           for (int ks = 0; ks < p.num_k_stages; ++ks) {
             // pairs storing scales: the scale warps waited for the scales only
             if (PAIR && ST && !mbar_wait(full_bar(stage), phase, abort_flag, p.wait_limit_ns)) { ok = false; break; }
-            if (!mbar_wait(sfr_bar(stage), phase, abort_flag, p.wait_limit_ns)) { ok = false; break; }
+            // the stage's operands (and scales, through the scale warp or copier)
+            const uint32_t ready = SCALED ? sfr_bar(stage) : full_bar(stage);
+            if (!mbar_wait(ready, phase, abort_flag, p.wait_limit_ns)) { ok = false; break; }
             tc_fence_after();
             if (ks < full_stages) {
               issue_stage(d_tmem, stage, 4, ks ? 1u : 0u);
@@ -1098,7 +1116,8 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
         // Same stage sequence as the MMA issuer.  Writing a stage's tensor-memory
         // scale slot is safe once its "full" barrier completed: the refill behind
         // it waited for the MMAs that read the slot's previous contents.
-        if (lane == 0 && issues_mma) {
+        // (bfloat16 operands have no scales: the MMA issuer waits on "full".)
+        if (SCALED && lane == 0 && issues_mma) {
           int stage = 0;
           uint32_t phase = 0;
           bool ok = true;
@@ -1227,7 +1246,10 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
         // dSwiGLU backward ("Grouped GEMM + dGLU (SM100)", Block-scaled contract):
         // GEMM column j of pair b = j / 32 -> D (and saved C) columns 64b + r of
         // the input block and of the gate block, in the forward's block order
-        const float al2 = al * al, bt = (EPI == EPI_DSWIGLU && p.bwd_kind == 0) ? p.beta[g] : 1.0f;
+        // beta scales the saved C for dSwiGLU, and for dGeGLU on bfloat16
+        // operands (the BF16 contract's X = beta C)
+        const float al2 = al * al,
+                    bt = (EPI == EPI_DSWIGLU && (p.bwd_kind == 0 || IC == IC_BF16)) ? p.beta[g] : 1.0f;
         const bool gf = p.gate_first != 0;
         float dprob_local = 0.0f;
 #pragma unroll
@@ -1276,11 +1298,12 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
             }
           } else {
             // dGeGLU: the gate clamped above, the up value both ways; each
-            // gradient masked where its own raw value lies beyond a bound
+            // gradient masked where its own raw value lies beyond a bound.
+            // bfloat16 operands: of beta C (the BF16 contract's X = beta C)
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float ref = al2 * __uint_as_float(r[32 * c + i]);
-              const float U = x[i], G = gv[i];
+              const float U = IC == IC_BF16 ? bt * x[i] : x[i], G = IC == IC_BF16 ? bt * gv[i] : gv[i];
               const float gc = fminf(G, p.clamp_max);
               const float uc = fminf(fmaxf(U, p.clamp_min), p.clamp_max);
               const float sg = __fdividef(1.0f, 1.0f + __expf(-p.geglu_a * gc));

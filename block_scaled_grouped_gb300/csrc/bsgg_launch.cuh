@@ -14,7 +14,7 @@ cudaError_t launch_one(const Launch& L) {
   constexpr bool kCluster = CM != CM_SINGLE;
   constexpr bool kStores = scale_stores<FP4, CM>();
   using Ro = Roles<kStores>;
-  const int smem = Layout<FP4, BN, CM == CM_PAIR>::kSmemBytes;
+  const int smem = Layout<FP4, BN, CM == CM_PAIR, ic_scaled(IC)>::kSmemBytes;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -55,15 +55,20 @@ cudaError_t launch_one(const Launch& L) {
 
 template <int IC, int BN, int CM, int EPI, bool XC>
 cudaError_t launch_outc(const Launch& L) {
-  switch (L.outc) {
-    case OUTC_FLOAT: return launch_one<IC, BN, CM, EPI, OUTC_FLOAT, XC>(L);
-    case OUTC_FP8:
-      // FP8 outputs come from MXFP8 inputs only (the host refuses them for FP4)
-      if constexpr (ic_fp4(IC)) return cudaErrorInvalidValue;
-      else return launch_one<IC, BN, CM, EPI, OUTC_FP8, XC>(L);
-    case OUTC_FP4: return launch_one<IC, BN, CM, EPI, OUTC_FP4, XC>(L);
+  // bfloat16 operands (the BF16 backend): 16/32-bit outputs only
+  if constexpr (IC == IC_BF16) {
+    return L.outc == OUTC_FLOAT ? launch_one<IC, BN, CM, EPI, OUTC_FLOAT, XC>(L) : cudaErrorInvalidValue;
+  } else {
+    switch (L.outc) {
+      case OUTC_FLOAT: return launch_one<IC, BN, CM, EPI, OUTC_FLOAT, XC>(L);
+      case OUTC_FP8:
+        // FP8 outputs come from MXFP8 inputs only (the host refuses them for FP4)
+        if constexpr (ic_fp4(IC)) return cudaErrorInvalidValue;
+        else return launch_one<IC, BN, CM, EPI, OUTC_FP8, XC>(L);
+      case OUTC_FP4: return launch_one<IC, BN, CM, EPI, OUTC_FP4, XC>(L);
+    }
+    return cudaErrorInvalidValue;
   }
-  return cudaErrorInvalidValue;
 }
 
 // The XC instances: forward launches with a bias, a stored C or the Hadamard
@@ -90,7 +95,10 @@ template <int IC, int BN, int CM>
 cudaError_t launch_shape_bwd(const Launch& L) {
   switch (L.epi) {
     case EPI_DSWIGLU: return launch_xc<IC, BN, CM, EPI_DSWIGLU>(L);
-    case EPI_DSITUGLU: return launch_xc<IC, BN, CM, EPI_DSITUGLU>(L);
+    case EPI_DSITUGLU:
+      // dSiTU-GLU is not a BF16-backend activation
+      if constexpr (IC == IC_BF16) return cudaErrorInvalidValue;
+      else return launch_xc<IC, BN, CM, EPI_DSITUGLU>(L);
   }
   return cudaErrorInvalidValue;
 }

@@ -89,9 +89,15 @@ typedef enum {
   BSGG_IN_MXFP8_E5M2 = 1,  /* float8_e5m2 data,   float8_e8m0fnu scales, v = 32 */
   BSGG_IN_NVFP4 = 2,       /* float4_e2m1fn_x2 data, float8_e4m3fn scales, v = 16 */
   BSGG_IN_FP4_UE8M0_16 = 3,/* float4_e2m1fn_x2 data, float8_e8m0fnu scales, v = 16 */
-  BSGG_IN_MXFP4 = 4        /* float4_e2m1fn_x2 data, float8_e8m0fnu scales, v = 32 */
+  BSGG_IN_MXFP4 = 4,       /* float4_e2m1fn_x2 data, float8_e8m0fnu scales, v = 32 */
   /* The two UE8M0-scaled FP4 formats run on single CTAs and CTA pairs; the (2, 1)
      multicast clusters of 128 x 256 tiles return BSGG_ERR_UNSUPPORTED for them. */
+  BSGG_IN_BF16 = 5         /* bfloat16 A and B, no scale factors: the BF16 backend of
+                              "Grouped GEMM + dGLU (SM100)" (Backend dispatch, BF16
+                              contract).  Backward DSWIGLU / DGEGLU only (dGeGLU with
+                              its fixed constants: dgeglu_custom = 0), BF16/F16/F32 D,
+                              no D_col; K % 8 == 0; single CTAs and CTA pairs.  The
+                              dGeGLU saved C is scaled by beta as well (X = beta C). */
 } bsgg_in_format;
 
 /* Output formats of D (and D_col). */
@@ -205,7 +211,8 @@ typedef struct {
  * want_col; sfd_row/sfd_col/norm_const for 16/32-bit outputs; amax for
  * quantized outputs; bias unless want_bias; c unless want_c.  amax is
  * required for BF16/F16 outputs and optional for F32 ("Grouped GEMM + Quant
- * (SM100)", Scale Factor Output Requirements). */
+ * (SM100)", Scale Factor Output Requirements); with BSGG_IN_BF16 inputs it is
+ * optional, and sfa, sfb and sfb_ptrs are not read (NULL). */
 typedef struct {
   const void* a;
   const void* sfa;
@@ -229,7 +236,8 @@ typedef struct {
   const int64_t* b_ptrs;
   const int64_t* sfb_ptrs;
   /* DSWIGLU, DGEGLU and DSITUGLU: the saved forward C (m_pad, 2N) N-major in saved_c_format,
-     its per-group scale beta (L; DSWIGLU only), and dprob (m_pad), which the kernel
+     its per-group scale beta (L; DSWIGLU, and DGEGLU with BSGG_IN_BF16), and dprob
+     (m_pad), which the kernel
      ACCUMULATES into:
      zero it before the call ("Grouped GEMM + dGLU (SM100)": dprob must be
      zero-initialized).  amax then holds 2L floats: [2g] over the input-gradient

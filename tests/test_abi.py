@@ -124,6 +124,13 @@ def _create(**over):
     (dict(in_format="fp4_ue8m0_16", tile_m=128, tile_n=256, cluster_m=2, cluster_n=1), 2),
     (dict(in_format="mxfp4", out_format="e5m2"), 2),
     (dict(in_format="mxfp4", k=48), 1),                           # K % 32 for packed FP4
+    # the BF16 backend: dSwiGLU / dGeGLU (fixed constants), 16/32-bit D, K % 8
+    (dict(in_format="bf16"), 1),                                  # no forward epilogues
+    (dict(in_format="bf16", epilogue="dsituglu"), 1),
+    (dict(in_format="bf16", epilogue="dgeglu", dgeglu_params=(1.0, -7.0, 7.0, 1.0)), 1),
+    (dict(in_format="bf16", epilogue="dswiglu", out_format="e4m3"), 1),
+    (dict(in_format="bf16", epilogue="dswiglu", k=252), 1),
+    (dict(in_format="bf16", epilogue="dswiglu", tile_m=128, tile_n=256, cluster_m=2, cluster_n=1), 2),
 ])
 def test_create_rejects(lib, over, code):
     assert _create(**over) == code
@@ -142,6 +149,9 @@ def test_create_rejects(lib, over, code):
     dict(in_format="mxfp4", epilogue="srelu", out_format="e2m1", want_col=1, tile_m=256, tile_n=256,
          cluster_m=2, cluster_n=1),
     dict(in_format="fp4_ue8m0_16", epilogue="dswiglu", out_format="bf16"),
+    dict(in_format="bf16", epilogue="dswiglu", out_format="f32", k=264),
+    dict(in_format="bf16", epilogue="dgeglu", out_format="bf16", tile_m=256, tile_n=256, cluster_m=2,
+         cluster_n=1, discrete_b=True),
 ])
 def test_create_accepts_epilogue_options(lib, over):
     # validation passes: 0 with a GPU, else the device query that follows
