@@ -1,7 +1,7 @@
 """Benchmark of the grouped block-scaled GEMM on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gpu|reference]
-                    [--workload fc1_swiglu|fc2_gate|fine_nvfp4|skewed|tiny]
+                    [--workload fc1_swiglu|fc2_gate|fine_nvfp4|skewed|fc1_dswiglu|fc1_dswiglu_bf16|tiny]
 
 A step is one bsgg_run over one batch of the workload (all of the hot path:
 scheduling, operand fetch, block-scaled MMA, alpha/prob, activation,
@@ -40,9 +40,10 @@ sys.path.insert(0, ROOT)
 METRIC = "grouped GEMM TFLOP/s (valid rows) and % of GB300 dense FP8/FP4 peak, 1 GPU"
 UNIT = "TFLOP/s"
 # nominal dense tensor throughput relative to bf16 (2.25 PFLOP/s): fp8 4.5, fp4 13.5
-DTYPE_RATIO = {"mxfp8_e4m3": 2.0, "mxfp8_e5m2": 2.0, "nvfp4": 6.0, "fp4_ue8m0_16": 6.0, "mxfp4": 6.0}
+DTYPE_RATIO = {"mxfp8_e4m3": 2.0, "mxfp8_e5m2": 2.0, "nvfp4": 6.0, "fp4_ue8m0_16": 6.0, "mxfp4": 6.0, "bf16": 1.0}
 DTYPE_NAME = {"mxfp8_e4m3": "mxfp8(e4m3,ue8m0/32)", "mxfp8_e5m2": "mxfp8(e5m2,ue8m0/32)",
-              "nvfp4": "nvfp4(e2m1,e4m3/16)", "fp4_ue8m0_16": "fp4(e2m1,ue8m0/16)", "mxfp4": "mxfp4(e2m1,ue8m0/32)"}
+              "nvfp4": "nvfp4(e2m1,e4m3/16)", "fp4_ue8m0_16": "fp4(e2m1,ue8m0/16)", "mxfp4": "mxfp4(e2m1,ue8m0/32)",
+              "bf16": "bf16"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -204,7 +205,7 @@ def oracle_sample(p, ins, budget_s: float, max_blocks: int = 64, seed: int = 0):
     budget_s of wall time is spent.  Returns (flops, seconds, blocks, threads)."""
     import oracle as orc
     code_in = {"mxfp8_e4m3": orc.IN_MXFP8_E4M3, "mxfp8_e5m2": orc.IN_MXFP8_E5M2, "nvfp4": orc.IN_NVFP4,
-               "fp4_ue8m0_16": orc.IN_FP4_UE8M0_16, "mxfp4": orc.IN_MXFP4}
+               "fp4_ue8m0_16": orc.IN_FP4_UE8M0_16, "mxfp4": orc.IN_MXFP4, "bf16": orc.IN_BF16}
     code_out = {"bf16": orc.OUT_BF16, "f16": orc.OUT_F16, "f32": orc.OUT_F32, "e4m3": orc.OUT_E4M3,
                 "e5m2": orc.OUT_E5M2, "e2m1": orc.OUT_E2M1}
     code_epi = {"gate": orc.EPI_GATE, "swiglu": orc.EPI_SWIGLU, "srelu": orc.EPI_SRELU, "geglu": orc.EPI_GEGLU,
@@ -251,7 +252,8 @@ def algorithmic_bytes(p) -> int:
         return 512 * slices * cdiv(rows, 128) * cdiv(cdiv(cols, v), 4)
     fp4 = p.in_fmt in ("nvfp4", "fp4_ue8m0_16", "mxfp4")
     v = p.sf_vec
-    kb = p.k // 2 if fp4 else p.k
+    kb = p.k // 2 if fp4 else 2 * p.k if p.in_fmt == "bf16" else p.k
+    ks = 0 if p.in_fmt == "bf16" else p.k      # bf16 operands have no scale factors
     off = [int(x) for x in p.padded_offsets.tolist()]
     nonempty = sum(1 for g, e in enumerate(off) if e > (off[g - 1] if g else 0))
     n_out = p.n_out
@@ -265,7 +267,7 @@ def algorithmic_bytes(p) -> int:
     extra = 0
     if p.epi in W.BWD_EPILOGUES:
         extra = p.saved_c.numel() * p.saved_c.element_size() + 4 * p.m_pad + 4 * p.num_groups
-    return (p.m_pad * kb + sfb(p.m_pad, p.k, v) + nonempty * p.n * kb + sfb(p.n, p.k, v, nonempty) + out
+    return (p.m_pad * kb + sfb(p.m_pad, ks, v) + nonempty * p.n * kb + sfb(p.n, ks, v, nonempty) + out
             + extra)
 
 

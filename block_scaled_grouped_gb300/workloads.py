@@ -2,7 +2,7 @@
 
 This module is the one input generator that the tests, the smoke check and the
 benchmark share.  It holds the input recipe only -- routing, value draws and
-the quantization of those draws into MXFP8 / NVFP4 codes -- and none of the
+the quantization of those draws into MXFP8 / FP4 codes or bfloat16 -- and none of the
 operation's own arithmetic (no GEMM, no epilogue, no output quantization, no
 scale-factor layout: scale factors leave here row-major and are packed by each
 consumer with its own packer).
@@ -16,6 +16,10 @@ Five named workloads follow the expert-layer shapes of the pages' MoE use:
                  NVFP4 in, sReLU with tanh clamp s=8, NVFP4 out
 5. ``skewed``    L=128, 65536 rows sized by Dirichlet(0.1), K=7168, N=4096,
                  sReLU, E4M3 row + column outputs, norm_const 0.5
+
+and two backward ones, the dSwiGLU backward of the FC1 layer (routing of 2,
+K=4096, N=14336, saved C 28672 wide): ``fc1_dswiglu`` (MXFP8 in, E4M3 row and
+column outputs) and ``fc1_dswiglu_bf16`` (the BF16 backend: bfloat16 in and out).
 
 Routing and per-group/per-row scalars are drawn with numpy's PCG64 from the
 workload's seed (CPU, device independent).  Matrix values are drawn with a
@@ -390,7 +394,7 @@ def build_problem(*, name: str, counts: Sequence[int], k: int, n: int, in_fmt: s
         a=a, sfa_rows=sfa, b=b, sfb_rows=sfb, saved_c=saved_c, beta=beta)
 
 
-WORKLOADS = ("tiny", "fc1_swiglu", "fc2_gate", "fine_nvfp4", "skewed", "fc1_dswiglu")
+WORKLOADS = ("tiny", "fc1_swiglu", "fc2_gate", "fine_nvfp4", "skewed", "fc1_dswiglu", "fc1_dswiglu_bf16")
 
 
 def workload(name: str, device="cpu") -> Problem:
@@ -401,7 +405,7 @@ def workload(name: str, device="cpu") -> Problem:
         return build_problem(name=name, counts=[128, 256], k=256, n=256, in_fmt="mxfp8_e4m3",
                              out_fmt="bf16", epi="gate", seed=0, device=device,
                              alpha=[1.0, 0.5])
-    if name in ("fc1_swiglu", "fc2_gate", "fc1_dswiglu"):
+    if name in ("fc1_swiglu", "fc2_gate", "fc1_dswiglu", "fc1_dswiglu_bf16"):
         T, L = 4096, 8
         tokens, probs = route_softmax_topk(T, L, 2, seed=1)
         counts = [t.size for t in tokens]
@@ -414,6 +418,12 @@ def workload(name: str, device="cpu") -> Problem:
                                  out_fmt="e4m3", epi="dswiglu", seed=5, device=device,
                                  token_rows=tokens, num_tokens=T, row_prob=probs,
                                  norm_const=1.0, want_col=True)
+        if name == "fc1_dswiglu_bf16":
+            # the same backward on the BF16 backend: bfloat16 gradients and
+            # weights, bfloat16 D_row (no column output or scales)
+            return build_problem(name=name, counts=counts, k=4096, n=14336, in_fmt="bf16",
+                                 out_fmt="bf16", epi="dswiglu", seed=6, device=device,
+                                 token_rows=tokens, num_tokens=T, row_prob=probs)
         if name == "fc1_swiglu":
             return build_problem(name=name, counts=counts, k=4096, n=28672, in_fmt="mxfp8_e4m3",
                                  out_fmt="e4m3", epi="swiglu", seed=1, device=device,

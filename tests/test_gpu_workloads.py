@@ -1,5 +1,5 @@
 """Parity at full size: the four large forward workloads and the FC1 backward
-(dSwiGLU), generated on the GPU with their real shapes and run in every tile
+(dSwiGLU, MXFP8 and the BF16 backend), generated on the GPU with their real shapes and run in every tile
 shape (the library's default is the one bench.py times; two shapes for the
 backward), compared element by element with the CPU oracle on
 sampled 32-row blocks -- each group's first and last block, the first and last
@@ -42,6 +42,8 @@ def _oracle(p, blocks):
                padded_offsets=np_(p.padded_offsets), alpha=np_(p.alpha), prob=np_(p.prob))
     if p.epi == "dswiglu":
         ins.update(saved_c=np_(p.saved_c.double()), beta=np_(p.beta))
+    if p.in_fmt == "bf16":
+        ins.update(sfa=np.zeros(0, np.uint8), sfb=np.zeros(0, np.uint8))
     return orc.run(m_pad=p.m_pad, n=p.n, k=p.k, num_groups=p.num_groups, in_fmt=IN_CODE[p.in_fmt],
                    out_fmt=OUT_CODE[p.out_fmt], epi=EPI_CODE[p.epi], norm_const=p.norm_const,
                    tanh_clamp_s=p.tanh_clamp_s, want_col=p.want_col, blocks=blocks, **ins)
@@ -78,14 +80,16 @@ def test_full_size_parity_on_sampled_blocks(workload, tile):
         assert np.all(amax >= sampled * (1 - 2.0 ** -20))
 
 
+@pytest.mark.parametrize("name", ["fc1_dswiglu", "fc1_dswiglu_bf16"])
 @pytest.mark.parametrize("tile", [(0, 0), (256, 256, 2, 1)], ids=tile_id)
-def test_full_size_backward_on_sampled_blocks(tile):
+def test_full_size_backward_on_sampled_blocks(tile, name):
     """The FC1 + SwiGLU backward at full size (T=4096 top-2 of 8, K=4096,
-    N=14336, E4M3 row and column outputs 28672 wide): D, D_col and the scale
-    factors on sampled blocks, and dprob on every row of those blocks."""
+    N=14336, outputs 28672 wide; MXFP8 with E4M3 row and column outputs, or
+    the BF16 backend with a bfloat16 D_row): D (D_col and the scale factors) on
+    sampled blocks, and dprob on every row of those blocks."""
     import block_scaled_grouped_gb300 as bsgg
     from gpu_harness import alloc_outputs, check_float_d
-    p = W.workload("fc1_dswiglu", device="cuda")
+    p = W.workload(name, device="cuda")
     blocks = _sample_blocks(p)
     ref = _oracle(p, blocks)
     plan = bsgg.Plan(m_pad=p.m_pad, n=p.n, k=p.k, num_groups=p.num_groups, in_format=p.in_fmt,
