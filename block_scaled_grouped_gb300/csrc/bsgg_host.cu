@@ -286,9 +286,13 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
   // accumulator columns per thread and runs without register spills (measured
   // on GB300: 1418 TFLOP/s on the FC1 backward against 582 with 256 x 256
   // pairs, whose epilogue spills to local memory).
+  // The bfloat16 backward (no scale slots in tensor memory) holds two 256-column
+  // accumulators and reads them 32 columns at a time: pairs measured 1371
+  // TFLOP/s on the FC1 backward against 1215 for 128 x 256 and 907 for 128 x 128.
   const bool bwd = is_bwd_epi(desc->epilogue);
+  const bool pair_default = !bwd || desc->in_format == BSGG_IN_BF16;
   int tm = desc->tile_m, tn = desc->tile_n, cm = desc->cluster_m;
-  if (tm == 0) tm = (tn != 128 && cm != 1 && !bwd) ? 256 : 128;
+  if (tm == 0) tm = (tn != 128 && cm != 1 && pair_default) ? 256 : 128;
   if (tn == 0) tn = (bwd && tm == 128 && cm != 2) ? 128 : 256;
   if (cm == 0) cm = (tm == 256) ? 2 : 1;
   P->pair = (tm == 256);

@@ -186,7 +186,9 @@ struct Layout {
   static constexpr int kSfbBytes = kAtoms * kHalves * 512;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;   // one CTA's bytes
   static constexpr int kStages = (221184 / kStageBytes) > 8 ? 8 : (221184 / kStageBytes);
-  static constexpr int kNumAcc = (BN == 128) ? 2 : 1;
+  // two accumulators where they fit beside the scale slots: 128-column tiles,
+  // and 256-column tiles without scales (bfloat16 operands)
+  static constexpr int kNumAcc = (BN == 128 || !SCALED) ? 2 : 1;
   static constexpr int kSfaCols = kAtoms * 4;
   static constexpr int kSfbCols = kAtoms * kHalves * 4;
   static constexpr int kSfColsPerStage = kSfaCols + kSfbCols;
@@ -1163,6 +1165,12 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
     if constexpr (ST) setmaxnreg_inc<Ro::kHighRegs>();
     // ------------------------------------------------------------ epilogue
     constexpr int kWarpCols = BN / 2;                 // accumulator columns per warp
+    // 256-column tiles with two accumulators (bfloat16 operands, no scale
+    // slots): the warp reads its columns 32 at a time as it uses them and hands
+    // the accumulator back at the end of the tile, while the MMAs fill the
+    // other one.  Holding all 128 in registers spills the backward epilogue.
+    constexpr bool kChunkLd = NA == 2 && BN == 256;
+    static_assert(!kChunkLd || is_bwd_inst(EPI), "chunked accumulator reads: backward epilogues");
     const int q = warp & 3;                           // tensor-memory lane quadrant
     const int e = (warp - Ro::kEpiFirst) >> 2;        // which half of the columns
     const float norm = (OUTC == OUTC_FLOAT) ? 1.0f : *p.norm_const;
@@ -1197,18 +1205,27 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
       tc_fence_after();
       uint32_t r[kWarpCols];
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + e * kWarpCols;
+      const int acc_cur = acc;
+      auto release = [&]() {
+        // this warp is done with the accumulator: hand it back
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR) mbar_arrive_cluster(mapa_shared(acce_bar(acc_cur), 0));
+          else mbar_arrive(acce_bar(acc_cur));
+        }
+      };
+      if (!kChunkLd) {
 #pragma unroll
-      for (int c = 0; c < kWarpCols / 32; ++c) tmem_ld32p(taddr + 32 * c, &r[32 * c]);
-      tmem_wait_ld();
-      // this warp's columns are in registers: hand the accumulator back
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (PAIR) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));
-        else mbar_arrive(acce_bar(acc));
+        for (int c = 0; c < kWarpCols / 32; ++c) tmem_ld32p(taddr + 32 * c, &r[32 * c]);
+        tmem_wait_ld();
+        release();       // all of this warp's columns are in registers
       }
       if (++acc == NA) { acc = 0; acc_phase ^= 1u; }
-      if (!valid) continue;
+      if (!valid) {
+        if (kChunkLd) release();
+        continue;
+      }
       const int row = mt * kBM + q * 32 + lane;
       const float pr = p.prob[row];
       const float al = p.alpha[g];
@@ -1252,10 +1269,18 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
                     bt = (EPI == EPI_DSWIGLU && (p.bwd_kind == 0 || IC == IC_BF16)) ? p.beta[g] : 1.0f;
         const bool gf = p.gate_first != 0;
         float dprob_local = 0.0f;
-#pragma unroll
+        // chunked reads: one 32-column buffer; with dbias the loop stays rolled
+        // (unrolled, that instance spills 7 KB)
+        uint32_t rbuf[32];
+#pragma unroll((kChunkLd && XC) ? 1 : kWarpCols / 32)
         for (int c = 0; c < kWarpCols / 32; ++c) {
           const int j0 = nt * BN + e * kWarpCols + 32 * c;
           if (j0 >= p.n) continue;
+          if (kChunkLd) {
+            tmem_ld32p(taddr + 32 * c, rbuf);
+            tmem_wait_ld();
+          }
+          const uint32_t* rc = kChunkLd ? rbuf : &r[32 * c];
           const int xo = 2 * j0 + (gf ? 32 : 0), go = 2 * j0 + (gf ? 0 : 32);
           float x[32], gv[32];
           const int64_t srow = static_cast<int64_t>(row) * 2 * p.n;
@@ -1265,7 +1290,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
           if (EPI == EPI_DSWIGLU && p.bwd_kind == 0) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const float ref = al2 * __uint_as_float(r[32 * c + i]);
+              const float ref = al2 * __uint_as_float(rc[i]);
               const float X = bt * x[i], G = bt * gv[i];
               const float sg = __fdividef(1.0f, 1.0f + __expf(-G));
               const float sw = G * sg;
@@ -1281,7 +1306,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
             // which keeps its relative precision where tanh^2 rounds to 1
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const float ref = al2 * __uint_as_float(r[32 * c + i]);
+              const float ref = al2 * __uint_as_float(rc[i]);
               const float U = x[i], G = gv[i];
               const float yg = G / p.situ_b1, yu = U / p.situ_b2;
               const float thg = tanhf(yg), thu = tanhf(yu);
@@ -1302,7 +1327,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
             // bfloat16 operands: of beta C (the BF16 contract's X = beta C)
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const float ref = al2 * __uint_as_float(r[32 * c + i]);
+              const float ref = al2 * __uint_as_float(rc[i]);
               const float U = IC == IC_BF16 ? bt * x[i] : x[i], G = IC == IC_BF16 ? bt * gv[i] : gv[i];
               const float gc = fminf(G, p.clamp_max);
               const float uc = fminf(fmaxf(U, p.clamp_min), p.clamp_max);
@@ -1326,6 +1351,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
             add_column_sums32(gv, db + go, lane);
           }
         }
+        if (kChunkLd) release();
         atomicAdd(p.dprob + row, dprob_local);
       } else if (EPI == EPI_SWIGLU) {
         const bool gf = p.gate_first != 0;

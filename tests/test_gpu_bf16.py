@@ -18,8 +18,9 @@ from helpers import oracle_run, small_problem
 
 pytestmark = pytest.mark.gpu
 
-# the library's default (128 x 128 for the backward), 128 x 256, CTA pairs
-BF16_TILES = [(0, 0), (128, 256, 1, 1), (256, 256, 2, 1)]
+# the library's default (256 x 256 CTA pairs for the bfloat16 backward: two
+# accumulators read 32 columns at a time), 128 x 128, 128 x 256 (two accumulators)
+BF16_TILES = [(0, 0), (128, 128, 1, 1), (128, 256, 1, 1)]
 
 
 def _run(p, tile=(0, 0), gate_first=False, saved_fmt="bf16", discrete=False, with_dbias=True):
@@ -77,7 +78,7 @@ def test_bf16_saved_c_formats_and_f16_out(saved_fmt):
     _run(p, saved_fmt=saved_fmt)
 
 
-@pytest.mark.parametrize("tile", [(0, 0), (256, 256, 2, 1)], ids=tile_id)
+@pytest.mark.parametrize("tile", [(0, 0), (128, 128, 1, 1)], ids=tile_id)
 def test_bf16_discrete_equals_dense(tile):
     p = small_problem(counts=(0, 200, 129, 0), k=192, n=128, pad_to=128, in_fmt="bf16", epi="dgeglu",
                       out_fmt="bf16", seed=113)
