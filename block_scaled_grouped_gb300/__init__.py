@@ -59,7 +59,8 @@ def make_desc(*, m_pad: int, n: int, k: int, num_groups: int, in_format: str, ou
               saved_c_format: str = "bf16", rht_format: Optional[str] = None,
               dgeglu_params: Optional[tuple] = None, situ_betas: Optional[tuple] = None,
               rht_colwise: bool = False) -> "Desc":
-    """A bsgg_desc.  c_format ("bf16"/"f16") asks for the pre-activation C
+    """A bsgg_desc.  c_format ("bf16"/"f16"; with MXFP8 inputs also "f32",
+    "e4m3", "e5m2", "e2m1") asks for the pre-activation C
     output, bias_format ("bf16"/"f16"/"f32") for a bias; None = neither.
     discrete_b: per-expert weights through the b_ptrs / sfb_ptrs arrays.
     saved_c_format: storage type of the saved C read by the dSwiGLU backward.
@@ -230,7 +231,8 @@ class Plan:
         else:
             out["amax"] = 4 * d.num_groups * (2 if self.epilogue in BWD_EPILOGUES else 1)
         if self.c_format is not None:
-            out["c"] = d.m_pad * d.n * 2
+            bits = {"bf16": 16, "f16": 16, "f32": 32, "e4m3": 8, "e5m2": 8, "e2m1": 4}[self.c_format]
+            out["c"] = d.m_pad * d.n * bits // 8
         if self.rht_format == "bf16":
             out["rht"] = d.m_pad * self.n_out * 2
         elif self.rht_format == "e2m1":

@@ -155,7 +155,12 @@ bsgg_status validate(const bsgg_desc* d) {
   // C is stored as float16 or bfloat16; the bias is float16, bfloat16 or float32
   // ("Grouped GEMM + GLU + Hadamard + Quant (SM100)", Input/output tensors)
   if (d->want_c != 0 && d->want_c != 1) return BSGG_ERR_INVALID_ARG;
-  if (d->want_c && d->c_format != BSGG_OUT_BF16 && d->c_format != BSGG_OUT_F16) return BSGG_ERR_INVALID_ARG;
+  // C with FP8 inputs may also be float32, float8_e4m3fn, float8_e5m2 or
+  // float4_e2m1fn_x2 ("Grouped GEMM + SwiGLU (SM100)" and "Grouped GEMM + sReLU
+  // (SM100)", output tensor C; no scale factor: a saturating conversion)
+  if (d->want_c && d->c_format != BSGG_OUT_BF16 && d->c_format != BSGG_OUT_F16 &&
+      !(d->in_format <= BSGG_IN_MXFP8_E5M2 && d->c_format >= BSGG_OUT_F32 && d->c_format <= BSGG_OUT_E2M1))
+    return BSGG_ERR_INVALID_ARG;
   if (d->want_bias != 0 && d->want_bias != 1) return BSGG_ERR_INVALID_ARG;
   if (d->want_bias && d->bias_format != BSGG_OUT_BF16 && d->bias_format != BSGG_OUT_F16 &&
       d->bias_format != BSGG_OUT_F32)
@@ -719,7 +724,7 @@ bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* 
            uint64_t(d.m_pad) * (d.rht_format == BSGG_OUT_E2M1 ? P->n_out / 2 : P->n_out * 2)) &&
        d2h(d.want_rht && d.rht_format == BSGG_OUT_E2M1 ? host->sfrht : nullptr, dev->sfrht,
            d.want_rht == 2 ? uint64_t(d.m_pad) * P->n_out / 16 : sf_bytes_impl(d.m_pad, P->n_out, 16, 1)) &&
-       d2h(d.want_c ? host->c : nullptr, dev->c, uint64_t(d.m_pad) * d.n * 2);
+       d2h(d.want_c ? host->c : nullptr, dev->c, uint64_t(d.m_pad) * d.n * out_elem_bits(d.c_format) / 8);
   if (!ok) return BSGG_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return BSGG_ERR_CUDA;
   if (h2d_bytes) *h2d_bytes = in_bytes;

@@ -140,7 +140,7 @@ struct Params {
   const void* bias;         // (L, N), N contiguous, or null
   void* c_out;              // (m_pad, N) N-major, or null
   int32_t bias_kind;        // OK_BF16, OK_F16 or OK_F32
-  int32_t c_kind;           // OK_BF16 or OK_F16
+  int32_t c_kind;           // OK_BF16 or OK_F16; with MXFP8 inputs also OK_F32, OK_E4M3, OK_E5M2, OK_E2M1
   int32_t glu_kind;         // EPI_SWIGLU instances: 0 = SwiGLU, 1 = GeGLU
   float glu_limit;          // both GLU halves clamped to [-glu_limit, glu_limit]; 0 = none
   float glu_gamma;          // GLU output scale (1 = none)
@@ -460,6 +460,57 @@ __device__ __forceinline__ void store_q32(void* dst, const float (&v)[32], const
       w[i] = x;
     }
     st_v4(dst, w[0], w[1], w[2], w[3]);
+  }
+}
+
+// The stored pre-activation C of one row's 32-column chunk (fp32 bit patterns):
+// bf16 / f16 inline; f32, or, without a scale factor, the saturating
+// round-to-nearest FP8 / FP4 conversion of C itself, in a function of its own
+// (called only for those formats, so that the bias / C instances keep their
+// registers for the common bf16 / f16 C).
+struct C32 {
+  uint32_t v[32];
+};
+static __device__ __noinline__ void store_c32_wide(void* c_out, int64_t rc, int kind, C32 c) {
+  if (kind == OK_F32) {
+    uint32_t* dst = static_cast<uint32_t*>(c_out) + rc;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) st_v4(dst + 4 * i, c.v[4 * i], c.v[4 * i + 1], c.v[4 * i + 2], c.v[4 * i + 3]);
+  } else if (kind == OK_E2M1) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        x |= cvt_e2m1x2(__uint_as_float(c.v[8 * i + 2 * j]), __uint_as_float(c.v[8 * i + 2 * j + 1])) << (8 * j);
+      w[i] = x;
+    }
+    st_v4(static_cast<uint8_t*>(c_out) + rc / 2, w[0], w[1], w[2], w[3]);
+  } else {
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float a = __uint_as_float(c.v[4 * i]), b = __uint_as_float(c.v[4 * i + 1]);
+      const float d = __uint_as_float(c.v[4 * i + 2]), e = __uint_as_float(c.v[4 * i + 3]);
+      const uint32_t lo = kind == OK_E4M3 ? cvt_e4m3x2(a, b) : cvt_e5m2x2(a, b);
+      const uint32_t hi = kind == OK_E4M3 ? cvt_e4m3x2(d, e) : cvt_e5m2x2(d, e);
+      w[i] = lo | (hi << 16);
+    }
+    uint8_t* dst = static_cast<uint8_t*>(c_out) + rc;
+    st_v4(dst, w[0], w[1], w[2], w[3]);
+    st_v4(dst + 16, w[4], w[5], w[6], w[7]);
+  }
+}
+__device__ __forceinline__ void store_c32(const Params& p, const uint32_t* v, int row, int col0) {
+  const int64_t rc = static_cast<int64_t>(row) * p.n + col0;   // element offset
+  if (p.c_kind == OK_BF16 || p.c_kind == OK_F16) {
+    store_h32(static_cast<uint16_t*>(p.c_out) + rc, v, p.c_kind);
+  } else {
+    C32 c;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) c.v[i] = v[i];
+    store_c32_wide(p.c_out, rc, p.c_kind, c);
   }
 }
 
@@ -1250,9 +1301,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
                          static_cast<const uint8_t*>(p.bias) + (static_cast<int64_t>(g) * p.n + col0) * esz,
                          p.bias_kind);
             }
-            if (p.c_out != nullptr)
-              store_h32(static_cast<uint16_t*>(p.c_out) + static_cast<int64_t>(row) * p.n + col0, &r[32 * c],
-                        p.c_kind);
+            if (p.c_out != nullptr) store_c32(p, &r[32 * c], row, col0);
           }
         }
         al_epi = 1.0f;

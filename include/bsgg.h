@@ -164,7 +164,9 @@ typedef struct {
   float glu_alpha;        /* SWIGLU/GEGLU: output scale gamma; 0 (unset) or 1 = none; finite */
   int32_t want_c;         /* 1: also store C = alpha_g * acc (+ bias), before any clamp or
                              activation, (m_pad, N) N-major, in c_format */
-  int32_t c_format;       /* BSGG_OUT_BF16 or BSGG_OUT_F16 (when want_c) */
+  int32_t c_format;       /* BSGG_OUT_BF16 or BSGG_OUT_F16 (when want_c); with MXFP8 inputs
+                             also BSGG_OUT_F32, or BSGG_OUT_E4M3 / E5M2 / E2M1: C converted
+                             with round-to-nearest-even and saturation, no scale factor */
   int32_t want_bias;      /* 1: add bias_g[n] to C; bias is (L, N), N contiguous per expert
                              (the pages' (N, L) tensor with stride (1, N)) */
   int32_t bias_format;    /* BSGG_OUT_BF16, BSGG_OUT_F16 or BSGG_OUT_F32 (when want_bias) */

@@ -100,7 +100,9 @@ def _create(**over):
     (dict(glu_alpha=float("nan"), epilogue="swiglu"), 1),
     (dict(glu_limit=7.0, epilogue="gate"), 1),  # GLU options belong to the GLUs
     (dict(glu_alpha=2.0, epilogue="srelu"), 1),
-    (dict(c_format="f32"), 1), (dict(c_format_code=3), 1),    # C is bf16 or f16
+    # C is bf16 or f16 (with MXFP8 inputs also f32, e4m3, e5m2, e2m1)
+    (dict(c_format="f32", in_format="nvfp4"), 1), (dict(c_format_code=3, in_format="mxfp4"), 1),
+    (dict(c_format_code=6), 1),
     (dict(bias_format="e4m3"), 1), (dict(bias_format_code=9), 1),
     (dict(want_c_raw=2), 1),
     (dict(discrete_raw=2), 1),
@@ -140,6 +142,8 @@ def test_create_rejects(lib, over, code):
     dict(epilogue="geglu", n=128, glu_limit=7.0, glu_alpha=1.5),
     dict(epilogue="swiglu", glu_alpha=1.0, c_format="bf16", bias_format="f32"),
     dict(epilogue="srelu", glu_alpha=0.0, c_format="f16", bias_format="bf16"),
+    dict(epilogue="gate", c_format="f32"), dict(epilogue="swiglu", c_format="e4m3"),
+    dict(epilogue="srelu", c_format="e2m1", in_format="mxfp8_e5m2"),
     dict(epilogue="gate", bias_format="f16"),
     dict(discrete_b=True, num_groups=1024),
     dict(epilogue="dswiglu", n=96, saved_c_format="f32", out_format="e4m3", want_col=1),

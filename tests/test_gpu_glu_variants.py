@@ -50,10 +50,35 @@ def _run(p, tile, *, gate_first=False, glu_limit=0.0, glu_alpha=0.0, c_format=No
     compare(p, outs, ref)
     if "amax" in outs:
         np.testing.assert_allclose(outs["amax"].cpu().numpy(), ref["amax"], rtol=2.0 ** -10, atol=0)
-    if c_format is not None:
+    if c_format in ("bf16", "f16", "f32"):
         c = decode_float_out(outs["c"].cpu().numpy(), c_format, p.m_pad, p.n)
         check_float_d(c, ref["c_ref"], what="C")
+    elif c_format is not None:
+        _check_quantized_c(outs["c"].cpu().numpy(), ref["c_ref"], c_format, p.m_pad, p.n)
     return outs, ref
+
+
+def _check_quantized_c(raw, c_ref, fmt, m_pad, n):
+    """FP8 / FP4 C without a scale factor: the codes equal the oracle's
+    round-to-nearest-even saturating encoding of its fp64 C (rounded to fp32,
+    the precision the kernel converts from) on >= 99.9 % of the elements, and
+    every code decodes within one code step of C (the kernel's C is an fp32 sum
+    in another order)."""
+    import oracle as orc
+    code_fmt = {"e4m3": 0, "e5m2": 1, "e2m1": 2}[fmt]
+    if fmt == "e2m1":
+        codes = np.stack([raw & 0xF, raw >> 4], axis=-1).reshape(m_pad, n)
+    else:
+        codes = raw.reshape(m_pad, n)
+    rows = c_ref.shape[0]
+    want = np.array([[orc.encode_rne_satfinite(code_fmt, float(np.float32(x))) for x in r] for r in c_ref])
+    got = codes[:rows]
+    match = np.mean(got == want)
+    assert match >= 0.999, (fmt, match)
+    dec = np.vectorize(lambda c: orc.decode(code_fmt, int(c)))
+    g, w = dec(got), dec(want)
+    step = {"e4m3": 2.0 ** -3, "e5m2": 2.0 ** -2, "e2m1": 0.5}[fmt]
+    assert np.all(np.abs(g - w) <= step * np.maximum(np.abs(w), 1.0) + 1e-30)
 
 
 @pytest.mark.parametrize("gate_first", [False, True])
@@ -97,6 +122,16 @@ def test_nvfp4_geglu_e2m1_bias_and_c(tile):
     p = small_problem(counts=(150, 0, 300), k=512, n=512, pad_to=128, in_fmt="nvfp4", epi="geglu",
                       out_fmt="e2m1", want_col=True, seed=55)
     _run(p, tile, glu_limit=12.0, c_format="bf16", bias_format="bf16", seed=4)
+
+
+@pytest.mark.parametrize("c_format", ["f32", "e4m3", "e5m2", "e2m1"])
+@pytest.mark.parametrize("tile", [(128, 128, 1, 1), (256, 256, 2, 1)], ids=tile_id)
+def test_mxfp8_c_in_f32_fp8_and_fp4(tile, c_format):
+    # "Grouped GEMM + SwiGLU (SM100)" / "Grouped GEMM + sReLU (SM100)": with FP8
+    # inputs C may be f32, e4m3, e5m2 or e2m1 (no scale factor for C)
+    p = small_problem(counts=(130, 0, 256), k=256, n=256, pad_to=128, epi="swiglu", out_fmt="e4m3",
+                      seed=6)
+    _run(p, tile, c_format=c_format, bias_format="f32", seed=6)
 
 
 def test_bias_and_c_required_when_described():
