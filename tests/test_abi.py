@@ -189,3 +189,27 @@ def test_binding_structs_match_the_header():
     args = _struct_fields("bsgg_args")
     assert [n for _, _, n in args] == [n for n, _ in bsgg.Args._fields_]
     assert all(star == "*" for _, star, _ in args)
+
+
+def _enum_values(name):
+    """{enumerator: value} of the header's typedef enum `name` (explicit values)."""
+    src = open(HEADER).read()
+    end = src.index("} " + name + ";")
+    start = src.rindex("typedef enum {", 0, end)
+    body = re.sub(r"/\*.*?\*/", "", src[start + len("typedef enum {"):end], flags=re.S)
+    return {k: int(v) for k, v in re.findall(r"([A-Z0-9_]+)\s*=\s*(\d+)", body)}
+
+
+def test_binding_enums_match_the_header():
+    """The binding's format and epilogue names map to the header's values (the
+    descriptor carries them as plain integers), and the generator knows every
+    input format the binding does."""
+    from block_scaled_grouped_gb300 import workloads as W
+    ins = _enum_values("bsgg_in_format")
+    assert ins == {"BSGG_IN_" + k.upper(): v for k, v in bsgg.IN_FORMATS.items()}
+    outs = _enum_values("bsgg_out_format")
+    assert outs == {"BSGG_OUT_" + k.upper(): v for k, v in bsgg.OUT_FORMATS.items()}
+    epis = _enum_values("bsgg_epilogue")
+    assert epis == {"BSGG_EPI_" + k.upper(): v for k, v in bsgg.EPILOGUES.items()}
+    assert set(W.IN_FORMATS) == set(bsgg.IN_FORMATS)
+    assert set(W.EPILOGUES) == set(bsgg.EPILOGUES) and set(W.BWD_EPILOGUES) == set(bsgg.BWD_EPILOGUES)
