@@ -46,25 +46,38 @@ class OrcDesc(ctypes.Structure):
     ]
 
 
+def compile_source(src: str, out: str) -> None:
+    """Compile one copy of the oracle's source into a shared object with g++
+    (plain C++17, no intrinsics, no fast-math)."""
+    cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread",
+           "-ffp-contract=off", "-fno-fast-math", "-o", out, src]
+    subprocess.run(cmd, check=True)
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle with g++ (plain C++17, no intrinsics, no fast-math)."""
+    """Compile the oracle (``oracle/_build/liboracle.so``) unless it is current."""
     with _lock:
         if (not force and os.path.exists(_LIB_PATH)
                 and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
             return _LIB_PATH
         os.makedirs(_OUT_DIR, exist_ok=True)
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread",
-               "-ffp-contract=off", "-fno-fast-math", "-o", tmp, _SRC]
-        subprocess.run(cmd, check=True)
+        compile_source(_SRC, tmp)
         os.replace(tmp, _LIB_PATH)
         return _LIB_PATH
+
+
+def source_path() -> str:
+    return _SRC
 
 
 def lib():
     global _lib
     if _lib is None:
-        path = build()
+        # BSGG_ORACLE_LIB loads another build of this source instead: the
+        # mutation test of the pins runs them against copies that each carry
+        # one planted mistake.
+        path = os.environ.get("BSGG_ORACLE_LIB") or build()
         L = ctypes.CDLL(path)
         L.orc_decode.restype = ctypes.c_double
         L.orc_decode.argtypes = [ctypes.c_int, ctypes.c_uint32]

@@ -270,21 +270,48 @@ def _decode_sf(codes, in_fmt):
     return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(dt).double().numpy()
 
 
-@pytest.mark.parametrize("in_fmt,out_fmt,norm", [("mxfp8_e4m3", "e4m3", 1.0),
-                                                 ("mxfp8_e4m3", "e5m2", 0.5),
-                                                 ("mxfp8_e5m2", "e4m3", 2.0),
-                                                 ("mxfp8_e4m3", "e2m1", 1.0),
-                                                 ("nvfp4", "e2m1", 1.0),
-                                                 ("nvfp4", "e2m1", 2.0 ** -12)])
-def test_row_and_column_quantization_properties(in_fmt, out_fmt, norm):
-    want_col = in_fmt != "nvfp4"
-    p = _randomize_scales(small_problem(in_fmt=in_fmt, out_fmt=out_fmt, epi="srelu",
-                                        n=128, k=64, counts=(64, 40), pad_to=32,
-                                        norm_const=norm, want_col=want_col))
+def _check_scale(sf, target, in_fmt):
+    """The block scale's rounding rule: UE8M0 is the least power of two at or
+    above the target; an E4M3 scale is the nearest E4M3 value (half a step is
+    2^-4 relative), saturating at 448, and zero below half the smallest
+    subnormal 2^-9.  Returns "ok", "saturated" (the data saturate too) or
+    "zero" (the block is written as zeros)."""
+    if in_fmt != "nvfp4":
+        assert sf >= target * (1 - 1e-6) and sf / 2 < target * (1 + 1e-6)
+        return "ok"
+    if target >= 448.0:
+        assert sf == 448.0
+        return "saturated"
+    if sf == 0.0:
+        assert target <= 2.0 ** -10
+        return "zero"
+    assert abs(sf - target) <= target * 2 ** -4 + 2 ** -10
+    return "ok"
+
+
+# Signed D (gating) and non-negative D (sReLU); more than one 128-row tile of
+# the scale layout (m_pad 224), column blocks of 32 and of 16 rows.
+@pytest.mark.parametrize("in_fmt,out_fmt,norm,epi", [("mxfp8_e4m3", "e4m3", 1.0, "srelu"),
+                                                     ("mxfp8_e4m3", "e4m3", 1.0, "gate"),
+                                                     ("mxfp8_e4m3", "e5m2", 0.5, "srelu"),
+                                                     ("mxfp8_e5m2", "e4m3", 2.0, "gate"),
+                                                     ("mxfp8_e4m3", "e2m1", 1.0, "srelu"),
+                                                     ("nvfp4", "e2m1", 1.0, "srelu"),
+                                                     ("nvfp4", "e2m1", 1.0, "gate"),
+                                                     ("nvfp4", "e2m1", 2.0 ** -12, "srelu"),
+                                                     ("fp4_ue8m0_16", "e2m1", 1.0, "gate")])
+def test_row_and_column_quantization_properties(in_fmt, out_fmt, norm, epi):
+    p = _randomize_scales(small_problem(in_fmt=in_fmt, out_fmt=out_fmt, epi=epi,
+                                        n=128, k=64, counts=(100, 90), pad_to=32,
+                                        norm_const=norm, want_col=1))
+    assert p.m_pad > 128
     res = oracle_run(p)
     v = p.sf_vec
     qmax = {"e4m3": 448.0, "e5m2": 57344.0, "e2m1": 6.0}[out_fmt]
+    step = {"e4m3": 2 ** -3, "e5m2": 2 ** -2, "e2m1": 1.0 / 3.0}[out_fmt]
     D = res["d_ref"].astype(np.float32).astype(np.float64)
+    if epi == "gate":
+        assert (D < 0).any()
     nd = p.n_out
     rows = _rows_in_groups(p)
     # row blocks
@@ -298,39 +325,34 @@ def test_row_and_column_quantization_properties(in_fmt, out_fmt, norm):
             am = np.abs(blk).max()
             if am == 0:
                 continue
-            target = norm * am / qmax
-            if in_fmt != "nvfp4":
-                # UE8M0: the smallest power of two at or above the target
-                assert sfd[r, j] >= target * (1 - 1e-6) and sfd[r, j] / 2 < target * (1 + 1e-6)
-            else:
-                # E4M3 scale: round to nearest (half a step is 2^-4 relative),
-                # saturating at 448 -- then the data saturate too
-                if target >= 448.0:
-                    assert sfd[r, j] == 448.0
-                    continue
-                assert abs(sfd[r, j] - target) <= target * 2 ** -4 + 2 ** -10
+            kind = _check_scale(sfd[r, j], norm * am / qmax, in_fmt)
+            if kind == "zero":
+                assert np.all(Dq[r, j * v:(j + 1) * v] == 0)
+            if kind != "ok":
+                continue
             deq = Dq[r, j * v:(j + 1) * v] * sfd[r, j] / norm
             # within one output step of the block's scale (coarsest step at the top)
-            step = {"e4m3": 2 ** -3, "e5m2": 2 ** -2, "e2m1": 1.0 / 3.0}[out_fmt]
             assert np.all(np.abs(deq - blk) <= step * am + 1e-30)
-    if want_col:
-        Dc = _decode_out(res["d_col"], out_fmt)
-        for j in range(nd):
-            for b in range(p.m_pad // 32):
-                blk_rows = np.arange(b * 32, b * 32 + 32)
-                blk_rows = blk_rows[rows[blk_rows]]
-                if blk_rows.size == 0:
-                    continue
-                am = np.abs(D[blk_rows, j]).max()
-                sf = _decode_sf(np.array([res["sfd_col"][orc.sf_offset(j, b, 0, nd, p.m_pad // 32)]]),
-                                in_fmt)[0]
-                if am == 0:
-                    continue
-                target = norm * am / qmax
-                assert sf >= target * (1 - 1e-6) and sf / 2 < target * (1 + 1e-6)
-                deq = Dc[blk_rows, j] * sf / norm
-                step = {"e4m3": 2 ** -3, "e5m2": 2 ** -2, "e2m1": 1.0 / 3.0}[out_fmt]
-                assert np.all(np.abs(deq - D[blk_rows, j]) <= step * am + 1e-30)
+    # column blocks of v rows, SFD_col in SF(n_d, m_pad)
+    Dc = _decode_out(res["d_col"], out_fmt)
+    for j in range(nd):
+        for b in range(p.m_pad // v):
+            blk_rows = np.arange(b * v, b * v + v)
+            blk_rows = blk_rows[rows[blk_rows]]
+            if blk_rows.size == 0:
+                continue
+            am = np.abs(D[blk_rows, j]).max()
+            sf = _decode_sf(np.array([res["sfd_col"][orc.sf_offset(j, b, 0, nd, p.m_pad // v)]]),
+                            in_fmt)[0]
+            if am == 0:
+                continue
+            kind = _check_scale(sf, norm * am / qmax, in_fmt)
+            if kind == "zero":
+                assert np.all(Dc[blk_rows, j] == 0)
+            if kind != "ok":
+                continue
+            deq = Dc[blk_rows, j] * sf / norm
+            assert np.all(np.abs(deq - D[blk_rows, j]) <= step * am + 1e-30)
 
 
 @pytest.mark.parametrize("in_fmt", ["fp4_ue8m0_16", "mxfp4"])
