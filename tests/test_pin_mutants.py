@@ -14,7 +14,8 @@ the FP4 INPUTS changes nothing observable: both operands go through the same
 decoder, so every dot product only sees k permuted within a pair that shares
 one scale (the packed OUTPUT's nibble order is a case below).  A wrong size of
 a scale buffer writes out of bounds in the copy itself rather than giving a
-wrong value.
+wrong value; every planted index stays inside its buffer, so that a copy
+fails by its values and never by corrupting its own memory.
 
 The oracle in the repository is never modified: the mistakes live in
 temporary copies only.  A control case compiles the unmodified source through
@@ -68,6 +69,12 @@ MUTANTS = [
     ("alpha dropped", "(is_bwd(P) ? a * a : a) * acc", "(is_bwd(P) ? a * a : 1.0) * acc"),
     ("backward alpha not squared", "(is_bwd(P) ? a * a : a) * acc", "(is_bwd(P) ? a : a) * acc"),
     ("bias of group 0", "c += double(J.bias[g * P->n + n]);", "c += double(J.bias[n]);"),
+    ("bias scaled by alpha", "c += double(J.bias[g * P->n + n]);",
+     "c += double(J.alpha[g]) * double(J.bias[g * P->n + n]);"),
+    ("C stored before the bias",
+     "if (J.bias) c += double(J.bias[g * P->n + n]);\n      if (J.c_ref) J.c_ref[size_t((bi * 32 + i) * P->n + n)] = c;",
+     "if (J.c_ref) J.c_ref[size_t((bi * 32 + i) * P->n + n)] = c;\n      if (J.bias) c += double(J.bias[g * P->n + n]);"),
+    ("prob of the row within the block", "const double p = J.prob[m];", "const double p = J.prob[i];"),
     # -- forward epilogue (Step 2; SwiGLU, sReLU and GLU pages) --
     ("gating prob dropped", "d = p * Cv(j);", "d = Cv(j);"),
     ("sigmoid sign", "return 1.0 / (1.0 + std::exp(-x));", "return 1.0 / (1.0 + std::exp(x));"),
@@ -89,8 +96,8 @@ MUTANTS = [
     ("norm dropped from the scale factor", "const float sf = (norm * amax_blk) * rcp_max;",
      "const float sf = amax_blk * rcp_max;"),
     ("norm dropped from the data scale", "? 0.0f : norm / sfd;\n  return b;", "? 0.0f : 1.0f / sfd;\n  return b;"),
-    ("row SFD k-blocks of the column count", "J.sfd_row[sf_offset(m, jb / v, 0, P->m_pad, kb_row)]",
-     "J.sfd_row[sf_offset(m, jb / v, 0, P->m_pad, nd)]"),
+    ("row SFD of the first 128-row tile", "J.sfd_row[sf_offset(m, jb / v, 0, P->m_pad, kb_row)]",
+     "J.sfd_row[sf_offset(m % 128, jb / v, 0, P->m_pad, kb_row)]"),
     ("column amax without abs", "if (grp[size_t(i)] >= 0) am = std::max(am, std::fabs(Dv(i, j)));",
      "if (grp[size_t(i)] >= 0) am = std::max(am, Dv(i, j));"),
     ("column SFD of the tile's first block", "J.sfd_col[sf_offset(j, (m0 + ib) / v, 0, nd, kb_col)]",
@@ -113,12 +120,19 @@ MUTANTS = [
      "const int64_t e = nd * start + (t0 + t) * nd + j;"),
     ("colwise rht scales without the expert's segment offset", "J.sfrht[nd * start / 16 + sf_offset(",
      "J.sfrht[sf_offset("),
+    ("colwise rht q_max 4", "\n        const float sf = (norm * am) * float(1.0 / 6.0);",
+     "\n        const float sf = (norm * am) * float(1.0 / 4.0);"),
+    ("rowwise rht scale without rht_norm", "\n          const float sf = (norm * am) * float(1.0 / 6.0);",
+     "\n          const float sf = am * float(1.0 / 6.0);"),
     # -- backward (dGLU page) --
     ("dswiglu beta dropped", "return scale_c ? double(J.beta[g]) * c : c;", "return c;"),
     ("dswiglu d input without prob", "if (is_input) d = ref * p * (gt * sg);", "if (is_input) d = ref * (gt * sg);"),
     ("dswiglu d gate derivative", "else d = ref * p * x * sg * (1.0 + gt * (1.0 - sg));",
      "else d = ref * p * x * sg * (1.0 + gt * sg);"),
     ("dswiglu dprob without G", "+= x * (gt * orc_sigmoid(gt)) * Cv(jr);", "+= x * orc_sigmoid(gt) * Cv(jr);"),
+    ("saved C blocks ignore gate_first",
+     "const bool second = (gate != bool(P->gate_first));\n      const double c",
+     "const bool second = gate;\n      const double c"),
     ("backward blocks swapped", "const bool is_input = (second == bool(P->gate_first));",
      "const bool is_input = (second != bool(P->gate_first));"),
     ("backward amax halves swapped", "amax_idx = 2 * g + (is_input ? 0 : 1);", "amax_idx = 2 * g + (is_input ? 1 : 0);"),
