@@ -5,7 +5,8 @@
 * closed forms of SwiGLU, sReLU and the tanh soft clamp at chosen points;
 * invariants: zero prob, linearity in alpha, expert permutation, padding rows,
   empty groups;
-* the hand-worked example in tests/golden/hand_example.json;
+* the hand-worked examples in tests/golden/hand_example.json (MXFP8) and
+  tests/golden/hand_example_nvfp4.json (NVFP4);
 * defining properties of the block quantizer (scale is the power of two at or
   above norm*amax/q_max; dequantized values within one output step of D).
 """
@@ -136,6 +137,39 @@ def test_hand_worked_example():
     assert (res["sfd_row"][:orc.sf_bytes(m, 1, 1)].reshape(-1)[
         [orc.sf_offset(r, 0, 0, m, 1) for r in range(m)]] == e["sfd_code"]).all()
     assert (res["sfd_col"][[orc.sf_offset(c, 0, 0, n, 1) for c in range(n)]] == e["sfd_code"]).all()
+
+
+def test_hand_worked_nvfp4_example():
+    """tests/golden/hand_example_nvfp4.json: E2M1 data with E4M3 scales per 16
+    (two K blocks holding different values and scales), E2M1 output with
+    E4M3 row scales, 16-row column blocks and a round-to-nearest-even tie."""
+    g = json.load(open(os.path.join(GOLDEN, "hand_example_nvfp4.json")))
+    m, n, k = g["m"], g["n"], g["k"]
+    p = small_problem(counts=(m,), k=k, n=n, in_fmt="nvfp4", out_fmt="e2m1", pad_to=32,
+                      want_col=True, norm_const=g["norm_const"])
+    nib_a = np.repeat(np.array(g["a_codes_by_kblock"], dtype=np.uint8), 16)          # (k,)
+    a = nib_a[0::2] | (nib_a[1::2] << 4)
+    p.a = torch.from_numpy(np.tile(a, (m, 1)))
+    p.sfa_rows = torch.from_numpy(np.tile(np.array(g["sfa_by_kblock"], dtype=np.uint8), (1, m, 1)))
+    b_codes = np.concatenate([np.tile(np.array(blk, dtype=np.uint8), 4) for blk in g["b_pattern"]])  # (n,)
+    p.b = torch.from_numpy(np.repeat((b_codes | (b_codes << 4))[None, :, None], k // 2, axis=2))
+    p.sfb_rows = torch.full((1, n, k // 16), g["sfb_code"], dtype=torch.uint8)
+    p.alpha = torch.tensor([g["alpha"]])
+    p.prob = torch.full((m,), g["prob"])
+    res = oracle_run(p)
+    e = g["expected"]
+    per_col = lambda key: np.concatenate([np.tile(np.array(blk), 4) for blk in e[key]])
+    assert (res["d_ref"] == per_col("d_by_block")[None, :]).all()
+    unpack = lambda raw: np.stack([raw & 0xF, raw >> 4], axis=-1).reshape(m, n)
+    assert (unpack(res["d"].reshape(m, n // 2)) == per_col("dq_codes_by_block")[None, :]).all()
+    assert (unpack(res["d_col"].reshape(m, n // 2)) == per_col("dcol_codes_by_block")[None, :]).all()
+    for r in range(m):
+        for b in range(n // 16):
+            assert res["sfd_row"][orc.sf_offset(r, b, 0, m, n // 16)] == e["sfd_row_codes"][b]
+    sfd_col = per_col("sfd_col_codes_by_block")
+    for c in range(n):
+        for b in range(m // 16):
+            assert res["sfd_col"][orc.sf_offset(c, b, 0, n, m // 16)] == sfd_col[c]
 
 
 def test_swiglu_closed_forms_and_block_pairing():
