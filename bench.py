@@ -1,7 +1,7 @@
 """Benchmark of the grouped block-scaled GEMM on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gpu|reference]
-                    [--workload fc1_swiglu|fc2_gate|fine_nvfp4|skewed|fc1_dswiglu|fc1_dswiglu_bf16|tiny]
+                    [--workload fc1_swiglu|fc2_gate|fine_nvfp4|skewed|fc1_dswiglu|fc1_dswiglu_bf16|skinny|tiny]
 
 A step is one bsgg_run over one batch of the workload (all of the hot path:
 scheduling, operand fetch, block-scaled MMA, alpha/prob, activation,
@@ -271,6 +271,12 @@ def algorithmic_bytes(p) -> int:
             + extra)
 
 
+def roofline_bound(flops: float, alg_bytes: float, peak_tflops: float, peak_gbs: float) -> str:
+    """"tensor" when the launch's arithmetic intensity (valid FLOPs per
+    algorithmic byte) reaches the ridge point of the two peaks, else "hbm"."""
+    return "tensor" if flops / alg_bytes >= (peak_tflops * 1e12) / (peak_gbs * 1e9) else "hbm"
+
+
 def config_of(p, extra=None):
     c = {"workload": p.name, "experts": p.num_groups, "rows_valid": p.m_real, "rows_padded": p.m_pad,
          "n": p.n, "k": p.k, "in": DTYPE_NAME[p.in_fmt], "out": p.out_fmt, "epilogue": p.epi,
@@ -385,15 +391,23 @@ def run_gpu(args, world, rank, local):
     traffic = recorded_traffic(p.name) if not (args.tile or args.cluster) else None
     alg_bytes = algorithmic_bytes(p)
     hbm_gbs = alg_bytes / (elapsed_ms / args.steps * 1e-3) / 1e9
+    bound = roofline_bound(p.flops, alg_bytes, peak, peaks["hbm_gbs"])
     hbm = {"algorithmic_bytes": alg_bytes, "achieved_gbs": hbm_gbs, "peak_gbs": peaks["hbm_gbs"],
            "frac": hbm_gbs / peaks["hbm_gbs"],
-           "what": "algorithmic bytes per launch / kernel time (not the bound of this kernel)"}
+           "what": "algorithmic bytes per launch / kernel time" + (
+               " (not the bound of this kernel)" if bound == "tensor" else " (the bound of this kernel)")}
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": (f"{peak_kind} bf16 burst {peaks['bf16_tflops']} TFLOP/s x "
                                 f"{ratio:g} (nominal dense {DTYPE_NAME[p.in_fmt]}/bf16 ratio)"),
                 "kernel": "bsgg_kernel", "flops_per_launch": p.flops,
                 "flops_incl_padding": 2.0 * p.m_pad * p.n * p.k}
+    if bound == "hbm":
+        # below the ridge point (few rows per expert): the bound is the bytes
+        roofline.update({"bound": "hbm", "achieved": hbm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": hbm_gbs / peaks["hbm_gbs"],
+                         "peak_source": f"{peak_kind} HBM copy bandwidth {peaks['hbm_gbs']} GB/s",
+                         "bytes_per_launch": alg_bytes})
 
     # end to end through the host-buffer C-ABI call.  Headline: an MoE layer's
     # step -- the expert weights (B, SFB) and alpha stay resident in HBM, the

@@ -394,7 +394,8 @@ def build_problem(*, name: str, counts: Sequence[int], k: int, n: int, in_fmt: s
         a=a, sfa_rows=sfa, b=b, sfb_rows=sfb, saved_c=saved_c, beta=beta)
 
 
-WORKLOADS = ("tiny", "fc1_swiglu", "fc2_gate", "fine_nvfp4", "skewed", "fc1_dswiglu", "fc1_dswiglu_bf16")
+WORKLOADS = ("tiny", "fc1_swiglu", "fc2_gate", "fine_nvfp4", "skewed", "fc1_dswiglu", "fc1_dswiglu_bf16",
+             "skinny")
 
 
 def workload(name: str, device="cpu") -> Problem:
@@ -447,4 +448,16 @@ def workload(name: str, device="cpu") -> Problem:
         return build_problem(name=name, counts=counts, k=7168, n=4096, in_fmt="mxfp8_e4m3",
                              out_fmt="e4m3", epi="srelu", seed=4, device=device,
                              norm_const=0.5, want_col=True)
+    if name == "skinny":
+        # a decode-like step: 128 tokens routed top-8 over 64 experts (softmax of
+        # N(0,1) router logits), about 16 rows per expert, each group padded to
+        # 128 rows; the fine-grained layer's K = 7168, N = 2048 in MXFP8, gating,
+        # BF16 D + amax.  Every expert's weights are read for a few rows, so the
+        # launch is bound by HBM, not by the tensor cores.
+        T, L = 128, 64
+        tokens, probs = route_softmax_topk(T, L, 8, seed=7)
+        counts = [t.size for t in tokens]
+        return build_problem(name=name, counts=counts, k=7168, n=2048, in_fmt="mxfp8_e4m3",
+                             out_fmt="bf16", epi="gate", seed=7, device=device,
+                             token_rows=tokens, num_tokens=T, row_prob=probs)
     raise KeyError(name)
