@@ -41,10 +41,11 @@
  *      D, D_col (m_pad, N_out)  N-major; N_out = N/2 for SWIGLU/GEGLU, 2N for
  *                               the backward epilogues, else N;
  *                               bf16/f16/f32, or 1-byte FP8 codes, or packed FP4
- *      C        (m_pad, N)      N-major, bf16/f16 (optional pre-activation output)
+ *      C        (m_pad, N)      N-major, bf16/f16, with MXFP8 inputs also f32 or
+ *                               unscaled FP8/FP4 codes (optional pre-activation output)
  *      bias     (L, N)          N contiguous, bf16/f16/f32 (optional)
  *      SFD_row  swizzled SF(m_pad, N_out); SFD_col swizzled SF(N_out, m_pad)
- *      amax     float (L)
+ *      amax     float (L), 2L for the backward epilogues
  *    where SF(rows, cols) is the pages' (32, 4, ceil(rows/128), 4,
  *    ceil(ceil(cols/v)/4), L) layout in physical order (L, ceil(rows/128),
  *    ceil(ceil(cols/v)/4), 32, 4, 4) ("Grouped GEMM + SwiGLU (SM100)",
