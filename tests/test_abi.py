@@ -213,3 +213,20 @@ def test_binding_enums_match_the_header():
     assert epis == {"BSGG_EPI_" + k.upper(): v for k, v in bsgg.EPILOGUES.items()}
     assert set(W.IN_FORMATS) == set(bsgg.IN_FORMATS)
     assert set(W.EPILOGUES) == set(bsgg.EPILOGUES) and set(W.BWD_EPILOGUES) == set(bsgg.BWD_EPILOGUES)
+
+
+def test_noalloc_refuses_before_any_device_call(lib):
+    """bsgg_run_noalloc validates the description first, exactly as
+    bsgg_create does, and refuses what its static scratch cannot hold
+    (discrete weight mode's per-expert tensor maps) before it touches a
+    device; so these answers need no GPU."""
+    import ctypes
+    assert lib.bsgg_run_noalloc(None, None, None, 1) == 1
+    args = bsgg.Args()
+    for over, code in [(dict(m_pad=200), 1), (dict(num_groups=1025), 1),
+                       (dict(n=96, epilogue="swiglu"), 1), (dict(discrete_b=True), 2)]:
+        d = dict(m_pad=384, n=256, k=256, num_groups=2, in_format="mxfp8_e4m3", out_format="bf16",
+                 epilogue="gate")
+        d.update(over)
+        desc = bsgg.make_desc(**d)
+        assert lib.bsgg_run_noalloc(ctypes.byref(desc), ctypes.byref(args), None, 1) == code, over
