@@ -131,7 +131,10 @@ typedef enum {
 /* Problem description, fixed at plan creation (the pages' constructor +
  * check_support + compile, "Grouped GEMM + Quant (SM100)", Class API). */
 typedef struct {
-  int64_t m_pad;          /* rows of A/D/prob = padded_offsets[L-1]; multiple of 128 */
+  int64_t m_pad;          /* rows of A/D/prob = padded_offsets[L-1]; a positive multiple
+                             of 128 (a batch whose groups are all empty, m_pad = 0, is
+                             refused with BSGG_ERR_INVALID_ARG: the caller skips the call,
+                             and every amax of such a batch is 0) */
   int64_t n;              /* GEMM N (rows of each expert's B); multiple of 32 (64 for SWIGLU
                              and GEGLU); for DSWIGLU the compact gradient width (D is 2N wide) */
   int64_t k;              /* reduction length in elements; multiple of 16 (FP8) / 32 (FP4) */

@@ -78,6 +78,8 @@ def _create(**over):
 
 @pytest.mark.parametrize("over,code", [
     (dict(m_pad=200), 1),                       # groups are padded to 128 rows
+    (dict(m_pad=0), 1),                         # an all-empty batch: refused, no zero-row descriptors
+    (dict(m_pad=-128), 1),
     (dict(num_groups=0), 1), (dict(num_groups=1025), 1),   # L <= 1024
     (dict(k=40), 1),                            # 16-byte K-major rows
     (dict(k=48, in_format="nvfp4"), 1),         # FP4: K % 32
