@@ -52,6 +52,12 @@ MUTANTS = [
      "if (ax >= decode(fmt, top)) return sgn | (top + 1);"),
     ("ue8m0 one step up at exact powers", "int e = (m == 0.5) ? p - 1 : p;", "int e = p;"),
     ("ue8m0 rounds down", "int e = (m == 0.5) ? p - 1 : p;", "int e = p - 1;"),
+    ("e5m2 infinity decoded as NaN", "if (e == 0x1F) v = (m == 0) ? INFINITY : NAN;", "if (e == 0x1F) v = NAN;"),
+    ("ue8m0 0xFF decoded as a number", "return c == 0xFF ? NAN : std::ldexp(1.0, int(c) - 127);",
+     "return std::ldexp(1.0, int(c) - 127);"),
+    ("ue8m0 encoder overflows to the NaN code", "return uint32_t(std::min(254, std::max(0, code)));",
+     "return uint32_t(std::min(255, std::max(0, code)));"),
+    ("ue8m0 zero block encoded as 1.0", "if (!(sf > 0.0f)) return 0;", "if (!(sf > 0.0f)) return 127;"),
     # -- scale-factor layout ("Grouped GEMM + Quant (SM100)", Shapes) --
     ("sf layout i0/i1 swapped", "* 32 + i0) * 4 + i1) * 4 + i3;", "* 32 + i1) * 4 + i0) * 4 + i3;"),
     ("sf layout row/k tiles swapped", "return ((((l * R + i2) * KQ + i4)", "return ((((l * KQ + i4) * R + i2)"),
@@ -85,6 +91,8 @@ MUTANTS = [
     ("glu limit upper only on the gate", "gt = std::min(std::max(gt, -P->glu_limit), P->glu_limit);",
      "gt = std::min(gt, P->glu_limit);"),
     ("glu alpha dropped", "d *= P->glu_alpha;", "d *= 1.0;"),
+    ("glu limit upper only on the input", "x = std::min(std::max(x, -P->glu_limit), P->glu_limit);",
+     "x = std::min(x, P->glu_limit);"),
     ("srelu as square of |C|", "double r = c > 0.0 ? c : 0.0;", "double r = c > 0.0 ? c : -c;"),
     ("srelu clamp without s", "r = s * std::min(std::tanh(r / s), 1.0);", "r = std::min(std::tanh(r / s), 1.0);"),
     ("srelu prob inside the square", "d = p * orc_srelu(Cv(j), P->tanh_clamp_s);",
@@ -124,6 +132,10 @@ MUTANTS = [
      "\n        const float sf = (norm * am) * float(1.0 / 4.0);"),
     ("rowwise rht scale without rht_norm", "\n          const float sf = (norm * am) * float(1.0 / 6.0);",
      "\n          const float sf = am * float(1.0 / 6.0);"),
+    ("rowwise rht E2M1 nibbles swapped", "if ((jb + t) % 2 == 0) byte = uint8_t((byte & 0xF0) | (c & 0xF));",
+     "if ((jb + t) % 2 == 1) byte = uint8_t((byte & 0xF0) | (c & 0xF));"),
+    ("colwise rht E2M1 nibbles swapped", "if (e % 2 == 0) byte = uint8_t((byte & 0xF0) | (c & 0xF));",
+     "if (e % 2 == 1) byte = uint8_t((byte & 0xF0) | (c & 0xF));"),
     # -- backward (dGLU page) --
     ("dswiglu beta dropped", "return scale_c ? double(J.beta[g]) * c : c;", "return c;"),
     ("dswiglu d input without prob", "if (is_input) d = ref * p * (gt * sg);", "if (is_input) d = ref * (gt * sg);"),
@@ -143,6 +155,19 @@ MUTANTS = [
      "const double up_mask = 1.0;"),
     ("dsitu b1 dropped in the derivative", "+ b1 * th_g * sg * (1.0 - sg);", "+ th_g * sg * (1.0 - sg);"),
     ("dbias of group 0", "J.dbias[g * nd + j] += D[", "J.dbias[j] += D["),
+    ("dgeglu gate not clamped", "const double gc = std::min(gate, P->glu_clamp_max);", "const double gc = gate;"),
+    ("dgeglu up not clamped", "const double uc = std::min(std::max(up, P->glu_clamp_min), P->glu_clamp_max);",
+     "const double uc = up;"),
+    ("dgeglu gate mask dropped", "const double gate_mask = gate <= P->glu_clamp_max ? 1.0 : 0.0;",
+     "const double gate_mask = 1.0;"),
+    ("dgeglu dprob with prob", "dprob_term = ref * gc * s * (uc + P->linear_offset);",
+     "dprob_term = ref * p * gc * s * (uc + P->linear_offset);"),
+    ("dsitu up gradient without dT_u", "d_up = ref * p * t_g * dtu;", "d_up = ref * p * t_g;"),
+    ("dsitu sech^2 as 1 - tanh", "const double dtu = 1.0 - th_u * th_u;", "const double dtu = 1.0 - th_u;"),
+    ("dsitu dprob without T_u", "dprob_term = ref * t_g * t_u;", "dprob_term = ref * t_g;"),
+    ("bf16 dgeglu without beta",
+     "const bool scale_c = P->epi == EPI_DSWIGLU || (P->in_fmt == IN_BF16 && P->epi == EPI_DGEGLU);",
+     "const bool scale_c = P->epi == EPI_DSWIGLU;"),
     ("dswiglu beta of group 0", "return scale_c ? double(J.beta[g]) * c : c;",
      "return scale_c ? double(J.beta[0]) * c : c;"),
     ("saved C row stride n", "J.saved_c[m * 2 * P->n + 64 * b", "J.saved_c[m * P->n + 64 * b"),
