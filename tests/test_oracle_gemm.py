@@ -53,6 +53,29 @@ def test_gate_matches_brute_force(in_fmt):
     np.testing.assert_allclose(res["d_ref"][rows], want[rows], rtol=1e-12, atol=0)
 
 
+def test_1024_groups_mostly_empty_match_brute_force():
+    """The largest group count the pages allow (L = 1024), with a few
+    non-empty groups scattered among empty ones, some at either end: every
+    row takes its own expert's B, scales and alpha; per-group amax is the
+    maximum over the group's rows, 0 for an empty group."""
+    counts = np.zeros(1024, dtype=np.int64)
+    rng = np.random.default_rng(9)
+    for g in [0, 1, 517, 518, 900, 1023] + list(rng.choice(np.arange(2, 1023), 6, replace=False)):
+        counts[g] = int(rng.integers(1, 70))
+    p = _randomize_scales(small_problem(counts=tuple(int(c) for c in counts), k=64, n=64, seed=90))
+    res = oracle_run(p)
+    C = brute_force_C(p)
+    want = np_(p.prob)[:, None].astype(np.float64) * C
+    rows = _rows_in_groups(p)
+    np.testing.assert_allclose(res["d_ref"][rows], want[rows], rtol=1e-12, atol=0)
+    off = np_(p.padded_offsets)
+    start = 0
+    for g in range(1024):
+        blk = res["d_ref"][start:int(off[g])]
+        assert res["amax"][g] == (np.float32(np.abs(blk).astype(np.float32).max()) if blk.size else 0.0)
+        start = int(off[g])
+
+
 def test_nonsquare_operands_are_not_transposed():
     p = _randomize_scales(small_problem(counts=(40, 24), k=64, n=160))
     res = oracle_run(p)
