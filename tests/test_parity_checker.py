@@ -211,3 +211,22 @@ def test_bf16_nan_fails():
     d[10, 17] = np.nan
     with pytest.raises(AssertionError, match="out of tolerance"):
         compare(p, {"d": _bf16_bytes(d)}, ref)
+
+
+def test_sampled_blocks(e4m3_case):
+    """The full-size tests compare a GPU run with the oracle on a list of 32-row
+    blocks: the full outputs pass against the oracle's sampled run, and a
+    difference inside a sampled block fails (one outside it is not looked at)."""
+    p, full = e4m3_case
+    blocks = np.array([0, 4, 6], dtype=np.int64)
+    ref = oracle_run(p, blocks=blocks)
+    compare(p, _outs(full), ref, blocks=blocks)
+    for row, caught in [(4 * 32 + 3, True), (2 * 32 + 3, False)]:
+        j = int(np.argwhere((full["d"].reshape(p.m_pad, -1)[row] & 0x7F) >= 0x10)[0, 0])
+        outs = _outs(full)
+        outs["d"] = torch.from_numpy(_bump(full["d"].reshape(p.m_pad, -1), [(row, j)], 2).reshape(-1))
+        if caught:
+            with pytest.raises(AssertionError, match="steps off"):
+                compare(p, outs, ref, blocks=blocks)
+        else:
+            compare(p, outs, ref, blocks=blocks)
