@@ -13,8 +13,10 @@
 // epilogue in FP32; "Grouped GEMM + sReLU", section "Tanh soft clamp").
 //
 // Parity pins: every function here is pinned by tests/test_oracle_*.py against
-// closed forms, brute force, invariants and a hand-worked example.  No function
-// is "parity unpinned".  The one unpinned quantity is the *rate* of one-code
+// closed forms, brute force, invariants and hand-worked examples, and
+// tests/test_pin_mutants.py checks that those pins fail on copies of this file
+// with one plausible mistake planted in each.  No function is "parity
+// unpinned".  The one unpinned quantity is the *rate* of one-code
 // flips caused by the device's approximate tanh; the tolerance covers it.
 //
 // Where the pages are silent this file takes a reading of them, marked
