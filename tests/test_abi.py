@@ -232,3 +232,25 @@ def test_noalloc_refuses_before_any_device_call(lib):
         d.update(over)
         desc = bsgg.make_desc(**d)
         assert lib.bsgg_run_noalloc(ctypes.byref(desc), ctypes.byref(args), None, 1) == code, over
+
+
+def test_helper_entry_points_refuse_bad_arguments_before_any_device_call(lib):
+    """The helpers check their arguments on the host first, as the header
+    states, so these refusals need no GPU."""
+    import ctypes
+    out = ctypes.c_double(0.0)
+    # packer: null buffers, empty extents
+    assert lib.bsgg_pack_sf(None, None, 128, 4, 1, None) == 1
+    dummy = ctypes.c_void_p(16)          # never dereferenced: the extents are refused first
+    for rows, kb, sl in [(0, 4, 1), (128, 0, 1), (128, 4, 0), (-1, 4, 1)]:
+        assert lib.bsgg_pack_sf(dummy, dummy, rows, kb, sl, None) == 1
+    # scale-factor sizes of empty extents are 0
+    assert lib.bsgg_sf_bytes(0, 256, 32, 1) == 0 and lib.bsgg_sf_bytes(128, 256, 0, 1) == 0
+    # MMA-rate measurement: output pointer, tile_n, instruction count, input format
+    assert lib.bsgg_measure_mma_peak(0, 128, 1024, None, None) == 1
+    for fmt, tn, cnt in [(0, 192, 1024), (0, 128, 3), (0, 128, (1 << 22) + 1), (5, 128, 1024), (-1, 256, 1024)]:
+        assert lib.bsgg_measure_mma_peak(fmt, tn, cnt, ctypes.byref(out), None) == 1
+    # plan-taking entry points with no plan
+    assert lib.bsgg_run_host(None, None, None, None, None, None) == 1
+    assert lib.bsgg_debug_force_timeout(None, 1) == 1
+    assert lib.bsgg_launches_per_run(None) == -1
