@@ -5,7 +5,7 @@ source (a dropped term, a wrong sign, bias or index, a swapped operand or
 block, a rounding rule turned the wrong way), compiles the copy into a
 temporary shared object, and runs the oracle's pin suite
 (``tests/test_oracle_*.py``: closed forms, brute force, invariants, the
-hand-worked example, library decodings) against it in a subprocess.  The case
+hand-worked examples, library decodings) against it in a subprocess.  The case
 passes when the pin suite FAILS on the copy: a mistake that every pin lets
 through marks a part of the oracle whose pins are too weak.
 
