@@ -12,9 +12,13 @@ before timing; they are larger than L2, and steps run back to back.
 
 Metric: TFLOP/s of 2 * valid_rows * N * K (padding rows excluded).  The JSON
 line also carries the roofline of the kernel (against the measured bf16 peak
-scaled to the dtype by the nominal dense ratio), the end-to-end number through
-the host-buffer C-ABI call, the CPU oracle baseline, and the SM clocks sampled
-during the timed region.
+scaled to the dtype by the nominal dense ratio, and against this GPU's measured
+block-scaled MMA rate of the instruction form the launch issues), the
+end-to-end number through the host-buffer C-ABI call, the CPU oracle baseline,
+and the SM clocks sampled during the timed region.  After the headline
+workload the default run times every other hot-path workload (FC2 gated,
+fine-grained NVFP4, skewed, skinny, tiny) the same way, --extra-steps steps
+each, under the line's "workloads" key.
 
 N > 1 (torchrun): every rank runs an independent replica on its own GPU (the
 operation has no exchange step); value = all ranks' FLOPs / max rank time.
@@ -321,16 +325,56 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def run_gpu(args, world, rank, local):
+def mma_form(p, tile_arg: str):
+    """(tile_m, tile_n) of the MMA instruction form a launch of p issues: the
+    --tile given, else the library's default (CTA pairs, 256 x 256, except
+    128 x 128 single CTAs for the block-scaled backward epilogues)."""
+    if tile_arg:
+        tm, tn = (int(x) for x in tile_arg.split("x"))
+        return tm, tn
+    from block_scaled_grouped_gb300 import workloads as W
+    if p.epi in W.BWD_EPILOGUES and p.in_fmt != "bf16":
+        return 128, 128
+    return 256, 256
+
+
+_MMA_PEAK_CACHE = {}
+
+
+def measured_mma_peak(in_fmt: str, form):
+    """The block-scaled MMA rate of this GPU for the dtype and instruction form
+    (bsgg_measure_mma_peak_tile: operands resident in shared memory, no loads,
+    no epilogue), best of three, with the SM clock sampled meanwhile; None for
+    bfloat16 operands (no block-scaled form)."""
     import block_scaled_grouped_gb300 as bsgg
-    from block_scaled_grouped_gb300 import build as bsgg_build
-    bsgg_build.build()
-    dev = torch.device("cuda", local if world > 1 else 0)
-    t0 = time.time()
-    p = make_workload(args.workload, dev)
-    torch.cuda.synchronize()
-    log(f"[bench] workload {p.name}: m_pad={p.m_pad} valid={p.m_real} n={p.n} k={p.k} "
-        f"generated in {time.time() - t0:.1f}s")
+    probe = {"mxfp8_e4m3": "mxfp8_e4m3", "mxfp8_e5m2": "mxfp8_e4m3", "nvfp4": "nvfp4",
+             "fp4_ue8m0_16": "nvfp4", "mxfp4": "nvfp4"}.get(in_fmt)
+    if probe is None:
+        return None
+    key = (probe, tuple(form))
+    if key not in _MMA_PEAK_CACHE:
+        tm, tn = form
+        bsgg.measure_mma_peak_tile(probe, tm, tn, 1 << 16)          # warm-up
+        sampler = ClockSampler(torch.cuda.current_device())
+        sampler.start()
+        sampler.mark(True)
+        v = max(bsgg.measure_mma_peak_tile(probe, tm, tn, 1 << 21) for _ in range(3))
+        sampler.mark(False)
+        clocks = sampler.stop()
+        _MMA_PEAK_CACHE[key] = {"value": v, "unit": UNIT,
+                                "form": f"cta_group::{2 if tm == 256 else 1} M={tm} N={tn} "
+                                        f"({'kind::mxf4nvf4 K=64' if probe == 'nvfp4' else 'kind::mxf8f6f4 K=32'})",
+                                "sm_mhz": clocks.get("sm_mhz"), "reasons": clocks.get("reasons")}
+    return _MMA_PEAK_CACHE[key]
+
+
+def time_workload(p, args, dev, world, steps: int, warmup: int):
+    """Times `steps` back-to-back runs of one workload's launch after `warmup`
+    untimed ones (CUDA events on the launching stream, a barrier and a device
+    synchronize on both sides, SM clocks sampled meanwhile).  Returns the
+    record (value, ms_per_step, roofline, hbm, clocks, ...), the plan and the
+    tensors."""
+    import block_scaled_grouped_gb300 as bsgg
     tile = tuple(int(x) for x in args.tile.split("x")) if args.tile else (0, 0)
     cluster = tuple(int(x) for x in args.cluster.split("x")) if args.cluster else (0, 0)
     plan = bsgg.Plan(m_pad=p.m_pad, n=p.n, k=p.k, num_groups=p.num_groups, in_format=p.in_fmt,
@@ -354,11 +398,11 @@ def run_gpu(args, world, rank, local):
                        dprob=torch.zeros(p.m_pad, dtype=torch.float32, device=dev))
     stream = torch.cuda.current_stream(dev)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         plan.run(stream=stream, **tensors)
     st = plan.device_status(stream)
     if st != 0:
-        raise RuntimeError(f"device status {st} after warm-up")
+        raise RuntimeError(f"device status {st} after warm-up ({p.name})")
 
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.start()
@@ -367,7 +411,7 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize(dev)
     sampler.mark(True)
     ev0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         plan.run(stream=stream, **tensors)
     ev1.record(stream)
     torch.cuda.synchronize(dev)
@@ -377,20 +421,20 @@ def run_gpu(args, world, rank, local):
     elapsed_ms = ev0.elapsed_time(ev1)
     st = plan.device_status(stream)
     if st != 0:
-        raise RuntimeError(f"device status {st} after the timed region")
+        raise RuntimeError(f"device status {st} after the timed region ({p.name})")
     t_max_ms = max_over_ranks(elapsed_ms, world)
-    ms_per_step = t_max_ms / args.steps
-    value = world * args.steps * p.flops / (t_max_ms * 1e-3) / 1e12
+    ms_per_step = t_max_ms / steps
+    value = world * steps * p.flops / (t_max_ms * 1e-3) / 1e12
 
     # roofline of the (single) kernel of a step
     peaks, peak_kind = measured_peaks()
     ratio = DTYPE_RATIO[p.in_fmt]
     peak = peaks["bf16_tflops"] * ratio
-    achieved = p.flops / (elapsed_ms / args.steps * 1e-3) / 1e12
+    achieved = p.flops / (elapsed_ms / steps * 1e-3) / 1e12
     # the recorded counters are of the library's default tile shape
     traffic = recorded_traffic(p.name) if not (args.tile or args.cluster) else None
     alg_bytes = algorithmic_bytes(p)
-    hbm_gbs = alg_bytes / (elapsed_ms / args.steps * 1e-3) / 1e9
+    hbm_gbs = alg_bytes / (elapsed_ms / steps * 1e-3) / 1e9
     bound = roofline_bound(p.flops, alg_bytes, peak, peaks["hbm_gbs"])
     hbm = {"algorithmic_bytes": alg_bytes, "achieved_gbs": hbm_gbs, "peak_gbs": peaks["hbm_gbs"],
            "frac": hbm_gbs / peaks["hbm_gbs"],
@@ -402,12 +446,42 @@ def run_gpu(args, world, rank, local):
                                 f"{ratio:g} (nominal dense {DTYPE_NAME[p.in_fmt]}/bf16 ratio)"),
                 "kernel": "bsgg_kernel", "flops_per_launch": p.flops,
                 "flops_incl_padding": 2.0 * p.m_pad * p.n * p.k}
+    # the stricter denominator: this GPU's measured rate of the instruction form
+    # the launch issues
+    mma = measured_mma_peak(p.in_fmt, mma_form(p, args.tile))
+    if mma is not None:
+        roofline["measured_mma_peak"] = mma
+        roofline["frac_of_measured_mma"] = achieved / mma["value"]
     if bound == "hbm":
         # below the ridge point (few rows per expert): the bound is the bytes
         roofline.update({"bound": "hbm", "achieved": hbm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": hbm_gbs / peaks["hbm_gbs"],
                          "peak_source": f"{peak_kind} HBM copy bandwidth {peaks['hbm_gbs']} GB/s",
-                         "bytes_per_launch": alg_bytes})
+                         "bytes_per_launch": alg_bytes, "tflops": achieved})
+    rec = {"value": value, "unit": UNIT, "steps": steps, "warmup": warmup, "ms_per_step": ms_per_step,
+           "elapsed_ms": elapsed_ms, "clocks": clocks, "roofline": roofline, "hbm": hbm,
+           "pct_of_dtype_peak": 100.0 * achieved / peak, "config": config_of(p),
+           "gpu_launches": steps * plan.launches_per_run}
+    return rec, plan, tensors
+
+
+# the other workloads the default run also times (every hot-path config and the
+# decode-like skinny case), after the headline
+EXTRA_WORKLOADS = ("fc2_gate", "fine_nvfp4", "skewed", "skinny", "tiny")
+
+
+def run_gpu(args, world, rank, local):
+    import block_scaled_grouped_gb300 as bsgg
+    from block_scaled_grouped_gb300 import build as bsgg_build
+    bsgg_build.build()
+    dev = torch.device("cuda", local if world > 1 else 0)
+    t0 = time.time()
+    p = make_workload(args.workload, dev)
+    torch.cuda.synchronize()
+    log(f"[bench] workload {p.name}: m_pad={p.m_pad} valid={p.m_real} n={p.n} k={p.k} "
+        f"generated in {time.time() - t0:.1f}s")
+    rec, plan, tensors = time_workload(p, args, dev, world, args.steps, args.warmup)
+    stream = torch.cuda.current_stream(dev)
 
     # end to end through the host-buffer C-ABI call.  Headline: an MoE layer's
     # step -- the expert weights (B, SFB) and alpha stay resident in HBM, the
@@ -446,6 +520,30 @@ def run_gpu(args, world, rank, local):
                "all_inputs_copied": {"value": world * p.flops / all_s / 1e12, "unit": UNIT,
                                      "h2d_bytes_per_step": h2d_all, "d2h_bytes_per_step": d2h_all,
                                      "ms_per_step": all_s * 1e3}}
+        del host, host_layer, dev_bufs
+    plan.close()
+    gpu_launches = rec["gpu_launches"]
+    del tensors
+
+    # every other workload of the hot path, each timed the same way (its own
+    # warm-up, extra_steps steps), its tensors freed before the next one
+    workloads = {}
+    if not args.no_extra_workloads:
+        for name in EXTRA_WORKLOADS:
+            if name == p.name:
+                continue
+            t0 = time.time()
+            q = make_workload(name, dev)
+            torch.cuda.synchronize(dev)
+            log(f"[bench] workload {q.name}: m_pad={q.m_pad} valid={q.m_real} generated in "
+                f"{time.time() - t0:.1f}s")
+            r, qplan, qt = time_workload(q, args, dev, world, args.extra_steps, args.warmup)
+            qplan.close()
+            del qt, q
+            torch.cuda.empty_cache()
+            gpu_launches += r["gpu_launches"]
+            workloads[name] = {k_: r[k_] for k_ in ("value", "unit", "steps", "ms_per_step", "roofline",
+                                                    "hbm", "clocks", "pct_of_dtype_peak", "config")}
 
     cpu_baseline = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -456,18 +554,19 @@ def run_gpu(args, world, rank, local):
                                   f"{threads} threads"}
 
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        line = {"metric": METRIC, "value": rec["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": rec["ms_per_step"], "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[p.in_fmt],
                 "data": "synthetic (seeded MoE routing, N(0,1) draws quantized to the input format)",
                 "config": config_of(p, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                                         "tile": args.tile or "library default",
                                         "cluster": args.cluster or "library default"}),
-                "gpu_launches": args.steps * plan.launches_per_run, "clocks": clocks, "roofline": roofline,
-                "e2e": e2e, "cpu_baseline": cpu_baseline, "hbm": hbm,
-                "pct_of_dtype_peak": 100.0 * achieved / peak}
+                "gpu_launches": gpu_launches, "clocks": rec["clocks"], "roofline": rec["roofline"],
+                "e2e": e2e, "cpu_baseline": cpu_baseline, "hbm": rec["hbm"],
+                "pct_of_dtype_peak": rec["pct_of_dtype_peak"]}
+        if workloads:
+            line["workloads"] = workloads
         print(json.dumps(line), flush=True)
-    plan.close()
 
 
 def run_mma_peak():
@@ -478,14 +577,17 @@ def run_mma_peak():
     bsgg_build.build()
     sampler = ClockSampler(0)
     res = {}
+    forms = ((128, 128), (128, 256), (256, 256))      # cta_group::1 M=128; cta_group::2 M=256
     for fmt in ("mxfp8_e4m3", "nvfp4"):
-        for n in (128, 256):
-            bsgg.measure_mma_peak(fmt, n, 40000)          # warm-up
+        for tm, tn in forms:
+            bsgg.measure_mma_peak_tile(fmt, tm, tn, 40000)          # warm-up
     sampler.start()
     sampler.mark(True)
     for fmt in ("mxfp8_e4m3", "nvfp4"):
-        for n in (128, 256):
-            res[f"{DTYPE_NAME[fmt]} M=128 N={n}"] = max(bsgg.measure_mma_peak(fmt, n, 1 << 20) for _ in range(3))
+        for tm, tn in forms:
+            grp = 2 if tm == 256 else 1
+            res[f"{DTYPE_NAME[fmt]} cta_group::{grp} M={tm} N={tn}"] = max(
+                bsgg.measure_mma_peak_tile(fmt, tm, tn, 1 << 22) for _ in range(3))
     sampler.mark(False)
     clocks = sampler.stop()
     print(json.dumps({"metric": "dense block-scaled MMA TFLOP/s, operands resident in shared memory",
@@ -501,11 +603,13 @@ def main():
     ap.add_argument("--workload", default="fc1_swiglu")
     ap.add_argument("--tile", default="", help="MxN tile shape: 128x128, 128x256 or 256x256 "
                     "(a CTA pair); default: the library's choice")
-    ap.add_argument("--cluster", default="", help="MxN cluster shape: 1x1, or 2x1 (with 256x256 "
-                    "tiles the CTA pair, with 128x256 tiles two CTAs sharing an operand by TMA "
-                    "multicast); default: the library's choice")
+    ap.add_argument("--cluster", default="", help="MxN cluster shape: 1x1 (128-row tiles) or 2x1 "
+                    "(256x256 tiles on a CTA pair); default: the library's choice")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="time only --workload (by default the other hot-path workloads follow it)")
+    ap.add_argument("--extra-steps", type=int, default=20, help="timed steps of each other workload")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=0.0)
     ap.add_argument("--mma-peak", action="store_true", help="print the measured dense block-scaled "

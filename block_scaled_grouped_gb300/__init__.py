@@ -24,7 +24,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CU
 
 SYMBOLS = ("bsgg_create", "bsgg_run", "bsgg_run_host", "bsgg_query_device_status", "bsgg_destroy",
            "bsgg_status_string", "bsgg_sf_bytes", "bsgg_sf_offset", "bsgg_pack_sf", "bsgg_run_noalloc",
-           "bsgg_measure_mma_peak", "bsgg_debug_force_timeout", "bsgg_launches_per_run")
+           "bsgg_measure_mma_peak", "bsgg_measure_mma_peak_tile", "bsgg_debug_force_timeout",
+           "bsgg_launches_per_run")
 
 
 class BsggError(RuntimeError):
@@ -127,6 +128,9 @@ def lib():
         L.bsgg_measure_mma_peak.restype = ctypes.c_int
         L.bsgg_measure_mma_peak.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
                                             ctypes.POINTER(ctypes.c_double), ctypes.c_void_p]
+        L.bsgg_measure_mma_peak_tile.restype = ctypes.c_int
+        L.bsgg_measure_mma_peak_tile.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                                 ctypes.POINTER(ctypes.c_double), ctypes.c_void_p]
         L.bsgg_debug_force_timeout.restype = ctypes.c_int
         L.bsgg_debug_force_timeout.argtypes = [ctypes.c_void_p, ctypes.c_int32]
         L.bsgg_launches_per_run.restype = ctypes.c_int32
@@ -291,6 +295,16 @@ def measure_mma_peak(in_format: str, tile_n: int = 256, mmas_per_sm: int = 40000
     out = ctypes.c_double()
     _check(lib().bsgg_measure_mma_peak(IN_FORMATS[in_format], int(tile_n), int(mmas_per_sm),
                                        ctypes.byref(out), _stream(stream)), "bsgg_measure_mma_peak")
+    return float(out.value)
+
+
+def measure_mma_peak_tile(in_format: str, tile_m: int = 256, tile_n: int = 256, mmas: int = 400000,
+                          stream=None) -> float:
+    """bsgg_measure_mma_peak_tile: the same for the cta_group::1 (tile_m = 128)
+    or cta_group::2 (tile_m = 256, tile_n = 256, an SM pair) instruction form."""
+    out = ctypes.c_double()
+    _check(lib().bsgg_measure_mma_peak_tile(IN_FORMATS[in_format], int(tile_m), int(tile_n), int(mmas),
+                                            ctypes.byref(out), _stream(stream)), "bsgg_measure_mma_peak_tile")
     return float(out.value)
 
 

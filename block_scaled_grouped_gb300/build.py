@@ -17,8 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libbsgg.so")
-_SHAPES = ["mxf8_128", "mxf8_256", "mxf8_pair", "mxf8_mc", "nvf4_128", "nvf4_256", "nvf4_pair", "nvf4_mc",
-           "f4e8_128", "f4e8_256", "f4e8_pair"]
+_SHAPES = ["mxf8_128", "mxf8_256", "mxf8_pair", "nvf4_128", "nvf4_256", "nvf4_pair", "f4e8_128", "f4e8_256",
+           "f4e8_pair"]
 # forward and backward instances of each input family and tile shape in units
 # of their own, so that they compile in parallel
 UNITS = (["bsgg_host.cu", "bsgg_peak.cu"] + [f"bsgg_launch_{s}.cu" for s in _SHAPES] +

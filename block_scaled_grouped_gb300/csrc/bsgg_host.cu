@@ -21,7 +21,6 @@ struct bsgg_plan {
   int num_sms;
   int grid;                // CTAs per launch (a multiple of 2 for clusters)
   bool pair;               // 256 x 256 tiles on CTA pairs (2-CTA MMAs)
-  bool mc;                 // clusters of two 128 x 256 CTAs sharing an operand by TMA multicast
   int bn;
   int epi;
   int outc;
@@ -95,15 +94,17 @@ bsgg_status validate(const bsgg_desc* d) {
   if (d->tile_m == 256 && d->tile_n == 128) return BSGG_ERR_UNSUPPORTED;
   // cluster shape: the pages' cluster_shape_mn, powers of two <= 4 (both or
   // neither given); 2-CTA tiles need an even CLUSTER_M ("Grouped GEMM + Quant
-  // (SM100)", Tiling and Cluster).  Built: (1, 1) and (2, 1).
+  // (SM100)", Tiling and Cluster).  Built: (1, 1) with 128-row tiles and
+  // (2, 1) with 256 x 256 tiles (the CTA pair).  A (2, 1) cluster of 128-row
+  // tiles would share an operand tile between the two CTAs by TMA multicast;
+  // this library issues no multicast loads, so it is refused.
   auto pow2le4 = [](int v) { return v == 1 || v == 2 || v == 4; };
   if ((d->cluster_m == 0) != (d->cluster_n == 0)) return BSGG_ERR_INVALID_ARG;
   if (d->cluster_m != 0) {
     if (!pow2le4(d->cluster_m) || !pow2le4(d->cluster_n)) return BSGG_ERR_INVALID_ARG;
     if (d->tile_m == 256 && d->cluster_m % 2 != 0) return BSGG_ERR_INVALID_ARG;
     if (d->cluster_n != 1 || d->cluster_m > 2) return BSGG_ERR_UNSUPPORTED;
-    // a (2, 1) cluster of 1-CTA tiles is built for 128 x 256 tiles
-    if (d->cluster_m == 2 && d->tile_m != 256 && d->tile_n == 128) return BSGG_ERR_UNSUPPORTED;
+    if (d->cluster_m == 2 && (d->tile_m == 128 || d->tile_n == 128)) return BSGG_ERR_UNSUPPORTED;
   }
   if (d->num_groups < 1 || d->num_groups > 1024) return BSGG_ERR_INVALID_ARG;   // L <= 1024
   if (d->m_pad <= 0 || d->m_pad % 128 != 0 || d->m_pad > (int64_t(1) << 30)) return BSGG_ERR_INVALID_ARG;
@@ -130,11 +131,6 @@ bsgg_status validate(const bsgg_desc* d) {
   // Layouts and Strides): K % 16 for FP8, K % 32 for packed FP4, K % 8 for bf16.
   const bool fp4 = is_fp4_in(d->in_format), bf16_in = d->in_format == BSGG_IN_BF16;
   if (d->k % (fp4 ? 32 : bf16_in ? 8 : 16) != 0) return BSGG_ERR_INVALID_ARG;
-  // UE8M0-scaled FP4 and bfloat16 operands have kernel instances for single
-  // CTAs and CTA pairs only (one scale per 32 values reaches the MMA through
-  // the scale-store warps, which the multicast clusters do not have)
-  if ((is_f4e8_in(d->in_format) || bf16_in) && d->cluster_m == 2 && d->tile_m != 256)
-    return BSGG_ERR_UNSUPPORTED;
   // The BF16 backend ("Grouped GEMM + dGLU (SM100)", Backend dispatch and BF16
   // contract): dSwiGLU and dGeGLU with the source GeGLU constants, 16/32-bit
   // D_row, no D_col, scale factors or norm_const
@@ -221,8 +217,8 @@ bsgg_status encode_one(CUtensorMap* map, const void* base, int rank, const cuuin
 }
 
 // A (m_pad, K bytes) and B (L, N, K bytes) as 128-byte-swizzled boxes of
-// 128 K-bytes x 128 rows (64 in multicast clusters) / x (rows of B one load
-// moves: the tile's, half of it in clusters); the scale factors as
+// 128 K-bytes x 128 rows / x (rows of B one load moves: the tile's, half of it
+// in a CTA pair); the scale factors as
 // (256 bytes, 2 * atoms, 128-row blocks) so that one box moves a stage's
 // 512-byte atoms of one (SFA) or two (SFB, tile_n = 256) row blocks.
 bsgg_status encode_maps(const bsgg_plan* P, const bsgg_args* a, bsgg::Launch* L) {
@@ -236,8 +232,7 @@ bsgg_status encode_maps(const bsgg_plan* P, const bsgg_args* a, bsgg::Launch* L)
   {
     cuuint64_t dims[2] = {cuuint64_t(P->kbytes), cuuint64_t(d.m_pad)};
     cuuint64_t strides[1] = {cuuint64_t(P->kbytes)};
-    // multicast clusters move A as 64-row halves
-    cuuint32_t box[2] = {bsgg::kBKBytes, cuuint32_t(P->mc ? bsgg::kBM / 2 : bsgg::kBM)};
+    cuuint32_t box[2] = {bsgg::kBKBytes, cuuint32_t(bsgg::kBM)};
     if ((st = encode_one(&L->tmA, a->a, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) != BSGG_OK) return st;
   }
   // discrete weight mode: B and SFB maps of one expert (one slice) whose global
@@ -250,7 +245,7 @@ bsgg_status encode_maps(const bsgg_plan* P, const bsgg_args* a, bsgg::Launch* L)
   {
     cuuint64_t dims[3] = {cuuint64_t(P->kbytes), cuuint64_t(d.n), cuuint64_t(slices)};
     cuuint64_t strides[2] = {cuuint64_t(P->kbytes), cuuint64_t(P->kbytes * d.n)};
-    cuuint32_t box[3] = {bsgg::kBKBytes, cuuint32_t(P->pair || P->mc ? P->bn / 2 : P->bn), 1};
+    cuuint32_t box[3] = {bsgg::kBKBytes, cuuint32_t(P->pair ? P->bn / 2 : P->bn), 1};
     if ((st = encode_one(&L->tmB, b_base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) != BSGG_OK)
       return st;
   }
@@ -296,12 +291,13 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
   // TFLOP/s on the FC1 backward against 1215 for 128 x 256 and 907 for 128 x 128.
   const bool bwd = is_bwd_epi(desc->epilogue);
   const bool pair_default = !bwd || desc->in_format == BSGG_IN_BF16;
-  int tm = desc->tile_m, tn = desc->tile_n, cm = desc->cluster_m;
-  if (tm == 0) tm = (tn != 128 && cm != 1 && pair_default) ? 256 : 128;
-  if (tn == 0) tn = (bwd && tm == 128 && cm != 2) ? 128 : 256;
-  if (cm == 0) cm = (tm == 256) ? 2 : 1;
+  // a (2, 1) cluster is always a CTA pair (validation refuses it with 128-row
+  // or 128-column tiles)
+  int tm = desc->tile_m, tn = desc->tile_n;
+  const int cm = desc->cluster_m;
+  if (tm == 0) tm = (cm == 2 || (tn != 128 && cm != 1 && pair_default)) ? 256 : 128;
+  if (tn == 0) tn = (bwd && tm == 128) ? 128 : 256;
   P->pair = (tm == 256);
-  P->mc = (tm == 128 && cm == 2);
   P->bn = P->pair ? 256 : tn;
   // GeGLU runs in the SwiGLU instances (Params::glu_kind selects the activation)
   // the dGeGLU backward runs in the dSwiGLU instances (Params::bwd_kind)
@@ -319,8 +315,8 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
              : is_bwd_epi(desc->epilogue)                                             ? 2 * desc->n
                                                                                       : desc->n;
   P->out_row_bytes = P->n_out * out_elem_bits(desc->out_format) / 8;
-  if (P->pair || P->mc) {
-    int resident = bsgg::cluster_resident_ctas(fp4, P->mc);
+  if (P->pair) {
+    int resident = bsgg::cluster_resident_ctas(fp4);
     if (resident <= 0) resident = num_sms;
     P->grid = std::max(2, (std::min(resident, num_sms) / 2) * 2);
   } else {
@@ -425,6 +421,15 @@ __global__ void expert_maps_kernel(const __grid_constant__ CUtensorMap tB, const
 
 // Bytes of the discrete-mode workspace: two maps per expert and a flag word.
 size_t maps_bytes(int L) { return sizeof(CUtensorMap) * (2 * size_t(L) + 1); }
+
+// The status a device status word stands for.  A bit this library does not
+// define (it never writes one) reads as a CUDA error rather than as success.
+bsgg_status status_of_word(uint32_t w) {
+  if (w & bsgg::kStatusBadPointers) return BSGG_ERR_BAD_POINTERS;
+  if (w & bsgg::kStatusBadOffsets) return BSGG_ERR_BAD_OFFSETS;
+  if (w & bsgg::kStatusTimeout) return BSGG_ERR_DEVICE_TIMEOUT;
+  return w == 0 ? BSGG_OK : BSGG_ERR_CUDA;
+}
 
 }  // namespace
 
@@ -591,14 +596,13 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   p.force_timeout = P->force_timeout ? 1u : 0u;
   p.wait_limit_ns = P->force_timeout ? kTestWaitLimitNs : bsgg::kWaitLimitNs;
 
-  // an upper bound of the scheduling units (clusters may add one 256-row
-  // tile row per group)
-  const bool cl = P->pair || P->mc;
+  // an upper bound of the scheduling units (pairs may add one 256-row tile
+  // row per group)
+  const bool cl = P->pair;
   const int64_t rows = cl ? ceil_div(d.m_pad, 256) + d.num_groups : d.m_pad / bsgg::kBM;
   const int64_t tiles = rows * p.num_n_tiles;
   L.grid = static_cast<int>(std::min<int64_t>(P->grid, cl ? 2 * tiles : tiles));
   L.pair = P->pair;
-  L.mc = P->mc;
   L.bn = P->bn;
   L.epi = P->epi;
   L.outc = P->outc;
@@ -620,22 +624,18 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
           : P->bn == 256 ? bsgg::launch_f4e8_256_bwd(L) : bsgg::launch_f4e8_128_bwd(L);
     else if (d.in_format == BSGG_IN_NVFP4)
       e = P->pair ? bsgg::launch_nvf4_pair_bwd(L)
-          : P->mc ? bsgg::launch_nvf4_mc_bwd(L)
           : P->bn == 256 ? bsgg::launch_nvf4_256_bwd(L) : bsgg::launch_nvf4_128_bwd(L);
     else
       e = P->pair ? bsgg::launch_mxf8_pair_bwd(L)
-          : P->mc ? bsgg::launch_mxf8_mc_bwd(L)
           : P->bn == 256 ? bsgg::launch_mxf8_256_bwd(L) : bsgg::launch_mxf8_128_bwd(L);
   } else if (is_f4e8_in(d.in_format))
     e = P->pair ? bsgg::launch_f4e8_pair(L)
         : P->bn == 256 ? bsgg::launch_f4e8_256(L) : bsgg::launch_f4e8_128(L);
   else if (d.in_format == BSGG_IN_NVFP4)
     e = P->pair ? bsgg::launch_nvf4_pair(L)
-        : P->mc ? bsgg::launch_nvf4_mc(L)
         : P->bn == 256 ? bsgg::launch_nvf4_256(L) : bsgg::launch_nvf4_128(L);
   else
     e = P->pair ? bsgg::launch_mxf8_pair(L)
-        : P->mc ? bsgg::launch_mxf8_mc(L)
         : P->bn == 256 ? bsgg::launch_mxf8_256(L) : bsgg::launch_mxf8_128(L);
   return e == cudaSuccess ? BSGG_OK : BSGG_ERR_CUDA;
 }
@@ -658,10 +658,7 @@ bsgg_status bsgg_query_device_status(bsgg_plan* P, void* stream) {
   uint32_t w = 0;
   if (cudaMemcpy(&w, P->status, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return BSGG_ERR_CUDA;
   if (cudaMemset(P->status, 0, sizeof(w)) != cudaSuccess) return BSGG_ERR_CUDA;
-  if (w & bsgg::kStatusBadPointers) return BSGG_ERR_BAD_POINTERS;
-  if (w & bsgg::kStatusBadOffsets) return BSGG_ERR_BAD_OFFSETS;
-  if (w & bsgg::kStatusTimeout) return BSGG_ERR_DEVICE_TIMEOUT;
-  return BSGG_OK;
+  return status_of_word(w);
 }
 
 bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* dev, void* stream,
@@ -751,13 +748,42 @@ constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[kNoAllocMaxDevices];
 int g_noalloc_sms[kNoAllocMaxDevices];
+unsigned long long g_noalloc_ctx[kNoAllocMaxDevices];   // id of the context the address belongs to
 
-// Once per device, with that device current: the array's device address (a
-// host-side reference to the array is only a stand-in, never a device
-// pointer) and the SM count.
+// Unique id of the current context (driver cuCtxGetCurrent + cuCtxGetId,
+// reached through the runtime's entry-point query), 0 if unavailable.  A
+// context reset (cudaDeviceReset) gives the device a new context and a new id.
+unsigned long long current_ctx_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Once per device (and again after that device's context was reset), with the
+// device current: the array's device address (a host-side reference to the
+// array is only a stand-in, never a device pointer) and the SM count.
 bsgg_status noalloc_setup(int dev, uint32_t** scratch, int* sms) {
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
+  const unsigned long long ctx = current_ctx_id();
+  if (!g_noalloc_addr[dev] || (ctx != 0 && ctx != g_noalloc_ctx[dev])) {
     void* addr = nullptr;
     if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr)
       return BSGG_ERR_CUDA;
@@ -766,6 +792,8 @@ bsgg_status noalloc_setup(int dev, uint32_t** scratch, int* sms) {
       return BSGG_ERR_CUDA;
     g_noalloc_sms[dev] = n;
     g_noalloc_addr[dev] = addr;
+    // the symbol lookup made the runtime's context current if it was not yet
+    g_noalloc_ctx[dev] = ctx != 0 ? ctx : current_ctx_id();
   }
   *scratch = static_cast<uint32_t*>(g_noalloc_addr[dev]);
   *sms = g_noalloc_sms[dev];
@@ -803,7 +831,5 @@ extern "C" bsgg_status bsgg_run_noalloc(const bsgg_desc* desc, const bsgg_args* 
   if (cudaMemcpyAsync(&w, scratch, sizeof(w), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess)
     return BSGG_ERR_CUDA;
-  if (w & bsgg::kStatusBadOffsets) return BSGG_ERR_BAD_OFFSETS;
-  if (w & bsgg::kStatusTimeout) return BSGG_ERR_DEVICE_TIMEOUT;
-  return BSGG_OK;
+  return status_of_word(w);
 }

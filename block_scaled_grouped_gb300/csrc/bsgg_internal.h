@@ -18,7 +18,6 @@ struct Launch {
   int grid;      // CTAs (a multiple of 2 for clusters)
   int bn;        // 128 or 256
   bool pair;     // 256 x 256 tiles on a CTA pair
-  bool mc;       // clusters of two 128 x 256 CTAs sharing an operand by multicast
   int epi;
   int outc;
   cudaStream_t stream;
@@ -29,11 +28,9 @@ struct Launch {
 cudaError_t launch_mxf8_128(const Launch& L);
 cudaError_t launch_mxf8_256(const Launch& L);
 cudaError_t launch_mxf8_pair(const Launch& L);
-cudaError_t launch_mxf8_mc(const Launch& L);
 cudaError_t launch_nvf4_128(const Launch& L);
 cudaError_t launch_nvf4_256(const Launch& L);
 cudaError_t launch_nvf4_pair(const Launch& L);
-cudaError_t launch_nvf4_mc(const Launch& L);
 cudaError_t launch_f4e8_128(const Launch& L);
 cudaError_t launch_f4e8_256(const Launch& L);
 cudaError_t launch_f4e8_pair(const Launch& L);
@@ -41,19 +38,17 @@ cudaError_t launch_f4e8_pair(const Launch& L);
 cudaError_t launch_mxf8_128_bwd(const Launch& L);
 cudaError_t launch_mxf8_256_bwd(const Launch& L);
 cudaError_t launch_mxf8_pair_bwd(const Launch& L);
-cudaError_t launch_mxf8_mc_bwd(const Launch& L);
 cudaError_t launch_nvf4_128_bwd(const Launch& L);
 cudaError_t launch_nvf4_256_bwd(const Launch& L);
 cudaError_t launch_nvf4_pair_bwd(const Launch& L);
-cudaError_t launch_nvf4_mc_bwd(const Launch& L);
 cudaError_t launch_f4e8_128_bwd(const Launch& L);
 cudaError_t launch_f4e8_256_bwd(const Launch& L);
 cudaError_t launch_f4e8_pair_bwd(const Launch& L);
 cudaError_t launch_bf16_128_bwd(const Launch& L);
 cudaError_t launch_bf16_256_bwd(const Launch& L);
 cudaError_t launch_bf16_pair_bwd(const Launch& L);
-// Largest number of CTAs of the pair (mc = false) or multicast-cluster kernel
-// that can be resident at once (clusters x 2) on the current device, 0 if unknown.
-int cluster_resident_ctas(bool fp4, bool mc);
+// Largest number of CTAs of the CTA-pair kernel that can be resident at once
+// (clusters x 2) on the current device, 0 if unknown.
+int cluster_resident_ctas(bool fp4);
 
 }  // namespace bsgg

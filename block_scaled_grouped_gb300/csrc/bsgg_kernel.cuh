@@ -2,17 +2,9 @@
 //
 // Tiles never straddle two expert groups because groups are padded to
 // multiples of 128 rows ("Grouped GEMM + Quant (SM100)", Tiling and Cluster:
-// tiles must not span groups).  Three cluster modes (CM) share this file:
+// tiles must not span groups).  Two cluster modes (CM) share this file:
 //   * single (CM_SINGLE): one CTA computes a 128 x BN tile (BN = 128 or 256)
 //     with tcgen05 .cta_group::1 MMAs.
-//   * multicast cluster (CM_MC, BN = 256): a cluster of two CTAs, each
-//     computing its own 128 x 256 tile with .cta_group::1 MMAs, shares one
-//     operand through TMA multicast: two m-tiles of one n-tile (each CTA loads
-//     half of the common B tile into both CTAs), or, for the last m-tile of a
-//     group with an odd count, two n-tiles of that m-tile (each CTA loads half
-//     of the common A tile).  A stage is refilled only after both CTAs'
-//     MMAs released it.  Two thirds (B shared) or five sixths (A shared) of
-//     the L2-to-SM bytes of a single CTA; no odd-half recomputation.
 //   * CTA pair (CM_PAIR, BN = 256): a cluster of two CTAs computes a
 //     256 x 256 tile with .cta_group::2 MMAs: each CTA loads its own 128 rows
 //     of A and half of the 256 rows of B, both CTAs hold all 256 columns' B
@@ -20,6 +12,7 @@
 //     receives its 128 rows of D.  Half the operand bytes per FLOP of 1-CTA
 //     tiles.  A group with an odd number of 128-row tiles ends in a pair tile
 //     whose odd half recomputes the even half's rows and stores nothing.
+//     Every TMA load of a CTA writes only that CTA's own shared memory.
 // Warp roles.  Eleven warps (352 threads) when the scale factors are copied:
 //   warp 0      TMA producer: A, B[g] (128-byte swizzle) and the scale-factor
 //               atoms (512-byte boxes) into a multi-stage ring; in a pair both
@@ -35,8 +28,7 @@
 //               half into registers (then the accumulator is released), alpha,
 //               the activation and prob (Step 2), per-group amax or the row /
 //               column block quantization (Step 3), global stores
-// NVFP4 single-CTA tiles and CTA pairs (sixteen warps, 512 threads) store
-// the scales instead: the copies of an NVFP4 stage's twelve atoms held the
+// FP4 inputs (sixteen warps, 512 threads) store the scales instead: the copies of an NVFP4 stage's twelve atoms held the
 // tensor pipe back.  Warps 0 and 1 as above; warps 2..5 write the scales with
 // tcgen05.st, one per lane quadrant, A's atoms without the copy path's
 // four-fold replication (in a pair each CTA's warps write its own tensor
@@ -75,13 +67,13 @@ enum : int { OK_BF16 = 0, OK_F16 = 1, OK_F32 = 2, OK_E4M3 = 3, OK_E5M2 = 4, OK_E
 constexpr int kBM = 128;          // rows per CTA tile (TMEM lanes)
 constexpr int kBKBytes = 128;     // K bytes per pipeline stage (one 128-byte swizzle span)
 constexpr int kEpiWarps = 8;      // two warps per tensor-memory lane quadrant
-enum : int { CM_SINGLE = 0, CM_PAIR = 1, CM_MC = 2 };
+enum : int { CM_SINGLE = 0, CM_PAIR = 1 };
 // Scale factors reach tensor memory by tcgen05.st from four warps (one per
-// lane quadrant) for NVFP4 single-CTA tiles and pairs, by tcgen05.cp from one
-// thread otherwise (see the kernel's role table).  Measured on GB300: stores
-// raise NVFP4 by 19 % (single) and 14 % (pairs) and lower MXFP8 pairs by 17 %.
-template <bool FP4, int CM>
-constexpr bool scale_stores() { return FP4 && CM != CM_MC; }
+// lane quadrant) for FP4 inputs, by tcgen05.cp from one thread otherwise (see
+// the kernel's role table).  Measured on GB300: stores raise NVFP4 by 19 %
+// (single) and 14 % (pairs) and lower MXFP8 pairs by 17 %.
+template <bool FP4>
+constexpr bool scale_stores() { return FP4; }
 template <bool ST>
 struct Roles {
   static constexpr int kThreads = ST ? 512 : 96 + 32 * kEpiWarps;
@@ -217,13 +209,11 @@ __device__ __forceinline__ int64_t sf_off(int64_t row, int64_t kblk, int64_t kq)
   return ((row >> 7) * kq + (kblk >> 2)) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (kblk & 3);
 }
 
-// Scheduling units of a group with mt 128-row tiles and ntn n-tiles: tiles
-// (single), 256-row tile rows (pair; x ntn) or cluster tiles (multicast).
+// Scheduling units of a group with mt 128-row tiles: tiles (single) or
+// 256-row tile rows (pair).
 template <int CM>
-__device__ __forceinline__ int group_units(int mt, int ntn) {
-  if (CM == CM_PAIR) return (mt + 1) / 2;
-  if (CM == CM_MC) return (mt / 2) * ntn + ((mt & 1) ? (ntn + 1) / 2 : 0);
-  return mt;
+__device__ __forceinline__ int group_units(int mt) {
+  return CM == CM_PAIR ? (mt + 1) / 2 : mt;
 }
 
 // Tile t of the static schedule -> (group, this CTA's 128-row tile, n-tile).
@@ -235,48 +225,11 @@ __device__ __forceinline__ int group_units(int mt, int ntn) {
 // while the group's rows pass over it.  Empty groups own no tiles.  `valid` is
 // false only for the odd half of a pair tile past the group's last row; that
 // half then reuses the even half's rows (m_load) and stores nothing.
-//
-// Multicast clusters: t is a cluster tile and s_trow the prefix of
-// group_units<CM_MC>.  A group's first (mt / 2) * ntn cluster tiles pair
-// m-tiles (2i, 2i + 1) on one n-tile (B shared; banded like the other modes);
-// an odd group's last m-tile then takes n-tiles (2j, 2j + 1) (A shared).  For
-// an odd ntn the last of those has no second n-tile: that CTA loads the
-// group's last n-tile again and stores nothing (valid = false).
 template <int CM>
 __device__ __forceinline__ void decode_tile(int t, const Params& p, const int32_t* s_off, const int32_t* s_trow,
-                                            uint32_t rank, int& g, int& m_load, int& n_tile, bool& valid,
-                                            bool& share_b) {
+                                            uint32_t rank, int& g, int& m_load, int& n_tile, bool& valid) {
   constexpr bool PAIR = CM == CM_PAIR;
   const int ntn = p.num_n_tiles;
-  share_b = true;
-  if (CM == CM_MC) {
-    int lo = 0, hi = p.L;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (s_trow[mid] > t) hi = mid; else lo = mid + 1;
-    }
-    g = lo;
-    const int r = t - (g ? s_trow[g - 1] : 0);
-    const int m0 = (g ? s_off[g - 1] : 0) / kBM;
-    const int mtg = s_off[g] / kBM - m0;
-    const int pairs = mtg / 2;
-    if (r < pairs * ntn) {
-      const int W = p.raster_w;
-      const int band = r / (pairs * W);
-      const int w = min(W, ntn - band * W);
-      const int rr = r - band * pairs * W;
-      n_tile = band * W + rr % w;
-      m_load = m0 + 2 * (rr / w) + static_cast<int>(rank);
-      valid = true;
-    } else {
-      const int nt = 2 * (r - pairs * ntn) + static_cast<int>(rank);
-      valid = nt < ntn;
-      n_tile = valid ? nt : ntn - 1;
-      m_load = m0 + mtg - 1;
-      share_b = false;
-    }
-    return;
-  }
   const int u = t / ntn;
   int lo = 0, hi = p.L;
   while (lo < hi) {
@@ -780,24 +733,19 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* 
 // output; a backward launch accumulates dbias (separate instances, so that the
 // register budget of the plain epilogue is untouched).
 template <int IC, int BN, int CM, int EPI, int OUTC, bool XC>
-__global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThreads, 1)
+__global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC)>()>::kThreads, 1)
     bsgg_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                 const __grid_constant__ Params p) {
   constexpr bool FP4 = ic_fp4(IC);
   constexpr bool SCALED = ic_scaled(IC);
-  static_assert(IC != IC_F4E8 || CM != CM_MC, "UE8M0-scaled FP4 needs the scale stores");
-  static_assert(SCALED || CM != CM_MC, "bfloat16 operands run on single CTAs and pairs");
   constexpr bool PAIR = CM == CM_PAIR;
-  constexpr bool MC = CM == CM_MC;
   constexpr bool CLUSTER = CM != CM_SINGLE;
-  static_assert(!MC || BN == 256, "multicast clusters use 128 x 256 tiles");
-  constexpr bool ST = scale_stores<FP4, CM>();
+  constexpr bool ST = scale_stores<FP4>();
   using Ro = Roles<ST>;
   using Ly = Layout<FP4, BN, PAIR, SCALED>;
   constexpr int S = Ly::kStages;
   constexpr int NA = Ly::kNumAcc;
-  constexpr uint32_t kABytesHalf = Ly::kABytes / 2;   // one 64-row A box (multicast clusters)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -828,8 +776,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
 
   for (int i = tid; i < p.L; i += Ro::kThreads) s_off[i] = p.offsets[i];
   if (tid == 0) {
-    // multicast clusters: a stage is free once both CTAs' MMAs released it
-    for (int s = 0; s < S; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), MC ? 2 : 1); }
+    for (int s = 0; s < S; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
     for (int a = 0; a < NA; ++a) {
       mbar_init(accf_bar(a), 1);
       mbar_init(acce_bar(a), PAIR ? 2 * kEpiWarps : kEpiWarps);
@@ -873,7 +820,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
     int local = 0;
     for (int g = g0; g < g1; ++g) {
       const int mt = (s_off[g] - (g ? s_off[g - 1] : 0)) / kBM;
-      local += group_units<CM>(mt, p.num_n_tiles);
+      local += group_units<CM>(mt);
     }
     int incl = local;
 #pragma unroll
@@ -884,12 +831,12 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
     int run = incl - local;
     for (int g = g0; g < g1; ++g) {
       const int mt = (s_off[g] - (g ? s_off[g - 1] : 0)) / kBM;
-      run += group_units<CM>(mt, p.num_n_tiles);
+      run += group_units<CM>(mt);
       s_trow[g] = run;
     }
   }
   __syncthreads();
-  const int num_tiles = bad ? 0 : s_trow[p.L - 1] * (MC ? 1 : p.num_n_tiles);
+  const int num_tiles = bad ? 0 : s_trow[p.L - 1] * p.num_n_tiles;
 
   if (bad) {
     // (bad pointers were reported by the kernel that wrote the maps)
@@ -911,8 +858,8 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
         int fenced_g = -1;
         for (int t = unit; t < num_tiles && ok; t += num_units) {
           int g, mt, nt;
-          bool valid, share_b;
-          decode_tile<CM>(t, p, s_off, s_trow, rank, g, mt, nt, valid, share_b);
+          bool valid;
+          decode_tile<CM>(t, p, s_off, s_trow, rank, g, mt, nt, valid);
           const int b_row = nt * BN + (PAIR ? static_cast<int>(rank) * Ly::kBRows : 0);
           // dense weights: expert g is slice g of B and of SFB; discrete weights:
           // expert g's own maps, each of one slice
@@ -962,23 +909,6 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
                 tma_load_3d_pair(sSa, &tmSFA, fbl, 0, ka, mt);
                 tma_load_3d_pair(sSb, mSFB, fbl, 0, ka, sfb_rb);
               }
-            } else if (MC) {
-              // every byte of this CTA's stage counts on its own barrier; the
-              // shared operand arrives half from each CTA (A boxes are 64 rows,
-              // B boxes 128 rows)
-              const int r = static_cast<int>(rank);
-              mbar_expect_tx(fb, Ly::kStageBytes);
-              if (share_b) {
-                tma_load_2d(sA, &tmA, fb, k0, mt * kBM);
-                tma_load_2d(sA + kABytesHalf, &tmA, fb, k0, mt * kBM + kBM / 2);
-                tma_load_3d_mc(sB + r * (Ly::kBBytes / 2), mB, fb, k0, b_row + r * (BN / 2), bz, 0x3);
-              } else {
-                tma_load_2d_mc(sA + r * kABytesHalf, &tmA, fb, k0, mt * kBM + r * (kBM / 2), 0x3);
-                tma_load_3d(sB, mB, fb, k0, b_row, bz);
-                tma_load_3d(sB + Ly::kBBytes / 2, mB, fb, k0, b_row + BN / 2, bz);
-              }
-              tma_load_3d(sSa, &tmSFA, fb, 0, ka, mt);
-              tma_load_3d(sSb, mSFB, fb, 0, ka, sfb_rb);
             } else {
               mbar_expect_tx(fb, Ly::kABytes + Ly::kBBytes + sf_tx);
               tma_load_2d(sA, &tmA, fb, k0, mt * kBM);
@@ -994,9 +924,9 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
           }
         }
         if (ok && CLUSTER) {
-          // wait until the last use of every stage was released (by both CTAs'
-          // MMAs in a multicast cluster): no commit or load of the other CTA
-          // still targets this CTA's shared memory when the CTAs part
+          // wait until the last use of every stage was released: no commit or
+          // MMA read of the even CTA still targets this CTA's shared memory when
+          // the CTAs part
           for (int i = 0; i < S; ++i) {
             if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit_ns)) { ok = false; break; }
             if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -1005,9 +935,8 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
         if (!ok) {
           atomicOr(p.status, kStatusTimeout);
           // drain: wait (bounded) for every load this thread issued to land.  In a
-          // cluster the loads also complete barriers of the other CTA (pair: the
-          // even CTA's; multicast: both), which cannot be polled from here: wait
-          // out the drain bound instead.
+          // pair the loads also complete the even CTA's barriers, which cannot be
+          // polled from here: wait out the drain bound instead.
           for (int s = 0; s < S; ++s)
             if (issued[s]) {
               const uint64_t t0 = globaltimer_ns();
@@ -1064,7 +993,6 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
           }
           // release the stage (in both CTAs of a cluster)
           if (PAIR) tc_commit_pair(empty_bar(st), 3);
-          else if (MC) tc_commit_mc(empty_bar(st), 3);
           else tc_commit(empty_bar(st));
         };
         // failure-path test: nothing arrives on the drain barrier before an abort
@@ -1229,8 +1157,8 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC), CM>()>::kThread
     uint32_t acc_phase = 0;
     for (int t = unit; t < num_tiles; t += num_units) {
       int g, mt, nt;
-      bool valid, share_b;
-      decode_tile<CM>(t, p, s_off, s_trow, rank, g, mt, nt, valid, share_b);
+      bool valid;
+      decode_tile<CM>(t, p, s_off, s_trow, rank, g, mt, nt, valid);
       // dSwiGLU backward: the saved-C values this thread will read are fetched
       // into L2 while the tile's MMAs run (+3.6 % on the FC1 backward).  Holding
       // them in registers instead spills the epilogue to local memory, which

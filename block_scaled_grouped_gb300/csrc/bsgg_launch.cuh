@@ -3,6 +3,10 @@
 // class) instance.
 #pragma once
 
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
 #include "bsgg_internal.h"
 
 namespace bsgg {
@@ -12,29 +16,39 @@ cudaError_t launch_one(const Launch& L) {
   auto kern = bsgg_kernel<IC, BN, CM, EPI, OUTC, XC>;
   constexpr bool FP4 = ic_fp4(IC);
   constexpr bool kCluster = CM != CM_SINGLE;
-  constexpr bool kStores = scale_stores<FP4, CM>();
+  constexpr bool kStores = scale_stores<FP4>();
   using Ro = Roles<kStores>;
   const int smem = Layout<FP4, BN, CM == CM_PAIR, ic_scaled(IC)>::kSmemBytes;
-  static int configured_device = -1;
+  // The function attributes are set once per device and instance.  Bit d of
+  // `configured` says device d is done; host threads that launch this instance
+  // at the same time serialise on the mutex until the bit is set.
+  static std::atomic<uint64_t> configured{0};
+  static std::mutex configure_mu;
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    if (kCluster) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const uint64_t bit = uint64_t(1) << dev;
+  if ((configured.load(std::memory_order_acquire) & bit) == 0) {
+    std::lock_guard<std::mutex> lk(configure_mu);
+    if ((configured.load(std::memory_order_relaxed) & bit) == 0) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
+      if (kCluster) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+        if (e != cudaSuccess) return e;
+      }
+      if (kStores) {
+        // the warpgroups' setmaxnreg shares add up to exactly the launch's
+        // registers only if the kernel was compiled to kLaunchRegs per thread;
+        // with fewer the raising warps would wait forever: refuse to launch
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != Ro::kLaunchRegs) return cudaErrorInvalidConfiguration;
+      }
+      configured.fetch_or(bit, std::memory_order_release);
     }
-    if (kStores) {
-      // the warpgroups' setmaxnreg shares add up to exactly the launch's
-      // registers only if the kernel was compiled to kLaunchRegs per thread;
-      // with fewer the raising warps would wait forever: refuse to launch
-      cudaFuncAttributes fa;
-      e = cudaFuncGetAttributes(&fa, kern);
-      if (e != cudaSuccess) return e;
-      if (fa.numRegs != Ro::kLaunchRegs) return cudaErrorInvalidConfiguration;
-    }
-    configured_device = dev;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(L.grid), 1, 1);
@@ -103,16 +117,16 @@ cudaError_t launch_shape_bwd(const Launch& L) {
   return cudaErrorInvalidValue;
 }
 
-// Clusters of two of this kernel that fit on the device at once, x 2.
-template <int IC, int CM>
+// CTA pairs of this kernel that fit on the device at once, x 2.
+template <int IC>
 int cluster_resident_ctas_impl() {
   constexpr bool FP4 = ic_fp4(IC);
-  auto kern = bsgg_kernel<IC, 256, CM, EPI_GATE, OUTC_FLOAT, false>;
-  const int smem = Layout<FP4, 256, CM == CM_PAIR>::kSmemBytes;
+  auto kern = bsgg_kernel<IC, 256, CM_PAIR, EPI_GATE, OUTC_FLOAT, false>;
+  const int smem = Layout<FP4, 256, true>::kSmemBytes;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(Roles<scale_stores<FP4, CM>()>::kThreads, 1, 1);
+  cfg.blockDim = dim3(Roles<scale_stores<FP4>()>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;

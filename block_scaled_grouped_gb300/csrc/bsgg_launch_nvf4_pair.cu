@@ -3,8 +3,7 @@
 
 namespace bsgg {
 cudaError_t launch_nvf4_pair(const Launch& L) { return launch_shape_fwd<IC_NVF4, 256, CM_PAIR>(L); }
-int cluster_resident_ctas(bool fp4, bool mc) {
-  if (mc) return fp4 ? cluster_resident_ctas_impl<IC_NVF4, CM_MC>() : cluster_resident_ctas_impl<IC_MXF8, CM_MC>();
-  return fp4 ? cluster_resident_ctas_impl<IC_NVF4, CM_PAIR>() : cluster_resident_ctas_impl<IC_MXF8, CM_PAIR>();
+int cluster_resident_ctas(bool fp4) {
+  return fp4 ? cluster_resident_ctas_impl<IC_NVF4>() : cluster_resident_ctas_impl<IC_MXF8>();
 }
 }  // namespace bsgg

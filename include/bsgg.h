@@ -91,8 +91,6 @@ typedef enum {
   BSGG_IN_NVFP4 = 2,       /* float4_e2m1fn_x2 data, float8_e4m3fn scales, v = 16 */
   BSGG_IN_FP4_UE8M0_16 = 3,/* float4_e2m1fn_x2 data, float8_e8m0fnu scales, v = 16 */
   BSGG_IN_MXFP4 = 4,       /* float4_e2m1fn_x2 data, float8_e8m0fnu scales, v = 32 */
-  /* The two UE8M0-scaled FP4 formats run on single CTAs and CTA pairs; the (2, 1)
-     multicast clusters of 128 x 256 tiles return BSGG_ERR_UNSUPPORTED for them. */
   BSGG_IN_BF16 = 5         /* bfloat16 A and B, no scale factors: the BF16 backend of
                               "Grouped GEMM + dGLU (SM100)" (Backend dispatch, BF16
                               contract).  Backward DSWIGLU / DGEGLU only (dGeGLU with
@@ -155,10 +153,11 @@ typedef struct {
   /* Thread-block cluster shape (cluster_m, cluster_n): the pages' cluster_shape_mn
      ("Grouped GEMM + Quant (SM100)", Common Parameters; Support Surface and Constraints,
      Tiling and Cluster).  Built: (1, 1) with tile_m = 128; (2, 1) with tile 256 x 256 (the
-     CTA pair); (2, 1) with tile 128 x 256: two CTAs, each computing its own 128 x 256 tile,
-     share one operand tile through TMA multicast.  (0, 0) = the library's choice.  Other
-     powers of two up to 4 are valid on the pages and return BSGG_ERR_UNSUPPORTED; any other
-     value returns BSGG_ERR_INVALID_ARG. */
+     CTA pair; tile (0, 0) with cluster (2, 1) selects it).  (0, 0) = the library's choice.
+     A (2, 1) cluster of 128-row or 128-column tiles would share an operand tile between two
+     CTAs by TMA multicast, which this library never issues: it returns
+     BSGG_ERR_UNSUPPORTED, as do the other powers of two up to 4 that the pages allow; any
+     other value returns BSGG_ERR_INVALID_ARG. */
   int32_t cluster_m;
   int32_t cluster_n;
   /* Forward epilogue options of "Grouped GEMM + GLU + Hadamard + Quant (SM100)"
@@ -293,7 +292,8 @@ bsgg_status bsgg_run_host(bsgg_plan* plan, const bsgg_args* host, const bsgg_arg
 int32_t bsgg_launches_per_run(const bsgg_plan* plan);
 
 /* Synchronize `stream`, then read and clear the plan's device status word:
- * BSGG_OK, BSGG_ERR_DEVICE_TIMEOUT, BSGG_ERR_BAD_OFFSETS or BSGG_ERR_BAD_POINTERS. */
+ * BSGG_OK, BSGG_ERR_DEVICE_TIMEOUT, BSGG_ERR_BAD_OFFSETS or BSGG_ERR_BAD_POINTERS
+ * (a status bit the library does not define reads as BSGG_ERR_CUDA). */
 bsgg_status bsgg_query_device_status(bsgg_plan* plan, void* stream);
 
 /* Test hook for the failure path; the pages have no counterpart.  With enable =
@@ -342,14 +342,18 @@ bsgg_status bsgg_pack_sf(const uint8_t* rowmajor, uint8_t* swizzled, int64_t row
  * descriptors (256 * L + 256 bytes) never fit, so discrete_b = 1 is rejected.
  *
  * The first call on a device looks up the array's device address with that
- * device current (cudaGetSymbolAddress); make that first call before any
- * stream capture.  Every call clears the status word on `stream` before its
- * kernel.  All calls share the array, which keeps the last call's contents:
+ * device current (cudaGetSymbolAddress) and remembers it with the id of the
+ * device's context; a call that finds a different context (after
+ * cudaDeviceReset, say) looks it up again.  Make the first call on a device,
+ * and the first after a reset, before any stream capture.  Every call clears
+ * the status word on `stream` before its kernel.  All calls share the array, which keeps the last call's contents:
  * calls whose kernels overlap on the GPU (several streams, several host
  * threads) race on it, so run them on one stream when the status matters.
  * With wait_status != 0 the call synchronizes `stream` after the launch and
- * returns the device status (BSGG_OK, BSGG_ERR_DEVICE_TIMEOUT or
- * BSGG_ERR_BAD_OFFSETS); with 0 it returns once the kernel is enqueued. */
+ * returns the device status as bsgg_query_device_status would (BSGG_OK,
+ * BSGG_ERR_DEVICE_TIMEOUT or BSGG_ERR_BAD_OFFSETS; a status bit the library
+ * does not define reads as BSGG_ERR_CUDA); with 0 it returns once the kernel
+ * is enqueued. */
 bsgg_status bsgg_run_noalloc(const bsgg_desc* desc, const bsgg_args* args, void* stream,
                              int32_t wait_status);
 
@@ -366,6 +370,21 @@ bsgg_status bsgg_run_noalloc(const bsgg_desc* desc, const bsgg_args* args, void*
  * wait ran out (2 s). */
 bsgg_status bsgg_measure_mma_peak(int32_t in_format, int32_t tile_n, int64_t mmas_per_sm, double* tflops,
                                   void* stream);
+
+/* Measurement utility; the pages have no counterpart.  The same measurement for
+ * either instruction form the GEMM issues: tile_m = 128 is bsgg_measure_mma_peak
+ * (cta_group::1, M = 128, one issuing CTA per SM, tile_n 128 or 256); tile_m = 256
+ * is cta_group::2 with M = 256, N = 256 (tile_n must be 256): clusters of two
+ * CTAs, each holding its 128 rows of A and half of B's rows, the even CTA issuing
+ * `mmas` instructions for the pair, on floor(SMs / 2) pairs.  Each CTA reserves
+ * 120 KB of shared memory so that every SM holds one.  TFLOP/s counts 2*M*N*K per
+ * instruction.  Synchronizes the stream; allocates and frees a 4-byte status
+ * word.  Errors: BSGG_ERR_INVALID_ARG for tile_m not 128 or 256 and the
+ * arguments bsgg_measure_mma_peak refuses (mmas: 4 .. 2^22 per issuing thread),
+ * BSGG_ERR_UNSUPPORTED for tile_m = 256 with tile_n = 128, BSGG_ERR_CUDA for a
+ * failed CUDA call, BSGG_ERR_DEVICE_TIMEOUT if the final wait ran out (2 s). */
+bsgg_status bsgg_measure_mma_peak_tile(int32_t in_format, int32_t tile_m, int32_t tile_n, int64_t mmas,
+                                       double* tflops, void* stream);
 
 #ifdef __cplusplus
 }

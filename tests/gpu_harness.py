@@ -24,8 +24,8 @@ def to_device(p: W.Problem, device="cuda") -> W.Problem:
 
 
 # (tile_m, tile_n, cluster_m, cluster_n): single CTA 128 x 128 and 128 x 256,
-# multicast clusters of two 128 x 256 CTAs, and 256 x 256 CTA pairs
-TILES = [(128, 128, 1, 1), (128, 256, 1, 1), (128, 256, 2, 1), (256, 256, 2, 1)]
+# and 256 x 256 CTA pairs
+TILES = [(128, 128, 1, 1), (128, 256, 1, 1), (256, 256, 2, 1)]
 
 
 def tile_id(t) -> str:

@@ -94,7 +94,13 @@ def _create(**over):
     (dict(cluster_m=3, cluster_n=1), 1), (dict(cluster_m=8, cluster_n=1), 1),   # powers of 2 <= 4
     (dict(tile_m=256, cluster_m=1, cluster_n=1), 1),         # 2-CTA tiles need an even CLUSTER_M
     (dict(cluster_m=4, cluster_n=1), 2), (dict(cluster_m=1, cluster_n=2), 2),   # valid, not built
+    # (2, 1) clusters of 128-row or 128-column tiles would share an operand by
+    # TMA multicast, which this library does not issue
     (dict(tile_m=128, tile_n=128, cluster_m=2, cluster_n=1), 2),
+    (dict(tile_m=128, tile_n=256, cluster_m=2, cluster_n=1), 2),
+    (dict(tile_m=128, tile_n=256, cluster_m=2, cluster_n=1, in_format="nvfp4"), 2),
+    (dict(tile_m=128, tile_n=256, cluster_m=2, cluster_n=1, epilogue="dswiglu"), 2),
+    (dict(tile_n=128, cluster_m=2, cluster_n=1), 2),
     (dict(in_format="nvfp4", out_format="e4m3"), 2),   # not on the pages
     (dict(n=96, epilogue="geglu"), 1),          # GeGLU pairs 32-column blocks too
     (dict(glu_limit=-1.0, epilogue="swiglu"), 1),
@@ -123,7 +129,7 @@ def _create(**over):
     (dict(n=128, epilogue="swiglu", rht_format="e2m1", rht_colwise=True), 1),   # N_out % 128
     (dict(epilogue="dsituglu", situ_betas=(1.0, float("inf"))), 1),
     (dict(epilogue="dswiglu", situ_betas=(2.0, 2.0)), 1),          # dSiTU-GLU's own
-    # UE8M0-scaled FP4: no multicast-cluster instances; no FP8 outputs from FP4
+    # UE8M0-scaled FP4: (2, 1) clusters only as CTA pairs; no FP8 outputs from FP4
     (dict(in_format="mxfp4", tile_m=128, tile_n=256, cluster_m=2, cluster_n=1), 2),
     (dict(in_format="fp4_ue8m0_16", tile_m=128, tile_n=256, cluster_m=2, cluster_n=1), 2),
     (dict(in_format="mxfp4", out_format="e5m2"), 2),
@@ -250,6 +256,12 @@ def test_helper_entry_points_refuse_bad_arguments_before_any_device_call(lib):
     assert lib.bsgg_measure_mma_peak(0, 128, 1024, None, None) == 1
     for fmt, tn, cnt in [(0, 192, 1024), (0, 128, 3), (0, 128, (1 << 22) + 1), (5, 128, 1024), (-1, 256, 1024)]:
         assert lib.bsgg_measure_mma_peak(fmt, tn, cnt, ctypes.byref(out), None) == 1
+    # the same for either instruction form: tile_m 128 or 256, pairs 256 x 256 only
+    assert lib.bsgg_measure_mma_peak_tile(0, 256, 256, 1024, None, None) == 1
+    for fmt, tm, tn, cnt in [(0, 64, 256, 1024), (0, 512, 256, 1024), (0, 256, 192, 1024), (0, 256, 256, 3),
+                             (2, 256, 256, (1 << 22) + 1), (5, 256, 256, 1024)]:
+        assert lib.bsgg_measure_mma_peak_tile(fmt, tm, tn, cnt, ctypes.byref(out), None) == 1
+    assert lib.bsgg_measure_mma_peak_tile(0, 256, 128, 1024, ctypes.byref(out), None) == 2
     # plan-taking entry points with no plan
     assert lib.bsgg_run_host(None, None, None, None, None, None) == 1
     assert lib.bsgg_debug_force_timeout(None, 1) == 1
