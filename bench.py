@@ -448,7 +448,7 @@ def time_workload(p, args, dev, world, steps: int, warmup: int):
                 "flops_incl_padding": 2.0 * p.m_pad * p.n * p.k}
     # the stricter denominator: this GPU's measured rate of the instruction form
     # the launch issues
-    mma = measured_mma_peak(p.in_fmt, mma_form(p, args.tile))
+    mma = None if args.no_mma_peak else measured_mma_peak(p.in_fmt, mma_form(p, args.tile))
     if mma is not None:
         roofline["measured_mma_peak"] = mma
         roofline["frac_of_measured_mma"] = achieved / mma["value"]
@@ -610,6 +610,8 @@ def main():
     ap.add_argument("--no-extra-workloads", action="store_true",
                     help="time only --workload (by default the other hot-path workloads follow it)")
     ap.add_argument("--extra-steps", type=int, default=20, help="timed steps of each other workload")
+    ap.add_argument("--no-mma-peak", action="store_true",
+                    help="skip the MMA-rate measurement behind roofline.frac_of_measured_mma")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=0.0)
     ap.add_argument("--mma-peak", action="store_true", help="print the measured dense block-scaled "

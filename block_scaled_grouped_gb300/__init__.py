@@ -20,12 +20,14 @@ EPILOGUES = {"gate": 0, "swiglu": 1, "srelu": 2, "geglu": 3, "dswiglu": 4, "dgeg
 BWD_EPILOGUES = ("dswiglu", "dgeglu", "dsituglu")
 GLU_EPILOGUES = ("swiglu", "geglu")
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
-          4: "device wait timed out", 5: "padded_offsets invalid", 6: "expert weight pointer invalid"}
+          4: "device wait timed out", 5: "padded_offsets invalid", 6: "expert weight pointer invalid",
+          7: "an index failed its range check"}
 
 SYMBOLS = ("bsgg_create", "bsgg_run", "bsgg_run_host", "bsgg_query_device_status", "bsgg_destroy",
            "bsgg_status_string", "bsgg_sf_bytes", "bsgg_sf_offset", "bsgg_pack_sf", "bsgg_run_noalloc",
            "bsgg_measure_mma_peak", "bsgg_measure_mma_peak_tile", "bsgg_debug_force_timeout",
-           "bsgg_launches_per_run")
+           "bsgg_launches_per_run", "bsgg_debug_bounds_checked", "bsgg_debug_bounds_margin",
+           "bsgg_debug_bounds_violation")
 
 
 class BsggError(RuntimeError):
@@ -89,20 +91,21 @@ class Args(ctypes.Structure):
         "dprob", "rht", "sfrht", "rht_norm_const", "dbias")]
 
 
-_lib = None
+_libs = {}
 
 
-def library_path() -> str:
-    return _build.LIB_PATH
+def library_path(debug_bounds: bool = False) -> str:
+    return _build.DEBUG_LIB_PATH if debug_bounds else _build.LIB_PATH
 
 
-def lib():
-    """Load libbsgg.so (raises if it has not been built)."""
-    global _lib
-    if _lib is None:
-        path = _build.LIB_PATH
+def lib(debug_bounds: bool = False):
+    """Load libbsgg.so, or with debug_bounds the range-checking build
+    libbsgg_debug.so (raises if it has not been built)."""
+    L = _libs.get(debug_bounds)
+    if L is None:
+        path = library_path(debug_bounds)
         if not os.path.exists(path):
-            raise RuntimeError(f"libbsgg.so is not built ({path}); run block_scaled_grouped_gb300.build")
+            raise RuntimeError(f"{os.path.basename(path)} is not built ({path}); run block_scaled_grouped_gb300.build")
         L = ctypes.CDLL(path)
         L.bsgg_create.restype = ctypes.c_int
         L.bsgg_create.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(ctypes.c_void_p)]
@@ -138,8 +141,14 @@ def lib():
         L.bsgg_pack_sf.restype = ctypes.c_int
         L.bsgg_pack_sf.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                    ctypes.c_int32, ctypes.c_void_p]
-        _lib = L
-    return _lib
+        L.bsgg_debug_bounds_checked.restype = ctypes.c_int32
+        L.bsgg_debug_bounds_checked.argtypes = []
+        L.bsgg_debug_bounds_margin.restype = ctypes.c_int
+        L.bsgg_debug_bounds_margin.argtypes = [ctypes.c_void_p, ctypes.c_int32]
+        L.bsgg_debug_bounds_violation.restype = ctypes.c_int
+        L.bsgg_debug_bounds_violation.argtypes = [ctypes.c_void_p] + [ctypes.POINTER(ctypes.c_uint32)] * 3
+        _libs[debug_bounds] = L
+    return L
 
 
 def _check(code: int, what: str) -> None:
@@ -191,9 +200,12 @@ def pack_sf(rowmajor, out=None, stream=None):
 class Plan:
     """A validated problem description (bsgg_create); run() launches it."""
 
-    def __init__(self, **kw):
+    def __init__(self, debug_bounds: bool = False, **kw):
         """Keyword arguments of make_desc.  tile = the pages' mma_tiler_mn,
-        cluster = cluster_shape_mn; (0, 0) lets the library choose."""
+        cluster = cluster_shape_mn; (0, 0) lets the library choose.
+        debug_bounds: create and run the plan in the range-checking build
+        (libbsgg_debug.so)."""
+        self._lib = lib(debug_bounds)
         self.desc = make_desc(**kw)
         self.in_format, self.out_format, self.epilogue = kw["in_format"], kw["out_format"], kw["epilogue"]
         self.want_col = bool(kw.get("want_col", False))
@@ -201,7 +213,7 @@ class Plan:
         self.rht_format = kw.get("rht_format")
         self.rht_colwise = bool(kw.get("rht_colwise", False))
         h = ctypes.c_void_p()
-        _check(lib().bsgg_create(ctypes.byref(self.desc), ctypes.byref(h)), "bsgg_create")
+        _check(self._lib.bsgg_create(ctypes.byref(self.desc), ctypes.byref(h)), "bsgg_create")
         self._h = h
 
     # shapes --------------------------------------------------------------
@@ -252,34 +264,45 @@ class Plan:
     def run(self, stream=None, **tensors) -> None:
         """Enqueue the kernel; tensors by the bsgg_args names (device)."""
         args = self._args(tensors)
-        _check(lib().bsgg_run(self._h, ctypes.byref(args), _stream(stream)), "bsgg_run")
+        _check(self._lib.bsgg_run(self._h, ctypes.byref(args), _stream(stream)), "bsgg_run")
 
     def run_host(self, host: dict, dev: dict, stream=None):
         """Host-buffer call: copies host inputs in, runs, copies outputs out
         and synchronizes.  Returns (h2d_bytes, d2h_bytes)."""
         hi, di = self._args(host), self._args(dev)
         h2d, d2h = ctypes.c_uint64(), ctypes.c_uint64()
-        _check(lib().bsgg_run_host(self._h, ctypes.byref(hi), ctypes.byref(di), _stream(stream),
+        _check(self._lib.bsgg_run_host(self._h, ctypes.byref(hi), ctypes.byref(di), _stream(stream),
                                    ctypes.byref(h2d), ctypes.byref(d2h)), "bsgg_run_host")
         return int(h2d.value), int(d2h.value)
 
     @property
     def launches_per_run(self) -> int:
         """Kernel launches one run() enqueues (bsgg_launches_per_run)."""
-        return int(lib().bsgg_launches_per_run(self._h))
+        return int(self._lib.bsgg_launches_per_run(self._h))
 
     def device_status(self, stream=None) -> int:
         """Synchronize and read/clear the device status word (0 = ok)."""
-        return int(lib().bsgg_query_device_status(self._h, _stream(stream)))
+        return int(self._lib.bsgg_query_device_status(self._h, _stream(stream)))
 
     def debug_force_timeout(self, enable: bool) -> None:
         """Test hook (bsgg_debug_force_timeout): later launches give up after a
         forced barrier timeout and report BSGG_ERR_DEVICE_TIMEOUT."""
-        _check(lib().bsgg_debug_force_timeout(self._h, int(bool(enable))), "bsgg_debug_force_timeout")
+        _check(self._lib.bsgg_debug_force_timeout(self._h, int(bool(enable))), "bsgg_debug_force_timeout")
+
+    def debug_bounds_margin(self, rows: int) -> None:
+        """Test hook of the range-checking build (bsgg_debug_bounds_margin)."""
+        _check(self._lib.bsgg_debug_bounds_margin(self._h, int(rows)), "bsgg_debug_bounds_margin")
+
+    def debug_bounds_violation(self) -> tuple:
+        """(site, value, limit) of the last range-check failure read back."""
+        v = [ctypes.c_uint32() for _ in range(3)]
+        _check(self._lib.bsgg_debug_bounds_violation(self._h, *[ctypes.byref(x) for x in v]),
+               "bsgg_debug_bounds_violation")
+        return tuple(int(x.value) for x in v)
 
     def close(self) -> None:
         if getattr(self, "_h", None):
-            lib().bsgg_destroy(self._h)
+            self._lib.bsgg_destroy(self._h)
             self._h = None
 
     def __del__(self):

@@ -21,6 +21,8 @@ struct bsgg_plan {
   int num_sms;
   int grid;                // CTAs per launch (a multiple of 2 for clusters)
   bool pair;               // 256 x 256 tiles on CTA pairs (2-CTA MMAs)
+  int ic;                  // the kernel's input class (bsgg::IC_*)
+  int slices;              // 128-byte K slices per pipeline stage (bsgg::stage_slices)
   int bn;
   int epi;
   int outc;
@@ -30,6 +32,8 @@ struct bsgg_plan {
   int64_t out_row_bytes;
   uint32_t* status;        // device word: kStatus* bits
   bool force_timeout;      // bsgg_debug_force_timeout
+  int32_t dbg_margin;      // bsgg_debug_bounds_margin (range-checking build)
+  uint32_t violation[3];   // the last range-check failure read back: site, value, limit
   CUtensorMap* maps;       // discrete weight mode: {B_g, SFB_g} per expert, then the bad-pointer flag
 };
 
@@ -224,10 +228,10 @@ bsgg_status encode_one(CUtensorMap* map, const void* base, int rank, const cuuin
 bsgg_status encode_maps(const bsgg_plan* P, const bsgg_args* a, bsgg::Launch* L) {
   const bsgg_desc& d = P->desc;
   const int64_t kq = ceil_div(ceil_div(d.k, P->sf_vec), 4);
-  // scale atoms per stage (an atom = 4 scales of 128 rows): 4 for FP4 with one
-  // scale per 16 values, 2 per 32, 1 for MXFP8
+  // scale atoms per stage (an atom = 4 scales of 128 rows): per 128-byte K
+  // slice 4 for FP4 with one scale per 16 values, 2 per 32, 1 for MXFP8
   const bool fp4 = is_fp4_in(P->desc.in_format);
-  const int atoms = !fp4 ? 1 : P->sf_vec == 32 ? 2 : 4;
+  const int atoms = (!fp4 ? 1 : P->sf_vec == 32 ? 2 : 4) * P->slices;
   bsgg_status st;
   {
     cuuint64_t dims[2] = {cuuint64_t(P->kbytes), cuuint64_t(d.m_pad)};
@@ -299,6 +303,11 @@ bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan*
   if (tn == 0) tn = (bwd && tm == 128) ? 128 : 256;
   P->pair = (tm == 256);
   P->bn = P->pair ? 256 : tn;
+  P->ic = desc->in_format == BSGG_IN_BF16    ? bsgg::IC_BF16
+          : desc->in_format == BSGG_IN_NVFP4 ? bsgg::IC_NVF4
+          : is_f4e8_in(desc->in_format)      ? bsgg::IC_F4E8
+                                             : bsgg::IC_MXF8;
+  P->slices = bsgg::stage_slices(P->ic, P->pair ? bsgg::CM_PAIR : bsgg::CM_SINGLE);
   // GeGLU runs in the SwiGLU instances (Params::glu_kind selects the activation)
   // the dGeGLU backward runs in the dSwiGLU instances (Params::bwd_kind)
   P->epi = desc->epilogue == BSGG_EPI_GEGLU ? bsgg::EPI_SWIGLU
@@ -425,6 +434,7 @@ size_t maps_bytes(int L) { return sizeof(CUtensorMap) * (2 * size_t(L) + 1); }
 // The status a device status word stands for.  A bit this library does not
 // define (it never writes one) reads as a CUDA error rather than as success.
 bsgg_status status_of_word(uint32_t w) {
+  if (w & bsgg::kStatusBounds) return BSGG_ERR_DEVICE_BOUNDS;
   if (w & bsgg::kStatusBadPointers) return BSGG_ERR_BAD_POINTERS;
   if (w & bsgg::kStatusBadOffsets) return BSGG_ERR_BAD_OFFSETS;
   if (w & bsgg::kStatusTimeout) return BSGG_ERR_DEVICE_TIMEOUT;
@@ -444,6 +454,7 @@ const char* bsgg_status_string(bsgg_status s) {
     case BSGG_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case BSGG_ERR_BAD_OFFSETS: return "padded_offsets invalid";
     case BSGG_ERR_BAD_POINTERS: return "expert weight pointer invalid";
+    case BSGG_ERR_DEVICE_BOUNDS: return "an index failed its range check";
   }
   return "unknown status";
 }
@@ -544,13 +555,13 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   p.L = d.num_groups;
   p.n_out = static_cast<int32_t>(P->n_out);
   p.num_n_tiles = static_cast<int32_t>(ceil_div(d.n, P->bn));
-  p.num_k_stages = static_cast<int32_t>(ceil_div(P->kbytes, bsgg::kBKBytes));
+  p.num_k_stages = static_cast<int32_t>(ceil_div(P->kbytes, bsgg::kBKBytes * P->slices));
   p.raster_w = P->bn == 256 ? 8 : 16;
   p.rn_b = static_cast<int32_t>(ceil_div(d.n, 128));
   p.kq_row = static_cast<int32_t>(ceil_div(ceil_div(P->n_out, P->sf_vec), 4));
   p.kq_col = static_cast<int32_t>(ceil_div(ceil_div(d.m_pad, P->sf_vec), 4));
   p.out_kind = d.out_format;
-  p.sf_atoms = !is_fp4_in(d.in_format) ? 1 : P->sf_vec == 32 ? 2 : 4;
+  p.sf_atoms = (!is_fp4_in(d.in_format) ? 1 : P->sf_vec == 32 ? 2 : 4) * P->slices;
   p.sf_v32 = P->sf_vec == 32 ? 1 : 0;
   p.want_col = d.want_col;
   p.gate_first = d.gate_first;
@@ -594,7 +605,10 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
     p.maps_bad = reinterpret_cast<const uint32_t*>(P->maps + 2 * d.num_groups);
   }
   p.force_timeout = P->force_timeout ? 1u : 0u;
-  p.wait_limit_ns = P->force_timeout ? kTestWaitLimitNs : bsgg::kWaitLimitNs;
+  // a test that makes the range checks fire also shortens the waits: the CTA
+  // that stops loading leaves its partner's barriers incomplete
+  p.wait_limit_ns = (P->force_timeout || P->dbg_margin) ? kTestWaitLimitNs : bsgg::kWaitLimitNs;
+  p.dbg_rows = static_cast<int32_t>(d.m_pad - P->dbg_margin);
 
   // an upper bound of the scheduling units (pairs may add one 256-row tile
   // row per group)
@@ -655,10 +669,28 @@ bsgg_status bsgg_query_device_status(bsgg_plan* P, void* stream) {
   if (!P) return BSGG_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return BSGG_ERR_CUDA;
-  uint32_t w = 0;
-  if (cudaMemcpy(&w, P->status, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return BSGG_ERR_CUDA;
+  uint32_t w[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(w, P->status, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return BSGG_ERR_CUDA;
   if (cudaMemset(P->status, 0, sizeof(w)) != cudaSuccess) return BSGG_ERR_CUDA;
-  return status_of_word(w);
+  if (w[0] & bsgg::kStatusBounds) std::memcpy(P->violation, w + 1, sizeof(P->violation));
+  return status_of_word(w[0]);
+}
+
+int32_t bsgg_debug_bounds_checked(void) { return bsgg::kDebugBounds ? 1 : 0; }
+
+bsgg_status bsgg_debug_bounds_margin(bsgg_plan* P, int32_t rows) {
+  if (!P || rows < 0 || rows % 128 != 0 || rows >= P->desc.m_pad) return BSGG_ERR_INVALID_ARG;
+  if (!bsgg::kDebugBounds) return BSGG_ERR_UNSUPPORTED;
+  P->dbg_margin = rows;
+  return BSGG_OK;
+}
+
+bsgg_status bsgg_debug_bounds_violation(const bsgg_plan* P, uint32_t* site, uint32_t* value, uint32_t* limit) {
+  if (!P || !site || !value || !limit) return BSGG_ERR_INVALID_ARG;
+  *site = P->violation[0];
+  *value = P->violation[1];
+  *limit = P->violation[2];
+  return BSGG_OK;
 }
 
 bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* dev, void* stream,
@@ -743,7 +775,8 @@ static __device__ __align__(256) uint32_t g_noalloc_scratch[BSGG_NOALLOC_SCRATCH
 
 namespace {
 
-constexpr size_t kNoAllocStatusBytes = sizeof(uint32_t);   // scratch one call needs
+constexpr size_t kNoAllocStatusBytes = 4 * sizeof(uint32_t);   // scratch one call needs: the status
+                                                                 // word and the range-check record
 constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[kNoAllocMaxDevices];
@@ -827,7 +860,7 @@ extern "C" bsgg_status bsgg_run_noalloc(const bsgg_desc* desc, const bsgg_args* 
   if (cudaMemsetAsync(scratch, 0, kNoAllocStatusBytes, s) != cudaSuccess) return BSGG_ERR_CUDA;
   const bsgg_status st = bsgg_run(&P, args, stream);
   if (st != BSGG_OK || !wait_status) return st;
-  uint32_t w = 0;
+  uint32_t w = 0;   // (the range-check record behind it is not reported here)
   if (cudaMemcpyAsync(&w, scratch, sizeof(w), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess)
     return BSGG_ERR_CUDA;

@@ -65,9 +65,15 @@ enum : int { OUTC_FLOAT = 0, OUTC_FP8 = 1, OUTC_FP4 = 2 };
 enum : int { OK_BF16 = 0, OK_F16 = 1, OK_F32 = 2, OK_E4M3 = 3, OK_E5M2 = 4, OK_E2M1 = 5 };
 
 constexpr int kBM = 128;          // rows per CTA tile (TMEM lanes)
-constexpr int kBKBytes = 128;     // K bytes per pipeline stage (one 128-byte swizzle span)
+constexpr int kBKBytes = 128;     // K bytes per slice: one 128-byte swizzle span, one TMA box row
 constexpr int kEpiWarps = 8;      // two warps per tensor-memory lane quadrant
 enum : int { CM_SINGLE = 0, CM_PAIR = 1 };
+// K slices per pipeline stage (each slice one 128-byte box per operand and
+// four MMAs).  Every instance takes one: two slices per stage (eight MMAs per
+// barrier round trip, three stages in the shared memory of six) measured no
+// faster on GB300 for the MXFP8 CTA pairs (FC1 +1 %, FC2 -4 %, skewed +0 %),
+// so the ring stays deep rather than wide.
+__host__ __device__ constexpr int stage_slices(int, int) { return 1; }
 // Scale factors reach tensor memory by tcgen05.st from four warps (one per
 // lane quadrant) for FP4 inputs, by tcgen05.cp from one thread otherwise (see
 // the kernel's role table).  Measured on GB300: stores raise NVFP4 by 19 %
@@ -91,6 +97,7 @@ constexpr int kMaxGroups = 1024;
 constexpr uint32_t kStatusTimeout = 1u;
 constexpr uint32_t kStatusBadOffsets = 2u;
 constexpr uint32_t kStatusBadPointers = 4u;
+constexpr uint32_t kStatusBounds = 8u;               // range-checking build: an index failed its check
 constexpr uint64_t kWaitLimitNs = 2000000000ull;     // 2 s per wait (Params::wait_limit_ns)
 constexpr uint64_t kDrainLimitNs = 200000000ull;     // 0.2 s per drain wait
 
@@ -127,6 +134,8 @@ struct Params {
   uint32_t force_timeout;   // test of the failure path: the MMA thread first waits on a
                             // barrier nothing completes, so every role gives up and returns
   uint64_t wait_limit_ns;   // bound of every barrier wait (kWaitLimitNs; shorter in that test)
+  int32_t dbg_rows;         // range-checking build: rows of A, D, prob the checks accept (m_pad,
+                            // less a margin a test may set to see the checks fire)
   // "Grouped GEMM + GLU + Hadamard + Quant (SM100)", Equations: C = alpha_g * acc +
   // bias_g[n], optionally stored before any clamp or activation; GLU clamp and scale
   const void* bias;         // (L, N), N contiguous, or null
@@ -163,17 +172,23 @@ struct Params {
 
 // SCALED = false (bfloat16 operands): no scale buffers, 64 K elements per
 // 128-byte stage, 16 per MMA.
-template <bool FP4, int BN, bool PAIR, bool SCALED = true>
+template <bool FP4, int BN, bool PAIR, bool SCALED = true, int SL = 1>
 struct Layout {
   static_assert(BN == 128 || BN == 256, "tile width");
   static_assert(!PAIR || BN == 256, "CTA pairs use 256 x 256 tiles");
+  static_assert(SL == 1 || SL == 2, "one or two K slices per stage");
+  static constexpr int kSlices = SL;
+  static constexpr int kStageK = SL * kBKBytes;            // K bytes per stage
   static constexpr int kHalves = BN / 128;                 // 128-row SF blocks of the MMA's N
   static constexpr int kBRows = PAIR ? BN / 2 : BN;        // B rows held by this CTA
-  static constexpr int kAtoms = !SCALED ? 0 : FP4 ? 4 : 1;          // SF atoms per stage per 128 rows
-  static constexpr int kKElems = !SCALED ? 64 : FP4 ? 256 : 128;    // K elements per stage
-  static constexpr int kMmaK = !SCALED ? 16 : FP4 ? 64 : 32;        // K elements per MMA instruction
-  static constexpr int kABytes = kBM * kBKBytes;
-  static constexpr int kBBytes = kBRows * kBKBytes;
+  static constexpr int kAtoms = (!SCALED ? 0 : FP4 ? 4 : 1) * SL;        // SF atoms per stage per 128 rows
+  static constexpr int kKElems = (!SCALED ? 64 : FP4 ? 256 : 128) * SL;  // K elements per stage
+  static constexpr int kMmaK = !SCALED ? 16 : FP4 ? 64 : 32;             // K elements per MMA instruction
+  static constexpr int kMmas = 4 * SL;                                   // MMAs per stage
+  static constexpr int kASlice = kBM * kBKBytes;           // one slice of A (a 128-byte swizzled box)
+  static constexpr int kBSlice = kBRows * kBKBytes;
+  static constexpr int kABytes = kASlice * SL;
+  static constexpr int kBBytes = kBSlice * SL;
   static constexpr int kSfaBytes = kAtoms * 512;
   static constexpr int kSfbBytes = kAtoms * kHalves * 512;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;   // one CTA's bytes
@@ -201,6 +216,42 @@ struct Layout {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kOffB % 1024 == 0 && kOffSfa % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 };
+
+// Range-checking build (compiled with BSGG_DEBUG_BOUNDS): every TMA box
+// origin, scale-factor offset and output index is checked against the
+// problem's extents before use.  A failed check records the first failure
+// (site, value, limit in status words 1..3), raises kStatusBounds and skips the
+// access; in the producer it also raises the CTA's abort flag, so that every
+// role drains and returns as after a timeout.  Without the macro the checks
+// compile to nothing.
+#ifdef BSGG_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
+// check sites (status word 1)
+enum : uint32_t {
+  kSiteARows = 1, kSiteBRow = 2, kSiteBSlice = 3, kSiteSfa = 4, kSiteSfb = 5, kSiteK = 6,
+  kSiteDRow = 10, kSiteDCol = 11, kSiteSfdRow = 12, kSiteSfdCol = 13, kSiteAmax = 14, kSiteC = 15,
+  kSiteRht = 16, kSiteDprob = 17, kSiteDbias = 18, kSiteGroup = 19
+};
+static __device__ __noinline__ void bounds_fail(uint32_t* status, uint32_t site, int64_t v, int64_t lim) {
+  if (atomicCAS(status + 1, 0u, site) == 0u) {
+    status[2] = static_cast<uint32_t>(v);
+    status[3] = static_cast<uint32_t>(lim);
+  }
+  atomicOr(status, kStatusBounds);
+}
+// 0 <= v < lim (always true without BSGG_DEBUG_BOUNDS).
+__device__ __forceinline__ bool in_range(uint32_t* status, uint32_t site, int64_t v, int64_t lim) {
+  if constexpr (!kDebugBounds) {
+    return true;
+  } else {
+    if (v >= 0 && v < lim) return true;
+    bounds_fail(status, site, v, lim);
+    return false;
+  }
+}
 
 // Byte offset of the scale of (row, k-block) in a swizzled SF buffer whose
 // rows hold kq 512-byte atoms: 128-row block, then k-atom, then inside the atom
@@ -473,6 +524,26 @@ __device__ __forceinline__ void store_c32(const Params& p, const uint32_t* v, in
 template <int IC, int OUTC>
 __device__ __forceinline__ void output_chunk(const Params& p, const float (&v)[32], int row, int col0,
                                              float norm, int lane, int kblk_col, float& amax_local) {
+  if constexpr (kDebugBounds) {
+    // the chunk's D / D_col bytes and the scale-factor bytes it writes; the
+    // whole warp skips the chunk when a lane fails (the column blocks are
+    // warp-collective)
+    bool ok = in_range(p.status, kSiteDRow, row, p.dbg_rows) && in_range(p.status, kSiteDCol, col0 + 31, p.n_out);
+    if (OUTC != OUTC_FLOAT) {
+      const bool v16 = ic_fp4(IC) && !(IC == IC_F4E8 && p.sf_v32);
+      const int kr = v16 ? col0 / 16 + 1 : col0 / 32;                    // last row block written
+      const int64_t row_bytes = 512 * static_cast<int64_t>((p.m_pad + 127) / 128) * p.kq_row;
+      ok = ok && in_range(p.status, kSiteSfdRow, kr >> 2, p.kq_row) &&
+           in_range(p.status, kSiteSfdRow, sf_off(row, kr, p.kq_row), row_bytes);
+      if (p.want_col) {
+        const int kc = v16 ? 2 * kblk_col + 1 : kblk_col;                  // last column block written
+        const int64_t col_bytes = 512 * static_cast<int64_t>((p.n_out + 127) / 128) * p.kq_col;
+        ok = ok && in_range(p.status, kSiteSfdCol, kc >> 2, p.kq_col) &&
+             in_range(p.status, kSiteSfdCol, sf_off(col0 + 31, kc, p.kq_col), col_bytes);
+      }
+    }
+    if (__any_sync(0xffffffffu, !ok)) return;
+  }
   if (OUTC == OUTC_FLOAT) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) amax_local = fmaxf(amax_local, fabsf(v[i]));
@@ -658,6 +729,9 @@ __device__ __forceinline__ void rht_chunk(const Params& p, const float (&v)[32],
 // bytes at flat element n_out * seg_start + column * em + token.
 __device__ __forceinline__ void rht_col_chunk(const Params& p, const float (&v)[32], int row, int col0, int lane,
                                               int64_t seg_start, int em, float rnorm) {
+  if constexpr (kDebugBounds) {
+    if (__any_sync(0xffffffffu, !in_range(p.status, kSiteRht, seg_start + em - 1, p.m_pad))) return;
+  }
   const int t = static_cast<int>(row - seg_start);     // token within the expert
   const int64_t seg_elem = static_cast<int64_t>(p.n_out) * seg_start;
   const int kq = (em / 16 + 3) / 4;                    // SF atoms per 128 columns of the segment
@@ -723,7 +797,7 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* 
     }
   }
   output_chunk<IC, OUTC>(p, v, row, col0, norm, lane, kblk_col, amax_local);
-  if (XC && p.rht != nullptr) {
+  if (XC && p.rht != nullptr && in_range(p.status, kSiteRht, col0 + 31, p.n_out)) {
     if (p.rht_colwise) rht_col_chunk(p, v, row, col0, lane, seg_start, seg_rows, *p.rht_norm_const);
     else rht_chunk(p, v, row, col0, *p.rht_norm_const);
   }
@@ -743,7 +817,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC)>()>::kThreads, 1
   constexpr bool CLUSTER = CM != CM_SINGLE;
   constexpr bool ST = scale_stores<FP4>();
   using Ro = Roles<ST>;
-  using Ly = Layout<FP4, BN, PAIR, SCALED>;
+  using Ly = Layout<FP4, BN, PAIR, SCALED, stage_slices(IC, CM)>;
   constexpr int S = Ly::kStages;
   constexpr int NA = Ly::kNumAcc;
   extern __shared__ uint8_t smem_raw[];
@@ -883,36 +957,71 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC)>()>::kThreads, 1
             // scale atoms this stage loads (FP4 with one scale per 32 values: half)
             const int atoms_ld = IC == IC_F4E8 ? p.sf_atoms : Ly::kAtoms;
             const uint32_t sf_tx = static_cast<uint32_t>(atoms_ld * 512 * (1 + Ly::kHalves));
-            const int k0 = ks * kBKBytes, ka = 2 * ks * atoms_ld;
+            const int k0 = ks * Ly::kStageK, ka = 2 * ks * atoms_ld;
+            // the K slices of this stage inside K (a two-slice stage at the K
+            // tail may hold only its first); a slice is one box per operand
+            const int kb_bytes = !SCALED ? 2 * p.k : FP4 ? p.k / 2 : p.k;
+            const int nsl = (Ly::kSlices == 1 || k0 + kBKBytes < kb_bytes) ? Ly::kSlices : 1;
+            const uint32_t op_tx = static_cast<uint32_t>(nsl * (Ly::kASlice + Ly::kBSlice));
             const uint32_t sA = sbase + Ly::kOffA + stage * Ly::kABytes;
             const uint32_t sB = sbase + Ly::kOffB + stage * Ly::kBBytes;
             const uint32_t sSa = sbase + Ly::kOffSfa + stage * Ly::kSfaBytes;
             const uint32_t sSb = sbase + Ly::kOffSfb + stage * Ly::kSfbBytes;
+            if constexpr (kDebugBounds) {
+              // box origins: A's 128 rows, the K byte offset, B's n-tile and
+              // slice (a B box may start or run past N: those rows are
+              // zero-filled and their columns are not stored), the
+              // scale boxes' atom row and first 128-row block, inside the
+              // expert's blocks (with N not a multiple of the tile the SFB box
+              // runs on into the next expert's blocks or past the end: those
+              // rows' B data is zero-filled and their columns are not stored)
+              const int v = !FP4 ? 32 : (IC == IC_F4E8 && p.sf_v32) ? 32 : 16;
+              const int kq = ((p.k + v - 1) / v + 3) / 4;
+              const int slices = p.b_maps != nullptr ? 1 : p.L;
+              bool in = in_range(p.status, kSiteARows, mt * kBM + kBM - 1, p.dbg_rows) &&
+                        in_range(p.status, kSiteK, k0, kb_bytes) && in_range(p.status, kSiteBRow, nt, p.num_n_tiles) &&
+                        in_range(p.status, kSiteBSlice, bz, slices);
+              if (SCALED)
+                in = in && in_range(p.status, kSiteSfa, ka, 2 * kq) &&
+                     in_range(p.status, kSiteSfb, nt * Ly::kHalves, p.rn_b) &&
+                     in_range(p.status, kSiteSfb, sfb_rb, p.rn_b * slices);
+              if (!in) {
+                *abort_flag = 1;
+                ok = false;
+                break;
+              }
+            }
             if (PAIR && ST) {
               // both CTAs' operand bytes complete the even CTA's barrier, each
               // CTA's scale bytes its own (its scale warps wait there)
               const uint32_t fbl = mapa_shared(fb, 0);
               const uint32_t sfb_own = sfull_bar(stage);
-              if (leader) mbar_expect_tx(fb, 2u * (Ly::kABytes + Ly::kBBytes));
+              if (leader) mbar_expect_tx(fb, 2u * op_tx);
               mbar_expect_tx(sfb_own, sf_tx);
-              tma_load_2d_pair(sA, &tmA, fbl, k0, mt * kBM);
-              tma_load_3d_pair(sB, mB, fbl, k0, b_row, bz);
+              for (int j = 0; j < nsl; ++j) {
+                tma_load_2d_pair(sA + j * Ly::kASlice, &tmA, fbl, k0 + j * kBKBytes, mt * kBM);
+                tma_load_3d_pair(sB + j * Ly::kBSlice, mB, fbl, k0 + j * kBKBytes, b_row, bz);
+              }
               tma_load_3d(sSa, &tmSFA, sfb_own, 0, ka, mt);
               tma_load_3d(sSb, mSFB, sfb_own, 0, ka, sfb_rb);
             } else if (PAIR) {
               // both CTAs' bytes complete the even CTA's barrier
               const uint32_t fbl = mapa_shared(fb, 0);
-              if (leader) mbar_expect_tx(fb, 2u * Ly::kStageBytes);
-              tma_load_2d_pair(sA, &tmA, fbl, k0, mt * kBM);
-              tma_load_3d_pair(sB, mB, fbl, k0, b_row, bz);
+              if (leader) mbar_expect_tx(fb, 2u * (op_tx + (SCALED ? sf_tx : 0u)));
+              for (int j = 0; j < nsl; ++j) {
+                tma_load_2d_pair(sA + j * Ly::kASlice, &tmA, fbl, k0 + j * kBKBytes, mt * kBM);
+                tma_load_3d_pair(sB + j * Ly::kBSlice, mB, fbl, k0 + j * kBKBytes, b_row, bz);
+              }
               if (SCALED) {
                 tma_load_3d_pair(sSa, &tmSFA, fbl, 0, ka, mt);
                 tma_load_3d_pair(sSb, mSFB, fbl, 0, ka, sfb_rb);
               }
             } else {
-              mbar_expect_tx(fb, Ly::kABytes + Ly::kBBytes + sf_tx);
-              tma_load_2d(sA, &tmA, fb, k0, mt * kBM);
-              tma_load_3d(sB, mB, fb, k0, b_row, bz);
+              mbar_expect_tx(fb, op_tx + (SCALED ? sf_tx : 0u));
+              for (int j = 0; j < nsl; ++j) {
+                tma_load_2d(sA + j * Ly::kASlice, &tmA, fb, k0 + j * kBKBytes, mt * kBM);
+                tma_load_3d(sB + j * Ly::kBSlice, mB, fb, k0 + j * kBKBytes, b_row, bz);
+              }
               if (SCALED) {
                 tma_load_3d(sSa, &tmSFA, fb, 0, ka, mt);
                 tma_load_3d(sSb, mSFB, fb, 0, ka, sfb_rb);
@@ -968,27 +1077,34 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC)>()>::kThreads, 1
         for (int kk = 0; kk < 4; ++kk)
           idk[kk] = (FP4 || !SCALED) ? p.idesc
                                      : (p.idesc | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4));
-        const int full_stages = p.k / Ly::kKElems;      // stages with all four MMAs
+        const int full_stages = p.k / Ly::kKElems;      // stages with all of their MMAs
         auto issue_stage = [&](uint32_t d_tmem, int st, int n_mma, uint32_t acc0) {
           const uint32_t sfa_t = sf_tmem0 + st * Ly::kSfColsPerStage;
           const uint32_t sfb_t = sfa_t + Ly::kSfaCols;
           const uint64_t ad = a_desc0 + static_cast<uint64_t>((st * Ly::kABytes) >> 4);
           const uint64_t bd = b_desc0 + static_cast<uint64_t>((st * Ly::kBBytes) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
+          for (int kk = 0; kk < Ly::kMmas; ++kk) {
             if (kk >= n_mma) break;
             const uint32_t accum = kk ? 1u : acc0;
-            // one MMA consumes 32 K-bytes: +2 in descriptor units
+            // MMA kk reads K bytes [32 (kk % 4), + 32) of slice kk / 4: +2 in
+            // descriptor units per MMA, a slice's bytes / 16 per slice
+            const int sl = kk / 4, kq = kk % 4;
+            const uint64_t adk = ad + static_cast<uint64_t>(sl * (Ly::kASlice >> 4) + 2 * kq);
+            const uint64_t bdk = bd + static_cast<uint64_t>(sl * (Ly::kBSlice >> 4) + 2 * kq);
             if (!SCALED) {
-              if (PAIR) tc_mma_bf16_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], accum);
-              else tc_mma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], accum);
+              if (PAIR) tc_mma_bf16_pair(d_tmem, adk, bdk, idk[kq], accum);
+              else tc_mma_bf16(d_tmem, adk, bdk, idk[kq], accum);
             } else if (FP4) {
+              // one scale atom per MMA
               const uint32_t sa = sfa_t + 4 * kk, sb = sfb_t + 4 * Ly::kHalves * kk;
-              if (PAIR) tc_mma_nvf4_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sa, sb, accum);
-              else tc_mma_nvf4(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sa, sb, accum);
+              if (PAIR) tc_mma_nvf4_pair(d_tmem, adk, bdk, idk[kq], sa, sb, accum);
+              else tc_mma_nvf4(d_tmem, adk, bdk, idk[kq], sa, sb, accum);
             } else {
-              if (PAIR) tc_mma_mxf8_pair(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sfa_t, sfb_t, accum);
-              else tc_mma_mxf8(d_tmem, ad + 2 * kk, bd + 2 * kk, idk[kk], sfa_t, sfb_t, accum);
+              // one scale atom per slice, the instruction descriptor selects its byte
+              const uint32_t sa = sfa_t + 4 * sl, sb = sfb_t + 4 * Ly::kHalves * sl;
+              if (PAIR) tc_mma_mxf8_pair(d_tmem, adk, bdk, idk[kq], sa, sb, accum);
+              else tc_mma_mxf8(d_tmem, adk, bdk, idk[kq], sa, sb, accum);
             }
           }
           // release the stage (in both CTAs of a cluster)
@@ -1009,7 +1125,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC)>()>::kThreads, 1
             if (!mbar_wait(ready, phase, abort_flag, p.wait_limit_ns)) { ok = false; break; }
             tc_fence_after();
             if (ks < full_stages) {
-              issue_stage(d_tmem, stage, 4, ks ? 1u : 0u);
+              issue_stage(d_tmem, stage, Ly::kMmas, ks ? 1u : 0u);
             } else {
               const int k_left = p.k - ks * Ly::kKElems;
               issue_stage(d_tmem, stage, (k_left + Ly::kMmaK - 1) / Ly::kMmaK, ks ? 1u : 0u);
@@ -1205,6 +1321,15 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC)>()>::kThreads, 1
         if (kChunkLd) release();
         continue;
       }
+      if constexpr (kDebugBounds) {
+        // the rows of prob / D / dprob this warp touches and the group of alpha, bias, amax
+        const bool in = in_range(p.status, kSiteDRow, mt * kBM + q * 32 + lane, p.dbg_rows) &&
+                        in_range(p.status, kSiteGroup, g, p.L);
+        if (__any_sync(0xffffffffu, !in)) {
+          if (kChunkLd) release();
+          continue;
+        }
+      }
       const int row = mt * kBM + q * 32 + lane;
       const float pr = p.prob[row];
       const float al = p.alpha[g];
@@ -1229,7 +1354,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC)>()>::kThreads, 1
                          static_cast<const uint8_t*>(p.bias) + (static_cast<int64_t>(g) * p.n + col0) * esz,
                          p.bias_kind);
             }
-            if (p.c_out != nullptr) store_c32(p, &r[32 * c], row, col0);
+            if (p.c_out != nullptr && in_range(p.status, kSiteC, col0 + 31, p.n)) store_c32(p, &r[32 * c], row, col0);
           }
         }
         al_epi = 1.0f;
@@ -1322,7 +1447,7 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC)>()>::kThreads, 1
           }
           output_chunk<IC, OUTC>(p, x, row, xo, norm, lane, kblk_col, amax_local);
           output_chunk<IC, OUTC>(p, gv, row, go, norm, lane, kblk_col, amax_local2);
-          if (XC && p.dbias != nullptr) {
+          if (XC && p.dbias != nullptr && in_range(p.status, kSiteDbias, max(xo, go) + 31, p.n_out)) {
             float* db = p.dbias + static_cast<int64_t>(g) * p.n_out;
             add_column_sums32(x, db + xo, lane);
             add_column_sums32(gv, db + go, lane);

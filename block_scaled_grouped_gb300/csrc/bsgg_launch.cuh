@@ -18,7 +18,7 @@ cudaError_t launch_one(const Launch& L) {
   constexpr bool kCluster = CM != CM_SINGLE;
   constexpr bool kStores = scale_stores<FP4>();
   using Ro = Roles<kStores>;
-  const int smem = Layout<FP4, BN, CM == CM_PAIR, ic_scaled(IC)>::kSmemBytes;
+  const int smem = Layout<FP4, BN, CM == CM_PAIR, ic_scaled(IC), stage_slices(IC, CM)>::kSmemBytes;
   // The function attributes are set once per device and instance.  Bit d of
   // `configured` says device d is done; host threads that launch this instance
   // at the same time serialise on the mutex until the bit is set.
@@ -122,7 +122,7 @@ template <int IC>
 int cluster_resident_ctas_impl() {
   constexpr bool FP4 = ic_fp4(IC);
   auto kern = bsgg_kernel<IC, 256, CM_PAIR, EPI_GATE, OUTC_FLOAT, false>;
-  const int smem = Layout<FP4, 256, true>::kSmemBytes;
+  const int smem = Layout<FP4, 256, true, true, stage_slices(IC, CM_PAIR)>::kSmemBytes;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);

@@ -71,6 +71,16 @@
 extern "C" {
 #endif
 
+/* Every entry point below is exported with default visibility; the library is
+ * compiled with hidden visibility otherwise, so that two builds of it (the
+ * release and the range-checking one) can live in one process without sharing
+ * any internal symbol. */
+#if defined(__GNUC__)
+#define BSGG_API __attribute__((visibility("default")))
+#else
+#define BSGG_API
+#endif
+
 typedef enum {
   BSGG_OK = 0,
   BSGG_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, bad shape or enum */
@@ -79,9 +89,12 @@ typedef enum {
   BSGG_ERR_DEVICE_TIMEOUT = 4,  /* a kernel wait ran out; the kernel returned early */
   BSGG_ERR_BAD_OFFSETS = 5,     /* padded_offsets not non-decreasing multiples of 128
                                    ending at m_pad; the kernel wrote nothing */
-  BSGG_ERR_BAD_POINTERS = 6     /* discrete weight mode: a b_ptrs / sfb_ptrs entry of a
+  BSGG_ERR_BAD_POINTERS = 6,    /* discrete weight mode: a b_ptrs / sfb_ptrs entry of a
                                    non-empty group is null or not 16-byte aligned; the
                                    kernel wrote nothing */
+  BSGG_ERR_DEVICE_BOUNDS = 7    /* range-checking build only (libbsgg_debug.so): an index
+                                   failed its range check; that access was skipped (see
+                                   bsgg_debug_bounds_violation) */
 } bsgg_status;
 
 /* Input formats ("Grouped GEMM + Quant (SM100)", Data Types table). */
@@ -268,11 +281,11 @@ typedef struct bsgg_plan bsgg_plan;
  * device status word).  The plan belongs to the device that is current at
  * creation.  Returns BSGG_ERR_INVALID_ARG / BSGG_ERR_UNSUPPORTED for
  * descriptions the pages or this build reject; *plan is NULL then. */
-bsgg_status bsgg_create(const bsgg_desc* desc, bsgg_plan** plan);
+BSGG_API bsgg_status bsgg_create(const bsgg_desc* desc, bsgg_plan** plan);
 
 /* Enqueue one grouped GEMM on `stream` (asynchronous, no host sync, graph
  * capturable).  Checks pointers for presence and 16-byte alignment. */
-bsgg_status bsgg_run(bsgg_plan* plan, const bsgg_args* args, void* stream);
+BSGG_API bsgg_status bsgg_run(bsgg_plan* plan, const bsgg_args* args, void* stream);
 
 /* End-to-end call with HOST buffers: `host` holds host pointers (pinned for
  * speed) for every input and output to move; `dev` holds device buffers of the
@@ -283,18 +296,18 @@ bsgg_status bsgg_run(bsgg_plan* plan, const bsgg_args* args, void* stream);
  * (either may be NULL).  Allocates nothing.  In discrete weight mode the
  * experts' weights are taken as resident (dev->b_ptrs / dev->sfb_ptrs; host->b
  * and host->sfb must be NULL). */
-bsgg_status bsgg_run_host(bsgg_plan* plan, const bsgg_args* host, const bsgg_args* dev,
+BSGG_API bsgg_status bsgg_run_host(bsgg_plan* plan, const bsgg_args* host, const bsgg_args* dev,
                           void* stream, uint64_t* h2d_bytes, uint64_t* d2h_bytes);
 
 /* Number of kernel launches one bsgg_run of this plan enqueues (the pages have
  * no counterpart): 1, or 2 in discrete weight mode (the per-expert descriptor
  * kernel, then the GEMM).  -1 for a null plan. */
-int32_t bsgg_launches_per_run(const bsgg_plan* plan);
+BSGG_API int32_t bsgg_launches_per_run(const bsgg_plan* plan);
 
 /* Synchronize `stream`, then read and clear the plan's device status word:
  * BSGG_OK, BSGG_ERR_DEVICE_TIMEOUT, BSGG_ERR_BAD_OFFSETS or BSGG_ERR_BAD_POINTERS
  * (a status bit the library does not define reads as BSGG_ERR_CUDA). */
-bsgg_status bsgg_query_device_status(bsgg_plan* plan, void* stream);
+BSGG_API bsgg_status bsgg_query_device_status(bsgg_plan* plan, void* stream);
 
 /* Test hook for the failure path; the pages have no counterpart.  With enable =
  * 1, every later bsgg_run / bsgg_run_host of this plan launches a kernel whose
@@ -303,23 +316,23 @@ bsgg_status bsgg_query_device_status(bsgg_plan* plan, void* stream);
  * in-flight work and returns, no output is complete, and the status word reads
  * BSGG_ERR_DEVICE_TIMEOUT; the CUDA context stays usable.  enable = 0 restores
  * normal launches.  Errors: BSGG_ERR_INVALID_ARG (null plan, enable not 0/1). */
-bsgg_status bsgg_debug_force_timeout(bsgg_plan* plan, int32_t enable);
+BSGG_API bsgg_status bsgg_debug_force_timeout(bsgg_plan* plan, int32_t enable);
 
-void bsgg_destroy(bsgg_plan* plan);
-const char* bsgg_status_string(bsgg_status status);
+BSGG_API void bsgg_destroy(bsgg_plan* plan);
+BSGG_API const char* bsgg_status_string(bsgg_status status);
 
 /* Bytes of the swizzled SF(rows, cols) layout with L slices and vector v:
  * 512 * L * ceil(rows/128) * ceil(ceil(cols/v)/4). */
-uint64_t bsgg_sf_bytes(int64_t rows, int64_t cols, int32_t sf_vec, int32_t num_slices);
+BSGG_API uint64_t bsgg_sf_bytes(int64_t rows, int64_t cols, int32_t sf_vec, int32_t num_slices);
 
 /* Byte offset of the scale of (row, k-block, slice l) in that layout, where
  * kblocks = ceil(cols/v).  Pure host function. */
-int64_t bsgg_sf_offset(int64_t row, int64_t kblk, int64_t l, int64_t rows, int64_t kblocks);
+BSGG_API int64_t bsgg_sf_offset(int64_t row, int64_t kblk, int64_t l, int64_t rows, int64_t kblocks);
 
 /* Pack row-major scale codes (L, rows, kblocks) into the swizzled layout,
  * writing every byte (padding = 0, "Grouped GEMM + SwiGLU (SM100)", JAX
  * execution: untouched SF padding is zero).  Device pointers; asynchronous. */
-bsgg_status bsgg_pack_sf(const uint8_t* rowmajor, uint8_t* swizzled, int64_t rows,
+BSGG_API bsgg_status bsgg_pack_sf(const uint8_t* rowmajor, uint8_t* swizzled, int64_t rows,
                          int64_t kblocks, int32_t num_slices, void* stream);
 
 /* Size of the library-owned device scratch used by bsgg_run_noalloc. */
@@ -334,19 +347,20 @@ bsgg_status bsgg_pack_sf(const uint8_t* rowmajor, uint8_t* swizzled, int64_t row
  * that must not let cudaMalloc/cudaFree synchronize the device, or a plug-in
  * inside a host application that owns memory management.
  *
- * The kernel's only scratch, its 4-byte device status word, lives in a
- * file-scope static device array of BSGG_NOALLOC_SCRATCH_BYTES bytes that every
- * GPU which loads the library holds until the process exits.  A call whose
- * scratch need exceeds that array is rejected with BSGG_ERR_UNSUPPORTED: the
- * need is one word, except in discrete weight mode, whose per-expert
- * descriptors (256 * L + 256 bytes) never fit, so discrete_b = 1 is rejected.
+ * The kernel's only scratch, its device status word (16 bytes with the record a
+ * range-checking build keeps behind it), lives in a file-scope static device
+ * array of BSGG_NOALLOC_SCRATCH_BYTES bytes that every GPU which loads the
+ * library holds until the process exits.  A call whose scratch need exceeds
+ * that array is rejected with BSGG_ERR_UNSUPPORTED: the need is those 16 bytes,
+ * except in discrete weight mode, whose per-expert descriptors (256 * L + 256
+ * bytes) never fit, so discrete_b = 1 is rejected.
  *
  * The first call on a device looks up the array's device address with that
  * device current (cudaGetSymbolAddress) and remembers it with the id of the
  * device's context; a call that finds a different context (after
  * cudaDeviceReset, say) looks it up again.  Make the first call on a device,
  * and the first after a reset, before any stream capture.  Every call clears
- * the status word on `stream` before its kernel.  All calls share the array, which keeps the last call's contents:
+ * the 16 status bytes on `stream` before its kernel.  All calls share the array, which keeps the last call's contents:
  * calls whose kernels overlap on the GPU (several streams, several host
  * threads) race on it, so run them on one stream when the status matters.
  * With wait_status != 0 the call synchronizes `stream` after the launch and
@@ -354,8 +368,34 @@ bsgg_status bsgg_pack_sf(const uint8_t* rowmajor, uint8_t* swizzled, int64_t row
  * BSGG_ERR_DEVICE_TIMEOUT or BSGG_ERR_BAD_OFFSETS; a status bit the library
  * does not define reads as BSGG_ERR_CUDA); with 0 it returns once the kernel
  * is enqueued. */
-bsgg_status bsgg_run_noalloc(const bsgg_desc* desc, const bsgg_args* args, void* stream,
+BSGG_API bsgg_status bsgg_run_noalloc(const bsgg_desc* desc, const bsgg_args* args, void* stream,
                              int32_t wait_status);
+
+/* Range-checking build; the pages have no counterpart.  The library is also
+ * built as libbsgg_debug.so with every TMA box origin (A rows, K offset, B row
+ * and slice, scale-factor atoms), every output index (D and D_col rows and
+ * columns, SFD_row / SFD_col offsets, C, the Hadamard output, dbias) and every
+ * per-row / per-group read (prob, alpha) checked against the problem's extents
+ * before use.  A failed check skips the access, records the first failure and
+ * raises a status bit that bsgg_query_device_status returns as
+ * BSGG_ERR_DEVICE_BOUNDS; a failure in the operand loads also makes every role
+ * of the CTA give up and drain as after a timeout.  No trap, no fault.  The
+ * release build compiles the checks away.
+ *
+ * bsgg_debug_bounds_checked: 1 in the range-checking build, 0 otherwise.
+ * bsgg_debug_bounds_margin: test hook: later launches of the plan check rows
+ *   against m_pad - rows instead of m_pad (rows: a multiple of 128 below m_pad),
+ *   so that in-range accesses fail their checks without any out-of-range access
+ *   being made; barrier waits are then bounded by 50 ms.  0 restores the checks.
+ *   BSGG_ERR_UNSUPPORTED in the release build; BSGG_ERR_INVALID_ARG for other rows.
+ * bsgg_debug_bounds_violation: the failure recorded by the last
+ *   bsgg_query_device_status that returned BSGG_ERR_DEVICE_BOUNDS (site code,
+ *   value, limit; all 0 if none).  Site codes: 1 A rows, 2 B n-tile, 3 B slice,
+ *   4 SFA atom, 5 SFB row block, 6 K offset, 10 D row, 11 D column, 12 SFD_row,
+ *   13 SFD_col, 15 C column, 16 Hadamard output, 18 dbias column, 19 group. */
+BSGG_API int32_t bsgg_debug_bounds_checked(void);
+BSGG_API bsgg_status bsgg_debug_bounds_margin(bsgg_plan* plan, int32_t rows);
+BSGG_API bsgg_status bsgg_debug_bounds_violation(const bsgg_plan* plan, uint32_t* site, uint32_t* value, uint32_t* limit);
 
 /* Measurement utility; the pages have no counterpart.  Measures the dense
  * block-scaled tensor-core throughput of the current device, the denominator of
@@ -368,7 +408,7 @@ bsgg_status bsgg_run_noalloc(const bsgg_desc* desc, const bsgg_args* args, void*
  * 4-byte status word.  Errors: BSGG_ERR_INVALID_ARG for other arguments,
  * BSGG_ERR_CUDA for a failed CUDA call, BSGG_ERR_DEVICE_TIMEOUT if the final
  * wait ran out (2 s). */
-bsgg_status bsgg_measure_mma_peak(int32_t in_format, int32_t tile_n, int64_t mmas_per_sm, double* tflops,
+BSGG_API bsgg_status bsgg_measure_mma_peak(int32_t in_format, int32_t tile_n, int64_t mmas_per_sm, double* tflops,
                                   void* stream);
 
 /* Measurement utility; the pages have no counterpart.  The same measurement for
@@ -383,7 +423,7 @@ bsgg_status bsgg_measure_mma_peak(int32_t in_format, int32_t tile_n, int64_t mma
  * arguments bsgg_measure_mma_peak refuses (mmas: 4 .. 2^22 per issuing thread),
  * BSGG_ERR_UNSUPPORTED for tile_m = 256 with tile_n = 128, BSGG_ERR_CUDA for a
  * failed CUDA call, BSGG_ERR_DEVICE_TIMEOUT if the final wait ran out (2 s). */
-bsgg_status bsgg_measure_mma_peak_tile(int32_t in_format, int32_t tile_m, int32_t tile_n, int64_t mmas,
+BSGG_API bsgg_status bsgg_measure_mma_peak_tile(int32_t in_format, int32_t tile_m, int32_t tile_n, int64_t mmas,
                                        double* tflops, void* stream);
 
 #ifdef __cplusplus

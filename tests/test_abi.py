@@ -36,6 +36,19 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_range_checking_build_exports_the_same_symbols(lib):
+    """libbsgg_debug.so (-DBSGG_DEBUG_BOUNDS) has the same entry points; only it
+    reports the checks as compiled in, and only it accepts a test margin."""
+    bsgg_build.build(debug_bounds=True)
+    dbg = bsgg.lib(debug_bounds=True)
+    for name in declared_functions():
+        assert hasattr(dbg, name), name
+    assert dbg.bsgg_debug_bounds_checked() == 1
+    assert lib.bsgg_debug_bounds_checked() == 0
+    assert lib.bsgg_debug_bounds_margin(None, 0) == 1 and dbg.bsgg_debug_bounds_margin(None, 0) == 1
+    assert lib.bsgg_debug_bounds_violation(None, None, None, None) == 1
+
+
 def test_status_strings(lib):
     for code, text in bsgg.STATUS.items():
         assert lib.bsgg_status_string(code).decode() == text

@@ -67,6 +67,29 @@ def test_single_group_f32_and_f16(tile):
 
 
 @pytest.mark.parametrize("tile", TILES, ids=tile_id)
+def test_f16_overflow_reads_as_infinity(tile):
+    """F16 D beyond the format's range is converted as IEEE round-to-nearest-
+    even does: |D| >= 65520 (half-way to the next binade) becomes +-inf, no
+    saturation.  The per-group amax is taken from the unrounded D, so it stays
+    finite and matches the oracle's.  alpha = 2048 on the first group puts a
+    part of its D above the range; the second group stays inside it."""
+    p = small_problem(counts=(256, 100), k=512, n=256, pad_to=128, out_fmt="f16", seed=27,
+                      alpha=[2048.0, 1.0])
+    ref = oracle_run(p)
+    outs, _, _ = run_gpu(p, tile=tile)
+    from gpu_harness import decode_float_out, check_float_d
+    d = decode_float_out(outs["d"].cpu().numpy(), "f16", p.m_pad, p.n_out)
+    r = ref["d_ref"]
+    over = np.abs(r) >= 65520.0 * (1 + 2.0 ** -7)
+    inside = np.abs(r) <= 65504.0 * (1 - 2.0 ** -7)
+    assert over.sum() > 100 and inside.sum() > 100, (over.sum(), inside.sum())
+    assert np.all(np.isinf(d[over])) and np.all(np.sign(d[over]) == np.sign(r[over]))
+    check_float_d(d[inside], r[inside])
+    assert np.all(np.isfinite(outs["amax"].cpu().numpy()))
+    np.testing.assert_allclose(outs["amax"].cpu().numpy(), ref["amax"], rtol=2.0 ** -10, atol=0)
+
+
+@pytest.mark.parametrize("tile", TILES, ids=tile_id)
 def test_e5m2_inputs(tile):
     p = small_problem(counts=(128, 100), k=256, n=128, pad_to=128, in_fmt="mxfp8_e5m2", seed=24)
     _parity(p, tile=tile)

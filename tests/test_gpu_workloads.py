@@ -6,7 +6,8 @@ sampled 32-row blocks -- each group's first and last block, the first and last
 block of the problem and random blocks -- with the same tolerances as the
 small parity tests.  For BF16 outputs the per-group amax is checked over whole
 groups against the GPU's own D (|amax - max|D_bf16|| <= 2^-8 amax, as D_bf16 is
-D rounded to 8 significant bits)."""
+D rounded to 8 significant bits), and, for the two smallest non-empty groups
+of the FC2 workload, against the oracle run over every row of those groups."""
 import numpy as np
 import pytest
 import torch
@@ -78,6 +79,27 @@ def test_full_size_parity_on_sampled_blocks(workload, tile):
         # the oracle's amax over the sampled rows bounds the full amax from below
         sampled = ref["amax"]
         assert np.all(amax >= sampled * (1 - 2.0 ** -20))
+
+
+def test_full_size_group_amax_against_oracle():
+    """Per-group amax of the FC2 gated workload (BF16 D, K=14336, N=4096) for
+    its two smallest non-empty groups, every 32-row block of them computed by
+    the oracle: within 2^-10 relative, as in the small parity tests ("Grouped
+    GEMM + Quant (SM100)", Outputs: amax per group for bfloat16 D)."""
+    p = W.workload("fc2_gate", device="cuda")
+    off = np_(p.padded_offsets)
+    starts = np.concatenate([[0], off[:-1]])
+    nonempty = [g for g in range(p.num_groups) if p.counts[g] > 0]
+    groups = sorted(nonempty, key=lambda g: (p.counts[g], g))[:2]
+    blocks = np.concatenate([np.arange(starts[g] // 32, off[g] // 32) for g in groups]).astype(np.int64)
+    ref = _oracle(p, blocks)
+    outs, _, _ = run_gpu(p)
+    amax = outs["amax"].cpu().numpy()
+    for g in groups:
+        assert ref["amax"][g] > 0.0
+        np.testing.assert_allclose(amax[g], ref["amax"][g], rtol=2.0 ** -10, atol=0, err_msg=f"group {g}")
+    del p, outs
+    torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("name", ["fc1_dswiglu", "fc1_dswiglu_bf16"])
