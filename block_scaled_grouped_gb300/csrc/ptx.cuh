@@ -32,14 +32,20 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Test phase `parity`, suspending the thread for at most kSuspendHintNs while
+// it is incomplete.  Without the hint a suspended thread was woken well after
+// the phase completed: on GB300 the hint (any value from 8 to 512 ns) raised
+// the CTA pairs by 3.5-4.6 % (FC1, FC2, NVFP4), all of it from the waits of
+// the producer, scale and MMA threads.
+constexpr uint32_t kSuspendHintNs = 32;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
