@@ -276,6 +276,24 @@ bsgg_status encode_maps(const bsgg_plan* P, const bsgg_args* a, bsgg::Launch* L)
   return BSGG_OK;
 }
 
+// D and D_col as byte tensors (row bytes, m_pad) whose boxes are one warp's
+// 32-row chunk (32 values: 64 bytes of bf16/f16, 32 of FP8, 16 of packed FP4),
+// stored by the epilogue through TMA; fp32 D is stored directly (zero maps).
+bsgg_status encode_out_maps(const bsgg_plan* P, const bsgg_args* a, bsgg::Launch* L) {
+  const bsgg_desc& d = P->desc;
+  std::memset(&L->tmD, 0, sizeof(L->tmD));
+  std::memset(&L->tmDcol, 0, sizeof(L->tmDcol));
+  if (d.out_format == BSGG_OUT_F32) return BSGG_OK;
+  const cuuint32_t chunk = static_cast<cuuint32_t>(32 * out_elem_bits(d.out_format) / 8);
+  cuuint64_t dims[2] = {cuuint64_t(P->out_row_bytes), cuuint64_t(d.m_pad)};
+  cuuint64_t strides[1] = {cuuint64_t(P->out_row_bytes)};
+  cuuint32_t box[2] = {chunk, 32};
+  bsgg_status st = encode_one(&L->tmD, a->d, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st == BSGG_OK && d.want_col)
+    st = encode_one(&L->tmDcol, a->d_col, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+  return st;
+}
+
 // Everything a plan derives from its description and the current device.
 bsgg_status init_plan(const bsgg_desc* desc, int device, int num_sms, bsgg_plan* P) {
   P->desc = *desc;
@@ -532,6 +550,7 @@ bsgg_status bsgg_run(bsgg_plan* P, const bsgg_args* a, void* stream) {
   Launch L;
   std::memset(&L, 0, sizeof(L));
   st = encode_maps(P, a, &L);
+  if (st == BSGG_OK) st = encode_out_maps(P, a, &L);
   if (st != BSGG_OK) return st;
   // amax: one float per group, two for the backward (input / gate gradients)
   const int64_t n_amax = d.num_groups * (is_bwd_epi(d.epilogue) ? 2 : 1);

@@ -14,6 +14,8 @@ struct Launch {
   CUtensorMap tmB;
   CUtensorMap tmSFA;
   CUtensorMap tmSFB;
+  CUtensorMap tmD;      // D and D_col as (row bytes, m_pad) byte tensors, boxes of one 32-row chunk
+  CUtensorMap tmDcol;   // (zero where the output is not stored through TMA)
   Params p;
   int grid;      // CTAs (a multiple of 2 for clusters)
   int bn;        // 128 or 256

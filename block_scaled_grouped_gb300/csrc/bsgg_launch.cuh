@@ -64,7 +64,7 @@ cudaError_t launch_one(const Launch& L) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmSFA, L.tmSFB, L.p);
+  return cudaLaunchKernelEx(&cfg, kern, L.tmA, L.tmB, L.tmSFA, L.tmSFB, L.tmD, L.tmDcol, L.p);
 }
 
 template <int IC, int BN, int CM, int EPI, bool XC>
