@@ -204,9 +204,17 @@ def test_bad_offsets_are_reported_and_nothing_is_written():
         assert (outs["d"] == SENTINEL).all()
 
 
-def test_host_buffer_call_matches_device_call():
-    p = small_problem(counts=(200, 60), k=256, n=256, pad_to=128, epi="swiglu", out_fmt="e4m3",
-                      want_col=True, seed=35)
+@pytest.mark.parametrize("size", ["small", "large"])
+def test_host_buffer_call_matches_device_call(size):
+    """bsgg_run_host against bsgg_run on the same inputs, bit for bit, on a small
+    problem and on one whose A, B, D and D_col copies are several MB each."""
+    if size == "small":
+        p = small_problem(counts=(200, 60), k=256, n=256, pad_to=128, epi="swiglu", out_fmt="e4m3",
+                          want_col=True, seed=35)
+    else:
+        p = small_problem(counts=(1500, 700), k=2048, n=4096, pad_to=128, epi="swiglu", out_fmt="e4m3",
+                          want_col=True, seed=36)
+        assert p.a.numel() >= 4 << 20 and p.m_pad * p.n // 2 >= 4 << 20
     pd = to_device(p)
     outs, sfa, sfb = run_gpu(pd)
     plan = make_plan(pd)
