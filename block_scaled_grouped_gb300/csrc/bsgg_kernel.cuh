@@ -450,21 +450,32 @@ __device__ __forceinline__ void load_f32x32(float (&v)[32], const void* src, int
   }
 }
 
+// Two products: one packed f32x2 multiply, or (PACKED false: the backward
+// epilogues, whose register allocation spills with the packed form) two
+// scalar ones; the same round-to-nearest results either way.
+template <bool PACKED>
+__device__ __forceinline__ float2 mul_pair(float a0, float a1, float b0, float b1) {
+  if (PACKED) return __fmul2_rn(make_float2(a0, a1), make_float2(b0, b1));
+  return make_float2(a0 * b0, a1 * b1);
+}
+
 // 32 values of one row -> quantized codes stored at `dst` (32 bytes for FP8,
 // 16 bytes for FP4), each value multiplied by its block's scale first.
-template <int OUTC, typename Dst>
+template <int OUTC, bool PACKED = true, typename Dst>
 __device__ __forceinline__ void store_q32_to(Dst dst, const float (&v)[32], const float (&sc)[32], int out_kind) {
   if (OUTC == OUTC_FP8) {
     uint32_t w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       uint32_t lo, hi;
+      const float2 a = mul_pair<PACKED>(v[4 * i], v[4 * i + 1], sc[4 * i], sc[4 * i + 1]);
+      const float2 b = mul_pair<PACKED>(v[4 * i + 2], v[4 * i + 3], sc[4 * i + 2], sc[4 * i + 3]);
       if (out_kind == OK_E4M3) {
-        lo = cvt_e4m3x2(v[4 * i] * sc[4 * i], v[4 * i + 1] * sc[4 * i + 1]);
-        hi = cvt_e4m3x2(v[4 * i + 2] * sc[4 * i + 2], v[4 * i + 3] * sc[4 * i + 3]);
+        lo = cvt_e4m3x2(a.x, a.y);
+        hi = cvt_e4m3x2(b.x, b.y);
       } else {
-        lo = cvt_e5m2x2(v[4 * i] * sc[4 * i], v[4 * i + 1] * sc[4 * i + 1]);
-        hi = cvt_e5m2x2(v[4 * i + 2] * sc[4 * i + 2], v[4 * i + 3] * sc[4 * i + 3]);
+        lo = cvt_e5m2x2(a.x, a.y);
+        hi = cvt_e5m2x2(b.x, b.y);
       }
       w[i] = lo | (hi << 16);
     }
@@ -478,16 +489,53 @@ __device__ __forceinline__ void store_q32_to(Dst dst, const float (&v)[32], cons
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int e = 8 * i + 2 * j;
-        x |= cvt_e2m1x2(v[e] * sc[e], v[e + 1] * sc[e + 1]) << (8 * j);
+        const float2 q = mul_pair<PACKED>(v[e], v[e + 1], sc[e], sc[e + 1]);
+        x |= cvt_e2m1x2(q.x, q.y) << (8 * j);
       }
       w[i] = x;
     }
     put16(dst, 0, w[0], w[1], w[2], w[3]);
   }
 }
-template <int OUTC>
+template <int OUTC, bool PACKED = true>
 __device__ __forceinline__ void store_q32(void* dst, const float (&v)[32], const float (&sc)[32], int out_kind) {
-  store_q32_to<OUTC>(static_cast<uint8_t*>(dst), v, sc, out_kind);
+  store_q32_to<OUTC, PACKED>(static_cast<uint8_t*>(dst), v, sc, out_kind);
+}
+
+// The codes of 32 values of one row whose column j is scaled by lane j's
+// `scale` (the 32-row column blocks of the MXFP8 path), each factor fetched
+// from its lane as its codes are formed.
+template <int OUTC, typename Dst>
+__device__ __forceinline__ void store_q32_cols_to(Dst dst, const float (&v)[32], float scale, int out_kind) {
+  auto scaled = [&](int e) {
+    return __fmul2_rn(make_float2(v[e], v[e + 1]),
+                      make_float2(__shfl_sync(0xffffffffu, scale, e), __shfl_sync(0xffffffffu, scale, e + 1)));
+  };
+  if (OUTC == OUTC_FP8) {
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 a = scaled(4 * i), b = scaled(4 * i + 2);
+      const uint32_t lo = out_kind == OK_E4M3 ? cvt_e4m3x2(a.x, a.y) : cvt_e5m2x2(a.x, a.y);
+      const uint32_t hi = out_kind == OK_E4M3 ? cvt_e4m3x2(b.x, b.y) : cvt_e5m2x2(b.x, b.y);
+      w[i] = lo | (hi << 16);
+    }
+    put16(dst, 0, w[0], w[1], w[2], w[3]);
+    put16(dst, 16, w[4], w[5], w[6], w[7]);
+  } else {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 q = scaled(8 * i + 2 * j);
+        x |= cvt_e2m1x2(q.x, q.y) << (8 * j);
+      }
+      w[i] = x;
+    }
+    put16(dst, 0, w[0], w[1], w[2], w[3]);
+  }
 }
 
 // The stored pre-activation C of one row's 32-column chunk (fp32 bit patterns):
@@ -557,7 +605,7 @@ struct OutStage {
 // a staging slot the warp writes its 32 rows' chunk bytes into it (row after
 // row, as the TMA box lays them out) and one lane stores the whole 32-row box
 // with a TMA store; the scale factors are stored directly either way.
-template <int IC, int OUTC>
+template <int IC, int OUTC, bool BWD = false>
 __device__ __forceinline__ void output_chunk(const Params& p, const float (&v)[32], int row, int col0,
                                              float norm, int lane, int kblk_col, float& amax_local,
                                              const OutStage& os) {
@@ -651,8 +699,8 @@ __device__ __forceinline__ void output_chunk(const Params& p, const float (&v)[3
       p.sfd_row[sf_off(row, col0 / 32, p.kq_row)] = static_cast<uint8_t>(code);
     }
     store_x = static_cast<int>(col_byte0);
-    if (staged) store_q32_to<OUTC>(d_stage, v, sc, p.out_kind);
-    else store_q32<OUTC>(static_cast<uint8_t*>(p.d) + row * row_bytes + col_byte0, v, sc, p.out_kind);
+    if (staged) store_q32_to<OUTC, !BWD>(d_stage, v, sc, p.out_kind);
+    else store_q32<OUTC, !BWD>(static_cast<uint8_t*>(p.d) + row * row_bytes + col_byte0, v, sc, p.out_kind);
     // ---- column blocks of v rows: the warp's 32 lanes are its 32 rows
     if (p.want_col) {
       if (!FP4) {
@@ -667,10 +715,18 @@ __device__ __forceinline__ void output_chunk(const Params& p, const float (&v)[3
         uint32_t my_code;
         float my_scale;
         block_scale<false>(my_am, norm, p.rcp_qmax, my_code, my_scale);
+        uint8_t* const dcol = static_cast<uint8_t*>(p.d_col) + row * row_bytes + col_byte0;
+        if (BWD) {
+          // the backward epilogues gather the 32 factors first (streamed, their
+          // register allocation spills)
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sc[j] = __shfl_sync(0xffffffffu, my_scale, j);
-        if (staged) store_q32_to<OUTC>(dcol_stage, v, sc, p.out_kind);
-        else store_q32<OUTC>(static_cast<uint8_t*>(p.d_col) + row * row_bytes + col_byte0, v, sc, p.out_kind);
+          for (int j = 0; j < 32; ++j) sc[j] = __shfl_sync(0xffffffffu, my_scale, j);
+          if (staged) store_q32_to<OUTC, false>(dcol_stage, v, sc, p.out_kind);
+          else store_q32<OUTC, false>(dcol, v, sc, p.out_kind);
+        } else {
+          if (staged) store_q32_cols_to<OUTC>(dcol_stage, v, my_scale, p.out_kind);
+          else store_q32_cols_to<OUTC>(dcol, v, my_scale, p.out_kind);
+        }
         p.sfd_col[sf_off(col0 + lane, kblk_col, p.kq_col)] = static_cast<uint8_t>(my_code);
       } else {
         // FP4: each half-warp is one 16-row block (the whole warp one 32-row
@@ -702,8 +758,8 @@ __device__ __forceinline__ void output_chunk(const Params& p, const float (&v)[3
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           sc[j] = __shfl_sync(0xffffffffu, j < 16 ? sc_lo : sc_hi, 16 * h + (j & 15));
-        if (staged) store_q32_to<OUTC>(dcol_stage, v, sc, p.out_kind);
-        else store_q32<OUTC>(static_cast<uint8_t*>(p.d_col) + row * row_bytes + col_byte0, v, sc, p.out_kind);
+        if (staged) store_q32_to<OUTC, !BWD>(dcol_stage, v, sc, p.out_kind);
+        else store_q32<OUTC, !BWD>(static_cast<uint8_t*>(p.d_col) + row * row_bytes + col_byte0, v, sc, p.out_kind);
         if (!v32 || h == 0) {
           const int kb = v32 ? kblk_col : 2 * kblk_col + h;   // row-block index
           p.sfd_col[sf_off(col0 + i, kb, p.kq_col)] = static_cast<uint8_t>(code_lo);
@@ -836,33 +892,49 @@ __device__ __forceinline__ void epilogue_chunk(const Params& p, const uint32_t* 
                                                int col0, float al, float pr, float norm, int lane, int kblk_col,
                                                float& amax_local, int64_t seg_start, int seg_rows,
                                                const OutStage& os) {
+  // two values per instruction where the arithmetic is a plain product or sum
+  // (packed f32x2, the same IEEE round-to-nearest as the scalar operations)
   float v[32];
+  const float2 al2 = make_float2(al, al), pr2 = make_float2(pr, pr);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float c = al * __uint_as_float(xs[i]);
+  for (int i = 0; i < 32; i += 2) {
+    const float2 c = __fmul2_rn(al2, make_float2(__uint_as_float(xs[i]), __uint_as_float(xs[i + 1])));
+    float2 o;
     if (EPI == EPI_GATE) {
-      v[i] = pr * c;
+      o = __fmul2_rn(pr2, c);
     } else if (EPI == EPI_SRELU) {
-      float r = fmaxf(c, 0.0f);
-      if (p.tanh_s > 0.0f) r = p.tanh_s * fminf(tanh_approx(r * p.tanh_rcp_s), 1.0f);
-      v[i] = pr * (r * r);
+      float2 r = make_float2(fmaxf(c.x, 0.0f), fmaxf(c.y, 0.0f));
+      if (p.tanh_s > 0.0f) {
+        const float2 t = __fmul2_rn(r, make_float2(p.tanh_rcp_s, p.tanh_rcp_s));
+        r = __fmul2_rn(make_float2(p.tanh_s, p.tanh_s),
+                       make_float2(fminf(tanh_approx(t.x), 1.0f), fminf(tanh_approx(t.y), 1.0f)));
+      }
+      o = __fmul2_rn(pr2, __fmul2_rn(r, r));
     } else {
       // SwiGLU: X * G * sigmoid(G); GeGLU: (X + 1) * G * sigmoid(1.702 G); both
       // halves first clamped to [-glu_limit, glu_limit] when a limit is set
-      float x = c, gt = al * __uint_as_float(gs[i]);
+      float2 x = c;
+      float2 gt = __fmul2_rn(al2, make_float2(__uint_as_float(gs[i]), __uint_as_float(gs[i + 1])));
       if (p.glu_limit > 0.0f) {
-        x = fminf(fmaxf(x, -p.glu_limit), p.glu_limit);
-        gt = fminf(fmaxf(gt, -p.glu_limit), p.glu_limit);
+        x.x = fminf(fmaxf(x.x, -p.glu_limit), p.glu_limit);
+        x.y = fminf(fmaxf(x.y, -p.glu_limit), p.glu_limit);
+        gt.x = fminf(fmaxf(gt.x, -p.glu_limit), p.glu_limit);
+        gt.y = fminf(fmaxf(gt.y, -p.glu_limit), p.glu_limit);
       }
+      float2 sig;
       if (p.glu_kind) {
-        const float sig = __fdividef(1.0f, 1.0f + __expf(-1.702f * gt));
-        v[i] = pr * (x + 1.0f) * (gt * sig);
+        sig.x = __fdividef(1.0f, 1.0f + __expf(-1.702f * gt.x));
+        sig.y = __fdividef(1.0f, 1.0f + __expf(-1.702f * gt.y));
+        o = __fmul2_rn(__fmul2_rn(pr2, __fadd2_rn(x, make_float2(1.0f, 1.0f))), __fmul2_rn(gt, sig));
       } else {
-        const float sig = __fdividef(1.0f, 1.0f + __expf(-gt));
-        v[i] = pr * x * (gt * sig);
+        sig.x = __fdividef(1.0f, 1.0f + __expf(-gt.x));
+        sig.y = __fdividef(1.0f, 1.0f + __expf(-gt.y));
+        o = __fmul2_rn(__fmul2_rn(pr2, x), __fmul2_rn(gt, sig));
       }
-      if (p.glu_gamma != 1.0f) v[i] *= p.glu_gamma;
+      if (p.glu_gamma != 1.0f) o = __fmul2_rn(o, make_float2(p.glu_gamma, p.glu_gamma));
     }
+    v[i] = o.x;
+    v[i + 1] = o.y;
   }
   output_chunk<IC, OUTC>(p, v, row, col0, norm, lane, kblk_col, amax_local, os);
   if (XC && p.rht != nullptr && in_range(p.status, kSiteRht, col0 + 31, p.n_out)) {
@@ -1335,6 +1407,9 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC)>()>::kThreads, 1
     // other one.  Holding all 128 in registers spills the backward epilogue.
     constexpr bool kChunkLd = NA == 2 && BN == 256;
     static_assert(!kChunkLd || is_bwd_inst(EPI), "chunked accumulator reads: backward epilogues");
+    // the forward GLU pairs its up and gate blocks as it reads the accumulator
+    // (the bias / C instances keep the accumulator's column order in registers)
+    constexpr bool kPairOnLoad = EPI == EPI_SWIGLU && !XC;
     const int q = warp & 3;                           // tensor-memory lane quadrant
     const int e = (warp - Ro::kEpiFirst) >> 2;        // which half of the columns
     const float norm = (OUTC == OUTC_FLOAT) ? 1.0f : *p.norm_const;
@@ -1387,8 +1462,12 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC)>()>::kThreads, 1
         }
       };
       if (!kChunkLd) {
+        // SwiGLU / GeGLU without bias or C: each 64-column pair's up block is
+        // read into its first 32 registers and its gate block into the next 32,
+        // whichever comes first in the accumulator (gate_first)
+        const uint32_t swap = (kPairOnLoad && p.gate_first) ? 32u : 0u;
 #pragma unroll
-        for (int c = 0; c < kWarpCols / 32; ++c) tmem_ld32p(taddr + 32 * c, &r[32 * c]);
+        for (int c = 0; c < kWarpCols / 32; ++c) tmem_ld32p(taddr + ((32u * c) ^ swap), &r[32 * c]);
         tmem_wait_ld();
         release();       // all of this warp's columns are in registers
       }
@@ -1521,8 +1600,8 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC)>()>::kThreads, 1
               gv[i] = ref * pr * uo * sg * (1.0f + p.geglu_a * gc * (1.0f - sg)) * gate_mask;      // d gate
             }
           }
-          output_chunk<IC, OUTC>(p, x, row, xo, norm, lane, kblk_col, amax_local, os);
-          output_chunk<IC, OUTC>(p, gv, row, go, norm, lane, kblk_col, amax_local2, os);
+          output_chunk<IC, OUTC, true>(p, x, row, xo, norm, lane, kblk_col, amax_local, os);
+          output_chunk<IC, OUTC, true>(p, gv, row, go, norm, lane, kblk_col, amax_local2, os);
           if (XC && p.dbias != nullptr && in_range(p.status, kSiteDbias, max(xo, go) + 31, p.n_out)) {
             float* db = p.dbias + static_cast<int64_t>(g) * p.n_out;
             add_column_sums32(x, db + xo, lane);
@@ -1537,14 +1616,19 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC)>()>::kThreads, 1
         for (int j = 0; j < kWarpCols / 64; ++j) {
           const int col0 = nt * (BN / 2) + e * (kWarpCols / 2) + 32 * j;
           if (col0 >= p.n_out) continue;
-          uint32_t xs[32], gs[32];
+          if (kPairOnLoad) {
+            epilogue_chunk<IC, EPI, OUTC, XC>(p, &r[64 * j], &r[64 * j + 32], row, col0, al_epi, pr, norm, lane,
+                                               kblk_col, amax_local, seg_start, seg_rows, os);
+          } else {
+            uint32_t xs[32], gs[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            xs[i] = gf ? r[64 * j + 32 + i] : r[64 * j + i];
-            gs[i] = gf ? r[64 * j + i] : r[64 * j + 32 + i];
+            for (int i = 0; i < 32; ++i) {
+              xs[i] = gf ? r[64 * j + 32 + i] : r[64 * j + i];
+              gs[i] = gf ? r[64 * j + i] : r[64 * j + 32 + i];
+            }
+            epilogue_chunk<IC, EPI, OUTC, XC>(p, xs, gs, row, col0, al_epi, pr, norm, lane, kblk_col, amax_local,
+                                               seg_start, seg_rows, os);
           }
-          epilogue_chunk<IC, EPI, OUTC, XC>(p, xs, gs, row, col0, al_epi, pr, norm, lane, kblk_col, amax_local,
-                                             seg_start, seg_rows, os);
         }
       } else {
 #pragma unroll
