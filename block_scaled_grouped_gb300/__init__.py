@@ -23,7 +23,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CU
           4: "device wait timed out", 5: "padded_offsets invalid", 6: "expert weight pointer invalid",
           7: "an index failed its range check"}
 
-SYMBOLS = ("bsgg_create", "bsgg_run", "bsgg_run_host", "bsgg_query_device_status", "bsgg_destroy",
+SYMBOLS = ("bsgg_create", "bsgg_run", "bsgg_run_host", "bsgg_run_host_async", "bsgg_query_device_status",
+           "bsgg_destroy",
            "bsgg_status_string", "bsgg_sf_bytes", "bsgg_sf_offset", "bsgg_pack_sf", "bsgg_run_noalloc",
            "bsgg_measure_mma_peak", "bsgg_measure_mma_peak_tile", "bsgg_debug_force_timeout",
            "bsgg_launches_per_run", "bsgg_debug_bounds_checked", "bsgg_debug_bounds_margin",
@@ -115,6 +116,10 @@ def lib(debug_bounds: bool = False):
         L.bsgg_run_host.argtypes = [ctypes.c_void_p, ctypes.POINTER(Args), ctypes.POINTER(Args),
                                     ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint64),
                                     ctypes.POINTER(ctypes.c_uint64)]
+        L.bsgg_run_host_async.restype = ctypes.c_int
+        L.bsgg_run_host_async.argtypes = [ctypes.c_void_p, ctypes.POINTER(Args), ctypes.POINTER(Args),
+                                          ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint64),
+                                          ctypes.POINTER(ctypes.c_uint64)]
         L.bsgg_query_device_status.restype = ctypes.c_int
         L.bsgg_query_device_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
         L.bsgg_destroy.restype = None
@@ -266,13 +271,16 @@ class Plan:
         args = self._args(tensors)
         _check(self._lib.bsgg_run(self._h, ctypes.byref(args), _stream(stream)), "bsgg_run")
 
-    def run_host(self, host: dict, dev: dict, stream=None):
+    def run_host(self, host: dict, dev: dict, stream=None, sync: bool = True):
         """Host-buffer call: copies host inputs in, runs, copies outputs out
-        and synchronizes.  Returns (h2d_bytes, d2h_bytes)."""
+        and, with sync, synchronizes (bsgg_run_host; without sync
+        bsgg_run_host_async, whose outputs are complete once `stream` has
+        finished).  Returns (h2d_bytes, d2h_bytes)."""
         hi, di = self._args(host), self._args(dev)
         h2d, d2h = ctypes.c_uint64(), ctypes.c_uint64()
-        _check(self._lib.bsgg_run_host(self._h, ctypes.byref(hi), ctypes.byref(di), _stream(stream),
-                                   ctypes.byref(h2d), ctypes.byref(d2h)), "bsgg_run_host")
+        fn = self._lib.bsgg_run_host if sync else self._lib.bsgg_run_host_async
+        _check(fn(self._h, ctypes.byref(hi), ctypes.byref(di), _stream(stream), ctypes.byref(h2d),
+                  ctypes.byref(d2h)), "bsgg_run_host" if sync else "bsgg_run_host_async")
         return int(h2d.value), int(d2h.value)
 
     @property

@@ -712,8 +712,15 @@ bsgg_status bsgg_debug_bounds_violation(const bsgg_plan* P, uint32_t* site, uint
   return BSGG_OK;
 }
 
-bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* dev, void* stream,
-                          uint64_t* h2d_bytes, uint64_t* d2h_bytes) {
+}  // extern "C"
+
+namespace {
+
+// bsgg_run_host / bsgg_run_host_async: the inputs present in `host` copied in,
+// the kernel, the outputs present in `host` copied back, all on `stream`;
+// `sync` waits for them.
+bsgg_status run_host_impl(bsgg_plan* P, const bsgg_args* host, const bsgg_args* dev, void* stream,
+                          uint64_t* h2d_bytes, uint64_t* d2h_bytes, bool sync) {
   if (!P || !host || !dev) return BSGG_ERR_INVALID_ARG;
   const bsgg_desc& d = P->desc;
   // discrete weights are taken as resident on the device
@@ -774,10 +781,24 @@ bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* 
            d.want_rht == 2 ? uint64_t(d.m_pad) * P->n_out / 16 : sf_bytes_impl(d.m_pad, P->n_out, 16, 1)) &&
        d2h(d.want_c ? host->c : nullptr, dev->c, uint64_t(d.m_pad) * d.n * out_elem_bits(d.c_format) / 8);
   if (!ok) return BSGG_ERR_CUDA;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return BSGG_ERR_CUDA;
+  if (sync && cudaStreamSynchronize(s) != cudaSuccess) return BSGG_ERR_CUDA;
   if (h2d_bytes) *h2d_bytes = in_bytes;
   if (d2h_bytes) *d2h_bytes = out_bytes;
   return BSGG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+bsgg_status bsgg_run_host(bsgg_plan* P, const bsgg_args* host, const bsgg_args* dev, void* stream,
+                          uint64_t* h2d_bytes, uint64_t* d2h_bytes) {
+  return run_host_impl(P, host, dev, stream, h2d_bytes, d2h_bytes, true);
+}
+
+bsgg_status bsgg_run_host_async(bsgg_plan* P, const bsgg_args* host, const bsgg_args* dev, void* stream,
+                                uint64_t* h2d_bytes, uint64_t* d2h_bytes) {
+  return run_host_impl(P, host, dev, stream, h2d_bytes, d2h_bytes, false);
 }
 
 }  // extern "C"

@@ -299,6 +299,20 @@ BSGG_API bsgg_status bsgg_run(bsgg_plan* plan, const bsgg_args* args, void* stre
 BSGG_API bsgg_status bsgg_run_host(bsgg_plan* plan, const bsgg_args* host, const bsgg_args* dev,
                           void* stream, uint64_t* h2d_bytes, uint64_t* d2h_bytes);
 
+/* bsgg_run_host without the final synchronization (the pages have no
+ * counterpart): the copies in, the kernel and the copies out are enqueued on
+ * `stream` and the call returns.  The host buffers (pinned, or the copies are
+ * synchronous on the host side) and the device buffers must stay valid, and
+ * the outputs in `host` are complete only once the stream's work has
+ * finished.  Lets a caller keep several batches in flight on several streams,
+ * so that one batch's outputs travel to the host while the next batch's
+ * inputs travel to the device and its kernel runs; each stream in flight
+ * needs its own `dev` buffers, its own output buffers in `host` and its own
+ * plan (the status word is per plan).  Same arguments, byte counts and errors
+ * as bsgg_run_host. */
+BSGG_API bsgg_status bsgg_run_host_async(bsgg_plan* plan, const bsgg_args* host, const bsgg_args* dev,
+                                void* stream, uint64_t* h2d_bytes, uint64_t* d2h_bytes);
+
 /* Number of kernel launches one bsgg_run of this plan enqueues (the pages have
  * no counterpart): 1, or 2 in discrete weight mode (the per-expert descriptor
  * kernel, then the GEMM).  -1 for a null plan. */

@@ -277,5 +277,6 @@ def test_helper_entry_points_refuse_bad_arguments_before_any_device_call(lib):
     assert lib.bsgg_measure_mma_peak_tile(0, 256, 128, 1024, ctypes.byref(out), None) == 2
     # plan-taking entry points with no plan
     assert lib.bsgg_run_host(None, None, None, None, None, None) == 1
+    assert lib.bsgg_run_host_async(None, None, None, None, None, None) == 1
     assert lib.bsgg_debug_force_timeout(None, 1) == 1
     assert lib.bsgg_launches_per_run(None) == -1

@@ -237,6 +237,47 @@ def test_host_buffer_call_matches_device_call(size):
         assert torch.equal(host[k_], t.cpu()), k_
 
 
+def test_async_host_calls_in_flight_on_two_streams():
+    """bsgg_run_host_async: four batches (the same A, different routing
+    probabilities), two in flight at a time on two streams, each stream with
+    its own plan, device buffers and host output buffers; every batch's
+    outputs equal bsgg_run's on its inputs, bit for bit."""
+    import dataclasses
+    p = small_problem(counts=(300, 200), k=512, n=512, pad_to=128, epi="swiglu", out_fmt="e4m3",
+                      want_col=True, seed=40)
+    pd = to_device(p)
+    probs = [p.prob * f for f in (1.0, 0.5, 2.0, 0.25)]
+    refs = []
+    for pr in probs:
+        outs, sfa, sfb = run_gpu(dataclasses.replace(pd, prob=pr.cuda()))
+        refs.append({k_: t.cpu() for k_, t in outs.items()})
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    plans = [make_plan(pd) for _ in range(2)]
+    devs = []
+    for plan in plans:
+        dev = alloc_outputs(plan)
+        dev.update(a=torch.empty_like(pd.a), sfa=torch.empty_like(sfa), b=pd.b, sfb=sfb,
+                   padded_offsets=pd.padded_offsets, alpha=pd.alpha, prob=torch.empty_like(pd.prob),
+                   norm_const=torch.tensor([p.norm_const], device="cuda"))
+        devs.append(dev)
+    host_in = dict(a=p.a.pin_memory(), sfa=sfa.cpu().pin_memory())
+    host_outs = [{k_: torch.empty(t.shape, dtype=t.dtype).pin_memory() for k_, t in refs[0].items()}
+                 for _ in probs]
+    host_probs = [pr.pin_memory() for pr in probs]   # alive until the copies have run
+    torch.cuda.synchronize()
+    for i, pr in enumerate(host_probs):
+        j = i % 2
+        host = dict(host_in, prob=pr, **host_outs[i])
+        h2d, d2h = plans[j].run_host(host, devs[j], stream=streams[j], sync=False)
+        assert h2d == sum(host[k_].numel() * host[k_].element_size() for k_ in ("a", "sfa", "prob"))
+    torch.cuda.synchronize()
+    for j in range(2):
+        assert plans[j].device_status(streams[j]) == 0
+    for i in range(len(probs)):
+        for k_, t in refs[i].items():
+            assert torch.equal(host_outs[i][k_], t), (i, k_)
+
+
 @pytest.mark.parametrize("in_fmt", ["fp4_ue8m0_16", "mxfp4"])
 @pytest.mark.parametrize("tile", TILES, ids=tile_id)
 def test_fp4_with_ue8m0_scales(tile, in_fmt):
