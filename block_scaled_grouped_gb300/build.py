@@ -49,7 +49,8 @@ def _sources_mtime() -> float:
 
 def build(force: bool = False, verbose: bool = False, debug_bounds: bool = False) -> str:
     out_dir, lib_path = (DEBUG_OUT_DIR, DEBUG_LIB_PATH) if debug_bounds else (OUT_DIR, LIB_PATH)
-    if not force and os.path.exists(lib_path) and os.path.getmtime(lib_path) >= _sources_mtime():
+    src_mtime = _sources_mtime()
+    if not force and os.path.exists(lib_path) and os.path.getmtime(lib_path) >= src_mtime:
         return lib_path
     os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
@@ -75,6 +76,9 @@ def build(force: bool = False, verbose: bool = False, debug_bounds: bool = False
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
+    # the library carries the sources' time as the build found them: a source
+    # edited while it compiled is newer, and the next call rebuilds
+    os.utime(tmp, (src_mtime, src_mtime))
     os.replace(tmp, lib_path)
     return lib_path
 
