@@ -368,6 +368,33 @@ def measured_mma_peak(in_fmt: str, form):
     return _MMA_PEAK_CACHE[key]
 
 
+L2_FLUSH_BYTES = 512 << 20           # four times the 129 MB L2
+
+
+def time_l2_cold(p, plan, tensors, stream, dev, steps: int) -> dict:
+    """Each launch after a write of L2_FLUSH_BYTES to a scratch buffer (so that
+    no input or output line stays in L2 from the previous step), timed alone
+    with CUDA events on the launching stream; the writes fall outside the
+    events."""
+    scratch = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for e0, e1 in evs:
+        scratch.fill_(1)
+        e0.record(stream)
+        plan.run(stream=stream, **tensors)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if plan.device_status(stream) != 0:
+        raise RuntimeError(f"device status after the L2-cold steps ({p.name})")
+    ms = sorted(e0.elapsed_time(e1) for e0, e1 in evs)
+    mean = sum(ms) / len(ms)
+    del scratch
+    return {"value": p.flops / (mean * 1e-3) / 1e12, "unit": UNIT, "steps": steps, "ms_per_step": mean,
+            "median_ms": ms[len(ms) // 2], "flush_bytes": L2_FLUSH_BYTES,
+            "what": "each launch timed alone (CUDA events) after a write of flush_bytes evicted L2"}
+
+
 def make_plan(p, args):
     """The plan of workload `p` in the tile shape and cluster `args` ask for."""
     import block_scaled_grouped_gb300 as bsgg
@@ -488,6 +515,9 @@ def run_gpu(args, world, rank, local):
         f"generated in {time.time() - t0:.1f}s")
     rec, plan, tensors = time_workload(p, args, dev, world, args.steps, args.warmup)
     stream = torch.cuda.current_stream(dev)
+    # the same launches with L2 evicted before each (the main timing relies on
+    # inputs larger than L2 instead)
+    l2_cold = time_l2_cold(p, plan, tensors, stream, dev, min(args.steps, 20))
 
     # end to end through the host-buffer C-ABI call.  Headline: an MoE layer's
     # step -- the expert weights (B, SFB) and alpha stay resident in HBM, the
@@ -605,7 +635,7 @@ def run_gpu(args, world, rank, local):
                                         "tile": args.tile or "library default",
                                         "cluster": args.cluster or "library default"}),
                 "gpu_launches": gpu_launches, "clocks": rec["clocks"], "roofline": rec["roofline"],
-                "e2e": e2e, "cpu_baseline": cpu_baseline, "hbm": rec["hbm"],
+                "e2e": e2e, "cpu_baseline": cpu_baseline, "hbm": rec["hbm"], "l2_cold": l2_cold,
                 "pct_of_dtype_peak": rec["pct_of_dtype_peak"]}
         if workloads:
             line["workloads"] = workloads
