@@ -1,4 +1,6 @@
-"""Parity at full size: the four large forward workloads and the FC1 backward
+"""Parity at full size: the four large forward workloads, the decode-like
+skinny one (64 experts of a few rows each, every group one padded tile) and the
+FC1 backward
 (dSwiGLU, MXFP8 and the BF16 backend), generated on the GPU with their real shapes and run in every tile
 shape (the library's default is the one bench.py times; two shapes for the
 backward), compared element by element with the CPU oracle on
@@ -50,7 +52,7 @@ def _oracle(p, blocks):
                    tanh_clamp_s=p.tanh_clamp_s, want_col=p.want_col, blocks=blocks, **ins)
 
 
-@pytest.fixture(scope="module", params=["fc1_swiglu", "fc2_gate", "fine_nvfp4", "skewed"])
+@pytest.fixture(scope="module", params=["fc1_swiglu", "fc2_gate", "fine_nvfp4", "skewed", "skinny"])
 def workload(request):
     p = W.workload(request.param, device="cuda")
     blocks = _sample_blocks(p)
