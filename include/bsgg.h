@@ -280,7 +280,7 @@ typedef struct bsgg_plan bsgg_plan;
 /* Validate `desc` and build a plan (kernel choice, launch shape, a 16-byte
  * device status word).  The plan belongs to the device that is current at
  * creation.  Returns BSGG_ERR_INVALID_ARG / BSGG_ERR_UNSUPPORTED for
- * descriptions the pages or this build reject; *plan is NULL then. */
+ * descriptions the pages or this library reject; *plan is NULL then. */
 BSGG_API bsgg_status bsgg_create(const bsgg_desc* desc, bsgg_plan** plan);
 
 /* Enqueue one grouped GEMM on `stream` (asynchronous, no host sync, graph
