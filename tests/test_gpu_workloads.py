@@ -22,7 +22,7 @@ from block_scaled_grouped_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def _sample_blocks(p, n_random=3, seed=0):
+def _sample_blocks(p, n_random=12, seed=0):
     """First and last block of the problem; for the first three and last three
     non-empty groups their first block, last block and the block holding their
     last real row; a few random blocks."""
