@@ -1309,14 +1309,23 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC)>()>::kThreads, 1
             const uint8_t* sa = smem + Ly::kOffSfa + stage * Ly::kSfaBytes + 16 * lane;
             const uint8_t* sb = smem + Ly::kOffSfb + stage * Ly::kSfbBytes + 16 * lane;
             if (IC != IC_F4E8 || p.sf_atoms == Ly::kAtoms) {
+              // sixteen columns per store: A's atoms whole (the 16 bytes a
+              // lane holds are rows lane + 32j; quadrant q's MMA rows read
+              // column q of each atom's group, the other three are not read
+              // by them), then B's atoms in the column order 4 (i * halves + h)
+              static_assert(Ly::kAtoms == 4, "four scale atoms per stage and 128 rows");
+              uint4 v[4];
 #pragma unroll
-              for (int i = 0; i < Ly::kAtoms; ++i) {
-                const uint4 va = *reinterpret_cast<const uint4*>(sa + 512 * i);
-                tmem_st_x1(slot + 4 * i + q, q == 0 ? va.x : q == 1 ? va.y : q == 2 ? va.z : va.w);
+              for (int i = 0; i < 4; ++i) v[i] = *reinterpret_cast<const uint4*>(sa + 512 * i);
+              tmem_st_x16(slot, v);
 #pragma unroll
-                for (int h = 0; h < Ly::kHalves; ++h)
-                  tmem_st_x4(slot + Ly::kSfaCols + 4 * (i * Ly::kHalves + h),
-                             *reinterpret_cast<const uint4*>(sb + 512 * (h * Ly::kAtoms + i)));
+              for (int c0 = 0; c0 < 4 * Ly::kHalves; c0 += 4) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const int i = (c0 + k) / Ly::kHalves, h = (c0 + k) % Ly::kHalves;
+                  v[k] = *reinterpret_cast<const uint4*>(sb + 512 * (h * Ly::kAtoms + i));
+                }
+                tmem_st_x16(slot + Ly::kSfaCols + 4 * c0, v);
               }
             } else {
               // one scale per 32 values: a loaded word [s0 s1 s2 s3] covers two

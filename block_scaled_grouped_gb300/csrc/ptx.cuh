@@ -359,6 +359,15 @@ __device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint4 v) {
                "r"(v.z), "r"(v.w)
                : "memory");
 }
+// 16 consecutive columns of the warp's 32 lanes: v[k] into columns 4k .. 4k + 3.
+__device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint4 (&v)[4]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};" ::"r"(taddr),
+      "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y), "r"(v[1].z), "r"(v[1].w),
+      "r"(v[2].x), "r"(v[2].y), "r"(v[2].z), "r"(v[2].w), "r"(v[3].x), "r"(v[3].y), "r"(v[3].z), "r"(v[3].w)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // Per-warpgroup register budget (all four warps of the warpgroup execute it).
 template <uint32_t N>
