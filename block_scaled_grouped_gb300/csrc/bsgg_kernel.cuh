@@ -1139,12 +1139,14 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC)>()>::kThreads, 1
               const uint32_t sfb_own = sfull_bar(stage);
               if (leader) mbar_expect_tx(fb, 2u * op_tx);
               mbar_expect_tx(sfb_own, sf_tx);
+              // the scales first: the scale warps' stores into tensor memory
+              // follow their arrival, the MMAs wait for both
+              tma_load_3d(sSb, mSFB, sfb_own, 0, ka, sfb_rb);
+              tma_load_3d(sSa, &tmSFA, sfb_own, 0, ka, mt);
               for (int j = 0; j < nsl; ++j) {
                 tma_load_2d_pair(sA + j * Ly::kASlice, &tmA, fbl, k0 + j * kBKBytes, mt * kBM);
                 tma_load_3d_pair(sB + j * Ly::kBSlice, mB, fbl, k0 + j * kBKBytes, b_row, bz);
               }
-              tma_load_3d(sSa, &tmSFA, sfb_own, 0, ka, mt);
-              tma_load_3d(sSb, mSFB, sfb_own, 0, ka, sfb_rb);
             } else if (PAIR) {
               // both CTAs' bytes complete the even CTA's barrier
               const uint32_t fbl = mapa_shared(fb, 0);
