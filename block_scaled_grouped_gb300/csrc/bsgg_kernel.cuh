@@ -450,9 +450,9 @@ __device__ __forceinline__ void load_f32x32(float (&v)[32], const void* src, int
   }
 }
 
-// Two products: one packed f32x2 multiply, or (PACKED false: the backward
-// epilogues, whose register allocation spills with the packed form) two
-// scalar ones; the same round-to-nearest results either way.
+// Two products: one packed f32x2 multiply, or (PACKED false: the 256-column
+// backward epilogues, whose register allocation spills with the packed form)
+// two scalar ones; the same round-to-nearest results either way.
 template <bool PACKED>
 __device__ __forceinline__ float2 mul_pair(float a0, float a1, float b0, float b1) {
   if (PACKED) return __fmul2_rn(make_float2(a0, a1), make_float2(b0, b1));
@@ -605,7 +605,7 @@ struct OutStage {
 // a staging slot the warp writes its 32 rows' chunk bytes into it (row after
 // row, as the TMA box lays them out) and one lane stores the whole 32-row box
 // with a TMA store; the scale factors are stored directly either way.
-template <int IC, int OUTC, bool BWD = false>
+template <int IC, int OUTC, bool SCALAR = false>
 __device__ __forceinline__ void output_chunk(const Params& p, const float (&v)[32], int row, int col0,
                                              float norm, int lane, int kblk_col, float& amax_local,
                                              const OutStage& os) {
@@ -699,8 +699,8 @@ __device__ __forceinline__ void output_chunk(const Params& p, const float (&v)[3
       p.sfd_row[sf_off(row, col0 / 32, p.kq_row)] = static_cast<uint8_t>(code);
     }
     store_x = static_cast<int>(col_byte0);
-    if (staged) store_q32_to<OUTC, !BWD>(d_stage, v, sc, p.out_kind);
-    else store_q32<OUTC, !BWD>(static_cast<uint8_t*>(p.d) + row * row_bytes + col_byte0, v, sc, p.out_kind);
+    if (staged) store_q32_to<OUTC, !SCALAR>(d_stage, v, sc, p.out_kind);
+    else store_q32<OUTC, !SCALAR>(static_cast<uint8_t*>(p.d) + row * row_bytes + col_byte0, v, sc, p.out_kind);
     // ---- column blocks of v rows: the warp's 32 lanes are its 32 rows
     if (p.want_col) {
       if (!FP4) {
@@ -716,9 +716,9 @@ __device__ __forceinline__ void output_chunk(const Params& p, const float (&v)[3
         float my_scale;
         block_scale<false>(my_am, norm, p.rcp_qmax, my_code, my_scale);
         uint8_t* const dcol = static_cast<uint8_t*>(p.d_col) + row * row_bytes + col_byte0;
-        if (BWD) {
-          // the backward epilogues gather the 32 factors first (streamed, their
-          // register allocation spills)
+        if (SCALAR) {
+          // SCALAR (the 256-column backward epilogues): the 32 factors gathered
+          // first; with them streamed those instances spill
 #pragma unroll
           for (int j = 0; j < 32; ++j) sc[j] = __shfl_sync(0xffffffffu, my_scale, j);
           if (staged) store_q32_to<OUTC, false>(dcol_stage, v, sc, p.out_kind);
@@ -758,8 +758,8 @@ __device__ __forceinline__ void output_chunk(const Params& p, const float (&v)[3
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           sc[j] = __shfl_sync(0xffffffffu, j < 16 ? sc_lo : sc_hi, 16 * h + (j & 15));
-        if (staged) store_q32_to<OUTC, !BWD>(dcol_stage, v, sc, p.out_kind);
-        else store_q32<OUTC, !BWD>(static_cast<uint8_t*>(p.d_col) + row * row_bytes + col_byte0, v, sc, p.out_kind);
+        if (staged) store_q32_to<OUTC, !SCALAR>(dcol_stage, v, sc, p.out_kind);
+        else store_q32<OUTC, !SCALAR>(static_cast<uint8_t*>(p.d_col) + row * row_bytes + col_byte0, v, sc, p.out_kind);
         if (!v32 || h == 0) {
           const int kb = v32 ? kblk_col : 2 * kblk_col + h;   // row-block index
           p.sfd_col[sf_off(col0 + i, kb, p.kq_col)] = static_cast<uint8_t>(code_lo);
@@ -1421,6 +1421,10 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC)>()>::kThreads, 1
     // the forward GLU pairs its up and gate blocks as it reads the accumulator
     // (the bias / C instances keep the accumulator's column order in registers)
     constexpr bool kPairOnLoad = EPI == EPI_SWIGLU && !XC;
+    // the backward's arithmetic and quantization packed two values per
+    // instruction on 128-column tiles (the 256-column backward instances spill
+    // with the packed form and keep the scalar one)
+    constexpr bool kPackedBwd = is_bwd_inst(EPI) && BN == 128;
     const int q = warp & 3;                           // tensor-memory lane quadrant
     const int e = (warp - Ro::kEpiFirst) >> 2;        // which half of the columns
     const float norm = (OUTC == OUTC_FLOAT) ? 1.0f : *p.norm_const;
@@ -1555,7 +1559,30 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC)>()>::kThreads, 1
           const int esz = p.saved_c_kind == OK_F32 ? 4 : 2;
           load_f32x32(x, static_cast<const uint8_t*>(p.saved_c) + (srow + xo) * esz, p.saved_c_kind);
           load_f32x32(gv, static_cast<const uint8_t*>(p.saved_c) + (srow + go) * esz, p.saved_c_kind);
-          if (EPI == EPI_DSWIGLU && p.bwd_kind == 0) {
+          if (EPI == EPI_DSWIGLU && p.bwd_kind == 0 && kPackedBwd) {
+            // the same arithmetic two values per instruction (packed f32x2)
+            const float2 al2v = make_float2(al2, al2), btv = make_float2(bt, bt), prv = make_float2(pr, pr);
+            const float2 one = make_float2(1.0f, 1.0f);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float2 ref = __fmul2_rn(al2v, make_float2(__uint_as_float(rc[i]), __uint_as_float(rc[i + 1])));
+              const float2 X = __fmul2_rn(btv, make_float2(x[i], x[i + 1]));
+              const float2 G = __fmul2_rn(btv, make_float2(gv[i], gv[i + 1]));
+              const float2 sg = make_float2(__fdividef(1.0f, 1.0f + __expf(-G.x)), __fdividef(1.0f, 1.0f + __expf(-G.y)));
+              const float2 sw = __fmul2_rn(G, sg);
+              const float2 dp = __fmul2_rn(__fmul2_rn(X, sw), ref);
+              dprob_local += dp.x;                                      // dprob += X swish(G) ref
+              dprob_local += dp.y;
+              const float2 rp = __fmul2_rn(ref, prv);
+              const float2 dx = __fmul2_rn(rp, sw);                     // d input
+              const float2 dg = __fmul2_rn(__fmul2_rn(__fmul2_rn(rp, X), sg),
+                                           __ffma2_rn(G, __fadd2_rn(one, make_float2(-sg.x, -sg.y)), one));   // d gate
+              x[i] = dx.x;
+              x[i + 1] = dx.y;
+              gv[i] = dg.x;
+              gv[i + 1] = dg.y;
+            }
+          } else if (EPI == EPI_DSWIGLU && p.bwd_kind == 0) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float ref = al2 * __uint_as_float(rc[i]);
@@ -1611,8 +1638,8 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC)>()>::kThreads, 1
               gv[i] = ref * pr * uo * sg * (1.0f + p.geglu_a * gc * (1.0f - sg)) * gate_mask;      // d gate
             }
           }
-          output_chunk<IC, OUTC, true>(p, x, row, xo, norm, lane, kblk_col, amax_local, os);
-          output_chunk<IC, OUTC, true>(p, gv, row, go, norm, lane, kblk_col, amax_local2, os);
+          output_chunk<IC, OUTC, !kPackedBwd>(p, x, row, xo, norm, lane, kblk_col, amax_local, os);
+          output_chunk<IC, OUTC, !kPackedBwd>(p, gv, row, go, norm, lane, kblk_col, amax_local2, os);
           if (XC && p.dbias != nullptr && in_range(p.status, kSiteDbias, max(xo, go) + 31, p.n_out)) {
             float* db = p.dbias + static_cast<int64_t>(g) * p.n_out;
             add_column_sums32(x, db + xo, lane);
