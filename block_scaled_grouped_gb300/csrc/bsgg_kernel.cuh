@@ -1422,9 +1422,10 @@ __global__ void __launch_bounds__(Roles<scale_stores<ic_fp4(IC)>()>::kThreads, 1
     // (the bias / C instances keep the accumulator's column order in registers)
     constexpr bool kPairOnLoad = EPI == EPI_SWIGLU && !XC;
     // the backward's arithmetic and quantization packed two values per
-    // instruction on 128-column tiles (the 256-column backward instances spill
-    // with the packed form and keep the scalar one)
-    constexpr bool kPackedBwd = is_bwd_inst(EPI) && BN == 128;
+    // instruction on 128-column tiles and where the accumulator is read 32
+    // columns at a time (the other 256-column backward instances spill with
+    // the packed form and keep the scalar one)
+    constexpr bool kPackedBwd = is_bwd_inst(EPI) && (BN == 128 || kChunkLd);
     const int q = warp & 3;                           // tensor-memory lane quadrant
     const int e = (warp - Ro::kEpiFirst) >> 2;        // which half of the columns
     const float norm = (OUTC == OUTC_FLOAT) ? 1.0f : *p.norm_const;
